@@ -1,0 +1,422 @@
+#!/usr/bin/env python3
+"""Benchmark: one step = fwd + bwd_data + bwd_weight + bwd_bias of the AlexNet-style
+2-group convolution (x [128,96,27,27] bf16, w [256,48,5,5], groups 2, pad 2,
+stride 1; fp32 outputs), through the C ABI of libgconv.
+
+Prints ONE JSON line (rank 0).  `value` is whole-job TFLOP/s with inputs resident
+in HBM (3 x 2*N*C_out*Ho*Wo*(C_in/G)*kH*kW FLOP per step over the device time of
+the step, CUDA events on the launch stream, L2 flushed between steps outside the
+timed events).  `e2e` is the same metric with the inputs copied from pinned host
+memory and the four outputs copied back inside the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+`--impl reference` times the fp64 CPU oracle (the only reference this project
+has) on a bounded sample of the same workload on the host cores.
+Multi-GPU (torchrun): every rank runs an independent replica (the path needs no
+exchange); the step time is the max over ranks and value sums all ranks' work.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "grouped-conv fwd+bwd TFLOP/s and % roofline on 1 GB300"
+WORKLOAD = "alexnet_g2"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def flop_per_pass(geom):
+    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+    from bwd_gconv_fwd_gb300.workloads import out_hw
+    Ho, Wo = out_hw(geom)
+    return 2.0 * N * Cout * Ho * Wo * (Cin // G) * kH * kW
+
+
+def algorithmic_bytes(geom, in_bytes=2):
+    """Minimum bytes per pass: read inputs once, write fp32 outputs once."""
+    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+    from bwd_gconv_fwd_gb300.workloads import out_hw
+    Ho, Wo = out_hw(geom)
+    x, y, w = N * Cin * H * W, N * Cout * Ho * Wo, Cout * (Cin // G) * kH * kW
+    return {"fwd": x * in_bytes + w * in_bytes + Cout * in_bytes + y * 4,
+            "bwd_data": y * in_bytes + w * in_bytes + x * 4,
+            "bwd_weight": x * in_bytes + y * in_bytes + w * 4,
+            "bwd_bias": y * in_bytes + Cout * 4}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "bwd_gconv_fwd_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(pass_name):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(pass_name)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            out_dir = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp"
+            self.path = os.path.join(out_dir, f"clocks_{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu_index), "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        smax = max(r[1] for r in rows)
+        loaded = [r for r in rows if r[0] > 0.5 * smax] or rows
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def reduce_max(value, world):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------
+
+def cpu_oracle_sample(geom, x, w, b, dy, target_s=12.0, max_images=None):
+    """Times the oracle (as it stands) on the first n images of the workload, n chosen
+    so the four passes take about target_s seconds.  Returns (TFLOP/s, cores, sample text)."""
+    import oracle
+    import torch
+    N = geom[0]
+    f64 = lambda t: None if t is None else t.to(torch.float64).numpy()
+
+    def run(n):
+        g = (n,) + tuple(geom[1:])
+        xs, dys = f64(x[:n]), f64(dy[:n])
+        ws, bs = f64(w), f64(b)
+        t0 = time.perf_counter()
+        oracle.fwd(g, xs, ws, bs)
+        oracle.bwd_data(g, dys, ws)
+        oracle.bwd_weight(g, xs, dys)
+        oracle.bwd_bias(g, dys)
+        return time.perf_counter() - t0, 3 * flop_per_pass(g)
+
+    t1, f1 = run(1)
+    n = max(1, min(max_images or N, int(target_s / max(t1, 1e-3))))
+    if n > 1:
+        t1, f1 = run(n)
+    return f1 / t1 / 1e12, oracle.max_threads(), f"first {n} of {N} images, all four passes", t1
+
+
+def bench_reference(args):
+    """The reference arm: the fp64 CPU oracle, timed per step on a bounded sample."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    from bwd_gconv_fwd_gb300 import workloads as wl
+    wk = wl.WORKLOADS[WORKLOAD]
+    x, w, b, dy = wl.make_inputs(wk)
+    import oracle
+    oracle.build()
+    # calibrate the per-step sample so K + W steps end within a few minutes
+    _, _, _, t_one = cpu_oracle_sample(wk.geom, x, w, b, dy, target_s=0.0, max_images=1)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    n = max(1, min(wk.geom[0], int(budget / max(t_one, 1e-3))))
+    f64 = lambda t: t.to(torch.float64).numpy()
+    g = (n,) + tuple(wk.geom[1:])
+    xs, dys, ws, bs = f64(x[:n]), f64(dy[:n]), f64(w), f64(b)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.fwd(g, xs, ws, bs)
+        oracle.bwd_data(g, dys, ws)
+        oracle.bwd_weight(g, xs, dys)
+        oracle.bwd_bias(g, dys)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    step = statistics.mean(times)
+    value = 3 * flop_per_pass(g) / step / 1e12
+    sample = f"first {n} of {wk.geom[0]} images per step, fwd+bwd_data+bwd_weight+bwd_bias in fp64"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(wk),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(wk):
+    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = wk.geom
+    return {"workload": f"{wk.name}: x[{N},{Cin},{H},{W}] bf16, w[{Cout},{Cin // G},{kH},{kW}], groups {G}, "
+                        f"stride {s}, pads {pt}/{pb}/{pl}/{pr}, dilation {d}; fp32 outputs",
+            "step": "fwd + bwd_data + bwd_weight + bwd_bias", "N": N, "C_in": Cin, "H": H, "W": W,
+            "C_out": Cout, "kH": kH, "kW": kW, "groups": G, "stride": s, "pads": [pt, pb, pl, pr],
+            "dilation": d, "l2": "flushed between steps by a 256 MiB write outside the timed events",
+            "parallelism": "replicas"}
+
+
+def bench_gpu(args):
+    import torch
+    import bwd_gconv_fwd_gb300 as gc
+    from bwd_gconv_fwd_gb300 import binding as B
+    from bwd_gconv_fwd_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from bwd_gconv_fwd_gb300 import build
+    build.build()
+
+    wk = wl.WORKLOADS[WORKLOAD]
+    geom = wk.geom
+    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+    Ho, Wo = wl.out_hw(geom)
+    x, w, b, dy = wl.make_inputs(wk)
+    xd, wd, bd, dyd = (t.to(dev) for t in (x, w, b, dy))
+    y = torch.empty((N, Cout, Ho, Wo), device=dev)
+    dx = torch.empty((N, Cin, H, W), device=dev)
+    dw = torch.empty(tuple(w.shape), device=dev)
+    db = torch.empty((Cout,), device=dev)
+    dt = B.GCONV_BF16
+    ws_bytes = max(gc.gconv_workspace_size(geom, dt, p) for p in range(4))
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    kw = dict(stride=s, padding=(pt, pb, pl, pr), dilation=d, groups=G)
+    wsp, wsb = ws.data_ptr(), ws.numel()
+
+    def step_passes():
+        B.gconv_fwd_ptr(geom, dt, xd.data_ptr(), wd.data_ptr(), bd.data_ptr(), y.data_ptr(), wsp, wsb, sp)
+        yield "fwd"
+        B.gconv_bwd_data_ptr(geom, dt, dyd.data_ptr(), wd.data_ptr(), dx.data_ptr(), wsp, wsb, sp)
+        yield "bwd_data"
+        B.gconv_bwd_weight_ptr(geom, dt, xd.data_ptr(), dyd.data_ptr(), dw.data_ptr(), wsp, wsb, sp)
+        yield "bwd_weight"
+        B.gconv_bwd_bias_ptr(geom, dt, dyd.data_ptr(), db.data_ptr(), wsp, wsb, sp)
+        yield "bwd_bias"
+
+    names = ["fwd", "bwd_data", "bwd_weight", "bwd_bias"]
+    plans = {nm: gc.gconv_plan(geom, dt, p) for p, nm in enumerate(names)}
+    launches_per_step = sum(l for _, l in plans.values())
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        for _ in step_passes():
+            pass
+    torch.cuda.synchronize()
+    assert gc.gconv_check_device_error(stream) == B.GCONV_OK
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            for j, _ in enumerate(step_passes()):
+                ev[k][j + 1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    assert gc.gconv_check_device_error(stream) == B.GCONV_OK
+    per_pass = {nm: [ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(args.steps)] for j, nm in enumerate(names)}
+    step_ms = [ev[k][0].elapsed_time(ev[k][4]) for k in range(args.steps)]
+    total_ms = reduce_max(sum(step_ms), world)
+    ms_per_step = total_ms / args.steps
+    fpp = flop_per_pass(geom)
+    value = world * 3 * fpp * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- end-to-end: pinned host inputs in, four outputs back, every step ----
+    hx, hw_, hb, hdy = (t.pin_memory() for t in (x, w, b, dy))
+    hy, hdx, hdw, hdb = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (y, dx, dw, db))
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hw_, hb, hdy))
+    d2h = sum(t.numel() * t.element_size() for t in (hy, hdx, hdw, hdb))
+
+    def e2e_step():
+        xd.copy_(hx, non_blocking=True)
+        wd.copy_(hw_, non_blocking=True)
+        bd.copy_(hb, non_blocking=True)
+        dyd.copy_(hdy, non_blocking=True)
+        gc.gconv_fwd(xd, wd, bd, y, workspace=ws, stream=stream, **kw)
+        gc.gconv_bwd_data(dyd, wd, dx, workspace=ws, stream=stream, **kw)
+        gc.gconv_bwd_weight(xd, dyd, dw, workspace=ws, stream=stream, **kw)
+        gc.gconv_bwd_bias(dyd, db, geom=geom, workspace=ws, stream=stream)
+        hy.copy_(y, non_blocking=True)
+        hdx.copy_(dx, non_blocking=True)
+        hdw.copy_(dw, non_blocking=True)
+        hdb.copy_(db, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, args.steps // 2)
+    if world > 1:
+        torch.distributed.barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1), world)
+    e2e_value = world * 3 * fpp * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    if world > 1:
+        torch.distributed.barrier()
+    if rank != 0:
+        return 0
+
+    # ---- roofline of the dominant pass ----
+    peaks, peak_src = load_peaks()
+    avg = {nm: statistics.mean(v) for nm, v in per_pass.items()}
+    dom = max(avg, key=avg.get)
+    abytes = algorithmic_bytes(geom)
+    hbm = peaks["hbm_gbs"] * 1e9
+    tc = peaks["bf16_tflops"] * 1e12
+    if dom == "bwd_bias":
+        bound, ach, peak, unit = "hbm", abytes[dom] / (avg[dom] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        t_c, t_m = fpp / tc, abytes[dom] / hbm
+        if t_c >= t_m:
+            bound, ach, peak, unit = "tensor", fpp / (avg[dom] * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        else:
+            bound, ach, peak, unit = "hbm", abytes[dom] / (avg[dom] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    roof_step_s = sum(max(fpp / tc, abytes[nm] / hbm) if nm != "bwd_bias" else abytes[nm] / hbm for nm in names)
+    clocks = clk.summary()
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v, cores, sample, secs = cpu_oracle_sample(geom, x, w, b, dy, target_s=args.cpu_seconds)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{sample} ({secs:.1f} s, fp64 direct loops, OpenMP)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(wk),
+        "roofline": {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
+                     "traffic": recorded_traffic(dom), "kernel": f"{dom} ({plans[dom][1]} launch(es), "
+                     f"{gc.PATH_NAMES[plans[dom][0]]})", "peak_source": f"{peak_src} (burst)",
+                     "algorithmic": (f"{fpp / 1e9:.2f} GFLOP" if bound == "tensor" else f"{abytes[dom] / 1e6:.1f} MB")
+                     + " per launch"},
+        "step_roofline_frac": roof_step_s * 1e3 / ms_per_step,
+        "passes": {nm: {"us": avg[nm] * 1e3, "path": gc.PATH_NAMES[plans[nm][0]], "launches": plans[nm][1],
+                        "tflops": (fpp / (avg[nm] * 1e-3) / 1e12) if nm != "bwd_bias" else None,
+                        "gbs": abytes[nm] / (avg[nm] * 1e-3) / 1e9} for nm in names},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / e2e_steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gconv", choices=["gconv", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps, whatever is asked
+    if args.impl == "reference":
+        return bench_reference(args)
+    return bench_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,247 @@
+"""ctypes binding of libgconv.so (include/gconv.h): argument marshalling only.
+
+Every function here forwards to the C entry point of the same name; all
+arithmetic runs in the library's CUDA kernels.  There is no CPU fallback: if
+libgconv.so is missing the first call raises.  PyTorch only supplies device
+memory (tensors, workspaces) and the CUDA stream.
+
+Geometry is the ABI's 14-tuple ``(N, C_in, H, W, C_out, kH, kW, stride, pad_top,
+pad_bottom, pad_left, pad_right, dilation, groups)``; the tensor-level wrappers
+derive it from the tensor shapes plus ``stride``, ``padding`` (an int or a
+(top, bottom, left, right) tuple), ``dilation`` and ``groups``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgconv.so")
+
+GCONV_OK, GCONV_ERR_INVALID_ARG, GCONV_ERR_UNSUPPORTED, GCONV_ERR_WORKSPACE, GCONV_ERR_CUDA, \
+    GCONV_ERR_TIMEOUT = range(6)
+GCONV_F32, GCONV_BF16 = 0, 1
+PASS_FWD, PASS_BWD_DATA, PASS_BWD_WEIGHT, PASS_BWD_BIAS = range(4)
+PATH_NONE, PATH_DIRECT, PATH_TC_IGEMM, PATH_TC_FC, PATH_REDUCE = range(5)
+PATH_NAMES = {PATH_NONE: "none", PATH_DIRECT: "direct", PATH_TC_IGEMM: "tc_igemm",
+              PATH_TC_FC: "tc_fc", PATH_REDUCE: "reduce"}
+
+EXPORTED = ("gconv_out_shape", "gconv_workspace_size", "gconv_plan", "gconv_fwd", "gconv_bwd_data",
+            "gconv_bwd_weight", "gconv_bwd_bias", "gconv_check_device_error", "gconv_status_string",
+            "gconv_debug_force_path", "gconv_debug_set_wait_limit")
+
+_lib = None
+
+
+class GconvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+def lib():
+    """Load libgconv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is not built; run bwd_gconv_fwd_gb300.build.build() "
+                           "(or __graft_entry__.build()) -- there is no fallback path")
+    L = ctypes.CDLL(LIB_PATH)
+    i, vp, sz = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+    geo = [i] * 14
+    L.gconv_out_shape.argtypes = geo + [ctypes.POINTER(i), ctypes.POINTER(i)]
+    L.gconv_out_shape.restype = i
+    L.gconv_workspace_size.argtypes = geo + [i, i]
+    L.gconv_workspace_size.restype = sz
+    L.gconv_plan.argtypes = geo + [i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+    L.gconv_plan.restype = i
+    L.gconv_fwd.argtypes = geo + [i, vp, vp, vp, vp, vp, sz, vp]
+    L.gconv_fwd.restype = i
+    L.gconv_bwd_data.argtypes = geo + [i, vp, vp, vp, vp, sz, vp]
+    L.gconv_bwd_data.restype = i
+    L.gconv_bwd_weight.argtypes = geo + [i, vp, vp, vp, vp, sz, vp]
+    L.gconv_bwd_weight.restype = i
+    L.gconv_bwd_bias.argtypes = geo + [i, vp, vp, vp, sz, vp]
+    L.gconv_bwd_bias.restype = i
+    L.gconv_check_device_error.argtypes = [vp]
+    L.gconv_check_device_error.restype = i
+    L.gconv_status_string.argtypes = [i]
+    L.gconv_status_string.restype = ctypes.c_char_p
+    L.gconv_debug_force_path.argtypes = [i]
+    L.gconv_debug_force_path.restype = None
+    L.gconv_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
+    L.gconv_debug_set_wait_limit.restype = None
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().gconv_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != GCONV_OK:
+        raise GconvError(status, what)
+
+
+# ---- host-only queries ---------------------------------------------------------
+
+def gconv_out_shape(geom):
+    ho, wo = ctypes.c_int(), ctypes.c_int()
+    _check(lib().gconv_out_shape(*map(int, geom), ctypes.byref(ho), ctypes.byref(wo)), "gconv_out_shape")
+    return ho.value, wo.value
+
+
+def gconv_workspace_size(geom, dtype: int, pass_: int) -> int:
+    n = lib().gconv_workspace_size(*map(int, geom), int(dtype), int(pass_))
+    if n == ctypes.c_size_t(-1).value:
+        raise GconvError(GCONV_ERR_INVALID_ARG, "gconv_workspace_size")
+    return int(n)
+
+
+def gconv_plan(geom, dtype: int, pass_: int):
+    """(path, launches) the library would use for this call."""
+    path, launches = ctypes.c_int(), ctypes.c_int()
+    _check(lib().gconv_plan(*map(int, geom), int(dtype), int(pass_), ctypes.byref(path),
+                            ctypes.byref(launches)), "gconv_plan")
+    return path.value, launches.value
+
+
+def gconv_debug_force_path(path: int):
+    lib().gconv_debug_force_path(int(path))
+
+
+def gconv_debug_set_wait_limit(limit: int):
+    lib().gconv_debug_set_wait_limit(int(limit))
+
+
+def gconv_check_device_error(stream=None) -> int:
+    """Synchronise the stream and return the status of the device error word."""
+    return int(lib().gconv_check_device_error(_stream_ptr(stream)))
+
+
+# ---- marshalling helpers -----------------------------------------------------
+
+def _stream_ptr(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return GCONV_BF16
+    if t == torch.float32:
+        return GCONV_F32
+    raise TypeError(f"unsupported input dtype {t}; use bfloat16 or float32")
+
+
+def _pads(padding):
+    if isinstance(padding, int):
+        return (padding,) * 4
+    p = tuple(int(v) for v in padding)
+    if len(p) == 2:
+        return (p[0], p[0], p[1], p[1])
+    if len(p) != 4:
+        raise ValueError("padding is an int, (ph, pw) or (top, bottom, left, right)")
+    return p
+
+
+def geometry(x_shape, w_shape, stride=1, padding=0, dilation=1, groups=1):
+    N, Cin, H, W = (int(v) for v in x_shape)
+    Cout, cgi, kH, kW = (int(v) for v in w_shape)
+    if cgi * int(groups) != Cin:
+        raise GconvError(GCONV_ERR_INVALID_ARG, f"weight has {cgi} input channels per group, "
+                                                f"x has {Cin} channels for {groups} groups")
+    pt, pb, pl, pr = _pads(padding)
+    return (N, Cin, H, W, Cout, kH, kW, int(stride), pt, pb, pl, pr, int(dilation), int(groups))
+
+
+def _dev(t: torch.Tensor, name: str):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _workspace(geom, dt, pass_, workspace, device):
+    need = gconv_workspace_size(geom, dt, pass_)
+    if need == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    return ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size()
+
+
+# ---- the four passes (tensor level) -------------------------------------------
+
+def gconv_fwd(x, w, bias, y, *, stride=1, padding=0, dilation=1, groups=1, workspace=None, stream=None):
+    """y <- conv(x, w) + bias (bias may be None).  y: fp32 [N, C_out, Ho, Wo]."""
+    geom = geometry(x.shape, w.shape, stride, padding, dilation, groups)
+    dt = dtype_code(x.dtype)
+    ws, wsb = _workspace(geom, dt, PASS_FWD, workspace, x.device)
+    _check(lib().gconv_fwd(*geom, dt, _dev(x, "x"), _dev(w, "w"), _dev(bias, "bias"), _dev(y, "y"),
+                           ws, wsb, _stream_ptr(stream)), "gconv_fwd")
+    return y
+
+
+def gconv_bwd_data(dy, w, dx, *, stride=1, padding=0, dilation=1, groups=1, workspace=None, stream=None):
+    """dx <- gradient of <y, dy> w.r.t. x.  dx: fp32 [N, C_in, H, W]."""
+    geom = geometry(dx.shape, w.shape, stride, padding, dilation, groups)
+    dt = dtype_code(dy.dtype)
+    ws, wsb = _workspace(geom, dt, PASS_BWD_DATA, workspace, dy.device)
+    _check(lib().gconv_bwd_data(*geom, dt, _dev(dy, "dy"), _dev(w, "w"), _dev(dx, "dx"), ws, wsb,
+                                _stream_ptr(stream)), "gconv_bwd_data")
+    return dx
+
+
+def gconv_bwd_weight(x, dy, dw, *, stride=1, padding=0, dilation=1, groups=1, workspace=None, stream=None):
+    """dw <- gradient of <y, dy> w.r.t. w.  dw: fp32 [C_out, C_in/G, kH, kW]."""
+    geom = geometry(x.shape, dw.shape, stride, padding, dilation, groups)
+    dt = dtype_code(x.dtype)
+    ws, wsb = _workspace(geom, dt, PASS_BWD_WEIGHT, workspace, x.device)
+    _check(lib().gconv_bwd_weight(*geom, dt, _dev(x, "x"), _dev(dy, "dy"), _dev(dw, "dw"), ws, wsb,
+                                  _stream_ptr(stream)), "gconv_bwd_weight")
+    return dw
+
+
+def gconv_bwd_bias(dy, db, *, geom=None, workspace=None, stream=None):
+    """db <- sum of dy over (N, Ho, Wo).  geom defaults to a 1x1 geometry on dy's shape."""
+    if geom is None:
+        N, C, Ho, Wo = (int(v) for v in dy.shape)
+        geom = (N, C, Ho, Wo, C, 1, 1, 1, 0, 0, 0, 0, 1, 1)
+    dt = dtype_code(dy.dtype)
+    ws, wsb = _workspace(geom, dt, PASS_BWD_BIAS, workspace, dy.device)
+    _check(lib().gconv_bwd_bias(*geom, dt, _dev(dy, "dy"), _dev(db, "db"), ws, wsb, _stream_ptr(stream)),
+           "gconv_bwd_bias")
+    return db
+
+
+# ---- raw pointer level (same C signatures), for callers holding pointers ------
+
+def gconv_fwd_ptr(geom, dt, x, w, bias, y, ws=0, ws_bytes=0, stream=0):
+    _check(lib().gconv_fwd(*map(int, geom), int(dt), x, w, bias or None, y, ws or None, int(ws_bytes),
+                           stream or None), "gconv_fwd")
+
+
+def gconv_bwd_data_ptr(geom, dt, dy, w, dx, ws=0, ws_bytes=0, stream=0):
+    _check(lib().gconv_bwd_data(*map(int, geom), int(dt), dy, w, dx, ws or None, int(ws_bytes),
+                                stream or None), "gconv_bwd_data")
+
+
+def gconv_bwd_weight_ptr(geom, dt, x, dy, dw, ws=0, ws_bytes=0, stream=0):
+    _check(lib().gconv_bwd_weight(*map(int, geom), int(dt), x, dy, dw, ws or None, int(ws_bytes),
+                                  stream or None), "gconv_bwd_weight")
+
+
+def gconv_bwd_bias_ptr(geom, dt, dy, db, ws=0, ws_bytes=0, stream=0):
+    _check(lib().gconv_bwd_bias(*map(int, geom), int(dt), dy, db, ws or None, int(ws_bytes),
+                                stream or None), "gconv_bwd_bias")

@@ -1,0 +1,40 @@
+// internal.h -- declarations shared by the host-side translation units.
+#pragma once
+
+#include "../../include/gconv.h"
+#include "common.cuh"
+
+namespace gconv {
+
+constexpr int kNumSMs = 152;                       // GB300: 2 dies x 76 SMs
+constexpr long long kDefaultWaitLimit = 1LL << 26; // polls before a device wait gives up (~seconds)
+
+// What one call will launch.  Filled by plan_pass; TC families fill `tc`.
+struct Plan {
+    int path = 0;             // gconv_path, or -1 when a forced family cannot serve
+    int launches = 0;         // kernel launches per call
+    size_t ws_bytes = 0;      // caller workspace needed
+    int splits = 1;           // split-K slices (CUDA-core weight / bias reductions)
+    int64_t pos_per_split = 0;
+    int n_per_split = 0;
+    int tc[32] = {};          // tensor-core family parameters (see the family's .cu)
+};
+
+gconv_status make_geom(int N, int C_in, int H, int W, int C_out, int kH, int kW, int stride,
+                       int pt, int pb, int pl, int pr, int dil, int groups, Geom *g);
+Plan plan_pass(const Geom &g, gconv_dtype dt, gconv_pass pass);
+long long wait_limit();
+unsigned int *device_error_word();   // device address of the error word, nullptr on failure
+int forced_path();
+
+// tcgen05 implicit-GEMM family (tc_conv.cu)
+bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p);
+gconv_status tc_igemm_launch(const Geom &g, const Plan &p, gconv_pass pass, const void *a,
+                             const void *b, const void *bias, float *out, void *ws, cudaStream_t s);
+
+// tcgen05 dense-GEMM family for input size == kernel size (tc_gemm.cu)
+bool tc_fc_plan(const Geom &g, gconv_pass pass, Plan *p);
+gconv_status tc_fc_launch(const Geom &g, const Plan &p, gconv_pass pass, const void *a,
+                          const void *b, const void *bias, float *out, void *ws, cudaStream_t s);
+
+}  // namespace gconv

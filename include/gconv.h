@@ -1,0 +1,176 @@
+/*
+ * gconv.h -- C ABI of the GB300 (sm_103a) grouped 2D convolution library
+ * (libgconv.so, built from bwd_gconv_fwd_gb300/csrc).
+ *
+ * Operation.  Grouped 2D cross-correlation in channels-first (NCHW) layout:
+ * C_in and C_out are split into `groups` equal contiguous blocks and block g of
+ * the output depends only on block g of the input ("[Feature request] Groups
+ * support for SpatialConvolutionMM", clnn issue #4: the description of groups
+ * and the per-group offsets answer).  For output (n, o, oh, ow), g = o / (C_out/G):
+ *
+ *   y[n,o,oh,ow] = bias[o] + sum_{c < C_in/G, kh < kH, kw < kW}
+ *                  w[o,c,kh,kw] * x[n, g*C_in/G + c, oh*stride - pad_top + kh*dilation,
+ *                                                   ow*stride - pad_left + kw*dilation]
+ *
+ * with x read as 0 outside the image; padding may differ per side (DLPrimitives
+ * blog, "TensorFlow" section: asymmetric padding without a padded copy).  There
+ * is no kernel flip: the fully-connected case (input size == kernel size) is then
+ * exactly a matrix product with the same weight ("SpatialConvolution running in
+ * fully-connected mode is very slow", cudnn.torch issue #118).
+ *
+ *   Ho = floor((H + pad_top + pad_bottom - dilation*(kH-1) - 1) / stride) + 1
+ *   Wo = floor((W + pad_left + pad_right - dilation*(kW-1) - 1) / stride) + 1
+ *
+ * Layouts (all dense, contiguous, row-major):
+ *   x, dx   [N][C_in][H][W]
+ *   w, dw   [C_out][C_in/groups][kH][kW]
+ *   bias,db [C_out]
+ *   y, dy   [N][C_out][Ho][Wo]
+ * Inputs x, w, bias, dy are `dtype` (fp32 or bf16); outputs y, dx, dw, db are
+ * always fp32.  Outputs are overwritten, never accumulated into.
+ *
+ * Common leading arguments of every call, in this order:
+ *   N, C_in, H, W, C_out, kH, kW, stride, pad_top, pad_bottom, pad_left,
+ *   pad_right, dilation, groups
+ * Requirements: C_in, H, W, C_out, kH, kW, stride, dilation, groups >= 1;
+ * N >= 0 (N == 0 is a successful no-op); pads >= 0; C_in and C_out divisible by
+ * groups; Ho, Wo >= 1; every tensor below 2^31 elements.
+ *
+ * Ownership.  The caller owns every buffer; the library allocates no device or
+ * host memory and keeps no per-call state.  Device pointers must be device
+ * memory of the current CUDA device.  Scratch space, where a pass needs it,
+ * comes from the caller's `workspace` (size from gconv_workspace_size; it may
+ * be NULL when that size is 0).  Each call enqueues its kernels on `stream` (a
+ * cudaStream_t; NULL means the legacy default stream) and returns without
+ * synchronising.  Calls are reentrant; two calls that share an output or a
+ * workspace must not overlap on the GPU.
+ *
+ * Errors.  Every call returns a status; nothing aborts or throws across the
+ * ABI.  Arguments are validated on the host before any launch, so an invalid
+ * call launches nothing.  GCONV_ERR_CUDA reports a failed launch (the CUDA
+ * error is left for cudaGetLastError-style inspection).  Bounded device-side
+ * waits never spin forever: a wait that gives up sets a device error word, the
+ * kernel drains its own copies and returns; gconv_check_device_error reports it
+ * as GCONV_ERR_TIMEOUT.
+ */
+#ifndef GCONV_H
+#define GCONV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GCONV_OK = 0,
+    GCONV_ERR_INVALID_ARG = 1,   /* bad geometry, null pointer, misaligned pointer */
+    GCONV_ERR_UNSUPPORTED = 2,   /* valid request no kernel here implements */
+    GCONV_ERR_WORKSPACE = 3,     /* workspace smaller than gconv_workspace_size */
+    GCONV_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    GCONV_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up */
+} gconv_status;
+
+typedef enum { GCONV_F32 = 0, GCONV_BF16 = 1 } gconv_dtype;
+
+typedef enum {
+    GCONV_PASS_FWD = 0,
+    GCONV_PASS_BWD_DATA = 1,
+    GCONV_PASS_BWD_WEIGHT = 2,
+    GCONV_PASS_BWD_BIAS = 3
+} gconv_pass;
+
+/* Kernel families a call can be routed to (reported by gconv_plan). */
+typedef enum {
+    GCONV_PATH_NONE = 0,        /* nothing to launch (N == 0) */
+    GCONV_PATH_DIRECT = 1,      /* CUDA-core fp32 FMA direct loops (fp32 inputs, thin groups) */
+    GCONV_PATH_TC_IGEMM = 2,    /* tcgen05/TMEM implicit GEMM, bf16 in, fp32 accumulate */
+    GCONV_PATH_TC_FC = 3,       /* tcgen05/TMEM dense GEMM for input size == kernel size */
+    GCONV_PATH_REDUCE = 4       /* CUDA-core warp-shuffle reduction (bias gradient) */
+} gconv_path;
+
+/* Output extent (formula above).  GCONV_ERR_INVALID_ARG when the geometry is
+ * malformed or leaves no output pixel.  Ho, Wo must be non-null host pointers. */
+gconv_status gconv_out_shape(int N, int C_in, int H, int W, int C_out, int kH, int kW,
+                             int stride, int pad_top, int pad_bottom, int pad_left,
+                             int pad_right, int dilation, int groups, int *Ho, int *Wo);
+
+/* Bytes of caller-provided device workspace the given pass needs (0 if none;
+ * (size_t)-1 for an invalid geometry).  The size depends only on the
+ * arguments, so it can be queried once and the buffer reused. */
+size_t gconv_workspace_size(int N, int C_in, int H, int W, int C_out, int kH, int kW,
+                            int stride, int pad_top, int pad_bottom, int pad_left,
+                            int pad_right, int dilation, int groups, gconv_dtype dtype,
+                            gconv_pass pass);
+
+/* Which kernel family serves the pass, and how many kernel launches one call
+ * makes.  Host-only; launches nothing.  Either output pointer may be NULL. */
+gconv_status gconv_plan(int N, int C_in, int H, int W, int C_out, int kH, int kW,
+                        int stride, int pad_top, int pad_bottom, int pad_left,
+                        int pad_right, int dilation, int groups, gconv_dtype dtype,
+                        gconv_pass pass, int *path, int *launches);
+
+/* Forward: y = conv(x, w) + bias.  bias may be NULL (no bias term).
+ * Definition: the sum above (clnn issue #4, groups; DLPrimitives blog,
+ * "Pointwise Broadcast Reduce": bias added as x + bias.reshape((C,1,1))). */
+gconv_status gconv_fwd(int N, int C_in, int H, int W, int C_out, int kH, int kW,
+                       int stride, int pad_top, int pad_bottom, int pad_left,
+                       int pad_right, int dilation, int groups, gconv_dtype dtype,
+                       const void *x, const void *w, const void *bias, float *y,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward-data: dx = d<y, dy>/dx, the adjoint of the forward over the full
+ * C_out/G output channels of each group ("Support groups in DenseConvDims",
+ * NNlib.jl PR #289, the conv-data gradient remark):
+ *   dx[n,ci,ih,iw] = sum_{o in group(ci), kh, kw} w[o, ci mod C_in/G, kh, kw] * dy[n,o,oh,ow]
+ * over oh = (ih + pad_top - kh*dilation)/stride exact and in range (same for ow);
+ * pixels that no tap reaches get exactly 0. */
+gconv_status gconv_bwd_data(int N, int C_in, int H, int W, int C_out, int kH, int kW,
+                            int stride, int pad_top, int pad_bottom, int pad_left,
+                            int pad_right, int dilation, int groups, gconv_dtype dtype,
+                            const void *dy, const void *w, float *dx,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward-weight (gradWeight of the cudnn.torch issue #118 script):
+ *   dw[o,c,kh,kw] = sum_{n,oh,ow} dy[n,o,oh,ow] * x[n, g*C_in/G + c,
+ *                   oh*stride - pad_top + kh*dilation, ow*stride - pad_left + kw*dilation]
+ * The sum over N*Ho*Wo is split across CTAs; partial sums go to the workspace
+ * and a second kernel adds them in a fixed order (bitwise reproducible). */
+gconv_status gconv_bwd_weight(int N, int C_in, int H, int W, int C_out, int kH, int kW,
+                              int stride, int pad_top, int pad_bottom, int pad_left,
+                              int pad_right, int dilation, int groups, gconv_dtype dtype,
+                              const void *x, const void *dy, float *dw,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bias gradient: db[o] = sum_{n,oh,ow} dy[n,o,oh,ow], the np.sum(dy, dims=(0,2,3))
+ * reduction of the DLPrimitives blog ("Pointwise Broadcast Reduce").  Reduced
+ * with warp shuffles in a fixed order (bitwise reproducible). */
+gconv_status gconv_bwd_bias(int N, int C_in, int H, int W, int C_out, int kH, int kW,
+                            int stride, int pad_top, int pad_bottom, int pad_left,
+                            int pad_right, int dilation, int groups, gconv_dtype dtype,
+                            const void *dy, float *db,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronises `stream`, then reads and clears the device error word that
+ * bounded waits set.  GCONV_OK, GCONV_ERR_TIMEOUT, or GCONV_ERR_CUDA. */
+gconv_status gconv_check_device_error(void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *gconv_status_string(gconv_status status);
+
+/* Test hooks (process-wide, not thread-safe; not for production use).
+ * gconv_debug_force_path: route every later call to `path` where that family
+ * can serve it (GCONV_PATH_NONE restores automatic choice); a family that
+ * cannot serve a request makes the call return GCONV_ERR_UNSUPPORTED.
+ * gconv_debug_set_wait_limit: iteration limit of device-side waits
+ * (a negative value restores the default); 0 makes every bounded wait give up
+ * at once, which exercises the timeout path without hanging anything. */
+void gconv_debug_force_path(int path);
+void gconv_debug_set_wait_limit(long long limit);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GCONV_H */

@@ -1,0 +1,149 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared
+symbol, and its host-side validation, shape arithmetic, planning and workspace
+sizing behave as include/gconv.h states.  No call here reaches a kernel launch.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import bwd_gconv_fwd_gb300 as gc
+from bwd_gconv_fwd_gb300 import binding as B
+from bwd_gconv_fwd_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from bwd_gconv_fwd_gb300 import build
+    build.build()
+    return B.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "gconv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gconv_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    declared = _declared()
+    assert len(declared) >= 10
+    for name in declared:
+        assert hasattr(L, name), name
+    assert set(declared) == set(B.EXPORTED)
+
+
+def test_out_shape_matches_floor_formula(L, oracle_mod):
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        geom = wl.random_geometry(rng, max_hw=40, max_k=7, max_s=4, max_d=3, max_pad=4)
+        assert gc.gconv_out_shape(geom) == oracle_mod.out_shape(geom)
+
+
+BAD = [
+    (1, 6, 5, 5, 4, 3, 3, 1, 0, 0, 0, 0, 1, 4),      # C_in % G
+    (1, 4, 5, 5, 6, 3, 3, 1, 0, 0, 0, 0, 1, 4),      # C_out % G
+    (1, 4, 2, 5, 4, 3, 3, 1, 0, 0, 0, 0, 1, 1),      # no output row
+    (1, 4, 5, 5, 4, 3, 3, 0, 0, 0, 0, 0, 1, 1),      # stride 0
+    (1, 4, 5, 5, 4, 3, 3, 1, 0, -1, 0, 0, 1, 1),     # negative pad
+    (1, 4, 5, 5, 4, 3, 3, 1, 0, 0, 0, 0, 0, 1),      # dilation 0
+    (-1, 4, 5, 5, 4, 3, 3, 1, 0, 0, 0, 0, 1, 1),     # negative N
+    (1, 0, 5, 5, 4, 3, 3, 1, 0, 0, 0, 0, 1, 1),      # no channels
+    (70000, 4096, 100, 100, 4, 3, 3, 1, 0, 0, 0, 0, 1, 1),  # x beyond 2^31 elements
+]
+
+
+@pytest.mark.parametrize("geom", BAD)
+def test_invalid_geometry_rejected(L, geom):
+    ho, wo = ctypes.c_int(), ctypes.c_int()
+    assert L.gconv_out_shape(*geom, ctypes.byref(ho), ctypes.byref(wo)) == B.GCONV_ERR_INVALID_ARG
+    assert L.gconv_workspace_size(*geom, B.GCONV_BF16, B.PASS_FWD) == ctypes.c_size_t(-1).value
+    fake = ctypes.c_void_p(1 << 20)
+    for call in (lambda: L.gconv_fwd(*geom, 1, fake, fake, None, fake, None, 0, None),
+                 lambda: L.gconv_bwd_data(*geom, 1, fake, fake, fake, None, 0, None),
+                 lambda: L.gconv_bwd_weight(*geom, 1, fake, fake, fake, None, 0, None),
+                 lambda: L.gconv_bwd_bias(*geom, 1, fake, fake, None, 0, None)):
+        assert call() == B.GCONV_ERR_INVALID_ARG
+
+
+def test_null_and_misaligned_pointers_rejected(L):
+    geom = (2, 8, 6, 6, 8, 3, 3, 1, 1, 1, 1, 1, 1, 1)
+    ok = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 2)
+    assert L.gconv_fwd(*geom, 1, None, ok, None, ok, None, 0, None) == B.GCONV_ERR_INVALID_ARG
+    assert L.gconv_fwd(*geom, 1, ok, None, None, ok, None, 0, None) == B.GCONV_ERR_INVALID_ARG
+    assert L.gconv_fwd(*geom, 1, ok, ok, None, None, None, 0, None) == B.GCONV_ERR_INVALID_ARG
+    assert L.gconv_fwd(*geom, 1, mis, ok, None, ok, None, 0, None) == B.GCONV_ERR_INVALID_ARG
+    assert L.gconv_fwd(*geom, 1, ok, ok, mis, ok, None, 0, None) == B.GCONV_ERR_INVALID_ARG
+    assert L.gconv_bwd_data(*geom, 1, ok, ok, None, None, 0, None) == B.GCONV_ERR_INVALID_ARG
+    assert L.gconv_bwd_weight(*geom, 1, ok, None, ok, None, 0, None) == B.GCONV_ERR_INVALID_ARG
+    assert L.gconv_bwd_bias(*geom, 1, None, ok, None, 0, None) == B.GCONV_ERR_INVALID_ARG
+    assert L.gconv_fwd(*geom, 7, ok, ok, None, ok, None, 0, None) == B.GCONV_ERR_INVALID_ARG  # dtype
+
+
+def test_empty_batch_is_a_noop(L):
+    geom = (0, 8, 6, 6, 8, 3, 3, 1, 1, 1, 1, 1, 1, 1)
+    for p in range(4):
+        path, launches = gc.gconv_plan(geom, B.GCONV_BF16, p)
+        assert path == B.PATH_NONE and launches == 0
+        assert gc.gconv_workspace_size(geom, B.GCONV_BF16, p) == 0
+    # null pointers are fine when nothing is launched
+    assert L.gconv_fwd(*geom, 1, None, None, None, None, None, 0, None) == B.GCONV_OK
+    assert L.gconv_bwd_weight(*geom, 1, None, None, None, None, 0, None) == B.GCONV_OK
+
+
+def test_workspace_too_small_rejected_before_launch(L):
+    for name, wk in wl.WORKLOADS.items():
+        geom = wk.geom
+        dt = B.GCONV_BF16 if wk.dtype == "bf16" else B.GCONV_F32
+        need = gc.gconv_workspace_size(geom, dt, B.PASS_BWD_WEIGHT)
+        if need == 0:
+            continue
+        ok = ctypes.c_void_p(1 << 20)
+        st = L.gconv_bwd_weight(*geom, dt, ok, ok, ok, ok, need - 16, None)
+        assert st == B.GCONV_ERR_WORKSPACE, name
+        st = L.gconv_bwd_weight(*geom, dt, ok, ok, ok, None, 0, None)
+        assert st == B.GCONV_ERR_WORKSPACE, name
+
+
+def test_plans_are_consistent(L):
+    for name, wk in wl.WORKLOADS.items():
+        dt = B.GCONV_BF16 if wk.dtype == "bf16" else B.GCONV_F32
+        for p in range(4):
+            path, launches = gc.gconv_plan(wk.geom, dt, p)
+            assert path in (B.PATH_DIRECT, B.PATH_TC_IGEMM, B.PATH_TC_FC, B.PATH_REDUCE), (name, p)
+            assert 1 <= launches <= 4
+            if p == B.PASS_BWD_BIAS:
+                assert path == B.PATH_REDUCE
+            if dt == B.GCONV_F32:
+                assert path in (B.PATH_DIRECT, B.PATH_REDUCE)
+
+
+def test_forcing_a_family(L):
+    geom = wl.WORKLOADS["tiny_g5"].geom
+    try:
+        gc.binding.gconv_debug_force_path(B.PATH_TC_IGEMM)
+        with pytest.raises(gc.GconvError) as e:
+            gc.gconv_plan(geom, B.GCONV_F32, B.PASS_FWD)   # no tensor-core path for fp32
+        assert e.value.status == B.GCONV_ERR_UNSUPPORTED
+        gc.binding.gconv_debug_force_path(B.PATH_DIRECT)
+        assert gc.gconv_plan(wl.WORKLOADS["alexnet_g2"].geom, B.GCONV_BF16, B.PASS_FWD)[0] == B.PATH_DIRECT
+    finally:
+        gc.binding.gconv_debug_force_path(B.PATH_NONE)
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert B.status_string(s).startswith("GCONV_")
+    assert "unknown" in B.status_string(99)
+
+
+def test_python_geometry_helper():
+    assert gc.geometry((2, 6, 9, 9), (4, 3, 3, 3), 2, (1, 0, 2, 1), 1, 2) == (2, 6, 9, 9, 4, 3, 3, 2, 1, 0, 2, 1, 1, 2)
+    assert gc.geometry((2, 6, 9, 9), (4, 6, 3, 3), padding=1) == (2, 6, 9, 9, 4, 3, 3, 1, 1, 1, 1, 1, 1, 1)
+    with pytest.raises(gc.GconvError):
+        gc.geometry((2, 6, 9, 9), (4, 4, 3, 3), groups=2)

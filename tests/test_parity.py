@@ -1,0 +1,228 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs.
+
+Tolerances (per output tensor): max |gpu - oracle| <= 1e-2 * RMS(oracle) for
+bf16 inputs with fp32 accumulation, <= 1e-4 * RMS(oracle) for fp32 inputs on
+the CUDA-core path.  Shapes, untouched-pixel zeros and the all-ones
+fully-connected script are checked bit-exactly.  Small geometries are compared
+element by element over whole tensors; the full-size workloads, in the launch
+configuration the benchmark uses, on sampled elements the oracle computes one by
+one (RMS taken over the same sample).
+"""
+import numpy as np
+import pytest
+import torch
+
+import bwd_gconv_fwd_gb300 as gc
+from bwd_gconv_fwd_gb300 import binding as B
+from bwd_gconv_fwd_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 1e-2, "f32": 1e-4}
+
+
+@pytest.fixture(scope="module")
+def dev(oracle_mod):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bwd_gconv_fwd_gb300 import build
+    build.build()
+    gc.binding.gconv_debug_force_path(B.PATH_NONE)
+    return torch.device("cuda:0")
+
+
+def _kw(geom):
+    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+    return dict(stride=s, padding=(pt, pb, pl, pr), dilation=d, groups=G)
+
+
+def run_gpu(geom, x, w, b, dy, dev, passes=("y", "dx", "dw", "db")):
+    """All four passes on the GPU; returns fp32 CPU tensors."""
+    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+    Ho, Wo = wl.out_hw(geom)
+    kw = _kw(geom)
+    xd, wd, dyd = x.to(dev), w.to(dev), dy.to(dev)
+    bd = None if b is None else b.to(dev)
+    out = {}
+    if "y" in passes:
+        y = torch.full((N, Cout, Ho, Wo), float("nan"), device=dev)
+        gc.gconv_fwd(xd, wd, bd, y, **kw)
+        out["y"] = y
+    if "dx" in passes:
+        dx = torch.full((N, Cin, H, W), float("nan"), device=dev)
+        gc.gconv_bwd_data(dyd, wd, dx, **kw)
+        out["dx"] = dx
+    if "dw" in passes:
+        dw = torch.full(tuple(w.shape), float("nan"), device=dev)
+        gc.gconv_bwd_weight(xd, dyd, dw, **kw)
+        out["dw"] = dw
+    if "db" in passes:
+        db = torch.full((Cout,), float("nan"), device=dev)
+        gc.gconv_bwd_bias(dyd, db, geom=geom)
+        out["db"] = db
+    torch.cuda.synchronize()
+    assert gc.gconv_check_device_error() == B.GCONV_OK
+    return {k: v.cpu() for k, v in out.items()}
+
+
+def f64(t):
+    return None if t is None else t.to(torch.float64).numpy()
+
+
+def check(name, got, ref, tol):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite output"
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    err = float(np.abs(got - ref).max()) if ref.size else 0.0
+    assert err <= tol * rms + 1e-30, f"{name}: max err {err:.3e} > {tol:g} * rms {rms:.3e}"
+    return err / rms if rms else 0.0
+
+
+def full_compare(geom, dtype, x, w, b, dy, dev, oracle_mod, label=""):
+    got = run_gpu(geom, x, w, b, dy, dev)
+    tol = TOL[dtype]
+    check(f"{label} y", got["y"].numpy(), oracle_mod.fwd(geom, f64(x), f64(w), f64(b)), tol)
+    check(f"{label} dx", got["dx"].numpy(), oracle_mod.bwd_data(geom, f64(dy), f64(w)), tol)
+    check(f"{label} dw", got["dw"].numpy(), oracle_mod.bwd_weight(geom, f64(x), f64(dy)), tol)
+    check(f"{label} db", got["db"].numpy(), oracle_mod.bwd_bias(geom, f64(dy)), tol)
+    return got
+
+
+SMALL = [
+    # (N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G)
+    (2, 32, 14, 13, 64, 3, 3, 1, 1, 0, 2, 1, 1, 2),
+    (3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2),       # AlexNet-like, ragged
+    (2, 64, 17, 15, 64, 3, 3, 1, 1, 1, 1, 1, 1, 1),
+    (2, 64, 19, 16, 64, 3, 3, 2, 0, 1, 0, 1, 1, 1),         # stride 2, asymmetric pads
+    (2, 16, 9, 9, 16, 3, 3, 1, 2, 2, 2, 2, 2, 1),           # dilation 2
+    (1, 40, 7, 23, 24, 2, 4, 1, 0, 3, 1, 0, 1, 1),          # odd channel counts
+    (2, 128, 6, 6, 96, 6, 6, 1, 0, 0, 0, 0, 1, 1),          # input == kernel (FC mode)
+    (2, 32, 12, 12, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8),         # 4 channels per group
+    (2, 16, 10, 10, 16, 3, 3, 1, 1, 1, 1, 1, 1, 16),        # depthwise
+    (1, 8, 9, 7, 12, 1, 1, 1, 0, 0, 0, 0, 1, 1),            # 1x1
+    (1, 16, 8, 8, 16, 2, 2, 3, 0, 0, 0, 0, 1, 1),           # stride > kernel
+    (2, 256, 9, 9, 256, 3, 3, 1, 1, 1, 1, 1, 1, 1),         # several channel tiles
+    (1, 96, 13, 40, 160, 3, 3, 1, 1, 1, 1, 1, 1, 2),        # wide rows, Cout/G = 80
+]
+
+
+@pytest.mark.parametrize("geom", SMALL)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_small_geometries_full(dev, oracle_mod, geom, dtype):
+    wk = wl.Workload("small", geom, dtype, w=("normal", 0.2))
+    x, w, b, dy = wl.make_inputs(wk, seed=sum(geom) * 7 + (dtype == "f32"))
+    full_compare(geom, dtype, x, w, b, dy, dev, oracle_mod, label=str(geom))
+
+
+def test_random_sweep(dev, oracle_mod):
+    rng = np.random.default_rng(1234)
+    for i in range(40):
+        geom = wl.random_geometry(rng, max_n=3, max_c=40, max_hw=15, max_k=4)
+        dtype = "bf16" if i % 3 else "f32"
+        wk = wl.Workload("sweep", geom, dtype, w=("normal", 0.3))
+        x, w, b, dy = wl.make_inputs(wk, seed=5000 + i)
+        full_compare(geom, dtype, x, w, b, dy, dev, oracle_mod, label=f"sweep{i} {geom}")
+
+
+def test_tiny_g5_full(dev, oracle_mod):
+    """The NNlib.jl groups=5 example at its own size, fp32, whole tensors at 1e-4."""
+    wk = wl.WORKLOADS["tiny_g5"]
+    x, w, b, dy = wl.make_inputs(wk)
+    full_compare(wk.geom, wk.dtype, x, w, b, dy, dev, oracle_mod, label="tiny_g5")
+
+
+def _sampled(wk, dev, oracle_mod, n_out=6000, n_w=1500, seed=77):
+    x, w, b, dy = wl.make_inputs(wk)
+    geom = wk.geom
+    got = run_gpu(geom, x, w, b, dy, dev)
+    rng = np.random.default_rng(seed)
+    tol = TOL[wk.dtype]
+    X, Wt, Bt, DY = f64(x), f64(w), f64(b), f64(dy)
+    iy = rng.choice(got["y"].numel(), min(n_out, got["y"].numel()), replace=False)
+    check(f"{wk.name} y", got["y"].numpy().ravel()[iy], oracle_mod.fwd_points(geom, X, Wt, Bt, iy), tol)
+    ix = rng.choice(got["dx"].numel(), min(n_out, got["dx"].numel()), replace=False)
+    check(f"{wk.name} dx", got["dx"].numpy().ravel()[ix], oracle_mod.bwd_data_points(geom, DY, Wt, ix), tol)
+    iw = rng.choice(got["dw"].numel(), min(n_w, got["dw"].numel()), replace=False)
+    check(f"{wk.name} dw", got["dw"].numpy().ravel()[iw], oracle_mod.bwd_weight_points(geom, X, DY, iw), tol)
+    check(f"{wk.name} db", got["db"].numpy(), oracle_mod.bwd_bias(geom, DY), tol)
+    return got
+
+
+@pytest.mark.parametrize("name", ["alexnet_g2", "fc_mode", "fc_mode_ones_x", "dense3x3",
+                                  "dense3x3_s2_asym", "resnext_g32", "depthwise"])
+def test_workload_sampled(dev, oracle_mod, name):
+    got = _sampled(wl.WORKLOADS[name], dev, oracle_mod)
+    if name == "fc_mode_ones_x":
+        # x = 1: every image gives the same y row; gradOutput = 1: every dx row is the same
+        y = got["y"].reshape(1600, 4096)
+        assert torch.equal(y, y[:1].expand_as(y))
+        dx = got["dx"].reshape(1600, -1)
+        assert torch.equal(dx, dx[:1].expand_as(dx))
+
+
+def test_fc_all_ones_script_exact(dev):
+    """The all-ones script of cudnn.torch issue #118 at its size: every value is an
+    exactly representable integer, so the GPU must match bit for bit."""
+    wk = wl.WORKLOADS["fc_mode_all_ones"]
+    x, w, b, dy = wl.make_inputs(wk)
+    got = run_gpu(wk.geom, x, w, b, dy, dev)
+    assert torch.all(got["y"] == 256 * 6 * 6 + 1)
+    assert torch.all(got["dx"] == 4096)
+    assert torch.all(got["dw"] == 1600)
+    assert torch.all(got["db"] == 1600)
+
+
+def test_untouched_pixels_exact_zero(dev):
+    geom = (2, 16, 11, 11, 16, 2, 2, 3, 0, 0, 0, 0, 1, 1)
+    wk = wl.Workload("gap", geom, "bf16")
+    x, w, b, dy = wl.make_inputs(wk, seed=3)
+    dx = run_gpu(geom, x, w, b, dy, dev, passes=("dx",))["dx"]
+    assert torch.all(dx[:, :, 2::3, :] == 0) and torch.all(dx[:, :, :, 2::3] == 0)
+
+
+def test_results_are_bitwise_reproducible(dev):
+    wk = wl.Workload("rep", (4, 64, 20, 20, 64, 3, 3, 1, 1, 1, 1, 1, 1, 2), "bf16")
+    x, w, b, dy = wl.make_inputs(wk, seed=8)
+    a = run_gpu(wk.geom, x, w, b, dy, dev)
+    c = run_gpu(wk.geom, x, w, b, dy, dev)
+    for k in a:
+        assert torch.equal(a[k], c[k]), k
+
+
+def test_outputs_overwritten_not_accumulated(dev, oracle_mod):
+    geom = (2, 32, 10, 10, 32, 3, 3, 1, 1, 1, 1, 1, 1, 1)
+    wk = wl.Workload("ovw", geom, "bf16")
+    x, w, b, dy = wl.make_inputs(wk, seed=9)
+    xd, wd, dyd = x.to(dev), w.to(dev), dy.to(dev)
+    dw = torch.full(tuple(w.shape), 1e6, device=dev)
+    gc.gconv_bwd_weight(xd, dyd, dw, **_kw(geom))
+    torch.cuda.synchronize()
+    check("dw", dw.cpu().numpy(), oracle_mod.bwd_weight(geom, f64(x), f64(dy)), 1e-2)
+
+
+def test_empty_batch_noop(dev):
+    geom = (0, 8, 6, 6, 8, 3, 3, 1, 1, 1, 1, 1, 1, 1)
+    x = torch.empty((0, 8, 6, 6), dtype=torch.bfloat16, device=dev)
+    w = torch.randn((8, 8, 3, 3), device=dev).to(torch.bfloat16)
+    y = torch.empty((0, 8, 6, 6), device=dev)
+    gc.gconv_fwd(x, w, None, y, padding=1)
+    torch.cuda.synchronize()
+
+
+def test_forced_direct_agrees_with_default(dev):
+    """The CUDA-core family and whatever the planner picks agree on the same inputs."""
+    geom = (3, 64, 15, 14, 128, 3, 3, 1, 1, 1, 1, 1, 1, 2)
+    wk = wl.Workload("cross", geom, "bf16", w=("normal", 0.1))
+    x, w, b, dy = wl.make_inputs(wk, seed=21)
+    auto = run_gpu(geom, x, w, b, dy, dev)
+    try:
+        gc.binding.gconv_debug_force_path(B.PATH_DIRECT)
+        direct = run_gpu(geom, x, w, b, dy, dev)
+    finally:
+        gc.binding.gconv_debug_force_path(B.PATH_NONE)
+    for k in auto:
+        r = direct[k].double().numpy()
+        check(f"cross {k}", auto[k].numpy(), r, 1e-2)
