@@ -66,6 +66,11 @@ static int elementwise_grid(int64_t total)
     return (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)kNumSMs * 16));
 }
 
+void launch_reduce_splits(const float *part, int splits, int64_t count, float *out, cudaStream_t s)
+{
+    reduce_splits_kernel<<<elementwise_grid(count), kDirectThreads, 0, s>>>(part, splits, count, out);
+}
+
 // ---- CUDA-core plans ------------------------------------------------------
 
 static void direct_weight_split(const Geom &g, int *splits, int64_t *per_split)

@@ -7,7 +7,7 @@
 namespace gconv {
 
 constexpr int kNumSMs = 152;                       // GB300: 2 dies x 76 SMs
-constexpr long long kDefaultWaitLimit = 1LL << 26; // polls before a device wait gives up (~seconds)
+constexpr long long kDefaultWaitLimit = 1000000000LL; // ns before a device-side wait gives up
 
 // What one call will launch.  Filled by plan_pass; TC families fill `tc`.
 struct Plan {
