@@ -30,7 +30,8 @@ PATH_NAMES = {PATH_NONE: "none", PATH_DIRECT: "direct", PATH_TC_IGEMM: "tc_igemm
 
 EXPORTED = ("gconv_out_shape", "gconv_workspace_size", "gconv_plan", "gconv_fwd", "gconv_bwd_data",
             "gconv_bwd_weight", "gconv_bwd_bias", "gconv_check_device_error", "gconv_status_string",
-            "gconv_debug_force_path", "gconv_debug_set_wait_limit")
+            "gconv_debug_force_path", "gconv_debug_set_wait_limit", "gconv_bwd_weight_noalloc",
+            "gconv_noalloc_scratch_bytes")
 
 _lib = None
 
@@ -66,6 +67,10 @@ def lib():
     L.gconv_bwd_weight.restype = i
     L.gconv_bwd_bias.argtypes = geo + [i, vp, vp, vp, sz, vp]
     L.gconv_bwd_bias.restype = i
+    L.gconv_bwd_weight_noalloc.argtypes = geo + [i, vp, vp, vp, vp]
+    L.gconv_bwd_weight_noalloc.restype = i
+    L.gconv_noalloc_scratch_bytes.argtypes = []
+    L.gconv_noalloc_scratch_bytes.restype = sz
     L.gconv_check_device_error.argtypes = [vp]
     L.gconv_check_device_error.restype = i
     L.gconv_status_string.argtypes = [i]
@@ -211,6 +216,20 @@ def gconv_bwd_weight(x, dy, dw, *, stride=1, padding=0, dilation=1, groups=1, wo
     _check(lib().gconv_bwd_weight(*geom, dt, _dev(x, "x"), _dev(dy, "dy"), _dev(dw, "dw"), ws, wsb,
                                   _stream_ptr(stream)), "gconv_bwd_weight")
     return dw
+
+
+def gconv_bwd_weight_noalloc(x, dy, dw, *, stride=1, padding=0, dilation=1, groups=1, stream=None):
+    """dw <- gradient w.r.t. w, using the library's fixed scratch instead of a workspace
+    (for callers that cannot allocate device memory; see include/gconv.h)."""
+    geom = geometry(x.shape, dw.shape, stride, padding, dilation, groups)
+    dt = dtype_code(x.dtype)
+    _check(lib().gconv_bwd_weight_noalloc(*geom, dt, _dev(x, "x"), _dev(dy, "dy"), _dev(dw, "dw"),
+                                          _stream_ptr(stream)), "gconv_bwd_weight_noalloc")
+    return dw
+
+
+def gconv_noalloc_scratch_bytes() -> int:
+    return int(lib().gconv_noalloc_scratch_bytes())
 
 
 def gconv_bwd_bias(dy, db, *, geom=None, workspace=None, stream=None):

@@ -198,6 +198,30 @@ static gconv_status run_pass(const int *geo, gconv_dtype dt, gconv_pass pass, co
     return cudaGetLastError() == cudaSuccess ? GCONV_OK : GCONV_ERR_CUDA;
 }
 
+// ---- fixed scratch for the no-allocation weight-gradient entry point ----------
+//
+// Scratch of gconv_bwd_weight_noalloc: a file-scope device array, so a caller
+// that cannot allocate device memory still gets the split-K slices the weight
+// gradient needs.  Every device that loads this library keeps it until exit.
+constexpr size_t kNoAllocScratchBytes = (size_t)32 << 20;   // 32 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the array on the current device.  In host code the array's
+// name is only a host-side stand-in, so the address is taken once per device with
+// that device current and cached.
+static void *noalloc_scratch_ptr()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    static void *cache[64] = {};
+    if (!cache[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress((void **)&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        cache[dev] = ptr;
+    }
+    return cache[dev];
+}
+
 }  // namespace gconv
 
 using namespace gconv;
@@ -274,6 +298,29 @@ gconv_status gconv_bwd_bias(GEO_ARGS, gconv_dtype dtype, const void *dy, float *
     const int geo[14] = GEO_ARRAY;
     return run_pass(geo, dtype, GCONV_PASS_BWD_BIAS, dy, nullptr, nullptr, db, workspace, workspace_bytes, stream);
 }
+
+gconv_status gconv_bwd_weight_noalloc(GEO_ARGS, gconv_dtype dtype, const void *x, const void *dy, float *dw,
+                                      void *stream)
+{
+    Geom g;
+    gconv_status st = make_geom(N, C_in, H, W, C_out, kH, kW, stride, pad_top, pad_bottom, pad_left, pad_right,
+                                dilation, groups, &g);
+    if (st != GCONV_OK) return st;
+    if (dtype != GCONV_F32 && dtype != GCONV_BF16) return GCONV_ERR_INVALID_ARG;
+    if (g.N == 0) return GCONV_OK;
+    const Plan p = plan_pass(g, dtype, GCONV_PASS_BWD_WEIGHT);
+    if (p.path < 0) return GCONV_ERR_UNSUPPORTED;
+    if (p.ws_bytes > kNoAllocScratchBytes) return GCONV_ERR_WORKSPACE;   // beyond the fixed 32 MiB scratch
+    void *scratch = nullptr;
+    if (p.ws_bytes > 0) {
+        scratch = noalloc_scratch_ptr();
+        if (!scratch) return GCONV_ERR_CUDA;
+    }
+    const int geo[14] = GEO_ARRAY;
+    return run_pass(geo, dtype, GCONV_PASS_BWD_WEIGHT, x, dy, nullptr, dw, scratch, kNoAllocScratchBytes, stream);
+}
+
+size_t gconv_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
 
 gconv_status gconv_check_device_error(void *stream)
 {

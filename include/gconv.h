@@ -152,6 +152,36 @@ gconv_status gconv_bwd_bias(int N, int C_in, int H, int W, int C_out, int kH, in
                             const void *dy, float *db,
                             void *workspace, size_t workspace_bytes, void *stream);
 
+/* Weight gradient that allocates nothing, for callers that cannot allocate device
+ * memory themselves: code embedded in a host application that owns every
+ * device allocation through its own pool or budget (plug-ins, engines with a
+ * fixed memory plan), and callers that must not trigger a cudaMalloc on the
+ * critical path because an allocation can implicitly synchronise the device.
+ * The studied pages have no counterpart of this entry point.
+ *
+ * Same operation, arguments, layouts and result as gconv_bwd_weight, minus the
+ * workspace: the split-K partial sums go to a fixed 32 MiB scratch array that the
+ * library holds in device memory (every device that loads the library keeps it
+ * until the process exits).  A geometry whose scratch need (what
+ * gconv_workspace_size reports for GCONV_PASS_BWD_WEIGHT) exceeds
+ * gconv_noalloc_scratch_bytes() is rejected with GCONV_ERR_WORKSPACE before any
+ * launch.  No cudaMalloc, cudaFree or allocating library routine is called.
+ *
+ * The first call on a device looks up the scratch array's device address with
+ * that device current (cudaGetSymbolAddress) and caches it; make that first call
+ * before any stream capture.  All calls share the one array and every call
+ * overwrites the slices it uses before reading them, so nothing needs clearing
+ * between calls; calls that overlap on the GPU (different streams, or other
+ * threads, without ordering between them) race on the array and must be
+ * serialised by the caller. */
+gconv_status gconv_bwd_weight_noalloc(int N, int C_in, int H, int W, int C_out, int kH, int kW,
+                                      int stride, int pad_top, int pad_bottom, int pad_left,
+                                      int pad_right, int dilation, int groups, gconv_dtype dtype,
+                                      const void *x, const void *dy, float *dw, void *stream);
+
+/* Size in bytes of the fixed scratch array used by gconv_bwd_weight_noalloc. */
+size_t gconv_noalloc_scratch_bytes(void);
+
 /* Synchronises `stream`, then reads and clears the device error word that
  * bounded waits set.  GCONV_OK, GCONV_ERR_TIMEOUT, or GCONV_ERR_CUDA. */
 gconv_status gconv_check_device_error(void *stream);
