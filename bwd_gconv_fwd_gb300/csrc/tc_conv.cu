@@ -41,8 +41,11 @@
 
 namespace gconv {
 
-constexpr int kTcThreads = 192;        // warps 0-3 staging + epilogue, 4 TMEM/weights, 5 MMA
-constexpr int kStageThreads = 128;
+constexpr int kStageWarps = 8;                      // staging + epilogue warps
+constexpr int kStageThreads = kStageWarps * 32;
+constexpr int kWarpAux = kStageWarps;               // TMEM allocation, weight producer
+constexpr int kWarpMma = kStageWarps + 1;           // MMA issuer
+constexpr int kTcThreads = kStageThreads + 64;
 constexpr int kMaxTaps = 64;
 constexpr int kMaxPlanes = 4;
 constexpr int kWeightStages = 4;
@@ -78,58 +81,75 @@ __device__ __forceinline__ RowRange stage_rows(const StageDesc &d)
     return r;
 }
 
-// Pass 1: contiguous input rows [lo, hi] of each valid channel -> scratch (cp.async).
-__device__ __forceinline__ void stage_pass1(const StageDesc &d, RowRange rr, uint8_t *scratch, int tid)
+// Pass 1: contiguous input rows [lo, hi] of each valid channel -> scratch, in
+// aligned 16-byte cp.async pieces (one warp per channel, one lane per piece).
+// Channel ch's run starts at scratch element ch * scr_stride and keeps the global
+// alignment, so element (row, col) sits at ch_tab[ch] + pos_tab[position].
+__device__ __forceinline__ void stage_pass1(const StageDesc &d, RowRange rr, uint8_t *scratch, int warp, int lane)
 {
     if (rr.lo > rr.hi) return;
     const int64_t hw = (int64_t)d.IH * d.IW;
     const int span = (rr.hi - rr.lo + 1) * d.IW;
-    const int nq_max = span / 8 + 2;
     const uint32_t sbase = ptx::smem_u32(scratch);
-    for (int item = tid; item < d.nch_valid * nq_max; item += kStageThreads) {
-        const int ch = item / nq_max, q = item - ch * nq_max;
+    for (int ch = warp; ch < d.nch_valid; ch += kStageWarps) {
         const int64_t e_lo = d.chan0 + ch * hw + (int64_t)rr.lo * d.IW;
         const int64_t q0 = e_lo >> 3;
-        const int64_t qe = (e_lo + span + 7) >> 3;
-        if (q0 + q >= qe) continue;
-        const int64_t first = (q0 + q) * 8;
-        const int64_t avail = d.U_elems - first;
-        if (avail <= 0) continue;
-        const uint32_t bytes = avail >= 8 ? 16u : (uint32_t)(avail * 2);
-        ptx::cp_async16(sbase + (uint32_t)((ch * d.scr_stride + q * 8) * 2), d.U + first, bytes);
+        const int nq = (int)(((e_lo + span + 7) >> 3) - q0);
+        for (int q = lane; q < nq; q += 32) {
+            const int64_t first = (q0 + q) * 8;
+            const int64_t avail = d.U_elems - first;
+            if (avail <= 0) break;
+            const uint32_t bytes = avail >= 8 ? 16u : (uint32_t)(avail * 2);
+            ptx::cp_async16(sbase + (uint32_t)((ch * d.scr_stride + q * 8) * 2), d.U + first, bytes);
+        }
     }
 }
 
-// Pass 2: scratch -> octet planes, one 16-byte row (8 channels) per position.
-__device__ __forceinline__ void stage_pass2(const StageDesc &d, RowRange rr, const uint8_t *scratch,
-                                            uint8_t *dst, int tid)
+// Position table (once per tile): scratch offset of each staged position's input
+// element relative to its channel's run, or -1 when the position reads zero.
+__device__ __forceinline__ void build_pos_table(const StageDesc &d, RowRange rr, int *tab, int tid)
 {
-    const int per_octet = d.nplanes * d.plane_elems;
-    const int total = (d.nch / 8) * per_octet;
-    const int64_t hw = (int64_t)d.IH * d.IW;
-    const __nv_bfloat16 *scr = reinterpret_cast<const __nv_bfloat16 *>(scratch);
-    for (int item = tid; item < total; item += kStageThreads) {
-        const int j = item / per_octet;
-        const int rem = item - j * per_octet;
-        const int P = rem / d.plane_elems;
-        const int i = rem - P * d.plane_elems;
+    const int total = d.nplanes * d.plane_elems;
+    for (int q = tid; q < total; q += kStageThreads) {
+        const int P = q / d.plane_elems, i = q - P * d.plane_elems;
         const int r = i / d.Wp, c = i - r * d.Wp;
         const int row = d.us * (d.row_base + r) + d.ph[P];
         const int col = d.us * (d.col0 + c) + d.pw[P];
         const bool inside = r < d.rows_valid && row >= rr.lo && row <= rr.hi && col >= 0 && col < d.IW;
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (inside) {
-            #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int ch = j * 8 + e;
-                if (ch < d.nch_valid) {
-                    const int off = (int)((d.chan0 + ch * hw + (int64_t)rr.lo * d.IW) & 7);
-                    const uint32_t v = __bfloat16_as_ushort(scr[ch * d.scr_stride + off + (row - rr.lo) * d.IW + col]);
-                    w[e >> 1] |= v << ((e & 1) * 16);
-                }
+        tab[q] = inside ? (row - rr.lo) * d.IW + col : -1;
+    }
+}
+
+// Channel table (once per staged chunk): scratch index of each channel's run start
+// plus its alignment offset, or -1 for channels past nch_valid.
+__device__ __forceinline__ void build_ch_table(const StageDesc &d, RowRange rr, int *tab, int tid)
+{
+    const int64_t hw = (int64_t)d.IH * d.IW;
+    for (int ch = tid; ch < d.nch; ch += kStageThreads)
+        tab[ch] = ch < d.nch_valid ? ch * d.scr_stride + (int)((d.chan0 + ch * hw + (int64_t)rr.lo * d.IW) & 7) : -1;
+}
+
+// Pass 2: scratch -> octet planes, one 16-byte row (8 channels) per position.
+__device__ __forceinline__ void stage_pass2(const StageDesc &d, const int *pos_tab, const int *ch_tab,
+                                            const uint8_t *scratch, uint8_t *dst, int tid)
+{
+    const int total = d.nplanes * d.plane_elems;
+    const uint16_t *scr = reinterpret_cast<const uint16_t *>(scratch);
+    for (int j = 0; j < d.nch / 8; ++j) {
+        int cb[8];
+        #pragma unroll
+        for (int e = 0; e < 8; ++e) cb[e] = ch_tab[j * 8 + e];
+        uint4 *dj = reinterpret_cast<uint4 *>(dst + (size_t)j * total * 16);
+        for (int q = tid; q < total; q += kStageThreads) {
+            const int off = pos_tab[q];
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            if (off >= 0) {
+                #pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    if (cb[e] >= 0) w[e >> 1] |= (uint32_t)scr[cb[e] + off] << ((e & 1) * 16);
             }
+            dj[q] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        *reinterpret_cast<uint4 *>(dst + (size_t)item * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -182,6 +202,8 @@ corr_kernel(const __grid_constant__ CorrParams p)
     uint8_t *stage_buf0 = smem;
     uint8_t *wring = smem + 2 * stage_bytes;
     uint8_t *scratch = wring + kWeightStages * wstage_bytes;
+    int *pos_tab = reinterpret_cast<int *>(scratch + (size_t)16 * p.scr_stride * 2);
+    int *ch_tab = pos_tab + p.nplanes * p.plane_elems;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -196,7 +218,7 @@ corr_kernel(const __grid_constant__ CorrParams p)
         ptx::mbar_init(ptx::smem_u32(&bar_acc), 1);
         ptx::fence_mbar_init();
     }
-    if (warp == 4) {
+    if (warp == kWarpAux) {
         ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), p.tmem_cols);
         ptx::tmem_relinquish();
     }
@@ -206,7 +228,7 @@ corr_kernel(const __grid_constant__ CorrParams p)
     const uint32_t tmem = tmem_base_sh;
     const int nblocks = p.nkc * p.ntaps;
 
-    if (warp < 4) {
+    if (warp < kStageWarps) {
         // ---------------- staging: one 16-channel chunk per step ----------------
         StageDesc d;
         d.U = p.U;
@@ -216,11 +238,13 @@ corr_kernel(const __grid_constant__ CorrParams p)
         d.nplanes = p.nplanes; d.Wp = p.Wp; d.plane_elems = p.plane_elems; d.rows_valid = 1 << 30;
         d.scr_stride = p.scr_stride; d.ph = p.plane_ph; d.pw = p.plane_pw;
         const RowRange rr = stage_rows(d);
+        if (p.ntaps > 0) build_pos_table(d, rr, pos_tab, threadIdx.x);
         for (int kc = 0; kc < p.nkc && p.ntaps > 0; ++kc) {
             const int b = kc & 1;
             d.chan0 = ((int64_t)n * p.G * p.Cu + (int64_t)g * p.Cu + kc * 16) * p.IH * p.IW;
             d.nch_valid = min(16, p.Cu - kc * 16);
-            stage_pass1(d, rr, scratch, threadIdx.x);
+            stage_pass1(d, rr, scratch, warp, lane);
+            build_ch_table(d, rr, ch_tab, threadIdx.x);
             ptx::cp_async_wait_all();
             bool bad = false;
             if (kc >= 2) bad = !ptx::mbar_wait(ptx::smem_u32(&bar_stage_empty[b]), ((kc >> 1) - 1) & 1, p.wait_ns);
@@ -229,12 +253,12 @@ corr_kernel(const __grid_constant__ CorrParams p)
                 if (threadIdx.x == 0) { abort_flag = 1; raise_device_error(p.err, DEVERR_WAIT_TIMEOUT); }
                 break;
             }
-            stage_pass2(d, rr, scratch, stage_buf0 + b * stage_bytes, threadIdx.x);
+            stage_pass2(d, pos_tab, ch_tab, scratch, stage_buf0 + b * stage_bytes, threadIdx.x);
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(ptx::smem_u32(&bar_stage_full[b]));
             ptx::named_sync(1, kStageThreads);
         }
-    } else if (warp == 4) {
+    } else if (warp == kWarpAux) {
         // ---------------- weight producer ----------------
         if (lane == 0 && p.ntaps > 0) {
             const int nstages = (nblocks + p.bps - 1) / p.bps;
@@ -260,7 +284,7 @@ corr_kernel(const __grid_constant__ CorrParams p)
                 if (!ptx::mbar_wait(ptx::smem_u32(&bar_w_full[s % kWeightStages]), (s / kWeightStages) & 1, kDrainNs))
                     raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
         }
-    } else {
+    } else if (warp == kWarpMma) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const uint32_t idesc = ptx::idesc_bf16(128, p.NT, 0, 0);
@@ -302,8 +326,10 @@ corr_kernel(const __grid_constant__ CorrParams p)
         }
     }
 
-    if (warp < 4) {
+    if (warp < kStageWarps) {
         // ---------------- epilogue: TMEM -> registers -> NCHW fp32 ----------------
+        // warp w reads TMEM lanes 32*(w%4).. and every other 16-column chunk (w/4)
+        const int lg = warp & 3, half = warp >> 2;
         bool ready = true;
         if (p.ntaps > 0) {
             ready = ptx::mbar_wait(ptx::smem_u32(&bar_acc), 0, p.wait_ns);
@@ -315,14 +341,14 @@ corr_kernel(const __grid_constant__ CorrParams p)
         const int64_t out_hw = (int64_t)p.OH * p.OW;
         float *vbase = p.V + ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv) * out_hw;
         for (int mb = 0; mb < p.MB; ++mb) {
-            const int m = mb * 128 + warp * 32 + lane;
+            const int m = mb * 128 + lg * 32 + lane;
             const int r = m / p.Wp, c = m - r * p.Wp;
             const bool valid = ready && m < p.TH * p.Wp && c < p.Qw && qh0 + r < p.Qh;
             const int64_t pix = (int64_t)(p.vs * (qh0 + r) + p.vr) * p.OW + (p.vs * c + p.vc);
-            for (int v0 = 0; v0 < p.NT; v0 += 16) {
+            for (int v0 = half * 16; v0 < p.NT; v0 += 32) {
                 uint32_t acc[16];
                 if (p.ntaps > 0 && ready) {
-                    ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(mb * p.NT + v0), acc);
+                    ptx::tmem_ld16(tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)(mb * p.NT + v0), acc);
                     ptx::tmem_ld_wait();
                 } else {
                     #pragma unroll
@@ -344,7 +370,7 @@ corr_kernel(const __grid_constant__ CorrParams p)
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 4) ptx::tmem_dealloc(tmem, p.tmem_cols);
+    if (warp == kWarpAux) ptx::tmem_dealloc(tmem, p.tmem_cols);
 }
 
 // ===========================================================================
@@ -402,6 +428,10 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
     const int buf_bytes = dy_bytes + x_bytes;
     uint8_t *scratch_dy = smem + 2 * buf_bytes;
     uint8_t *scratch_x = scratch_dy + (size_t)128 * p.scr_dy * 2;
+    int *pos_dy = reinterpret_cast<int *>(scratch_x + (size_t)p.NC * p.scr_x * 2);
+    int *pos_x = pos_dy + 128;
+    int *ch_dy = pos_x + p.nplanes * p.plane_elems;
+    int *ch_x = ch_dy + 128;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -412,7 +442,7 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
         ptx::mbar_init(ptx::smem_u32(&bar_acc), 1);
         ptx::fence_mbar_init();
     }
-    if (warp == 4) {
+    if (warp == kWarpAux) {
         ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), p.tmem_cols);
         ptx::tmem_relinquish();
     }
@@ -421,7 +451,7 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
-    if (warp < 4) {
+    if (warp < kStageWarps) {
         // Octets of the dy operand beyond o_lim are never staged: they only feed
         // accumulator rows that are dropped.  Zero them once so those rows stay finite.
         for (int b = 0; b < 2; ++b)
@@ -440,16 +470,25 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
         dx.IH = p.H; dx.IW = p.W; dx.nch = p.NC; dx.nch_valid = c_lim;
         dx.us = p.us; dx.col0 = p.col0; dx.nplanes = p.nplanes; dx.Wp = p.Wp; dx.plane_elems = p.plane_elems;
         dx.rows_valid = 1 << 30; dx.scr_stride = p.scr_x; dx.ph = p.plane_ph; dx.pw = p.plane_pw;
+        int table_rb = -1;
         for (int it = tile0, k = 0; it < tile1; ++it, ++k) {
             const int b = k & 1;
-            const int n = it / p.n_rowblk, qh0 = (it - n * p.n_rowblk) * p.TH;
+            // tiles are ordered image-fastest, so consecutive tiles share a row block
+            const int rb = it / p.N, n = it - rb * p.N, qh0 = rb * p.TH;
             dd.chan0 = ((int64_t)n * p.G * p.Cgo + (int64_t)g * p.Cgo + ot * 128) * p.Ho * p.Wo;
             dd.row_base = qh0;
             dx.chan0 = ((int64_t)n * p.G * p.Cgi + (int64_t)g * p.Cgi + ct * p.NC) * p.H * p.W;
             dx.row_base = qh0 + p.row0;
             const RowRange rd = stage_rows(dd), rx = stage_rows(dx);
-            stage_pass1(dd, rd, scratch_dy, threadIdx.x);
-            stage_pass1(dx, rx, scratch_x, threadIdx.x);
+            stage_pass1(dd, rd, scratch_dy, warp, lane);
+            stage_pass1(dx, rx, scratch_x, warp, lane);
+            if (rb != table_rb) {
+                build_pos_table(dd, rd, pos_dy, threadIdx.x);
+                build_pos_table(dx, rx, pos_x, threadIdx.x);
+                table_rb = rb;
+            }
+            build_ch_table(dd, rd, ch_dy, threadIdx.x);
+            build_ch_table(dx, rx, ch_x, threadIdx.x);
             ptx::cp_async_wait_all();
             bool bad = false;
             if (k >= 2) bad = !ptx::mbar_wait(ptx::smem_u32(&bar_empty[b]), ((k >> 1) - 1) & 1, p.wait_ns);
@@ -459,13 +498,13 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
                 break;
             }
             uint8_t *buf = smem + b * buf_bytes;
-            stage_pass2(dd, rd, scratch_dy, buf, threadIdx.x);
-            stage_pass2(dx, rx, scratch_x, buf + dy_bytes, threadIdx.x);
+            stage_pass2(dd, pos_dy, ch_dy, scratch_dy, buf, threadIdx.x);
+            stage_pass2(dx, pos_x, ch_x, scratch_x, buf + dy_bytes, threadIdx.x);
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(ptx::smem_u32(&bar_full[b]));
             ptx::named_sync(1, kStageThreads);
         }
-    } else if (warp == 5 && lane == 0) {
+    } else if (warp == kWarpMma && lane == 0) {
         // ---------------- MMA issuer ----------------
         const uint32_t idesc = ptx::idesc_bf16(128, p.NC, 1, 1);
         const uint32_t a_lbo = p.lbo_is_k ? 128u : (uint32_t)dy_octet_bytes;
@@ -499,8 +538,10 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
         if (!ptx::mbar_wait(ptx::smem_u32(&bar_acc), 0, kDrainNs)) raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
     }
 
-    if (warp < 4) {
+    if (warp < kStageWarps) {
         // ---------------- epilogue: D_tap[o][c] -> part[split][o][c][tap] ----------------
+        // warp w reads TMEM lanes 32*(w%4).. and every other tap accumulator (w/4)
+        const int lg = warp & 3, half = warp >> 2;
         const bool has_work = tile1 > tile0;
         bool ready = true;
         if (has_work) {
@@ -509,15 +550,15 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
             ptx::tc_fence_after();
         }
         ready = __all_sync(0xffffffffu, ready && !abort_flag);
-        const int o = warp * 32 + lane;
+        const int o = lg * 32 + lane;
         const int og = g * p.Cgo + ot * 128 + o;
         float *dst = p.part + (int64_t)split * ((int64_t)p.G * p.Cgo * p.Cgi * p.kHW);
-        for (int j = 0; j < ntg; ++j) {
+        for (int j = half; j < ntg; j += 2) {
             const int tp = tap0 + j;
             for (int c0 = 0; c0 < p.NC; c0 += 16) {
                 uint32_t acc[16];
                 if (has_work && ready) {
-                    ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(j * p.NC + c0), acc);
+                    ptx::tmem_ld16(tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)(j * p.NC + c0), acc);
                     ptx::tmem_ld_wait();
                 } else {
                     #pragma unroll
@@ -537,7 +578,7 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 4) ptx::tmem_dealloc(tmem, p.tmem_cols);
+    if (warp == kWarpAux) ptx::tmem_dealloc(tmem, p.tmem_cols);
 }
 
 // ===========================================================================
@@ -671,7 +712,13 @@ bool build_corr(const Geom &g, bool bwd_data, const std::vector<Tap> &taps, int 
     for (int i = 0; i < kMaxPlanes; ++i) { c.plane_ph[i] = tg.plane_ph[i]; c.plane_pw[i] = tg.plane_pw[i]; }
     c.row0 = tg.row0; c.col0 = tg.col0;
     c.Wp = Qw + tg.maxb;
-    // tile height: 128-position M blocks; least padded work, light penalty for re-streaming weights
+    // tile height: 128-position M blocks; least padded work, a light penalty for
+    // re-streaming weights with few M blocks, and a penalty when the accumulators
+    // need more than half of TMEM (one CTA per SM: no overlap between CTAs).
+    // Blockings whose shared memory does not fit are skipped.
+    const int max_off = tg.maxa * c.Wp + tg.maxb;
+    const int wblk = c.NT * 32;
+    c.bps = std::max(1, std::min(c.ntaps > 0 ? c.ntaps : 1, 16384 / wblk));
     long best = -1;
     for (int MB = 1; MB <= 4; ++MB) {
         if (MB * c.NT > 512) break;
@@ -679,25 +726,27 @@ bool build_corr(const Geom &g, bool bwd_data, const std::vector<Tap> &taps, int 
         if (TH < 1) continue;
         const int blocks = (Qh + TH - 1) / TH;
         const int MBe = (TH * c.Wp + 127) / 128;
-        const long cost = (long)blocks * MBe * 128 * (8 + 8 / MBe);
-        if (best < 0 || cost < best) { best = cost; c.MB = MBe; c.TH = TH; }
+        const int plane_elems = round_up(MBe * 128 + max_off, 8);
+        const int rows_touched = (plane_elems + c.Wp - 1) / c.Wp;
+        const int scr_stride = round_up((us * rows_touched + 1) * c.IW + 16, 8);
+        const size_t smem = (size_t)4 * c.nplanes * plane_elems * 16 + (size_t)kWeightStages * c.bps * wblk +
+                            (size_t)16 * scr_stride * 2 + (size_t)(c.nplanes * plane_elems + 16) * sizeof(int);
+        if (smem > kMaxSmem) continue;
+        long cost = (long)blocks * MBe * 128 * (8 + 8 / MBe);
+        if (next_pow2(MBe * c.NT) > 256) cost = cost * 5 / 4;
+        if (best < 0 || cost < best) {
+            best = cost;
+            c.MB = MBe; c.TH = TH; c.plane_elems = plane_elems; c.scr_stride = scr_stride;
+            L->smem = smem;
+        }
     }
-    if (best < 0) return false;   // a padded row longer than 512 positions: not served here
+    if (best < 0) return false;   // no blocking fits (e.g. a padded row longer than 512 positions)
     c.n_rowblk = (Qh + c.TH - 1) / c.TH;
-    const int max_off = tg.maxa * c.Wp + tg.maxb;
-    c.plane_elems = round_up(c.MB * 128 + max_off, 8);
     for (size_t i = 0; i < taps.size(); ++i) {
         c.tap_plane[i] = tg.tap_plane[i];
         c.tap_off[i] = tg.tap_a[i] * c.Wp + tg.tap_b[i];
     }
-    const int rows_touched = (c.plane_elems + c.Wp - 1) / c.Wp;
-    c.scr_stride = round_up((us * rows_touched + 1) * c.IW + 16, 8);
     c.tmem_cols = next_pow2(c.MB * c.NT);
-    const int wblk = c.NT * 32;
-    c.bps = std::max(1, std::min(c.ntaps > 0 ? c.ntaps : 1, 16384 / wblk));
-    const size_t stage_bytes = (size_t)2 * c.nplanes * c.plane_elems * 16;
-    L->smem = 2 * stage_bytes + (size_t)kWeightStages * c.bps * wblk + (size_t)16 * c.scr_stride * 2;
-    if (L->smem > kMaxSmem) return false;
     L->grid = g.G * g.N * c.n_rowblk * c.n_ntile;
     L->wpk_bytes = (size_t)g.G * c.n_ntile * c.nkc * std::max(1, c.ntaps) * wblk;
     PackParams &k = L->pk;
@@ -781,12 +830,14 @@ bool build_wgrad(const Geom &g, WgradLaunch *L)
     const int rows_touched = (w.plane_elems + w.Wp - 1) / w.Wp;
     w.scr_x = round_up((g.s * rows_touched + 1) * g.W + 16, 8);
     const size_t buf = (size_t)16 * 128 * 16 + (size_t)(w.NC / 8) * w.nplanes * w.plane_elems * 16;
-    L->smem = 2 * buf + (size_t)128 * w.scr_dy * 2 + (size_t)w.NC * w.scr_x * 2;
+    L->smem = 2 * buf + (size_t)128 * w.scr_dy * 2 + (size_t)w.NC * w.scr_x * 2 +
+              (size_t)(128 + w.nplanes * w.plane_elems + 128 + w.NC) * sizeof(int);
     if (L->smem > kMaxSmem) return false;
     const int base = g.G * w.n_otile * w.n_ctile * w.n_tgrp;
     const int total_tiles = g.N * w.n_rowblk;
     const int occ = (w.tmem_cols <= 256 && L->smem <= kMaxSmem / 2) ? 2 : 1;
-    const int S = std::max(1, std::min(total_tiles, (kNumSMs * occ + base - 1) / base));
+    // as many slices as fill the SMs in one wave (a partial second wave doubles the time)
+    const int S = std::max(1, std::min(total_tiles, (kNumSMs * occ) / base));
     w.tiles_per_split = (total_tiles + S - 1) / S;
     w.splits = (total_tiles + w.tiles_per_split - 1) / w.tiles_per_split;
     L->grid = base * w.splits;
