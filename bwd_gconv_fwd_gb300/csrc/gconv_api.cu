@@ -66,11 +66,6 @@ static int elementwise_grid(int64_t total)
     return (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)kNumSMs * 16));
 }
 
-void launch_reduce_splits(const float *part, int splits, int64_t count, float *out, cudaStream_t s)
-{
-    reduce_splits_kernel<<<elementwise_grid(count), kDirectThreads, 0, s>>>(part, splits, count, out);
-}
-
 // ---- CUDA-core plans ------------------------------------------------------
 
 static void direct_weight_split(const Geom &g, int *splits, int64_t *per_split)
@@ -86,7 +81,7 @@ static void direct_weight_split(const Geom &g, int *splits, int64_t *per_split)
 
 static void bias_split(const Geom &g, int *splits, int *n_per_split)
 {
-    int S = (4 * kNumSMs + g.Cout - 1) / g.Cout;
+    int S = (16 * kNumSMs + g.Cout - 1) / g.Cout;
     S = std::max(1, std::min(S, g.N));
     const int per = (g.N + S - 1) / S;
     *n_per_split = per;
@@ -203,7 +198,7 @@ static gconv_status run_pass(const int *geo, gconv_dtype dt, gconv_pass pass, co
 // Scratch of gconv_bwd_weight_noalloc: a file-scope device array, so a caller
 // that cannot allocate device memory still gets the split-K slices the weight
 // gradient needs.  Every device that loads this library keeps it until exit.
-constexpr size_t kNoAllocScratchBytes = (size_t)32 << 20;   // 32 MiB
+constexpr size_t kNoAllocScratchBytes = (size_t)128 << 20;   // 128 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of the array on the current device.  In host code the array's
@@ -310,7 +305,7 @@ gconv_status gconv_bwd_weight_noalloc(GEO_ARGS, gconv_dtype dtype, const void *x
     if (g.N == 0) return GCONV_OK;
     const Plan p = plan_pass(g, dtype, GCONV_PASS_BWD_WEIGHT);
     if (p.path < 0) return GCONV_ERR_UNSUPPORTED;
-    if (p.ws_bytes > kNoAllocScratchBytes) return GCONV_ERR_WORKSPACE;   // beyond the fixed 32 MiB scratch
+    if (p.ws_bytes > kNoAllocScratchBytes) return GCONV_ERR_WORKSPACE;   // beyond the fixed 128 MiB scratch
     void *scratch = nullptr;
     if (p.ws_bytes > 0) {
         scratch = noalloc_scratch_ptr();

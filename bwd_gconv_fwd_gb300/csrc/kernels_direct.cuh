@@ -177,8 +177,8 @@ reduce_splits_kernel(const float *__restrict__ part, int splits, int64_t count,
 }
 
 // ---------------------------------------------------------------------------
-// Sum of the contiguous range [begin, begin + len) of a bf16 / fp32 array of
-// `array_len` elements (base 16-byte aligned) by one warp, with aligned 16-byte
+// Per-lane share of the sum of the contiguous range [begin, begin + len) of a
+// bf16 / fp32 array of `array_len` elements (base 16-byte aligned) over one warp, with aligned 16-byte
 // loads (elements outside the range are masked), so it streams at full width
 // whatever the alignment of `begin`.  A final partial chunk of the array is read
 // element by element, so no load leaves the array.  Fixed order.
@@ -208,9 +208,7 @@ __device__ __forceinline__ float warp_range_sum(const T *__restrict__ base, int6
             }
         }
     }
-    #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    return acc;
+    return acc;   // this lane's share; the caller reduces across the warp
 }
 
 // Bias gradient.  Block (o, split) sums planes dy[n, o, :, :] for n in its range;
@@ -227,6 +225,8 @@ bias_grad_kernel(Geom g, const T *__restrict__ dy, float *__restrict__ out, int 
     float acc = 0.f;
     for (int n = n0 + warp; n < n1; n += nwarps)
         acc += warp_range_sum(dy, ((int64_t)n * g.Cout + o) * HWo, HWo, (int64_t)g.N * g.Cout * HWo);
+    #pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     __syncthreads();
     if ((threadIdx.x & 31) == 0) red[warp] = acc;
     __syncthreads();

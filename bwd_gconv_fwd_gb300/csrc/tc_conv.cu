@@ -38,6 +38,7 @@
 
 #include <algorithm>
 #include <vector>
+#include <tuple>
 
 namespace gconv {
 
@@ -374,64 +375,122 @@ corr_kernel(const __grid_constant__ CorrParams p)
 }
 
 // ===========================================================================
-// Backward-weight kernel
+// Blocked copy of an NCHW activation for the tensor-core kernels
 // ===========================================================================
+// out[n][g][j][r][c][0..63] = in[n][g*Cg + 64*j + e][r + r_off][c + c_off], zero outside
+// the image and for channels past Cg.  One 128-byte row per (r, c): 64 channels of one
+// position, so a tile of consecutive positions is a contiguous run of rows.  The
+// transpose goes through shared memory; loads run along image rows, stores are
+// 16-byte vectors along the output rows.  HBM-bound.
+struct BlockifyParams {
+    const __nv_bfloat16 *in;
+    __nv_bfloat16 *out;
+    int N, G, Cg, nchunk, IH, IW, R, C, r_off, c_off;
+};
+
+constexpr int kBlockifyThreads = 256;
+
+__global__ void __launch_bounds__(kBlockifyThreads)
+blockify_kernel(const __grid_constant__ BlockifyParams p)
+{
+    extern __shared__ uint16_t tile[];            // [64][C + 1]
+    const int ld = p.C + 1;
+    int t = blockIdx.x;
+    const int r = t % p.R; t /= p.R;
+    const int j = t % p.nchunk; t /= p.nchunk;
+    const int g = t % p.G;
+    const int n = t / p.G;
+    const int row = r + p.r_off;
+    const bool row_ok = row >= 0 && row < p.IH;
+    const int64_t plane = (int64_t)p.IH * p.IW;
+    const uint16_t *src = reinterpret_cast<const uint16_t *>(p.in) +
+                          ((int64_t)n * p.G * p.Cg + (int64_t)g * p.Cg + 64 * j) * plane + (int64_t)row * p.IW;
+    for (int idx = threadIdx.x; idx < 64 * p.C; idx += kBlockifyThreads) {
+        const int e = idx / p.C, c = idx - e * p.C;
+        const int col = c + p.c_off;
+        uint16_t v = 0;
+        if (row_ok && col >= 0 && col < p.IW && 64 * j + e < p.Cg) v = __ldg(src + (int64_t)e * plane + col);
+        tile[e * ld + c] = v;
+    }
+    __syncthreads();
+    uint4 *dst = reinterpret_cast<uint4 *>(p.out) + ((((int64_t)n * p.G + g) * p.nchunk + j) * p.R + r) * p.C * 8;
+    for (int idx = threadIdx.x; idx < p.C * 8; idx += kBlockifyThreads) {
+        const int c = idx >> 3, k = idx & 7;
+        uint32_t w[4];
+        #pragma unroll
+        for (int q = 0; q < 4; ++q)
+            w[q] = (uint32_t)tile[(k * 8 + 2 * q) * ld + c] | ((uint32_t)tile[(k * 8 + 2 * q + 1) * ld + c] << 16);
+        dst[idx] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// ===========================================================================
+// Backward-weight kernel (stride 1)
+// ===========================================================================
+// D[o][c] for every tap, K = output positions of the padded grid (pitch Wp = padded
+// input width).  Both operands are MN-major with 128-byte swizzle, staged straight
+// from the blocked copies of gradOutput and x by 16-byte cp.async: a tile is a
+// contiguous run of 128-byte position rows, and piece k of row m lands at
+// ((k ^ (m & 7)) * 16) in its row (the pattern the tensor core reads back from a
+// 1024-byte aligned region, whatever the start row).  A "job" packs up to four taps
+// that lie at equal position distances into the N dimension of one MMA: N-chunk j
+// (64 channels) of the input operand is read `delta` positions further on by
+// setting the descriptor's MN-chunk stride to delta rows.  A 5x5 kernel therefore
+// runs as six N = 256 MMAs and one N = 64 MMA per K step.
+constexpr int kMaxJobs = 32;
+
 struct WgradParams {
-    const __nv_bfloat16 *X;      // x  [N][G*Cgi][H][W]
-    const __nv_bfloat16 *DY;     // dy [N][G*Cgo][Ho][Wo]
-    float *part;                 // partial dw per split: [splits][C_out][Cgi][kH][kW]
+    const __nv_bfloat16 *XT;     // blocked x  [N][G][ncx][Rx][Wp][64] (padded grid, zero padding)
+    const __nv_bfloat16 *DYT;    // blocked dy [N][G][ncy][Ho][Wp][64] (zero past column Wo)
+    float *part;                 // partial dw per split: [splits][kH*kW][C_out][Cgi]
     unsigned int *err;
     uint64_t wait_ns;
-    int N, G, Cgi, Cgo, H, W, Ho, Wo, kHW;
-    int us, row0, col0;          // x plane sampling (as in the forward)
-    int TH, Wp, n_rowblk;        // output rows per tile (128 positions), padded pitch
-    int nplanes, plane_elems;    // x planes
-    int n_otile, n_ctile, NC;    // o tiles (128 rows), c tiles, columns per tap (c tile, multiple of 16)
-    int n_tgrp, TG, ntaps;       // tap groups, taps per group
-    int splits, tiles_per_split; // over N*n_rowblk tiles
-    int tmem_cols;
-    int scr_dy, scr_x;           // scratch elements per channel
-    int lbo_is_k;                // MN-major descriptor: 1 if LBO is the K-direction stride
-    int plane_ph[kMaxPlanes], plane_pw[kMaxPlanes];
-    int tap_plane[kMaxTaps], tap_off[kMaxTaps], tap_k[kMaxTaps];
+    int N, G, Cgi, Cgo, kHW;
+    int Ho, Wp, Rx, ncx, ncy;
+    int TH, n_rowblk;            // output rows per tile (<= 128 positions), row blocks per image
+    int plane_elems;             // x positions staged per tile
+    int n_otile, n_ctile;        // 128-channel gradOutput tiles, 64-channel input tiles
+    int n_tgrp;                  // job groups (one TMEM allocation each)
+    int splits;                  // partial slices in the workspace (the largest group split count)
+    int cta_per_cg;              // CTAs per (group, o tile, c tile): sum of the group split counts
+    int grp_splits[kMaxJobs];    // split count of each job group
+    int grp_cta0[kMaxJobs + 1];  // first CTA index of each job group within cta_per_cg
+    int grp_first[kMaxJobs + 1]; // jobs of group gi: [grp_first[gi], grp_first[gi+1])
+    int grp_cols[kMaxJobs];      // TMEM columns allocated by group gi (power of two)
+    int job_off[kMaxJobs], job_delta[kMaxJobs], job_count[kMaxJobs], job_col[kMaxJobs];
+    int job_tapk[kMaxJobs][4];   // kh*kW + kw of the packed taps
 };
 
 __global__ void __launch_bounds__(kTcThreads, 1)
 wgrad_kernel(const __grid_constant__ WgradParams p)
 {
-    extern __shared__ __align__(1024) uint8_t smem[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[2], bar_empty[2], bar_acc;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
 
+    // 128-byte swizzle regions need 1024-byte alignment
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int t = blockIdx.x;
-    const int split = t % p.splits; t /= p.splits;
-    const int tg = t % p.n_tgrp; t /= p.n_tgrp;
+    const int r = t % p.cta_per_cg; t /= p.cta_per_cg;
     const int ct = t % p.n_ctile; t /= p.n_ctile;
     const int ot = t % p.n_otile;
     const int g = t / p.n_otile;
-    const int tap0 = tg * p.TG;
-    const int ntg = min(p.TG, p.ntaps - tap0);
+    int gi = 0;
+    while (gi + 1 < p.n_tgrp && r >= p.grp_cta0[gi + 1]) ++gi;
+    const int split = r - p.grp_cta0[gi];
+    const int job0 = p.grp_first[gi], job1 = p.grp_first[gi + 1];
+    const int tmem_cols = p.grp_cols[gi];
     const int total_tiles = p.N * p.n_rowblk;
-    const int tile0 = split * p.tiles_per_split;
-    const int tile1 = min(total_tiles, tile0 + p.tiles_per_split);
-    const int o_lim = min(128, p.Cgo - ot * 128);     // valid gradOutput channels of this tile
-    const int c_lim = min(p.NC, p.Cgi - ct * p.NC);   // valid input channels of this tile
-    const int dy_oct = (o_lim + 7) / 8;
+    const int tiles_per_split = (total_tiles + p.grp_splits[gi] - 1) / p.grp_splits[gi];
+    const int tile0 = split * tiles_per_split;
+    const int tile1 = min(total_tiles, tile0 + tiles_per_split);
+    const int o_lim = min(128, p.Cgo - ot * 128);    // valid gradOutput channels of this tile
+    const int c_lim = min(64, p.Cgi - ct * 64);      // valid input channels of this tile
 
-    const int dy_octet_bytes = 128 * 16;              // 128 positions per octet
-    const int dy_bytes = 16 * dy_octet_bytes;         // room for 16 octets (M = 128)
-    const int x_plane_bytes = p.plane_elems * 16;
-    const int x_octet_bytes = p.nplanes * x_plane_bytes;
-    const int x_bytes = (p.NC / 8) * x_octet_bytes;
-    const int buf_bytes = dy_bytes + x_bytes;
-    uint8_t *scratch_dy = smem + 2 * buf_bytes;
-    uint8_t *scratch_x = scratch_dy + (size_t)128 * p.scr_dy * 2;
-    int *pos_dy = reinterpret_cast<int *>(scratch_x + (size_t)p.NC * p.scr_x * 2);
-    int *pos_x = pos_dy + 128;
-    int *ch_dy = pos_x + p.nplanes * p.plane_elems;
-    int *ch_x = ch_dy + 128;
+    const int dy_bytes = 2 * 128 * 128;              // two 64-channel chunks x 128 positions
+    const int buf_bytes = dy_bytes + p.plane_elems * 128;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -443,7 +502,7 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
         ptx::fence_mbar_init();
     }
     if (warp == kWarpAux) {
-        ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), p.tmem_cols);
+        ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), tmem_cols);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
@@ -452,65 +511,55 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
     const uint32_t tmem = tmem_base_sh;
 
     if (warp < kStageWarps) {
-        // Octets of the dy operand beyond o_lim are never staged: they only feed
-        // accumulator rows that are dropped.  Zero them once so those rows stay finite.
-        for (int b = 0; b < 2; ++b)
-            for (int i = threadIdx.x; i < (16 - dy_oct) * 128; i += kStageThreads)
-                *reinterpret_cast<uint4 *>(smem + b * buf_bytes + (size_t)dy_oct * dy_octet_bytes + (size_t)i * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-        // ---------------- staging: dy tile + x halo per (image, row block) ----------------
-        const int zph[1] = {0};
-        StageDesc dd;   // gradOutput: 128 positions of the padded grid, one plane
-        dd.U = p.DY; dd.U_elems = (int64_t)p.N * p.G * p.Cgo * p.Ho * p.Wo;
-        dd.IH = p.Ho; dd.IW = p.Wo; dd.nch = dy_oct * 8; dd.nch_valid = o_lim;
-        dd.us = 1; dd.col0 = 0; dd.nplanes = 1; dd.Wp = p.Wp; dd.plane_elems = 128; dd.rows_valid = p.TH;
-        dd.scr_stride = p.scr_dy; dd.ph = zph; dd.pw = zph;
-        StageDesc dx;   // input halo, stride-phase planes
-        dx.U = p.X; dx.U_elems = (int64_t)p.N * p.G * p.Cgi * p.H * p.W;
-        dx.IH = p.H; dx.IW = p.W; dx.nch = p.NC; dx.nch_valid = c_lim;
-        dx.us = p.us; dx.col0 = p.col0; dx.nplanes = p.nplanes; dx.Wp = p.Wp; dx.plane_elems = p.plane_elems;
-        dx.rows_valid = 1 << 30; dx.scr_stride = p.scr_x; dx.ph = p.plane_ph; dx.pw = p.plane_pw;
-        int table_rb = -1;
+        // ---------------- staging: cp.async of position rows, double buffered ----------------
+        const int plane_y = p.Ho * p.Wp, plane_x = p.Rx * p.Wp;
+        const int th_pos = p.TH * p.Wp;
+        auto issue = [&](int it, int b) {
+            const int rb = it / p.N, n = it - rb * p.N;
+            const int pos0 = rb * p.TH * p.Wp;
+            const uint32_t buf = ptx::smem_u32(smem + b * buf_bytes);
+            // gradOutput: chunks 2*ot, 2*ot+1; positions past the tile's rows read as zero
+            for (int idx = threadIdx.x; idx < 2 * 128 * 8; idx += kStageThreads) {
+                const int h = idx >> 10, m = (idx >> 3) & 127, k = idx & 7;
+                const int chunk = 2 * ot + h;
+                const bool ok = m < th_pos && pos0 + m < plane_y && chunk < p.ncy;
+                const __nv_bfloat16 *src = ok ? p.DYT + ((((int64_t)n * p.G + g) * p.ncy + chunk) * plane_y + pos0 + m) * 64 + k * 8
+                                              : p.DYT;
+                ptx::cp_async16(buf + (uint32_t)(h * 16384 + m * 128 + ((k ^ (m & 7)) << 4)), src, ok ? 16u : 0u);
+            }
+            // input: chunk ct, positions [pos0, pos0 + plane_elems) of the padded plane
+            for (int idx = threadIdx.x; idx < p.plane_elems * 8; idx += kStageThreads) {
+                const int m = idx >> 3, k = idx & 7;
+                const bool ok = pos0 + m < plane_x;
+                const __nv_bfloat16 *src = ok ? p.XT + ((((int64_t)n * p.G + g) * p.ncx + ct) * plane_x + pos0 + m) * 64 + k * 8
+                                              : p.XT;
+                ptx::cp_async16(buf + (uint32_t)(dy_bytes + m * 128 + ((k ^ (m & 7)) << 4)), src, ok ? 16u : 0u);
+            }
+        };
+        if (tile1 > tile0) issue(tile0, 0);
+        ptx::cp_async_commit();
         for (int it = tile0, k = 0; it < tile1; ++it, ++k) {
             const int b = k & 1;
-            // tiles are ordered image-fastest, so consecutive tiles share a row block
-            const int rb = it / p.N, n = it - rb * p.N, qh0 = rb * p.TH;
-            dd.chan0 = ((int64_t)n * p.G * p.Cgo + (int64_t)g * p.Cgo + ot * 128) * p.Ho * p.Wo;
-            dd.row_base = qh0;
-            dx.chan0 = ((int64_t)n * p.G * p.Cgi + (int64_t)g * p.Cgi + ct * p.NC) * p.H * p.W;
-            dx.row_base = qh0 + p.row0;
-            const RowRange rd = stage_rows(dd), rx = stage_rows(dx);
-            stage_pass1(dd, rd, scratch_dy, warp, lane);
-            stage_pass1(dx, rx, scratch_x, warp, lane);
-            if (rb != table_rb) {
-                build_pos_table(dd, rd, pos_dy, threadIdx.x);
-                build_pos_table(dx, rx, pos_x, threadIdx.x);
-                table_rb = rb;
-            }
-            build_ch_table(dd, rd, ch_dy, threadIdx.x);
-            build_ch_table(dx, rx, ch_x, threadIdx.x);
-            ptx::cp_async_wait_all();
             bool bad = false;
-            if (k >= 2) bad = !ptx::mbar_wait(ptx::smem_u32(&bar_empty[b]), ((k >> 1) - 1) & 1, p.wait_ns);
-            bad = ptx::bar_red_or(1, kStageThreads, bad || abort_flag);
-            if (bad) {
-                if (threadIdx.x == 0) { abort_flag = 1; raise_device_error(p.err, DEVERR_WAIT_TIMEOUT); }
-                break;
+            if (it + 1 < tile1) {
+                // the other buffer must be free before the next tile's copies go in
+                if (k + 1 >= 2)
+                    bad = !ptx::mbar_wait(ptx::smem_u32(&bar_empty[b ^ 1]), ((k + 1) / 2 - 1) & 1, p.wait_ns);
+                bad = ptx::bar_red_or(1, kStageThreads, bad || abort_flag);
+                if (bad) {
+                    if (threadIdx.x == 0) { abort_flag = 1; raise_device_error(p.err, DEVERR_WAIT_TIMEOUT); }
+                    break;
+                }
+                issue(it + 1, b ^ 1);
             }
-            uint8_t *buf = smem + b * buf_bytes;
-            stage_pass2(dd, pos_dy, ch_dy, scratch_dy, buf, threadIdx.x);
-            stage_pass2(dx, pos_x, ch_x, scratch_x, buf + dy_bytes, threadIdx.x);
+            ptx::cp_async_commit();
+            ptx::cp_async_wait_group<1>();           // this tile's rows have landed
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(ptx::smem_u32(&bar_full[b]));
-            ptx::named_sync(1, kStageThreads);
         }
+        ptx::cp_async_wait_group<0>();               // nothing may land after the CTA exits
     } else if (warp == kWarpMma && lane == 0) {
         // ---------------- MMA issuer ----------------
-        const uint32_t idesc = ptx::idesc_bf16(128, p.NC, 1, 1);
-        const uint32_t a_lbo = p.lbo_is_k ? 128u : (uint32_t)dy_octet_bytes;
-        const uint32_t a_sbo = p.lbo_is_k ? (uint32_t)dy_octet_bytes : 128u;
-        const uint32_t b_lbo = p.lbo_is_k ? 128u : (uint32_t)x_octet_bytes;
-        const uint32_t b_sbo = p.lbo_is_k ? (uint32_t)x_octet_bytes : 128u;
         bool ok = true;
         for (int it = tile0, k = 0; it < tile1; ++it, ++k) {
             const int b = k & 1;
@@ -519,12 +568,13 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
             const uint32_t dyb = ptx::smem_u32(smem + b * buf_bytes);
             const uint32_t xbb = dyb + (uint32_t)dy_bytes;
             for (int ks = 0; ks < 8; ++ks) {            // 8 K steps of 16 positions
-                const uint64_t adesc = ptx::smem_desc(dyb + (uint32_t)(ks * 16 * 16), a_lbo, a_sbo, 0);
-                for (int j = 0; j < ntg; ++j) {
-                    const int tp = tap0 + j;
-                    const uint32_t bs = xbb + (uint32_t)(p.tap_plane[tp] * x_plane_bytes + (p.tap_off[tp] + ks * 16) * 16);
-                    const uint64_t bdesc = ptx::smem_desc(bs, b_lbo, b_sbo, 0);
-                    ptx::mma_f16(tmem + (uint32_t)(j * p.NC), adesc, bdesc, idesc, (k > 0 || ks > 0) ? 1u : 0u);
+                // gradOutput: M = 128 channels as two 64-channel chunks 16 KB apart
+                const uint64_t adesc = ptx::smem_desc(dyb + (uint32_t)(ks * 16 * 128), 128u * 128u, 1024u, 2);
+                for (int jb = job0; jb < job1; ++jb) {
+                    const uint32_t bs = xbb + (uint32_t)((p.job_off[jb] + ks * 16) * 128);
+                    const uint64_t bdesc = ptx::smem_desc(bs, (uint32_t)(p.job_delta[jb] * 128), 1024u, 2);
+                    const uint32_t idesc = ptx::idesc_bf16(128, p.job_count[jb] * 64, 1, 1);
+                    ptx::mma_f16(tmem + (uint32_t)p.job_col[jb], adesc, bdesc, idesc, (k > 0 || ks > 0) ? 1u : 0u);
                 }
             }
             ptx::mma_commit(ptx::smem_u32(&bar_empty[b]));
@@ -539,8 +589,8 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
     }
 
     if (warp < kStageWarps) {
-        // ---------------- epilogue: D_tap[o][c] -> part[split][o][c][tap] ----------------
-        // warp w reads TMEM lanes 32*(w%4).. and every other tap accumulator (w/4)
+        // ---------------- epilogue: D_tap[o][c] -> part[split][tap][o][c] ----------------
+        // warp w reads TMEM lanes 32*(w%4).. and every other packed tap (w/4)
         const int lg = warp & 3, half = warp >> 2;
         const bool has_work = tile1 > tile0;
         bool ready = true;
@@ -553,32 +603,54 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
         const int o = lg * 32 + lane;
         const int og = g * p.Cgo + ot * 128 + o;
         float *dst = p.part + (int64_t)split * ((int64_t)p.G * p.Cgo * p.Cgi * p.kHW);
-        for (int j = half; j < ntg; j += 2) {
-            const int tp = tap0 + j;
-            for (int c0 = 0; c0 < p.NC; c0 += 16) {
-                uint32_t acc[16];
-                if (has_work && ready) {
-                    ptx::tmem_ld16(tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)(j * p.NC + c0), acc);
-                    ptx::tmem_ld_wait();
-                } else {
-                    #pragma unroll
-                    for (int e = 0; e < 16; ++e) acc[e] = 0u;
-                }
-                if (o < o_lim && ready) {
-                    #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        if (c0 + e < c_lim) {
-                            const int c = ct * p.NC + c0 + e;
-                            dst[((int64_t)og * p.Cgi + c) * p.kHW + p.tap_k[tp]] = __uint_as_float(acc[e]);
-                        }
+        int pair = 0;
+        for (int jb = job0; jb < job1; ++jb)
+            for (int j = 0; j < p.job_count[jb]; ++j, ++pair) {
+                if ((pair & 1) != half) continue;
+                const int tapk = p.job_tapk[jb][j];
+                for (int c0 = 0; c0 < 64; c0 += 16) {
+                    uint32_t acc[16];
+                    if (has_work && ready) {
+                        ptx::tmem_ld16(tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)(p.job_col[jb] + j * 64 + c0), acc);
+                        ptx::tmem_ld_wait();
+                    } else {
+                        #pragma unroll
+                        for (int e = 0; e < 16; ++e) acc[e] = 0u;
+                    }
+                    if (o < o_lim && ready && c0 < c_lim) {
+                        // 16 consecutive input channels of one (tap, o): contiguous per thread
+                        float *row = dst + ((int64_t)tapk * p.G * p.Cgo + og) * p.Cgi + ct * 64 + c0;
+                        #pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (c0 + e < c_lim) row[e] = __uint_as_float(acc[e]);
                     }
                 }
             }
-        }
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == kWarpAux) ptx::tmem_dealloc(tmem, p.tmem_cols);
+    if (warp == kWarpAux) ptx::tmem_dealloc(tmem, tmem_cols);
+}
+
+struct ReduceParams {
+    const float *part;
+    float *dw;
+    int O, Cgi, kHW;
+    int tap_splits[kMaxTaps];   // slices written for each tap (its job group's split count)
+};
+
+__global__ void wgrad_reduce_kernel(const __grid_constant__ ReduceParams p)
+{
+    const int64_t count = (int64_t)p.kHW * p.O * p.Cgi;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (int64_t)gridDim.x * blockDim.x) {
+        const int c = (int)(i % p.Cgi);
+        const int64_t t2 = i / p.Cgi;
+        const int o = (int)(t2 % p.O);
+        const int tap = (int)(t2 / p.O);
+        float s = 0.f;
+        for (int k = 0; k < p.tap_splits[tap]; ++k) s += p.part[(int64_t)k * count + i];
+        p.dw[((int64_t)o * p.Cgi + c) * p.kHW + tap] = s;
+    }
 }
 
 // ===========================================================================
@@ -784,64 +856,164 @@ bool build_bwd_data_phase(const Geom &g, int rh, int rw, CorrLaunch *L, bool *em
     return build_corr(g, true, taps, Qh, Qw, g.s, rh, rw, 1, L);
 }
 
+
+
+// Covers the taps with jobs of up to four taps at equal position distances (a row
+// of taps first, else a column), then packs jobs into TMEM groups of <= 512 columns.
+bool build_wgrad_jobs(const TapGeometry &tg, const std::vector<Tap> &taps, int Wp, WgradParams *w)
+{
+    const int T = (int)taps.size();
+    std::vector<int> off(T), used(T, 0);
+    for (int i = 0; i < T; ++i) off[i] = tg.tap_a[i] * Wp + tg.tap_b[i];
+    auto find = [&](int a, int b) {
+        for (int i = 0; i < T; ++i)
+            if (!used[i] && tg.tap_a[i] == a && tg.tap_b[i] == b) return i;
+        return -1;
+    };
+    struct Job { int first, delta, count; int tap[4]; };
+    std::vector<Job> jobs;
+    while (true) {
+        int s0 = -1;   // remaining tap with the smallest (a, b)
+        for (int i = 0; i < T; ++i)
+            if (!used[i] && (s0 < 0 || std::make_pair(tg.tap_a[i], tg.tap_b[i]) < std::make_pair(tg.tap_a[s0], tg.tap_b[s0])))
+                s0 = i;
+        if (s0 < 0) break;
+        const int a = tg.tap_a[s0], b = tg.tap_b[s0];
+        auto run = [&](bool along_row, Job *J) {
+            J->first = off[s0]; J->count = 1; J->tap[0] = s0; J->delta = 1;
+            int nxt = -1, best = 1 << 30;
+            for (int i = 0; i < T; ++i) {   // nearest following tap in that direction
+                if (used[i] || i == s0) continue;
+                if (along_row && tg.tap_a[i] == a && tg.tap_b[i] > b && tg.tap_b[i] - b < best) { best = tg.tap_b[i] - b; nxt = i; }
+                if (!along_row && tg.tap_b[i] == b && tg.tap_a[i] > a && tg.tap_a[i] - a < best) { best = tg.tap_a[i] - a; nxt = i; }
+            }
+            if (nxt < 0) return;
+            const int da = along_row ? 0 : best, db = along_row ? best : 0;
+            J->delta = da * Wp + db;
+            int cur = nxt;
+            while (cur >= 0 && J->count < 4) {
+                J->tap[J->count++] = cur;
+                cur = find(tg.tap_a[cur] + da, tg.tap_b[cur] + db);
+                if (cur == s0) cur = -1;
+            }
+        };
+        Job jr, jc;
+        run(true, &jr);
+        run(false, &jc);
+        const Job &J = jr.count >= jc.count ? jr : jc;
+        for (int c = 0; c < J.count; ++c) used[J.tap[c]] = 1;
+        jobs.push_back(J);
+    }
+    if ((int)jobs.size() > kMaxJobs) return false;
+    std::vector<int> order(jobs.size());
+    for (size_t i = 0; i < jobs.size(); ++i) order[i] = (int)i;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return jobs[x].count > jobs[y].count; });
+    std::vector<std::vector<int>> groups;
+    std::vector<int> gcols;
+    for (int ji : order) {
+        const int cols = jobs[ji].count * 64;
+        size_t gsel = groups.size();
+        for (size_t gq = 0; gq < groups.size(); ++gq)
+            if (gcols[gq] + cols <= 512) { gsel = gq; break; }
+        if (gsel == groups.size()) { groups.push_back({}); gcols.push_back(0); }
+        groups[gsel].push_back(ji);
+        gcols[gsel] += cols;
+    }
+    int n = 0;
+    w->n_tgrp = (int)groups.size();
+    for (size_t gq = 0; gq < groups.size(); ++gq) {
+        w->grp_first[gq] = n;
+        int col = 0;
+        for (int ji : groups[gq]) {
+            const Job &J = jobs[ji];
+            w->job_off[n] = J.first; w->job_delta[n] = J.delta; w->job_count[n] = J.count; w->job_col[n] = col;
+            for (int c = 0; c < 4; ++c) w->job_tapk[n][c] = c < J.count ? taps[J.tap[c]].k : 0;
+            col += J.count * 64;
+            ++n;
+        }
+        w->grp_cols[gq] = next_pow2(col);
+    }
+    w->grp_first[groups.size()] = n;
+    return true;
+}
+
 struct WgradLaunch {
     WgradParams wp;
+    BlockifyParams bx, by;
     size_t smem = 0;
+    size_t part_bytes = 0, xt_bytes = 0, yt_bytes = 0;
     size_t ws_bytes = 0;
     int grid = 0;
 };
 
-// MN-major no-swizzle descriptors: which of LBO / SBO holds the K-direction stride.
-constexpr int kMnLboIsK = 1;
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 bool build_wgrad(const Geom &g, WgradLaunch *L)
 {
-    if (g.s > 2 || g.Cgi < 8 || g.Cgo < 16) return false;
+    if (g.s != 1 || g.Cgi < 8 || g.Cgo < 16) return false;
     const std::vector<Tap> taps = forward_taps(g);
     if ((int)taps.size() > kMaxTaps) return false;
     TapGeometry tg;
-    if (!tap_geometry(taps, g.s, &tg)) return false;
+    if (!tap_geometry(taps, 1, &tg)) return false;
     WgradParams &w = L->wp;
     w = WgradParams{};
-    w.N = g.N; w.G = g.G; w.Cgi = g.Cgi; w.Cgo = g.Cgo; w.H = g.H; w.W = g.W; w.Ho = g.Ho; w.Wo = g.Wo;
-    w.kHW = g.kH * g.kW;
-    w.us = g.s; w.row0 = tg.row0; w.col0 = tg.col0;
-    w.Wp = g.Wo + tg.maxb;
+    w.N = g.N; w.G = g.G; w.Cgi = g.Cgi; w.Cgo = g.Cgo; w.kHW = g.kH * g.kW;
+    w.Ho = g.Ho;
+    w.Wp = g.Wo + tg.maxb;            // = W + pad_left + pad_right for stride 1
+    w.Rx = g.Ho + tg.maxa;            // = H + pad_top + pad_bottom
+    w.ncx = (g.Cgi + 63) / 64;
+    w.ncy = (g.Cgo + 63) / 64;
     w.TH = std::min(128 / w.Wp, g.Ho);
     if (w.TH < 1) return false;
     w.n_rowblk = (g.Ho + w.TH - 1) / w.TH;
-    w.nplanes = tg.nplanes;
-    for (int i = 0; i < kMaxPlanes; ++i) { w.plane_ph[i] = tg.plane_ph[i]; w.plane_pw[i] = tg.plane_pw[i]; }
-    w.plane_elems = round_up(128 + tg.maxa * w.Wp + tg.maxb, 8);
-    w.ntaps = (int)taps.size();
-    for (int i = 0; i < w.ntaps; ++i) {
-        w.tap_plane[i] = tg.tap_plane[i];
-        w.tap_off[i] = tg.tap_a[i] * w.Wp + tg.tap_b[i];
-        w.tap_k[i] = taps[i].k;
-    }
-    w.NC = std::min(256, round_up(g.Cgi, 16));
-    w.n_ctile = (g.Cgi + w.NC - 1) / w.NC;
+    // positions read: 128 of the tile plus the farthest tap, plus the packed-tap chunks beyond it
+    w.plane_elems = round_up(128 + tg.maxa * w.Wp + tg.maxb + 8, 8);
+    if (!build_wgrad_jobs(tg, taps, w.Wp, &w)) return false;
+    for (int jb = 0; jb < w.grp_first[w.n_tgrp]; ++jb)
+        if (w.job_off[jb] + (w.job_count[jb] - 1) * w.job_delta[jb] + 128 > w.plane_elems) return false;
+    w.n_ctile = w.ncx;
     w.n_otile = (g.Cgo + 127) / 128;
-    w.TG = std::max(1, std::min(w.ntaps, 512 / w.NC));
-    w.n_tgrp = (w.ntaps + w.TG - 1) / w.TG;
-    w.tmem_cols = next_pow2(w.TG * w.NC);
-    w.lbo_is_k = kMnLboIsK;
-    w.scr_dy = round_up((w.TH + 1) * g.Wo + 16, 8);
-    const int rows_touched = (w.plane_elems + w.Wp - 1) / w.Wp;
-    w.scr_x = round_up((g.s * rows_touched + 1) * g.W + 16, 8);
-    const size_t buf = (size_t)16 * 128 * 16 + (size_t)(w.NC / 8) * w.nplanes * w.plane_elems * 16;
-    L->smem = 2 * buf + (size_t)128 * w.scr_dy * 2 + (size_t)w.NC * w.scr_x * 2 +
-              (size_t)(128 + w.nplanes * w.plane_elems + 128 + w.NC) * sizeof(int);
+    L->smem = 1024 + 2 * ((size_t)2 * 128 * 128 + (size_t)w.plane_elems * 128);
     if (L->smem > kMaxSmem) return false;
-    const int base = g.G * w.n_otile * w.n_ctile * w.n_tgrp;
+    // One wave of CTAs (a partial second wave doubles the time), shared among the job
+    // groups in proportion to their MMA work per K step plus the staging share.
+    const int outer = g.G * w.n_otile * w.n_ctile;
     const int total_tiles = g.N * w.n_rowblk;
-    const int occ = (w.tmem_cols <= 256 && L->smem <= kMaxSmem / 2) ? 2 : 1;
-    // as many slices as fill the SMs in one wave (a partial second wave doubles the time)
-    const int S = std::max(1, std::min(total_tiles, (kNumSMs * occ) / base));
-    w.tiles_per_split = (total_tiles + S - 1) / S;
-    w.splits = (total_tiles + w.tiles_per_split - 1) / w.tiles_per_split;
-    L->grid = base * w.splits;
-    L->ws_bytes = w.splits > 1 ? (size_t)w.splits * g.Cout * g.Cgi * w.kHW * sizeof(float) : 0;
+    const int budget = std::max(w.n_tgrp, kNumSMs / std::max(1, outer));
+    std::vector<double> cost(w.n_tgrp, 0.0);
+    double total_cost = 0.0;
+    for (int gi = 0; gi < w.n_tgrp; ++gi) {
+        cost[gi] = 150.0;   // staging and epilogue share
+        for (int jb = w.grp_first[gi]; jb < w.grp_first[gi + 1]; ++jb)
+            cost[gi] += w.job_count[jb] == 4 ? 136.0 : 118.0;
+        total_cost += cost[gi];
+    }
+    w.splits = 1;
+    w.grp_cta0[0] = 0;
+    for (int gi = 0; gi < w.n_tgrp; ++gi) {
+        int S = (int)(budget * cost[gi] / total_cost);
+        S = std::max(1, std::min(total_tiles, S));
+        const int per = (total_tiles + S - 1) / S;
+        S = (total_tiles + per - 1) / per;   // no empty slices
+        w.grp_splits[gi] = S;
+        w.grp_cta0[gi + 1] = w.grp_cta0[gi] + S;
+        w.splits = std::max(w.splits, S);
+    }
+    w.cta_per_cg = w.grp_cta0[w.n_tgrp];
+    L->grid = outer * w.cta_per_cg;
+    // workspace: split-K slices, blocked x, blocked gradOutput
+    L->part_bytes = align256((size_t)w.splits * g.Cout * g.Cgi * w.kHW * sizeof(float));
+    L->xt_bytes = align256((size_t)g.N * g.G * w.ncx * w.Rx * w.Wp * 64 * 2);
+    L->yt_bytes = align256((size_t)g.N * g.G * w.ncy * g.Ho * w.Wp * 64 * 2);
+    L->ws_bytes = L->part_bytes + L->xt_bytes + L->yt_bytes;
+    BlockifyParams &bx = L->bx;
+    bx = BlockifyParams{};
+    bx.N = g.N; bx.G = g.G; bx.Cg = g.Cgi; bx.nchunk = w.ncx; bx.IH = g.H; bx.IW = g.W;
+    bx.R = w.Rx; bx.C = w.Wp; bx.r_off = -g.pt; bx.c_off = -g.pl;
+    BlockifyParams &by = L->by;
+    by = BlockifyParams{};
+    by.N = g.N; by.G = g.G; by.Cg = g.Cgo; by.nchunk = w.ncy; by.IH = g.Ho; by.IW = g.Wo;
+    by.R = g.Ho; by.C = w.Wp; by.r_off = 0; by.c_off = 0;
     return true;
 }
 
@@ -886,9 +1058,6 @@ gconv_status launch_corr(CorrLaunch &L, const void *U, const void *w, const void
 
 }  // namespace
 
-// Adds `splits` slices of `count` floats in slice order (defined with the CUDA-core kernels).
-void launch_reduce_splits(const float *part, int splits, int64_t count, float *out, cudaStream_t s);
-
 bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p)
 {
     if (fc_like(g) && forced_path() != GCONV_PATH_TC_IGEMM) return false;
@@ -922,7 +1091,7 @@ bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p)
         WgradLaunch L;
         if (!build_wgrad(g, &L)) return false;
         p->path = GCONV_PATH_TC_IGEMM;
-        p->launches = L.wp.splits > 1 ? 2 : 1;
+        p->launches = 4;   // two blocked copies, the weight-gradient kernel, the slice reduction
         p->ws_bytes = L.ws_bytes;
         return true;
     }
@@ -957,15 +1126,31 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
         if (!build_wgrad(g, &L)) return GCONV_ERR_UNSUPPORTED;
         unsigned int *err = device_error_word();
         if (!err) return GCONV_ERR_CUDA;
-        L.wp.X = static_cast<const __nv_bfloat16 *>(a);
-        L.wp.DY = static_cast<const __nv_bfloat16 *>(b);
-        L.wp.part = L.wp.splits > 1 ? reinterpret_cast<float *>(wsb) : out;
+        __nv_bfloat16 *xt = reinterpret_cast<__nv_bfloat16 *>(wsb + L.part_bytes);
+        __nv_bfloat16 *yt = reinterpret_cast<__nv_bfloat16 *>(wsb + L.part_bytes + L.xt_bytes);
+        L.bx.in = static_cast<const __nv_bfloat16 *>(a);
+        L.bx.out = xt;
+        L.by.in = static_cast<const __nv_bfloat16 *>(b);
+        L.by.out = yt;
+        blockify_kernel<<<L.bx.N * L.bx.G * L.bx.nchunk * L.bx.R, kBlockifyThreads, 64 * (L.bx.C + 1) * 2, s>>>(L.bx);
+        blockify_kernel<<<L.by.N * L.by.G * L.by.nchunk * L.by.R, kBlockifyThreads, 64 * (L.by.C + 1) * 2, s>>>(L.by);
+        L.wp.XT = xt;
+        L.wp.DYT = yt;
+        L.wp.part = reinterpret_cast<float *>(wsb);
         L.wp.err = err;
         L.wp.wait_ns = (uint64_t)wait_limit();
         if (!smem_attr_once((const void *)wgrad_kernel, 1)) return GCONV_ERR_CUDA;
         wgrad_kernel<<<L.grid, kTcThreads, L.smem, s>>>(L.wp);
-        if (L.wp.splits > 1)
-            launch_reduce_splits(L.wp.part, L.wp.splits, (int64_t)g.Cout * g.Cgi * g.kH * g.kW, out, s);
+        ReduceParams rp{};
+        rp.part = L.wp.part;
+        rp.dw = out;
+        rp.O = g.Cout; rp.Cgi = g.Cgi; rp.kHW = g.kH * g.kW;
+        for (int gi = 0; gi < L.wp.n_tgrp; ++gi)
+            for (int jb = L.wp.grp_first[gi]; jb < L.wp.grp_first[gi + 1]; ++jb)
+                for (int c = 0; c < L.wp.job_count[jb]; ++c) rp.tap_splits[L.wp.job_tapk[jb][c]] = L.wp.grp_splits[gi];
+        const int64_t count = (int64_t)g.Cout * g.Cgi * g.kH * g.kW;
+        const int blocks = (int)std::min<int64_t>((count + 255) / 256, (int64_t)kNumSMs * 8);
+        wgrad_reduce_kernel<<<blocks, 256, 0, s>>>(rp);
         return GCONV_OK;
     }
     return GCONV_ERR_UNSUPPORTED;

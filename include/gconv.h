@@ -160,7 +160,8 @@ gconv_status gconv_bwd_bias(int N, int C_in, int H, int W, int C_out, int kH, in
  * The studied pages have no counterpart of this entry point.
  *
  * Same operation, arguments, layouts and result as gconv_bwd_weight, minus the
- * workspace: the split-K partial sums go to a fixed 32 MiB scratch array that the
+ * workspace: its scratch (split-K partial sums and blocked copies of the inputs) goes to
+ * a fixed 128 MiB array that the
  * library holds in device memory (every device that loads the library keeps it
  * until the process exits).  A geometry whose scratch need (what
  * gconv_workspace_size reports for GCONV_PASS_BWD_WEIGHT) exceeds
