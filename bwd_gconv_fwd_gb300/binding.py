@@ -30,7 +30,7 @@ PATH_NAMES = {PATH_NONE: "none", PATH_DIRECT: "direct", PATH_TC_IGEMM: "tc_igemm
 
 EXPORTED = ("gconv_out_shape", "gconv_workspace_size", "gconv_plan", "gconv_fwd", "gconv_bwd_data",
             "gconv_bwd_weight", "gconv_bwd_bias", "gconv_check_device_error", "gconv_status_string",
-            "gconv_debug_force_path", "gconv_debug_set_wait_limit", "gconv_bwd_weight_noalloc",
+            "gconv_debug_force_path", "gconv_debug_set_wait_limit", "gconv_debug_set_trace", "gconv_bwd_weight_noalloc",
             "gconv_noalloc_scratch_bytes")
 
 _lib = None
@@ -79,6 +79,8 @@ def lib():
     L.gconv_debug_force_path.restype = None
     L.gconv_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
     L.gconv_debug_set_wait_limit.restype = None
+    L.gconv_debug_set_trace.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+    L.gconv_debug_set_trace.restype = None
     _lib = L
     return L
 
@@ -121,6 +123,12 @@ def gconv_debug_force_path(path: int):
 
 def gconv_debug_set_wait_limit(limit: int):
     lib().gconv_debug_set_wait_limit(int(limit))
+
+
+
+def gconv_debug_set_trace(device_ptr: int, nbytes: int):
+    """Sets (or, with 0, clears) the device buffer the correlation kernel writes phase stamps to."""
+    lib().gconv_debug_set_trace(ctypes.c_void_p(device_ptr or None), int(nbytes))
 
 
 def gconv_check_device_error(stream=None) -> int:

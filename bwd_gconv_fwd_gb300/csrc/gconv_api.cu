@@ -30,6 +30,8 @@ unsigned int *device_error_word()
 
 static int g_force_path = GCONV_PATH_NONE;
 static long long g_wait_limit = -1;
+static void *g_trace = nullptr;
+static size_t g_trace_bytes = 0;
 
 long long wait_limit()
 {
@@ -37,6 +39,11 @@ long long wait_limit()
 }
 
 int forced_path() { return g_force_path; }
+void *debug_trace(size_t *bytes)
+{
+    *bytes = g_trace_bytes;
+    return g_trace;
+}
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -347,5 +354,12 @@ const char *gconv_status_string(gconv_status status)
 void gconv_debug_force_path(int path) { g_force_path = path; }
 
 void gconv_debug_set_wait_limit(long long limit) { g_wait_limit = limit; }
+
+void gconv_debug_set_trace(void *device_buffer, size_t bytes)
+{
+    g_trace = device_buffer;
+    g_trace_bytes = device_buffer ? bytes : 0;
+}
+
 
 }  // extern "C"

@@ -26,6 +26,7 @@ Plan plan_pass(const Geom &g, gconv_dtype dt, gconv_pass pass);
 long long wait_limit();
 unsigned int *device_error_word();   // device address of the error word, nullptr on failure
 int forced_path();
+void *debug_trace(size_t *bytes);     // gconv_debug_set_trace buffer, nullptr when off
 
 // tcgen05 implicit-GEMM family (tc_conv.cu)
 bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p);

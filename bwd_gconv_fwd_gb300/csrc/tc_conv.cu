@@ -379,9 +379,10 @@ corr_kernel(const __grid_constant__ CorrParams p)
 // ===========================================================================
 // out[n][g][j][r][c][0..63] = in[n][g*Cg + 64*j + e][r + r_off][c + c_off], zero outside
 // the image and for channels past Cg.  One 128-byte row per (r, c): 64 channels of one
-// position, so a tile of consecutive positions is a contiguous run of rows.  The
-// transpose goes through shared memory; loads run along image rows, stores are
-// 16-byte vectors along the output rows.  HBM-bound.
+// position, so a tile of consecutive positions is a contiguous run of rows.  Each thread
+// builds one position row: 64 two-byte loads (the lanes of a warp take consecutive
+// positions, so each load instruction reads a contiguous stretch of an image row),
+// packed into eight 16-byte stores.  No shared memory; HBM-bound.
 struct BlockifyParams {
     const __nv_bfloat16 *in;
     __nv_bfloat16 *out;
@@ -393,35 +394,31 @@ constexpr int kBlockifyThreads = 256;
 __global__ void __launch_bounds__(kBlockifyThreads)
 blockify_kernel(const __grid_constant__ BlockifyParams p)
 {
-    extern __shared__ uint16_t tile[];            // [64][C + 1]
-    const int ld = p.C + 1;
-    int t = blockIdx.x;
-    const int r = t % p.R; t /= p.R;
-    const int j = t % p.nchunk; t /= p.nchunk;
-    const int g = t % p.G;
-    const int n = t / p.G;
-    const int row = r + p.r_off;
-    const bool row_ok = row >= 0 && row < p.IH;
+    const int plane_out = p.R * p.C;
+    const int64_t total = (int64_t)p.N * p.G * p.nchunk * plane_out;
+    const int64_t q = (int64_t)blockIdx.x * kBlockifyThreads + threadIdx.x;
+    if (q >= total) return;
+    const int64_t blk = q / plane_out;                 // (n*G + g)*nchunk + j
+    const int pos = (int)(q - blk * plane_out);
+    const int r = pos / p.C, c = pos - r * p.C;
+    const int j = (int)(blk % p.nchunk);
+    const int64_t ng = blk / p.nchunk;                 // n*G + g
+    const int row = r + p.r_off, col = c + p.c_off;
+    const bool inside = row >= 0 && row < p.IH && col >= 0 && col < p.IW;
+    const int cvalid = inside ? min(64, p.Cg - 64 * j) : 0;
     const int64_t plane = (int64_t)p.IH * p.IW;
-    const uint16_t *src = reinterpret_cast<const uint16_t *>(p.in) +
-                          ((int64_t)n * p.G * p.Cg + (int64_t)g * p.Cg + 64 * j) * plane + (int64_t)row * p.IW;
-    for (int idx = threadIdx.x; idx < 64 * p.C; idx += kBlockifyThreads) {
-        const int e = idx / p.C, c = idx - e * p.C;
-        const int col = c + p.c_off;
-        uint16_t v = 0;
-        if (row_ok && col >= 0 && col < p.IW && 64 * j + e < p.Cg) v = __ldg(src + (int64_t)e * plane + col);
-        tile[e * ld + c] = v;
+    const unsigned short *src = reinterpret_cast<const unsigned short *>(p.in) + (ng * p.Cg + 64 * j) * plane +
+                                (inside ? (int64_t)row * p.IW + col : 0);
+    uint32_t w[32];
+    #pragma unroll
+    for (int h = 0; h < 32; ++h) {
+        const uint32_t lo = 2 * h < cvalid ? (uint32_t)__ldg(src + (2 * h) * plane) : 0u;
+        const uint32_t hi = 2 * h + 1 < cvalid ? (uint32_t)__ldg(src + (2 * h + 1) * plane) : 0u;
+        w[h] = lo | (hi << 16);
     }
-    __syncthreads();
-    uint4 *dst = reinterpret_cast<uint4 *>(p.out) + ((((int64_t)n * p.G + g) * p.nchunk + j) * p.R + r) * p.C * 8;
-    for (int idx = threadIdx.x; idx < p.C * 8; idx += kBlockifyThreads) {
-        const int c = idx >> 3, k = idx & 7;
-        uint32_t w[4];
-        #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            w[q] = (uint32_t)tile[(k * 8 + 2 * q) * ld + c] | ((uint32_t)tile[(k * 8 + 2 * q + 1) * ld + c] << 16);
-        dst[idx] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+    uint4 *dst = reinterpret_cast<uint4 *>(p.out) + q * 8;
+    #pragma unroll
+    for (int k = 0; k < 8; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
 // ===========================================================================
@@ -630,6 +627,354 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == kWarpAux) ptx::tmem_dealloc(tmem, tmem_cols);
+}
+
+// ===========================================================================
+// Correlation kernel, stride 1: output channels on M, output positions on N
+// ===========================================================================
+// Persistent: one CTA per SM walks the tiles (image, group, 128-channel tile, 256
+// consecutive positions of the padded output grid with pitch Wp).  A tile's
+// D[v][position] accumulates in one of two 256-column TMEM buffers, so the epilogue
+// of one tile overlaps the MMAs of the next.
+//   A = packed weight block of one (64-channel chunk, tap): [128 v][64 u], K-major,
+//       128-byte swizzle, streamed through a ring by several issuing threads (one
+//       thread's bulk-copy stream is too slow to feed the tensor core alone).
+//   B = the blocked input's position rows [p0, p0 + stage_rows) of one chunk, staged
+//       by cp.async into the 128-byte swizzle layout; tap t reads them tap_off[t]
+//       rows further on (a whole-row shift of the descriptor's start address).
+// Every MMA is M = 128, N = 256, K = 16; K steps past the last real channel of a
+// chunk are skipped.  The epilogue transposes 32 x 32 blocks through shared memory
+// so that a warp stores 32 consecutive pixels of one output channel.
+struct Corr2Params {
+    const __nv_bfloat16 *UB;    // blocked input [N][G][nchu][R][Wp][64]
+    const uint8_t *Wpk;         // packed weight blocks [G][n_vtile][nchu][ntaps][16 KB]
+    const __nv_bfloat16 *bias;  // [G*Cv] or nullptr
+    float *V;                   // output [N][G*Cv][Qh][Qw]
+    unsigned int *err;
+    uint64_t wait_ns;
+    int N, G, Cu, Cv, Qh, Qw, R, Wp, nchu;
+    int n_ptile, n_vtile, n_tiles;  // 256-position tiles per image, 128-channel tiles, all tiles
+    int stage_rows;             // positions staged per chunk (256 + farthest tap, multiple of 8)
+    int nsb, wstages;           // staging buffers (1 or 2), weight ring depth (3 or 4)
+    int ntaps;
+    int tap_off[kMaxTaps];
+    unsigned long long *trace;  // optional per-CTA phase stamps (kTraceWords each), nullptr when off
+};
+
+constexpr int kWblkBytes = 128 * 128;   // one packed weight block: 128 rows x 64 channels (bf16)
+constexpr int kC2EpiWarps = 4;          // warps 0-3: epilogue (TMEM lane groups 0-3)
+constexpr int kC2StageWarps = 4;        // warps 4-7: staging
+constexpr int kC2StageThreads = kC2StageWarps * 32;
+constexpr int kC2WarpMma = 8;           // TMEM allocation and MMA issue
+constexpr int kC2WarpProd = 9;          // warps 9-12: weight producers (one issuing lane each)
+constexpr int kC2MaxWStages = 4;
+constexpr int kC2Threads = (kC2WarpProd + kC2MaxWStages) * 32;
+constexpr int kC2EpiBytes = kC2EpiWarps * 32 * 33 * 4;
+// Trace words per CTA: start, SM id, MMA issuer's waits for staged chunks, for weight
+// blocks and for a free accumulator (ns), time of the last MMA, epilogue warp 0's
+// waits for accumulators (ns), end.
+constexpr int kTraceWords = 8;
+
+__device__ __forceinline__ void corr2_tile(const Corr2Params &p, int t, int *ptile, int *n, int *vt, int *g)
+{
+    *ptile = t % p.n_ptile; t /= p.n_ptile;
+    *n = t % p.N; t /= p.N;
+    *vt = t % p.n_vtile;
+    *g = t / p.n_vtile;
+}
+
+__global__ void __launch_bounds__(kC2Threads, 1)
+corr2_kernel(const __grid_constant__ Corr2Params p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_sfull[2], bar_sempty[2], bar_wfull[kC2MaxWStages],
+        bar_wempty[kC2MaxWStages], bar_afull[2], bar_aempty[2], bar_drain;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_flag;
+    __shared__ int tap_off_sh[kMaxTaps];
+
+    uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int stage_bytes = p.stage_rows * 128;
+    if (threadIdx.x < p.ntaps) tap_off_sh[threadIdx.x] = p.tap_off[threadIdx.x];
+    uint8_t *ring = smem + p.nsb * stage_bytes;
+    float *epi = reinterpret_cast<float *>(ring + p.wstages * kWblkBytes);
+    const int nblocks = p.nchu * p.ntaps;
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(ptx::smem_u32(&bar_sfull[i]), kC2StageThreads);
+            ptx::mbar_init(ptx::smem_u32(&bar_sempty[i]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bar_afull[i]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bar_aempty[i]), kC2EpiWarps);
+        }
+        for (int i = 0; i < kC2MaxWStages; ++i) {
+            ptx::mbar_init(ptx::smem_u32(&bar_wfull[i]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bar_wempty[i]), 1);
+        }
+        ptx::mbar_init(ptx::smem_u32(&bar_drain), 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == kC2WarpMma) {
+        ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+    unsigned long long *trace = p.trace ? p.trace + (size_t)blockIdx.x * kTraceWords : nullptr;
+    if (trace && threadIdx.x == 0) {
+        trace[0] = ptx::globaltimer();
+        trace[1] = ptx::smid();
+    }
+
+    if (warp >= kC2EpiWarps && warp < kC2EpiWarps + kC2StageWarps) {
+        // ---------------- staging: one 64-channel chunk of position rows at a time ----------------
+        const int st = threadIdx.x - kC2EpiWarps * 32;
+        const int plane = p.R * p.Wp;
+        int seq = 0;
+        bool stop = false;
+        for (int t = blockIdx.x; t < p.n_tiles && !stop; t += gridDim.x) {
+            int ptile, n, vt, g;
+            corr2_tile(p, t, &ptile, &n, &vt, &g);
+            const int p0 = ptile * 256;
+            for (int kc = 0; kc < p.nchu; ++kc, ++seq) {
+                const int sb = seq % p.nsb;
+                bool bad = false;
+                if (seq >= p.nsb)
+                    bad = !ptx::mbar_wait(ptx::smem_u32(&bar_sempty[sb]), (seq / p.nsb - 1) & 1, p.wait_ns);
+                bad = ptx::bar_red_or(1, kC2StageThreads, bad || abort_flag);
+                if (bad) {
+                    if (st == 0) { abort_flag = 1; raise_device_error(p.err, DEVERR_WAIT_TIMEOUT); }
+                    stop = true;
+                    break;
+                }
+                const uint32_t buf = ptx::smem_u32(smem + sb * stage_bytes);
+                const __nv_bfloat16 *src0 = p.UB + ((((int64_t)n * p.G + g) * p.nchu + kc) * plane) * 64;
+                for (int idx = st; idx < p.stage_rows * 8; idx += kC2StageThreads) {
+                    const int m = idx >> 3, k = idx & 7;
+                    const bool ok = p0 + m < plane;
+                    const __nv_bfloat16 *src = ok ? src0 + ((int64_t)(p0 + m) * 64 + k * 8) : p.UB;
+                    ptx::cp_async16(buf + (uint32_t)(m * 128 + ((k ^ (m & 7)) << 4)), src, ok ? 16u : 0u);
+                }
+                ptx::cp_async_wait_all();
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(ptx::smem_u32(&bar_sfull[sb]));
+            }
+        }
+    } else if (warp >= kC2WarpProd && warp - kC2WarpProd < p.wstages) {
+        // ---------------- weight producers: producer q owns ring slot q ----------------
+        if (lane == 0) {
+            const int q = warp - kC2WarpProd;
+            int b = 0, last = -1;
+            bool stop = false;
+            for (int t = blockIdx.x; t < p.n_tiles && !stop; t += gridDim.x) {
+                int ptile, n, vt, g;
+                corr2_tile(p, t, &ptile, &n, &vt, &g);
+                const uint8_t *wsrc = p.Wpk + ((size_t)g * p.n_vtile + vt) * (size_t)nblocks * kWblkBytes;
+                for (int j = 0; j < nblocks; ++j, ++b) {
+                    if (b % p.wstages != q) continue;
+                    if (b >= p.wstages &&
+                        !ptx::mbar_wait(ptx::smem_u32(&bar_wempty[q]), (b / p.wstages - 1) & 1, p.wait_ns)) {
+                        abort_flag = 1;
+                        raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
+                    }
+                    if (abort_flag) { stop = true; break; }
+                    const uint32_t fb = ptx::smem_u32(&bar_wfull[q]);
+                    ptx::mbar_arrive_expect_tx(fb, kWblkBytes);
+                    ptx::bulk_g2s(ptx::smem_u32(ring + q * kWblkBytes), wsrc + (size_t)j * kWblkBytes, kWblkBytes, fb);
+                    last = b;
+                }
+            }
+            // the last copy into this slot must land before the CTA exits
+            if (last >= 0 && !ptx::mbar_wait(ptx::smem_u32(&bar_wfull[q]), (last / p.wstages) & 1, kDrainNs))
+                raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
+        }
+    } else if (warp == kC2WarpMma) {
+        // ---------------- MMA issuer ----------------
+        // The tensor core runs only a couple of MMAs ahead of this thread, so the loop is
+        // kept lean: descriptors are a base plus an address offset (address >> 4 sits in
+        // the low bits), the next tap's row shift is loaded one step ahead, ring slots and
+        // phases advance incrementally, and timers are read only on a slow wait.
+        if (lane == 0) {
+            const uint32_t idesc = ptx::idesc_bf16(128, 256, 0, 0);
+            const uint64_t adesc0 = ptx::smem_desc(ptx::smem_u32(ring), 16u, 1024u, 2);
+            const uint64_t bdesc0 = ptx::smem_desc(ptx::smem_u32(smem), 16u, 1024u, 2);
+            bool ok = true;
+            int seq = 0, slot = 0;
+            uint32_t wphase = 0;
+            uint64_t w_stage = 0, w_weight = 0, w_acc = 0;
+            int k = 0;
+            for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++k) {
+                const int acc = k & 1;
+                if (k >= 2) {
+                    const uint32_t bar = ptx::smem_u32(&bar_aempty[acc]);
+                    const uint32_t ph = (k / 2 - 1) & 1;
+                    if (!ptx::mbar_try_wait(bar, ph)) {
+                        const uint64_t t0 = ptx::globaltimer();
+                        if (!ptx::mbar_wait(bar, ph, p.wait_ns)) { ok = false; break; }
+                        w_acc += ptx::globaltimer() - t0;
+                    }
+                }
+                ptx::tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(acc * 256);
+                for (int kc = 0; kc < p.nchu; ++kc, ++seq) {
+                    const int sb = seq % p.nsb;
+                    {
+                        const uint32_t bar = ptx::smem_u32(&bar_sfull[sb]);
+                        const uint32_t ph = (seq / p.nsb) & 1;
+                        if (!ptx::mbar_try_wait(bar, ph)) {
+                            const uint64_t t0 = ptx::globaltimer();
+                            if (!ptx::mbar_wait(bar, ph, p.wait_ns)) { ok = false; break; }
+                            w_stage += ptx::globaltimer() - t0;
+                        }
+                    }
+                    ptx::tc_fence_after();
+                    const uint64_t bdesc_c = bdesc0 + (uint64_t)((sb * stage_bytes) >> 4);
+                    const int nks = min(4, (p.Cu - 64 * kc + 15) >> 4);
+                    int off_next = tap_off_sh[0];
+                    for (int tp = 0; tp < p.ntaps; ++tp) {
+                        const int off = off_next;
+                        off_next = tap_off_sh[tp + 1 < p.ntaps ? tp + 1 : 0];
+                        const uint32_t wbar = ptx::smem_u32(&bar_wfull[slot]);
+                        if (!ptx::mbar_try_wait(wbar, wphase)) {
+                            const uint64_t t0 = ptx::globaltimer();
+                            if (!ptx::mbar_wait(wbar, wphase, p.wait_ns)) { ok = false; break; }
+                            w_weight += ptx::globaltimer() - t0;
+                        }
+                        ptx::tc_fence_after();
+                        const uint64_t ad = adesc0 + (uint64_t)(slot * (kWblkBytes >> 4));
+                        const uint64_t bd = bdesc_c + (uint64_t)(off * 8);     // off rows of 128 bytes
+                        const uint32_t acc0 = (kc > 0 || tp > 0) ? 1u : 0u;
+                        ptx::mma_f16(d, ad, bd, idesc, acc0);
+                        if (nks > 1) ptx::mma_f16(d, ad + 2, bd + 2, idesc, 1u);   // +32 bytes: next 16 channels
+                        if (nks > 2) ptx::mma_f16(d, ad + 4, bd + 4, idesc, 1u);
+                        if (nks > 3) ptx::mma_f16(d, ad + 6, bd + 6, idesc, 1u);
+                        ptx::mma_commit(ptx::smem_u32(&bar_wempty[slot]));
+                        if (++slot == p.wstages) { slot = 0; wphase ^= 1u; }
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit(ptx::smem_u32(&bar_sempty[sb]));
+                }
+                if (!ok) break;
+                ptx::mma_commit(ptx::smem_u32(&bar_afull[acc]));
+                if (abort_flag) ok = false;
+            }
+            if (!ok) {
+                abort_flag = 1;
+                raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
+            }
+            if (trace) {
+                trace[2] = w_stage;
+                trace[3] = w_weight;
+                trace[4] = w_acc;
+                trace[5] = ptx::globaltimer();
+            }
+            // every MMA this thread issued completes before TMEM is released
+            ptx::mma_commit(ptx::smem_u32(&bar_drain));
+            if (!ptx::mbar_wait(ptx::smem_u32(&bar_drain), 0, kDrainNs)) raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
+        }
+    } else if (warp < kC2EpiWarps) {
+        // ---------------- epilogue: TMEM -> 32 x 32 smem transpose -> coalesced NCHW rows ----------------
+        const int lg = warp;
+        float *tb = epi + warp * (32 * 33);
+        const int64_t out_hw = (int64_t)p.Qh * p.Qw;
+        uint64_t w_epi = 0;
+        int k = 0;
+        for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++k) {
+            int ptile, n, vt, g;
+            corr2_tile(p, t, &ptile, &n, &vt, &g);
+            const int acc = k & 1;
+            const uint64_t t0 = trace ? ptx::globaltimer() : 0;
+            bool ready = ptx::mbar_wait(ptx::smem_u32(&bar_afull[acc]), (k / 2) & 1, p.wait_ns);
+            if (trace) w_epi += ptx::globaltimer() - t0;
+            ready = __all_sync(0xffffffffu, ready);
+            if (!ready || abort_flag) {
+                if (lane == 0) { abort_flag = 1; raise_device_error(p.err, DEVERR_WAIT_TIMEOUT); }
+                break;
+            }
+            ptx::tc_fence_after();
+            const int p0 = ptile * 256;
+            const int v0 = vt * 128 + lg * 32;
+            const int vcount = min(32, p.Cv - v0);
+            float *vout = p.V + ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv + v0) * out_hw;
+            const float bias_lane = (p.bias && lane < vcount) ? __bfloat162float(p.bias[g * p.Cv + v0 + lane]) : 0.f;
+            for (int pc = 0; pc < 256; pc += 32) {
+                uint32_t a0[16], a1[16];
+                const uint32_t taddr = tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)(acc * 256 + pc);
+                ptx::tmem_ld16(taddr, a0);
+                ptx::tmem_ld16(taddr + 16, a1);
+                ptx::tmem_ld_wait();
+                if (vcount > 0) {
+                    #pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        tb[lane * 33 + j] = __uint_as_float(a0[j]) + bias_lane;
+                        tb[lane * 33 + 16 + j] = __uint_as_float(a1[j]) + bias_lane;
+                    }
+                    __syncwarp();
+                    const int pos = p0 + pc + lane;
+                    const int qh = pos / p.Wp, qw = pos - qh * p.Wp;
+                    if (qh < p.Qh && qw < p.Qw) {
+                        float *o = vout + (int64_t)qh * p.Qw + qw;
+                        for (int vv = 0; vv < vcount; ++vv) o[vv * out_hw] = tb[vv * 33 + lane];
+                    }
+                    __syncwarp();
+                }
+            }
+            // this warp's TMEM reads are done: the accumulator may be overwritten
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bar_aempty[acc]));
+        }
+        if (trace && threadIdx.x == 0) trace[6] = w_epi;
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (trace && threadIdx.x == 0) trace[7] = ptx::globaltimer();
+    if (warp == kC2WarpMma) ptx::tmem_dealloc(tmem, 512);
+}
+
+// Packs weights for corr2_kernel: block (g, vt, kc, tap) = [128 rows v][64 u] in the
+// 128-byte swizzle layout (16-byte piece k of row r at ((k ^ (r & 7)) * 16)).
+//   forward:       v = output channel, u = input channel:  w[g*Cv + v][u][tap]
+//   backward-data: v = input channel,  u = output channel: w[g*Cu + u][v][tap]
+struct Pack2Params {
+    const __nv_bfloat16 *w;
+    uint8_t *out;
+    int G, Cu, Cv, n_vtile, nchu, ntaps;
+    int transpose;          // 0 forward, 1 backward-data
+    int w_cin_g, kHW;
+};
+
+__global__ void pack2_kernel(const __grid_constant__ Pack2Params p)
+{
+    const int64_t pieces = (int64_t)p.G * p.n_vtile * p.nchu * p.ntaps * 128 * 8;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < pieces; e += (int64_t)gridDim.x * blockDim.x) {
+        const int k = (int)(e & 7);
+        const int r = (int)((e >> 3) & 127);
+        int64_t b = e >> 10;
+        const int tp = (int)(b % p.ntaps); b /= p.ntaps;
+        const int kc = (int)(b % p.nchu); b /= p.nchu;
+        const int vt = (int)(b % p.n_vtile);
+        const int g = (int)(b / p.n_vtile);
+        const int v = vt * 128 + r;
+        uint32_t wv[4] = {0u, 0u, 0u, 0u};
+        if (v < p.Cv) {
+            #pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int u = kc * 64 + k * 8 + q;
+                if (u < p.Cu) {
+                    const int64_t idx = p.transpose ? ((int64_t)(g * p.Cu + u) * p.w_cin_g + v) * p.kHW + tp
+                                                    : ((int64_t)(g * p.Cv + v) * p.w_cin_g + u) * p.kHW + tp;
+                    wv[q >> 1] |= (uint32_t)__bfloat16_as_ushort(p.w[idx]) << ((q & 1) * 16);
+                }
+            }
+        }
+        uint8_t *blk = p.out + (e >> 10) * (int64_t)kWblkBytes;
+        *reinterpret_cast<uint4 *>(blk + r * 128 + ((k ^ (r & 7)) << 4)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
 }
 
 struct ReduceParams {
@@ -1017,6 +1362,81 @@ bool build_wgrad(const Geom &g, WgradLaunch *L)
     return true;
 }
 
+struct Corr2Launch {
+    Corr2Params cp;
+    Pack2Params pk;
+    BlockifyParams bu;
+    size_t smem = 0;
+    size_t ub_bytes = 0, wpk_bytes = 0, ws_bytes = 0;
+    int grid = 0;
+};
+
+// Stride-1 correlation on the blocked layout: the forward pass, or backward-data as the
+// correlation of gradOutput with the mirrored taps (stride 1 makes every output
+// position of dx a full correlation, no phases).
+bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
+{
+    if (g.s != 1) return false;
+    const int Cu = bwd_data ? g.Cgo : g.Cgi;    // reduced channels (K)
+    const int Cv = bwd_data ? g.Cgi : g.Cgo;    // produced channels (M)
+    if (Cu < 16 || Cv < 16) return false;
+    const int ntaps = g.kH * g.kW;
+    if (ntaps > kMaxTaps) return false;
+    Corr2Params &c = L->cp;
+    c = Corr2Params{};
+    const int Qh = bwd_data ? g.H : g.Ho, Qw = bwd_data ? g.W : g.Wo;
+    const int maxa = (g.kH - 1) * g.d, maxb = (g.kW - 1) * g.d;
+    c.N = g.N; c.G = g.G; c.Cv = Cv; c.Qh = Qh; c.Qw = Qw;
+    c.Wp = Qw + maxb;
+    c.R = Qh + maxa;
+    c.nchu = (Cu + 63) / 64;
+    c.n_vtile = (Cv + 127) / 128;
+    c.ntaps = ntaps;
+    int maxoff = 0;
+    for (int kh = 0; kh < g.kH; ++kh)
+        for (int kw = 0; kw < g.kW; ++kw) {
+            const int a = bwd_data ? (g.kH - 1 - kh) * g.d : kh * g.d;
+            const int b = bwd_data ? (g.kW - 1 - kw) * g.d : kw * g.d;
+            c.tap_off[kh * g.kW + kw] = a * c.Wp + b;
+            maxoff = std::max(maxoff, a * c.Wp + b);
+        }
+    const int positions = Qh * c.Wp;   // padded output grid rows that hold real outputs
+    c.Cu = Cu;
+    c.n_ptile = (positions + 255) / 256;
+    c.n_tiles = g.N * g.G * c.n_vtile * c.n_ptile;
+    c.stage_rows = round_up(256 + maxoff, 8);
+    const size_t stage = (size_t)c.stage_rows * 128;
+    // Two staging buffers and four weight slots when they fit; never below 120 KB, so
+    // that one CTA holds its SM (it takes all 512 TMEM columns).
+    const int shapes[3][2] = {{2, 4}, {2, 3}, {1, 4}};
+    bool fit = false;
+    for (const auto &sh : shapes) {
+        c.nsb = sh[0];
+        c.wstages = sh[1];
+        L->smem = 1024 + c.nsb * stage + (size_t)c.wstages * kWblkBytes + kC2EpiBytes;
+        if (L->smem <= kMaxSmem) { fit = true; break; }
+    }
+    if (!fit) return false;
+    L->smem = std::max(L->smem, (size_t)120 * 1024);
+    L->grid = std::min(c.n_tiles, kNumSMs);
+    Pack2Params &k = L->pk;
+    k = Pack2Params{};
+    k.G = g.G; k.Cu = Cu; k.Cv = Cv; k.n_vtile = c.n_vtile; k.nchu = c.nchu; k.ntaps = ntaps;
+    k.transpose = bwd_data ? 1 : 0;
+    k.w_cin_g = g.Cgi; k.kHW = ntaps;
+    BlockifyParams &bu = L->bu;
+    bu = BlockifyParams{};
+    bu.N = g.N; bu.G = g.G; bu.Cg = Cu; bu.nchunk = c.nchu;
+    bu.IH = bwd_data ? g.Ho : g.H; bu.IW = bwd_data ? g.Wo : g.W;
+    bu.R = c.R; bu.C = c.Wp;
+    bu.r_off = bwd_data ? g.pt - maxa : -g.pt;
+    bu.c_off = bwd_data ? g.pl - maxb : -g.pl;
+    L->ub_bytes = align256((size_t)g.N * g.G * c.nchu * c.R * c.Wp * 128);
+    L->wpk_bytes = align256((size_t)g.G * c.n_vtile * c.nchu * ntaps * kWblkBytes);
+    L->ws_bytes = L->ub_bytes + L->wpk_bytes;
+    return true;
+}
+
 bool fc_like(const Geom &g) { return g.Ho == 1 && g.Wo == 1; }
 
 // Raises the dynamic shared-memory limit of a kernel once per device.
@@ -1031,6 +1451,42 @@ bool smem_attr_once(const void *fn, int slot)
         done[dev][slot] = true;
     }
     return true;
+}
+
+void launch_blockify(const BlockifyParams &b, cudaStream_t s)
+{
+    const int64_t total = (int64_t)b.N * b.G * b.nchunk * b.R * b.C;
+    if (total == 0) return;
+    blockify_kernel<<<(unsigned)((total + kBlockifyThreads - 1) / kBlockifyThreads), kBlockifyThreads, 0, s>>>(b);
+}
+
+gconv_status launch_corr2(Corr2Launch &L, const void *U, const void *w, const void *bias, float *out, uint8_t *ws,
+                          cudaStream_t s)
+{
+    unsigned int *err = device_error_word();
+    if (!err) return GCONV_ERR_CUDA;
+    __nv_bfloat16 *ub = reinterpret_cast<__nv_bfloat16 *>(ws);
+    uint8_t *wpk = ws + L.ub_bytes;
+    L.bu.in = static_cast<const __nv_bfloat16 *>(U);
+    L.bu.out = ub;
+    launch_blockify(L.bu, s);
+    L.pk.w = static_cast<const __nv_bfloat16 *>(w);
+    L.pk.out = wpk;
+    const int64_t pieces = (int64_t)L.pk.G * L.pk.n_vtile * L.pk.nchu * L.pk.ntaps * 1024;
+    pack2_kernel<<<(int)std::min<int64_t>((pieces + 255) / 256, 4096), 256, 0, s>>>(L.pk);
+    L.cp.UB = ub;
+    L.cp.Wpk = wpk;
+    L.cp.bias = static_cast<const __nv_bfloat16 *>(bias);
+    L.cp.V = out;
+    L.cp.err = err;
+    L.cp.wait_ns = (uint64_t)wait_limit();
+    size_t trace_bytes = 0;
+    void *trace = debug_trace(&trace_bytes);
+    L.cp.trace = (trace && trace_bytes >= (size_t)L.grid * kTraceWords * 8) ? static_cast<unsigned long long *>(trace)
+                                                                              : nullptr;
+    if (!smem_attr_once((const void *)corr2_kernel, 2)) return GCONV_ERR_CUDA;
+    corr2_kernel<<<L.grid, kC2Threads, L.smem, s>>>(L.cp);
+    return GCONV_OK;
 }
 
 gconv_status launch_corr(CorrLaunch &L, const void *U, const void *w, const void *bias, float *out,
@@ -1061,6 +1517,15 @@ gconv_status launch_corr(CorrLaunch &L, const void *U, const void *w, const void
 bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p)
 {
     if (fc_like(g) && forced_path() != GCONV_PATH_TC_IGEMM) return false;
+    if (pass == GCONV_PASS_FWD || pass == GCONV_PASS_BWD_DATA) {
+        Corr2Launch L2;
+        if (build_corr2(g, pass == GCONV_PASS_BWD_DATA, &L2)) {
+            p->path = GCONV_PATH_TC_IGEMM;
+            p->launches = 3;   // blocked input copy, weight packing, the correlation kernel
+            p->ws_bytes = L2.ws_bytes;
+            return true;
+        }
+    }
     if (pass == GCONV_PASS_FWD) {
         CorrLaunch L;
         if (!build_fwd(g, &L)) return false;
@@ -1102,6 +1567,10 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
                              const void *bias, float *out, void *ws, cudaStream_t s)
 {
     uint8_t *wsb = static_cast<uint8_t *>(ws);
+    if (pass == GCONV_PASS_FWD || pass == GCONV_PASS_BWD_DATA) {
+        Corr2Launch L2;
+        if (build_corr2(g, pass == GCONV_PASS_BWD_DATA, &L2)) return launch_corr2(L2, a, b, bias, out, wsb, s);
+    }
     if (pass == GCONV_PASS_FWD) {
         CorrLaunch L;
         if (!build_fwd(g, &L)) return GCONV_ERR_UNSUPPORTED;
@@ -1132,8 +1601,8 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
         L.bx.out = xt;
         L.by.in = static_cast<const __nv_bfloat16 *>(b);
         L.by.out = yt;
-        blockify_kernel<<<L.bx.N * L.bx.G * L.bx.nchunk * L.bx.R, kBlockifyThreads, 64 * (L.bx.C + 1) * 2, s>>>(L.bx);
-        blockify_kernel<<<L.by.N * L.by.G * L.by.nchunk * L.by.R, kBlockifyThreads, 64 * (L.by.C + 1) * 2, s>>>(L.by);
+        launch_blockify(L.bx, s);
+        launch_blockify(L.by, s);
         L.wp.XT = xt;
         L.wp.DYT = yt;
         L.wp.part = reinterpret_cast<float *>(wsb);
