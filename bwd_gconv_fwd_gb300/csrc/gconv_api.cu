@@ -86,13 +86,33 @@ static void direct_weight_split(const Geom &g, int *splits, int64_t *per_split)
     *splits = (int)((P + per - 1) / per);
 }
 
-static void bias_split(const Geom &g, int *splits, int *n_per_split)
+// Bias gradient plan: tc[0] = 0 for per-plane sums (psum[N][C_out]), 1 for column
+// sums over rows of C_out*HW elements (tc[1] = 1 when rows are read in 16-byte chunks,
+// `splits` row ranges of `n_per_split` rows).
+static void bias_plan(const Geom &g, gconv_dtype dt, Plan *p)
 {
-    int S = (16 * kNumSMs + g.Cout - 1) / g.Cout;
-    S = std::max(1, std::min(S, g.N));
-    const int per = (g.N + S - 1) / S;
-    *n_per_split = per;
-    *splits = (g.N + per - 1) / per;
+    p->path = GCONV_PATH_REDUCE;
+    p->launches = 2;
+    const int64_t HW = (int64_t)g.Ho * g.Wo;
+    if (HW >= kBiasPlaneMin) {
+        p->tc[0] = 0;
+        p->splits = 1;
+        p->ws_bytes = (size_t)g.N * g.Cout * sizeof(float);
+        return;
+    }
+    const int64_t L = (int64_t)g.Cout * HW;
+    const int esize = dt == GCONV_BF16 ? 2 : 4;
+    const bool vec = (L * esize) % 16 == 0;
+    const int64_t threads = vec ? L / (16 / esize) : L;
+    // about two resident waves of threads, but at least 8 rows per split
+    int64_t S = (2 * (int64_t)kNumSMs * 2048 + threads - 1) / threads;
+    S = std::max<int64_t>(1, std::min<int64_t>(S, std::max(1, g.N / 8)));
+    const int rows = (int)((g.N + S - 1) / S);
+    p->tc[0] = 1;
+    p->tc[1] = vec ? 1 : 0;
+    p->n_per_split = rows;
+    p->splits = (g.N + rows - 1) / rows;
+    p->ws_bytes = (size_t)p->splits * L * sizeof(float);
 }
 
 Plan plan_pass(const Geom &g, gconv_dtype dt, gconv_pass pass)
@@ -100,10 +120,7 @@ Plan plan_pass(const Geom &g, gconv_dtype dt, gconv_pass pass)
     Plan p{};
     if (g.N == 0) { p.path = GCONV_PATH_NONE; return p; }
     if (pass == GCONV_PASS_BWD_BIAS) {
-        p.path = GCONV_PATH_REDUCE;
-        bias_split(g, &p.splits, &p.n_per_split);
-        p.launches = p.splits > 1 ? 2 : 1;
-        p.ws_bytes = p.splits > 1 ? (size_t)p.splits * g.Cout * sizeof(float) : 0;
+        bias_plan(g, dt, &p);
         return p;
     }
     const int force = forced_path();
@@ -154,10 +171,23 @@ static void launch_direct(const Geom &g, const Plan &p, gconv_pass pass, const v
         break;
     }
     case GCONV_PASS_BWD_BIAS: {
-        float *dst = p.splits > 1 ? static_cast<float *>(ws) : out;
-        bias_grad_kernel<T><<<dim3(g.Cout, p.splits), kDirectThreads, 0, st>>>(g, A, dst, p.n_per_split);
-        if (p.splits > 1)
-            reduce_splits_kernel<<<elementwise_grid(g.Cout), kDirectThreads, 0, st>>>(dst, p.splits, g.Cout, out);
+        float *part = static_cast<float *>(ws);
+        const int64_t HW = (int64_t)g.Ho * g.Wo;
+        const int fin_grid = (g.Cout + kDirectThreads / 32 - 1) / (kDirectThreads / 32);   // a warp per channel
+        if (p.tc[0] == 0) {
+            const int64_t nplanes = (int64_t)g.N * g.Cout;
+            const int64_t blocks = (nplanes + kDirectThreads / 32 - 1) / (kDirectThreads / 32);
+            plane_sum_kernel<T><<<(int)std::min<int64_t>(blocks, (int64_t)kNumSMs * 32), kDirectThreads, 0, st>>>(
+                A, nplanes, HW, part);
+            bias_finish_kernel<<<fin_grid, kDirectThreads, 0, st>>>(part, g.N, g.Cout, 1, g.Cout, out);
+        } else {
+            const int64_t L = (int64_t)g.Cout * HW;
+            const int64_t threads = p.tc[1] ? L / (16 / (int64_t)sizeof(T)) : L;
+            const dim3 grid((unsigned)((threads + kDirectThreads - 1) / kDirectThreads), (unsigned)p.splits);
+            if (p.tc[1]) col_sum_kernel<T, true><<<grid, kDirectThreads, 0, st>>>(A, g.N, L, p.n_per_split, part);
+            else col_sum_kernel<T, false><<<grid, kDirectThreads, 0, st>>>(A, g.N, L, p.n_per_split, part);
+            bias_finish_kernel<<<fin_grid, kDirectThreads, 0, st>>>(part, p.splits, L, (int)HW, g.Cout, out);
+        }
         break;
     }
     }

@@ -177,64 +177,111 @@ reduce_splits_kernel(const float *__restrict__ part, int splits, int64_t count,
 }
 
 // ---------------------------------------------------------------------------
-// Per-lane share of the sum of the contiguous range [begin, begin + len) of a
-// bf16 / fp32 array of `array_len` elements (base 16-byte aligned) over one warp, with aligned 16-byte
-// loads (elements outside the range are masked), so it streams at full width
-// whatever the alignment of `begin`.  A final partial chunk of the array is read
-// element by element, so no load leaves the array.  Fixed order.
+// Bias gradient db[o] = sum over n, h, w of dy[n][o][h][w], in two deterministic
+// stages (no atomics), chosen by the plane size HW = Ho*Wo.
+//
+// Planes of kBiasPlaneMin elements or more: one warp per (n, o) plane writes its sum
+// to psum[n*C_out + o]; the lanes take 16-byte chunks of the plane, issuing four
+// chunks per lane before adding them, and a fixed shuffle tree finishes the plane.
+constexpr int kBiasPlaneMin = 32;
+
 template <typename T>
-__device__ __forceinline__ float warp_range_sum(const T *__restrict__ base, int64_t begin, int64_t len,
-                                                int64_t array_len)
+__global__ void __launch_bounds__(kDirectThreads)
+plane_sum_kernel(const T *__restrict__ dy, int64_t nplanes, int64_t HW, float *__restrict__ psum)
 {
     constexpr int V = 16 / sizeof(T);
     const int lane = threadIdx.x & 31;
-    const int64_t end = begin + len;
-    const int64_t c0 = begin / V, c1 = (end + V - 1) / V;   // 16-byte chunks touched
-    const int64_t full_chunks = array_len / V;
-    float acc = 0.f;
-    for (int64_t c = c0 + lane; c < c1; c += 32) {
-        if (c < full_chunks) {
-            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(base) + c);
-            const T *v = reinterpret_cast<const T *>(&raw);
+    const int64_t nw = (int64_t)gridDim.x * (kDirectThreads / 32);
+    const int64_t full_chunks = nplanes * HW / V;     // whole 16-byte chunks of the array
+    for (int64_t pl = ((int64_t)blockIdx.x * kDirectThreads + threadIdx.x) >> 5; pl < nplanes; pl += nw) {
+        const int64_t begin = pl * HW, end = begin + HW;
+        const int64_t c0 = begin / V, c1 = (end + V - 1) / V;
+        float acc = 0.f;
+        for (int64_t cb = c0; cb < c1; cb += 4 * 32) {
+            uint4 raw[4];
             #pragma unroll
-            for (int j = 0; j < V; ++j) {
-                const int64_t idx = c * V + j;
-                if (idx >= begin && idx < end) acc += to_f(v[j]);
+            for (int u = 0; u < 4; ++u) {
+                const int64_t c = cb + u * 32 + lane;
+                raw[u] = (c < c1 && c < full_chunks) ? __ldg(reinterpret_cast<const uint4 *>(dy) + c)
+                                                     : make_uint4(0u, 0u, 0u, 0u);
             }
-        } else {
-            for (int j = 0; j < V; ++j) {
-                const int64_t idx = c * V + j;
-                if (idx >= begin && idx < end) acc += to_f(__ldg(base + idx));
+            #pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t c = cb + u * 32 + lane;
+                if (c >= c1) continue;
+                if (c < full_chunks) {
+                    const T *v = reinterpret_cast<const T *>(&raw[u]);
+                    #pragma unroll
+                    for (int j = 0; j < V; ++j) {
+                        const int64_t idx = c * V + j;
+                        if (idx >= begin && idx < end) acc += to_f(v[j]);
+                    }
+                } else {   // the array's last partial chunk, element by element
+                    for (int j = 0; j < V; ++j) {
+                        const int64_t idx = c * V + j;
+                        if (idx >= begin && idx < end) acc += to_f(__ldg(dy + idx));
+                    }
+                }
             }
         }
+        #pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) psum[pl] = acc;
     }
-    return acc;   // this lane's share; the caller reduces across the warp
 }
 
-// Bias gradient.  Block (o, split) sums planes dy[n, o, :, :] for n in its range;
-// warp w takes planes n0+w, n0+w+nwarps, ...; warp totals are added in warp order.
-template <typename T>
+// Smaller planes (down to the 1 x 1 output of FC mode): dy is read as a matrix of N
+// rows of L = C_out*HW elements; thread c sums columns [c*V, c*V + V) over the rows
+// [s*rows, (s+1)*rows) of split s = blockIdx.y into part[s][L].  Consecutive threads
+// read consecutive 16-byte chunks of a row (VEC: rows 16-byte aligned), else single
+// elements.
+template <typename T, bool VEC>
 __global__ void __launch_bounds__(kDirectThreads)
-bias_grad_kernel(Geom g, const T *__restrict__ dy, float *__restrict__ out, int n_per_split)
+col_sum_kernel(const T *__restrict__ dy, int N, int64_t L, int rows, float *__restrict__ part)
 {
-    __shared__ float red[32];
-    const int o = blockIdx.x, split = blockIdx.y;
-    const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    const int64_t HWo = (int64_t)g.Ho * g.Wo;
-    const int n0 = split * n_per_split, n1 = min(g.N, n0 + n_per_split);
-    float acc = 0.f;
-    for (int n = n0 + warp; n < n1; n += nwarps)
-        acc += warp_range_sum(dy, ((int64_t)n * g.Cout + o) * HWo, HWo, (int64_t)g.N * g.Cout * HWo);
+    constexpr int V = VEC ? 16 / sizeof(T) : 1;
+    const int64_t c = (int64_t)blockIdx.x * kDirectThreads + threadIdx.x;
+    if (c * V >= L) return;
+    const int s = blockIdx.y;
+    const int n0 = s * rows, n1 = min(N, n0 + rows);
+    float acc[V];
     #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[warp] = acc;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float s = 0.f;
-        for (int i = 0; i < nwarps; ++i) s += red[i];
-        out[(int64_t)split * g.Cout + o] = s;
+    for (int j = 0; j < V; ++j) acc[j] = 0.f;
+    #pragma unroll 4
+    for (int n = n0; n < n1; ++n) {
+        const T *row = dy + (int64_t)n * L;
+        if (VEC) {
+            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(row) + c);
+            const T *v = reinterpret_cast<const T *>(&raw);
+            #pragma unroll
+            for (int j = 0; j < V; ++j) acc[j] += to_f(v[j]);
+        } else {
+            acc[0] += to_f(__ldg(row + c));
+        }
     }
+    #pragma unroll
+    for (int j = 0; j < V; ++j) part[(int64_t)s * L + c * V + j] = acc[j];
+}
+
+// Second stage of both: out[o] = sum over r < rows, i < inner of part[r*cols + o*inner + i].
+// One warp per channel: lane l takes the flattened indices l, l + 32, ... (r outer),
+// then a fixed shuffle tree adds the lanes.
+__global__ void __launch_bounds__(kDirectThreads)
+bias_finish_kernel(const float *__restrict__ part, int rows, int64_t cols, int inner, int C_out,
+                   float *__restrict__ out)
+{
+    const int o = blockIdx.x * (kDirectThreads / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (o >= C_out) return;
+    const int64_t total = (int64_t)rows * inner;
+    float s = 0.f;
+    for (int64_t e = lane; e < total; e += 32) {
+        const int64_t r = e / inner, i = e - r * inner;
+        s += __ldg(part + r * cols + (int64_t)o * inner + i);
+    }
+    #pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) out[o] = s;
 }
 
 }  // namespace gconv

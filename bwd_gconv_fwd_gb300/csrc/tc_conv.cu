@@ -435,6 +435,12 @@ blockify_kernel(const __grid_constant__ BlockifyParams p)
 // setting the descriptor's MN-chunk stride to delta rows.  A 5x5 kernel therefore
 // runs as six N = 256 MMAs and one N = 64 MMA per K step.
 constexpr int kMaxJobs = 32;
+// Words per CTA of the optional phase trace (gconv_debug_set_trace).  Weight-gradient
+// kernel: start, SM id, MMA issuer's waits for staged tiles (ns), time of the last MMA,
+// accumulator ready, end, tiles processed, staging threads' waits for a free buffer (ns).
+constexpr int kTraceWords = 8;
+constexpr int kMaxGroupJobs = 8;
+constexpr int kWgradMaxBufs = 3;   // jobs of one group share 512 TMEM columns, at least 64 each
 
 struct WgradParams {
     const __nv_bfloat16 *XT;     // blocked x  [N][G][ncx][Rx][Wp][64] (padded grid, zero padding)
@@ -449,6 +455,7 @@ struct WgradParams {
     int n_otile, n_ctile;        // 128-channel gradOutput tiles, 64-channel input tiles
     int n_tgrp;                  // job groups (one TMEM allocation each)
     int splits;                  // partial slices in the workspace (the largest group split count)
+    int nbuf;                    // staging buffers (2 or 3)
     int cta_per_cg;              // CTAs per (group, o tile, c tile): sum of the group split counts
     int grp_splits[kMaxJobs];    // split count of each job group
     int grp_cta0[kMaxJobs + 1];  // first CTA index of each job group within cta_per_cg
@@ -456,13 +463,14 @@ struct WgradParams {
     int grp_cols[kMaxJobs];      // TMEM columns allocated by group gi (power of two)
     int job_off[kMaxJobs], job_delta[kMaxJobs], job_count[kMaxJobs], job_col[kMaxJobs];
     int job_tapk[kMaxJobs][4];   // kh*kW + kw of the packed taps
+    unsigned long long *trace;   // optional per-CTA phase stamps (kTraceWords each), nullptr when off
 };
 
 __global__ void __launch_bounds__(kTcThreads, 1)
 wgrad_kernel(const __grid_constant__ WgradParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bar_full[2], bar_empty[2], bar_acc;
+    __shared__ __align__(8) uint64_t bar_full[kWgradMaxBufs], bar_empty[kWgradMaxBufs], bar_acc;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
 
@@ -488,10 +496,16 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
 
     const int dy_bytes = 2 * 128 * 128;              // two 64-channel chunks x 128 positions
     const int buf_bytes = dy_bytes + p.plane_elems * 128;
+    unsigned long long *trace = p.trace ? p.trace + (size_t)blockIdx.x * kTraceWords : nullptr;
+    if (trace && threadIdx.x == 0) {
+        trace[0] = ptx::globaltimer();
+        trace[1] = ptx::smid();
+        trace[6] = (unsigned long long)(tile1 - tile0);
+    }
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kWgradMaxBufs; ++i) {
             ptx::mbar_init(ptx::smem_u32(&bar_full[i]), kStageThreads);
             ptx::mbar_init(ptx::smem_u32(&bar_empty[i]), 1);
         }
@@ -533,53 +547,91 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
                 ptx::cp_async16(buf + (uint32_t)(dy_bytes + m * 128 + ((k ^ (m & 7)) << 4)), src, ok ? 16u : 0u);
             }
         };
-        if (tile1 > tile0) issue(tile0, 0);
-        ptx::cp_async_commit();
+        // nbuf-deep pipeline: tiles it+1 .. it+nbuf-1 are in flight while tile it is consumed;
+        // one commit group per tile (empty groups keep the count uniform)
+        const int NB = p.nbuf;
+        for (int j = 0; j < NB - 1; ++j) {
+            if (tile0 + j < tile1) issue(tile0 + j, j);
+            ptx::cp_async_commit();
+        }
+        uint64_t w_empty = 0;
         for (int it = tile0, k = 0; it < tile1; ++it, ++k) {
-            const int b = k & 1;
+            const int b = k % NB;
             bool bad = false;
-            if (it + 1 < tile1) {
-                // the other buffer must be free before the next tile's copies go in
-                if (k + 1 >= 2)
-                    bad = !ptx::mbar_wait(ptx::smem_u32(&bar_empty[b ^ 1]), ((k + 1) / 2 - 1) & 1, p.wait_ns);
+            if (it + NB - 1 < tile1) {
+                // buffer nb last held tile k-1: it must be released before the copies go in
+                const int kn = k + NB - 1, nb = kn % NB;
+                const uint64_t t0 = trace ? ptx::globaltimer() : 0;
+                if (kn >= NB) bad = !ptx::mbar_wait(ptx::smem_u32(&bar_empty[nb]), (kn / NB - 1) & 1, p.wait_ns);
+                if (trace) w_empty += ptx::globaltimer() - t0;
                 bad = ptx::bar_red_or(1, kStageThreads, bad || abort_flag);
                 if (bad) {
                     if (threadIdx.x == 0) { abort_flag = 1; raise_device_error(p.err, DEVERR_WAIT_TIMEOUT); }
                     break;
                 }
-                issue(it + 1, b ^ 1);
+                issue(it + NB - 1, nb);
             }
             ptx::cp_async_commit();
-            ptx::cp_async_wait_group<1>();           // this tile's rows have landed
+            if (NB == 3) ptx::cp_async_wait_group<2>();   // this tile's rows have landed
+            else ptx::cp_async_wait_group<1>();
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(ptx::smem_u32(&bar_full[b]));
         }
         ptx::cp_async_wait_group<0>();               // nothing may land after the CTA exits
+        if (trace && threadIdx.x == 0) trace[7] = w_empty;
     } else if (warp == kWarpMma && lane == 0) {
         // ---------------- MMA issuer ----------------
+        // Lean loop (the tensor core runs only a couple of MMAs ahead of this thread):
+        // the group's job descriptors are built once into registers, each MMA adds the
+        // buffer and K-step address (address >> 4, in the descriptor's low bits).
+        const int nj = job1 - job0;            // at most kMaxGroupJobs (512 TMEM columns / 64)
+        uint64_t bd_job[kMaxGroupJobs];
+        uint32_t id_job[kMaxGroupJobs], col_job[kMaxGroupJobs];
+        #pragma unroll
+        for (int j = 0; j < kMaxGroupJobs; ++j) {
+            const int jb = job0 + min(j, nj - 1);
+            bd_job[j] = ptx::smem_desc(0u, (uint32_t)(p.job_delta[jb] * 128), 1024u, 2) + (uint64_t)(p.job_off[jb] * 8);
+            id_job[j] = ptx::idesc_bf16(128, p.job_count[jb] * 64, 1, 1);
+            col_job[j] = (uint32_t)p.job_col[jb];
+        }
+        // gradOutput: M = 128 channels as two 64-channel chunks 16 KB apart (the leading byte offset)
+        const uint64_t adesc0 = ptx::smem_desc(0u, 128u * 128u, 1024u, 2);
         bool ok = true;
-        for (int it = tile0, k = 0; it < tile1; ++it, ++k) {
-            const int b = k & 1;
-            if (!ptx::mbar_wait(ptx::smem_u32(&bar_full[b]), (k >> 1) & 1, p.wait_ns)) { ok = false; break; }
+        uint64_t w_full = 0;
+        for (int it = tile0, k = 0, b = 0, ph = 0; it < tile1; ++it, ++k) {
+            const uint32_t fb = ptx::smem_u32(&bar_full[b]);
+            if (!ptx::mbar_try_wait(fb, (uint32_t)ph)) {
+                const uint64_t t0 = ptx::globaltimer();
+                if (!ptx::mbar_wait(fb, (uint32_t)ph, p.wait_ns)) { ok = false; break; }
+                w_full += ptx::globaltimer() - t0;
+            }
             ptx::tc_fence_after();
             const uint32_t dyb = ptx::smem_u32(smem + b * buf_bytes);
-            const uint32_t xbb = dyb + (uint32_t)dy_bytes;
-            for (int ks = 0; ks < 8; ++ks) {            // 8 K steps of 16 positions
-                // gradOutput: M = 128 channels as two 64-channel chunks 16 KB apart
-                const uint64_t adesc = ptx::smem_desc(dyb + (uint32_t)(ks * 16 * 128), 128u * 128u, 1024u, 2);
-                for (int jb = job0; jb < job1; ++jb) {
-                    const uint32_t bs = xbb + (uint32_t)((p.job_off[jb] + ks * 16) * 128);
-                    const uint64_t bdesc = ptx::smem_desc(bs, (uint32_t)(p.job_delta[jb] * 128), 1024u, 2);
-                    const uint32_t idesc = ptx::idesc_bf16(128, p.job_count[jb] * 64, 1, 1);
-                    ptx::mma_f16(tmem + (uint32_t)p.job_col[jb], adesc, bdesc, idesc, (k > 0 || ks > 0) ? 1u : 0u);
-                }
+            const uint64_t ab = adesc0 + (uint64_t)(dyb >> 4);
+            const uint64_t bb = (uint64_t)((dyb + (uint32_t)dy_bytes) >> 4);
+            // job by job, its 8 K steps of 16 positions (16 rows x 128 B) back to back, so
+            // that consecutive MMAs accumulate into the same TMEM columns
+            #pragma unroll
+            for (int j = 0; j < kMaxGroupJobs; ++j) {
+                if (j >= nj) break;
+                const uint32_t dj = tmem + col_job[j];
+                const uint64_t bj = bd_job[j] + bb;
+                #pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    ptx::mma_f16(dj, ab + (uint64_t)(ks * 128), bj + (uint64_t)(ks * 128), id_job[j],
+                                 (k > 0 || ks > 0) ? 1u : 0u);
             }
             ptx::mma_commit(ptx::smem_u32(&bar_empty[b]));
+            if (++b == p.nbuf) { b = 0; ph ^= 1; }
             if (abort_flag) { ok = false; break; }
         }
         if (!ok) {
             abort_flag = 1;
             raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
+        }
+        if (trace) {
+            trace[2] = w_full;
+            trace[3] = ptx::globaltimer();
         }
         ptx::mma_commit(ptx::smem_u32(&bar_acc));
         if (!ptx::mbar_wait(ptx::smem_u32(&bar_acc), 0, kDrainNs)) raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
@@ -597,6 +649,7 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
             ptx::tc_fence_after();
         }
         ready = __all_sync(0xffffffffu, ready && !abort_flag);
+        if (trace && threadIdx.x == 0) trace[4] = ptx::globaltimer();
         const int o = lg * 32 + lane;
         const int og = g * p.Cgo + ot * 128 + o;
         float *dst = p.part + (int64_t)split * ((int64_t)p.G * p.Cgo * p.Cgi * p.kHW);
@@ -626,6 +679,7 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if (trace && threadIdx.x == 0) trace[5] = ptx::globaltimer();
     if (warp == kWarpAux) ptx::tmem_dealloc(tmem, tmem_cols);
 }
 
@@ -670,10 +724,9 @@ constexpr int kC2WarpProd = 9;          // warps 9-12: weight producers (one iss
 constexpr int kC2MaxWStages = 4;
 constexpr int kC2Threads = (kC2WarpProd + kC2MaxWStages) * 32;
 constexpr int kC2EpiBytes = kC2EpiWarps * 32 * 33 * 4;
-// Trace words per CTA: start, SM id, MMA issuer's waits for staged chunks, for weight
-// blocks and for a free accumulator (ns), time of the last MMA, epilogue warp 0's
-// waits for accumulators (ns), end.
-constexpr int kTraceWords = 8;
+// Correlation-kernel trace words per CTA: start, SM id, MMA issuer's waits for staged
+// chunks, for weight blocks and for a free accumulator (ns), time of the last MMA,
+// epilogue warp 0's waits for accumulators (ns), end.
 
 __device__ __forceinline__ void corr2_tile(const Corr2Params &p, int t, int *ptile, int *n, int *vt, int *g)
 {
@@ -1234,6 +1287,7 @@ bool build_wgrad_jobs(const TapGeometry &tg, const std::vector<Tap> &taps, int W
             }
             if (nxt < 0) return;
             const int da = along_row ? 0 : best, db = along_row ? best : 0;
+            if ((da * Wp + db) * 8 > 0x3FFF) return;   // row stride beyond the descriptor's offset field
             J->delta = da * Wp + db;
             int cur = nxt;
             while (cur >= 0 && J->count < 4) {
@@ -1318,7 +1372,9 @@ bool build_wgrad(const Geom &g, WgradLaunch *L)
         if (w.job_off[jb] + (w.job_count[jb] - 1) * w.job_delta[jb] + 128 > w.plane_elems) return false;
     w.n_ctile = w.ncx;
     w.n_otile = (g.Cgo + 127) / 128;
-    L->smem = 1024 + 2 * ((size_t)2 * 128 * 128 + (size_t)w.plane_elems * 128);
+    const size_t buf = (size_t)2 * 128 * 128 + (size_t)w.plane_elems * 128;
+    w.nbuf = 1024 + kWgradMaxBufs * buf <= kMaxSmem ? kWgradMaxBufs : 2;
+    L->smem = 1024 + w.nbuf * buf;
     if (L->smem > kMaxSmem) return false;
     // One wave of CTAs (a partial second wave doubles the time), shared among the job
     // groups in proportion to their MMA work per K step plus the staging share.
@@ -1608,6 +1664,10 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
         L.wp.part = reinterpret_cast<float *>(wsb);
         L.wp.err = err;
         L.wp.wait_ns = (uint64_t)wait_limit();
+        size_t trace_bytes = 0;
+        void *trace = debug_trace(&trace_bytes);
+        L.wp.trace = (trace && trace_bytes >= (size_t)L.grid * kTraceWords * 8) ? static_cast<unsigned long long *>(trace)
+                                                                                 : nullptr;
         if (!smem_attr_once((const void *)wgrad_kernel, 1)) return GCONV_ERR_CUDA;
         wgrad_kernel<<<L.grid, kTcThreads, L.smem, s>>>(L.wp);
         ReduceParams rp{};

@@ -200,14 +200,12 @@ const char *gconv_status_string(gconv_status status);
 void gconv_debug_force_path(int path);
 void gconv_debug_set_wait_limit(long long limit);
 
-/* Phase trace of the stride-1 correlation kernel (process-wide, not
- * thread-safe).  While a device buffer is set, every launch of that kernel whose
- * grid fits writes eight 64-bit words per CTA, indexed by CTA: %globaltimer at
- * start, the SM id, the nanoseconds its MMA issuer waited for staged input
- * chunks, for weight blocks and for a free accumulator, the time its last MMA
- * was issued, the nanoseconds the first epilogue warp waited for accumulators,
- * and the end time.  NULL turns tracing off.  The buffer stays owned by the
- * caller. */
+/* Phase trace of the tensor-core kernels (process-wide, not thread-safe).
+ * While a device buffer is set, every launch of the stride-1 correlation kernel
+ * or the weight-gradient kernel whose grid fits writes eight 64-bit words per
+ * CTA, indexed by CTA (%globaltimer stamps, the SM id, and nanoseconds spent in
+ * waits; the kernels' sources list the words).  NULL turns tracing off.  The
+ * buffer stays owned by the caller. */
 void gconv_debug_set_trace(void *device_buffer, size_t bytes);
 
 #ifdef __cplusplus
