@@ -1,0 +1,627 @@
+// direct_tiled.cu -- CUDA-core (fp32 FMA) kernels on shared-memory tiles.
+//
+// They serve groups too thin for a tensor-core tile (a few channels per group, down
+// to depthwise) and the fp32 path.  A block owns one (image, group) and a tile of
+// output rows x columns: it stages the input planes of the group that the tile
+// reads (zero outside the image) and the group's weights in shared memory, then each
+// thread produces every output channel of the group at one position, so an input
+// value read from shared memory feeds all of them.  Stores run along output rows.
+// The weight gradient keeps one register accumulator per tap for an (output
+// channel, input channel) pair and a run of positions, reduces the position lanes
+// in shared memory in a fixed order, and a second kernel adds the blocks' partial
+// sums in a fixed order: results are bitwise reproducible.
+#include "internal.h"
+
+#include <algorithm>
+
+namespace gconv {
+
+namespace {
+
+constexpr int kTT = 256;                  // threads per block
+constexpr int kTileSmem = 48 * 1024;      // shared-memory budget of a block (no opt-in needed)
+
+struct TileGeom {
+    int TH, TW;        // output rows and columns of a block
+    int RI, CI, CIp;   // staged input rows, columns, row pitch (floats)
+    int n_th, n_tw;    // tiles along rows and columns
+    int NB, n_nb;      // weight gradient: images per block, image chunks
+    int L, P;          // weight gradient: position lanes, (output, input) channel pairs
+};
+
+__host__ __device__ __forceinline__ int floordiv_i(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+// Stages rows [r0, r0 + RI) x columns [c0, c0 + CI) of `nch` planes (zero outside the
+// H x W image) as fp32 rows of pitch CIp: a warp per row, lanes along the row.  Plain
+// nested loops (no integer division per element, which would cost more than the data
+// movement itself for thin groups).
+template <typename T>
+__device__ __forceinline__ void stage_rows(const T *__restrict__ src, int64_t plane, int H, int W, int r0, int c0,
+                                           int nch, int RI, int CI, int CIp, float *__restrict__ dst)
+{
+    constexpr int kWarps = kTT / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int c = 0; c < nch; ++c) {
+        const T *sc = src + c * plane;
+        float *dc = dst + c * RI * CIp;
+        #pragma unroll 2
+        for (int r = warp; r < RI; r += kWarps) {
+            const int ih = r0 + r;
+            const bool row_ok = ih >= 0 && ih < H;
+            const T *sr = sc + (int64_t)ih * W;
+            float *dr = dc + r * CIp;
+            #pragma unroll 2
+            for (int col = lane; col < CI; col += 32) {
+                const int iw = c0 + col;
+                dr[col] = (row_ok && iw >= 0 && iw < W) ? to_f(__ldg(sr + iw)) : 0.f;
+            }
+        }
+    }
+}
+
+// a[0..CO) += w[0..CO) * v, with 16-byte weight loads when CO is a multiple of 4
+template <int CO>
+__device__ __forceinline__ void fma_row(float (&a)[CO], const float *__restrict__ w, float v)
+{
+    if constexpr (CO % 4 == 0) {
+        const float4 *w4 = reinterpret_cast<const float4 *>(w);
+        #pragma unroll
+        for (int q = 0; q < CO / 4; ++q) {
+            const float4 u = w4[q];
+            a[4 * q] = fmaf(u.x, v, a[4 * q]);
+            a[4 * q + 1] = fmaf(u.y, v, a[4 * q + 1]);
+            a[4 * q + 2] = fmaf(u.z, v, a[4 * q + 2]);
+            a[4 * q + 3] = fmaf(u.w, v, a[4 * q + 3]);
+        }
+    } else {
+        #pragma unroll
+        for (int q = 0; q < CO; ++q) a[q] = fmaf(w[q], v, a[q]);
+    }
+}
+
+// One output position of a correlation over a staged tile: a[o] = sum over c < nin,
+// taps (kh, kw) of ws[((c*kH + kh)*kW + kw)*CO + o] * src[c*cstride + kh*rstep + kw*cstep].
+// K = 3 unrolls a 3 x 3 kernel; K = 0 takes kH x kW at run time.
+template <int CO, int K>
+__device__ __forceinline__ void corr_point(float (&a)[CO], const float *__restrict__ src, const float *__restrict__ ws,
+                                           int nin, int cstride, int kh_n, int kw_n, int rstep, int cstep)
+{
+    #pragma unroll
+    for (int o = 0; o < CO; ++o) a[o] = 0.f;
+    for (int c = 0; c < nin; ++c) {
+        const float *sc = src + c * cstride;
+        if constexpr (K == 3) {
+            const float *wc = ws + c * 9 * CO;
+            #pragma unroll
+            for (int kh = 0; kh < 3; ++kh)
+                #pragma unroll
+                for (int kw = 0; kw < 3; ++kw) fma_row<CO>(a, wc + (kh * 3 + kw) * CO, sc[kh * rstep + kw * cstep]);
+        } else {
+            const float *wc = ws + c * kh_n * kw_n * CO;
+            for (int kh = 0; kh < kh_n; ++kh)
+                for (int kw = 0; kw < kw_n; ++kw, wc += CO) fma_row<CO>(a, wc, sc[kh * rstep + kw * cstep]);
+        }
+    }
+}
+
+// Four consecutive output positions of a 3 x 3, stride-1 correlation (dilation d):
+// a[j][o] = sum over c, kh, kw of ws[((c*3 + kh)*3 + kw)*CO + o] * src[c*cstride + kh*rstep +
+// j + kw*d].  The inputs of a row are loaded once for the four positions and each tap's
+// weights once for all of them.
+template <int CO>
+__device__ __forceinline__ void corr3_strip(float (&a)[4][CO], const float *__restrict__ src,
+                                            const float *__restrict__ ws, int nin, int cstride, int rstep, int d)
+{
+    #pragma unroll
+    for (int j = 0; j < 4; ++j)
+        #pragma unroll
+        for (int o = 0; o < CO; ++o) a[j][o] = 0.f;
+    for (int c = 0; c < nin; ++c) {
+        const float *sc = src + c * cstride;
+        const float *wc = ws + c * 9 * CO;
+        #pragma unroll
+        for (int kh = 0; kh < 3; ++kh) {
+            const float *row = sc + kh * rstep;
+            float v[3][4];
+            if (d == 1) {
+                float u[6];
+                #pragma unroll
+                for (int i = 0; i < 6; ++i) u[i] = row[i];
+                #pragma unroll
+                for (int kw = 0; kw < 3; ++kw)
+                    #pragma unroll
+                    for (int j = 0; j < 4; ++j) v[kw][j] = u[j + kw];
+            } else {
+                #pragma unroll
+                for (int kw = 0; kw < 3; ++kw)
+                    #pragma unroll
+                    for (int j = 0; j < 4; ++j) v[kw][j] = row[j + kw * d];
+            }
+            #pragma unroll
+            for (int kw = 0; kw < 3; ++kw) {
+                float wv[CO];
+                const float *wt = wc + (kh * 3 + kw) * CO;
+                if constexpr (CO % 4 == 0) {
+                    #pragma unroll
+                    for (int q = 0; q < CO / 4; ++q) {
+                        const float4 u4 = reinterpret_cast<const float4 *>(wt)[q];
+                        wv[4 * q] = u4.x; wv[4 * q + 1] = u4.y; wv[4 * q + 2] = u4.z; wv[4 * q + 3] = u4.w;
+                    }
+                } else {
+                    #pragma unroll
+                    for (int o = 0; o < CO; ++o) wv[o] = wt[o];
+                }
+                #pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    #pragma unroll
+                    for (int o = 0; o < CO; ++o) a[j][o] = fmaf(wv[o], v[kw][j], a[j][o]);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Forward.  ws[e][o] = w[g*Cgo + o][e] (e = c*kH*kW + kh*kW + kw), CO floats per e (zero
+// past Cgo).  Threads walk the tile's positions row-major (an incremental row and
+// column, no division per position), each producing all CO channels there.
+template <typename T, int CO, int K>
+__device__ __forceinline__ void fwd_tile(const Geom &g, const TileGeom &t, int b, const T *__restrict__ x,
+                                         const T *__restrict__ w, const T *__restrict__ bias, float *__restrict__ y)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int KK = g.kH * g.kW, E = g.Cgi * KK;
+    float *ws = sm;
+    float *xs = sm + E * CO;
+    const int tw = b % t.n_tw; b /= t.n_tw;
+    const int th = b % t.n_th; b /= t.n_th;
+    const int grp = b % g.G;
+    const int n = b / g.G;
+    const int oh0 = th * t.TH, ow0 = tw * t.TW;
+    for (int i = threadIdx.x; i < E * CO; i += kTT) {
+        const int e = i / CO, o = i - e * CO;
+        ws[i] = o < g.Cgo ? to_f(w[(int64_t)(grp * g.Cgo + o) * E + e]) : 0.f;
+    }
+    const int64_t plane = (int64_t)g.H * g.W;
+    stage_rows(x + ((int64_t)n * g.Cin + (int64_t)grp * g.Cgi) * plane, plane, g.H, g.W, oh0 * g.s - g.pt,
+               ow0 * g.s - g.pl, g.Cgi, t.RI, t.CI, t.CIp, xs);
+    __syncthreads();
+    const int64_t out_plane = (int64_t)g.Ho * g.Wo;
+    float *yg = y + ((int64_t)n * g.Cout + (int64_t)grp * g.Cgo) * out_plane;
+    float bv[CO];
+    #pragma unroll
+    for (int o = 0; o < CO; ++o) bv[o] = (bias && o < g.Cgo) ? to_f(bias[grp * g.Cgo + o]) : 0.f;
+    const int rows = min(t.TH, g.Ho - oh0), cols = min(t.TW, g.Wo - ow0);
+    if (K == 3 && g.s == 1) {
+        // strips of four consecutive columns (the staged rows carry 4 spare columns)
+        const int strips = (cols + 3) >> 2;
+        const int dr = kTT / strips, dc = kTT - dr * strips;
+        int r = threadIdx.x / strips, sc = threadIdx.x - r * strips;
+        for (int pi = threadIdx.x; pi < rows * strips; pi += kTT) {
+            float acc[4][CO];
+            corr3_strip<CO>(acc, xs + r * t.CIp + 4 * sc, ws, g.Cgi, t.RI * t.CIp, g.d * t.CIp, g.d);
+            float *yo = yg + (int64_t)(oh0 + r) * g.Wo + ow0 + 4 * sc;
+            #pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (4 * sc + j < cols)
+                    #pragma unroll
+                    for (int o = 0; o < CO; ++o)
+                        if (o < g.Cgo) yo[o * out_plane + j] = acc[j][o] + bv[o];
+            r += dr;
+            sc += dc;
+            if (sc >= strips) { sc -= strips; ++r; }
+        }
+        return;
+    }
+    const int dr = kTT / cols, dc = kTT - dr * cols;
+    int r = threadIdx.x / cols, col = threadIdx.x - r * cols;
+    for (int pi = threadIdx.x; pi < rows * cols; pi += kTT) {
+        float acc[CO];
+        corr_point<CO, K>(acc, xs + (r * g.s) * t.CIp + col * g.s, ws, g.Cgi, t.RI * t.CIp, g.kH, g.kW,
+                          g.d * t.CIp, g.d);
+        float *yo = yg + (int64_t)(oh0 + r) * g.Wo + ow0 + col;
+        #pragma unroll
+        for (int o = 0; o < CO; ++o)
+            if (o < g.Cgo) yo[o * out_plane] = acc[o] + bv[o];
+        r += dr;
+        col += dc;
+        if (col >= cols) { col -= cols; ++r; }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Backward-data: dx[n][g*Cgi + c][ih][iw] = sum over o, kh, kw of w[g*Cgo + o][c][kh][kw] *
+// dy[n][g*Cgo + o][(ih + pt - kh*d)/s][(iw + pl - kw*d)/s] where the division is exact
+// and in range.  The block stages the gradOutput rows and columns its tile reaches
+// (zero outside).  Stride 1 is a plain correlation of that tile with the mirrored
+// taps, ws[((o*kH + kh)*kW + kw)][c] = w[g*Cgo + o][c][kH-1-kh][kW-1-kw]; other strides
+// take only the taps whose division is exact (weights unmirrored in that case).
+template <typename T, int CI_, int K>
+__device__ __forceinline__ void bwd_data_tile(const Geom &g, const TileGeom &t, int b, const T *__restrict__ dy,
+                                              const T *__restrict__ w, float *__restrict__ dx)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int KK = g.kH * g.kW;
+    float *ws = sm;
+    float *ds = sm + g.Cgo * KK * CI_;
+    const int tw = b % t.n_tw; b /= t.n_tw;
+    const int th = b % t.n_th; b /= t.n_th;
+    const int grp = b % g.G;
+    const int n = b / g.G;
+    const int ih0 = th * t.TH, iw0 = tw * t.TW;
+    const int oh_s = floordiv_i(ih0 + g.pt - (g.kH - 1) * g.d, g.s);
+    const int ow_s = floordiv_i(iw0 + g.pl - (g.kW - 1) * g.d, g.s);
+    const bool unit = g.s == 1;
+    for (int i = threadIdx.x; i < g.Cgo * KK * CI_; i += kTT) {
+        const int ok = i / CI_, c = i - ok * CI_;
+        const int o = ok / KK, k = ok - o * KK;
+        const int ksrc = unit ? KK - 1 - k : k;   // stride 1: mirrored taps
+        ws[i] = c < g.Cgi ? to_f(w[((int64_t)(grp * g.Cgo + o) * g.Cgi + c) * KK + ksrc]) : 0.f;
+    }
+    const int64_t plane = (int64_t)g.Ho * g.Wo;
+    stage_rows(dy + ((int64_t)n * g.Cout + (int64_t)grp * g.Cgo) * plane, plane, g.Ho, g.Wo, oh_s, ow_s, g.Cgo,
+               t.RI, t.CI, t.CIp, ds);
+    __syncthreads();
+    const int64_t in_plane = (int64_t)g.H * g.W;
+    float *xg = dx + ((int64_t)n * g.Cin + (int64_t)grp * g.Cgi) * in_plane;
+    const int rows = min(t.TH, g.H - ih0), cols = min(t.TW, g.W - iw0);
+    if (K == 3 && unit) {
+        const int strips = (cols + 3) >> 2;
+        const int dr = kTT / strips, dc = kTT - dr * strips;
+        int r = threadIdx.x / strips, sc = threadIdx.x - r * strips;
+        for (int pi = threadIdx.x; pi < rows * strips; pi += kTT) {
+            float acc[4][CI_];
+            corr3_strip<CI_>(acc, ds + r * t.CIp + 4 * sc, ws, g.Cgo, t.RI * t.CIp, g.d * t.CIp, g.d);
+            float *xo = xg + (int64_t)(ih0 + r) * g.W + iw0 + 4 * sc;
+            #pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (4 * sc + j < cols)
+                    #pragma unroll
+                    for (int c = 0; c < CI_; ++c)
+                        if (c < g.Cgi) xo[c * in_plane + j] = acc[j][c];
+            r += dr;
+            sc += dc;
+            if (sc >= strips) { sc -= strips; ++r; }
+        }
+        return;
+    }
+    const int dr = kTT / cols, dc = kTT - dr * cols;
+    int r = threadIdx.x / cols, col = threadIdx.x - r * cols;
+    for (int pi = threadIdx.x; pi < rows * cols; pi += kTT) {
+        float acc[CI_];
+        if (unit) {
+            // staged row of (ih - kh*d + pt) is ihl + (kH-1-kh)*d: mirrored tap kh' = kH-1-kh
+            corr_point<CI_, K>(acc, ds + r * t.CIp + col, ws, g.Cgo, t.RI * t.CIp, g.kH, g.kW, g.d * t.CIp, g.d);
+        } else {
+            #pragma unroll
+            for (int c = 0; c < CI_; ++c) acc[c] = 0.f;
+            const int ih = ih0 + r, iw = iw0 + col;
+            for (int kh = 0; kh < g.kH; ++kh) {
+                const int tt = ih + g.pt - kh * g.d;
+                if (tt < 0 || tt % g.s) continue;
+                const int oh = tt / g.s;
+                if (oh >= g.Ho) continue;
+                for (int kw = 0; kw < g.kW; ++kw) {
+                    const int tu = iw + g.pl - kw * g.d;
+                    if (tu < 0 || tu % g.s) continue;
+                    const int ow = tu / g.s;
+                    if (ow >= g.Wo) continue;
+                    const float *dp = ds + (oh - oh_s) * t.CIp + (ow - ow_s);
+                    const float *wp = ws + (kh * g.kW + kw) * CI_;
+                    for (int o = 0; o < g.Cgo; ++o, dp += t.RI * t.CIp, wp += KK * CI_) fma_row<CI_>(acc, wp, *dp);
+                }
+            }
+        }
+        float *xo = xg + (int64_t)(ih0 + r) * g.W + iw0 + col;
+        #pragma unroll
+        for (int c = 0; c < CI_; ++c)
+            if (c < g.Cgi) xo[c * in_plane] = acc[c];
+        r += dr;
+        col += dc;
+        if (col >= cols) { col -= cols; ++r; }
+    }
+}
+
+// Persistent forms: a block walks tiles blockIdx.x, blockIdx.x + gridDim.x, ... so that its
+// set-up is paid once and the grid stays at a few resident waves.
+template <typename T, int CO, int K>
+__global__ void __launch_bounds__(kTT)
+fwd_tiled_kernel(Geom g, TileGeom t, const T *__restrict__ x, const T *__restrict__ w,
+                 const T *__restrict__ bias, float *__restrict__ y)
+{
+    const int ntiles = g.N * g.G * t.n_th * t.n_tw;
+    for (int b = blockIdx.x; b < ntiles; b += gridDim.x) {
+        fwd_tile<T, CO, K>(g, t, b, x, w, bias, y);
+        __syncthreads();   // the staged tile is no longer read
+    }
+}
+
+template <typename T, int CI_, int K>
+__global__ void __launch_bounds__(kTT)
+bwd_data_tiled_kernel(Geom g, TileGeom t, const T *__restrict__ dy, const T *__restrict__ w,
+                      float *__restrict__ dx)
+{
+    const int ntiles = g.N * g.G * t.n_th * t.n_tw;
+    for (int b = blockIdx.x; b < ntiles; b += gridDim.x) {
+        bwd_data_tile<T, CI_, K>(g, t, b, dy, w, dx);
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Backward-weight partial sums.  Block (image chunk, row tile, column tile, group):
+// thread (pair q, lane l) owns output channel o = q / Cgi, input channel c = q % Cgi,
+// and the tile positions l, l + L, ...; it keeps KK accumulators (one per tap) over
+// the chunk's images.  The L lanes of a pair are then added in lane order and the
+// block writes part[block][q*KK + tap].
+template <typename T, int KK>
+__global__ void __launch_bounds__(kTT)
+bwd_weight_tiled_kernel(Geom g, TileGeom t, const T *__restrict__ x, const T *__restrict__ dy,
+                        float *__restrict__ part)
+{
+    extern __shared__ __align__(16) float sm[];
+    float *xs = sm;                                   // [Cgi][RI][CIp]
+    float *ds = sm + g.Cgi * t.RI * t.CIp;            // [Cgo][TH][TW]
+    int b = blockIdx.x;
+    const int nb = b % t.n_nb; b /= t.n_nb;
+    const int tw = b % t.n_tw; b /= t.n_tw;
+    const int th = b % t.n_th; b /= t.n_th;
+    const int grp = b;
+    const int oh0 = th * t.TH, ow0 = tw * t.TW;
+    const int ih0 = oh0 * g.s - g.pt, iw0 = ow0 * g.s - g.pl;
+    const int q = threadIdx.x / t.L, l = threadIdx.x - q * t.L;
+    const bool active = q < t.P;
+    const int o = active ? q / g.Cgi : 0, c = active ? q - o * g.Cgi : 0;
+    int toff[KK];
+    #pragma unroll
+    for (int k = 0; k < KK; ++k) {
+        const int kh = k / g.kW, kw = k - kh * g.kW;
+        toff[k] = kh * g.d * t.CIp + kw * g.d;
+    }
+    float acc[KK];
+    #pragma unroll
+    for (int k = 0; k < KK; ++k) acc[k] = 0.f;
+    const int64_t in_plane = (int64_t)g.H * g.W, out_plane = (int64_t)g.Ho * g.Wo;
+    const int dtile = t.TH * t.TW;
+    const int n1 = min(g.N, (nb + 1) * t.NB);
+    for (int n = nb * t.NB; n < n1; ++n) {
+        const T *xg = x + ((int64_t)n * g.Cin + (int64_t)grp * g.Cgi) * in_plane;
+        const T *dg = dy + ((int64_t)n * g.Cout + (int64_t)grp * g.Cgo) * out_plane;
+        __syncthreads();   // the previous image's tiles are no longer read
+        stage_rows(xg, in_plane, g.H, g.W, ih0, iw0, g.Cgi, t.RI, t.CI, t.CIp, xs);
+        stage_rows(dg, out_plane, g.Ho, g.Wo, oh0, ow0, g.Cgo, t.TH, t.TW, t.TW, ds);   // zero past the output
+        __syncthreads();
+        if (active) {
+            const float *dsp = ds + o * dtile;
+            const float *xsp = xs + c * t.RI * t.CIp;
+            const int dr = t.L / t.TW, dc = t.L - dr * t.TW;
+            int r = l / t.TW, col = l - r * t.TW;
+            for (int pi = l; pi < dtile; pi += t.L) {
+                const float dv = dsp[pi];
+                const float *xb = xsp + (r * g.s) * t.CIp + col * g.s;
+                #pragma unroll
+                for (int k = 0; k < KK; ++k) acc[k] = fmaf(dv, xb[toff[k]], acc[k]);
+                r += dr;
+                col += dc;
+                if (col >= t.TW) { col -= t.TW; ++r; }
+            }
+        }
+    }
+    // add the L lanes of each pair in lane order (reusing the staged tiles' memory)
+    __syncthreads();
+    float *red = sm;   // [P*KK][L]
+    if (active) {
+        #pragma unroll
+        for (int k = 0; k < KK; ++k) red[(q * KK + k) * t.L + l] = acc[k];
+    }
+    __syncthreads();
+    float *dst = part + (int64_t)blockIdx.x * t.P * KK;
+    for (int i = threadIdx.x; i < t.P * KK; i += kTT) {
+        float s = 0.f;
+        for (int j = 0; j < t.L; ++j) s += red[i * t.L + j];
+        dst[i] = s;
+    }
+}
+
+// dw[(g*Cgo + o)][c][tap] = sum over the group's blocks of part[block][q*KK + tap], block
+// order, one warp per weight element (lanes over blocks, then a fixed shuffle tree).
+__global__ void __launch_bounds__(kTT)
+weight_finish_kernel(const float *__restrict__ part, int G, int nbg, int P, int KK, int Cgi,
+                     float *__restrict__ dw)
+{
+    const int64_t idx = (int64_t)blockIdx.x * (kTT / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int64_t per_group = (int64_t)P * KK;
+    if (idx >= (int64_t)G * per_group) return;
+    const int grp = (int)(idx / per_group);
+    const int i = (int)(idx - grp * per_group);         // q*KK + tap, q = o*Cgi + c
+    float s = 0.f;
+    for (int j = lane; j < nbg; j += 32) s += part[((int64_t)grp * nbg + j) * per_group + i];
+    #pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) {
+        const int q = i / KK, k = i - q * KK;
+        const int o = q / Cgi, c = q - o * Cgi;
+        dw[((int64_t)(grp * (P / Cgi) + o) * Cgi + c) * KK + k] = s;
+    }
+}
+
+// Output tile for the forward / backward-data kernels: about `target` positions, staged
+// input within the shared-memory budget next to `fixed` floats of weights.
+bool pick_tile(int out_h, int out_w, int s, int d, int k_h, int k_w, int in_ch, int fixed, bool transposed,
+               int target, TileGeom *t)
+{
+    int TW = std::min(out_w, 128);
+    for (; TW >= 8 || TW == out_w; TW = TW > 8 ? TW / 2 : 0) {
+        int TH = std::max(1, std::min(out_h, target / TW));
+        for (; TH >= 1; TH = TH > 1 ? TH / 2 : 0) {
+            int RI, CI;
+            if (!transposed) {
+                RI = (TH - 1) * s + (k_h - 1) * d + 1;
+                CI = (TW - 1) * s + (k_w - 1) * d + 1;
+            } else {   // gradOutput rows reachable from TH input rows
+                RI = (TH - 1 + (k_h - 1) * d) / s + 2;
+                CI = (TW - 1 + (k_w - 1) * d) / s + 2;
+            }
+            const int CIp = (CI + 4) | 1;   // spare columns for 4-wide strips; odd pitch spreads banks
+            const int64_t floats = (int64_t)fixed + (int64_t)in_ch * RI * CIp;
+            if (floats * 4 <= kTileSmem) {
+                t->TH = TH; t->TW = TW; t->RI = RI; t->CI = CI; t->CIp = CIp;
+                t->n_th = (out_h + TH - 1) / TH;
+                t->n_tw = (out_w + TW - 1) / TW;
+                return true;
+            }
+            if (TH == 1) break;
+        }
+        if (TW == out_w && TW < 8) break;
+    }
+    return false;
+}
+
+// Register accumulators per thread: produced channels rounded up to 1, 2, 4, 8 or 16.
+int produced_slots(int c) { return c <= 2 ? c : (c <= 4 ? 4 : (c <= 8 ? 8 : (c <= 16 ? 16 : 0))); }
+
+bool plan_fwd(const Geom &g, TileGeom *t, size_t *smem)
+{
+    const int CO = produced_slots(g.Cgo);
+    if (!CO) return false;
+    const int fixed = g.Cgi * g.kH * g.kW * CO;
+    if (!pick_tile(g.Ho, g.Wo, g.s, g.d, g.kH, g.kW, g.Cgi, fixed, false, 16384 / std::max(CO, 4), t)) return false;
+    *smem = (size_t)(fixed + g.Cgi * t->RI * t->CIp) * 4;
+    return true;
+}
+
+bool plan_bwd_data(const Geom &g, TileGeom *t, size_t *smem)
+{
+    const int CI_ = produced_slots(g.Cgi);
+    if (!CI_) return false;
+    const int fixed = g.Cgo * g.kH * g.kW * CI_;
+    if (!pick_tile(g.H, g.W, g.s, g.d, g.kH, g.kW, g.Cgo, fixed, true, 16384 / std::max(CI_, 4), t)) return false;
+    *smem = (size_t)(fixed + g.Cgo * t->RI * t->CIp) * 4;
+    return true;
+}
+
+bool plan_bwd_weight(const Geom &g, TileGeom *t, size_t *smem)
+{
+    const int KK = g.kH * g.kW;
+    if (KK != 1 && KK != 4 && KK != 9 && KK != 25) return false;   // instantiated tap counts
+    const int P = g.Cgi * g.Cgo;
+    if (P > kTT) return false;
+    t->P = P;
+    t->L = kTT / P;
+    int TW = std::min(g.Wo, 64);
+    int TH = std::max(1, std::min(g.Ho, 4096 / TW));
+    for (;; TH = TH > 1 ? TH / 2 : TH, TW = TH == 1 ? std::max(1, TW / 2) : TW) {
+        const int RI = (TH - 1) * g.s + (g.kH - 1) * g.d + 1, CI = (TW - 1) * g.s + (g.kW - 1) * g.d + 1;
+        const int CIp = CI | 1;
+        const int64_t floats = std::max<int64_t>((int64_t)g.Cgi * RI * CIp + (int64_t)g.Cgo * TH * TW,
+                                                 (int64_t)P * KK * t->L);
+        if (floats * 4 <= kTileSmem) {
+            t->TH = TH; t->TW = TW; t->RI = RI; t->CI = CI; t->CIp = CIp;
+            *smem = (size_t)floats * 4;
+            break;
+        }
+        if (TH == 1 && TW == 1) return false;
+    }
+    t->n_th = (g.Ho + t->TH - 1) / t->TH;
+    t->n_tw = (g.Wo + t->TW - 1) / t->TW;
+    // images per block: about four waves of blocks
+    const int64_t spatial = (int64_t)g.G * t->n_th * t->n_tw;
+    int n_nb = (int)std::max<int64_t>(1, std::min<int64_t>(g.N, (4 * (int64_t)kNumSMs * 4 + spatial - 1) / spatial));
+    t->NB = (g.N + n_nb - 1) / n_nb;
+    t->n_nb = (g.N + t->NB - 1) / t->NB;
+    return true;
+}
+
+template <typename T>
+gconv_status launch_typed(const Geom &g, const Plan &, gconv_pass pass, const void *a, const void *b,
+                          const void *bias, float *out, void *ws, cudaStream_t s)
+{
+    TileGeom t{};
+    size_t smem = 0;
+    const T *A = static_cast<const T *>(a), *B = static_cast<const T *>(b);
+    if (pass == GCONV_PASS_FWD) {
+        if (!plan_fwd(g, &t, &smem)) return GCONV_ERR_UNSUPPORTED;
+        const int grid = (int)std::min<int64_t>((int64_t)g.N * g.G * t.n_th * t.n_tw, (int64_t)kNumSMs * 8);
+        const T *bi = static_cast<const T *>(bias);
+        const bool k3 = g.kH == 3 && g.kW == 3;
+#define GCONV_FWD_TILED(CO)                                                                          \
+        if (k3) fwd_tiled_kernel<T, CO, 3><<<grid, kTT, smem, s>>>(g, t, A, B, bi, out);             \
+        else fwd_tiled_kernel<T, CO, 0><<<grid, kTT, smem, s>>>(g, t, A, B, bi, out);
+        switch (produced_slots(g.Cgo)) {
+        case 1: GCONV_FWD_TILED(1) break;
+        case 2: GCONV_FWD_TILED(2) break;
+        case 4: GCONV_FWD_TILED(4) break;
+        case 8: GCONV_FWD_TILED(8) break;
+        default: GCONV_FWD_TILED(16) break;
+        }
+#undef GCONV_FWD_TILED
+        return GCONV_OK;
+    }
+    if (pass == GCONV_PASS_BWD_DATA) {
+        if (!plan_bwd_data(g, &t, &smem)) return GCONV_ERR_UNSUPPORTED;
+        const int grid = (int)std::min<int64_t>((int64_t)g.N * g.G * t.n_th * t.n_tw, (int64_t)kNumSMs * 8);
+        const bool k3 = g.kH == 3 && g.kW == 3;
+#define GCONV_BWD_DATA_TILED(CI_)                                                                    \
+        if (k3) bwd_data_tiled_kernel<T, CI_, 3><<<grid, kTT, smem, s>>>(g, t, A, B, out);           \
+        else bwd_data_tiled_kernel<T, CI_, 0><<<grid, kTT, smem, s>>>(g, t, A, B, out);
+        switch (produced_slots(g.Cgi)) {
+        case 1: GCONV_BWD_DATA_TILED(1) break;
+        case 2: GCONV_BWD_DATA_TILED(2) break;
+        case 4: GCONV_BWD_DATA_TILED(4) break;
+        case 8: GCONV_BWD_DATA_TILED(8) break;
+        default: GCONV_BWD_DATA_TILED(16) break;
+        }
+#undef GCONV_BWD_DATA_TILED
+        return GCONV_OK;
+    }
+    if (pass == GCONV_PASS_BWD_WEIGHT) {
+        if (!plan_bwd_weight(g, &t, &smem)) return GCONV_ERR_UNSUPPORTED;
+        const int nbg = t.n_th * t.n_tw * t.n_nb;
+        const int grid = g.G * nbg;
+        float *part = static_cast<float *>(ws);
+        switch (g.kH * g.kW) {
+        case 1: bwd_weight_tiled_kernel<T, 1><<<grid, kTT, smem, s>>>(g, t, A, B, part); break;
+        case 4: bwd_weight_tiled_kernel<T, 4><<<grid, kTT, smem, s>>>(g, t, A, B, part); break;
+        case 9: bwd_weight_tiled_kernel<T, 9><<<grid, kTT, smem, s>>>(g, t, A, B, part); break;
+        default: bwd_weight_tiled_kernel<T, 25><<<grid, kTT, smem, s>>>(g, t, A, B, part); break;
+        }
+        const int64_t elems = (int64_t)g.G * t.P * g.kH * g.kW;
+        weight_finish_kernel<<<(unsigned)((elems + kTT / 32 - 1) / (kTT / 32)), kTT, 0, s>>>(
+            part, g.G, nbg, t.P, g.kH * g.kW, g.Cgi, out);
+        return GCONV_OK;
+    }
+    return GCONV_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+bool tiled_plan(const Geom &g, gconv_pass pass, Plan *p)
+{
+    TileGeom t{};
+    size_t smem = 0;
+    if (pass == GCONV_PASS_FWD && plan_fwd(g, &t, &smem)) {
+        p->launches = 1;
+        p->ws_bytes = 0;
+        return true;
+    }
+    if (pass == GCONV_PASS_BWD_DATA && plan_bwd_data(g, &t, &smem)) {
+        p->launches = 1;
+        p->ws_bytes = 0;
+        return true;
+    }
+    if (pass == GCONV_PASS_BWD_WEIGHT && plan_bwd_weight(g, &t, &smem)) {
+        p->launches = 2;
+        p->ws_bytes = (size_t)g.G * t.n_th * t.n_tw * t.n_nb * t.P * g.kH * g.kW * sizeof(float);
+        return true;
+    }
+    return false;
+}
+
+gconv_status tiled_launch(const Geom &g, const Plan &p, gconv_dtype dt, gconv_pass pass, const void *a,
+                          const void *b, const void *bias, float *out, void *ws, cudaStream_t s)
+{
+    return dt == GCONV_BF16 ? launch_typed<__nv_bfloat16>(g, p, pass, a, b, bias, out, ws, s)
+                            : launch_typed<float>(g, p, pass, a, b, bias, out, ws, s);
+}
+
+}  // namespace gconv

@@ -136,6 +136,10 @@ Plan plan_pass(const Geom &g, gconv_dtype dt, gconv_pass pass)
         return p;
     }
     p.path = GCONV_PATH_DIRECT;
+    if (tiled_plan(g, pass, &p)) {
+        p.tc[0] = 1;   // shared-memory tiled kernels
+        return p;
+    }
     if (pass == GCONV_PASS_BWD_WEIGHT) {
         direct_weight_split(g, &p.splits, &p.pos_per_split);
         p.launches = p.splits > 1 ? 2 : 1;
@@ -221,6 +225,8 @@ static gconv_status run_pass(const int *geo, gconv_dtype dt, gconv_pass pass, co
         st = tc_igemm_launch(g, p, pass, a, b, bias, out, ws, s);
     } else if (p.path == GCONV_PATH_TC_FC) {
         st = tc_fc_launch(g, p, pass, a, b, bias, out, ws, s);
+    } else if (p.path == GCONV_PATH_DIRECT && p.tc[0] == 1) {
+        st = tiled_launch(g, p, dt, pass, a, b, bias, out, ws, s);
     } else if (dt == GCONV_BF16) {
         launch_direct<__nv_bfloat16>(g, p, pass, a, b, bias, out, ws, s);
     } else {

@@ -33,6 +33,11 @@ bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p);
 gconv_status tc_igemm_launch(const Geom &g, const Plan &p, gconv_pass pass, const void *a,
                              const void *b, const void *bias, float *out, void *ws, cudaStream_t s);
 
+// CUDA-core kernels on shared-memory tiles for thin groups and fp32 (direct_tiled.cu)
+bool tiled_plan(const Geom &g, gconv_pass pass, Plan *p);
+gconv_status tiled_launch(const Geom &g, const Plan &p, gconv_dtype dt, gconv_pass pass, const void *a,
+                          const void *b, const void *bias, float *out, void *ws, cudaStream_t s);
+
 // tcgen05 dense-GEMM family for input size == kernel size (tc_gemm.cu)
 bool tc_fc_plan(const Geom &g, gconv_pass pass, Plan *p);
 gconv_status tc_fc_launch(const Geom &g, const Plan &p, gconv_pass pass, const void *a,
