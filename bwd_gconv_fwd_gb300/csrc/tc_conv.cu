@@ -421,6 +421,52 @@ blockify_kernel(const __grid_constant__ BlockifyParams p)
     for (int k = 0; k < 8; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
+// Stride-2 form of the blocked copy for the weight gradient: out[p][n][g][j][r][c][0..63]
+// = in[n][g*Cg + 64*j + e][r*s + roff[p]][c*s + coff[p]], zero outside the image.  Plane
+// p holds one stride phase of the padded input, so a strided tap of that phase reads
+// the plane at a plain (row, column) shift; each plane is laid out exactly like the
+// stride-1 blocked copy.
+struct PhaseBlockifyParams {
+    const __nv_bfloat16 *in;
+    __nv_bfloat16 *out;
+    int N, G, Cg, nchunk, IH, IW, R, C;
+    int s, nplane;
+    int roff[kMaxPlanes], coff[kMaxPlanes];
+};
+
+__global__ void __launch_bounds__(kBlockifyThreads)
+blockify_phase_kernel(const __grid_constant__ PhaseBlockifyParams p)
+{
+    const int plane_out = p.R * p.C;
+    const int64_t ngj = (int64_t)p.N * p.G * p.nchunk;
+    const int64_t total = ngj * p.nplane * plane_out;
+    const int64_t q = (int64_t)blockIdx.x * kBlockifyThreads + threadIdx.x;
+    if (q >= total) return;
+    const int64_t blk = q / plane_out;                 // (plane*N*G + n*G + g)*nchunk + j
+    const int pos = (int)(q - blk * plane_out);
+    const int r = pos / p.C, c = pos - r * p.C;
+    const int j = (int)(blk % p.nchunk);
+    const int64_t t = blk / p.nchunk;
+    const int64_t ng = t % ((int64_t)p.N * p.G);       // n*G + g
+    const int pl = (int)(t / ((int64_t)p.N * p.G));
+    const int row = r * p.s + p.roff[pl], col = c * p.s + p.coff[pl];
+    const bool inside = row >= 0 && row < p.IH && col >= 0 && col < p.IW;
+    const int cvalid = inside ? min(64, p.Cg - 64 * j) : 0;
+    const int64_t plane = (int64_t)p.IH * p.IW;
+    const unsigned short *src = reinterpret_cast<const unsigned short *>(p.in) + (ng * p.Cg + 64 * j) * plane +
+                                (inside ? (int64_t)row * p.IW + col : 0);
+    uint32_t w[32];
+    #pragma unroll
+    for (int h = 0; h < 32; ++h) {
+        const uint32_t lo = 2 * h < cvalid ? (uint32_t)__ldg(src + (2 * h) * plane) : 0u;
+        const uint32_t hi = 2 * h + 1 < cvalid ? (uint32_t)__ldg(src + (2 * h + 1) * plane) : 0u;
+        w[h] = lo | (hi << 16);
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(p.out) + q * 8;
+    #pragma unroll
+    for (int k = 0; k < 8; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+}
+
 // ===========================================================================
 // Backward-weight kernel (stride 1)
 // ===========================================================================
@@ -1347,35 +1393,18 @@ struct WgradLaunch {
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
-bool build_wgrad(const Geom &g, WgradLaunch *L)
+// Staging buffers, split-K slices and grid of one weight-gradient launch whose jobs are set.
+bool size_wgrad(const Geom &g, WgradParams *wp, size_t *smem, int *grid)
 {
-    if (g.s != 1 || g.Cgi < 8 || g.Cgo < 16) return false;
-    const std::vector<Tap> taps = forward_taps(g);
-    if ((int)taps.size() > kMaxTaps) return false;
-    TapGeometry tg;
-    if (!tap_geometry(taps, 1, &tg)) return false;
-    WgradParams &w = L->wp;
-    w = WgradParams{};
-    w.N = g.N; w.G = g.G; w.Cgi = g.Cgi; w.Cgo = g.Cgo; w.kHW = g.kH * g.kW;
-    w.Ho = g.Ho;
-    w.Wp = g.Wo + tg.maxb;            // = W + pad_left + pad_right for stride 1
-    w.Rx = g.Ho + tg.maxa;            // = H + pad_top + pad_bottom
-    w.ncx = (g.Cgi + 63) / 64;
-    w.ncy = (g.Cgo + 63) / 64;
-    w.TH = std::min(128 / w.Wp, g.Ho);
-    if (w.TH < 1) return false;
-    w.n_rowblk = (g.Ho + w.TH - 1) / w.TH;
-    // positions read: 128 of the tile plus the farthest tap, plus the packed-tap chunks beyond it
-    w.plane_elems = round_up(128 + tg.maxa * w.Wp + tg.maxb + 8, 8);
-    if (!build_wgrad_jobs(tg, taps, w.Wp, &w)) return false;
+    WgradParams &w = *wp;
     for (int jb = 0; jb < w.grp_first[w.n_tgrp]; ++jb)
         if (w.job_off[jb] + (w.job_count[jb] - 1) * w.job_delta[jb] + 128 > w.plane_elems) return false;
     w.n_ctile = w.ncx;
     w.n_otile = (g.Cgo + 127) / 128;
     const size_t buf = (size_t)2 * 128 * 128 + (size_t)w.plane_elems * 128;
     w.nbuf = 1024 + kWgradMaxBufs * buf <= kMaxSmem ? kWgradMaxBufs : 2;
-    L->smem = 1024 + w.nbuf * buf;
-    if (L->smem > kMaxSmem) return false;
+    *smem = 1024 + w.nbuf * buf;
+    if (*smem > kMaxSmem) return false;
     // One wave of CTAs (a partial second wave doubles the time), shared among the job
     // groups in proportion to their MMA work per K step plus the staging share.
     const int outer = g.G * w.n_otile * w.n_ctile;
@@ -1401,7 +1430,32 @@ bool build_wgrad(const Geom &g, WgradLaunch *L)
         w.splits = std::max(w.splits, S);
     }
     w.cta_per_cg = w.grp_cta0[w.n_tgrp];
-    L->grid = outer * w.cta_per_cg;
+    *grid = outer * w.cta_per_cg;
+    return true;
+}
+
+bool build_wgrad(const Geom &g, WgradLaunch *L)
+{
+    if (g.s != 1 || g.Cgi < 8 || g.Cgo < 16) return false;
+    const std::vector<Tap> taps = forward_taps(g);
+    if ((int)taps.size() > kMaxTaps) return false;
+    TapGeometry tg;
+    if (!tap_geometry(taps, 1, &tg)) return false;
+    WgradParams &w = L->wp;
+    w = WgradParams{};
+    w.N = g.N; w.G = g.G; w.Cgi = g.Cgi; w.Cgo = g.Cgo; w.kHW = g.kH * g.kW;
+    w.Ho = g.Ho;
+    w.Wp = g.Wo + tg.maxb;            // = W + pad_left + pad_right for stride 1
+    w.Rx = g.Ho + tg.maxa;            // = H + pad_top + pad_bottom
+    w.ncx = (g.Cgi + 63) / 64;
+    w.ncy = (g.Cgo + 63) / 64;
+    w.TH = std::min(128 / w.Wp, g.Ho);
+    if (w.TH < 1) return false;
+    w.n_rowblk = (g.Ho + w.TH - 1) / w.TH;
+    // positions read: 128 of the tile plus the farthest tap, plus the packed-tap chunks beyond it
+    w.plane_elems = round_up(128 + tg.maxa * w.Wp + tg.maxb + 8, 8);
+    if (!build_wgrad_jobs(tg, taps, w.Wp, &w)) return false;
+    if (!size_wgrad(g, &w, &L->smem, &L->grid)) return false;
     // workspace: split-K slices, blocked x, blocked gradOutput
     L->part_bytes = align256((size_t)w.splits * g.Cout * g.Cgi * w.kHW * sizeof(float));
     L->xt_bytes = align256((size_t)g.N * g.G * w.ncx * w.Rx * w.Wp * 64 * 2);
@@ -1490,6 +1544,79 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
     L->ub_bytes = align256((size_t)g.N * g.G * c.nchu * c.R * c.Wp * 128);
     L->wpk_bytes = align256((size_t)g.G * c.n_vtile * c.nchu * ntaps * kWblkBytes);
     L->ws_bytes = L->ub_bytes + L->wpk_bytes;
+    return true;
+}
+
+// Stride 2: the input is blocked as its stride phases (one plane per phase) and every
+// phase runs the stride-1 weight-gradient kernel on its own taps, which are plain
+// shifts within its plane; the launches write disjoint taps of the same split-K
+// slices, and one reduction adds them.
+struct WgradPhaseLaunch {
+    int nphase = 0;
+    WgradParams wp[kMaxPlanes];
+    size_t smem[kMaxPlanes] = {};
+    int grid[kMaxPlanes] = {};
+    PhaseBlockifyParams bx;
+    BlockifyParams by;
+    size_t part_bytes = 0, xt_bytes = 0, xplane_elems = 0, yt_bytes = 0, ws_bytes = 0;
+};
+
+bool build_wgrad_phases(const Geom &g, WgradPhaseLaunch *L)
+{
+    if (g.s != 2 || g.Cgi < 8 || g.Cgo < 16) return false;
+    const std::vector<Tap> taps = forward_taps(g);
+    if ((int)taps.size() > kMaxTaps) return false;
+    TapGeometry tg;
+    if (!tap_geometry(taps, g.s, &tg)) return false;
+    WgradParams c{};
+    c.N = g.N; c.G = g.G; c.Cgi = g.Cgi; c.Cgo = g.Cgo; c.kHW = g.kH * g.kW;
+    c.Ho = g.Ho;
+    c.Wp = g.Wo + tg.maxb;            // plane pitch: output columns plus the farthest column shift
+    c.Rx = g.Ho + tg.maxa;
+    c.ncx = (g.Cgi + 63) / 64;
+    c.ncy = (g.Cgo + 63) / 64;
+    c.TH = std::min(128 / c.Wp, g.Ho);
+    if (c.TH < 1) return false;
+    c.n_rowblk = (g.Ho + c.TH - 1) / c.TH;
+    c.plane_elems = round_up(128 + tg.maxa * c.Wp + tg.maxb + 8, 8);
+    int max_splits = 1;
+    L->nphase = tg.nplanes;
+    for (int pl = 0; pl < tg.nplanes; ++pl) {
+        TapGeometry sub;
+        sub.nplanes = 1;
+        sub.maxa = tg.maxa;
+        sub.maxb = tg.maxb;
+        std::vector<Tap> st;
+        for (size_t i = 0; i < taps.size(); ++i)
+            if (tg.tap_plane[i] == pl) {
+                sub.tap_plane.push_back(0);
+                sub.tap_a.push_back(tg.tap_a[i]);
+                sub.tap_b.push_back(tg.tap_b[i]);
+                st.push_back(taps[i]);
+            }
+        WgradParams &w = L->wp[pl];
+        w = c;
+        if (!build_wgrad_jobs(sub, st, w.Wp, &w)) return false;
+        if (!size_wgrad(g, &w, &L->smem[pl], &L->grid[pl])) return false;
+        max_splits = std::max(max_splits, w.splits);
+    }
+    L->part_bytes = align256((size_t)max_splits * g.Cout * g.Cgi * c.kHW * sizeof(float));
+    L->xplane_elems = (size_t)g.N * g.G * c.ncx * c.Rx * c.Wp * 64;
+    L->xt_bytes = align256((size_t)tg.nplanes * L->xplane_elems * 2);
+    L->yt_bytes = align256((size_t)g.N * g.G * c.ncy * g.Ho * c.Wp * 64 * 2);
+    L->ws_bytes = L->part_bytes + L->xt_bytes + L->yt_bytes;
+    PhaseBlockifyParams &bx = L->bx;
+    bx = PhaseBlockifyParams{};
+    bx.N = g.N; bx.G = g.G; bx.Cg = g.Cgi; bx.nchunk = c.ncx; bx.IH = g.H; bx.IW = g.W;
+    bx.R = c.Rx; bx.C = c.Wp; bx.s = g.s; bx.nplane = tg.nplanes;
+    for (int pl = 0; pl < tg.nplanes; ++pl) {
+        bx.roff[pl] = tg.row0 * g.s + tg.plane_ph[pl];
+        bx.coff[pl] = tg.col0 * g.s + tg.plane_pw[pl];
+    }
+    BlockifyParams &by = L->by;
+    by = BlockifyParams{};
+    by.N = g.N; by.G = g.G; by.Cg = g.Cgo; by.nchunk = c.ncy; by.IH = g.Ho; by.IW = g.Wo;
+    by.R = g.Ho; by.C = c.Wp; by.r_off = 0; by.c_off = 0;
     return true;
 }
 
@@ -1608,6 +1735,14 @@ bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p)
         p->ws_bytes = ws;
         return true;
     }
+    if (pass == GCONV_PASS_BWD_WEIGHT && g.s == 2) {
+        WgradPhaseLaunch L;
+        if (!build_wgrad_phases(g, &L)) return false;
+        p->path = GCONV_PATH_TC_IGEMM;
+        p->launches = 3 + L.nphase;   // two blocked copies, a weight-gradient kernel per phase, the reduction
+        p->ws_bytes = L.ws_bytes;
+        return true;
+    }
     if (pass == GCONV_PASS_BWD_WEIGHT) {
         WgradLaunch L;
         if (!build_wgrad(g, &L)) return false;
@@ -1644,6 +1779,43 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
                 if (st != GCONV_OK) return st;
                 off += (L.wpk_bytes + 255) / 256 * 256;
             }
+        return GCONV_OK;
+    }
+    if (pass == GCONV_PASS_BWD_WEIGHT && g.s == 2) {
+        WgradPhaseLaunch L;
+        if (!build_wgrad_phases(g, &L)) return GCONV_ERR_UNSUPPORTED;
+        unsigned int *err = device_error_word();
+        if (!err) return GCONV_ERR_CUDA;
+        __nv_bfloat16 *xt = reinterpret_cast<__nv_bfloat16 *>(wsb + L.part_bytes);
+        __nv_bfloat16 *yt = reinterpret_cast<__nv_bfloat16 *>(wsb + L.part_bytes + L.xt_bytes);
+        L.bx.in = static_cast<const __nv_bfloat16 *>(a);
+        L.bx.out = xt;
+        const int64_t total = (int64_t)L.bx.nplane * L.bx.N * L.bx.G * L.bx.nchunk * L.bx.R * L.bx.C;
+        blockify_phase_kernel<<<(unsigned)((total + kBlockifyThreads - 1) / kBlockifyThreads), kBlockifyThreads, 0, s>>>(L.bx);
+        L.by.in = static_cast<const __nv_bfloat16 *>(b);
+        L.by.out = yt;
+        launch_blockify(L.by, s);
+        if (!smem_attr_once((const void *)wgrad_kernel, 1)) return GCONV_ERR_CUDA;
+        ReduceParams rp{};
+        for (int pl = 0; pl < L.nphase; ++pl) {
+            WgradParams &w = L.wp[pl];
+            w.XT = xt + (size_t)pl * L.xplane_elems;
+            w.DYT = yt;
+            w.part = reinterpret_cast<float *>(wsb);
+            w.err = err;
+            w.wait_ns = (uint64_t)wait_limit();
+            w.trace = nullptr;
+            wgrad_kernel<<<L.grid[pl], kTcThreads, L.smem[pl], s>>>(w);
+            for (int gi = 0; gi < w.n_tgrp; ++gi)
+                for (int jb = w.grp_first[gi]; jb < w.grp_first[gi + 1]; ++jb)
+                    for (int c = 0; c < w.job_count[jb]; ++c) rp.tap_splits[w.job_tapk[jb][c]] = w.grp_splits[gi];
+        }
+        rp.part = reinterpret_cast<float *>(wsb);
+        rp.dw = out;
+        rp.O = g.Cout; rp.Cgi = g.Cgi; rp.kHW = g.kH * g.kW;
+        const int64_t count = (int64_t)g.Cout * g.Cgi * g.kH * g.kW;
+        const int blocks = (int)std::min<int64_t>((count + 255) / 256, (int64_t)kNumSMs * 8);
+        wgrad_reduce_kernel<<<blocks, 256, 0, s>>>(rp);
         return GCONV_OK;
     }
     if (pass == GCONV_PASS_BWD_WEIGHT) {

@@ -25,7 +25,7 @@ TOL = {"bf16": 1e-2, "f32": 1e-4}
 
 CASES = [
     ("alexnet_g2", wl.WORKLOADS["alexnet_g2"].geom, "bf16"),                  # tcgen05 path, ~106 MiB scratch
-    ("dense3x3_s2_asym", wl.WORKLOADS["dense3x3_s2_asym"].geom, "bf16"),      # CUDA-core split path
+    ("dense3x3_s2_asym", wl.WORKLOADS["dense3x3_s2_asym"].geom, "bf16"),      # stride 2: phase planes
     ("f32_split", (16, 16, 20, 20, 16, 3, 3, 1, 1, 1, 1, 1, 1, 1), "f32"),     # fp32 inputs, split-K
 ]
 
