@@ -4,6 +4,8 @@
 #include "../../include/gconv.h"
 #include "common.cuh"
 
+#include <cuda.h>
+
 namespace gconv {
 
 constexpr int kNumSMs = 152;                       // GB300: 2 dies x 76 SMs
@@ -37,6 +39,10 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &p, gconv_pass pass, cons
 bool tiled_plan(const Geom &g, gconv_pass pass, Plan *p);
 gconv_status tiled_launch(const Geom &g, const Plan &p, gconv_dtype dt, gconv_pass pass, const void *a,
                           const void *b, const void *bias, float *out, void *ws, cudaStream_t s);
+
+// Tensor map for TMA loads of 128-byte position rows (tc_gemm.cu); false when the
+// driver entry point is unavailable or the box is invalid.
+bool encode_rows_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t planes, uint32_t box_rows);
 
 // tcgen05 dense-GEMM family for input size == kernel size (tc_gemm.cu)
 bool tc_fc_plan(const Geom &g, gconv_pass pass, Plan *p);

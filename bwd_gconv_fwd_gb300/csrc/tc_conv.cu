@@ -486,7 +486,8 @@ constexpr int kMaxJobs = 32;
 // accumulator ready, end, tiles processed, staging threads' waits for a free buffer (ns).
 constexpr int kTraceWords = 8;
 constexpr int kMaxGroupJobs = 8;
-constexpr int kWgradMaxBufs = 3;   // jobs of one group share 512 TMEM columns, at least 64 each
+constexpr int kWgradMaxBufs = 3;
+constexpr int kWgradProducers = 4;   // TMA issuing threads of the weight-gradient kernel   // jobs of one group share 512 TMEM columns, at least 64 each
 
 struct WgradParams {
     const __nv_bfloat16 *XT;     // blocked x  [N][G][ncx][Rx][Wp][64] (padded grid, zero padding)
@@ -497,11 +498,15 @@ struct WgradParams {
     int N, G, Cgi, Cgo, kHW;
     int Ho, Wp, Rx, ncx, ncy;
     int TH, n_rowblk;            // output rows per tile (<= 128 positions), row blocks per image
-    int plane_elems;             // x positions staged per tile
+    int plane_elems;             // x positions read per tile
+    int xb, n_xbox, x_rows;      // x staging: TMA box rows, boxes per tile, rows reserved (n_xbox * xb)
     int n_otile, n_ctile;        // 128-channel gradOutput tiles, 64-channel input tiles
     int n_tgrp;                  // job groups (one TMEM allocation each)
     int splits;                  // partial slices in the workspace (the largest group split count)
     int nbuf;                    // staging buffers (2 or 3)
+    int tma;                     // 1: tiles arrive by TMA (tm_x, tm_dy); 0: by cp.async
+    alignas(64) CUtensorMap tm_x;   // blocked x  as [N*G*ncx][Rx*Wp][64], box {64, xb, 1}
+    alignas(64) CUtensorMap tm_dy;  // blocked dy as [N*G*ncy][Ho*Wp][64], box {64, TH*Wp, 1}
     int cta_per_cg;              // CTAs per (group, o tile, c tile): sum of the group split counts
     int grp_splits[kMaxJobs];    // split count of each job group
     int grp_cta0[kMaxJobs + 1];  // first CTA index of each job group within cta_per_cg
@@ -541,7 +546,7 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
     const int c_lim = min(64, p.Cgi - ct * 64);      // valid input channels of this tile
 
     const int dy_bytes = 2 * 128 * 128;              // two 64-channel chunks x 128 positions
-    const int buf_bytes = dy_bytes + p.plane_elems * 128;
+    const int buf_bytes = dy_bytes + p.x_rows * 128;
     unsigned long long *trace = p.trace ? p.trace + (size_t)blockIdx.x * kTraceWords : nullptr;
     if (trace && threadIdx.x == 0) {
         trace[0] = ptx::globaltimer();
@@ -552,11 +557,28 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int i = 0; i < kWgradMaxBufs; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&bar_full[i]), kStageThreads);
+            ptx::mbar_init(ptx::smem_u32(&bar_full[i]), p.tma ? kWgradProducers : kStageThreads);
             ptx::mbar_init(ptx::smem_u32(&bar_empty[i]), 1);
         }
         ptx::mbar_init(ptx::smem_u32(&bar_acc), 1);
         ptx::fence_mbar_init();
+        if (p.tma) {
+            ptx::prefetch_tmap(&p.tm_x);
+            ptx::prefetch_tmap(&p.tm_dy);
+        }
+    }
+    if (p.tma && warp < kStageWarps) {
+        // TMA fills dy rows [0, TH*Wp) of each present chunk; the rest of the 128-row
+        // K tile (and an absent second chunk) must read as zero: clear it once
+        const int th_pos = p.TH * p.Wp;
+        const int chunks = min(2, p.ncy - 2 * ot);
+        for (int b = 0; b < p.nbuf; ++b)
+            for (int h = 0; h < 2; ++h) {
+                const int r0 = h < chunks ? th_pos : 0;
+                uint4 *z = reinterpret_cast<uint4 *>(smem + b * buf_bytes + h * 16384 + r0 * 128);
+                for (int i = threadIdx.x; i < (128 - r0) * 8; i += kStageThreads) z[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        ptx::fence_proxy_async_smem();
     }
     if (warp == kWarpAux) {
         ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), tmem_cols);
@@ -567,7 +589,53 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
-    if (warp < kStageWarps) {
+    if (warp < kStageWarps && p.tma) {
+        // ---------------- staging by TMA: producer q (warp q, lane 0) issues copy q of each tile ----------------
+        // copies: 0, 1 = gradOutput chunks 2*ot, 2*ot + 1; 2.. = x boxes (several per producer
+        // when there are more than two); one issuing thread alone cannot feed the tensor core
+        if (warp < kWgradProducers && lane == 0) {
+            const int q = warp;
+            const int th_pos = p.TH * p.Wp;
+            const int chunks = min(2, p.ncy - 2 * ot);
+            const int ncopy = 2 + p.n_xbox;
+            int last_b = -1, last_ph = 0;
+            for (int it = tile0, k = 0, b = 0, ph = 0; it < tile1; ++it, ++k) {
+                if (k >= p.nbuf) {
+                    const uint32_t eb = ptx::smem_u32(&bar_empty[b]);
+                    if (!ptx::mbar_wait(eb, (uint32_t)(ph ^ 1), p.wait_ns)) {
+                        abort_flag = 1;
+                        raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
+                    }
+                }
+                if (abort_flag) break;
+                const int rb = it / p.N, n = it - rb * p.N;
+                const int pos0 = rb * th_pos;
+                const uint32_t buf = ptx::smem_u32(smem + b * buf_bytes);
+                const uint32_t fb = ptx::smem_u32(&bar_full[b]);
+                uint32_t bytes = 0;
+                for (int c = q; c < ncopy; c += kWgradProducers)
+                    bytes += c < 2 ? (c < chunks ? (uint32_t)th_pos * 128u : 0u) : (uint32_t)p.xb * 128u;
+                ptx::mbar_arrive_expect_tx(fb, bytes);
+                for (int c = q; c < ncopy; c += kWgradProducers) {
+                    if (c < 2) {
+                        if (c < chunks)
+                            ptx::tma_load_3d(buf + (uint32_t)(c * 16384), &p.tm_dy, 0, pos0,
+                                             ((n * p.G + g) * p.ncy + 2 * ot + c), fb);
+                    } else {
+                        const int i = c - 2;
+                        ptx::tma_load_3d(buf + (uint32_t)(dy_bytes + i * p.xb * 128), &p.tm_x, 0, pos0 + i * p.xb,
+                                         ((n * p.G + g) * p.ncx + ct), fb);
+                    }
+                }
+                last_b = b;
+                last_ph = ph;
+                if (++b == p.nbuf) { b = 0; ph ^= 1; }
+            }
+            // the last tile's copies must land before the CTA exits
+            if (last_b >= 0 && !ptx::mbar_wait(ptx::smem_u32(&bar_full[last_b]), (uint32_t)last_ph, kDrainNs))
+                raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
+        }
+    } else if (warp < kStageWarps) {
         // ---------------- staging: cp.async of position rows, double buffered ----------------
         const int plane_y = p.Ho * p.Wp, plane_x = p.Rx * p.Wp;
         const int th_pos = p.TH * p.Wp;
@@ -1401,7 +1469,10 @@ bool size_wgrad(const Geom &g, WgradParams *wp, size_t *smem, int *grid)
         if (w.job_off[jb] + (w.job_count[jb] - 1) * w.job_delta[jb] + 128 > w.plane_elems) return false;
     w.n_ctile = w.ncx;
     w.n_otile = (g.Cgo + 127) / 128;
-    const size_t buf = (size_t)2 * 128 * 128 + (size_t)w.plane_elems * 128;
+    w.n_xbox = (w.plane_elems + 255) / 256;
+    w.xb = round_up((w.plane_elems + w.n_xbox - 1) / w.n_xbox, 8);
+    w.x_rows = w.n_xbox * w.xb;
+    const size_t buf = (size_t)2 * 128 * 128 + (size_t)w.x_rows * 128;
     w.nbuf = 1024 + kWgradMaxBufs * buf <= kMaxSmem ? kWgradMaxBufs : 2;
     *smem = 1024 + w.nbuf * buf;
     if (*smem > kMaxSmem) return false;
@@ -1432,6 +1503,16 @@ bool size_wgrad(const Geom &g, WgradParams *wp, size_t *smem, int *grid)
     w.cta_per_cg = w.grp_cta0[w.n_tgrp];
     *grid = outer * w.cta_per_cg;
     return true;
+}
+
+// Tensor maps over the blocked copies for TMA staging; cp.async staging when they
+// cannot be encoded.
+void set_wgrad_tma(WgradParams *w)
+{
+    const uint64_t plane_x = (uint64_t)w->Rx * w->Wp, plane_y = (uint64_t)w->Ho * w->Wp;
+    w->tma = (encode_rows_tmap(&w->tm_x, w->XT, plane_x, (uint64_t)w->N * w->G * w->ncx, (uint32_t)w->xb) &&
+              encode_rows_tmap(&w->tm_dy, w->DYT, plane_y, (uint64_t)w->N * w->G * w->ncy, (uint32_t)(w->TH * w->Wp)))
+                 ? 1 : 0;
 }
 
 bool build_wgrad(const Geom &g, WgradLaunch *L)
@@ -1801,6 +1882,7 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
             WgradParams &w = L.wp[pl];
             w.XT = xt + (size_t)pl * L.xplane_elems;
             w.DYT = yt;
+            set_wgrad_tma(&w);
             w.part = reinterpret_cast<float *>(wsb);
             w.err = err;
             w.wait_ns = (uint64_t)wait_limit();
@@ -1833,6 +1915,7 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
         launch_blockify(L.by, s);
         L.wp.XT = xt;
         L.wp.DYT = yt;
+        set_wgrad_tma(&L.wp);
         L.wp.part = reinterpret_cast<float *>(wsb);
         L.wp.err = err;
         L.wp.wait_ns = (uint64_t)wait_limit();

@@ -241,6 +241,25 @@ bool make_tmap(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, u
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+// 3D bf16 tensor map over planes of 128-byte rows ([planes][rows][64]), box
+// {64, box_rows, 1}, 128-byte swizzle; rows past a plane's end read as zero.
+bool encode_rows_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t planes, uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn || box_rows == 0 || box_rows > 256) return false;
+    cuuint64_t dims[3] = {64, rows, planes};
+    cuuint64_t strides[2] = {128, rows * 128};
+    cuuint32_t box[3] = {64u, box_rows, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
 struct GemmShape {
     int M, N, K;
     int a_mn, b_mn;
