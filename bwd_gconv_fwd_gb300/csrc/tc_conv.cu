@@ -764,29 +764,45 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
         }
         ready = __all_sync(0xffffffffu, ready && !abort_flag);
         if (trace && threadIdx.x == 0) trace[4] = ptx::globaltimer();
+        // lane o of warp w holds row o = 32*(w%4) + lane of each packed tap (every other tap
+        // for the two warps of a lane group): its 64 columns go out as 16-byte stores
         const int o = lg * 32 + lane;
         const int og = g * p.Cgo + ot * 128 + o;
+        const bool vec = (p.Cgi & 3) == 0;            // rows of part start on 16-byte boundaries
         float *dst = p.part + (int64_t)split * ((int64_t)p.G * p.Cgo * p.Cgi * p.kHW);
         int pair = 0;
         for (int jb = job0; jb < job1; ++jb)
             for (int j = 0; j < p.job_count[jb]; ++j, ++pair) {
                 if ((pair & 1) != half) continue;
                 const int tapk = p.job_tapk[jb][j];
-                for (int c0 = 0; c0 < 64; c0 += 16) {
-                    uint32_t acc[16];
-                    if (has_work && ready) {
-                        ptx::tmem_ld16(tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)(p.job_col[jb] + j * 64 + c0), acc);
-                        ptx::tmem_ld_wait();
+                uint32_t acc[4][16];
+                if (has_work && ready) {
+                    #pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        ptx::tmem_ld16(tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)(p.job_col[jb] + j * 64 + cc * 16), acc[cc]);
+                    ptx::tmem_ld_wait();
+                } else {
+                    #pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        #pragma unroll
+                        for (int e = 0; e < 16; ++e) acc[cc][e] = 0u;
+                }
+                if (!ready || o >= o_lim) continue;
+                float *row = dst + ((int64_t)tapk * p.G * p.Cgo + og) * p.Cgi + ct * 64;
+                #pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int c0 = cc * 16;
+                    if (c0 >= c_lim) break;
+                    if (vec && c0 + 16 <= c_lim) {
+                        float4 *r4 = reinterpret_cast<float4 *>(row + c0);
+                        #pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            r4[q] = make_float4(__uint_as_float(acc[cc][4 * q]), __uint_as_float(acc[cc][4 * q + 1]),
+                                                __uint_as_float(acc[cc][4 * q + 2]), __uint_as_float(acc[cc][4 * q + 3]));
                     } else {
                         #pragma unroll
-                        for (int e = 0; e < 16; ++e) acc[e] = 0u;
-                    }
-                    if (o < o_lim && ready && c0 < c_lim) {
-                        // 16 consecutive input channels of one (tap, o): contiguous per thread
-                        float *row = dst + ((int64_t)tapk * p.G * p.Cgo + og) * p.Cgi + ct * 64 + c0;
-                        #pragma unroll
                         for (int e = 0; e < 16; ++e)
-                            if (c0 + e < c_lim) row[e] = __uint_as_float(acc[e]);
+                            if (c0 + e < c_lim) row[c0 + e] = __uint_as_float(acc[cc][e]);
                     }
                 }
             }
