@@ -381,8 +381,8 @@ corr_kernel(const __grid_constant__ CorrParams p)
 // the image and for channels past Cg.  One 128-byte row per (r, c): 64 channels of one
 // position, so a tile of consecutive positions is a contiguous run of rows.  Each thread
 // builds one position row: 64 two-byte loads (the lanes of a warp take consecutive
-// positions, so each load instruction reads a contiguous stretch of an image row),
-// packed into eight 16-byte stores.  No shared memory; HBM-bound.
+// positions, so each load instruction reads a contiguous stretch of an image row);
+// the rows are written four at a time through shared memory.  HBM-bound.
 struct BlockifyParams {
     const __nv_bfloat16 *in;
     __nv_bfloat16 *out;
@@ -391,34 +391,55 @@ struct BlockifyParams {
 
 constexpr int kBlockifyThreads = 256;
 
+// Writes the block's position rows (thread t holds row blockIdx.x*256 + t as 32 packed
+// words) with every store instruction covering four whole consecutive rows (512
+// contiguous bytes): the rows pass through shared memory, 16-byte pieces, row pitch
+// 144 bytes so neither the writes nor the reads collide on banks.
+__device__ __forceinline__ void store_rows_coalesced(const uint32_t (&w)[32], int64_t total, uint4 *out)
+{
+    __shared__ __align__(16) uint4 stage[kBlockifyThreads * 9];
+    uint4 *mine = stage + threadIdx.x * 9;
+    #pragma unroll
+    for (int k = 0; k < 8; ++k) mine[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    __syncwarp();
+    const int lane = threadIdx.x & 31, base = threadIdx.x & ~31;
+    #pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int row = base + 4 * k + (lane >> 3), piece = lane & 7;
+        const int64_t q = (int64_t)blockIdx.x * kBlockifyThreads + row;
+        if (q < total) out[q * 8 + piece] = stage[row * 9 + piece];
+    }
+}
+
 __global__ void __launch_bounds__(kBlockifyThreads)
 blockify_kernel(const __grid_constant__ BlockifyParams p)
 {
     const int plane_out = p.R * p.C;
     const int64_t total = (int64_t)p.N * p.G * p.nchunk * plane_out;
     const int64_t q = (int64_t)blockIdx.x * kBlockifyThreads + threadIdx.x;
-    if (q >= total) return;
-    const int64_t blk = q / plane_out;                 // (n*G + g)*nchunk + j
-    const int pos = (int)(q - blk * plane_out);
-    const int r = pos / p.C, c = pos - r * p.C;
-    const int j = (int)(blk % p.nchunk);
-    const int64_t ng = blk / p.nchunk;                 // n*G + g
-    const int row = r + p.r_off, col = c + p.c_off;
-    const bool inside = row >= 0 && row < p.IH && col >= 0 && col < p.IW;
-    const int cvalid = inside ? min(64, p.Cg - 64 * j) : 0;
-    const int64_t plane = (int64_t)p.IH * p.IW;
-    const unsigned short *src = reinterpret_cast<const unsigned short *>(p.in) + (ng * p.Cg + 64 * j) * plane +
-                                (inside ? (int64_t)row * p.IW + col : 0);
     uint32_t w[32];
     #pragma unroll
-    for (int h = 0; h < 32; ++h) {
-        const uint32_t lo = 2 * h < cvalid ? (uint32_t)__ldg(src + (2 * h) * plane) : 0u;
-        const uint32_t hi = 2 * h + 1 < cvalid ? (uint32_t)__ldg(src + (2 * h + 1) * plane) : 0u;
-        w[h] = lo | (hi << 16);
+    for (int h = 0; h < 32; ++h) w[h] = 0u;
+    if (q < total) {
+        const int64_t blk = q / plane_out;                 // (n*G + g)*nchunk + j
+        const int pos = (int)(q - blk * plane_out);
+        const int r = pos / p.C, c = pos - r * p.C;
+        const int j = (int)(blk % p.nchunk);
+        const int64_t ng = blk / p.nchunk;                 // n*G + g
+        const int row = r + p.r_off, col = c + p.c_off;
+        const bool inside = row >= 0 && row < p.IH && col >= 0 && col < p.IW;
+        const int cvalid = inside ? min(64, p.Cg - 64 * j) : 0;
+        const int64_t plane = (int64_t)p.IH * p.IW;
+        const unsigned short *src = reinterpret_cast<const unsigned short *>(p.in) + (ng * p.Cg + 64 * j) * plane +
+                                    (inside ? (int64_t)row * p.IW + col : 0);
+        #pragma unroll
+        for (int h = 0; h < 32; ++h) {
+            const uint32_t lo = 2 * h < cvalid ? (uint32_t)__ldg(src + (2 * h) * plane) : 0u;
+            const uint32_t hi = 2 * h + 1 < cvalid ? (uint32_t)__ldg(src + (2 * h + 1) * plane) : 0u;
+            w[h] = lo | (hi << 16);
+        }
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(p.out) + q * 8;
-    #pragma unroll
-    for (int k = 0; k < 8; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    store_rows_coalesced(w, total, reinterpret_cast<uint4 *>(p.out));
 }
 
 // Stride-2 form of the blocked copy for the weight gradient: out[p][n][g][j][r][c][0..63]
@@ -441,30 +462,31 @@ blockify_phase_kernel(const __grid_constant__ PhaseBlockifyParams p)
     const int64_t ngj = (int64_t)p.N * p.G * p.nchunk;
     const int64_t total = ngj * p.nplane * plane_out;
     const int64_t q = (int64_t)blockIdx.x * kBlockifyThreads + threadIdx.x;
-    if (q >= total) return;
-    const int64_t blk = q / plane_out;                 // (plane*N*G + n*G + g)*nchunk + j
-    const int pos = (int)(q - blk * plane_out);
-    const int r = pos / p.C, c = pos - r * p.C;
-    const int j = (int)(blk % p.nchunk);
-    const int64_t t = blk / p.nchunk;
-    const int64_t ng = t % ((int64_t)p.N * p.G);       // n*G + g
-    const int pl = (int)(t / ((int64_t)p.N * p.G));
-    const int row = r * p.s + p.roff[pl], col = c * p.s + p.coff[pl];
-    const bool inside = row >= 0 && row < p.IH && col >= 0 && col < p.IW;
-    const int cvalid = inside ? min(64, p.Cg - 64 * j) : 0;
-    const int64_t plane = (int64_t)p.IH * p.IW;
-    const unsigned short *src = reinterpret_cast<const unsigned short *>(p.in) + (ng * p.Cg + 64 * j) * plane +
-                                (inside ? (int64_t)row * p.IW + col : 0);
     uint32_t w[32];
     #pragma unroll
-    for (int h = 0; h < 32; ++h) {
-        const uint32_t lo = 2 * h < cvalid ? (uint32_t)__ldg(src + (2 * h) * plane) : 0u;
-        const uint32_t hi = 2 * h + 1 < cvalid ? (uint32_t)__ldg(src + (2 * h + 1) * plane) : 0u;
-        w[h] = lo | (hi << 16);
+    for (int h = 0; h < 32; ++h) w[h] = 0u;
+    if (q < total) {
+        const int64_t blk = q / plane_out;                 // (plane*N*G + n*G + g)*nchunk + j
+        const int pos = (int)(q - blk * plane_out);
+        const int r = pos / p.C, c = pos - r * p.C;
+        const int j = (int)(blk % p.nchunk);
+        const int64_t t = blk / p.nchunk;
+        const int64_t ng = t % ((int64_t)p.N * p.G);       // n*G + g
+        const int pl = (int)(t / ((int64_t)p.N * p.G));
+        const int row = r * p.s + p.roff[pl], col = c * p.s + p.coff[pl];
+        const bool inside = row >= 0 && row < p.IH && col >= 0 && col < p.IW;
+        const int cvalid = inside ? min(64, p.Cg - 64 * j) : 0;
+        const int64_t plane = (int64_t)p.IH * p.IW;
+        const unsigned short *src = reinterpret_cast<const unsigned short *>(p.in) + (ng * p.Cg + 64 * j) * plane +
+                                    (inside ? (int64_t)row * p.IW + col : 0);
+        #pragma unroll
+        for (int h = 0; h < 32; ++h) {
+            const uint32_t lo = 2 * h < cvalid ? (uint32_t)__ldg(src + (2 * h) * plane) : 0u;
+            const uint32_t hi = 2 * h + 1 < cvalid ? (uint32_t)__ldg(src + (2 * h + 1) * plane) : 0u;
+            w[h] = lo | (hi << 16);
+        }
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(p.out) + q * 8;
-    #pragma unroll
-    for (int k = 0; k < 8; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    store_rows_coalesced(w, total, reinterpret_cast<uint4 *>(p.out));
 }
 
 // ===========================================================================
