@@ -849,7 +849,12 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
 //       by cp.async into the 128-byte swizzle layout; tap t reads them tap_off[t]
 //       rows further on (a whole-row shift of the descriptor's start address).
 // Every MMA is M = 128, N = 256, K = 16; K steps past the last real channel of a
-// chunk are skipped.  The epilogue transposes 32 x 32 blocks through shared memory
+// chunk are skipped.  With at most 64 produced channels the tile's upper 64 rows would be
+// idle, so taps are paired: rows 64.. hold the weights of a second tap lying pair_delta
+// positions after the first in the same row of the kernel; both rows read the first
+// tap's shifted B, so the upper rows accumulate the second tap's contribution to the
+// output pair_delta positions earlier, and the epilogue adds lower row j and upper row
+// j + pair_delta (N = 240 then, tile_pos = 240 - pair_delta outputs per tile).  The epilogue transposes 32 x 32 blocks through shared memory
 // so that a warp stores 32 consecutive pixels of one output channel.
 struct Corr2Params {
     const __nv_bfloat16 *UB;    // blocked input [N][G][nchu][R][Wp][64]
@@ -859,11 +864,14 @@ struct Corr2Params {
     unsigned int *err;
     uint64_t wait_ns;
     int N, G, Cu, Cv, Qh, Qw, R, Wp, nchu;
-    int n_ptile, n_vtile, n_tiles;  // 256-position tiles per image, 128-channel tiles, all tiles
-    int stage_rows;             // positions staged per chunk (256 + farthest tap, multiple of 8)
+    int n_ptile, n_vtile, n_tiles;  // position tiles per image, 128-channel tiles, all tiles
+    int nmma;                   // MMA N: 256, or 240 with paired taps
+    int tile_pos;               // output positions per tile: nmma, or nmma - pair_delta with paired taps
+    int pair_delta;             // paired taps: the second tap's row shift past the first (0: unpaired)
+    int stage_rows;             // positions staged per chunk (nmma + farthest tap, multiple of 8)
     int nsb, wstages;           // staging buffers (1 or 2), weight ring depth (3 or 4)
-    int ntaps;
-    int tap_off[kMaxTaps];
+    int ntaps;                  // weight blocks per chunk (taps, or tap pairs)
+    int tap_off[kMaxTaps];      // row shift of each block's (first) tap
     unsigned long long *trace;  // optional per-CTA phase stamps (kTraceWords each), nullptr when off
 };
 
@@ -944,7 +952,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
         for (int t = blockIdx.x; t < p.n_tiles && !stop; t += gridDim.x) {
             int ptile, n, vt, g;
             corr2_tile(p, t, &ptile, &n, &vt, &g);
-            const int p0 = ptile * 256;
+            const int p0 = ptile * p.tile_pos;
             for (int kc = 0; kc < p.nchu; ++kc, ++seq) {
                 const int sb = seq % p.nsb;
                 bool bad = false;
@@ -1004,7 +1012,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
         // the low bits), the next tap's row shift is loaded one step ahead, ring slots and
         // phases advance incrementally, and timers are read only on a slow wait.
         if (lane == 0) {
-            const uint32_t idesc = ptx::idesc_bf16(128, 256, 0, 0);
+            const uint32_t idesc = ptx::idesc_bf16(128, p.nmma, 0, 0);
             const uint64_t adesc0 = ptx::smem_desc(ptx::smem_u32(ring), 16u, 1024u, 2);
             const uint64_t bdesc0 = ptx::smem_desc(ptx::smem_u32(smem), 16u, 1024u, 2);
             bool ok = true;
@@ -1095,13 +1103,51 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
             const uint64_t t0 = trace ? ptx::globaltimer() : 0;
             bool ready = ptx::mbar_wait(ptx::smem_u32(&bar_afull[acc]), (k / 2) & 1, p.wait_ns);
             if (trace) w_epi += ptx::globaltimer() - t0;
-            ready = __all_sync(0xffffffffu, ready);
-            if (!ready || abort_flag) {
+            ready = __all_sync(0xffffffffu, ready) && !abort_flag;
+            // paired warps must take the same decision: they meet on named barriers below
+            if (p.pair_delta) ready = !ptx::bar_red_or(2 + (lg & 1), 64, !ready);
+            if (!ready) {
                 if (lane == 0) { abort_flag = 1; raise_device_error(p.err, DEVERR_WAIT_TIMEOUT); }
                 break;
             }
             ptx::tc_fence_after();
-            const int p0 = ptile * 256;
+            const int p0 = ptile * p.tile_pos;
+            if (p.pair_delta) {
+                // lane groups 0, 1: first taps (rows v), 2, 3: second taps (rows 64 + v); the
+                // warps lg and lg + 2 hold the same channels and meet on named barrier 2 + (lg & 1)
+                const int part = lg & 1;
+                const bool upper = lg >= 2;
+                float *hb = epi + part * (32 * 17);                 // upper warp's columns
+                float *tbp = epi + (2 + part) * (32 * 17);          // lower warp's sums
+                const int v0 = part * 32;
+                const int vcount = min(32, p.Cv - v0);
+                float *vout = p.V + ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv + v0) * out_hw;
+                const float bias_lane = (p.bias && !upper && lane < vcount) ? __bfloat162float(p.bias[g * p.Cv + v0 + lane]) : 0.f;
+                for (int pc = 0; pc < p.tile_pos; pc += 16) {
+                    uint32_t a[16];
+                    const uint32_t col = (uint32_t)(acc * 256 + pc + (upper ? p.pair_delta : 0));
+                    ptx::tmem_ld16(tmem + ((uint32_t)(lg * 32) << 16) + col, a);
+                    ptx::tmem_ld_wait();
+                    if (upper) {
+                        #pragma unroll
+                        for (int j = 0; j < 16; ++j) hb[lane * 17 + j] = __uint_as_float(a[j]);
+                    }
+                    ptx::named_sync(2 + part, 64);
+                    if (!upper) {
+                        #pragma unroll
+                        for (int j = 0; j < 16; ++j) tbp[lane * 17 + j] = __uint_as_float(a[j]) + hb[lane * 17 + j] + bias_lane;
+                        __syncwarp();
+                        const int jc = pc + (lane & 15);
+                        const int pos = p0 + jc;
+                        const int qh = pos / p.Wp, qw = pos - qh * p.Wp;
+                        if (jc < p.tile_pos && qh < p.Qh && qw < p.Qw) {
+                            float *o = vout + (int64_t)qh * p.Qw + qw;
+                            for (int vv = lane >> 4; vv < vcount; vv += 2) o[vv * out_hw] = tbp[vv * 17 + (lane & 15)];
+                        }
+                    }
+                    ptx::named_sync(2 + part, 64);   // the upper warp may overwrite hb
+                }
+            } else {
             const int v0 = vt * 128 + lg * 32;
             const int vcount = min(32, p.Cv - v0);
             float *vout = p.V + ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv + v0) * out_hw;
@@ -1128,6 +1174,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                     __syncwarp();
                 }
             }
+            }
             // this warp's TMEM reads are done: the accumulator may be overwritten
             ptx::tc_fence_before();
             __syncwarp();
@@ -1141,7 +1188,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
     if (warp == kC2WarpMma) ptx::tmem_dealloc(tmem, 512);
 }
 
-// Packs weights for corr2_kernel: block (g, vt, kc, tap) = [128 rows v][64 u] in the
+// Packs weights for corr2_kernel: block (g, vt, kc, t) = [128 rows v][64 u] in the
 // 128-byte swizzle layout (16-byte piece k of row r at ((k ^ (r & 7)) * 16)).
 //   forward:       v = output channel, u = input channel:  w[g*Cv + v][u][tap]
 //   backward-data: v = input channel,  u = output channel: w[g*Cu + u][v][tap]
@@ -1151,6 +1198,8 @@ struct Pack2Params {
     int G, Cu, Cv, n_vtile, nchu, ntaps;
     int transpose;          // 0 forward, 1 backward-data
     int w_cin_g, kHW;
+    int pair;               // 1: rows 0..63 from tap tk1, rows 64..127 from tap tk2 (Cv <= 64)
+    int tk1[kMaxTaps], tk2[kMaxTaps];   // weight tap index (kh*kW + kw) of each block; tk2 -1: none
 };
 
 __global__ void pack2_kernel(const __grid_constant__ Pack2Params p)
@@ -1164,15 +1213,16 @@ __global__ void pack2_kernel(const __grid_constant__ Pack2Params p)
         const int kc = (int)(b % p.nchu); b /= p.nchu;
         const int vt = (int)(b % p.n_vtile);
         const int g = (int)(b / p.n_vtile);
-        const int v = vt * 128 + r;
+        const int tap = (p.pair && r >= 64) ? p.tk2[tp] : p.tk1[tp];
+        const int v = vt * 128 + (p.pair ? (r & 63) : r);
         uint32_t wv[4] = {0u, 0u, 0u, 0u};
-        if (v < p.Cv) {
+        if (tap >= 0 && v < p.Cv) {
             #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const int u = kc * 64 + k * 8 + q;
                 if (u < p.Cu) {
-                    const int64_t idx = p.transpose ? ((int64_t)(g * p.Cu + u) * p.w_cin_g + v) * p.kHW + tp
-                                                    : ((int64_t)(g * p.Cv + v) * p.w_cin_g + u) * p.kHW + tp;
+                    const int64_t idx = p.transpose ? ((int64_t)(g * p.Cu + u) * p.w_cin_g + v) * p.kHW + tap
+                                                    : ((int64_t)(g * p.Cv + v) * p.w_cin_g + u) * p.kHW + tap;
                     wv[q >> 1] |= (uint32_t)__bfloat16_as_ushort(p.w[idx]) << ((q & 1) * 16);
                 }
             }
@@ -1621,19 +1671,38 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
     c.nchu = (Cu + 63) / 64;
     c.n_vtile = (Cv + 127) / 128;
     c.ntaps = ntaps;
-    int maxoff = 0;
-    for (int kh = 0; kh < g.kH; ++kh)
-        for (int kw = 0; kw < g.kW; ++kw) {
-            const int a = bwd_data ? (g.kH - 1 - kh) * g.d : kh * g.d;
-            const int b = bwd_data ? (g.kW - 1 - kw) * g.d : kw * g.d;
-            c.tap_off[kh * g.kW + kw] = a * c.Wp + b;
-            maxoff = std::max(maxoff, a * c.Wp + b);
+    // Weight blocks: one per tap, or, with at most 64 produced channels, one per pair of taps
+    // that are neighbours (d positions apart) in a row of the kernel -- when the MMA work per
+    // tile outweighs the heavier paired epilogue (measured: a 5x5 kernel over two chunks
+    // gains, a 3x3 kernel over one chunk loses).
+    const bool pair = Cv <= 64 && g.kW >= 2 && g.d <= 16 && c.nchu * ntaps >= 16;
+    Pack2Params &k = L->pk;
+    k = Pack2Params{};
+    int nblk = 0, maxoff = 0;
+    for (int kh = 0; kh < g.kH; ++kh) {
+        const int a = bwd_data ? (g.kH - 1 - kh) * g.d : kh * g.d;
+        // the row's taps in increasing offset b
+        std::vector<std::pair<int, int>> row;   // (b, weight tap index)
+        for (int kw = 0; kw < g.kW; ++kw) row.push_back({bwd_data ? (g.kW - 1 - kw) * g.d : kw * g.d, kh * g.kW + kw});
+        std::sort(row.begin(), row.end());
+        for (size_t i = 0; i < row.size(); ++nblk) {
+            const bool two = pair && i + 1 < row.size() && row[i + 1].first == row[i].first + g.d;
+            c.tap_off[nblk] = a * c.Wp + row[i].first;
+            k.tk1[nblk] = row[i].second;
+            k.tk2[nblk] = two ? row[i + 1].second : -1;
+            maxoff = std::max(maxoff, c.tap_off[nblk]);
+            i += two ? 2 : 1;
         }
+    }
+    c.ntaps = nblk;
+    c.pair_delta = pair ? g.d : 0;
+    c.nmma = pair ? 240 : 256;
+    c.tile_pos = c.nmma - c.pair_delta;
     const int positions = Qh * c.Wp;   // padded output grid rows that hold real outputs
     c.Cu = Cu;
-    c.n_ptile = (positions + 255) / 256;
+    c.n_ptile = (positions + c.tile_pos - 1) / c.tile_pos;
     c.n_tiles = g.N * g.G * c.n_vtile * c.n_ptile;
-    c.stage_rows = round_up(256 + maxoff, 8);
+    c.stage_rows = round_up(c.nmma + maxoff, 8);
     const size_t stage = (size_t)c.stage_rows * 128;
     // Two staging buffers and four weight slots when they fit; never below 120 KB, so
     // that one CTA holds its SM (it takes all 512 TMEM columns).
@@ -1648,11 +1717,10 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
     if (!fit) return false;
     L->smem = std::max(L->smem, (size_t)120 * 1024);
     L->grid = std::min(c.n_tiles, kNumSMs);
-    Pack2Params &k = L->pk;
-    k = Pack2Params{};
-    k.G = g.G; k.Cu = Cu; k.Cv = Cv; k.n_vtile = c.n_vtile; k.nchu = c.nchu; k.ntaps = ntaps;
+    k.G = g.G; k.Cu = Cu; k.Cv = Cv; k.n_vtile = c.n_vtile; k.nchu = c.nchu; k.ntaps = c.ntaps;
     k.transpose = bwd_data ? 1 : 0;
     k.w_cin_g = g.Cgi; k.kHW = ntaps;
+    k.pair = pair ? 1 : 0;
     BlockifyParams &bu = L->bu;
     bu = BlockifyParams{};
     bu.N = g.N; bu.G = g.G; bu.Cg = Cu; bu.nchunk = c.nchu;
@@ -1661,7 +1729,7 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
     bu.r_off = bwd_data ? g.pt - maxa : -g.pt;
     bu.c_off = bwd_data ? g.pl - maxb : -g.pl;
     L->ub_bytes = align256((size_t)g.N * g.G * c.nchu * c.R * c.Wp * 128);
-    L->wpk_bytes = align256((size_t)g.G * c.n_vtile * c.nchu * ntaps * kWblkBytes);
+    L->wpk_bytes = align256((size_t)g.G * c.n_vtile * c.nchu * c.ntaps * kWblkBytes);
     L->ws_bytes = L->ub_bytes + L->wpk_bytes;
     return true;
 }
