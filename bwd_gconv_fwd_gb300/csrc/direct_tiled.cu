@@ -32,30 +32,74 @@ struct TileGeom {
 __host__ __device__ __forceinline__ int floordiv_i(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 
 // Stages rows [r0, r0 + RI) x columns [c0, c0 + CI) of `nch` planes (zero outside the
-// H x W image) as fp32 rows of pitch CIp: a warp per row, lanes along the row.  Plain
-// nested loops (no integer division per element, which would cost more than the data
-// movement itself for thin groups).
+// H x W image) as fp32 rows of pitch CIp.  A warp takes four rows at a time, lanes along
+// them, and issues all their loads before storing any (a load-store-load chain would
+// leave one DRAM latency per element in flight per warp).
 template <typename T>
 __device__ __forceinline__ void stage_rows(const T *__restrict__ src, int64_t plane, int H, int W, int r0, int c0,
                                            int nch, int RI, int CI, int CIp, float *__restrict__ dst)
 {
-    constexpr int kWarps = kTT / 32;
+    constexpr int kWarps = kTT / 32, kRows = 4, kCols = 4;   // up to 4 x 128 columns per batch
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int c = 0; c < nch; ++c) {
-        const T *sc = src + c * plane;
-        float *dc = dst + c * RI * CIp;
-        #pragma unroll 2
-        for (int r = warp; r < RI; r += kWarps) {
-            const int ih = r0 + r;
-            const bool row_ok = ih >= 0 && ih < H;
-            const T *sr = sc + (int64_t)ih * W;
-            float *dr = dc + r * CIp;
-            #pragma unroll 2
-            for (int col = lane; col < CI; col += 32) {
-                const int iw = c0 + col;
-                dr[col] = (row_ok && iw >= 0 && iw < W) ? to_f(__ldg(sr + iw)) : 0.f;
+    const int nrows = nch * RI;
+    for (int c0w = 0; c0w < CI; c0w += 32 * kCols)
+        for (int base = warp * kRows; base < nrows; base += kWarps * kRows) {
+            float v[kRows][kCols];
+            #pragma unroll
+            for (int i = 0; i < kRows; ++i) {
+                const int row = base + i;
+                const int c = row / RI, r = row - c * RI;
+                const int ih = r0 + r;
+                const bool row_ok = row < nrows && ih >= 0 && ih < H;
+                const T *sr = src + c * plane + (int64_t)ih * W;
+                #pragma unroll
+                for (int k = 0; k < kCols; ++k) {
+                    const int col = c0w + k * 32 + lane, iw = c0 + col;
+                    v[i][k] = (row_ok && col < CI && iw >= 0 && iw < W) ? to_f(__ldg(sr + iw)) : 0.f;
+                }
             }
+            #pragma unroll
+            for (int i = 0; i < kRows; ++i)
+                #pragma unroll
+                for (int k = 0; k < kCols; ++k) {
+                    const int row = base + i, col = c0w + k * 32 + lane;
+                    if (row < nrows && col < CI) dst[row * CIp + col] = v[i][k];
+                }
         }
+}
+
+// Vector form of the staging, for rows whose length is a multiple of the 16-byte vector
+// (W % V == 0, V = 16 / sizeof(T)): smem column j holds image column ca + j, where ca is
+// the first needed column cs rounded down to V; rows carry CIa = CIp columns (a multiple
+// of V covering [cs, cs + CI)).  Vectors inside the image are one 16-byte load each,
+// vectors across its edge go element by element; values are widened to fp32 and stored
+// as 16-byte pieces.
+template <typename T>
+__device__ __forceinline__ void stage_rows_vec(const T *__restrict__ src, int64_t plane, int H, int W, int r0, int ca,
+                                               int nch, int RI, int CIp, float *__restrict__ dst)
+{
+    constexpr int V = 16 / (int)sizeof(T);
+    const int nv = CIp / V;                    // vectors per staged row
+    const int total = nch * RI * nv;
+    for (int it = threadIdx.x; it < total; it += kTT) {
+        const int row = it / nv, vi = it - row * nv;
+        const int c = row / RI, r = row - c * RI;
+        const int ih = r0 + r, iw = ca + vi * V;
+        float f[V];
+        if (ih >= 0 && ih < H && iw >= 0 && iw + V <= W) {
+            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(src + c * plane + (int64_t)ih * W + iw));
+            const T *e = reinterpret_cast<const T *>(&raw);
+            #pragma unroll
+            for (int q = 0; q < V; ++q) f[q] = to_f(e[q]);
+        } else {
+            const bool row_ok = ih >= 0 && ih < H;
+            #pragma unroll
+            for (int q = 0; q < V; ++q)
+                f[q] = (row_ok && iw + q >= 0 && iw + q < W) ? to_f(__ldg(src + c * plane + (int64_t)ih * W + iw + q)) : 0.f;
+        }
+        float4 *d = reinterpret_cast<float4 *>(dst + row * CIp + vi * V);
+        #pragma unroll
+        for (int q = 0; q < V / 4; ++q) d[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
     }
 }
 
@@ -348,6 +392,234 @@ bwd_data_tiled_kernel(Geom g, TileGeom t, const T *__restrict__ dy, const T *__r
 }
 
 // ---------------------------------------------------------------------------
+// 3 x 3, stride 1, dilation 1, thin groups: register-blocked.  out[o][r][c] = sum over the
+// group's input planes i and taps (a, b) of W[i][a][b][o] * src[i][r + r_off + a][c + c_off + b]
+// (zero outside src).  Forward: src = x, r_off = -pt; backward-data: src = gradOutput,
+// r_off = pt - 2, W the mirrored, transposed weights.  A block takes an (image, group,
+// TH x TW output tile) tile -- four-channel groups walk tiles persistently, single
+// channels take one tile per block to keep more blocks resident -- and each thread
+// produces a 4 x 4 block of positions for all CO output channels, loading each input
+// value of its 6 x 6 window once per input plane.  Rows of src whose length is a
+// multiple of the 16-byte vector are staged as vectors (smem column j = image column
+// ca + j, ca the first needed column rounded down to the vector), so the integer work
+// stays off the per-element path.
+struct Conv3Params {
+    const void *src;
+    const void *w;
+    const void *bias;      // forward only, or nullptr
+    float *out;
+    int N, G, nin, nout, IH, IW, OH, OW;   // per-group in/out channels, src and out extents
+    int in_ctot, out_ctot;                 // channel counts of the whole tensors
+    int r_off, c_off;
+    int TH, TW, n_th, n_tw, tq, CIp;       // tile, tiles, thread columns (TW / BX), staged row pitch
+    int bwd;                               // 1: weights mirrored and transposed (backward-data)
+    int w_cin_g;                           // C_in/G of the weight tensor
+};
+
+template <typename T, int CO, int BX>
+__global__ void __launch_bounds__(kTT)
+conv3_s1_kernel(const __grid_constant__ Conv3Params p)
+{
+    extern __shared__ __align__(16) float sm3[];
+    constexpr int V = 16 / (int)sizeof(T);
+    const int RI = p.TH + 2, CI = p.TW + 2, CIp = p.CIp;
+    const bool vec_rows = (p.IW % V) == 0;
+    float *ws = sm3;                                  // [nin][9][CO]
+    float *xs = sm3 + ((p.nin * 9 * CO + 3) & ~3);   // [nin][RI][CIp], 16-byte aligned
+    const T *W = static_cast<const T *>(p.w);
+    const T *B = static_cast<const T *>(p.bias);
+    const int64_t plane = (int64_t)p.IH * p.IW, out_plane = (int64_t)p.OH * p.OW;
+    const int ntiles = p.N * p.G * p.n_th * p.n_tw;
+    // per-thread constants: compute block, staging slot
+    const int tx = threadIdx.x % p.tq, ty = threadIdx.x / p.tq;
+    const int rb = 4 * ty, cb = BX * tx;
+    const int nv = CIp / V;                               // staged vectors per row
+    const int rows_pass = kTT / nv;                       // rows staged per pass of the block
+    const int svi = threadIdx.x % nv, srow0 = threadIdx.x / nv;
+    const int nrows = p.nin * RI;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        int b = tile;
+        const int tw = b % p.n_tw; b /= p.n_tw;
+        const int th = b % p.n_th; b /= p.n_th;
+        const int grp = b % p.G;
+        const int n = b / p.G;
+        const int r0 = th * p.TH, c0 = tw * p.TW;
+        for (int i = threadIdx.x; i < p.nin * 9 * CO; i += kTT) {
+            const int ci = i / (9 * CO), rem = i - ci * 9 * CO, tap = rem / CO, o = rem - tap * CO;
+            float v = 0.f;
+            if (o < p.nout) {
+                // forward: w[g*nout + o][ci][tap]; backward-data: w[g*nin + ci][o][8 - tap]
+                const int64_t idx = p.bwd ? ((int64_t)(grp * p.nin + ci) * p.w_cin_g + o) * 9 + (8 - tap)
+                                          : ((int64_t)(grp * p.nout + o) * p.w_cin_g + ci) * 9 + tap;
+                v = to_f(W[idx]);
+            }
+            ws[i] = v;
+        }
+        const T *srcg = static_cast<const T *>(p.src) + ((int64_t)n * p.in_ctot + (int64_t)grp * p.nin) * plane;
+        const int cs = c0 + p.c_off;
+        int coff = 0;
+        if (vec_rows) {
+            const int ca = cs >= 0 ? cs / V * V : -((-cs + V - 1) / V) * V;
+            coff = cs - ca;
+            const int iw = ca + svi * V;
+            if (srow0 < rows_pass) {
+                int c = srow0 / RI, r = srow0 - c * RI;
+                const int dc = rows_pass / RI, dr = rows_pass - dc * RI;
+                for (int row = srow0; row < nrows; row += rows_pass) {
+                    const int ih = r0 + p.r_off + r;
+                    float f[V];
+                    const T *sr = srcg + c * plane + (int64_t)ih * p.IW;
+                    if (ih >= 0 && ih < p.IH && iw >= 0 && iw + V <= p.IW) {
+                        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(sr + iw));
+                        const T *e = reinterpret_cast<const T *>(&raw);
+                        #pragma unroll
+                        for (int q = 0; q < V; ++q) f[q] = to_f(e[q]);
+                    } else {
+                        const bool row_ok = ih >= 0 && ih < p.IH;
+                        #pragma unroll
+                        for (int q = 0; q < V; ++q)
+                            f[q] = (row_ok && iw + q >= 0 && iw + q < p.IW) ? to_f(__ldg(sr + iw + q)) : 0.f;
+                    }
+                    float4 *d = reinterpret_cast<float4 *>(xs + row * CIp + svi * V);
+                    #pragma unroll
+                    for (int q = 0; q < V / 4; ++q) d[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+                    c += dc;
+                    r += dr;
+                    if (r >= RI) { r -= RI; ++c; }
+                }
+            }
+        } else {
+            stage_rows(srcg, plane, p.IH, p.IW, r0 + p.r_off, cs, p.nin, RI, CI, CIp, xs);
+        }
+        __syncthreads();
+        if (rb < p.TH && r0 + rb < p.OH && c0 + cb < p.OW) {
+            float acc[4][BX][CO];
+            #pragma unroll
+            for (int i = 0; i < 4; ++i)
+                #pragma unroll
+                for (int j = 0; j < BX; ++j)
+                    #pragma unroll
+                    for (int o = 0; o < CO; ++o) acc[i][j][o] = 0.f;
+            for (int ci = 0; ci < p.nin; ++ci) {
+                const float *xw = xs + (ci * RI + rb) * CIp + cb + coff;
+                const float *wc = ws + ci * 9 * CO;
+                float win[6][BX + 2];
+                #pragma unroll
+                for (int i = 0; i < 6; ++i)
+                    #pragma unroll
+                    for (int j = 0; j < BX + 2; ++j) win[i][j] = xw[i * CIp + j];
+                #pragma unroll
+                for (int a = 0; a < 3; ++a)
+                    #pragma unroll
+                    for (int bb = 0; bb < 3; ++bb) {
+                        float wv[CO];
+                        #pragma unroll
+                        for (int o = 0; o < CO; ++o) wv[o] = wc[(a * 3 + bb) * CO + o];
+                        #pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            #pragma unroll
+                            for (int j = 0; j < BX; ++j)
+                                #pragma unroll
+                                for (int o = 0; o < CO; ++o) acc[i][j][o] = fmaf(wv[o], win[i + a][j + bb], acc[i][j][o]);
+                    }
+            }
+            float *og = p.out + ((int64_t)n * p.out_ctot + (int64_t)grp * p.nout) * out_plane;
+            const bool vec = (p.OW & 3) == 0 && c0 + cb + BX <= p.OW;
+            #pragma unroll
+            for (int o = 0; o < CO; ++o) {
+                if (o >= p.nout) break;
+                const float bv = B ? to_f(B[grp * p.nout + o]) : 0.f;
+                #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = r0 + rb + i;
+                    if (rb + i >= p.TH || r >= p.OH) break;
+                    float *row = og + o * out_plane + (int64_t)r * p.OW + c0 + cb;
+                    if (vec) {
+                        #pragma unroll
+                        for (int j = 0; j < BX; j += 4)
+                            *reinterpret_cast<float4 *>(row + j) = make_float4(acc[i][j][o] + bv, acc[i][j + 1][o] + bv,
+                                                                               acc[i][j + 2][o] + bv, acc[i][j + 3][o] + bv);
+                    } else {
+                        #pragma unroll
+                        for (int j = 0; j < BX; ++j)
+                            if (c0 + cb + j < p.OW) row[j] = acc[i][j][o] + bv;
+                    }
+                }
+            }
+        }
+        __syncthreads();   // the staged tile is no longer read
+    }
+}
+
+int conv3_slots(int nout) { return nout <= 1 ? 1 : (nout <= 2 ? 2 : 4); }
+int conv3_bx(int) { return 4; }
+
+// Tile for conv3_s1_kernel: TW = the output width rounded up to BX (at most 128), TH = 4 x the
+// thread rows, shrunk until the staged planes fit 96 KB.
+bool plan_conv3(const Geom &g, bool bwd, Conv3Params *p, size_t *smem)
+{
+    if (g.kH != 3 || g.kW != 3 || g.s != 1 || g.d != 1) return false;
+    const int nin = bwd ? g.Cgo : g.Cgi, nout = bwd ? g.Cgi : g.Cgo;
+    if (nout > 4 || nin > 16) return false;
+    const int CO = conv3_slots(nout), BX = conv3_bx(nout);
+    *p = Conv3Params{};
+    p->N = g.N; p->G = g.G; p->nin = nin; p->nout = nout;
+    p->IH = bwd ? g.Ho : g.H; p->IW = bwd ? g.Wo : g.W;
+    p->OH = bwd ? g.H : g.Ho; p->OW = bwd ? g.W : g.Wo;
+    p->in_ctot = bwd ? g.Cout : g.Cin; p->out_ctot = bwd ? g.Cin : g.Cout;
+    p->r_off = bwd ? g.pt - 2 : -g.pt;
+    p->c_off = bwd ? g.pl - 2 : -g.pl;
+    p->bwd = bwd ? 1 : 0;
+    p->w_cin_g = g.Cgi;
+    p->TW = std::min(128, (p->OW + BX - 1) / BX * BX);
+    p->tq = p->TW / BX;
+    // staged row pitch: a multiple of 8 floats covering TW + 2 columns after a shift of up to 7
+    p->CIp = (p->TW + 2 + 7 + 7) / 8 * 8;
+    int rows_q = std::max(1, kTT / p->tq);
+    rows_q = std::min(rows_q, (p->OH + 3) / 4);
+    for (;; rows_q = (rows_q + 1) / 2) {
+        p->TH = 4 * rows_q;
+        *smem = (size_t)(((nin * 9 * CO + 3) & ~3) + nin * (p->TH + 2) * p->CIp) * 4;
+        if (*smem <= 96 * 1024) break;
+        if (rows_q == 1) return false;
+    }
+    if (p->CIp / 4 > kTT) return false;   // one staging thread per vector of a row
+    p->n_th = (p->OH + p->TH - 1) / p->TH;
+    p->n_tw = (p->OW + p->TW - 1) / p->TW;
+    return true;
+}
+
+template <typename T, int CO, int BX>
+bool launch_conv3_t(const Conv3Params &p, size_t smem, cudaStream_t s)
+{
+    static bool attr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    if (!attr[dev]) {
+        if (cudaFuncSetAttribute((const void *)conv3_s1_kernel<T, CO, BX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 96 * 1024) != cudaSuccess)
+            return false;
+        attr[dev] = true;
+    }
+    // one tile per block keeps more blocks resident for the light single-channel form;
+    // the four-channel form walks tiles persistently
+    const int64_t ntiles = (int64_t)p.N * p.G * p.n_th * p.n_tw;
+    const unsigned grid = (unsigned)(CO >= 4 ? std::min<int64_t>(ntiles, (int64_t)kNumSMs * 8) : ntiles);
+    conv3_s1_kernel<T, CO, BX><<<grid, kTT, smem, s>>>(p);
+    return true;
+}
+
+template <typename T>
+bool launch_conv3(const Conv3Params &p, size_t smem, cudaStream_t s)
+{
+    switch (conv3_slots(p.nout)) {
+    case 1: return launch_conv3_t<T, 1, 4>(p, smem, s);
+    case 2: return launch_conv3_t<T, 2, 4>(p, smem, s);
+    default: return launch_conv3_t<T, 4, 4>(p, smem, s);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Backward-weight partial sums.  Block (image chunk, row tile, column tile, group):
 // thread (pair q, lane l) owns output channel o = q / Cgi, input channel c = q % Cgi,
 // and the tile positions l, l + L, ...; it keeps KK accumulators (one per tap) over
@@ -539,6 +811,17 @@ gconv_status launch_typed(const Geom &g, const Plan &, gconv_pass pass, const vo
     TileGeom t{};
     size_t smem = 0;
     const T *A = static_cast<const T *>(a), *B = static_cast<const T *>(b);
+    if (pass == GCONV_PASS_FWD || pass == GCONV_PASS_BWD_DATA) {
+        Conv3Params c3;
+        size_t sm3 = 0;
+        if (plan_conv3(g, pass == GCONV_PASS_BWD_DATA, &c3, &sm3)) {
+            c3.src = a;
+            c3.w = b;
+            c3.bias = pass == GCONV_PASS_FWD ? bias : nullptr;
+            c3.out = out;
+            return launch_conv3<T>(c3, sm3, s) ? GCONV_OK : GCONV_ERR_CUDA;
+        }
+    }
     if (pass == GCONV_PASS_FWD) {
         if (!plan_fwd(g, &t, &smem)) return GCONV_ERR_UNSUPPORTED;
         const int grid = (int)std::min<int64_t>((int64_t)g.N * g.G * t.n_th * t.n_tw, (int64_t)kNumSMs * 8);
@@ -599,6 +882,12 @@ bool tiled_plan(const Geom &g, gconv_pass pass, Plan *p)
 {
     TileGeom t{};
     size_t smem = 0;
+    Conv3Params c3;
+    if ((pass == GCONV_PASS_FWD || pass == GCONV_PASS_BWD_DATA) && plan_conv3(g, pass == GCONV_PASS_BWD_DATA, &c3, &smem)) {
+        p->launches = 1;
+        p->ws_bytes = 0;
+        return true;
+    }
     if (pass == GCONV_PASS_FWD && plan_fwd(g, &t, &smem)) {
         p->launches = 1;
         p->ws_bytes = 0;
