@@ -694,6 +694,123 @@ bwd_weight_tiled_kernel(Geom g, TileGeom t, const T *__restrict__ x, const T *__
     }
 }
 
+// 3 x 3, stride 1, dilation 1 weight gradient, register-blocked: block (image chunk, row
+// tile, column tile, group) as above; thread (pair q, lane l) takes 4 x 4 blocks of output
+// positions of its tile (l, l + L, ...) and, per image, adds the 16 gradOutput values of
+// channel o times the 6 x 6 input window of channel c into its 9 tap accumulators (about 3
+// shared-memory loads and 9 FMA per position).  Rows are staged as 16-byte vectors when
+// their length allows.  Partial sums go to part[block][q*9 + tap] like the general kernel.
+template <typename T>
+__global__ void __launch_bounds__(kTT)
+wgrad3_s1_kernel(Geom g, TileGeom t, int CIpx, int CIpy, const T *__restrict__ x, const T *__restrict__ dy,
+                 float *__restrict__ part)
+{
+    extern __shared__ __align__(16) float sm[];
+    constexpr int V = 16 / (int)sizeof(T);
+    const int RI = t.TH + 2;
+    float *xs = sm;                                        // [Cgi][RI][CIpx]
+    float *ds = sm + g.Cgi * RI * CIpx;                    // [Cgo][TH][CIpy]
+    int b = blockIdx.x;
+    const int nb = b % t.n_nb; b /= t.n_nb;
+    const int tw = b % t.n_tw; b /= t.n_tw;
+    const int th = b % t.n_th; b /= t.n_th;
+    const int grp = b;
+    const int r0 = th * t.TH, c0 = tw * t.TW;
+    const int q = threadIdx.x / t.L, l = threadIdx.x - q * t.L;
+    const bool active = q < t.P;
+    const int o = active ? q / g.Cgi : 0, c = active ? q - o * g.Cgi : 0;
+    const bool xvec = (g.W % V) == 0, yvec = (g.Wo % V) == 0;
+    const int csx = c0 - g.pl;
+    const int cax = xvec ? (csx >= 0 ? csx / V * V : -((-csx + V - 1) / V) * V) : csx;
+    const int cay = yvec ? c0 / V * V : c0;
+    const int coffx = csx - cax, coffy = c0 - cay;
+    const int nbc = t.TW / 4, nblk = (t.TH / 4) * nbc;
+    float acc[9];
+    #pragma unroll
+    for (int k = 0; k < 9; ++k) acc[k] = 0.f;
+    const int64_t in_plane = (int64_t)g.H * g.W, out_plane = (int64_t)g.Ho * g.Wo;
+    const int n1 = min(g.N, (nb + 1) * t.NB);
+    for (int n = nb * t.NB; n < n1; ++n) {
+        const T *xg = x + ((int64_t)n * g.Cin + (int64_t)grp * g.Cgi) * in_plane;
+        const T *dg = dy + ((int64_t)n * g.Cout + (int64_t)grp * g.Cgo) * out_plane;
+        __syncthreads();   // the previous image's tiles are no longer read
+        if (xvec) stage_rows_vec(xg, in_plane, g.H, g.W, r0 - g.pt, cax, g.Cgi, RI, CIpx, xs);
+        else stage_rows(xg, in_plane, g.H, g.W, r0 - g.pt, cax, g.Cgi, RI, t.TW + 2, CIpx, xs);
+        if (yvec) stage_rows_vec(dg, out_plane, g.Ho, g.Wo, r0, cay, g.Cgo, t.TH, CIpy, ds);
+        else stage_rows(dg, out_plane, g.Ho, g.Wo, r0, cay, g.Cgo, t.TH, t.TW, CIpy, ds);
+        __syncthreads();
+        if (active) {
+            const float *xsp = xs + c * RI * CIpx + coffx;
+            const float *dsp = ds + o * t.TH * CIpy + coffy;
+            for (int blk = l; blk < nblk; blk += t.L) {
+                const int br = blk / nbc, bc = blk - br * nbc;
+                const int rr = 4 * br, cc = 4 * bc;
+                if (r0 + rr >= g.Ho || c0 + cc >= g.Wo) continue;
+                float d[4][4], w6[6][6];
+                #pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    #pragma unroll
+                    for (int j = 0; j < 4; ++j) d[i][j] = dsp[(rr + i) * CIpy + cc + j];
+                #pragma unroll
+                for (int i = 0; i < 6; ++i)
+                    #pragma unroll
+                    for (int j = 0; j < 6; ++j) w6[i][j] = xsp[(rr + i) * CIpx + cc + j];
+                #pragma unroll
+                for (int a = 0; a < 3; ++a)
+                    #pragma unroll
+                    for (int bb = 0; bb < 3; ++bb)
+                        #pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            #pragma unroll
+                            for (int j = 0; j < 4; ++j) acc[a * 3 + bb] = fmaf(d[i][j], w6[i + a][j + bb], acc[a * 3 + bb]);
+            }
+        }
+    }
+    // add the L lanes of each pair in lane order (reusing the staged tiles' memory)
+    __syncthreads();
+    float *red = sm;   // [P*9][L]
+    if (active) {
+        #pragma unroll
+        for (int k = 0; k < 9; ++k) red[(q * 9 + k) * t.L + l] = acc[k];
+    }
+    __syncthreads();
+    float *dst = part + (int64_t)blockIdx.x * t.P * 9;
+    for (int i = threadIdx.x; i < t.P * 9; i += kTT) {
+        float sum = 0.f;
+        for (int j = 0; j < t.L; ++j) sum += red[i * t.L + j];
+        dst[i] = sum;
+    }
+}
+
+// Tile for wgrad3_s1_kernel (3 x 3, stride 1, dilation 1, (C_in/G)*(C_out/G) <= 256).
+bool plan_wgrad3(const Geom &g, TileGeom *t, size_t *smem, int *CIpx, int *CIpy)
+{
+    if (g.kH != 3 || g.kW != 3 || g.s != 1 || g.d != 1) return false;
+    const int P = g.Cgi * g.Cgo;
+    if (P > kTT) return false;
+    *t = TileGeom{};
+    t->P = P;
+    t->L = kTT / P;
+    t->TW = std::min(128, (g.Wo + 3) / 4 * 4);
+    *CIpx = (t->TW + 2 + 7 + 7) / 8 * 8;
+    *CIpy = (t->TW + 7 + 7) / 8 * 8;
+    for (int TH = std::min(64, (g.Ho + 3) / 4 * 4);; TH = std::max(4, TH / 2 / 4 * 4)) {
+        t->TH = TH;
+        const int64_t floats = std::max<int64_t>((int64_t)g.Cgi * (TH + 2) * *CIpx + (int64_t)g.Cgo * TH * *CIpy,
+                                                 (int64_t)P * 9 * t->L);
+        *smem = (size_t)floats * 4;
+        if (*smem <= 96 * 1024) break;
+        if (TH == 4) return false;
+    }
+    t->n_th = (g.Ho + t->TH - 1) / t->TH;
+    t->n_tw = (g.Wo + t->TW - 1) / t->TW;
+    const int64_t spatial = (int64_t)g.G * t->n_th * t->n_tw;
+    const int n_nb = (int)std::max<int64_t>(1, std::min<int64_t>(g.N, (4 * (int64_t)kNumSMs * 4 + spatial - 1) / spatial));
+    t->NB = (g.N + n_nb - 1) / n_nb;
+    t->n_nb = (g.N + t->NB - 1) / t->NB;
+    return true;
+}
+
 // dw[(g*Cgo + o)][c][tap] = sum over the group's blocks of part[block][q*KK + tap], block
 // order, one warp per weight element (lanes over blocks, then a fixed shuffle tree).
 __global__ void __launch_bounds__(kTT)
@@ -858,6 +975,25 @@ gconv_status launch_typed(const Geom &g, const Plan &, gconv_pass pass, const vo
         return GCONV_OK;
     }
     if (pass == GCONV_PASS_BWD_WEIGHT) {
+        int cx = 0, cy = 0;
+        if (plan_wgrad3(g, &t, &smem, &cx, &cy)) {
+            static bool attr[64] = {};
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GCONV_ERR_CUDA;
+            if (!attr[dev]) {
+                if (cudaFuncSetAttribute((const void *)wgrad3_s1_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         96 * 1024) != cudaSuccess)
+                    return GCONV_ERR_CUDA;
+                attr[dev] = true;
+            }
+            const int nbg = t.n_th * t.n_tw * t.n_nb;
+            float *part = static_cast<float *>(ws);
+            wgrad3_s1_kernel<T><<<g.G * nbg, kTT, smem, s>>>(g, t, cx, cy, A, B, part);
+            const int64_t elems = (int64_t)g.G * t.P * 9;
+            weight_finish_kernel<<<(unsigned)((elems + kTT / 32 - 1) / (kTT / 32)), kTT, 0, s>>>(
+                part, g.G, nbg, t.P, 9, g.Cgi, out);
+            return GCONV_OK;
+        }
         if (!plan_bwd_weight(g, &t, &smem)) return GCONV_ERR_UNSUPPORTED;
         const int nbg = t.n_th * t.n_tw * t.n_nb;
         const int grid = g.G * nbg;
@@ -896,6 +1032,12 @@ bool tiled_plan(const Geom &g, gconv_pass pass, Plan *p)
     if (pass == GCONV_PASS_BWD_DATA && plan_bwd_data(g, &t, &smem)) {
         p->launches = 1;
         p->ws_bytes = 0;
+        return true;
+    }
+    int cx = 0, cy = 0;
+    if (pass == GCONV_PASS_BWD_WEIGHT && plan_wgrad3(g, &t, &smem, &cx, &cy)) {
+        p->launches = 2;
+        p->ws_bytes = (size_t)g.G * t.n_th * t.n_tw * t.n_nb * t.P * 9 * sizeof(float);
         return true;
     }
     if (pass == GCONV_PASS_BWD_WEIGHT && plan_bwd_weight(g, &t, &smem)) {
