@@ -7,7 +7,7 @@
 //     backward-wt    dW = dY^T X          (A = dY MN-major, B = X  MN-major)
 // so every pass is one GEMM on the tensors as they lie, no transposes.
 //
-// Kernel: persistent CTAs over 128 x BN output tiles; warp 0 issues TMA tile
+// Kernel: persistent CTAs over 128 x BN output tiles; warps 0, 6 and 7 issue TMA tile
 // loads (128-byte swizzle) into a shared-memory ring, warp 1 issues tcgen05.mma
 // into one of two TMEM accumulators, warps 2-5 drain the other accumulator
 // (TMEM -> registers -> fp32 global, + bias) while the next tile accumulates.
@@ -22,7 +22,8 @@ namespace gconv {
 
 namespace {
 
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 256;   // warps 0, 6, 7: TMA producers; 1: MMA; 2-5: epilogue
+constexpr int kGemmProducers = 3;
 constexpr int kBM = 128, kBK = 64;
 constexpr uint64_t kGemmDrainNs = 1000000000ull;
 
@@ -56,7 +57,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int i = 0; i < p.stages; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&bar_full[i]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bar_full[i]), kGemmProducers);
             ptx::mbar_init(ptx::smem_u32(&bar_empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -77,9 +78,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
+    if (warp == 0 || warp >= 6) {
+        // ---------------- TMA producers ----------------
+        // a stage is 1-2 A boxes and 1-4 B boxes; producer pi issues boxes pi, pi + 3, ...
+        // (one thread's copy stream alone is capped well below what the MMAs consume)
         if (lane == 0) {
+            const int pi = warp == 0 ? 0 : warp - 5;
+            const int nA = p.a_mn ? 2 : 1, nB = p.b_mn ? BN / 64 : 1;
+            const uint32_t bytesA = p.a_mn ? 8192u : 16384u, bytesB = p.b_mn ? 8192u : (uint32_t)BN * 128u;
+            uint32_t my_bytes = 0;
+            for (int i = pi; i < nA + nB; i += kGemmProducers) my_bytes += i < nA ? bytesA : bytesB;
             int it = 0;   // global k-block counter across tiles
             for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x) {
                 const int mb = tile % p.n_mblk, nb = tile / p.n_mblk;
@@ -93,21 +101,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     }
                     const uint32_t fb = ptx::smem_u32(&bar_full[slot]);
                     const uint32_t sa = sbase + slot * stage_bytes, sb = sa + a_bytes;
-                    ptx::mbar_arrive_expect_tx(fb, stage_bytes);
-                    // A tile: 128 rows of M x 64 of K
-                    if (p.a_mn) {
-                        ptx::tma_load_2d(sa, &tmA, mb * kBM, kb * kBK, fb);
-                        ptx::tma_load_2d(sa + 8192, &tmA, mb * kBM + 64, kb * kBK, fb);
-                    } else {
-                        ptx::tma_load_2d(sa, &tmA, kb * kBK, mb * kBM, fb);
-                    }
-                    // B tile: BN rows of N x 64 of K
-                    if (p.b_mn) {
-                        #pragma unroll
-                        for (int c = 0; c < BN / 64; ++c)
-                            ptx::tma_load_2d(sb + c * 8192, &tmB, nb * BN + c * 64, kb * kBK, fb);
-                    } else {
-                        ptx::tma_load_2d(sb, &tmB, kb * kBK, nb * BN, fb);
+                    ptx::mbar_arrive_expect_tx(fb, my_bytes);
+                    for (int i = pi; i < nA + nB; i += kGemmProducers) {
+                        if (i < nA) {   // A tile: 128 rows of M x 64 of K
+                            if (p.a_mn) ptx::tma_load_2d(sa + i * 8192, &tmA, mb * kBM + i * 64, kb * kBK, fb);
+                            else ptx::tma_load_2d(sa, &tmA, kb * kBK, mb * kBM, fb);
+                        } else {        // B tile: BN rows of N x 64 of K
+                            const int c = i - nA;
+                            if (p.b_mn) ptx::tma_load_2d(sb + c * 8192, &tmB, nb * BN + c * 64, kb * kBK, fb);
+                            else ptx::tma_load_2d(sb, &tmB, kb * kBK, nb * BN, fb);
+                        }
                     }
                 }
             }
@@ -120,8 +123,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
+            // lean issue loop: descriptors are a base plus an address offset (address >> 4 in
+            // the low bits), ring slots and phases advance incrementally, the fast path of a
+            // wait is one try_wait (the tensor core runs only a couple of MMAs ahead)
             const uint32_t idesc = ptx::idesc_bf16(kBM, BN, p.a_mn, p.b_mn);
-            int it = 0, local = 0;
+            const uint64_t a0 = p.a_mn ? ptx::smem_desc(sbase, 8192, 1024, 2) : ptx::smem_desc(sbase, 16, 1024, 2);
+            const uint64_t b0 = p.b_mn ? ptx::smem_desc(sbase + a_bytes, 8192, 1024, 2)
+                                       : ptx::smem_desc(sbase + a_bytes, 16, 1024, 2);
+            const uint64_t ak = p.a_mn ? 2048 >> 4 : 32 >> 4, bk = p.b_mn ? 2048 >> 4 : 32 >> 4;
+            int local = 0, slot = 0;
+            uint32_t phase = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++local) {
                 const int buf = local & 1;
@@ -132,23 +143,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 }
                 ptx::tc_fence_after();
                 const uint32_t dt = tmem + (uint32_t)(buf * BN);
-                for (int kb = 0; kb < p.n_kblk; ++kb, ++it) {
-                    const int slot = it % p.stages;
-                    if (!ptx::mbar_wait(ptx::smem_u32(&bar_full[slot]), (it / p.stages) & 1, p.wait_ns)) {
+                for (int kb = 0; kb < p.n_kblk; ++kb) {
+                    const uint32_t fb = ptx::smem_u32(&bar_full[slot]);
+                    if (!ptx::mbar_try_wait(fb, phase) && !ptx::mbar_wait(fb, phase, p.wait_ns)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t sa = sbase + slot * stage_bytes, sb = sa + a_bytes;
+                    const uint64_t so = (uint64_t)((slot * stage_bytes) >> 4);
+                    const uint64_t ad = a0 + so, bd = b0 + so;
                     #pragma unroll
-                    for (int k = 0; k < kBK / 16; ++k) {
-                        const uint64_t ad = p.a_mn ? ptx::smem_desc(sa + k * 2048, 8192, 1024, 2)
-                                                   : ptx::smem_desc(sa + k * 32, 16, 1024, 2);
-                        const uint64_t bd = p.b_mn ? ptx::smem_desc(sb + k * 2048, 8192, 1024, 2)
-                                                   : ptx::smem_desc(sb + k * 32, 16, 1024, 2);
-                        ptx::mma_f16(dt, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-                    }
+                    for (int k = 0; k < kBK / 16; ++k)
+                        ptx::mma_f16(dt, ad + k * ak, bd + k * bk, idesc, (kb > 0 || k > 0) ? 1u : 0u);
                     ptx::mma_commit(ptx::smem_u32(&bar_empty[slot]));
+                    if (++slot == p.stages) { slot = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
                 ptx::mma_commit(ptx::smem_u32(&bar_acc_full[buf]));
