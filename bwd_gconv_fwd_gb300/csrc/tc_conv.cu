@@ -896,6 +896,45 @@ __device__ __forceinline__ void corr2_tile(const Corr2Params &p, int t, int *pti
     *g = t / p.n_vtile;
 }
 
+// Issues one staged chunk's MMAs: for every weight block, wait for its ring slot, then
+// NKS K steps of 16 channels against the chunk's rows shifted by the block's tap offset,
+// then release the slot.  NKS is a template argument so that no branch sits between the
+// MMAs: with branches around them the issuing thread fell behind the tensor core
+// (measured about 190 cycles per 128 x 256 x 16 MMA against 128 without).  Returns false
+// when a slot wait runs out of time.
+template <int NKS>
+__device__ __forceinline__ bool corr2_issue_taps(uint32_t d, uint64_t adesc0, uint64_t bdesc_c, uint32_t idesc,
+                                                 uint32_t acc_first, const int *tap_off, int ntaps, int wstages,
+                                                 uint32_t wfull0, uint32_t wempty0, int &slot, uint32_t &wphase,
+                                                 uint64_t wait_ns, uint64_t &w_weight)
+{
+    int off_next = tap_off[0];
+    uint32_t acc = acc_first;
+    for (int tp = 0; tp < ntaps; ++tp) {
+        const int off = off_next;
+        off_next = tap_off[tp + 1];
+        const uint32_t wbar = wfull0 + (uint32_t)(slot * 8);
+        if (!ptx::mbar_try_wait(wbar, wphase)) {
+            const uint64_t t0 = ptx::globaltimer();
+            if (!ptx::mbar_wait(wbar, wphase, wait_ns)) return false;
+            w_weight += ptx::globaltimer() - t0;
+        }
+        ptx::tc_fence_after();
+        const uint64_t ad = adesc0 + (uint64_t)(slot * (kWblkBytes >> 4));
+        const uint64_t bd = bdesc_c + (uint64_t)(off * 8);     // off rows of 128 bytes
+        ptx::mma_f16(d, ad, bd, idesc, acc);
+        if (NKS > 1) ptx::mma_f16(d, ad + 2, bd + 2, idesc, 1u);   // +32 bytes: next 16 channels
+        if (NKS > 2) ptx::mma_f16(d, ad + 4, bd + 4, idesc, 1u);
+        if (NKS > 3) ptx::mma_f16(d, ad + 6, bd + 6, idesc, 1u);
+        ptx::mma_commit(wempty0 + (uint32_t)(slot * 8));
+        acc = 1u;
+        const int nxt = slot + 1;
+        slot = nxt == wstages ? 0 : nxt;
+        wphase ^= nxt == wstages ? 1u : 0u;
+    }
+    return true;
+}
+
 __global__ void __launch_bounds__(kC2Threads, 1)
 corr2_kernel(const __grid_constant__ Corr2Params p)
 {
@@ -904,12 +943,12 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
         bar_wempty[kC2MaxWStages], bar_afull[2], bar_aempty[2], bar_drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
-    __shared__ int tap_off_sh[kMaxTaps];
+    __shared__ int tap_off_sh[kMaxTaps + 1];   // one spare entry: the issue loop reads one tap ahead
 
     uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int stage_bytes = p.stage_rows * 128;
-    if (threadIdx.x < p.ntaps) tap_off_sh[threadIdx.x] = p.tap_off[threadIdx.x];
+    if (threadIdx.x <= p.ntaps) tap_off_sh[threadIdx.x] = threadIdx.x < p.ntaps ? p.tap_off[threadIdx.x] : 0;
     uint8_t *ring = smem + p.nsb * stage_bytes;
     float *epi = reinterpret_cast<float *>(ring + p.wstages * kWblkBytes);
     const int nblocks = p.nchu * p.ntaps;
@@ -1047,26 +1086,13 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                     ptx::tc_fence_after();
                     const uint64_t bdesc_c = bdesc0 + (uint64_t)((sb * stage_bytes) >> 4);
                     const int nks = min(4, (p.Cu - 64 * kc + 15) >> 4);
-                    int off_next = tap_off_sh[0];
-                    for (int tp = 0; tp < p.ntaps; ++tp) {
-                        const int off = off_next;
-                        off_next = tap_off_sh[tp + 1 < p.ntaps ? tp + 1 : 0];
-                        const uint32_t wbar = ptx::smem_u32(&bar_wfull[slot]);
-                        if (!ptx::mbar_try_wait(wbar, wphase)) {
-                            const uint64_t t0 = ptx::globaltimer();
-                            if (!ptx::mbar_wait(wbar, wphase, p.wait_ns)) { ok = false; break; }
-                            w_weight += ptx::globaltimer() - t0;
-                        }
-                        ptx::tc_fence_after();
-                        const uint64_t ad = adesc0 + (uint64_t)(slot * (kWblkBytes >> 4));
-                        const uint64_t bd = bdesc_c + (uint64_t)(off * 8);     // off rows of 128 bytes
-                        const uint32_t acc0 = (kc > 0 || tp > 0) ? 1u : 0u;
-                        ptx::mma_f16(d, ad, bd, idesc, acc0);
-                        if (nks > 1) ptx::mma_f16(d, ad + 2, bd + 2, idesc, 1u);   // +32 bytes: next 16 channels
-                        if (nks > 2) ptx::mma_f16(d, ad + 4, bd + 4, idesc, 1u);
-                        if (nks > 3) ptx::mma_f16(d, ad + 6, bd + 6, idesc, 1u);
-                        ptx::mma_commit(ptx::smem_u32(&bar_wempty[slot]));
-                        if (++slot == p.wstages) { slot = 0; wphase ^= 1u; }
+                    const uint32_t acc_first = kc > 0 ? 1u : 0u;
+                    const uint32_t wf0 = ptx::smem_u32(&bar_wfull[0]), we0 = ptx::smem_u32(&bar_wempty[0]);
+                    switch (nks) {
+                    case 4: ok = corr2_issue_taps<4>(d, adesc0, bdesc_c, idesc, acc_first, tap_off_sh, p.ntaps, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                    case 3: ok = corr2_issue_taps<3>(d, adesc0, bdesc_c, idesc, acc_first, tap_off_sh, p.ntaps, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                    case 2: ok = corr2_issue_taps<2>(d, adesc0, bdesc_c, idesc, acc_first, tap_off_sh, p.ntaps, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                    default: ok = corr2_issue_taps<1>(d, adesc0, bdesc_c, idesc, acc_first, tap_off_sh, p.ntaps, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
                     }
                     if (!ok) break;
                     ptx::mma_commit(ptx::smem_u32(&bar_sempty[sb]));
