@@ -17,6 +17,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <algorithm>
+#include <cstdint>
 
 namespace gconv {
 
@@ -37,6 +38,10 @@ struct GemmParams {
     int n_mblk, n_nblk, n_kblk;
     int stages;
 };
+
+// TMEM columns for two BN-wide accumulators (allocations are powers of two)
+template <int BN>
+constexpr uint32_t kTmemCols = 2 * BN <= 256 ? 256u : 512u;
 
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -70,7 +75,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         ptx::prefetch_tmap(&tmB);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), 2 * BN);
+        ptx::tmem_alloc(ptx::smem_u32(&tmem_base_sh), kTmemCols<BN>);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
@@ -215,7 +220,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 1) ptx::tmem_dealloc(tmem, 2 * BN);
+    if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols<BN>);
 }
 
 // ---- host side ----------------------------------------------------------------
@@ -284,18 +289,20 @@ GemmShape fc_shape(const Geom &g, gconv_pass pass)
     }
 }
 
-// Picks the N tile: fewest rounds of persistent CTAs, 256-wide preferred on ties
-// (it halves the shared-memory traffic per MMA).
+// Picks the N tile.  The kernel is bound by how fast an SM fills its shared memory
+// (about 80 GB/s per CTA measured, well below what the MMAs consume), so the cost of a
+// choice is the bytes the busiest SM loads: rounds of persistent tiles times the tile's
+// (128 + BN) rows per K step.
 int pick_bn(int M, int N)
 {
     const int mb = (M + kBM - 1) / kBM;
-    double best = 1e30;
+    int64_t best = INT64_MAX;
     int bn = 256;
-    for (int cand : {256, 128}) {
-        const int tiles = mb * ((N + cand - 1) / cand);
-        const int rounds = (tiles + kNumSMs - 1) / kNumSMs;
-        const double cost = rounds * cand * (cand == 128 ? 1.15 : 1.0);
-        if (cost < best - 1e-9) { best = cost; bn = cand; }
+    for (int cand : {256, 192, 128}) {
+        const int64_t tiles = (int64_t)mb * ((N + cand - 1) / cand);
+        const int64_t rounds = (tiles + kNumSMs - 1) / kNumSMs;
+        const int64_t cost = rounds * (kBM + cand);
+        if (cost < best) { best = cost; bn = cand; }
     }
     return bn;
 }
@@ -360,22 +367,20 @@ gconv_status tc_fc_launch(const Geom &g, const Plan &, gconv_pass pass, const vo
     const size_t smem = gp.stages * stage + 1024;
     const int tiles = gp.n_mblk * gp.n_nblk;
     const int grid = std::min(tiles, kNumSMs);
-    static bool attr[64][2] = {};
+    static bool attr[64][3] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GCONV_ERR_CUDA;
-    if (sh.BN == 256) {
-        if (!attr[dev][0] && cudaFuncSetAttribute(gemm_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  220 * 1024) != cudaSuccess)
+    const int ai = sh.BN == 256 ? 0 : sh.BN == 192 ? 1 : 2;
+    const void *fn = sh.BN == 256 ? (const void *)gemm_kernel<256>
+                   : sh.BN == 192 ? (const void *)gemm_kernel<192> : (const void *)gemm_kernel<128>;
+    if (!attr[dev][ai]) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024) != cudaSuccess)
             return GCONV_ERR_CUDA;
-        attr[dev][0] = true;
-        gemm_kernel<256><<<grid, kGemmThreads, smem, s>>>(tA, tB, gp);
-    } else {
-        if (!attr[dev][1] && cudaFuncSetAttribute(gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  220 * 1024) != cudaSuccess)
-            return GCONV_ERR_CUDA;
-        attr[dev][1] = true;
-        gemm_kernel<128><<<grid, kGemmThreads, smem, s>>>(tA, tB, gp);
+        attr[dev][ai] = true;
     }
+    if (sh.BN == 256) gemm_kernel<256><<<grid, kGemmThreads, smem, s>>>(tA, tB, gp);
+    else if (sh.BN == 192) gemm_kernel<192><<<grid, kGemmThreads, smem, s>>>(tA, tB, gp);
+    else gemm_kernel<128><<<grid, kGemmThreads, smem, s>>>(tA, tB, gp);
     return GCONV_OK;
 }
 
