@@ -275,9 +275,17 @@ bias_finish_kernel(const float *__restrict__ part, int rows, int64_t cols, int i
     if (o >= C_out) return;
     const int64_t total = (int64_t)rows * inner;
     float s = 0.f;
-    for (int64_t e = lane; e < total; e += 32) {
-        const int64_t r = e / inner, i = e - r * inner;
-        s += __ldg(part + r * cols + (int64_t)o * inner + i);
+    for (int64_t e0 = lane; e0 < total; e0 += 4 * 32) {
+        float v[4];
+        #pragma unroll
+        for (int u = 0; u < 4; ++u) {          // four loads in flight, then added in index order
+            const int64_t e = e0 + u * 32;
+            const int64_t r = inner == 1 ? e : e / inner, i = e - r * inner;
+            v[u] = e < total ? __ldg(part + r * cols + (int64_t)o * inner + i) : 0.f;
+        }
+        #pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (e0 + u * 32 < total) s += v[u];
     }
     #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);

@@ -1230,30 +1230,32 @@ struct Pack2Params {
 
 __global__ void pack2_kernel(const __grid_constant__ Pack2Params p)
 {
-    const int64_t pieces = (int64_t)p.G * p.n_vtile * p.nchu * p.ntaps * 128 * 8;
-    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < pieces; e += (int64_t)gridDim.x * blockDim.x) {
-        const int k = (int)(e & 7);
-        const int r = (int)((e >> 3) & 127);
-        int64_t b = e >> 10;
-        const int tp = (int)(b % p.ntaps); b /= p.ntaps;
-        const int kc = (int)(b % p.nchu); b /= p.nchu;
-        const int vt = (int)(b % p.n_vtile);
-        const int g = (int)(b / p.n_vtile);
+    // 32-bit index arithmetic: the packed blocks of any supported layer stay far below 2^31 pieces
+    const int pieces = p.G * p.n_vtile * p.nchu * p.ntaps * 128 * 8;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < pieces; e += gridDim.x * blockDim.x) {
+        const int k = e & 7;
+        const int r = (e >> 3) & 127;
+        int b = e >> 10;
+        const int tp = b % p.ntaps; b /= p.ntaps;
+        const int kc = b % p.nchu; b /= p.nchu;
+        const int vt = b % p.n_vtile;
+        const int g = b / p.n_vtile;
         const int tap = (p.pair && r >= 64) ? p.tk2[tp] : p.tk1[tp];
         const int v = vt * 128 + (p.pair ? (r & 63) : r);
         uint32_t wv[4] = {0u, 0u, 0u, 0u};
         if (tap >= 0 && v < p.Cv) {
+            unsigned short h[8];
             #pragma unroll
-            for (int q = 0; q < 8; ++q) {
+            for (int q = 0; q < 8; ++q) {          // eight independent loads, then packed
                 const int u = kc * 64 + k * 8 + q;
-                if (u < p.Cu) {
-                    const int64_t idx = p.transpose ? ((int64_t)(g * p.Cu + u) * p.w_cin_g + v) * p.kHW + tap
-                                                    : ((int64_t)(g * p.Cv + v) * p.w_cin_g + u) * p.kHW + tap;
-                    wv[q >> 1] |= (uint32_t)__bfloat16_as_ushort(p.w[idx]) << ((q & 1) * 16);
-                }
+                const int64_t idx = p.transpose ? ((int64_t)(g * p.Cu + u) * p.w_cin_g + v) * p.kHW + tap
+                                                : ((int64_t)(g * p.Cv + v) * p.w_cin_g + u) * p.kHW + tap;
+                h[q] = u < p.Cu ? __bfloat16_as_ushort(p.w[idx]) : (unsigned short)0;
             }
+            #pragma unroll
+            for (int q = 0; q < 4; ++q) wv[q] = (uint32_t)h[2 * q] | ((uint32_t)h[2 * q + 1] << 16);
         }
-        uint8_t *blk = p.out + (e >> 10) * (int64_t)kWblkBytes;
+        uint8_t *blk = p.out + (int64_t)(e >> 10) * kWblkBytes;
         *reinterpret_cast<uint4 *>(blk + r * 128 + ((k ^ (r & 7)) << 4)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
     }
 }
