@@ -6,8 +6,10 @@ stride 1; fp32 outputs), through the C ABI of libgconv.
 Prints ONE JSON line (rank 0).  `value` is whole-job TFLOP/s with inputs resident
 in HBM (3 x 2*N*C_out*Ho*Wo*(C_in/G)*kH*kW FLOP per step over the device time of
 the step, CUDA events on the launch stream, L2 flushed between steps outside the
-timed events).  `e2e` is the same metric with the inputs copied from pinned host
-memory and the four outputs copied back inside the timed region.
+timed events).  `e2e` is the same metric through the host-buffer entry point
+gconv_step_host: every step copies the inputs from pinned host memory and the four
+outputs back inside the timed region (the library overlaps those copies with the
+passes on its own copy streams).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -268,7 +270,6 @@ def bench_gpu(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
-    kw = dict(stride=s, padding=(pt, pb, pl, pr), dilation=d, groups=G)
     wsp, wsb = ws.data_ptr(), ws.numel()
 
     def step_passes():
@@ -315,25 +316,19 @@ def bench_gpu(args):
     fpp = flop_per_pass(geom)
     value = world * 3 * fpp * args.steps / (total_ms * 1e-3) / 1e12
 
-    # ---- end-to-end: pinned host inputs in, four outputs back, every step ----
+    # ---- end-to-end: pinned host inputs in, four outputs back, every step, through the
+    # library's host-buffer entry point (copies on its own streams, overlapped with the passes)
     hx, hw_, hb, hdy = (t.pin_memory() for t in (x, w, b, dy))
     hy, hdx, hdw, hdb = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (y, dx, dw, db))
     h2d = sum(t.numel() * t.element_size() for t in (hx, hw_, hb, hdy))
     d2h = sum(t.numel() * t.element_size() for t in (hy, hdx, hdw, hdb))
+    step_bytes = gc.gconv_step_device_bytes(geom, dt, True)
+    step_buf = torch.empty(step_bytes, dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        xd.copy_(hx, non_blocking=True)
-        wd.copy_(hw_, non_blocking=True)
-        bd.copy_(hb, non_blocking=True)
-        dyd.copy_(hdy, non_blocking=True)
-        gc.gconv_fwd(xd, wd, bd, y, workspace=ws, stream=stream, **kw)
-        gc.gconv_bwd_data(dyd, wd, dx, workspace=ws, stream=stream, **kw)
-        gc.gconv_bwd_weight(xd, dyd, dw, workspace=ws, stream=stream, **kw)
-        gc.gconv_bwd_bias(dyd, db, geom=geom, workspace=ws, stream=stream)
-        hy.copy_(y, non_blocking=True)
-        hdx.copy_(dx, non_blocking=True)
-        hdw.copy_(dw, non_blocking=True)
-        hdb.copy_(db, non_blocking=True)
+        B.gconv_step_host_ptr(geom, dt, hx.data_ptr(), hw_.data_ptr(), hb.data_ptr(), hdy.data_ptr(),
+                              hy.data_ptr(), hdx.data_ptr(), hdw.data_ptr(), hdb.data_ptr(),
+                              step_buf.data_ptr(), step_bytes, sp)
 
     for _ in range(max(1, args.warmup)):
         e2e_step()
@@ -349,6 +344,10 @@ def bench_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = reduce_max(e0.elapsed_time(e1), world)
     e2e_value = world * 3 * fpp * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    assert gc.gconv_check_device_error(stream) == B.GCONV_OK
+    # the host results are the device passes' results, bit for bit
+    for host_t, dev_t in ((hy, y), (hdx, dx), (hdw, dw), (hdb, db)):
+        assert torch.equal(host_t, dev_t.cpu()), "host-buffer step disagrees with the device passes"
 
     if world > 1:
         torch.distributed.barrier()

@@ -31,7 +31,7 @@ PATH_NAMES = {PATH_NONE: "none", PATH_DIRECT: "direct", PATH_TC_IGEMM: "tc_igemm
 EXPORTED = ("gconv_out_shape", "gconv_workspace_size", "gconv_plan", "gconv_fwd", "gconv_bwd_data",
             "gconv_bwd_weight", "gconv_bwd_bias", "gconv_check_device_error", "gconv_status_string",
             "gconv_debug_force_path", "gconv_debug_set_wait_limit", "gconv_debug_set_trace", "gconv_bwd_weight_noalloc",
-            "gconv_noalloc_scratch_bytes")
+            "gconv_noalloc_scratch_bytes", "gconv_step_host", "gconv_step_device_bytes")
 
 _lib = None
 
@@ -71,6 +71,10 @@ def lib():
     L.gconv_bwd_weight_noalloc.restype = i
     L.gconv_noalloc_scratch_bytes.argtypes = []
     L.gconv_noalloc_scratch_bytes.restype = sz
+    L.gconv_step_host.argtypes = geo + [i, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.gconv_step_host.restype = i
+    L.gconv_step_device_bytes.argtypes = geo + [i, i]
+    L.gconv_step_device_bytes.restype = sz
     L.gconv_check_device_error.argtypes = [vp]
     L.gconv_check_device_error.restype = i
     L.gconv_status_string.argtypes = [i]
@@ -238,6 +242,42 @@ def gconv_bwd_weight_noalloc(x, dy, dw, *, stride=1, padding=0, dilation=1, grou
 
 def gconv_noalloc_scratch_bytes() -> int:
     return int(lib().gconv_noalloc_scratch_bytes())
+
+
+def gconv_step_device_bytes(geom, dtype: int, with_bias: bool = True) -> int:
+    n = lib().gconv_step_device_bytes(*map(int, geom), int(dtype), int(bool(with_bias)))
+    if n == ctypes.c_size_t(-1).value:
+        raise GconvError(GCONV_ERR_INVALID_ARG, "gconv_step_device_bytes")
+    return int(n)
+
+
+def _host(t, name: str):
+    if t is None:
+        return None
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous host tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def gconv_step_host(x, w, bias, dy, y, dx, dw, db, device_buffer, *, stride=1, padding=0, dilation=1,
+                    groups=1, stream=None):
+    """One step on host tensors (pinned for overlap): inputs copied in, the four passes,
+    y/dx/dw/db copied back; done when `stream` reaches this point (see include/gconv.h)."""
+    geom = geometry(x.shape, w.shape, stride, padding, dilation, groups)
+    dt = dtype_code(x.dtype)
+    if not device_buffer.is_cuda:
+        raise ValueError("device_buffer must be a device tensor")
+    _check(lib().gconv_step_host(*geom, dt, _host(x, "x"), _host(w, "w"), _host(bias, "bias"), _host(dy, "dy"),
+                                 _host(y, "y"), _host(dx, "dx"), _host(dw, "dw"), _host(db, "db"),
+                                 ctypes.c_void_p(device_buffer.data_ptr()),
+                                 device_buffer.numel() * device_buffer.element_size(), _stream_ptr(stream)),
+           "gconv_step_host")
+
+
+def gconv_step_host_ptr(geom, dt, x, w, bias, dy, y, dx, dw, db, buf, buf_bytes, stream=0):
+    """Pointer-level form of gconv_step_host (host pointers for tensors, a device buffer)."""
+    _check(lib().gconv_step_host(*map(int, geom), int(dt), x, w, bias or None, dy, y, dx, dw, db, buf,
+                                 int(buf_bytes), stream or None), "gconv_step_host")
 
 
 def gconv_bwd_bias(dy, db, *, geom=None, workspace=None, stream=None):

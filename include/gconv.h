@@ -183,6 +183,52 @@ gconv_status gconv_bwd_weight_noalloc(int N, int C_in, int H, int W, int C_out, 
 /* Size in bytes of the fixed scratch array used by gconv_bwd_weight_noalloc. */
 size_t gconv_noalloc_scratch_bytes(void);
 
+/* One training step of the layer on HOST tensors: copies x, w, bias and dy from
+ * host memory into `device_buffer`, runs the four passes above on them (forward,
+ * backward-data, backward-weight, bias gradient: the same operations, layouts,
+ * kernels and results as gconv_fwd, gconv_bwd_data, gconv_bwd_weight and
+ * gconv_bwd_bias), and copies y, dx, dw and db back to host memory.  The studied
+ * pages have no counterpart of this entry point; it serves callers whose tensors
+ * live in host memory, with the copies overlapped with the kernels.
+ *
+ * x, w, dy: host inputs (dtype), NCHW / OIHW as above; bias: host [C_out] or NULL.
+ * y, dx: host fp32 outputs shaped like dy and x; dw: host fp32 [C_out][C_in/G][kH][kW];
+ * db: host fp32 [C_out].  Page-locked (pinned) host memory lets the copies run
+ * asynchronously and overlap the kernels; pageable memory works, with copies that
+ * block the calling thread.  All host buffers stay owned by the caller.
+ * device_buffer: caller-owned device memory (16-byte aligned) of at least
+ * gconv_step_device_bytes(..., with_bias = bias != NULL) bytes; it holds the
+ * device copies of inputs and outputs and the passes' workspace, and is
+ * overwritten.
+ *
+ * Ordering: the input copies start after all work previously enqueued on
+ * `stream`; the passes run on `stream`; inputs and results move on copy
+ * streams the library creates per device on first use (host-to-device and
+ * device-to-host), so that a pass's result copies out while the next passes run
+ * and gradOutput copies in while the forward pass runs.
+ * When `stream` reaches the point after this call, every host output has been
+ * written.  Concurrent calls from several host threads are serialised while
+ * they enqueue.
+ *
+ * Errors: GCONV_ERR_INVALID_ARG (geometry, dtype, a NULL host pointer other than
+ * bias, a misaligned device buffer), GCONV_ERR_WORKSPACE (device_buffer NULL or
+ * smaller than required), GCONV_ERR_UNSUPPORTED, GCONV_ERR_CUDA (a copy, an event
+ * or a launch failed; work enqueued before the failure may still run).  All
+ * argument checks happen before anything is enqueued.  N = 0 is a no-op. */
+gconv_status gconv_step_host(int N, int C_in, int H, int W, int C_out, int kH, int kW,
+                             int stride, int pad_top, int pad_bottom, int pad_left,
+                             int pad_right, int dilation, int groups, gconv_dtype dtype,
+                             const void *x, const void *w, const void *bias, const void *dy,
+                             float *y, float *dx, float *dw, float *db,
+                             void *device_buffer, size_t device_bytes, void *stream);
+
+/* Device bytes gconv_step_host needs for this layer (with_bias: 1 if a bias is
+ * passed), or (size_t)-1 for an invalid or unsupported request.  Host-only. */
+size_t gconv_step_device_bytes(int N, int C_in, int H, int W, int C_out, int kH, int kW,
+                               int stride, int pad_top, int pad_bottom, int pad_left,
+                               int pad_right, int dilation, int groups, gconv_dtype dtype,
+                               int with_bias);
+
 /* Synchronises `stream`, then reads and clears the device error word that
  * bounded waits set.  GCONV_OK, GCONV_ERR_TIMEOUT, or GCONV_ERR_CUDA. */
 gconv_status gconv_check_device_error(void *stream);

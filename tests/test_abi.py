@@ -147,3 +147,40 @@ def test_python_geometry_helper():
     assert gc.geometry((2, 6, 9, 9), (4, 6, 3, 3), padding=1) == (2, 6, 9, 9, 4, 3, 3, 1, 1, 1, 1, 1, 1, 1)
     with pytest.raises(gc.GconvError):
         gc.geometry((2, 6, 9, 9), (4, 4, 3, 3), groups=2)
+
+
+def test_step_host_sizing_and_argument_checks(L):
+    """gconv_step_host: its device-buffer size covers inputs, outputs and the largest
+    workspace; bad arguments are rejected before anything is enqueued (no GPU needed)."""
+    for name, wk in wl.WORKLOADS.items():
+        geom = wk.geom
+        N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+        Ho, Wo = wl.out_hw(geom)
+        dt = B.GCONV_BF16 if wk.dtype == "bf16" else B.GCONV_F32
+        es = 2 if dt == B.GCONV_BF16 else 4
+        ws = max(gc.gconv_workspace_size(geom, dt, p) for p in range(4))
+        tensors = (N * Cin * H * W * (es + 4) + Cout * (Cin // G) * kH * kW * (es + 4)
+                   + N * Cout * Ho * Wo * (es + 4) + Cout * 4)
+        with_b = gc.gconv_step_device_bytes(geom, dt, True)
+        without_b = gc.gconv_step_device_bytes(geom, dt, False)
+        assert with_b >= tensors + ws + Cout * es, name
+        assert without_b >= tensors + ws and without_b <= with_b, name
+        ok = ctypes.c_void_p(1 << 20)
+        full = (ok, ok, ok, ok, ok, ok, ok, ok)
+        # buffer too small / missing
+        assert L.gconv_step_host(*geom, dt, *full, ok, with_b - 16, None) == B.GCONV_ERR_WORKSPACE, name
+        assert L.gconv_step_host(*geom, dt, *full, None, 0, None) == B.GCONV_ERR_WORKSPACE, name
+        # a NULL host pointer (other than bias) or a misaligned device buffer
+        for i in (0, 1, 3, 4, 5, 6, 7):
+            args = list(full)
+            args[i] = None
+            assert L.gconv_step_host(*geom, dt, *args, ok, with_b, None) == B.GCONV_ERR_INVALID_ARG, (name, i)
+        mis = ctypes.c_void_p((1 << 20) + 8)
+        assert L.gconv_step_host(*geom, dt, *full, mis, with_b, None) == B.GCONV_ERR_INVALID_ARG, name
+        assert L.gconv_step_host(*geom, 9, *full, ok, with_b, None) == B.GCONV_ERR_INVALID_ARG, name
+    # empty batch: nothing to do, nothing checked past the geometry
+    geom = (0, 8, 6, 6, 8, 3, 3, 1, 1, 1, 1, 1, 1, 1)
+    ok = ctypes.c_void_p(1 << 20)
+    assert L.gconv_step_host(*geom, 1, ok, ok, None, ok, ok, ok, ok, ok, None, 0, None) == B.GCONV_OK
+    # invalid geometry
+    assert gc.binding.lib().gconv_step_device_bytes(1, 8, 6, 6, 8, 9, 9, 1, 0, 0, 0, 0, 1, 1, 1, 1) == ctypes.c_size_t(-1).value

@@ -226,3 +226,39 @@ def test_forced_direct_agrees_with_default(dev):
     for k in auto:
         r = direct[k].double().numpy()
         check(f"cross {k}", auto[k].numpy(), r, 1e-2)
+
+
+@pytest.mark.parametrize("geom,dtype,with_bias", [
+    ((3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2), "bf16", True),     # tensor-core passes
+    ((2, 32, 12, 12, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8), "f32", False),      # CUDA-core passes, no bias
+    ((2, 128, 6, 6, 96, 6, 6, 1, 0, 0, 0, 0, 1, 1), "bf16", True),       # FC mode
+])
+def test_step_host_matches_device_passes(dev, oracle_mod, geom, dtype, with_bias):
+    """gconv_step_host on pinned host tensors gives bit for bit what the four device
+    passes give, and meets the oracle tolerance; run twice in a row on one stream."""
+    wk = wl.Workload("host", geom, dtype)
+    x, w, b, dy = wl.make_inputs(wk, seed=31)
+    if not with_bias:
+        b = None
+    ref = run_gpu(geom, x, w, b, dy, dev)
+    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+    Ho, Wo = wl.out_hw(geom)
+    hx, hw_, hdy = (t.contiguous().pin_memory() for t in (x, w, dy))
+    hb = None if b is None else b.contiguous().pin_memory()
+    dt = B.GCONV_BF16 if dtype == "bf16" else B.GCONV_F32
+    nbytes = gc.gconv_step_device_bytes(geom, dt, with_bias)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream()
+    for rep in range(2):
+        outs = {"y": torch.full((N, Cout, Ho, Wo), float("nan")).pin_memory(),
+                "dx": torch.full((N, Cin, H, W), float("nan")).pin_memory(),
+                "dw": torch.full(tuple(w.shape), float("nan")).pin_memory(),
+                "db": torch.full((Cout,), float("nan")).pin_memory()}
+        gc.gconv_step_host(hx, hw_, hb, hdy, outs["y"], outs["dx"], outs["dw"], outs["db"], buf,
+                           stream=stream, **_kw(geom))
+        stream.synchronize()
+        assert gc.gconv_check_device_error(stream) == B.GCONV_OK
+        for k in ref:
+            assert torch.equal(outs[k], ref[k]), (rep, k)
+    check("host y", outs["y"].numpy(), oracle_mod.fwd(geom, f64(x), f64(w), f64(b)), TOL[dtype])
+    check("host db", outs["db"].numpy(), oracle_mod.bwd_bias(geom, f64(dy)), TOL[dtype])
