@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <climits>
 #include <mutex>
+#include <vector>
 
 namespace gconv {
 
@@ -297,19 +298,21 @@ static bool step_layout(const Geom &g, gconv_dtype dt, bool with_bias, StepLayou
     return true;
 }
 
-// Copy streams per device -- kStepLanes for host-to-device and kStepLanes for
-// device-to-host (a tensor of at least 2 x kStepChunkMin bytes moves in one chunk per
-// lane) -- and the events that order them against the caller's stream; created on
-// first use, kept until exit.  The mutex makes one call's enqueue sequence atomic
-// with respect to other threads.  One lane per direction: on GB300 two lanes made the
-// AlexNet-layer step slower (1.03 against 0.92 ms with pinned host buffers).
-constexpr int kStepLanes = 1;
-constexpr size_t kStepChunkMin = (size_t)8 << 20;
+// Copy streams per device (host-to-device, device-to-host) and the events that order
+// them against the caller's stream; created on first use, kept until exit.  The mutex
+// makes one call's enqueue sequence atomic with respect to other threads.  Measured on
+// GB300 (AlexNet layer, pinned host buffers): the device-to-host copies bound the step;
+// splitting each copy over two streams per direction was slower (1.03 against 0.92 ms),
+// and so was letting the kernels write results straight into host memory (1.71 ms).
+// The forward pass runs in kFwdChunks batch chunks, so that its result (the largest)
+// starts copying out after the first chunk instead of after the whole pass.
+constexpr int kFwdChunks = 2;
+constexpr int kFwdChunkMinN = 8;
 
 struct StepStreams {
-    cudaStream_t in[kStepLanes] = {}, out[kStepLanes] = {};
-    cudaEvent_t start = nullptr, in1[kStepLanes] = {}, in2[kStepLanes] = {}, done[kStepLanes] = {};
-    cudaEvent_t pass_done[4] = {};
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, dy_in = nullptr, done = nullptr;
+    cudaEvent_t x_in[kFwdChunks] = {}, y_done[kFwdChunks] = {}, pass_done[4] = {};
 };
 static std::mutex g_step_mutex;
 static StepStreams g_step[64];
@@ -319,37 +322,35 @@ static StepStreams *step_streams()
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     StepStreams &ss = g_step[dev];
-    if (!ss.in[0]) {
+    if (!ss.in) {
         StepStreams t;
-        bool ok = true;
-        for (int l = 0; l < kStepLanes && ok; ++l)
-            ok = cudaStreamCreateWithFlags(&t.in[l], cudaStreamNonBlocking) == cudaSuccess &&
-                 cudaStreamCreateWithFlags(&t.out[l], cudaStreamNonBlocking) == cudaSuccess &&
-                 cudaEventCreateWithFlags(&t.in1[l], cudaEventDisableTiming) == cudaSuccess &&
-                 cudaEventCreateWithFlags(&t.in2[l], cudaEventDisableTiming) == cudaSuccess &&
-                 cudaEventCreateWithFlags(&t.done[l], cudaEventDisableTiming) == cudaSuccess;
-        ok = ok && cudaEventCreateWithFlags(&t.start, cudaEventDisableTiming) == cudaSuccess;
-        for (int i = 0; i < 4 && ok; ++i) ok = cudaEventCreateWithFlags(&t.pass_done[i], cudaEventDisableTiming) == cudaSuccess;
+        bool ok = cudaStreamCreateWithFlags(&t.in, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&t.out, cudaStreamNonBlocking) == cudaSuccess;
+        std::vector<cudaEvent_t *> evs = {&t.start, &t.dy_in, &t.done};
+        for (int c = 0; c < kFwdChunks; ++c) { evs.push_back(&t.x_in[c]); evs.push_back(&t.y_done[c]); }
+        for (int i = 0; i < 4; ++i) evs.push_back(&t.pass_done[i]);
+        for (cudaEvent_t *e : evs)
+            if (ok) ok = cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
         if (!ok) return nullptr;
         ss = t;
     }
     return &ss;
 }
 
-// Copies `bytes` in up to kStepLanes chunks, chunk l on lane l's stream.
-static bool copy_split(void *dst, const void *src, size_t bytes, cudaMemcpyKind kind, const cudaStream_t *lanes)
+// Number of batch chunks for the forward pass of a host step: kFwdChunks when every
+// chunk plans onto the same kernel family as the whole batch (so the results are the
+// same, bit for bit) within the step's workspace, else 1.
+static int fwd_chunks(const Geom &g, gconv_dtype dt, size_t ws_bytes)
 {
-    const int n = bytes >= 2 * kStepChunkMin ? kStepLanes : 1;
-    const size_t chunk = ((bytes + n - 1) / n + 255) & ~(size_t)255;
-    for (int l = 0; l < n; ++l) {
-        const size_t off = (size_t)l * chunk;
-        if (off >= bytes) break;
-        const size_t len = std::min(chunk, bytes - off);
-        if (cudaMemcpyAsync(static_cast<uint8_t *>(dst) + off, static_cast<const uint8_t *>(src) + off, len, kind,
-                            lanes[l]) != cudaSuccess)
-            return false;
+    if (g.N < kFwdChunks * kFwdChunkMinN) return 1;
+    const Plan whole = plan_pass(g, dt, GCONV_PASS_FWD);
+    for (int c = 0; c < kFwdChunks; ++c) {
+        Geom gc = g;
+        gc.N = (c + 1) * g.N / kFwdChunks - c * g.N / kFwdChunks;
+        const Plan part = plan_pass(gc, dt, GCONV_PASS_FWD);
+        if (part.path != whole.path || part.tc[0] != whole.tc[0] || part.ws_bytes > ws_bytes) return 1;
     }
-    return true;
+    return kFwdChunks;
 }
 
 }  // namespace gconv
@@ -518,40 +519,57 @@ gconv_status gconv_step_host(GEO_ARGS, gconv_dtype dtype, const void *x, const v
     void *wsd = base + L.ws;
 #define STEP_CHECK(call) do { if ((call) != cudaSuccess) return GCONV_ERR_CUDA; } while (0)
     // inputs: after everything already on the caller's stream (a previous step may
-    // still read these buffers); x, w, bias first so that the forward pass can start
+    // still read these buffers); w, bias and x (chunk by chunk) first so that the forward
+    // pass can start, gradOutput while it runs
+    const int nfc = fwd_chunks(g, dtype, L.nws);
+    const size_t x_img = L.nx / g.N, y_img = L.ny / g.N;   // bytes per image
+    int n_lo[kFwdChunks + 1];
+    for (int c = 0; c <= nfc; ++c) n_lo[c] = c * g.N / nfc;
     STEP_CHECK(cudaEventRecord(ss->start, C));
-    for (int l = 0; l < kStepLanes; ++l) STEP_CHECK(cudaStreamWaitEvent(ss->in[l], ss->start, 0));
-    if (!copy_split(xd, x, L.nx, cudaMemcpyHostToDevice, ss->in)) return GCONV_ERR_CUDA;
-    if (!copy_split(wd, w, L.nw, cudaMemcpyHostToDevice, ss->in)) return GCONV_ERR_CUDA;
-    if (bias && !copy_split(bd, bias, L.nb, cudaMemcpyHostToDevice, ss->in)) return GCONV_ERR_CUDA;
-    for (int l = 0; l < kStepLanes; ++l) STEP_CHECK(cudaEventRecord(ss->in1[l], ss->in[l]));
-    if (!copy_split(dyd, dy, L.ndy, cudaMemcpyHostToDevice, ss->in)) return GCONV_ERR_CUDA;
-    for (int l = 0; l < kStepLanes; ++l) STEP_CHECK(cudaEventRecord(ss->in2[l], ss->in[l]));
-    // the four passes on the caller's stream; each result goes back as soon as it is ready
+    STEP_CHECK(cudaStreamWaitEvent(ss->in, ss->start, 0));
+    STEP_CHECK(cudaMemcpyAsync(wd, w, L.nw, cudaMemcpyHostToDevice, ss->in));
+    if (bias) STEP_CHECK(cudaMemcpyAsync(bd, bias, L.nb, cudaMemcpyHostToDevice, ss->in));
+    for (int c = 0; c < nfc; ++c) {
+        const size_t off = (size_t)n_lo[c] * x_img, len = (size_t)(n_lo[c + 1] - n_lo[c]) * x_img;
+        STEP_CHECK(cudaMemcpyAsync(static_cast<uint8_t *>(xd) + off, static_cast<const uint8_t *>(x) + off, len,
+                                   cudaMemcpyHostToDevice, ss->in));
+        STEP_CHECK(cudaEventRecord(ss->x_in[c], ss->in));
+    }
+    STEP_CHECK(cudaMemcpyAsync(dyd, dy, L.ndy, cudaMemcpyHostToDevice, ss->in));
+    STEP_CHECK(cudaEventRecord(ss->dy_in, ss->in));
+    // forward, chunk by chunk; each chunk's result goes back as soon as it is ready
+    for (int c = 0; c < nfc; ++c) {
+        int geo_c[14];
+        std::copy(geo, geo + 14, geo_c);
+        geo_c[0] = n_lo[c + 1] - n_lo[c];
+        const size_t xo = (size_t)n_lo[c] * x_img, yo = (size_t)n_lo[c] * y_img;
+        STEP_CHECK(cudaStreamWaitEvent(C, ss->x_in[c], 0));
+        st = run_pass(geo_c, dtype, GCONV_PASS_FWD, static_cast<uint8_t *>(xd) + xo, wd, bd,
+                      reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(yd) + yo), wsd, L.nws, C);
+        if (st != GCONV_OK) return st;
+        STEP_CHECK(cudaEventRecord(ss->y_done[c], C));
+        STEP_CHECK(cudaStreamWaitEvent(ss->out, ss->y_done[c], 0));
+        STEP_CHECK(cudaMemcpyAsync(reinterpret_cast<uint8_t *>(y) + yo, reinterpret_cast<const uint8_t *>(yd) + yo,
+                                   (size_t)(n_lo[c + 1] - n_lo[c]) * y_img, cudaMemcpyDeviceToHost, ss->out));
+    }
+    // the three backward passes
+    STEP_CHECK(cudaStreamWaitEvent(C, ss->dy_in, 0));
     struct Out { void *host; const void *dev; size_t bytes; };
     const Out outs[4] = {{y, yd, L.ny}, {dx, dxd, L.ndx}, {dw, dwd, L.ndw}, {db, dbd, L.ndb}};
-    for (int pass = GCONV_PASS_FWD; pass <= GCONV_PASS_BWD_BIAS; ++pass) {
-        if (pass == GCONV_PASS_FWD)
-            for (int l = 0; l < kStepLanes; ++l) STEP_CHECK(cudaStreamWaitEvent(C, ss->in1[l], 0));
-        if (pass == GCONV_PASS_BWD_DATA)
-            for (int l = 0; l < kStepLanes; ++l) STEP_CHECK(cudaStreamWaitEvent(C, ss->in2[l], 0));
+    for (int pass = GCONV_PASS_BWD_DATA; pass <= GCONV_PASS_BWD_BIAS; ++pass) {
         switch (pass) {
-        case GCONV_PASS_FWD: st = run_pass(geo, dtype, GCONV_PASS_FWD, xd, wd, bd, yd, wsd, L.nws, C); break;
         case GCONV_PASS_BWD_DATA: st = run_pass(geo, dtype, GCONV_PASS_BWD_DATA, dyd, wd, nullptr, dxd, wsd, L.nws, C); break;
         case GCONV_PASS_BWD_WEIGHT: st = run_pass(geo, dtype, GCONV_PASS_BWD_WEIGHT, xd, dyd, nullptr, dwd, wsd, L.nws, C); break;
         default: st = run_pass(geo, dtype, GCONV_PASS_BWD_BIAS, dyd, nullptr, nullptr, dbd, wsd, L.nws, C); break;
         }
         if (st != GCONV_OK) return st;
         STEP_CHECK(cudaEventRecord(ss->pass_done[pass], C));
-        for (int l = 0; l < kStepLanes; ++l) STEP_CHECK(cudaStreamWaitEvent(ss->out[l], ss->pass_done[pass], 0));
-        if (!copy_split(outs[pass].host, outs[pass].dev, outs[pass].bytes, cudaMemcpyDeviceToHost, ss->out))
-            return GCONV_ERR_CUDA;
+        STEP_CHECK(cudaStreamWaitEvent(ss->out, ss->pass_done[pass], 0));
+        STEP_CHECK(cudaMemcpyAsync(outs[pass].host, outs[pass].dev, outs[pass].bytes, cudaMemcpyDeviceToHost, ss->out));
     }
     // the caller's stream continues only when every result is in host memory
-    for (int l = 0; l < kStepLanes; ++l) {
-        STEP_CHECK(cudaEventRecord(ss->done[l], ss->out[l]));
-        STEP_CHECK(cudaStreamWaitEvent(C, ss->done[l], 0));
-    }
+    STEP_CHECK(cudaEventRecord(ss->done, ss->out));
+    STEP_CHECK(cudaStreamWaitEvent(C, ss->done, 0));
 #undef STEP_CHECK
     return GCONV_OK;
 }
