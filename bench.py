@@ -349,6 +349,8 @@ def bench_gpu(args):
     for host_t, dev_t in ((hy, y), (hdx, dx), (hdw, dw), (hdb, db)):
         assert torch.equal(host_t, dev_t.cpu()), "host-buffer step disagrees with the device passes"
 
+    launch_bound = time_launch_bound(dev)
+
     if world > 1:
         torch.distributed.barrier()
     if rank != 0:
@@ -395,10 +397,131 @@ def bench_gpu(args):
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / e2e_steps},
         "gpu_launches": launches_per_step * args.steps,
+        "launch_bound": launch_bound,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def time_launch_bound(dev, reps=200):
+    """The launch-bound case (tiny_g5: fp32, groups 5, x [2,100,28,28]): one step of the
+    four passes as separate API calls, and the same step captured once in a CUDA graph and
+    replayed; microseconds per step for each (inputs resident, L2 warm)."""
+    import torch
+    import bwd_gconv_fwd_gb300 as gc
+    from bwd_gconv_fwd_gb300 import binding as B
+    from bwd_gconv_fwd_gb300 import workloads as wl
+
+    wk = wl.WORKLOADS["tiny_g5"]
+    geom = wk.geom
+    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+    Ho, Wo = wl.out_hw(geom)
+    x, w, b, dy = (t.to(dev) for t in wl.make_inputs(wk))
+    y = torch.empty((N, Cout, Ho, Wo), device=dev)
+    dx = torch.empty((N, Cin, H, W), device=dev)
+    dw = torch.empty(tuple(w.shape), device=dev)
+    db = torch.empty((Cout,), device=dev)
+    dt = B.GCONV_F32
+    wsb = max(16, max(gc.gconv_workspace_size(geom, dt, p) for p in range(4)))
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream(dev)
+    sp = st.cuda_stream
+
+    def step():
+        B.gconv_fwd_ptr(geom, dt, x.data_ptr(), w.data_ptr(), b.data_ptr(), y.data_ptr(), ws.data_ptr(), wsb, sp)
+        B.gconv_bwd_data_ptr(geom, dt, dy.data_ptr(), w.data_ptr(), dx.data_ptr(), ws.data_ptr(), wsb, sp)
+        B.gconv_bwd_weight_ptr(geom, dt, x.data_ptr(), dy.data_ptr(), dw.data_ptr(), ws.data_ptr(), wsb, sp)
+        B.gconv_bwd_bias_ptr(geom, dt, dy.data_ptr(), db.data_ptr(), ws.data_ptr(), wsb, sp)
+
+    for _ in range(5):
+        step()
+    st.synchronize()
+    ref = [t.clone() for t in (y, dx, dw, db)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        step()
+    e1.record(st)
+    e1.synchronize()
+    us_calls = e0.elapsed_time(e1) * 1e3 / reps
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        step()
+    for _ in range(5):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0.record(st)
+    with torch.cuda.stream(st):
+        for _ in range(reps):
+            graph.replay()
+    e1.record(st)
+    e1.synchronize()
+    us_graph = e0.elapsed_time(e1) * 1e3 / reps
+    assert all(torch.equal(a, c) for a, c in zip(ref, (y, dx, dw, db))), "graph replay disagrees with the calls"
+    assert gc.gconv_check_device_error(st) == B.GCONV_OK
+    return {"workload": "tiny_g5: x[2,100,28,28] fp32, w[15,20,3,3], groups 5", "us_per_step_calls": us_calls,
+            "us_per_step_graph": us_graph, "launches_per_step": sum(gc.gconv_plan(geom, dt, p)[1] for p in range(4))}
+
+
+def bench_sweep(args):
+    """--sweep: per-pass timing of the model-zoo layer sweep (ResNeXt-50 32x4d grouped 3x3,
+    MobileNet-v2 depthwise 3x3) at batch 32; one JSON line per layer.  CUDA events on one
+    stream, L2 flushed before each pass, median of --steps repetitions after --warmup."""
+    import torch
+    import bwd_gconv_fwd_gb300 as gc
+    from bwd_gconv_fwd_gb300 import binding as B
+    from bwd_gconv_fwd_gb300 import workloads as wl
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    st = torch.cuda.current_stream(dev)
+    sp = st.cuda_stream
+    dt = B.GCONV_BF16
+    for name, wk in wl.model_zoo(32).items():
+        geom = wk.geom
+        N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+        Ho, Wo = wl.out_hw(geom)
+        x, w, b, dy = (t.to(dev) for t in wl.make_inputs(wk))
+        y = torch.empty((N, Cout, Ho, Wo), device=dev)
+        dx = torch.empty((N, Cin, H, W), device=dev)
+        dw = torch.empty(tuple(w.shape), device=dev)
+        db = torch.empty((Cout,), device=dev)
+        wsb = max(16, max(gc.gconv_workspace_size(geom, dt, p) for p in range(4)))
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        calls = {
+            "fwd": lambda: B.gconv_fwd_ptr(geom, dt, x.data_ptr(), w.data_ptr(), b.data_ptr(), y.data_ptr(), ws.data_ptr(), wsb, sp),
+            "bwd_data": lambda: B.gconv_bwd_data_ptr(geom, dt, dy.data_ptr(), w.data_ptr(), dx.data_ptr(), ws.data_ptr(), wsb, sp),
+            "bwd_weight": lambda: B.gconv_bwd_weight_ptr(geom, dt, x.data_ptr(), dy.data_ptr(), dw.data_ptr(), ws.data_ptr(), wsb, sp),
+            "bwd_bias": lambda: B.gconv_bwd_bias_ptr(geom, dt, dy.data_ptr(), db.data_ptr(), ws.data_ptr(), wsb, sp),
+        }
+        fpp = flop_per_pass(geom)
+        abytes = algorithmic_bytes(geom)
+        out = {}
+        for nm, f in calls.items():
+            times = []
+            for k in range(args.warmup + args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                f()
+                e1.record(st)
+                e1.synchronize()
+                if k >= args.warmup:
+                    times.append(e0.elapsed_time(e1) * 1e-3)
+            t = statistics.median(times)
+            path, launches = gc.gconv_plan(geom, dt, list(calls).index(nm))
+            t_roof = abytes[nm] / (peaks["hbm_gbs"] * 1e9)
+            if nm != "bwd_bias":
+                t_roof = max(t_roof, fpp / (peaks["bf16_tflops"] * 1e12))
+            out[nm] = {"us": t * 1e6, "path": gc.PATH_NAMES[path], "launches": launches,
+                       "gbs": abytes[nm] / t / 1e9, "roofline_frac": t_roof / t}
+        assert gc.gconv_check_device_error(st) == B.GCONV_OK
+        print(json.dumps({"sweep": name, "geom": list(geom), "gflop_per_pass": fpp / 1e9, "passes": out,
+                          "peak_source": peak_src}), flush=True)
     return 0
 
 
@@ -410,10 +533,13 @@ def main():
     ap.add_argument("--impl", default="gconv", choices=["gconv", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="time the model-zoo layer sweep instead")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps, whatever is asked
     if args.impl == "reference":
         return bench_reference(args)
+    if args.sweep:
+        return bench_sweep(args)
     return bench_gpu(args)
 
 

@@ -335,6 +335,27 @@ __device__ __forceinline__ void bwd_data_tile(const Geom &g, const TileGeom &t, 
         if (unit) {
             // staged row of (ih - kh*d + pt) is ihl + (kH-1-kh)*d: mirrored tap kh' = kH-1-kh
             corr_point<CI_, K>(acc, ds + r * t.CIp + col, ws, g.Cgo, t.RI * t.CIp, g.kH, g.kW, g.d * t.CIp, g.d);
+        } else if (g.s == 2) {
+            // stride 2: a tap reaches this pixel when ih + pt - kh*d is even (parity tests
+            // and shifts instead of divisions by the runtime stride)
+            #pragma unroll
+            for (int c = 0; c < CI_; ++c) acc[c] = 0.f;
+            const int ih = ih0 + r, iw = iw0 + col;
+            for (int kh = 0; kh < g.kH; ++kh) {
+                const int tt = ih + g.pt - kh * g.d;
+                if (tt < 0 || (tt & 1)) continue;
+                const int oh = tt >> 1;
+                if (oh >= g.Ho) continue;
+                for (int kw = 0; kw < g.kW; ++kw) {
+                    const int tu = iw + g.pl - kw * g.d;
+                    if (tu < 0 || (tu & 1)) continue;
+                    const int ow = tu >> 1;
+                    if (ow >= g.Wo) continue;
+                    const float *dp = ds + (oh - oh_s) * t.CIp + (ow - ow_s);
+                    const float *wp = ws + (kh * g.kW + kw) * CI_;
+                    for (int o = 0; o < g.Cgo; ++o, dp += t.RI * t.CIp, wp += KK * CI_) fma_row<CI_>(acc, wp, *dp);
+                }
+            }
         } else {
             #pragma unroll
             for (int c = 0; c < CI_; ++c) acc[c] = 0.f;

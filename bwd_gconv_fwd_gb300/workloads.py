@@ -29,6 +29,8 @@ once, round-to-nearest-even, to the storage dtype):
   ``dense3x3_s2_asym`` with pads top/bottom/left/right 0/1/0/1, stride 2.
 * ``resnext_g32`` -- x [64,128,56,56], w [128,4,3,3] N(0, sd=1/6), groups 32, pad 1;
   and ``depthwise`` x [64,256,56,56], w [256,1,3,3] N(0, sd=1/3), groups 256.
+* ``model_zoo(N)`` -- a shape sweep: the grouped 3x3 layers of ResNeXt-50 (32x4d) and
+  the depthwise 3x3 layers of MobileNet-v2 (stride 1 and 2, pad 1), batch N.
 """
 from __future__ import annotations
 
@@ -80,6 +82,30 @@ WORKLOADS = {
     "depthwise": Workload("depthwise", _g(64, 256, 56, 56, 256, 3, 3, 1, 1, 1, 1, 1, 1, 256), "bf16",
                           w=("normal", 1.0 / 3.0)),
 }
+
+
+
+def _zoo(name, N, C, HW, G, s):
+    """A 3x3, pad-1 grouped or depthwise layer of a model-zoo network (C in = C out)."""
+    return Workload(name, _g(N, C, HW, HW, C, 3, 3, s, 1, 1, 1, 1, 1, G), "bf16",
+                    w=("normal", 1.0 / math.sqrt((C // G) * 9)))
+
+
+def model_zoo(N):
+    """Shape sweep of the grouped 3x3 layers of ResNeXt-50 (32x4d) and the depthwise 3x3
+    layers of MobileNet-v2 at 224x224 input (the networks the pages validate grouped
+    convolutions on), batch N; weights N(0, sd = 1/sqrt(fan_in)), everything else N(0, 1)
+    or N(0, 0.1) for the bias, bf16 storage."""
+    rx = [("resnext_s1_128x56", 128, 56, 1), ("resnext_s2_256x56", 256, 56, 2), ("resnext_s1_256x28", 256, 28, 1),
+          ("resnext_s2_512x28", 512, 28, 2), ("resnext_s1_512x14", 512, 14, 1), ("resnext_s2_1024x14", 1024, 14, 2),
+          ("resnext_s1_1024x7", 1024, 7, 1)]
+    mb = [("mbv2_dw_32x112", 32, 112, 1), ("mbv2_dw_96x112_s2", 96, 112, 2), ("mbv2_dw_144x56", 144, 56, 1),
+          ("mbv2_dw_144x56_s2", 144, 56, 2), ("mbv2_dw_192x28", 192, 28, 1), ("mbv2_dw_192x28_s2", 192, 28, 2),
+          ("mbv2_dw_384x14", 384, 14, 1), ("mbv2_dw_576x14", 576, 14, 1), ("mbv2_dw_576x14_s2", 576, 14, 2),
+          ("mbv2_dw_960x7", 960, 7, 1)]
+    out = {nm: _zoo(nm, N, C, hw, 32, st) for nm, C, hw, st in rx}
+    out.update({nm: _zoo(nm, N, C, hw, C, st) for nm, C, hw, st in mb})
+    return out
 
 
 def out_hw(geom):

@@ -264,3 +264,12 @@ def test_step_host_matches_device_passes(dev, oracle_mod, geom, dtype, with_bias
             assert torch.equal(outs[k], ref[k]), (rep, k)
     check("host y", outs["y"].numpy(), oracle_mod.fwd(geom, f64(x), f64(w), f64(b)), TOL[dtype])
     check("host db", outs["db"].numpy(), oracle_mod.bwd_bias(geom, f64(dy)), TOL[dtype])
+
+
+@pytest.mark.parametrize("name", list(wl.model_zoo(2)))
+def test_model_zoo_layers_full(dev, oracle_mod, name):
+    """The grouped 3x3 layers of ResNeXt-50 (32x4d) and the depthwise 3x3 layers of
+    MobileNet-v2 (stride 1 and 2), batch 2, all four passes against the oracle."""
+    wk = wl.model_zoo(2)[name]
+    x, w, b, dy = wl.make_inputs(wk, seed=41)
+    full_compare(wk.geom, "bf16", x, w, b, dy, dev, oracle_mod, label=name)
