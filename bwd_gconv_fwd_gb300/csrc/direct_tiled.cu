@@ -433,6 +433,7 @@ struct Conv3Params {
     int in_ctot, out_ctot;                 // channel counts of the whole tensors
     int r_off, c_off;
     int TH, TW, n_th, n_tw, tq, CIp;       // tile, tiles, thread columns (TW / BX), staged row pitch
+    int GB, n_gb;                          // groups per tile (small planes share a block), group blocks
     int bwd;                               // 1: weights mirrored and transposed (backward-data)
     int w_cin_g;                           // C_in/G of the weight tensor
 };
@@ -445,28 +446,33 @@ conv3_s1_kernel(const __grid_constant__ Conv3Params p)
     constexpr int V = 16 / (int)sizeof(T);
     const int RI = p.TH + 2, CI = p.TW + 2, CIp = p.CIp;
     const bool vec_rows = (p.IW % V) == 0;
-    float *ws = sm3;                                  // [nin][9][CO]
-    float *xs = sm3 + ((p.nin * 9 * CO + 3) & ~3);   // [nin][RI][CIp], 16-byte aligned
+    float *ws = sm3;                                        // [GB][nin][9][CO]
+    float *xs = sm3 + ((p.GB * p.nin * 9 * CO + 3) & ~3);  // [GB][nin][RI][CIp], 16-byte aligned
     const T *W = static_cast<const T *>(p.w);
     const T *B = static_cast<const T *>(p.bias);
     const int64_t plane = (int64_t)p.IH * p.IW, out_plane = (int64_t)p.OH * p.OW;
-    const int ntiles = p.N * p.G * p.n_th * p.n_tw;
-    // per-thread constants: compute block, staging slot
-    const int tx = threadIdx.x % p.tq, ty = threadIdx.x / p.tq;
+    const int ntiles = p.N * p.n_gb * p.n_th * p.n_tw;
+    // per-thread constants: group of the tile, compute block, staging slot
+    const int tpg = p.tq * (p.TH / 4);                    // threads per group's tile
+    const int gsub = threadIdx.x / tpg, lt = threadIdx.x - gsub * tpg;
+    const int tx = lt % p.tq, ty = lt / p.tq;
     const int rb = 4 * ty, cb = BX * tx;
     const int nv = CIp / V;                               // staged vectors per row
     const int rows_pass = kTT / nv;                       // rows staged per pass of the block
     const int svi = threadIdx.x % nv, srow0 = threadIdx.x / nv;
-    const int nrows = p.nin * RI;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         int b = tile;
         const int tw = b % p.n_tw; b /= p.n_tw;
         const int th = b % p.n_th; b /= p.n_th;
-        const int grp = b % p.G;
-        const int n = b / p.G;
+        const int grp0 = (b % p.n_gb) * p.GB;
+        const int n = b / p.n_gb;
+        const int ngr = min(p.GB, p.G - grp0);           // groups of this tile (consecutive channels)
+        const int nrows = ngr * p.nin * RI;
         const int r0 = th * p.TH, c0 = tw * p.TW;
-        for (int i = threadIdx.x; i < p.nin * 9 * CO; i += kTT) {
-            const int ci = i / (9 * CO), rem = i - ci * 9 * CO, tap = rem / CO, o = rem - tap * CO;
+        for (int i = threadIdx.x; i < ngr * p.nin * 9 * CO; i += kTT) {
+            const int gi = i / (p.nin * 9 * CO), i2 = i - gi * (p.nin * 9 * CO);
+            const int ci = i2 / (9 * CO), rem = i2 - ci * 9 * CO, tap = rem / CO, o = rem - tap * CO;
+            const int grp = grp0 + gi;
             float v = 0.f;
             if (o < p.nout) {
                 // forward: w[g*nout + o][ci][tap]; backward-data: w[g*nin + ci][o][8 - tap]
@@ -476,7 +482,7 @@ conv3_s1_kernel(const __grid_constant__ Conv3Params p)
             }
             ws[i] = v;
         }
-        const T *srcg = static_cast<const T *>(p.src) + ((int64_t)n * p.in_ctot + (int64_t)grp * p.nin) * plane;
+        const T *srcg = static_cast<const T *>(p.src) + ((int64_t)n * p.in_ctot + (int64_t)grp0 * p.nin) * plane;
         const int cs = c0 + p.c_off;
         int coff = 0;
         if (vec_rows) {
@@ -510,10 +516,11 @@ conv3_s1_kernel(const __grid_constant__ Conv3Params p)
                 }
             }
         } else {
-            stage_rows(srcg, plane, p.IH, p.IW, r0 + p.r_off, cs, p.nin, RI, CI, CIp, xs);
+            stage_rows(srcg, plane, p.IH, p.IW, r0 + p.r_off, cs, ngr * p.nin, RI, CI, CIp, xs);
         }
         __syncthreads();
-        if (rb < p.TH && r0 + rb < p.OH && c0 + cb < p.OW) {
+        if (gsub < ngr && rb < p.TH && r0 + rb < p.OH && c0 + cb < p.OW) {
+            const int grp = grp0 + gsub;
             float acc[4][BX][CO];
             #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -522,8 +529,8 @@ conv3_s1_kernel(const __grid_constant__ Conv3Params p)
                     #pragma unroll
                     for (int o = 0; o < CO; ++o) acc[i][j][o] = 0.f;
             for (int ci = 0; ci < p.nin; ++ci) {
-                const float *xw = xs + (ci * RI + rb) * CIp + cb + coff;
-                const float *wc = ws + ci * 9 * CO;
+                const float *xw = xs + ((gsub * p.nin + ci) * RI + rb) * CIp + cb + coff;
+                const float *wc = ws + (gsub * p.nin + ci) * 9 * CO;
                 float win[6][BX + 2];
                 #pragma unroll
                 for (int i = 0; i < 6; ++i)
@@ -607,6 +614,14 @@ bool plan_conv3(const Geom &g, bool bwd, Conv3Params *p, size_t *smem)
     if (p->CIp / 4 > kTT) return false;   // one staging thread per vector of a row
     p->n_th = (p->OH + p->TH - 1) / p->TH;
     p->n_tw = (p->OW + p->TW - 1) / p->TW;
+    // small planes leave most of the block idle: several consecutive groups share a block
+    // (their channels are consecutive planes), as many as the threads and 96 KB allow
+    p->GB = std::max(1, std::min(g.G, kTT / (p->tq * rows_q)));
+    for (;; p->GB = std::max(1, p->GB / 2)) {
+        *smem = (size_t)(((p->GB * nin * 9 * CO + 3) & ~3) + p->GB * nin * (p->TH + 2) * p->CIp) * 4;
+        if (*smem <= 96 * 1024 || p->GB == 1) break;
+    }
+    p->n_gb = (g.G + p->GB - 1) / p->GB;
     return true;
 }
 
@@ -624,7 +639,7 @@ bool launch_conv3_t(const Conv3Params &p, size_t smem, cudaStream_t s)
     }
     // one tile per block keeps more blocks resident for the light single-channel form;
     // the four-channel form walks tiles persistently
-    const int64_t ntiles = (int64_t)p.N * p.G * p.n_th * p.n_tw;
+    const int64_t ntiles = (int64_t)p.N * p.n_gb * p.n_th * p.n_tw;
     const unsigned grid = (unsigned)(CO >= 4 ? std::min<int64_t>(ntiles, (int64_t)kNumSMs * 8) : ntiles);
     conv3_s1_kernel<T, CO, BX><<<grid, kTT, smem, s>>>(p);
     return true;
