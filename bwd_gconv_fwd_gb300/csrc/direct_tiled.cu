@@ -335,6 +335,28 @@ __device__ __forceinline__ void bwd_data_tile(const Geom &g, const TileGeom &t, 
         if (unit) {
             // staged row of (ih - kh*d + pt) is ihl + (kH-1-kh)*d: mirrored tap kh' = kH-1-kh
             corr_point<CI_, K>(acc, ds + r * t.CIp + col, ws, g.Cgo, t.RI * t.CIp, g.kH, g.kW, g.d * t.CIp, g.d);
+        } else if (K == 3 && g.s == 2) {
+            // 3 x 3, stride 2: the taps unrolled, a tap reaching this pixel when ih + pt - kh*d
+            // and iw + pl - kw*d are even (parity tests and shifts, no divisions, no tap loop)
+            #pragma unroll
+            for (int c = 0; c < CI_; ++c) acc[c] = 0.f;
+            const int ih = ih0 + r, iw = iw0 + col;
+            #pragma unroll
+            for (int kh = 0; kh < 3; ++kh) {
+                const int tt = ih + g.pt - kh * g.d;
+                const int oh = tt >> 1;
+                const bool okh = tt >= 0 && !(tt & 1) && oh < g.Ho;
+                #pragma unroll
+                for (int kw = 0; kw < 3; ++kw) {
+                    const int tu = iw + g.pl - kw * g.d;
+                    const int ow = tu >> 1;
+                    if (okh && tu >= 0 && !(tu & 1) && ow < g.Wo) {
+                        const float *dp = ds + (oh - oh_s) * t.CIp + (ow - ow_s);
+                        const float *wp = ws + (kh * 3 + kw) * CI_;
+                        for (int o = 0; o < g.Cgo; ++o, dp += t.RI * t.CIp, wp += 9 * CI_) fma_row<CI_>(acc, wp, *dp);
+                    }
+                }
+            }
         } else if (g.s == 2) {
             // stride 2: a tap reaches this pixel when ih + pt - kh*d is even (parity tests
             // and shifts instead of divisions by the runtime stride)
