@@ -27,6 +27,7 @@ struct TileGeom {
     int n_th, n_tw;    // tiles along rows and columns
     int NB, n_nb;      // weight gradient: images per block, image chunks
     int L, P;          // weight gradient: position lanes, (output, input) channel pairs
+    int IMG;           // 3x3 weight gradient: images staged together (small planes), 0 = 1
 };
 
 __host__ __device__ __forceinline__ int floordiv_i(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
@@ -766,8 +767,10 @@ wgrad3_s1_kernel(Geom g, TileGeom t, int CIpx, int CIpy, const T *__restrict__ x
     extern __shared__ __align__(16) float sm[];
     constexpr int V = 16 / (int)sizeof(T);
     const int RI = t.TH + 2;
-    float *xs = sm;                                        // [Cgi][RI][CIpx]
-    float *ds = sm + g.Cgi * RI * CIpx;                    // [Cgo][TH][CIpy]
+    const int IMG = max(1, t.IMG);
+    const int xsz = g.Cgi * RI * CIpx, dsz = g.Cgo * t.TH * CIpy;
+    float *xs = sm;                                        // [IMG][Cgi][RI][CIpx]
+    float *ds = sm + IMG * xsz;                            // [IMG][Cgo][TH][CIpy]
     int b = blockIdx.x;
     const int nb = b % t.n_nb; b /= t.n_nb;
     const int tw = b % t.n_tw; b /= t.n_tw;
@@ -788,19 +791,25 @@ wgrad3_s1_kernel(Geom g, TileGeom t, int CIpx, int CIpy, const T *__restrict__ x
     for (int k = 0; k < 9; ++k) acc[k] = 0.f;
     const int64_t in_plane = (int64_t)g.H * g.W, out_plane = (int64_t)g.Ho * g.Wo;
     const int n1 = min(g.N, (nb + 1) * t.NB);
-    for (int n = nb * t.NB; n < n1; ++n) {
-        const T *xg = x + ((int64_t)n * g.Cin + (int64_t)grp * g.Cgi) * in_plane;
-        const T *dg = dy + ((int64_t)n * g.Cout + (int64_t)grp * g.Cgo) * out_plane;
-        __syncthreads();   // the previous image's tiles are no longer read
-        if (xvec) stage_rows_vec(xg, in_plane, g.H, g.W, r0 - g.pt, cax, g.Cgi, RI, CIpx, xs);
-        else stage_rows(xg, in_plane, g.H, g.W, r0 - g.pt, cax, g.Cgi, RI, t.TW + 2, CIpx, xs);
-        if (yvec) stage_rows_vec(dg, out_plane, g.Ho, g.Wo, r0, cay, g.Cgo, t.TH, CIpy, ds);
-        else stage_rows(dg, out_plane, g.Ho, g.Wo, r0, cay, g.Cgo, t.TH, t.TW, CIpy, ds);
+    // images are staged IMG at a time (several for small planes, so that the lanes have
+    // enough 4 x 4 blocks), then the lanes take (image, block) items in a fixed order
+    for (int n = nb * t.NB; n < n1; n += IMG) {
+        const int ni = min(IMG, n1 - n);
+        __syncthreads();   // the previous images' tiles are no longer read
+        for (int ii = 0; ii < ni; ++ii) {
+            const T *xg = x + ((int64_t)(n + ii) * g.Cin + (int64_t)grp * g.Cgi) * in_plane;
+            const T *dg = dy + ((int64_t)(n + ii) * g.Cout + (int64_t)grp * g.Cgo) * out_plane;
+            if (xvec) stage_rows_vec(xg, in_plane, g.H, g.W, r0 - g.pt, cax, g.Cgi, RI, CIpx, xs + ii * xsz);
+            else stage_rows(xg, in_plane, g.H, g.W, r0 - g.pt, cax, g.Cgi, RI, t.TW + 2, CIpx, xs + ii * xsz);
+            if (yvec) stage_rows_vec(dg, out_plane, g.Ho, g.Wo, r0, cay, g.Cgo, t.TH, CIpy, ds + ii * dsz);
+            else stage_rows(dg, out_plane, g.Ho, g.Wo, r0, cay, g.Cgo, t.TH, t.TW, CIpy, ds + ii * dsz);
+        }
         __syncthreads();
         if (active) {
-            const float *xsp = xs + c * RI * CIpx + coffx;
-            const float *dsp = ds + o * t.TH * CIpy + coffy;
-            for (int blk = l; blk < nblk; blk += t.L) {
+            for (int it = l; it < ni * nblk; it += t.L) {
+                const int ii = it / nblk, blk = it - ii * nblk;
+                const float *xsp = xs + ii * xsz + c * RI * CIpx + coffx;
+                const float *dsp = ds + ii * dsz + o * t.TH * CIpy + coffy;
                 const int br = blk / nbc, bc = blk - br * nbc;
                 const int rr = 4 * br, cc = 4 * bc;
                 if (r0 + rr >= g.Ho || c0 + cc >= g.Wo) continue;
@@ -863,9 +872,18 @@ bool plan_wgrad3(const Geom &g, TileGeom *t, size_t *smem, int *CIpx, int *CIpy)
     t->n_th = (g.Ho + t->TH - 1) / t->TH;
     t->n_tw = (g.Wo + t->TW - 1) / t->TW;
     const int64_t spatial = (int64_t)g.G * t->n_th * t->n_tw;
-    const int n_nb = (int)std::max<int64_t>(1, std::min<int64_t>(g.N, (4 * (int64_t)kNumSMs * 4 + spatial - 1) / spatial));
+    int n_nb = (int)std::max<int64_t>(1, std::min<int64_t>(g.N, (4 * (int64_t)kNumSMs * 4 + spatial - 1) / spatial));
+    // small planes: fewer, larger image chunks, so that a block has about L (image, block)
+    // items, staged several images at a time
+    const int nblk = (t->TH / 4) * (t->TW / 4);
+    if (nblk < t->L) n_nb = std::max(1, std::min(n_nb, (g.N * nblk + t->L - 1) / t->L));
     t->NB = (g.N + n_nb - 1) / n_nb;
     t->n_nb = (g.N + t->NB - 1) / t->NB;
+    const int64_t per_img = (int64_t)g.Cgi * (t->TH + 2) * *CIpx + (int64_t)g.Cgo * t->TH * *CIpy;
+    int img = std::max(1, std::min(t->NB, t->L / std::max(1, nblk)));
+    while (img > 1 && std::max<int64_t>(img * per_img, (int64_t)P * 9 * t->L) * 4 > 96 * 1024) --img;
+    t->IMG = img;
+    *smem = (size_t)std::max<int64_t>(img * per_img, (int64_t)P * 9 * t->L) * 4;
     return true;
 }
 
