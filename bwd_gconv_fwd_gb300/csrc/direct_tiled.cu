@@ -842,10 +842,23 @@ wgrad3_s1_kernel(Geom g, TileGeom t, int CIpx, int CIpy, const T *__restrict__ x
     }
     __syncthreads();
     float *dst = part + (int64_t)blockIdx.x * t.P * 9;
-    for (int i = threadIdx.x; i < t.P * 9; i += kTT) {
-        float sum = 0.f;
-        for (int j = 0; j < t.L; ++j) sum += red[i * t.L + j];
-        dst[i] = sum;
+    if (t.L >= 32) {
+        // a warp per (pair, tap): lanes take lane j, j + 32, ... in order, then a fixed
+        // shuffle tree (one thread adding hundreds of lanes serially left the block idle)
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        for (int i = warp; i < t.P * 9; i += kTT / 32) {
+            float sum = 0.f;
+            for (int j = lane; j < t.L; j += 32) sum += red[i * t.L + j];
+            #pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            if (lane == 0) dst[i] = sum;
+        }
+    } else {
+        for (int i = threadIdx.x; i < t.P * 9; i += kTT) {
+            float sum = 0.f;
+            for (int j = 0; j < t.L; ++j) sum += red[i * t.L + j];
+            dst[i] = sum;
+        }
     }
 }
 
