@@ -184,3 +184,19 @@ def test_step_host_sizing_and_argument_checks(L):
     assert L.gconv_step_host(*geom, 1, ok, ok, None, ok, ok, ok, ok, ok, None, 0, None) == B.GCONV_OK
     # invalid geometry
     assert gc.binding.lib().gconv_step_device_bytes(1, 8, 6, 6, 8, 9, 9, 1, 0, 0, 0, 0, 1, 1, 1, 1) == ctypes.c_size_t(-1).value
+
+
+def test_model_zoo_layers_have_plans(L):
+    """Every layer of the model-zoo sweep (ResNeXt-50 grouped, MobileNet-v2 depthwise, stride 1
+    and 2) is served by some kernel family for every pass, with a bounded workspace, and the
+    host-step buffer covers it (host-only)."""
+    for N in (2, 32):
+        for name, wk in wl.model_zoo(N).items():
+            geom = wk.geom
+            for p in range(4):
+                path, launches = gc.gconv_plan(geom, B.GCONV_BF16, p)
+                assert path in (B.PATH_DIRECT, B.PATH_TC_IGEMM, B.PATH_TC_FC, B.PATH_REDUCE), (name, p)
+                assert 1 <= launches <= 9, (name, p)
+                ws = gc.gconv_workspace_size(geom, B.GCONV_BF16, p)
+                assert 0 <= ws < (1 << 32), (name, p)
+            assert gc.gconv_step_device_bytes(geom, B.GCONV_BF16, True) > 0, name
