@@ -378,3 +378,18 @@ def test_thread_count_does_not_change_results(oracle_mod):
     x, w, b, dy = _inputs(rng, geom)
     assert np.array_equal(oracle_mod.bwd_weight(geom, x, dy, threads=1), oracle_mod.bwd_weight(geom, x, dy, threads=4))
     assert np.array_equal(oracle_mod.fwd(geom, x, w, b, threads=1), oracle_mod.fwd(geom, x, w, b, threads=3))
+
+
+def test_model_zoo_layers_vs_torch_float64(oracle_mod):
+    """Library pin on the full-size channel counts of the model-zoo sweep (ResNeXt-50
+    grouped and MobileNet-v2 depthwise 3x3 layers, stride 1 and 2) at batch 1: the oracle
+    against torch conv2d in float64 + autograd."""
+    rng = np.random.default_rng(77)
+    for name, wk in wlm.model_zoo(1).items():
+        geom = wk.geom
+        x, w, b, dy = _inputs(rng, geom)
+        y_t, dx_t, dw_t, db_t = _torch_ref(geom, x, w, b, dy)
+        assert _rel(oracle_mod.fwd(geom, x, w, b), y_t) <= 1e-12, name
+        assert _rel(oracle_mod.bwd_data(geom, dy, w), dx_t) <= 1e-12, name
+        assert _rel(oracle_mod.bwd_weight(geom, x, dy), dw_t) <= 1e-12, name
+        assert _rel(oracle_mod.bwd_bias(geom, dy), db_t) <= 1e-12, name
