@@ -1,0 +1,75 @@
+"""CPU replays of the tensor-core launches' host planning and index arithmetic.
+
+The two programs under tests/replay/ include the library source, rebuild the launch
+parameters the library would use for a geometry, and walk every tile's reads and writes
+on the host, checking them against the buffers' extents (bounds are checked by reading
+the index arithmetic, not by running a possibly faulting kernel).  They need nvcc (to
+compile the included CUDA source) but no GPU.
+"""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+from bwd_gconv_fwd_gb300 import workloads as wl
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _nvcc():
+    return shutil.which("nvcc") or ("/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else None)
+
+
+@pytest.fixture(scope="module")
+def replay_bins(tmp_path_factory):
+    nvcc = _nvcc()
+    if not nvcc:
+        pytest.skip("nvcc not available")
+    out = tmp_path_factory.mktemp("replay")
+    bins = {}
+    for name in ("corr2_plan_replay", "wgrad_phase_replay"):
+        exe = str(out / name)
+        cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O1", "-std=c++17", "-o", exe,
+               os.path.join(HERE, "replay", name + ".cu"), "-lcuda"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr[-2000:]
+        bins[name] = exe
+    return bins
+
+
+def _run(exe, geom):
+    r = subprocess.run([exe, *map(str, geom)], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and "errors: 0" in r.stdout, (geom, r.stdout[-2000:])
+
+
+STRIDE1 = [
+    (3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2),       # AlexNet-like, ragged
+    (2, 32, 14, 13, 64, 3, 3, 1, 1, 0, 2, 1, 1, 2),
+    (2, 64, 17, 15, 64, 3, 3, 1, 1, 1, 1, 1, 1, 1),
+    (2, 16, 9, 9, 16, 3, 3, 1, 2, 2, 2, 2, 2, 1),           # dilation 2
+    (2, 256, 9, 9, 256, 3, 3, 1, 1, 1, 1, 1, 1, 1),         # several channel tiles
+    (1, 96, 13, 40, 160, 3, 3, 1, 1, 1, 1, 1, 1, 2),        # wide rows, 80 produced channels
+    (1, 40, 7, 23, 24, 2, 4, 1, 0, 3, 1, 0, 1, 1),          # odd channel counts, 2 x 4 kernel
+    (2, 64, 20, 20, 64, 7, 7, 1, 3, 3, 3, 3, 1, 1),         # 49 taps
+]
+
+
+@pytest.mark.parametrize("geom", STRIDE1 + [wk.geom for wk in wl.WORKLOADS.values() if wk.geom[7] == 1]
+                         + [wk.geom for wk in wl.model_zoo(2).values() if wk.geom[7] == 1])
+def test_correlation_plan_replay(replay_bins, geom):
+    _run(replay_bins["corr2_plan_replay"], geom)
+
+
+STRIDE2 = [
+    (2, 64, 19, 16, 64, 3, 3, 2, 0, 1, 0, 1, 1, 1),         # asymmetric pads
+    (2, 32, 15, 15, 64, 5, 5, 2, 2, 2, 2, 2, 1, 2),
+    (1, 48, 13, 17, 32, 3, 3, 2, 1, 1, 1, 1, 1, 1),
+    (2, 16, 12, 12, 32, 3, 3, 2, 2, 2, 2, 2, 2, 1),         # dilation 2
+]
+
+
+@pytest.mark.parametrize("geom", STRIDE2 + [wk.geom for wk in wl.WORKLOADS.values() if wk.geom[7] == 2]
+                         + [wk.geom for wk in wl.model_zoo(2).values() if wk.geom[7] == 2])
+def test_stride2_weight_gradient_plan_replay(replay_bins, geom):
+    _run(replay_bins["wgrad_phase_replay"], geom)
