@@ -28,7 +28,7 @@ def replay_bins(tmp_path_factory):
         pytest.skip("nvcc not available")
     out = tmp_path_factory.mktemp("replay")
     bins = {}
-    for name in ("corr2_plan_replay", "wgrad_phase_replay"):
+    for name in ("corr2_plan_replay", "wgrad_phase_replay", "thin3_plan_replay"):
         exe = str(out / name)
         cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O1", "-std=c++17", "-o", exe,
                os.path.join(HERE, "replay", name + ".cu"), "-lcuda"]
@@ -38,8 +38,8 @@ def replay_bins(tmp_path_factory):
     return bins
 
 
-def _run(exe, geom):
-    r = subprocess.run([exe, *map(str, geom)], capture_output=True, text=True, timeout=300)
+def _run(exe, geom, *extra):
+    r = subprocess.run([exe, *map(str, geom), *map(str, extra)], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0 and "errors: 0" in r.stdout, (geom, r.stdout[-2000:])
 
 
@@ -73,3 +73,19 @@ STRIDE2 = [
                          + [wk.geom for wk in wl.model_zoo(2).values() if wk.geom[7] == 2])
 def test_stride2_weight_gradient_plan_replay(replay_bins, geom):
     _run(replay_bins["wgrad_phase_replay"], geom)
+
+
+THIN3 = [
+    (2, 16, 10, 10, 16, 3, 3, 1, 1, 1, 1, 1, 1, 16),        # depthwise
+    (2, 32, 12, 12, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8),         # 4 channels per group
+    (3, 12, 13, 9, 12, 3, 3, 1, 1, 0, 2, 1, 1, 3),          # asymmetric pads, ragged
+    (1, 6, 5, 30, 6, 3, 3, 1, 2, 2, 0, 0, 1, 3),            # pads 2, wide rows
+    (4, 64, 7, 7, 64, 3, 3, 1, 1, 1, 1, 1, 1, 64),          # small planes, several groups per block
+]
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("geom", THIN3 + [wk.geom for wk in wl.WORKLOADS.values() if wk.geom[5:8] == (3, 3, 1)]
+                         + [wk.geom for wk in wl.model_zoo(32).values() if wk.geom[7] == 1])
+def test_thin_3x3_plan_replay(replay_bins, geom, dtype):
+    _run(replay_bins["thin3_plan_replay"], geom, dtype)
