@@ -1,0 +1,110 @@
+// CPU replay of the stride-1 weight-gradient launch plan and index arithmetic for one
+// geometry: the blocked copies' reads and writes, the jobs (rows and TMEM columns), every
+// staged gradOutput and input row within its blocked buffer, every split-K partial within
+// the workspace, every tap covered by exactly one job.  Host code only (library source
+// included, device-facing helpers stubbed).  Usage: wgrad_plan_replay <14 geometry ints>;
+// exits non-zero and prints FAIL lines on a violation.
+#include "../../bwd_gconv_fwd_gb300/csrc/tc_conv.cu"
+#include <cstdio>
+#include <cstdlib>
+namespace gconv {
+long long wait_limit() { return 1000000000LL; }
+unsigned int *device_error_word() { return nullptr; }
+int forced_path() { return 0; }
+void *debug_trace(size_t *b) { *b = 0; return nullptr; }
+bool encode_rows_tmap(CUtensorMap *, const void *, uint64_t, uint64_t, uint32_t) { return false; }
+}
+using namespace gconv;
+static long errors = 0;
+#define CHECK(cond, ...) do { if (!(cond)) { if (errors++ < 10) { printf("FAIL: " __VA_ARGS__); printf("\n"); } } } while (0)
+int main(int argc, char **argv)
+{
+    int v[14];
+    for (int i = 0; i < 14; ++i) v[i] = atoi(argv[1 + i]);
+    const int span_h = v[2] + v[8] + v[9] - v[12] * (v[5] - 1) - 1, span_w = v[3] + v[10] + v[11] - v[12] * (v[6] - 1) - 1;
+    Geom g{v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], v[8], v[9], v[10], v[11], v[12], v[13], span_h / v[7] + 1,
+           span_w / v[7] + 1, v[1] / v[13], v[4] / v[13]};
+    WgradLaunch L;
+    if (!build_wgrad(g, &L)) { printf("not served by this path\nerrors: 0\n"); return 0; }
+    printf("Ho=%d Wo=%d grid=%d smem=%zu ws=%zu\n", g.Ho, g.Wo, L.grid, L.smem, L.ws_bytes);
+    CHECK(L.smem <= kMaxSmem, "shared memory %zu", L.smem);
+    // blocked copies: every source element inside x / gradOutput, every row inside its buffer
+    for (int which = 0; which < 2; ++which) {
+        const BlockifyParams &p = which ? L.by : L.bx;
+        const size_t dst_bytes = which ? L.yt_bytes : L.xt_bytes;
+        const size_t src_elems = which ? (size_t)g.N * g.Cout * g.Ho * g.Wo : (size_t)g.N * g.Cin * g.H * g.W;
+        const int plane_out = p.R * p.C;
+        const int64_t total = (int64_t)p.N * p.G * p.nchunk * plane_out;
+        CHECK((size_t)total * 128 <= dst_bytes, "blocked copy %d: %lld rows > buffer", which, (long long)total);
+        for (int64_t q = 0; q < total; q += 7) {
+            const int64_t blk = q / plane_out;
+            const int pos = (int)(q - blk * plane_out);
+            const int r = pos / p.C, c = pos - r * p.C;
+            const int j = (int)(blk % p.nchunk);
+            const int64_t ng = blk / p.nchunk;
+            const int row = r + p.r_off, col = c + p.c_off;
+            const bool inside = row >= 0 && row < p.IH && col >= 0 && col < p.IW;
+            const int cvalid = inside ? std::min(64, p.Cg - 64 * j) : 0;
+            const int64_t plane = (int64_t)p.IH * p.IW;
+            const int64_t base = (ng * p.Cg + 64 * j) * plane + (inside ? (int64_t)row * p.IW + col : 0);
+            for (int e = 0; e < cvalid; ++e) CHECK((size_t)(base + e * plane) < src_elems, "blocked copy %d source", which);
+        }
+    }
+    const size_t xt_elems = L.xt_bytes / 2, yt_elems = L.yt_bytes / 2, part_elems = L.part_bytes / 4;
+    std::vector<int> tap_seen(g.kH * g.kW, 0);
+    {
+        const WgradParams &p = L.wp;
+        const size_t xoff = 0;
+        printf(" groups %d splits %d\n", p.n_tgrp, p.splits);
+        for (int gi = 0; gi < p.n_tgrp; ++gi)
+            for (int jb = p.grp_first[gi]; jb < p.grp_first[gi + 1]; ++jb) {
+                printf("   grp %d job off %d delta %d count %d taps %d %d %d %d\n", gi, p.job_off[jb], p.job_delta[jb], p.job_count[jb],
+                       p.job_tapk[jb][0], p.job_tapk[jb][1], p.job_tapk[jb][2], p.job_tapk[jb][3]);
+                for (int c = 0; c < p.job_count[jb]; ++c) tap_seen[p.job_tapk[jb][c]]++;
+                CHECK(p.job_off[jb] + (p.job_count[jb] - 1) * p.job_delta[jb] + 128 <= p.plane_elems, "B rows");
+                CHECK(p.job_col[jb] + p.job_count[jb] * 64 <= p.grp_cols[gi] && p.grp_cols[gi] <= 512, "cols");
+            }
+        for (int cta = 0; cta < L.grid; ++cta) {
+            int t = cta;
+            const int r = t % p.cta_per_cg; t /= p.cta_per_cg;
+            const int ct = t % p.n_ctile; t /= p.n_ctile;
+            const int ot = t % p.n_otile;
+            const int gg = t / p.n_otile;
+            int gi = 0;
+            while (gi + 1 < p.n_tgrp && r >= p.grp_cta0[gi + 1]) ++gi;
+            const int split = r - p.grp_cta0[gi];
+            const int total_tiles = p.N * p.n_rowblk;
+            const int tps = (total_tiles + p.grp_splits[gi] - 1) / p.grp_splits[gi];
+            const int tile0 = split * tps, tile1 = std::min(total_tiles, tile0 + tps);
+            const int plane_y = p.Ho * p.Wp, plane_x = p.Rx * p.Wp, th_pos = p.TH * p.Wp;
+            for (int it = tile0; it < tile1; ++it) {
+                const int rb = it / p.N, n = it - rb * p.N;
+                const int pos0 = rb * p.TH * p.Wp;
+                for (int h = 0; h < 2; ++h)
+                    for (int m = 0; m < 128; ++m) {
+                        const int chunk = 2 * ot + h;
+                        if (m < th_pos && pos0 + m < plane_y && chunk < p.ncy) {
+                            const int64_t e = ((((int64_t)n * p.G + gg) * p.ncy + chunk) * plane_y + pos0 + m) * 64 + 56;
+                            CHECK((size_t)(e + 8) <= yt_elems, "dy src");
+                        }
+                    }
+                for (int m = 0; m < p.plane_elems; ++m)
+                    if (pos0 + m < plane_x) {
+                        const int64_t e = ((((int64_t)n * p.G + gg) * p.ncx + ct) * plane_x + pos0 + m) * 64 + 56;
+                        CHECK(xoff + (size_t)(e + 8) <= xt_elems, "x src");
+                    }
+            }
+            for (int jb = p.grp_first[gi]; jb < p.grp_first[gi + 1]; ++jb)
+                for (int j = 0; j < p.job_count[jb]; ++j)
+                    for (int o = 0; o < std::min(128, p.Cgo - ot * 128); ++o) {
+                        const int64_t e = (int64_t)split * ((int64_t)p.G * p.Cgo * p.Cgi * p.kHW) +
+                                          ((int64_t)p.job_tapk[jb][j] * p.G * p.Cgo + gg * p.Cgo + ot * 128 + o) * p.Cgi + ct * 64 +
+                                          std::min(64, p.Cgi - ct * 64) - 1;
+                        CHECK((size_t)e < part_elems, "part");
+                    }
+        }
+    }
+    for (int k = 0; k < g.kH * g.kW; ++k) CHECK(tap_seen[k] == 1, "tap %d covered %d times", k, tap_seen[k]);
+    printf("errors: %ld\n", errors);
+    return errors ? 1 : 0;
+}

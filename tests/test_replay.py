@@ -1,6 +1,6 @@
 """CPU replays of the tensor-core launches' host planning and index arithmetic.
 
-The two programs under tests/replay/ include the library source, rebuild the launch
+The programs under tests/replay/ include the library source, rebuild the launch
 parameters the library would use for a geometry, and walk every tile's reads and writes
 on the host, checking them against the buffers' extents (bounds are checked by reading
 the index arithmetic, not by running a possibly faulting kernel).  They need nvcc (to
@@ -28,7 +28,7 @@ def replay_bins(tmp_path_factory):
         pytest.skip("nvcc not available")
     out = tmp_path_factory.mktemp("replay")
     bins = {}
-    for name in ("corr2_plan_replay", "wgrad_phase_replay", "thin3_plan_replay"):
+    for name in ("corr2_plan_replay", "wgrad_plan_replay", "wgrad_phase_replay", "thin3_plan_replay"):
         exe = str(out / name)
         cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O1", "-std=c++17", "-o", exe,
                os.path.join(HERE, "replay", name + ".cu"), "-lcuda"]
@@ -59,6 +59,12 @@ STRIDE1 = [
                          + [wk.geom for wk in wl.model_zoo(2).values() if wk.geom[7] == 1])
 def test_correlation_plan_replay(replay_bins, geom):
     _run(replay_bins["corr2_plan_replay"], geom)
+
+
+@pytest.mark.parametrize("geom", STRIDE1 + [wk.geom for wk in wl.WORKLOADS.values() if wk.geom[7] == 1]
+                         + [wk.geom for wk in wl.model_zoo(2).values() if wk.geom[7] == 1])
+def test_weight_gradient_plan_replay(replay_bins, geom):
+    _run(replay_bins["wgrad_plan_replay"], geom)
 
 
 STRIDE2 = [
