@@ -205,9 +205,9 @@ size_t gconv_noalloc_scratch_bytes(void);
  * `stream`; the passes run on `stream`; inputs and results move on copy
  * streams the library creates per device on first use (host-to-device and
  * device-to-host), so that a pass's result copies out while the next passes run
- * and gradOutput copies in while the forward pass runs.  The forward pass may run in batch
- * chunks (each chunk's result copies out as soon as it is done); its result is the
- * same, bit for bit, as one gconv_fwd call over the whole batch.
+ * and gradOutput copies in while the forward pass runs.  The forward pass may run
+ * in batch chunks (each chunk's result copies out as soon as it is done); its
+ * result is the same, bit for bit, as one gconv_fwd call over the whole batch.
  * When `stream` reaches the point after this call, every host output has been
  * written.  Concurrent calls from several host threads are serialised while
  * they enqueue.
