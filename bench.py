@@ -25,9 +25,11 @@ import glob
 import hashlib
 import json
 import os
+import shutil
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -106,8 +108,8 @@ class ClockSampler:
 
     def __enter__(self):
         try:
-            out_dir = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp"
-            self.path = os.path.join(out_dir, f"clocks_{os.getpid()}.csv")
+            self.tmpdir = tempfile.mkdtemp(prefix="gconv_clocks_")
+            self.path = os.path.join(self.tmpdir, "clocks.csv")
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                                           "-i", str(self.gpu_index), "-lms", "100"], stdout=self.fh,
@@ -139,6 +141,7 @@ class ClockSampler:
                 rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
             except ValueError:
                 continue
+        shutil.rmtree(self.tmpdir, ignore_errors=True)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         smax = max(r[1] for r in rows)
@@ -231,7 +234,7 @@ def bench_reference(args):
 
 def config_dict(wk):
     N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = wk.geom
-    return {"workload": f"{wk.name}: x[{N},{Cin},{H},{W}] bf16, w[{Cout},{Cin // G},{kH},{kW}], groups {G}, "
+    return {"workload": f"{wk.name}: x[{N},{Cin},{H},{W}] {wk.dtype}, w[{Cout},{Cin // G},{kH},{kW}], groups {G}, "
                         f"stride {s}, pads {pt}/{pb}/{pl}/{pr}, dilation {d}; fp32 outputs",
             "step": "fwd + bwd_data + bwd_weight + bwd_bias", "N": N, "C_in": Cin, "H": H, "W": W,
             "C_out": Cout, "kH": kH, "kW": kW, "groups": G, "stride": s, "pads": [pt, pb, pl, pr],
@@ -350,6 +353,8 @@ def bench_gpu(args):
         assert torch.equal(host_t, dev_t.cpu()), "host-buffer step disagrees with the device passes"
 
     launch_bound = time_launch_bound(dev)
+    peaks, peak_src = load_peaks()
+    configs = None if args.no_configs or world > 1 else bench_configs(dev, peaks, peak_src)
 
     if world > 1:
         torch.distributed.barrier()
@@ -357,7 +362,6 @@ def bench_gpu(args):
         return 0
 
     # ---- roofline of the dominant pass ----
-    peaks, peak_src = load_peaks()
     avg = {nm: statistics.mean(v) for nm, v in per_pass.items()}
     dom = max(avg, key=avg.get)
     abytes = algorithmic_bytes(geom)
@@ -398,6 +402,7 @@ def bench_gpu(args):
                 "ms_per_step": e2e_ms / e2e_steps},
         "gpu_launches": launches_per_step * args.steps,
         "launch_bound": launch_bound,
+        "configs": configs,
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
@@ -465,63 +470,119 @@ def time_launch_bound(dev, reps=200):
             "us_per_step_graph": us_graph, "launches_per_step": sum(gc.gconv_plan(geom, dt, p)[1] for p in range(4))}
 
 
+FP32_FMA_PER_SM_CLK = 128          # FP32 FMA lanes per SM per clock (4 SMSPs x 32)
+
+
+def fp32_peak_tflops(peaks):
+    """FP32 FMA peak of the CUDA-core kernels: SMs x 128 FMA lanes x 2 FLOP x max SM clock."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return sms * FP32_FMA_PER_SM_CLK * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+
+
+def time_workload(wk, dev, reps, warmup, flush, peaks):
+    """Per-pass timing of one workload: CUDA events on the current stream around each call, L2
+    flushed before every call, median of `reps` after `warmup`.  Returns the passes' records."""
+    import torch
+    import bwd_gconv_fwd_gb300 as gc
+    from bwd_gconv_fwd_gb300 import binding as B
+    from bwd_gconv_fwd_gb300 import workloads as wl
+    geom = wk.geom
+    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+    Ho, Wo = wl.out_hw(geom)
+    st = torch.cuda.current_stream(dev)
+    sp = st.cuda_stream
+    dt = B.GCONV_BF16 if wk.dtype == "bf16" else B.GCONV_F32
+    x, w, b, dy = (t.to(dev) for t in wl.make_inputs(wk))
+    y = torch.empty((N, Cout, Ho, Wo), device=dev)
+    dx = torch.empty((N, Cin, H, W), device=dev)
+    dw = torch.empty(tuple(w.shape), device=dev)
+    db = torch.empty((Cout,), device=dev)
+    wsb = max(16, max(gc.gconv_workspace_size(geom, dt, p) for p in range(4)))
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    calls = {
+        "fwd": lambda: B.gconv_fwd_ptr(geom, dt, x.data_ptr(), w.data_ptr(), b.data_ptr(), y.data_ptr(), ws.data_ptr(), wsb, sp),
+        "bwd_data": lambda: B.gconv_bwd_data_ptr(geom, dt, dy.data_ptr(), w.data_ptr(), dx.data_ptr(), ws.data_ptr(), wsb, sp),
+        "bwd_weight": lambda: B.gconv_bwd_weight_ptr(geom, dt, x.data_ptr(), dy.data_ptr(), dw.data_ptr(), ws.data_ptr(), wsb, sp),
+        "bwd_bias": lambda: B.gconv_bwd_bias_ptr(geom, dt, dy.data_ptr(), db.data_ptr(), ws.data_ptr(), wsb, sp),
+    }
+    in_bytes = 2 if wk.dtype == "bf16" else 4
+    fpp = flop_per_pass(geom)
+    abytes = algorithmic_bytes(geom, in_bytes)
+    hbm = peaks["hbm_gbs"] * 1e9
+    out = {}
+    for i, (nm, f) in enumerate(calls.items()):
+        times = []
+        for k in range(warmup + reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            f()
+            e1.record(st)
+            e1.synchronize()
+            if k >= warmup:
+                times.append(e0.elapsed_time(e1) * 1e-3)
+        t = statistics.median(times)
+        path, launches = gc.gconv_plan(geom, dt, i)
+        pname = gc.PATH_NAMES[path]
+        t_mem = abytes[nm] / hbm
+        if nm == "bwd_bias":
+            t_cmp, unit_peak = 0.0, None
+        elif pname in ("tc_igemm", "tc_fc"):
+            t_cmp, unit_peak = fpp / (peaks["bf16_tflops"] * 1e12), "bf16 tensor (measured burst)"
+        else:
+            t_cmp, unit_peak = fpp / (fp32_peak_tflops(peaks) * 1e12), "fp32 FMA (derived)"
+        out[nm] = {"us": t * 1e6, "path": pname, "launches": launches,
+                   "tflops": (fpp / t / 1e12) if nm != "bwd_bias" else None,
+                   "gbs": abytes[nm] / t / 1e9, "hbm_frac": abytes[nm] / t / hbm,
+                   "bound": "hbm" if t_mem >= t_cmp else ("tensor" if unit_peak.startswith("bf16") else "fp32"),
+                   "roofline_us": max(t_mem, t_cmp) * 1e6, "roofline_frac": max(t_mem, t_cmp) / t}
+    assert gc.gconv_check_device_error(st) == B.GCONV_OK
+    step_us = sum(v["us"] for v in out.values())
+    roof_us = sum(v["roofline_us"] for v in out.values())
+    return {"passes": out, "step_us": step_us, "step_tflops": 3 * fpp / (step_us * 1e-6) / 1e12,
+            "step_roofline_frac": roof_us / step_us, "gflop_per_pass": fpp / 1e9}
+
+
+# The other configurations of the metric, each timed pass by pass (c1 also as a graph, in
+# `launch_bound`); the headline line times the AlexNet-style layer.
+CONFIGS = [("c1", "tiny_g5"), ("c3", "fc_mode"), ("c3_ones", "fc_mode_ones_x"), ("c4", "dense3x3"),
+           ("c4b", "dense3x3_s2_asym"), ("c5", "resnext_g32"), ("c5b", "depthwise")]
+
+
+def bench_configs(dev, peaks, peak_src, reps=10, warmup=3):
+    import torch
+    from bwd_gconv_fwd_gb300 import workloads as wl
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    out = {}
+    for key, name in CONFIGS:
+        wk = wl.WORKLOADS[name]
+        rec = time_workload(wk, dev, reps, warmup, flush, peaks)
+        rec["workload"] = config_dict(wk)["workload"]
+        out[key] = rec
+        torch.cuda.empty_cache()
+    out["_timing"] = (f"per pass: median of {reps} calls after {warmup} warm-up calls, CUDA events on the "
+                      f"launch stream, L2 flushed by a 256 MiB write before every call; roofline per pass = "
+                      f"max(algorithmic bytes / HBM, FLOP / peak of the unit the path uses); peaks {peak_src}")
+    return out
+
+
 def bench_sweep(args):
     """--sweep: per-pass timing of the model-zoo layer sweep (ResNeXt-50 32x4d grouped 3x3,
     MobileNet-v2 depthwise 3x3) at batch 32; one JSON line per layer.  CUDA events on one
     stream, L2 flushed before each pass, median of --steps repetitions after --warmup."""
     import torch
-    import bwd_gconv_fwd_gb300 as gc
-    from bwd_gconv_fwd_gb300 import binding as B
     from bwd_gconv_fwd_gb300 import workloads as wl
-
+    from bwd_gconv_fwd_gb300 import build
+    build.build()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    st = torch.cuda.current_stream(dev)
-    sp = st.cuda_stream
-    dt = B.GCONV_BF16
     for name, wk in wl.model_zoo(32).items():
-        geom = wk.geom
-        N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
-        Ho, Wo = wl.out_hw(geom)
-        x, w, b, dy = (t.to(dev) for t in wl.make_inputs(wk))
-        y = torch.empty((N, Cout, Ho, Wo), device=dev)
-        dx = torch.empty((N, Cin, H, W), device=dev)
-        dw = torch.empty(tuple(w.shape), device=dev)
-        db = torch.empty((Cout,), device=dev)
-        wsb = max(16, max(gc.gconv_workspace_size(geom, dt, p) for p in range(4)))
-        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-        calls = {
-            "fwd": lambda: B.gconv_fwd_ptr(geom, dt, x.data_ptr(), w.data_ptr(), b.data_ptr(), y.data_ptr(), ws.data_ptr(), wsb, sp),
-            "bwd_data": lambda: B.gconv_bwd_data_ptr(geom, dt, dy.data_ptr(), w.data_ptr(), dx.data_ptr(), ws.data_ptr(), wsb, sp),
-            "bwd_weight": lambda: B.gconv_bwd_weight_ptr(geom, dt, x.data_ptr(), dy.data_ptr(), dw.data_ptr(), ws.data_ptr(), wsb, sp),
-            "bwd_bias": lambda: B.gconv_bwd_bias_ptr(geom, dt, dy.data_ptr(), db.data_ptr(), ws.data_ptr(), wsb, sp),
-        }
-        fpp = flop_per_pass(geom)
-        abytes = algorithmic_bytes(geom)
-        out = {}
-        for nm, f in calls.items():
-            times = []
-            for k in range(args.warmup + args.steps):
-                flush.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(st)
-                f()
-                e1.record(st)
-                e1.synchronize()
-                if k >= args.warmup:
-                    times.append(e0.elapsed_time(e1) * 1e-3)
-            t = statistics.median(times)
-            path, launches = gc.gconv_plan(geom, dt, list(calls).index(nm))
-            t_roof = abytes[nm] / (peaks["hbm_gbs"] * 1e9)
-            if nm != "bwd_bias":
-                t_roof = max(t_roof, fpp / (peaks["bf16_tflops"] * 1e12))
-            out[nm] = {"us": t * 1e6, "path": gc.PATH_NAMES[path], "launches": launches,
-                       "gbs": abytes[nm] / t / 1e9, "roofline_frac": t_roof / t}
-        assert gc.gconv_check_device_error(st) == B.GCONV_OK
-        print(json.dumps({"sweep": name, "geom": list(geom), "gflop_per_pass": fpp / 1e9, "passes": out,
-                          "peak_source": peak_src}), flush=True)
+        rec = time_workload(wk, dev, args.steps, args.warmup, flush, peaks)
+        print(json.dumps({"sweep": name, "geom": list(wk.geom), "gflop_per_pass": rec["gflop_per_pass"],
+                          "passes": rec["passes"], "peak_source": peak_src}), flush=True)
     return 0
 
 
@@ -533,6 +594,7 @@ def main():
     ap.add_argument("--impl", default="gconv", choices=["gconv", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config pass timings")
     ap.add_argument("--sweep", action="store_true", help="time the model-zoo layer sweep instead")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps, whatever is asked

@@ -663,7 +663,7 @@ bool launch_conv3_t(const Conv3Params &p, size_t smem, cudaStream_t s)
     // one tile per block keeps more blocks resident for the light single-channel form;
     // the four-channel form walks tiles persistently
     const int64_t ntiles = (int64_t)p.N * p.n_gb * p.n_th * p.n_tw;
-    const unsigned grid = (unsigned)(CO >= 4 ? std::min<int64_t>(ntiles, (int64_t)kNumSMs * 8) : ntiles);
+    const unsigned grid = (unsigned)(CO >= 4 ? std::min<int64_t>(ntiles, (int64_t)num_sms() * 8) : ntiles);
     conv3_s1_kernel<T, CO, BX><<<grid, kTT, smem, s>>>(p);
     return true;
 }
@@ -885,7 +885,7 @@ bool plan_wgrad3(const Geom &g, TileGeom *t, size_t *smem, int *CIpx, int *CIpy)
     t->n_th = (g.Ho + t->TH - 1) / t->TH;
     t->n_tw = (g.Wo + t->TW - 1) / t->TW;
     const int64_t spatial = (int64_t)g.G * t->n_th * t->n_tw;
-    int n_nb = (int)std::max<int64_t>(1, std::min<int64_t>(g.N, (4 * (int64_t)kNumSMs * 4 + spatial - 1) / spatial));
+    int n_nb = (int)std::max<int64_t>(1, std::min<int64_t>(g.N, (4 * (int64_t)num_sms() * 4 + spatial - 1) / spatial));
     // small planes: fewer, larger image chunks, so that a block has about L (image, block)
     // items, staged several images at a time
     const int nblk = (t->TH / 4) * (t->TW / 4);
@@ -1004,7 +1004,7 @@ bool plan_bwd_weight(const Geom &g, TileGeom *t, size_t *smem)
     t->n_tw = (g.Wo + t->TW - 1) / t->TW;
     // images per block: about four waves of blocks
     const int64_t spatial = (int64_t)g.G * t->n_th * t->n_tw;
-    int n_nb = (int)std::max<int64_t>(1, std::min<int64_t>(g.N, (4 * (int64_t)kNumSMs * 4 + spatial - 1) / spatial));
+    int n_nb = (int)std::max<int64_t>(1, std::min<int64_t>(g.N, (4 * (int64_t)num_sms() * 4 + spatial - 1) / spatial));
     t->NB = (g.N + n_nb - 1) / n_nb;
     t->n_nb = (g.N + t->NB - 1) / t->NB;
     return true;
@@ -1030,7 +1030,7 @@ gconv_status launch_typed(const Geom &g, const Plan &, gconv_pass pass, const vo
     }
     if (pass == GCONV_PASS_FWD) {
         if (!plan_fwd(g, &t, &smem)) return GCONV_ERR_UNSUPPORTED;
-        const int grid = (int)std::min<int64_t>((int64_t)g.N * g.G * t.n_th * t.n_tw, (int64_t)kNumSMs * 8);
+        const int grid = (int)std::min<int64_t>((int64_t)g.N * g.G * t.n_th * t.n_tw, (int64_t)num_sms() * 8);
         const T *bi = static_cast<const T *>(bias);
         const bool k3 = g.kH == 3 && g.kW == 3;
 #define GCONV_FWD_TILED(CO)                                                                          \
@@ -1048,7 +1048,7 @@ gconv_status launch_typed(const Geom &g, const Plan &, gconv_pass pass, const vo
     }
     if (pass == GCONV_PASS_BWD_DATA) {
         if (!plan_bwd_data(g, &t, &smem)) return GCONV_ERR_UNSUPPORTED;
-        const int grid = (int)std::min<int64_t>((int64_t)g.N * g.G * t.n_th * t.n_tw, (int64_t)kNumSMs * 8);
+        const int grid = (int)std::min<int64_t>((int64_t)g.N * g.G * t.n_th * t.n_tw, (int64_t)num_sms() * 8);
         const bool k3 = g.kH == 3 && g.kW == 3;
 #define GCONV_BWD_DATA_TILED(CI_)                                                                    \
         if (k3) bwd_data_tiled_kernel<T, CI_, 3><<<grid, kTT, smem, s>>>(g, t, A, B, out);           \

@@ -30,6 +30,25 @@ unsigned int *device_error_word()
     return cache[dev];
 }
 
+int num_sms()
+{
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();   // no device: keep the host-only planning deterministic
+        return 152;
+    }
+    if (!cache[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = 152;
+        }
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 static int g_force_path = GCONV_PATH_NONE;
 static long long g_wait_limit = -1;
 static void *g_trace = nullptr;
@@ -72,7 +91,7 @@ gconv_status make_geom(int N, int C_in, int H, int W, int C_out, int kH, int kW,
 static int elementwise_grid(int64_t total)
 {
     const int64_t blocks = (total + kDirectThreads - 1) / kDirectThreads;
-    return (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)kNumSMs * 16));
+    return (int)std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)num_sms() * 16));
 }
 
 // ---- CUDA-core plans ------------------------------------------------------
@@ -80,7 +99,7 @@ static int elementwise_grid(int64_t total)
 static void direct_weight_split(const Geom &g, int *splits, int64_t *per_split)
 {
     const int64_t P = (int64_t)g.N * g.Ho * g.Wo;
-    int64_t S = (4 * kNumSMs + g.Cout - 1) / g.Cout;
+    int64_t S = (4 * num_sms() + g.Cout - 1) / g.Cout;
     S = std::max<int64_t>(1, std::min<int64_t>(S, P / 2048));
     int64_t per = (P + S - 1) / S;
     per = std::max<int64_t>(per, 1);
@@ -107,7 +126,7 @@ static void bias_plan(const Geom &g, gconv_dtype dt, Plan *p)
     const bool vec = (L * esize) % 16 == 0;
     const int64_t threads = vec ? L / (16 / esize) : L;
     // about two resident waves of threads, but at least 8 rows per split
-    int64_t S = (2 * (int64_t)kNumSMs * 2048 + threads - 1) / threads;
+    int64_t S = (2 * (int64_t)num_sms() * 2048 + threads - 1) / threads;
     S = std::max<int64_t>(1, std::min<int64_t>(S, std::max(1, g.N / 8)));
     const int rows = (int)((g.N + S - 1) / S);
     p->tc[0] = 1;
@@ -183,7 +202,7 @@ static void launch_direct(const Geom &g, const Plan &p, gconv_pass pass, const v
         if (p.tc[0] == 0) {
             const int64_t nplanes = (int64_t)g.N * g.Cout;
             const int64_t blocks = (nplanes + kDirectThreads / 32 - 1) / (kDirectThreads / 32);
-            plane_sum_kernel<T><<<(int)std::min<int64_t>(blocks, (int64_t)kNumSMs * 32), kDirectThreads, 0, st>>>(
+            plane_sum_kernel<T><<<(int)std::min<int64_t>(blocks, (int64_t)num_sms() * 32), kDirectThreads, 0, st>>>(
                 A, nplanes, HW, part);
             bias_finish_kernel<<<fin_grid, kDirectThreads, 0, st>>>(part, g.N, g.Cout, 1, g.Cout, out);
         } else {
@@ -199,6 +218,19 @@ static void launch_direct(const Geom &g, const Plan &p, gconv_pass pass, const v
     }
 }
 
+// An empty batch (N == 0): y and dx have no elements, dw and db are sums over no terms,
+// so they are set to zero (the output pointer may then be NULL only if nothing is written).
+static gconv_status zero_empty_sum(const Geom &g, gconv_pass pass, float *out, void *stream)
+{
+    size_t n = 0;
+    if (pass == GCONV_PASS_BWD_WEIGHT) n = (size_t)g.Cout * g.Cgi * g.kH * g.kW;
+    else if (pass == GCONV_PASS_BWD_BIAS) n = (size_t)g.Cout;
+    if (n == 0) return GCONV_OK;
+    if (!out) return GCONV_ERR_INVALID_ARG;
+    return cudaMemsetAsync(out, 0, n * sizeof(float), static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GCONV_OK : GCONV_ERR_CUDA;
+}
+
 // One entry point body for all four passes.  a/b are the pass's two inputs in
 // ABI order (fwd: x, w; bwd_data: dy, w; bwd_weight: x, dy; bias: dy, unused).
 static gconv_status run_pass(const int *geo, gconv_dtype dt, gconv_pass pass, const void *a,
@@ -210,7 +242,7 @@ static gconv_status run_pass(const int *geo, gconv_dtype dt, gconv_pass pass, co
                                 geo[8], geo[9], geo[10], geo[11], geo[12], geo[13], &g);
     if (st != GCONV_OK) return st;
     if (dt != GCONV_F32 && dt != GCONV_BF16) return GCONV_ERR_INVALID_ARG;
-    if (g.N == 0) return GCONV_OK;
+    if (g.N == 0) return zero_empty_sum(g, pass, out, stream);
     const bool need_b = pass != GCONV_PASS_BWD_BIAS;
     if (!a || !out || (need_b && !b)) return GCONV_ERR_INVALID_ARG;
     if (!aligned16(a) || !aligned16(out) || (need_b && !aligned16(b)) || (bias && !aligned16(bias)))
@@ -344,7 +376,12 @@ static int fwd_chunks(const Geom &g, gconv_dtype dt, size_t ws_bytes)
 {
     if (g.N < kFwdChunks * kFwdChunkMinN) return 1;
     const Plan whole = plan_pass(g, dt, GCONV_PASS_FWD);
+    const size_t x_img = (size_t)g.Cin * g.H * g.W * (dt == GCONV_BF16 ? 2 : 4);
+    const size_t y_img = (size_t)g.Cout * g.Ho * g.Wo * 4;
     for (int c = 0; c < kFwdChunks; ++c) {
+        // every chunk's x and y must start on a 16-byte boundary (the passes require it)
+        const size_t n0 = (size_t)(c * g.N / kFwdChunks);
+        if ((n0 * x_img) % 16 || (n0 * y_img) % 16) return 1;
         Geom gc = g;
         gc.N = (c + 1) * g.N / kFwdChunks - c * g.N / kFwdChunks;
         const Plan part = plan_pass(gc, dt, GCONV_PASS_FWD);
@@ -438,7 +475,7 @@ gconv_status gconv_bwd_weight_noalloc(GEO_ARGS, gconv_dtype dtype, const void *x
                                 dilation, groups, &g);
     if (st != GCONV_OK) return st;
     if (dtype != GCONV_F32 && dtype != GCONV_BF16) return GCONV_ERR_INVALID_ARG;
-    if (g.N == 0) return GCONV_OK;
+    if (g.N == 0) return zero_empty_sum(g, GCONV_PASS_BWD_WEIGHT, dw, stream);
     const Plan p = plan_pass(g, dtype, GCONV_PASS_BWD_WEIGHT);
     if (p.path < 0) return GCONV_ERR_UNSUPPORTED;
     if (p.ws_bytes > kNoAllocScratchBytes) return GCONV_ERR_WORKSPACE;   // beyond the fixed 128 MiB scratch
@@ -502,11 +539,21 @@ gconv_status gconv_step_host(GEO_ARGS, gconv_dtype dtype, const void *x, const v
     if (st != GCONV_OK) return st;
     if (dtype != GCONV_F32 && dtype != GCONV_BF16) return GCONV_ERR_INVALID_ARG;
     if (!x || !w || !dy || !y || !dx || !dw || !db) return GCONV_ERR_INVALID_ARG;
-    if (g.N == 0) return GCONV_OK;
     StepLayout L;
     if (!step_layout(g, dtype, bias != nullptr, &L)) return GCONV_ERR_UNSUPPORTED;
     if (!device_buffer || device_bytes < L.total) return GCONV_ERR_WORKSPACE;
     if (!aligned16(device_buffer)) return GCONV_ERR_INVALID_ARG;
+    if (g.N == 0) {
+        // y and dx are empty; dw and db are sums over no terms: zeros, delivered in stream order
+        cudaStream_t C = static_cast<cudaStream_t>(stream);
+        uint8_t *base = static_cast<uint8_t *>(device_buffer);
+        if (cudaMemsetAsync(base + L.dw, 0, L.ndw, C) != cudaSuccess ||
+            cudaMemsetAsync(base + L.db, 0, L.ndb, C) != cudaSuccess ||
+            cudaMemcpyAsync(dw, base + L.dw, L.ndw, cudaMemcpyDeviceToHost, C) != cudaSuccess ||
+            cudaMemcpyAsync(db, base + L.db, L.ndb, cudaMemcpyDeviceToHost, C) != cudaSuccess)
+            return GCONV_ERR_CUDA;
+        return GCONV_OK;
+    }
 
     std::lock_guard<std::mutex> lock(g_step_mutex);
     StepStreams *ss = step_streams();

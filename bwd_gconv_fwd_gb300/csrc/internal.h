@@ -8,7 +8,10 @@
 
 namespace gconv {
 
-constexpr int kNumSMs = 152;                       // GB300: 2 dies x 76 SMs
+// Streaming multiprocessors of the current device (queried once per device; 152 on
+// GB300, 2 dies x 76 SMs, which is also the answer when no device can be queried, so
+// that host-only planning and workspace sizing work without a GPU).
+int num_sms();
 constexpr long long kDefaultWaitLimit = 1000000000LL; // ns before a device-side wait gives up
 
 // What one call will launch.  Filled by plan_pass; TC families fill `tc`.

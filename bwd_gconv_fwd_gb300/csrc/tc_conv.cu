@@ -620,7 +620,7 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
             const int th_pos = p.TH * p.Wp;
             const int chunks = min(2, p.ncy - 2 * ot);
             const int ncopy = 2 + p.n_xbox;
-            int last_b = -1, last_ph = 0;
+            int issued = 0;
             for (int it = tile0, k = 0, b = 0, ph = 0; it < tile1; ++it, ++k) {
                 if (k >= p.nbuf) {
                     const uint32_t eb = ptx::smem_u32(&bar_empty[b]);
@@ -649,13 +649,18 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
                                          ((n * p.G + g) * p.ncx + ct), fb);
                     }
                 }
-                last_b = b;
-                last_ph = ph;
+                issued = k + 1;
                 if (++b == p.nbuf) { b = 0; ph ^= 1; }
             }
-            // the last tile's copies must land before the CTA exits
-            if (last_b >= 0 && !ptx::mbar_wait(ptx::smem_u32(&bar_full[last_b]), (uint32_t)last_ph, kDrainNs))
-                raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
+            // no copy may land after the CTA exits: wait for every buffer still in flight (the
+            // last nbuf tiles issued; earlier ones were consumed before their buffer was reused).
+            // After an abort another producer may not have arrived on a buffer this one filled, so
+            // its phase never completes: one bounded wait then covers this thread's own copies.
+            for (int j = max(0, issued - p.nbuf); j < issued; ++j)
+                if (!ptx::mbar_wait(ptx::smem_u32(&bar_full[j % p.nbuf]), (uint32_t)((j / p.nbuf) & 1), kDrainNs)) {
+                    raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
+                    break;
+                }
         }
     } else if (warp < kStageWarps) {
         // ---------------- staging: cp.async of position rows, double buffered ----------------
@@ -1596,7 +1601,7 @@ bool size_wgrad(const Geom &g, WgradParams *wp, size_t *smem, int *grid)
     // groups in proportion to their MMA work per K step plus the staging share.
     const int outer = g.G * w.n_otile * w.n_ctile;
     const int total_tiles = g.N * w.n_rowblk;
-    const int budget = std::max(w.n_tgrp, kNumSMs / std::max(1, outer));
+    const int budget = std::max(w.n_tgrp, num_sms() / std::max(1, outer));
     std::vector<double> cost(w.n_tgrp, 0.0);
     double total_cost = 0.0;
     for (int gi = 0; gi < w.n_tgrp; ++gi) {
@@ -1744,7 +1749,7 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
     }
     if (!fit) return false;
     L->smem = std::max(L->smem, (size_t)120 * 1024);
-    L->grid = std::min(c.n_tiles, kNumSMs);
+    L->grid = std::min(c.n_tiles, num_sms());
     k.G = g.G; k.Cu = Cu; k.Cv = Cv; k.n_vtile = c.n_vtile; k.nchu = c.nchu; k.ntaps = c.ntaps;
     k.transpose = bwd_data ? 1 : 0;
     k.w_cin_g = g.Cgi; k.kHW = ntaps;
@@ -2030,7 +2035,7 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
         rp.dw = out;
         rp.O = g.Cout; rp.Cgi = g.Cgi; rp.kHW = g.kH * g.kW;
         const int64_t count = (int64_t)g.Cout * g.Cgi * g.kH * g.kW;
-        const int blocks = (int)std::min<int64_t>((count + 255) / 256, (int64_t)kNumSMs * 8);
+        const int blocks = (int)std::min<int64_t>((count + 255) / 256, (int64_t)num_sms() * 8);
         wgrad_reduce_kernel<<<blocks, 256, 0, s>>>(rp);
         return GCONV_OK;
     }
@@ -2067,7 +2072,7 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
             for (int jb = L.wp.grp_first[gi]; jb < L.wp.grp_first[gi + 1]; ++jb)
                 for (int c = 0; c < L.wp.job_count[jb]; ++c) rp.tap_splits[L.wp.job_tapk[jb][c]] = L.wp.grp_splits[gi];
         const int64_t count = (int64_t)g.Cout * g.Cgi * g.kH * g.kW;
-        const int blocks = (int)std::min<int64_t>((count + 255) / 256, (int64_t)kNumSMs * 8);
+        const int blocks = (int)std::min<int64_t>((count + 255) / 256, (int64_t)num_sms() * 8);
         wgrad_reduce_kernel<<<blocks, 256, 0, s>>>(rp);
         return GCONV_OK;
     }

@@ -96,7 +96,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             int it = 0;   // global k-block counter across tiles
             for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x) {
                 const int mb = tile % p.n_mblk, nb = tile / p.n_mblk;
-                for (int kb = 0; kb < p.n_kblk; ++kb, ++it) {
+                for (int kb = 0; kb < p.n_kblk && !abort_flag; ++kb, ++it) {
                     const int slot = it % p.stages;
                     if (it >= p.stages &&
                         !ptx::mbar_wait(ptx::smem_u32(&bar_empty[slot]), ((it / p.stages) - 1) & 1, p.wait_ns)) {
@@ -119,11 +119,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     }
                 }
             }
-            // drain: wait for the last stages' copies to land
+            // drain: wait for the last stages' copies to land.  After an abort another producer
+            // may not have arrived on a stage this one filled, so that stage never completes: one
+            // bounded wait is then enough for this thread's own copies (issued long before) to land.
             const int total = it;
             for (int j = max(0, total - p.stages); j < total; ++j)
-                if (!ptx::mbar_wait(ptx::smem_u32(&bar_full[j % p.stages]), (j / p.stages) & 1, kGemmDrainNs))
+                if (!ptx::mbar_wait(ptx::smem_u32(&bar_full[j % p.stages]), (j / p.stages) & 1, kGemmDrainNs)) {
                     raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
+                    break;
+                }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -300,7 +304,7 @@ int pick_bn(int M, int N)
     int bn = 256;
     for (int cand : {256, 192, 128}) {
         const int64_t tiles = (int64_t)mb * ((N + cand - 1) / cand);
-        const int64_t rounds = (tiles + kNumSMs - 1) / kNumSMs;
+        const int64_t rounds = (tiles + num_sms() - 1) / num_sms();
         const int64_t cost = rounds * (kBM + cand);
         if (cost < best) { best = cost; bn = cand; }
     }
@@ -366,7 +370,7 @@ gconv_status tc_fc_launch(const Geom &g, const Plan &, gconv_pass pass, const vo
     gp.stages = (int)std::min<size_t>(8, (220 * 1024 - 1024) / stage);
     const size_t smem = gp.stages * stage + 1024;
     const int tiles = gp.n_mblk * gp.n_nblk;
-    const int grid = std::min(tiles, kNumSMs);
+    const int grid = std::min(tiles, num_sms());
     static bool attr[64][3] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GCONV_ERR_CUDA;

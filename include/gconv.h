@@ -33,8 +33,11 @@
  *   N, C_in, H, W, C_out, kH, kW, stride, pad_top, pad_bottom, pad_left,
  *   pad_right, dilation, groups
  * Requirements: C_in, H, W, C_out, kH, kW, stride, dilation, groups >= 1;
- * N >= 0 (N == 0 is a successful no-op); pads >= 0; C_in and C_out divisible by
- * groups; Ho, Wo >= 1; every tensor below 2^31 elements.
+ * N >= 0; pads >= 0; C_in and C_out divisible by groups; Ho, Wo >= 1; every
+ * tensor below 2^31 elements.  N == 0 (an empty batch) launches no convolution
+ * kernel: y and dx are empty, and dw and db, being sums over no terms, are set
+ * to zero (so their pointers must be valid even then).  The host-level
+ * N == 0 pointer checks of gconv_fwd and gconv_bwd_data are skipped.
  *
  * Ownership.  The caller owns every buffer; the library allocates no device or
  * host memory and keeps no per-call state.  Device pointers must be device
@@ -242,9 +245,13 @@ const char *gconv_status_string(gconv_status status);
  * gconv_debug_force_path: route every later call to `path` where that family
  * can serve it (GCONV_PATH_NONE restores automatic choice); a family that
  * cannot serve a request makes the call return GCONV_ERR_UNSUPPORTED.
- * gconv_debug_set_wait_limit: iteration limit of device-side waits
- * (a negative value restores the default); 0 makes every bounded wait give up
- * at once, which exercises the timeout path without hanging anything. */
+ * gconv_debug_set_wait_limit: how long a device-side wait may poll before it
+ * gives up, in nanoseconds of the %globaltimer clock (default 1e9, one second;
+ * a negative value restores the default); 0 makes a wait give up after its
+ * first unsuccessful poll, which exercises the timeout path (the kernel records
+ * GCONV_ERR_TIMEOUT, drains its own copies and MMAs, frees its tensor memory and
+ * returns) without hanging anything.  Waits that drain a kernel's own in-flight
+ * work at exit keep their own one-second bound. */
 void gconv_debug_force_path(int path);
 void gconv_debug_set_wait_limit(long long limit);
 

@@ -91,9 +91,13 @@ def test_empty_batch_is_a_noop(L):
         path, launches = gc.gconv_plan(geom, B.GCONV_BF16, p)
         assert path == B.PATH_NONE and launches == 0
         assert gc.gconv_workspace_size(geom, B.GCONV_BF16, p) == 0
-    # null pointers are fine when nothing is launched
+    # nothing is read or written by the forward and backward-data passes: null pointers are fine
     assert L.gconv_fwd(*geom, 1, None, None, None, None, None, 0, None) == B.GCONV_OK
-    assert L.gconv_bwd_weight(*geom, 1, None, None, None, None, 0, None) == B.GCONV_OK
+    assert L.gconv_bwd_data(*geom, 1, None, None, None, None, 0, None) == B.GCONV_OK
+    # dw and db are sums over no terms and are written as zeros: they must be given
+    assert L.gconv_bwd_weight(*geom, 1, None, None, None, None, 0, None) == B.GCONV_ERR_INVALID_ARG
+    assert L.gconv_bwd_bias(*geom, 1, None, None, None, 0, None) == B.GCONV_ERR_INVALID_ARG
+    assert L.gconv_bwd_weight_noalloc(*geom, 1, None, None, None, None) == B.GCONV_ERR_INVALID_ARG
 
 
 def test_workspace_too_small_rejected_before_launch(L):
@@ -178,10 +182,11 @@ def test_step_host_sizing_and_argument_checks(L):
         mis = ctypes.c_void_p((1 << 20) + 8)
         assert L.gconv_step_host(*geom, dt, *full, mis, with_b, None) == B.GCONV_ERR_INVALID_ARG, name
         assert L.gconv_step_host(*geom, 9, *full, ok, with_b, None) == B.GCONV_ERR_INVALID_ARG, name
-    # empty batch: nothing to do, nothing checked past the geometry
+    # empty batch: dw and db still come back (as zeros) through the device buffer, so it is required
     geom = (0, 8, 6, 6, 8, 3, 3, 1, 1, 1, 1, 1, 1, 1)
     ok = ctypes.c_void_p(1 << 20)
-    assert L.gconv_step_host(*geom, 1, ok, ok, None, ok, ok, ok, ok, ok, None, 0, None) == B.GCONV_OK
+    assert L.gconv_step_host(*geom, 1, ok, ok, None, ok, ok, ok, ok, ok, None, 0, None) == B.GCONV_ERR_WORKSPACE
+    assert gc.gconv_step_device_bytes(geom, B.GCONV_BF16, False) >= 8 * 8 * 9 * 4 + 8 * 4
     # invalid geometry
     assert gc.binding.lib().gconv_step_device_bytes(1, 8, 6, 6, 8, 9, 9, 1, 0, 0, 0, 0, 1, 1, 1, 1) == ctypes.c_size_t(-1).value
 

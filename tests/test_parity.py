@@ -37,33 +37,69 @@ def _kw(geom):
     return dict(stride=s, padding=(pt, pb, pl, pr), dilation=d, groups=G)
 
 
+# Guard regions around every output: 4 KiB of a NaN bit pattern no kernel computes, checked
+# untouched after the call (a substitute for a memory checker, which this pool does not run).
+GUARD = 1024
+CANARY = 0x7FC0DEAD
+
+
+def guarded(shape, dev):
+    """An fp32 output of `shape` (NaN-filled, so unwritten elements show) inside a buffer whose
+    GUARD elements before and after hold CANARY; returns (output view, buffer)."""
+    n = 1
+    for v in shape:
+        n *= int(v)
+    buf = torch.full((GUARD + n + GUARD,), float("nan"), device=dev)
+    buf.view(torch.int32)[:GUARD] = CANARY
+    buf.view(torch.int32)[GUARD + n:] = CANARY
+    return buf[GUARD:GUARD + n].view(shape), buf
+
+
+def check_guards(name, buf):
+    words = buf.view(torch.int32)
+    n = buf.numel() - 2 * GUARD
+    assert bool((words[:GUARD] == CANARY).all()), f"{name}: write before the output"
+    assert bool((words[GUARD + n:] == CANARY).all()), f"{name}: write past the output"
+
+
 def run_gpu(geom, x, w, b, dy, dev, passes=("y", "dx", "dw", "db")):
-    """All four passes on the GPU; returns fp32 CPU tensors."""
+    """All four passes on the GPU; returns fp32 CPU tensors.  Every output sits between guard
+    regions that must come back untouched."""
     N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
     Ho, Wo = wl.out_hw(geom)
     kw = _kw(geom)
     xd, wd, dyd = x.to(dev), w.to(dev), dy.to(dev)
     bd = None if b is None else b.to(dev)
-    out = {}
+    out, bufs = {}, {}
     if "y" in passes:
-        y = torch.full((N, Cout, Ho, Wo), float("nan"), device=dev)
+        y, bufs["y"] = guarded((N, Cout, Ho, Wo), dev)
         gc.gconv_fwd(xd, wd, bd, y, **kw)
         out["y"] = y
     if "dx" in passes:
-        dx = torch.full((N, Cin, H, W), float("nan"), device=dev)
+        dx, bufs["dx"] = guarded((N, Cin, H, W), dev)
         gc.gconv_bwd_data(dyd, wd, dx, **kw)
         out["dx"] = dx
     if "dw" in passes:
-        dw = torch.full(tuple(w.shape), float("nan"), device=dev)
+        dw, bufs["dw"] = guarded(tuple(w.shape), dev)
         gc.gconv_bwd_weight(xd, dyd, dw, **kw)
         out["dw"] = dw
     if "db" in passes:
-        db = torch.full((Cout,), float("nan"), device=dev)
+        db, bufs["db"] = guarded((Cout,), dev)
         gc.gconv_bwd_bias(dyd, db, geom=geom)
         out["db"] = db
     torch.cuda.synchronize()
     assert gc.gconv_check_device_error() == B.GCONV_OK
+    for k, bf in bufs.items():
+        check_guards(f"{geom} {k}", bf)
     return {k: v.cpu() for k, v in out.items()}
+
+
+def assert_paths(geom, dtype, expect):
+    """The pass families the planner picks, as the test expects them (fwd, bwd_data,
+    bwd_weight, bwd_bias path codes)."""
+    dt = B.GCONV_BF16 if dtype == "bf16" else B.GCONV_F32
+    got = tuple(gc.gconv_plan(geom, dt, p)[0] for p in range(4))
+    assert got == tuple(expect), (geom, [B.PATH_NAMES[v] for v in got], [B.PATH_NAMES[v] for v in expect])
 
 
 def f64(t):
@@ -151,9 +187,20 @@ def _sampled(wk, dev, oracle_mod, n_out=6000, n_w=1500, seed=77):
     return got
 
 
+TC, FC, CC, RD = B.PATH_TC_IGEMM, B.PATH_TC_FC, B.PATH_DIRECT, B.PATH_REDUCE
+WORKLOAD_PATHS = {
+    "alexnet_g2": (TC, TC, TC, RD), "fc_mode": (FC, FC, FC, RD), "fc_mode_ones_x": (FC, FC, FC, RD),
+    "dense3x3": (TC, TC, TC, RD), "dense3x3_s2_asym": (TC, TC, TC, RD),
+    "resnext_g32": (CC, CC, CC, RD), "depthwise": (CC, CC, CC, RD),
+}
+
+
 @pytest.mark.parametrize("name", ["alexnet_g2", "fc_mode", "fc_mode_ones_x", "dense3x3",
                                   "dense3x3_s2_asym", "resnext_g32", "depthwise"])
 def test_workload_sampled(dev, oracle_mod, name):
+    """The full-size workloads in the benchmark's launch configuration, on the family the
+    benchmark times (asserted), against the oracle on sampled outputs."""
+    assert_paths(wl.WORKLOADS[name].geom, wl.WORKLOADS[name].dtype, WORKLOAD_PATHS[name])
     got = _sampled(wl.WORKLOADS[name], dev, oracle_mod)
     if name == "fc_mode_ones_x":
         # x = 1: every image gives the same y row; gradOutput = 1: every dx row is the same
@@ -167,6 +214,7 @@ def test_fc_all_ones_script_exact(dev):
     """The all-ones script of cudnn.torch issue #118 at its size: every value is an
     exactly representable integer, so the GPU must match bit for bit."""
     wk = wl.WORKLOADS["fc_mode_all_ones"]
+    assert_paths(wk.geom, wk.dtype, (FC, FC, FC, RD))
     x, w, b, dy = wl.make_inputs(wk)
     got = run_gpu(wk.geom, x, w, b, dy, dev)
     assert torch.all(got["y"] == 256 * 6 * 6 + 1)
@@ -203,13 +251,29 @@ def test_outputs_overwritten_not_accumulated(dev, oracle_mod):
     check("dw", dw.cpu().numpy(), oracle_mod.bwd_weight(geom, f64(x), f64(dy)), 1e-2)
 
 
-def test_empty_batch_noop(dev):
-    geom = (0, 8, 6, 6, 8, 3, 3, 1, 1, 1, 1, 1, 1, 1)
-    x = torch.empty((0, 8, 6, 6), dtype=torch.bfloat16, device=dev)
-    w = torch.randn((8, 8, 3, 3), device=dev).to(torch.bfloat16)
-    y = torch.empty((0, 8, 6, 6), device=dev)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_empty_batch(dev, dtype):
+    """N = 0: nothing to compute for y and dx; dw and db are sums over no terms and come
+    back as exact zeros (through every weight-gradient entry point)."""
+    geom = (0, 32, 6, 6, 32, 3, 3, 1, 1, 1, 1, 1, 1, 1)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    x = torch.empty((0, 32, 6, 6), dtype=tdt, device=dev)
+    dy = torch.empty((0, 32, 6, 6), dtype=tdt, device=dev)
+    w = torch.randn((32, 32, 3, 3), device=dev).to(tdt)
+    y = torch.empty((0, 32, 6, 6), device=dev)
+    dx = torch.empty((0, 32, 6, 6), device=dev)
     gc.gconv_fwd(x, w, None, y, padding=1)
+    gc.gconv_bwd_data(dy, w, dx, padding=1)
+    dw = torch.full((32, 32, 3, 3), float("nan"), device=dev)
+    gc.gconv_bwd_weight(x, dy, dw, padding=1)
+    dw2 = torch.full((32, 32, 3, 3), float("nan"), device=dev)
+    gc.binding.gconv_bwd_weight_noalloc(x, dy, dw2, padding=1)
+    db = torch.full((32,), float("nan"), device=dev)
+    gc.gconv_bwd_bias(dy, db, geom=geom)
     torch.cuda.synchronize()
+    assert gc.gconv_check_device_error() == B.GCONV_OK
+    for t in (dw, dw2, db):
+        assert bool((t == 0).all())
 
 
 def test_forced_direct_agrees_with_default(dev):
@@ -234,6 +298,7 @@ def test_forced_direct_agrees_with_default(dev):
     ((2, 128, 6, 6, 96, 6, 6, 1, 0, 0, 0, 0, 1, 1), "bf16", True),       # FC mode
     ((17, 32, 10, 9, 64, 3, 3, 1, 1, 1, 1, 1, 1, 2), "bf16", True),      # forward in four batch chunks, ragged
     ((16, 16, 8, 8, 16, 3, 3, 1, 1, 1, 1, 1, 1, 4), "f32", True),        # chunks on the CUDA-core path
+    ((18, 3, 7, 7, 8, 3, 3, 1, 0, 0, 0, 0, 1, 1), "bf16", True),         # 294-byte images: chunks would misalign
 ])
 def test_step_host_matches_device_passes(dev, oracle_mod, geom, dtype, with_bias):
     """gconv_step_host on pinned host tensors gives bit for bit what the four device
@@ -273,3 +338,59 @@ def test_model_zoo_layers_full(dev, oracle_mod, name):
     wk = wl.model_zoo(2)[name]
     x, w, b, dy = wl.make_inputs(wk, seed=41)
     full_compare(wk.geom, "bf16", x, w, b, dy, dev, oracle_mod, label=name)
+
+
+# Tensor-core edge cases, whole tensors against the oracle, each on the family asserted:
+# stride-2 phases that no tap reaches (their dx must be exactly 0), the largest kernels,
+# stride with dilation, asymmetric pads at stride 2 on both sides, and the channel counts at
+# the edges of the tensor-core thresholds.
+TC_EDGES = [
+    # geometry, expected (fwd, bwd_data, bwd_weight, bias) families, untouched dx (step, row phase, col phase)
+    ((2, 16, 11, 11, 16, 1, 1, 2, 0, 0, 0, 0, 1, 1), (TC, TC, TC, RD), (2, 1, 1)),   # 1x1 stride 2: odd rows, odd cols
+    ((2, 32, 12, 13, 32, 2, 2, 2, 0, 0, 0, 0, 1, 1), (TC, TC, TC, RD), None),     # 2x2 stride 2: last column untouched
+    ((2, 16, 13, 12, 32, 1, 1, 2, 1, 0, 0, 1, 1, 1), (TC, TC, TC, RD), (2, 0, 1)),   # 1x1 stride 2, pads shift the phase
+    ((2, 32, 15, 14, 32, 7, 7, 1, 3, 3, 3, 3, 1, 1), (TC, TC, TC, RD), None),     # 7x7, 49 taps
+    ((2, 16, 20, 19, 32, 7, 7, 2, 3, 3, 3, 3, 1, 1), (TC, TC, TC, RD), None),     # 7x7 stride 2
+    ((2, 32, 17, 16, 32, 3, 3, 2, 2, 2, 2, 2, 2, 1), (TC, TC, TC, RD), None),     # stride 2 with dilation 2
+    ((2, 32, 15, 16, 32, 3, 3, 2, 0, 2, 1, 0, 1, 1), (TC, TC, TC, RD), None),     # stride 2, pads 0/2/1/0
+    ((2, 64, 16, 15, 64, 4, 4, 2, 2, 1, 0, 3, 1, 2), (TC, TC, TC, RD), None),     # stride 2, pads 2/1/0/3, groups 2
+    ((2, 16, 12, 12, 16, 3, 3, 2, 1, 1, 1, 1, 1, 1), (TC, TC, TC, RD), None),     # 16 channels, stride 2
+    ((2, 32, 10, 11, 32, 3, 3, 1, 1, 1, 1, 1, 1, 2), (TC, TC, TC, RD), None),     # 16 channels per group
+    ((2, 32, 9, 9, 32, 1, 1, 1, 0, 0, 0, 0, 1, 1), (TC, TC, TC, RD), None),       # 1x1 stride 1
+]
+
+
+def _edge_paths():
+    return [(g, p, z) for g, p, z in TC_EDGES]
+
+
+@pytest.mark.parametrize("geom,paths,untouched", _edge_paths())
+def test_tensor_core_edges_full(dev, oracle_mod, geom, paths, untouched):
+    assert_paths(geom, "bf16", paths)
+    wk = wl.Workload("edge", geom, "bf16", w=("normal", 0.2))
+    x, w, b, dy = wl.make_inputs(wk, seed=sum(geom) * 13)
+    got = full_compare(geom, "bf16", x, w, b, dy, dev, oracle_mod, label=f"edge {geom}")
+    ref_dx = oracle_mod.bwd_data(geom, f64(dy), f64(w))
+    zero = ref_dx == 0.0
+    # every pixel the oracle leaves at exactly zero (no tap reaches it) is exactly zero here too
+    assert np.array_equal(got["dx"].numpy()[zero], np.zeros(int(zero.sum()), np.float32)), geom
+    if untouched is not None:
+        step, rp, cp = untouched
+        assert bool((got["dx"][:, :, rp::step, :] == 0).all()) and bool((got["dx"][:, :, :, cp::step] == 0).all())
+        assert int(zero.sum()) > 0
+
+
+# The thresholds of the tensor-core families: a group with 8 input and 16 output channels
+# (forward and weight gradient on tensor cores, backward-data on CUDA cores), and the mirror.
+THRESHOLDS = [
+    ((2, 16, 10, 10, 32, 3, 3, 1, 1, 1, 1, 1, 1, 2), (TC, CC, TC, RD)),
+    ((2, 32, 10, 10, 16, 3, 3, 1, 1, 1, 1, 1, 1, 2), (CC, TC, CC, RD)),
+]
+
+
+@pytest.mark.parametrize("geom,paths", THRESHOLDS)
+def test_tensor_core_thresholds_full(dev, oracle_mod, geom, paths):
+    assert_paths(geom, "bf16", paths)
+    wk = wl.Workload("threshold", geom, "bf16", w=("normal", 0.2))
+    x, w, b, dy = wl.make_inputs(wk, seed=sum(geom) * 17)
+    full_compare(geom, "bf16", x, w, b, dy, dev, oracle_mod, label=f"threshold {geom}")
