@@ -586,6 +586,25 @@ def bench_sweep(args):
     return 0
 
 
+def bench_one_workload(args):
+    """--workload NAME: per-pass timing of one named workload (the command the kernel profiles
+    run under ncu); one JSON line.  --warmup may be 0 here, so that each pass launches once."""
+    import torch
+    from bwd_gconv_fwd_gb300 import workloads as wl
+    from bwd_gconv_fwd_gb300 import build
+    build.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    wk = wl.WORKLOADS[args.workload] if args.workload in wl.WORKLOADS else wl.model_zoo(32)[args.workload]
+    rec = time_workload(wk, dev, args.steps, args.warmup, flush, peaks)
+    rec["workload"] = config_dict(wk)["workload"]
+    rec["peak_source"] = peak_src
+    print(json.dumps(rec), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -596,7 +615,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config pass timings")
     ap.add_argument("--sweep", action="store_true", help="time the model-zoo layer sweep instead")
+    ap.add_argument("--workload", default=None, help="time the passes of one named workload only")
     args = ap.parse_args()
+    if args.workload:
+        return bench_one_workload(args)
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps, whatever is asked
     if args.impl == "reference":
         return bench_reference(args)

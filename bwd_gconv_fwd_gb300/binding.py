@@ -6,9 +6,14 @@ libgconv.so is missing the first call raises.  PyTorch only supplies device
 memory (tensors, workspaces) and the CUDA stream.
 
 Geometry is the ABI's 14-tuple ``(N, C_in, H, W, C_out, kH, kW, stride, pad_top,
-pad_bottom, pad_left, pad_right, dilation, groups)``; the tensor-level wrappers
-derive it from the tensor shapes plus ``stride``, ``padding`` (an int or a
-(top, bottom, left, right) tuple), ``dilation`` and ``groups``.
+pad_bottom, pad_left, pad_right, dilation, groups)``, or the 16-tuple of the per-axis
+entry points ``(N, C_in, H, W, C_out, kH, kW, stride_h, stride_w, pad_top, pad_bottom,
+pad_left, pad_right, dilation_h, dilation_w, groups)`` (the ``gconv_geometry`` record);
+the tensor-level wrappers derive it from the tensor shapes plus ``stride`` (an int or
+(s_h, s_w)), ``padding`` (an int, (p_h, p_w) or (top, bottom, left, right)),
+``dilation`` (an int or (d_h, d_w)) and ``groups``.  They call the 14-integer entry
+points when the request fits them (equal strides and dilations, fp32 outputs, no fused
+bias gradient) and the per-axis ``*_ex`` entry points otherwise.
 """
 from __future__ import annotations
 
@@ -31,7 +36,40 @@ PATH_NAMES = {PATH_NONE: "none", PATH_DIRECT: "direct", PATH_TC_IGEMM: "tc_igemm
 EXPORTED = ("gconv_out_shape", "gconv_workspace_size", "gconv_plan", "gconv_fwd", "gconv_bwd_data",
             "gconv_bwd_weight", "gconv_bwd_bias", "gconv_check_device_error", "gconv_status_string",
             "gconv_debug_force_path", "gconv_debug_set_wait_limit", "gconv_debug_set_trace", "gconv_bwd_weight_noalloc",
-            "gconv_noalloc_scratch_bytes", "gconv_step_host", "gconv_step_device_bytes")
+            "gconv_noalloc_scratch_bytes", "gconv_step_host", "gconv_step_device_bytes",
+            "gconv_out_shape_ex", "gconv_workspace_size_ex", "gconv_plan_ex", "gconv_fwd_ex", "gconv_bwd_data_ex",
+            "gconv_bwd_weight_ex", "gconv_bwd_bias_ex")
+
+
+class Geometry(ctypes.Structure):
+    """The gconv_geometry record of include/gconv.h."""
+    _fields_ = [(n, ctypes.c_int) for n in ("N", "C_in", "H", "W", "C_out", "kH", "kW", "stride_h", "stride_w",
+                                             "pad_top", "pad_bottom", "pad_left", "pad_right", "dilation_h",
+                                             "dilation_w", "groups")]
+
+
+def per_axis(geom):
+    """16-integer form of a 14- or 16-integer geometry."""
+    g = tuple(int(v) for v in geom)
+    if len(g) == 16:
+        return g
+    if len(g) != 14:
+        raise ValueError("geometry must have 14 or 16 integers")
+    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = g
+    return (N, Cin, H, W, Cout, kH, kW, s, s, pt, pb, pl, pr, d, d, G)
+
+
+def square(geom):
+    """The 14-integer form when strides and dilations agree across axes, else None."""
+    g = per_axis(geom)
+    N, Cin, H, W, Cout, kH, kW, sh, sw, pt, pb, pl, pr, dh, dw, G = g
+    if sh != sw or dh != dw:
+        return None
+    return (N, Cin, H, W, Cout, kH, kW, sh, pt, pb, pl, pr, dh, G)
+
+
+def geometry_record(geom):
+    return Geometry(*per_axis(geom))
 
 _lib = None
 
@@ -85,6 +123,21 @@ def lib():
     L.gconv_debug_set_wait_limit.restype = None
     L.gconv_debug_set_trace.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
     L.gconv_debug_set_trace.restype = None
+    gp = ctypes.POINTER(Geometry)
+    L.gconv_out_shape_ex.argtypes = [gp, ctypes.POINTER(i), ctypes.POINTER(i)]
+    L.gconv_out_shape_ex.restype = i
+    L.gconv_workspace_size_ex.argtypes = [gp, i, i]
+    L.gconv_workspace_size_ex.restype = sz
+    L.gconv_plan_ex.argtypes = [gp, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+    L.gconv_plan_ex.restype = i
+    L.gconv_fwd_ex.argtypes = [gp, i, i, vp, vp, vp, vp, vp, sz, vp]
+    L.gconv_fwd_ex.restype = i
+    L.gconv_bwd_data_ex.argtypes = [gp, i, i, vp, vp, vp, vp, sz, vp]
+    L.gconv_bwd_data_ex.restype = i
+    L.gconv_bwd_weight_ex.argtypes = [gp, i, vp, vp, vp, vp, vp, sz, vp]
+    L.gconv_bwd_weight_ex.restype = i
+    L.gconv_bwd_bias_ex.argtypes = [gp, i, vp, vp, vp, sz, vp]
+    L.gconv_bwd_bias_ex.restype = i
     _lib = L
     return L
 
@@ -102,12 +155,20 @@ def _check(status: int, what: str):
 
 def gconv_out_shape(geom):
     ho, wo = ctypes.c_int(), ctypes.c_int()
-    _check(lib().gconv_out_shape(*map(int, geom), ctypes.byref(ho), ctypes.byref(wo)), "gconv_out_shape")
+    if len(geom) == 16:
+        rec = geometry_record(geom)
+        _check(lib().gconv_out_shape_ex(ctypes.byref(rec), ctypes.byref(ho), ctypes.byref(wo)), "gconv_out_shape_ex")
+    else:
+        _check(lib().gconv_out_shape(*map(int, geom), ctypes.byref(ho), ctypes.byref(wo)), "gconv_out_shape")
     return ho.value, wo.value
 
 
 def gconv_workspace_size(geom, dtype: int, pass_: int) -> int:
-    n = lib().gconv_workspace_size(*map(int, geom), int(dtype), int(pass_))
+    if len(geom) == 16:
+        rec = geometry_record(geom)
+        n = lib().gconv_workspace_size_ex(ctypes.byref(rec), int(dtype), int(pass_))
+    else:
+        n = lib().gconv_workspace_size(*map(int, geom), int(dtype), int(pass_))
     if n == ctypes.c_size_t(-1).value:
         raise GconvError(GCONV_ERR_INVALID_ARG, "gconv_workspace_size")
     return int(n)
@@ -116,8 +177,13 @@ def gconv_workspace_size(geom, dtype: int, pass_: int) -> int:
 def gconv_plan(geom, dtype: int, pass_: int):
     """(path, launches) the library would use for this call."""
     path, launches = ctypes.c_int(), ctypes.c_int()
-    _check(lib().gconv_plan(*map(int, geom), int(dtype), int(pass_), ctypes.byref(path),
-                            ctypes.byref(launches)), "gconv_plan")
+    if len(geom) == 16:
+        rec = geometry_record(geom)
+        _check(lib().gconv_plan_ex(ctypes.byref(rec), int(dtype), int(pass_), ctypes.byref(path),
+                                   ctypes.byref(launches)), "gconv_plan_ex")
+    else:
+        _check(lib().gconv_plan(*map(int, geom), int(dtype), int(pass_), ctypes.byref(path),
+                                ctypes.byref(launches)), "gconv_plan")
     return path.value, launches.value
 
 
@@ -169,14 +235,27 @@ def _pads(padding):
     return p
 
 
+def _pair(v):
+    if isinstance(v, int):
+        return int(v), int(v)
+    a, b = (int(u) for u in v)
+    return a, b
+
+
 def geometry(x_shape, w_shape, stride=1, padding=0, dilation=1, groups=1):
+    """The ABI geometry: a 14-tuple when strides and dilations agree across axes, else the
+    16-tuple of the per-axis entry points."""
     N, Cin, H, W = (int(v) for v in x_shape)
     Cout, cgi, kH, kW = (int(v) for v in w_shape)
     if cgi * int(groups) != Cin:
         raise GconvError(GCONV_ERR_INVALID_ARG, f"weight has {cgi} input channels per group, "
                                                 f"x has {Cin} channels for {groups} groups")
     pt, pb, pl, pr = _pads(padding)
-    return (N, Cin, H, W, Cout, kH, kW, int(stride), pt, pb, pl, pr, int(dilation), int(groups))
+    sh, sw = _pair(stride)
+    dh, dw = _pair(dilation)
+    if sh == sw and dh == dw:
+        return (N, Cin, H, W, Cout, kH, kW, sh, pt, pb, pl, pr, dh, int(groups))
+    return (N, Cin, H, W, Cout, kH, kW, sh, sw, pt, pb, pl, pr, dh, dw, int(groups))
 
 
 def _dev(t: torch.Tensor, name: str):
@@ -200,33 +279,56 @@ def _workspace(geom, dt, pass_, workspace, device):
 
 # ---- the four passes (tensor level) -------------------------------------------
 
+def _out_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return GCONV_F32
+    if t.dtype == torch.bfloat16:
+        return GCONV_BF16
+    raise TypeError(f"unsupported output dtype {t.dtype}; use float32 or bfloat16")
+
+
 def gconv_fwd(x, w, bias, y, *, stride=1, padding=0, dilation=1, groups=1, workspace=None, stream=None):
-    """y <- conv(x, w) + bias (bias may be None).  y: fp32 [N, C_out, Ho, Wo]."""
+    """y <- conv(x, w) + bias (bias may be None).  y: fp32 or bf16 [N, C_out, Ho, Wo]."""
     geom = geometry(x.shape, w.shape, stride, padding, dilation, groups)
-    dt = dtype_code(x.dtype)
+    dt, odt = dtype_code(x.dtype), _out_code(y)
     ws, wsb = _workspace(geom, dt, PASS_FWD, workspace, x.device)
-    _check(lib().gconv_fwd(*geom, dt, _dev(x, "x"), _dev(w, "w"), _dev(bias, "bias"), _dev(y, "y"),
-                           ws, wsb, _stream_ptr(stream)), "gconv_fwd")
+    args = (_dev(x, "x"), _dev(w, "w"), _dev(bias, "bias"), _dev(y, "y"), ws, wsb, _stream_ptr(stream))
+    if len(geom) == 14 and odt == GCONV_F32:
+        _check(lib().gconv_fwd(*geom, dt, *args), "gconv_fwd")
+    else:
+        rec = geometry_record(geom)
+        _check(lib().gconv_fwd_ex(ctypes.byref(rec), dt, odt, *args), "gconv_fwd_ex")
     return y
 
 
 def gconv_bwd_data(dy, w, dx, *, stride=1, padding=0, dilation=1, groups=1, workspace=None, stream=None):
-    """dx <- gradient of <y, dy> w.r.t. x.  dx: fp32 [N, C_in, H, W]."""
+    """dx <- gradient of <y, dy> w.r.t. x.  dx: fp32 or bf16 [N, C_in, H, W]."""
     geom = geometry(dx.shape, w.shape, stride, padding, dilation, groups)
-    dt = dtype_code(dy.dtype)
+    dt, odt = dtype_code(dy.dtype), _out_code(dx)
     ws, wsb = _workspace(geom, dt, PASS_BWD_DATA, workspace, dy.device)
-    _check(lib().gconv_bwd_data(*geom, dt, _dev(dy, "dy"), _dev(w, "w"), _dev(dx, "dx"), ws, wsb,
-                                _stream_ptr(stream)), "gconv_bwd_data")
+    args = (_dev(dy, "dy"), _dev(w, "w"), _dev(dx, "dx"), ws, wsb, _stream_ptr(stream))
+    if len(geom) == 14 and odt == GCONV_F32:
+        _check(lib().gconv_bwd_data(*geom, dt, *args), "gconv_bwd_data")
+    else:
+        rec = geometry_record(geom)
+        _check(lib().gconv_bwd_data_ex(ctypes.byref(rec), dt, odt, *args), "gconv_bwd_data_ex")
     return dx
 
 
-def gconv_bwd_weight(x, dy, dw, *, stride=1, padding=0, dilation=1, groups=1, workspace=None, stream=None):
-    """dw <- gradient of <y, dy> w.r.t. w.  dw: fp32 [C_out, C_in/G, kH, kW]."""
+def gconv_bwd_weight(x, dy, dw, *, db=None, stride=1, padding=0, dilation=1, groups=1, workspace=None,
+                     stream=None):
+    """dw <- gradient of <y, dy> w.r.t. w, fp32 [C_out, C_in/G, kH, kW]; with db (fp32
+    [C_out]) also the bias gradient of the same dy, in the same call."""
     geom = geometry(x.shape, dw.shape, stride, padding, dilation, groups)
     dt = dtype_code(x.dtype)
     ws, wsb = _workspace(geom, dt, PASS_BWD_WEIGHT, workspace, x.device)
-    _check(lib().gconv_bwd_weight(*geom, dt, _dev(x, "x"), _dev(dy, "dy"), _dev(dw, "dw"), ws, wsb,
-                                  _stream_ptr(stream)), "gconv_bwd_weight")
+    if len(geom) == 14 and db is None:
+        _check(lib().gconv_bwd_weight(*geom, dt, _dev(x, "x"), _dev(dy, "dy"), _dev(dw, "dw"), ws, wsb,
+                                      _stream_ptr(stream)), "gconv_bwd_weight")
+    else:
+        rec = geometry_record(geom)
+        _check(lib().gconv_bwd_weight_ex(ctypes.byref(rec), dt, _dev(x, "x"), _dev(dy, "dy"), _dev(dw, "dw"),
+                                         _dev(db, "db"), ws, wsb, _stream_ptr(stream)), "gconv_bwd_weight_ex")
     return dw
 
 
@@ -287,8 +389,13 @@ def gconv_bwd_bias(dy, db, *, geom=None, workspace=None, stream=None):
         geom = (N, C, Ho, Wo, C, 1, 1, 1, 0, 0, 0, 0, 1, 1)
     dt = dtype_code(dy.dtype)
     ws, wsb = _workspace(geom, dt, PASS_BWD_BIAS, workspace, dy.device)
-    _check(lib().gconv_bwd_bias(*geom, dt, _dev(dy, "dy"), _dev(db, "db"), ws, wsb, _stream_ptr(stream)),
-           "gconv_bwd_bias")
+    if len(geom) == 14:
+        _check(lib().gconv_bwd_bias(*geom, dt, _dev(dy, "dy"), _dev(db, "db"), ws, wsb, _stream_ptr(stream)),
+               "gconv_bwd_bias")
+    else:
+        rec = geometry_record(geom)
+        _check(lib().gconv_bwd_bias_ex(ctypes.byref(rec), dt, _dev(dy, "dy"), _dev(db, "db"), ws, wsb,
+                                       _stream_ptr(stream)), "gconv_bwd_bias_ex")
     return db
 
 
@@ -312,3 +419,23 @@ def gconv_bwd_weight_ptr(geom, dt, x, dy, dw, ws=0, ws_bytes=0, stream=0):
 def gconv_bwd_bias_ptr(geom, dt, dy, db, ws=0, ws_bytes=0, stream=0):
     _check(lib().gconv_bwd_bias(*map(int, geom), int(dt), dy, db, ws or None, int(ws_bytes),
                                 stream or None), "gconv_bwd_bias")
+
+
+# ---- per-axis entry points at pointer level (16-integer geometry) ------------
+
+def gconv_fwd_ex_ptr(geom, dt, out_dt, x, w, bias, y, ws=0, ws_bytes=0, stream=0):
+    rec = geometry_record(geom)
+    _check(lib().gconv_fwd_ex(ctypes.byref(rec), int(dt), int(out_dt), x, w, bias or None, y, ws or None,
+                              int(ws_bytes), stream or None), "gconv_fwd_ex")
+
+
+def gconv_bwd_data_ex_ptr(geom, dt, out_dt, dy, w, dx, ws=0, ws_bytes=0, stream=0):
+    rec = geometry_record(geom)
+    _check(lib().gconv_bwd_data_ex(ctypes.byref(rec), int(dt), int(out_dt), dy, w, dx, ws or None, int(ws_bytes),
+                                   stream or None), "gconv_bwd_data_ex")
+
+
+def gconv_bwd_weight_ex_ptr(geom, dt, x, dy, dw, db=0, ws=0, ws_bytes=0, stream=0):
+    rec = geometry_record(geom)
+    _check(lib().gconv_bwd_weight_ex(ctypes.byref(rec), int(dt), x, dy, dw, db or None, ws or None, int(ws_bytes),
+                                     stream or None), "gconv_bwd_weight_ex")

@@ -227,30 +227,30 @@ __device__ __forceinline__ void fwd_tile(const Geom &g, const TileGeom &t, int b
         ws[i] = o < g.Cgo ? to_f(w[(int64_t)(grp * g.Cgo + o) * E + e]) : 0.f;
     }
     const int64_t plane = (int64_t)g.H * g.W;
-    stage_rows(x + ((int64_t)n * g.Cin + (int64_t)grp * g.Cgi) * plane, plane, g.H, g.W, oh0 * g.s - g.pt,
-               ow0 * g.s - g.pl, g.Cgi, t.RI, t.CI, t.CIp, xs);
+    stage_rows(x + ((int64_t)n * g.Cin + (int64_t)grp * g.Cgi) * plane, plane, g.H, g.W, oh0 * g.s_h - g.pt,
+               ow0 * g.s_w - g.pl, g.Cgi, t.RI, t.CI, t.CIp, xs);
     __syncthreads();
     const int64_t out_plane = (int64_t)g.Ho * g.Wo;
-    float *yg = y + ((int64_t)n * g.Cout + (int64_t)grp * g.Cgo) * out_plane;
+    const int64_t yg = ((int64_t)n * g.Cout + (int64_t)grp * g.Cgo) * out_plane;   // element index in y
     float bv[CO];
     #pragma unroll
     for (int o = 0; o < CO; ++o) bv[o] = (bias && o < g.Cgo) ? to_f(bias[grp * g.Cgo + o]) : 0.f;
     const int rows = min(t.TH, g.Ho - oh0), cols = min(t.TW, g.Wo - ow0);
-    if (K == 3 && g.s == 1) {
+    if (K == 3 && g.s_h == 1 && g.s_w == 1) {
         // strips of four consecutive columns (the staged rows carry 4 spare columns)
         const int strips = (cols + 3) >> 2;
         const int dr = kTT / strips, dc = kTT - dr * strips;
         int r = threadIdx.x / strips, sc = threadIdx.x - r * strips;
         for (int pi = threadIdx.x; pi < rows * strips; pi += kTT) {
             float acc[4][CO];
-            corr3_strip<CO>(acc, xs + r * t.CIp + 4 * sc, ws, g.Cgi, t.RI * t.CIp, g.d * t.CIp, g.d);
-            float *yo = yg + (int64_t)(oh0 + r) * g.Wo + ow0 + 4 * sc;
+            corr3_strip<CO>(acc, xs + r * t.CIp + 4 * sc, ws, g.Cgi, t.RI * t.CIp, g.d_h * t.CIp, g.d_w);
+            const int64_t yo = yg + (int64_t)(oh0 + r) * g.Wo + ow0 + 4 * sc;
             #pragma unroll
             for (int j = 0; j < 4; ++j)
                 if (4 * sc + j < cols)
                     #pragma unroll
                     for (int o = 0; o < CO; ++o)
-                        if (o < g.Cgo) yo[o * out_plane + j] = acc[j][o] + bv[o];
+                        if (o < g.Cgo) store_out(y, yo + o * out_plane + j, acc[j][o] + bv[o], g.out_bf16);
             r += dr;
             sc += dc;
             if (sc >= strips) { sc -= strips; ++r; }
@@ -261,12 +261,12 @@ __device__ __forceinline__ void fwd_tile(const Geom &g, const TileGeom &t, int b
     int r = threadIdx.x / cols, col = threadIdx.x - r * cols;
     for (int pi = threadIdx.x; pi < rows * cols; pi += kTT) {
         float acc[CO];
-        corr_point<CO, K>(acc, xs + (r * g.s) * t.CIp + col * g.s, ws, g.Cgi, t.RI * t.CIp, g.kH, g.kW,
-                          g.d * t.CIp, g.d);
-        float *yo = yg + (int64_t)(oh0 + r) * g.Wo + ow0 + col;
+        corr_point<CO, K>(acc, xs + (r * g.s_h) * t.CIp + col * g.s_w, ws, g.Cgi, t.RI * t.CIp, g.kH, g.kW,
+                          g.d_h * t.CIp, g.d_w);
+        const int64_t yo = yg + (int64_t)(oh0 + r) * g.Wo + ow0 + col;
         #pragma unroll
         for (int o = 0; o < CO; ++o)
-            if (o < g.Cgo) yo[o * out_plane] = acc[o] + bv[o];
+            if (o < g.Cgo) store_out(y, yo + o * out_plane, acc[o] + bv[o], g.out_bf16);
         r += dr;
         col += dc;
         if (col >= cols) { col -= cols; ++r; }
@@ -293,9 +293,9 @@ __device__ __forceinline__ void bwd_data_tile(const Geom &g, const TileGeom &t, 
     const int grp = b % g.G;
     const int n = b / g.G;
     const int ih0 = th * t.TH, iw0 = tw * t.TW;
-    const int oh_s = floordiv_i(ih0 + g.pt - (g.kH - 1) * g.d, g.s);
-    const int ow_s = floordiv_i(iw0 + g.pl - (g.kW - 1) * g.d, g.s);
-    const bool unit = g.s == 1;
+    const int oh_s = floordiv_i(ih0 + g.pt - (g.kH - 1) * g.d_h, g.s_h);
+    const int ow_s = floordiv_i(iw0 + g.pl - (g.kW - 1) * g.d_w, g.s_w);
+    const bool unit = g.s_h == 1 && g.s_w == 1;
     for (int i = threadIdx.x; i < g.Cgo * KK * CI_; i += kTT) {
         const int ok = i / CI_, c = i - ok * CI_;
         const int o = ok / KK, k = ok - o * KK;
@@ -307,7 +307,7 @@ __device__ __forceinline__ void bwd_data_tile(const Geom &g, const TileGeom &t, 
                t.RI, t.CI, t.CIp, ds);
     __syncthreads();
     const int64_t in_plane = (int64_t)g.H * g.W;
-    float *xg = dx + ((int64_t)n * g.Cin + (int64_t)grp * g.Cgi) * in_plane;
+    const int64_t xg = ((int64_t)n * g.Cin + (int64_t)grp * g.Cgi) * in_plane;   // element index in dx
     const int rows = min(t.TH, g.H - ih0), cols = min(t.TW, g.W - iw0);
     if (K == 3 && unit) {
         const int strips = (cols + 3) >> 2;
@@ -315,14 +315,14 @@ __device__ __forceinline__ void bwd_data_tile(const Geom &g, const TileGeom &t, 
         int r = threadIdx.x / strips, sc = threadIdx.x - r * strips;
         for (int pi = threadIdx.x; pi < rows * strips; pi += kTT) {
             float acc[4][CI_];
-            corr3_strip<CI_>(acc, ds + r * t.CIp + 4 * sc, ws, g.Cgo, t.RI * t.CIp, g.d * t.CIp, g.d);
-            float *xo = xg + (int64_t)(ih0 + r) * g.W + iw0 + 4 * sc;
+            corr3_strip<CI_>(acc, ds + r * t.CIp + 4 * sc, ws, g.Cgo, t.RI * t.CIp, g.d_h * t.CIp, g.d_w);
+            const int64_t xo = xg + (int64_t)(ih0 + r) * g.W + iw0 + 4 * sc;
             #pragma unroll
             for (int j = 0; j < 4; ++j)
                 if (4 * sc + j < cols)
                     #pragma unroll
                     for (int c = 0; c < CI_; ++c)
-                        if (c < g.Cgi) xo[c * in_plane + j] = acc[j][c];
+                        if (c < g.Cgi) store_out(dx, xo + c * in_plane + j, acc[j][c], g.out_bf16);
             r += dr;
             sc += dc;
             if (sc >= strips) { sc -= strips; ++r; }
@@ -335,8 +335,8 @@ __device__ __forceinline__ void bwd_data_tile(const Geom &g, const TileGeom &t, 
         float acc[CI_];
         if (unit) {
             // staged row of (ih - kh*d + pt) is ihl + (kH-1-kh)*d: mirrored tap kh' = kH-1-kh
-            corr_point<CI_, K>(acc, ds + r * t.CIp + col, ws, g.Cgo, t.RI * t.CIp, g.kH, g.kW, g.d * t.CIp, g.d);
-        } else if (K == 3 && g.s == 2) {
+            corr_point<CI_, K>(acc, ds + r * t.CIp + col, ws, g.Cgo, t.RI * t.CIp, g.kH, g.kW, g.d_h * t.CIp, g.d_w);
+        } else if (K == 3 && g.s_h == 2 && g.s_w == 2) {
             // 3 x 3, stride 2: the taps unrolled, a tap reaching this pixel when ih + pt - kh*d
             // and iw + pl - kw*d are even (parity tests and shifts, no divisions, no tap loop)
             #pragma unroll
@@ -344,12 +344,12 @@ __device__ __forceinline__ void bwd_data_tile(const Geom &g, const TileGeom &t, 
             const int ih = ih0 + r, iw = iw0 + col;
             #pragma unroll
             for (int kh = 0; kh < 3; ++kh) {
-                const int tt = ih + g.pt - kh * g.d;
+                const int tt = ih + g.pt - kh * g.d_h;
                 const int oh = tt >> 1;
                 const bool okh = tt >= 0 && !(tt & 1) && oh < g.Ho;
                 #pragma unroll
                 for (int kw = 0; kw < 3; ++kw) {
-                    const int tu = iw + g.pl - kw * g.d;
+                    const int tu = iw + g.pl - kw * g.d_w;
                     const int ow = tu >> 1;
                     if (okh && tu >= 0 && !(tu & 1) && ow < g.Wo) {
                         const float *dp = ds + (oh - oh_s) * t.CIp + (ow - ow_s);
@@ -358,19 +358,19 @@ __device__ __forceinline__ void bwd_data_tile(const Geom &g, const TileGeom &t, 
                     }
                 }
             }
-        } else if (g.s == 2) {
+        } else if (g.s_h == 2 && g.s_w == 2) {
             // stride 2: a tap reaches this pixel when ih + pt - kh*d is even (parity tests
             // and shifts instead of divisions by the runtime stride)
             #pragma unroll
             for (int c = 0; c < CI_; ++c) acc[c] = 0.f;
             const int ih = ih0 + r, iw = iw0 + col;
             for (int kh = 0; kh < g.kH; ++kh) {
-                const int tt = ih + g.pt - kh * g.d;
+                const int tt = ih + g.pt - kh * g.d_h;
                 if (tt < 0 || (tt & 1)) continue;
                 const int oh = tt >> 1;
                 if (oh >= g.Ho) continue;
                 for (int kw = 0; kw < g.kW; ++kw) {
-                    const int tu = iw + g.pl - kw * g.d;
+                    const int tu = iw + g.pl - kw * g.d_w;
                     if (tu < 0 || (tu & 1)) continue;
                     const int ow = tu >> 1;
                     if (ow >= g.Wo) continue;
@@ -384,14 +384,14 @@ __device__ __forceinline__ void bwd_data_tile(const Geom &g, const TileGeom &t, 
             for (int c = 0; c < CI_; ++c) acc[c] = 0.f;
             const int ih = ih0 + r, iw = iw0 + col;
             for (int kh = 0; kh < g.kH; ++kh) {
-                const int tt = ih + g.pt - kh * g.d;
-                if (tt < 0 || tt % g.s) continue;
-                const int oh = tt / g.s;
+                const int tt = ih + g.pt - kh * g.d_h;
+                if (tt < 0 || tt % g.s_h) continue;
+                const int oh = tt / g.s_h;
                 if (oh >= g.Ho) continue;
                 for (int kw = 0; kw < g.kW; ++kw) {
-                    const int tu = iw + g.pl - kw * g.d;
-                    if (tu < 0 || tu % g.s) continue;
-                    const int ow = tu / g.s;
+                    const int tu = iw + g.pl - kw * g.d_w;
+                    if (tu < 0 || tu % g.s_w) continue;
+                    const int ow = tu / g.s_w;
                     if (ow >= g.Wo) continue;
                     const float *dp = ds + (oh - oh_s) * t.CIp + (ow - ow_s);
                     const float *wp = ws + (kh * g.kW + kw) * CI_;
@@ -399,10 +399,10 @@ __device__ __forceinline__ void bwd_data_tile(const Geom &g, const TileGeom &t, 
                 }
             }
         }
-        float *xo = xg + (int64_t)(ih0 + r) * g.W + iw0 + col;
+        const int64_t xo = xg + (int64_t)(ih0 + r) * g.W + iw0 + col;
         #pragma unroll
         for (int c = 0; c < CI_; ++c)
-            if (c < g.Cgi) xo[c * in_plane] = acc[c];
+            if (c < g.Cgi) store_out(dx, xo + c * in_plane, acc[c], g.out_bf16);
         r += dr;
         col += dc;
         if (col >= cols) { col -= cols; ++r; }
@@ -459,6 +459,7 @@ struct Conv3Params {
     int GB, n_gb;                          // groups per tile (small planes share a block), group blocks
     int bwd;                               // 1: weights mirrored and transposed (backward-data)
     int w_cin_g;                           // C_in/G of the weight tensor
+    int out_bf16;                          // output stored as bf16
 };
 
 template <typename T, int CO, int BX>
@@ -574,7 +575,7 @@ conv3_s1_kernel(const __grid_constant__ Conv3Params p)
                                 for (int o = 0; o < CO; ++o) acc[i][j][o] = fmaf(wv[o], win[i + a][j + bb], acc[i][j][o]);
                     }
             }
-            float *og = p.out + ((int64_t)n * p.out_ctot + (int64_t)grp * p.nout) * out_plane;
+            const int64_t og = ((int64_t)n * p.out_ctot + (int64_t)grp * p.nout) * out_plane;   // element index
             const bool vec = (p.OW & 3) == 0 && c0 + cb + BX <= p.OW;
             #pragma unroll
             for (int o = 0; o < CO; ++o) {
@@ -584,16 +585,16 @@ conv3_s1_kernel(const __grid_constant__ Conv3Params p)
                 for (int i = 0; i < 4; ++i) {
                     const int r = r0 + rb + i;
                     if (rb + i >= p.TH || r >= p.OH) break;
-                    float *row = og + o * out_plane + (int64_t)r * p.OW + c0 + cb;
+                    const int64_t row = og + o * out_plane + (int64_t)r * p.OW + c0 + cb;
                     if (vec) {
                         #pragma unroll
                         for (int j = 0; j < BX; j += 4)
-                            *reinterpret_cast<float4 *>(row + j) = make_float4(acc[i][j][o] + bv, acc[i][j + 1][o] + bv,
-                                                                               acc[i][j + 2][o] + bv, acc[i][j + 3][o] + bv);
+                            store_out4(p.out, row + j, acc[i][j][o] + bv, acc[i][j + 1][o] + bv,
+                                       acc[i][j + 2][o] + bv, acc[i][j + 3][o] + bv, p.out_bf16);
                     } else {
                         #pragma unroll
                         for (int j = 0; j < BX; ++j)
-                            if (c0 + cb + j < p.OW) row[j] = acc[i][j][o] + bv;
+                            if (c0 + cb + j < p.OW) store_out(p.out, row + j, acc[i][j][o] + bv, p.out_bf16);
                     }
                 }
             }
@@ -609,7 +610,7 @@ int conv3_bx(int) { return 4; }
 // thread rows, shrunk until the staged planes fit 96 KB.
 bool plan_conv3(const Geom &g, bool bwd, Conv3Params *p, size_t *smem)
 {
-    if (g.kH != 3 || g.kW != 3 || g.s != 1 || g.d != 1) return false;
+    if (g.kH != 3 || g.kW != 3 || g.s_h != 1 || g.s_w != 1 || g.d_h != 1 || g.d_w != 1) return false;
     const int nin = bwd ? g.Cgo : g.Cgi, nout = bwd ? g.Cgi : g.Cgo;
     if (nout > 4 || nin > 16) return false;
     const int CO = conv3_slots(nout), BX = conv3_bx(nout);
@@ -698,7 +699,7 @@ bwd_weight_tiled_kernel(Geom g, TileGeom t, const T *__restrict__ x, const T *__
     const int th = b % t.n_th; b /= t.n_th;
     const int grp = b;
     const int oh0 = th * t.TH, ow0 = tw * t.TW;
-    const int ih0 = oh0 * g.s - g.pt, iw0 = ow0 * g.s - g.pl;
+    const int ih0 = oh0 * g.s_h - g.pt, iw0 = ow0 * g.s_w - g.pl;
     const int q = threadIdx.x / t.L, l = threadIdx.x - q * t.L;
     const bool active = q < t.P;
     const int o = active ? q / g.Cgi : 0, c = active ? q - o * g.Cgi : 0;
@@ -706,7 +707,7 @@ bwd_weight_tiled_kernel(Geom g, TileGeom t, const T *__restrict__ x, const T *__
     #pragma unroll
     for (int k = 0; k < KK; ++k) {
         const int kh = k / g.kW, kw = k - kh * g.kW;
-        toff[k] = kh * g.d * t.CIp + kw * g.d;
+        toff[k] = kh * g.d_h * t.CIp + kw * g.d_w;
     }
     float acc[KK];
     #pragma unroll
@@ -728,7 +729,7 @@ bwd_weight_tiled_kernel(Geom g, TileGeom t, const T *__restrict__ x, const T *__
             int r = l / t.TW, col = l - r * t.TW;
             for (int pi = l; pi < dtile; pi += t.L) {
                 const float dv = dsp[pi];
-                const float *xb = xsp + (r * g.s) * t.CIp + col * g.s;
+                const float *xb = xsp + (r * g.s_h) * t.CIp + col * g.s_w;
                 #pragma unroll
                 for (int k = 0; k < KK; ++k) acc[k] = fmaf(dv, xb[toff[k]], acc[k]);
                 r += dr;
@@ -865,7 +866,7 @@ wgrad3_s1_kernel(Geom g, TileGeom t, int CIpx, int CIpy, const T *__restrict__ x
 // Tile for wgrad3_s1_kernel (3 x 3, stride 1, dilation 1, (C_in/G)*(C_out/G) <= 256).
 bool plan_wgrad3(const Geom &g, TileGeom *t, size_t *smem, int *CIpx, int *CIpy)
 {
-    if (g.kH != 3 || g.kW != 3 || g.s != 1 || g.d != 1) return false;
+    if (g.kH != 3 || g.kW != 3 || g.s_h != 1 || g.s_w != 1 || g.d_h != 1 || g.d_w != 1) return false;
     const int P = g.Cgi * g.Cgo;
     if (P > kTT) return false;
     *t = TileGeom{};
@@ -925,8 +926,8 @@ weight_finish_kernel(const float *__restrict__ part, int G, int nbg, int P, int 
 
 // Output tile for the forward / backward-data kernels: about `target` positions, staged
 // input within the shared-memory budget next to `fixed` floats of weights.
-bool pick_tile(int out_h, int out_w, int s, int d, int k_h, int k_w, int in_ch, int fixed, bool transposed,
-               int target, TileGeom *t)
+bool pick_tile(int out_h, int out_w, int s_h, int s_w, int d_h, int d_w, int k_h, int k_w, int in_ch, int fixed,
+               bool transposed, int target, TileGeom *t)
 {
     int TW = std::min(out_w, 128);
     for (; TW >= 8 || TW == out_w; TW = TW > 8 ? TW / 2 : 0) {
@@ -934,11 +935,11 @@ bool pick_tile(int out_h, int out_w, int s, int d, int k_h, int k_w, int in_ch, 
         for (; TH >= 1; TH = TH > 1 ? TH / 2 : 0) {
             int RI, CI;
             if (!transposed) {
-                RI = (TH - 1) * s + (k_h - 1) * d + 1;
-                CI = (TW - 1) * s + (k_w - 1) * d + 1;
+                RI = (TH - 1) * s_h + (k_h - 1) * d_h + 1;
+                CI = (TW - 1) * s_w + (k_w - 1) * d_w + 1;
             } else {   // gradOutput rows reachable from TH input rows
-                RI = (TH - 1 + (k_h - 1) * d) / s + 2;
-                CI = (TW - 1 + (k_w - 1) * d) / s + 2;
+                RI = (TH - 1 + (k_h - 1) * d_h) / s_h + 2;
+                CI = (TW - 1 + (k_w - 1) * d_w) / s_w + 2;
             }
             const int CIp = (CI + 4) | 1;   // spare columns for 4-wide strips; odd pitch spreads banks
             const int64_t floats = (int64_t)fixed + (int64_t)in_ch * RI * CIp;
@@ -963,7 +964,8 @@ bool plan_fwd(const Geom &g, TileGeom *t, size_t *smem)
     const int CO = produced_slots(g.Cgo);
     if (!CO) return false;
     const int fixed = g.Cgi * g.kH * g.kW * CO;
-    if (!pick_tile(g.Ho, g.Wo, g.s, g.d, g.kH, g.kW, g.Cgi, fixed, false, 16384 / std::max(CO, 4), t)) return false;
+    if (!pick_tile(g.Ho, g.Wo, g.s_h, g.s_w, g.d_h, g.d_w, g.kH, g.kW, g.Cgi, fixed, false, 16384 / std::max(CO, 4), t))
+        return false;
     *smem = (size_t)(fixed + g.Cgi * t->RI * t->CIp) * 4;
     return true;
 }
@@ -973,7 +975,8 @@ bool plan_bwd_data(const Geom &g, TileGeom *t, size_t *smem)
     const int CI_ = produced_slots(g.Cgi);
     if (!CI_) return false;
     const int fixed = g.Cgo * g.kH * g.kW * CI_;
-    if (!pick_tile(g.H, g.W, g.s, g.d, g.kH, g.kW, g.Cgo, fixed, true, 16384 / std::max(CI_, 4), t)) return false;
+    if (!pick_tile(g.H, g.W, g.s_h, g.s_w, g.d_h, g.d_w, g.kH, g.kW, g.Cgo, fixed, true, 16384 / std::max(CI_, 4), t))
+        return false;
     *smem = (size_t)(fixed + g.Cgo * t->RI * t->CIp) * 4;
     return true;
 }
@@ -989,7 +992,7 @@ bool plan_bwd_weight(const Geom &g, TileGeom *t, size_t *smem)
     int TW = std::min(g.Wo, 64);
     int TH = std::max(1, std::min(g.Ho, 4096 / TW));
     for (;; TH = TH > 1 ? TH / 2 : TH, TW = TH == 1 ? std::max(1, TW / 2) : TW) {
-        const int RI = (TH - 1) * g.s + (g.kH - 1) * g.d + 1, CI = (TW - 1) * g.s + (g.kW - 1) * g.d + 1;
+        const int RI = (TH - 1) * g.s_h + (g.kH - 1) * g.d_h + 1, CI = (TW - 1) * g.s_w + (g.kW - 1) * g.d_w + 1;
         const int CIp = CI | 1;
         const int64_t floats = std::max<int64_t>((int64_t)g.Cgi * RI * CIp + (int64_t)g.Cgo * TH * TW,
                                                  (int64_t)P * KK * t->L);
@@ -1025,6 +1028,7 @@ gconv_status launch_typed(const Geom &g, const Plan &, gconv_pass pass, const vo
             c3.w = b;
             c3.bias = pass == GCONV_PASS_FWD ? bias : nullptr;
             c3.out = out;
+            c3.out_bf16 = g.out_bf16;
             return launch_conv3<T>(c3, sm3, s) ? GCONV_OK : GCONV_ERR_CUDA;
         }
     }

@@ -68,24 +68,44 @@ void *debug_trace(size_t *bytes)
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-gconv_status make_geom(int N, int C_in, int H, int W, int C_out, int kH, int kW, int stride,
-                       int pt, int pb, int pl, int pr, int dil, int groups, Geom *g)
+// Validates a geometry given as 16 integers (N, C_in, H, W, C_out, kH, kW, stride_h,
+// stride_w, pad_top, pad_bottom, pad_left, pad_right, dilation_h, dilation_w, groups).
+gconv_status make_geom16(const int *v, Geom *g)
 {
-    if (N < 0 || C_in < 1 || H < 1 || W < 1 || C_out < 1 || kH < 1 || kW < 1 || stride < 1 ||
-        pt < 0 || pb < 0 || pl < 0 || pr < 0 || dil < 1 || groups < 1)
+    const int N = v[0], C_in = v[1], H = v[2], W = v[3], C_out = v[4], kH = v[5], kW = v[6];
+    const int sh = v[7], sw = v[8], pt = v[9], pb = v[10], pl = v[11], pr = v[12], dh = v[13], dw = v[14];
+    const int groups = v[15];
+    if (N < 0 || C_in < 1 || H < 1 || W < 1 || C_out < 1 || kH < 1 || kW < 1 || sh < 1 || sw < 1 ||
+        pt < 0 || pb < 0 || pl < 0 || pr < 0 || dh < 1 || dw < 1 || groups < 1)
         return GCONV_ERR_INVALID_ARG;
     if (C_in % groups || C_out % groups) return GCONV_ERR_INVALID_ARG;
-    const int64_t span_h = (int64_t)H + pt + pb - (int64_t)dil * (kH - 1) - 1;
-    const int64_t span_w = (int64_t)W + pl + pr - (int64_t)dil * (kW - 1) - 1;
+    const int64_t span_h = (int64_t)H + pt + pb - (int64_t)dh * (kH - 1) - 1;
+    const int64_t span_w = (int64_t)W + pl + pr - (int64_t)dw * (kW - 1) - 1;
     if (span_h < 0 || span_w < 0) return GCONV_ERR_INVALID_ARG;
-    const int64_t Ho = span_h / stride + 1, Wo = span_w / stride + 1;
+    const int64_t Ho = span_h / sh + 1, Wo = span_w / sw + 1;
     const int64_t lim = INT_MAX;
     if ((int64_t)N * C_in * H * W > lim || (int64_t)N * C_out * Ho * Wo > lim ||
         (int64_t)C_out * (C_in / groups) * kH * kW > lim || Ho > lim || Wo > lim)
         return GCONV_ERR_INVALID_ARG;
-    *g = Geom{N, C_in, H, W, C_out, kH, kW, stride, pt, pb, pl, pr, dil, groups,
-              (int)Ho, (int)Wo, C_in / groups, C_out / groups};
+    *g = Geom{N, C_in, H, W, C_out, kH, kW, sh, sw, pt, pb, pl, pr, dh, dw, groups,
+              (int)Ho, (int)Wo, C_in / groups, C_out / groups, 0};
     return GCONV_OK;
+}
+
+gconv_status make_geom(int N, int C_in, int H, int W, int C_out, int kH, int kW, int stride,
+                       int pt, int pb, int pl, int pr, int dil, int groups, Geom *g)
+{
+    const int v[16] = {N, C_in, H, W, C_out, kH, kW, stride, stride, pt, pb, pl, pr, dil, dil, groups};
+    return make_geom16(v, g);
+}
+
+static gconv_status make_geom_ex(const gconv_geometry *p, Geom *g)
+{
+    if (!p) return GCONV_ERR_INVALID_ARG;
+    const int v[16] = {p->N, p->C_in, p->H, p->W, p->C_out, p->kH, p->kW, p->stride_h, p->stride_w,
+                       p->pad_top, p->pad_bottom, p->pad_left, p->pad_right, p->dilation_h, p->dilation_w,
+                       p->groups};
+    return make_geom16(v, g);
 }
 
 static int elementwise_grid(int64_t total)
@@ -231,42 +251,67 @@ static gconv_status zero_empty_sum(const Geom &g, gconv_pass pass, float *out, v
                ? GCONV_OK : GCONV_ERR_CUDA;
 }
 
-// One entry point body for all four passes.  a/b are the pass's two inputs in
-// ABI order (fwd: x, w; bwd_data: dy, w; bwd_weight: x, dy; bias: dy, unused).
-static gconv_status run_pass(const int *geo, gconv_dtype dt, gconv_pass pass, const void *a,
-                             const void *b, const void *bias, float *out, void *ws,
-                             size_t ws_bytes, void *stream)
+// One entry point body for all four passes.  a/b are the pass's two inputs in ABI
+// order (fwd: x, w; bwd_data: dy, w; bwd_weight: x, dy; bias: dy, unused).  out_dt is
+// the dtype of y / dx (fp32 or bf16); db, for the weight gradient only, asks for the bias
+// gradient from the same call.
+static gconv_status run_pass(const Geom &g, gconv_dtype dt, gconv_dtype out_dt, gconv_pass pass,
+                             const void *a, const void *b, const void *bias, void *out, float *db,
+                             void *ws, size_t ws_bytes, void *stream)
 {
-    Geom g;
-    gconv_status st = make_geom(geo[0], geo[1], geo[2], geo[3], geo[4], geo[5], geo[6], geo[7],
-                                geo[8], geo[9], geo[10], geo[11], geo[12], geo[13], &g);
-    if (st != GCONV_OK) return st;
     if (dt != GCONV_F32 && dt != GCONV_BF16) return GCONV_ERR_INVALID_ARG;
-    if (g.N == 0) return zero_empty_sum(g, pass, out, stream);
+    if (out_dt != GCONV_F32 && out_dt != GCONV_BF16) return GCONV_ERR_INVALID_ARG;
+    if (out_dt == GCONV_BF16 && (pass == GCONV_PASS_BWD_WEIGHT || pass == GCONV_PASS_BWD_BIAS))
+        return GCONV_ERR_INVALID_ARG;   // dw and db are always fp32
+    if (g.N == 0) {
+        gconv_status st = zero_empty_sum(g, pass, static_cast<float *>(out), stream);
+        if (st == GCONV_OK && db) st = zero_empty_sum(g, GCONV_PASS_BWD_BIAS, db, stream);
+        return st;
+    }
     const bool need_b = pass != GCONV_PASS_BWD_BIAS;
     if (!a || !out || (need_b && !b)) return GCONV_ERR_INVALID_ARG;
-    if (!aligned16(a) || !aligned16(out) || (need_b && !aligned16(b)) || (bias && !aligned16(bias)))
+    if (!aligned16(a) || !aligned16(out) || (need_b && !aligned16(b)) || (bias && !aligned16(bias)) ||
+        (db && !aligned16(db)))
         return GCONV_ERR_INVALID_ARG;
     const Plan p = plan_pass(g, dt, pass);
     if (p.path < 0) return GCONV_ERR_UNSUPPORTED;
-    if (p.ws_bytes > 0) {
-        if (!ws || ws_bytes < p.ws_bytes) return GCONV_ERR_WORKSPACE;
+    // the weight gradient's workspace covers a bias gradient in the same call, whether or
+    // not this call asks for it (the size gconv_workspace_size reports)
+    Plan pb{};
+    if (pass == GCONV_PASS_BWD_WEIGHT) {
+        pb = plan_pass(g, dt, GCONV_PASS_BWD_BIAS);
+        if (pb.path < 0) return GCONV_ERR_UNSUPPORTED;
+    }
+    const size_t need = std::max(p.ws_bytes, pb.ws_bytes);
+    if (need > 0) {
+        if (!ws || ws_bytes < need) return GCONV_ERR_WORKSPACE;
         if (!aligned16(ws)) return GCONV_ERR_INVALID_ARG;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaGetLastError();  // clear a stale error so the check below is about this call
+    // y and dx are written through a float* base whatever their dtype; the kernels take
+    // the element size from out_bf16
+    float *o = static_cast<float *>(out);
+    Geom gk = g;
+    gk.out_bf16 = out_dt == GCONV_BF16 ? 1 : 0;
+    gconv_status st = GCONV_OK;
     if (p.path == GCONV_PATH_TC_IGEMM) {
-        st = tc_igemm_launch(g, p, pass, a, b, bias, out, ws, s);
+        st = tc_igemm_launch(gk, p, pass, a, b, bias, o, ws, s);
     } else if (p.path == GCONV_PATH_TC_FC) {
-        st = tc_fc_launch(g, p, pass, a, b, bias, out, ws, s);
+        st = tc_fc_launch(gk, p, pass, a, b, bias, o, ws, s);
     } else if (p.path == GCONV_PATH_DIRECT && p.tc[0] == 1) {
-        st = tiled_launch(g, p, dt, pass, a, b, bias, out, ws, s);
+        st = tiled_launch(gk, p, dt, pass, a, b, bias, o, ws, s);
     } else if (dt == GCONV_BF16) {
-        launch_direct<__nv_bfloat16>(g, p, pass, a, b, bias, out, ws, s);
+        launch_direct<__nv_bfloat16>(gk, p, pass, a, b, bias, o, ws, s);
     } else {
-        launch_direct<float>(g, p, pass, a, b, bias, out, ws, s);
+        launch_direct<float>(gk, p, pass, a, b, bias, o, ws, s);
     }
     if (st != GCONV_OK) return st;
+    if (db) {
+        // the bias gradient of the same gradOutput (b is dy for the weight gradient)
+        if (dt == GCONV_BF16) launch_direct<__nv_bfloat16>(g, pb, GCONV_PASS_BWD_BIAS, b, nullptr, nullptr, db, ws, s);
+        else launch_direct<float>(g, pb, GCONV_PASS_BWD_BIAS, b, nullptr, nullptr, db, ws, s);
+    }
     return cudaGetLastError() == cudaSuccess ? GCONV_OK : GCONV_ERR_CUDA;
 }
 
@@ -396,42 +441,43 @@ using namespace gconv;
 
 #define GEO_ARGS int N, int C_in, int H, int W, int C_out, int kH, int kW, int stride, \
                  int pad_top, int pad_bottom, int pad_left, int pad_right, int dilation, int groups
-#define GEO_ARRAY {N, C_in, H, W, C_out, kH, kW, stride, pad_top, pad_bottom, pad_left, pad_right, dilation, groups}
+#define MAKE_GEOM(g) make_geom(N, C_in, H, W, C_out, kH, kW, stride, pad_top, pad_bottom, pad_left, \
+                               pad_right, dilation, groups, &(g))
 
-extern "C" {
+namespace {
 
-gconv_status gconv_out_shape(GEO_ARGS, int *Ho, int *Wo)
+gconv_status out_shape_of(const Geom &g, int *Ho, int *Wo)
 {
     if (!Ho || !Wo) return GCONV_ERR_INVALID_ARG;
-    Geom g;
-    gconv_status st = make_geom(N, C_in, H, W, C_out, kH, kW, stride, pad_top, pad_bottom,
-                                pad_left, pad_right, dilation, groups, &g);
-    if (st != GCONV_OK) return st;
     *Ho = g.Ho;
     *Wo = g.Wo;
     return GCONV_OK;
 }
 
-size_t gconv_workspace_size(GEO_ARGS, gconv_dtype dtype, gconv_pass pass)
+bool valid_dtype_pass(gconv_dtype dtype, gconv_pass pass)
 {
-    Geom g;
-    if (make_geom(N, C_in, H, W, C_out, kH, kW, stride, pad_top, pad_bottom, pad_left, pad_right,
-                  dilation, groups, &g) != GCONV_OK)
-        return (size_t)-1;
-    if ((dtype != GCONV_F32 && dtype != GCONV_BF16) || pass < GCONV_PASS_FWD || pass > GCONV_PASS_BWD_BIAS)
-        return (size_t)-1;
-    const Plan p = plan_pass(g, dtype, pass);
-    return p.path < 0 ? (size_t)-1 : p.ws_bytes;
+    return (dtype == GCONV_F32 || dtype == GCONV_BF16) && pass >= GCONV_PASS_FWD && pass <= GCONV_PASS_BWD_BIAS;
 }
 
-gconv_status gconv_plan(GEO_ARGS, gconv_dtype dtype, gconv_pass pass, int *path, int *launches)
+// Workspace of a pass; the weight gradient's covers the bias gradient it may compute in
+// the same call.
+size_t workspace_of(const Geom &g, gconv_dtype dtype, gconv_pass pass)
 {
-    Geom g;
-    gconv_status st = make_geom(N, C_in, H, W, C_out, kH, kW, stride, pad_top, pad_bottom,
-                                pad_left, pad_right, dilation, groups, &g);
-    if (st != GCONV_OK) return st;
-    if ((dtype != GCONV_F32 && dtype != GCONV_BF16) || pass < GCONV_PASS_FWD || pass > GCONV_PASS_BWD_BIAS)
-        return GCONV_ERR_INVALID_ARG;
+    if (!valid_dtype_pass(dtype, pass)) return (size_t)-1;
+    const Plan p = plan_pass(g, dtype, pass);
+    if (p.path < 0) return (size_t)-1;
+    size_t ws = p.ws_bytes;
+    if (pass == GCONV_PASS_BWD_WEIGHT) {
+        const Plan pb = plan_pass(g, dtype, GCONV_PASS_BWD_BIAS);
+        if (pb.path < 0) return (size_t)-1;
+        ws = std::max(ws, pb.ws_bytes);
+    }
+    return ws;
+}
+
+gconv_status plan_of(const Geom &g, gconv_dtype dtype, gconv_pass pass, int *path, int *launches)
+{
+    if (!valid_dtype_pass(dtype, pass)) return GCONV_ERR_INVALID_ARG;
     const Plan p = plan_pass(g, dtype, pass);
     if (p.path < 0) return GCONV_ERR_UNSUPPORTED;
     if (path) *path = p.path;
@@ -439,56 +485,154 @@ gconv_status gconv_plan(GEO_ARGS, gconv_dtype dtype, gconv_pass pass, int *path,
     return GCONV_OK;
 }
 
+gconv_status noalloc_weight(const Geom &g, gconv_dtype dtype, const void *x, const void *dy, float *dw, void *stream)
+{
+    if (dtype != GCONV_F32 && dtype != GCONV_BF16) return GCONV_ERR_INVALID_ARG;
+    if (g.N == 0) return zero_empty_sum(g, GCONV_PASS_BWD_WEIGHT, dw, stream);
+    const size_t need = workspace_of(g, dtype, GCONV_PASS_BWD_WEIGHT);
+    if (need == (size_t)-1) return GCONV_ERR_UNSUPPORTED;
+    if (need > kNoAllocScratchBytes) return GCONV_ERR_WORKSPACE;   // beyond the fixed 128 MiB scratch
+    void *scratch = nullptr;
+    if (need > 0) {
+        scratch = noalloc_scratch_ptr();
+        if (!scratch) return GCONV_ERR_CUDA;
+    }
+    return run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_WEIGHT, x, dy, nullptr, dw, nullptr, scratch,
+                    kNoAllocScratchBytes, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+gconv_status gconv_out_shape(GEO_ARGS, int *Ho, int *Wo)
+{
+    Geom g;
+    const gconv_status st = MAKE_GEOM(g);
+    return st != GCONV_OK ? st : out_shape_of(g, Ho, Wo);
+}
+
+size_t gconv_workspace_size(GEO_ARGS, gconv_dtype dtype, gconv_pass pass)
+{
+    Geom g;
+    return MAKE_GEOM(g) != GCONV_OK ? (size_t)-1 : workspace_of(g, dtype, pass);
+}
+
+gconv_status gconv_plan(GEO_ARGS, gconv_dtype dtype, gconv_pass pass, int *path, int *launches)
+{
+    Geom g;
+    const gconv_status st = MAKE_GEOM(g);
+    return st != GCONV_OK ? st : plan_of(g, dtype, pass, path, launches);
+}
+
 gconv_status gconv_fwd(GEO_ARGS, gconv_dtype dtype, const void *x, const void *w, const void *bias,
                        float *y, void *workspace, size_t workspace_bytes, void *stream)
 {
-    const int geo[14] = GEO_ARRAY;
-    return run_pass(geo, dtype, GCONV_PASS_FWD, x, w, bias, y, workspace, workspace_bytes, stream);
+    Geom g;
+    const gconv_status st = MAKE_GEOM(g);
+    return st != GCONV_OK ? st : run_pass(g, dtype, GCONV_F32, GCONV_PASS_FWD, x, w, bias, y, nullptr,
+                                          workspace, workspace_bytes, stream);
 }
 
 gconv_status gconv_bwd_data(GEO_ARGS, gconv_dtype dtype, const void *dy, const void *w, float *dx,
                             void *workspace, size_t workspace_bytes, void *stream)
 {
-    const int geo[14] = GEO_ARRAY;
-    return run_pass(geo, dtype, GCONV_PASS_BWD_DATA, dy, w, nullptr, dx, workspace, workspace_bytes, stream);
+    Geom g;
+    const gconv_status st = MAKE_GEOM(g);
+    return st != GCONV_OK ? st : run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_DATA, dy, w, nullptr, dx, nullptr,
+                                          workspace, workspace_bytes, stream);
 }
 
 gconv_status gconv_bwd_weight(GEO_ARGS, gconv_dtype dtype, const void *x, const void *dy, float *dw,
                               void *workspace, size_t workspace_bytes, void *stream)
 {
-    const int geo[14] = GEO_ARRAY;
-    return run_pass(geo, dtype, GCONV_PASS_BWD_WEIGHT, x, dy, nullptr, dw, workspace, workspace_bytes, stream);
+    Geom g;
+    const gconv_status st = MAKE_GEOM(g);
+    return st != GCONV_OK ? st : run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_WEIGHT, x, dy, nullptr, dw, nullptr,
+                                          workspace, workspace_bytes, stream);
 }
 
 gconv_status gconv_bwd_bias(GEO_ARGS, gconv_dtype dtype, const void *dy, float *db, void *workspace,
                             size_t workspace_bytes, void *stream)
 {
-    const int geo[14] = GEO_ARRAY;
-    return run_pass(geo, dtype, GCONV_PASS_BWD_BIAS, dy, nullptr, nullptr, db, workspace, workspace_bytes, stream);
+    Geom g;
+    const gconv_status st = MAKE_GEOM(g);
+    return st != GCONV_OK ? st : run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_BIAS, dy, nullptr, nullptr, db,
+                                          nullptr, workspace, workspace_bytes, stream);
 }
 
 gconv_status gconv_bwd_weight_noalloc(GEO_ARGS, gconv_dtype dtype, const void *x, const void *dy, float *dw,
                                       void *stream)
 {
     Geom g;
-    gconv_status st = make_geom(N, C_in, H, W, C_out, kH, kW, stride, pad_top, pad_bottom, pad_left, pad_right,
-                                dilation, groups, &g);
-    if (st != GCONV_OK) return st;
-    if (dtype != GCONV_F32 && dtype != GCONV_BF16) return GCONV_ERR_INVALID_ARG;
-    if (g.N == 0) return zero_empty_sum(g, GCONV_PASS_BWD_WEIGHT, dw, stream);
-    const Plan p = plan_pass(g, dtype, GCONV_PASS_BWD_WEIGHT);
-    if (p.path < 0) return GCONV_ERR_UNSUPPORTED;
-    if (p.ws_bytes > kNoAllocScratchBytes) return GCONV_ERR_WORKSPACE;   // beyond the fixed 128 MiB scratch
-    void *scratch = nullptr;
-    if (p.ws_bytes > 0) {
-        scratch = noalloc_scratch_ptr();
-        if (!scratch) return GCONV_ERR_CUDA;
-    }
-    const int geo[14] = GEO_ARRAY;
-    return run_pass(geo, dtype, GCONV_PASS_BWD_WEIGHT, x, dy, nullptr, dw, scratch, kNoAllocScratchBytes, stream);
+    const gconv_status st = MAKE_GEOM(g);
+    return st != GCONV_OK ? st : noalloc_weight(g, dtype, x, dy, dw, stream);
 }
 
 size_t gconv_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+// ---- per-axis geometry ---------------------------------------------------------
+
+gconv_status gconv_out_shape_ex(const gconv_geometry *geometry, int *Ho, int *Wo)
+{
+    Geom g;
+    const gconv_status st = make_geom_ex(geometry, &g);
+    return st != GCONV_OK ? st : out_shape_of(g, Ho, Wo);
+}
+
+size_t gconv_workspace_size_ex(const gconv_geometry *geometry, gconv_dtype dtype, gconv_pass pass)
+{
+    Geom g;
+    return make_geom_ex(geometry, &g) != GCONV_OK ? (size_t)-1 : workspace_of(g, dtype, pass);
+}
+
+gconv_status gconv_plan_ex(const gconv_geometry *geometry, gconv_dtype dtype, gconv_pass pass, int *path,
+                           int *launches)
+{
+    Geom g;
+    const gconv_status st = make_geom_ex(geometry, &g);
+    return st != GCONV_OK ? st : plan_of(g, dtype, pass, path, launches);
+}
+
+gconv_status gconv_fwd_ex(const gconv_geometry *geometry, gconv_dtype dtype, gconv_dtype out_dtype, const void *x,
+                          const void *w, const void *bias, void *y, void *workspace, size_t workspace_bytes,
+                          void *stream)
+{
+    Geom g;
+    const gconv_status st = make_geom_ex(geometry, &g);
+    return st != GCONV_OK ? st : run_pass(g, dtype, out_dtype, GCONV_PASS_FWD, x, w, bias, y, nullptr, workspace,
+                                          workspace_bytes, stream);
+}
+
+gconv_status gconv_bwd_data_ex(const gconv_geometry *geometry, gconv_dtype dtype, gconv_dtype out_dtype,
+                               const void *dy, const void *w, void *dx, void *workspace, size_t workspace_bytes,
+                               void *stream)
+{
+    Geom g;
+    const gconv_status st = make_geom_ex(geometry, &g);
+    return st != GCONV_OK ? st : run_pass(g, dtype, out_dtype, GCONV_PASS_BWD_DATA, dy, w, nullptr, dx, nullptr,
+                                          workspace, workspace_bytes, stream);
+}
+
+gconv_status gconv_bwd_weight_ex(const gconv_geometry *geometry, gconv_dtype dtype, const void *x, const void *dy,
+                                 float *dw, float *db, void *workspace, size_t workspace_bytes, void *stream)
+{
+    Geom g;
+    const gconv_status st = make_geom_ex(geometry, &g);
+    return st != GCONV_OK ? st : run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_WEIGHT, x, dy, nullptr, dw, db,
+                                          workspace, workspace_bytes, stream);
+}
+
+gconv_status gconv_bwd_bias_ex(const gconv_geometry *geometry, gconv_dtype dtype, const void *dy, float *db,
+                               void *workspace, size_t workspace_bytes, void *stream)
+{
+    Geom g;
+    const gconv_status st = make_geom_ex(geometry, &g);
+    return st != GCONV_OK ? st : run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_BIAS, dy, nullptr, nullptr, db,
+                                          nullptr, workspace, workspace_bytes, stream);
+}
+
+// ---- status, host step ----------------------------------------------------------
 
 gconv_status gconv_check_device_error(void *stream)
 {
@@ -520,9 +664,7 @@ const char *gconv_status_string(gconv_status status)
 size_t gconv_step_device_bytes(GEO_ARGS, gconv_dtype dtype, int with_bias)
 {
     Geom g;
-    if (make_geom(N, C_in, H, W, C_out, kH, kW, stride, pad_top, pad_bottom, pad_left, pad_right,
-                  dilation, groups, &g) != GCONV_OK)
-        return (size_t)-1;
+    if (MAKE_GEOM(g) != GCONV_OK) return (size_t)-1;
     if (dtype != GCONV_F32 && dtype != GCONV_BF16) return (size_t)-1;
     StepLayout L;
     return step_layout(g, dtype, with_bias != 0, &L) ? L.total : (size_t)-1;
@@ -532,10 +674,8 @@ gconv_status gconv_step_host(GEO_ARGS, gconv_dtype dtype, const void *x, const v
                              const void *dy, float *y, float *dx, float *dw, float *db,
                              void *device_buffer, size_t device_bytes, void *stream)
 {
-    const int geo[14] = GEO_ARRAY;
     Geom g;
-    gconv_status st = make_geom(N, C_in, H, W, C_out, kH, kW, stride, pad_top, pad_bottom, pad_left,
-                                pad_right, dilation, groups, &g);
+    gconv_status st = MAKE_GEOM(g);
     if (st != GCONV_OK) return st;
     if (dtype != GCONV_F32 && dtype != GCONV_BF16) return GCONV_ERR_INVALID_ARG;
     if (!x || !w || !dy || !y || !dx || !dw || !db) return GCONV_ERR_INVALID_ARG;
@@ -586,13 +726,12 @@ gconv_status gconv_step_host(GEO_ARGS, gconv_dtype dtype, const void *x, const v
     STEP_CHECK(cudaEventRecord(ss->dy_in, ss->in));
     // forward, chunk by chunk; each chunk's result goes back as soon as it is ready
     for (int c = 0; c < nfc; ++c) {
-        int geo_c[14];
-        std::copy(geo, geo + 14, geo_c);
-        geo_c[0] = n_lo[c + 1] - n_lo[c];
+        Geom gc = g;
+        gc.N = n_lo[c + 1] - n_lo[c];
         const size_t xo = (size_t)n_lo[c] * x_img, yo = (size_t)n_lo[c] * y_img;
         STEP_CHECK(cudaStreamWaitEvent(C, ss->x_in[c], 0));
-        st = run_pass(geo_c, dtype, GCONV_PASS_FWD, static_cast<uint8_t *>(xd) + xo, wd, bd,
-                      reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(yd) + yo), wsd, L.nws, C);
+        st = run_pass(gc, dtype, GCONV_F32, GCONV_PASS_FWD, static_cast<uint8_t *>(xd) + xo, wd, bd,
+                      reinterpret_cast<uint8_t *>(yd) + yo, nullptr, wsd, L.nws, C);
         if (st != GCONV_OK) return st;
         STEP_CHECK(cudaEventRecord(ss->y_done[c], C));
         STEP_CHECK(cudaStreamWaitEvent(ss->out, ss->y_done[c], 0));
@@ -605,9 +744,9 @@ gconv_status gconv_step_host(GEO_ARGS, gconv_dtype dtype, const void *x, const v
     const Out outs[4] = {{y, yd, L.ny}, {dx, dxd, L.ndx}, {dw, dwd, L.ndw}, {db, dbd, L.ndb}};
     for (int pass = GCONV_PASS_BWD_DATA; pass <= GCONV_PASS_BWD_BIAS; ++pass) {
         switch (pass) {
-        case GCONV_PASS_BWD_DATA: st = run_pass(geo, dtype, GCONV_PASS_BWD_DATA, dyd, wd, nullptr, dxd, wsd, L.nws, C); break;
-        case GCONV_PASS_BWD_WEIGHT: st = run_pass(geo, dtype, GCONV_PASS_BWD_WEIGHT, xd, dyd, nullptr, dwd, wsd, L.nws, C); break;
-        default: st = run_pass(geo, dtype, GCONV_PASS_BWD_BIAS, dyd, nullptr, nullptr, dbd, wsd, L.nws, C); break;
+        case GCONV_PASS_BWD_DATA: st = run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_DATA, dyd, wd, nullptr, dxd, nullptr, wsd, L.nws, C); break;
+        case GCONV_PASS_BWD_WEIGHT: st = run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_WEIGHT, xd, dyd, nullptr, dwd, nullptr, wsd, L.nws, C); break;
+        default: st = run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_BIAS, dyd, nullptr, nullptr, dbd, nullptr, wsd, L.nws, C); break;
         }
         if (st != GCONV_OK) return st;
         STEP_CHECK(cudaEventRecord(ss->pass_done[pass], C));

@@ -34,24 +34,24 @@ direct_fwd_kernel(Geom g, const T *__restrict__ x, const T *__restrict__ w,
         const int grp = o / g.Cgo;
         const T *xp = x + ((int64_t)n * g.Cin + (int64_t)grp * g.Cgi) * g.H * g.W;
         const T *wp = w + (int64_t)o * g.Cgi * KK;
-        const int ih0 = oh * g.s - g.pt, iw0 = ow * g.s - g.pl;
+        const int ih0 = oh * g.s_h - g.pt, iw0 = ow * g.s_w - g.pl;
         float acc = 0.f;
         for (int c = 0; c < g.Cgi; ++c) {
             const T *xc = xp + (int64_t)c * g.H * g.W;
             const T *wc = wp + c * KK;
             for (int kh = 0; kh < g.kH; ++kh) {
-                const int ih = ih0 + kh * g.d;
+                const int ih = ih0 + kh * g.d_h;
                 if (ih < 0 || ih >= g.H) continue;
                 const T *xr = xc + (int64_t)ih * g.W;
                 for (int kw = 0; kw < g.kW; ++kw) {
-                    const int iw = iw0 + kw * g.d;
+                    const int iw = iw0 + kw * g.d_w;
                     if (iw < 0 || iw >= g.W) continue;
                     acc = fmaf(to_f(wc[kh * g.kW + kw]), to_f(__ldg(xr + iw)), acc);
                 }
             }
         }
         if (bias) acc += to_f(bias[o]);
-        y[e] = acc;
+        store_out(y, e, acc, g.out_bf16);
     }
 }
 
@@ -76,14 +76,14 @@ direct_bwd_data_kernel(Geom g, const T *__restrict__ dy, const T *__restrict__ w
         const int grp = ci / g.Cgi, c = ci - grp * g.Cgi;
         float acc = 0.f;
         for (int kh = 0; kh < g.kH; ++kh) {
-            const int th = ih + g.pt - kh * g.d;
-            if (th < 0 || th % g.s) continue;
-            const int oh = th / g.s;
+            const int th = ih + g.pt - kh * g.d_h;
+            if (th < 0 || th % g.s_h) continue;
+            const int oh = th / g.s_h;
             if (oh >= g.Ho) continue;
             for (int kw = 0; kw < g.kW; ++kw) {
-                const int tw = iw + g.pl - kw * g.d;
-                if (tw < 0 || tw % g.s) continue;
-                const int ow = tw / g.s;
+                const int tw = iw + g.pl - kw * g.d_w;
+                if (tw < 0 || tw % g.s_w) continue;
+                const int ow = tw / g.s_w;
                 if (ow >= g.Wo) continue;
                 const T *dyp = dy + (((int64_t)n * g.Cout + (int64_t)grp * g.Cgo) * g.Ho + oh) * g.Wo + ow;
                 const T *wp = w + ((int64_t)grp * g.Cgo * g.Cgi + c) * KK + kh * g.kW + kw;
@@ -93,7 +93,7 @@ direct_bwd_data_kernel(Geom g, const T *__restrict__ dy, const T *__restrict__ w
                     acc = fmaf(to_f(wp[oo * ws]), to_f(__ldg(dyp + oo * dys)), acc);
             }
         }
-        dx[e] = acc;
+        store_out(dx, e, acc, g.out_bf16);
     }
 }
 
@@ -148,8 +148,8 @@ direct_bwd_weight_kernel(Geom g, const T *__restrict__ x, const T *__restrict__ 
                 if (e < E) {
                     const int c = e / KK, kk = e - c * KK;
                     const int kh = kk / g.kW, kw = kk - kh * g.kW;
-                    const int ih = oh * g.s - g.pt + kh * g.d;
-                    const int iw = ow * g.s - g.pl + kw * g.d;
+                    const int ih = oh * g.s_h - g.pt + kh * g.d_h;
+                    const int iw = ow * g.s_w - g.pl + kw * g.d_w;
                     if (ih >= 0 && ih < g.H && iw >= 0 && iw < g.W)
                         acc[j] = fmaf(dv, to_f(__ldg(xn + ((int64_t)c * g.H + ih) * g.W + iw)), acc[j]);
                 }

@@ -55,7 +55,7 @@ constexpr size_t kMaxSmem = 220 * 1024;
 
 // One staged operand: channels [0, nch) (a multiple of 8) of image `n` starting at
 // channel `c_first` of a tensor [N][Ctot][IH][IW].  Plane row r / column c maps to
-// input (us*(row_base + r) + ph[P], us*(col0 + c) + pw[P]).  Rows r >= rows_valid,
+// input (us_h*(row_base + r) + ph[P], us_w*(col0 + c) + pw[P]).  Rows r >= rows_valid,
 // channels >= nch_valid and coordinates outside the image read as 0.
 struct StageDesc {
     const __nv_bfloat16 *U;
@@ -63,7 +63,7 @@ struct StageDesc {
     int64_t chan0;                // element index of (n, c_first, 0, 0)
     int IH, IW;
     int nch, nch_valid;
-    int us, row_base, col0;
+    int us_h, us_w, row_base, col0;
     int nplanes, Wp, plane_elems, rows_valid;
     int scr_stride;               // scratch elements per channel (multiple of 8)
     const int *ph, *pw;
@@ -77,8 +77,8 @@ __device__ __forceinline__ RowRange stage_rows(const StageDesc &d)
     int pmin = d.ph[0], pmax = d.ph[0];
     for (int P = 1; P < d.nplanes; ++P) { pmin = min(pmin, d.ph[P]); pmax = max(pmax, d.ph[P]); }
     RowRange r;
-    r.lo = max(0, d.us * d.row_base + pmin);
-    r.hi = min(d.IH - 1, d.us * (d.row_base + rows - 1) + pmax);
+    r.lo = max(0, d.us_h * d.row_base + pmin);
+    r.hi = min(d.IH - 1, d.us_h * (d.row_base + rows - 1) + pmax);
     return r;
 }
 
@@ -114,8 +114,8 @@ __device__ __forceinline__ void build_pos_table(const StageDesc &d, RowRange rr,
     for (int q = tid; q < total; q += kStageThreads) {
         const int P = q / d.plane_elems, i = q - P * d.plane_elems;
         const int r = i / d.Wp, c = i - r * d.Wp;
-        const int row = d.us * (d.row_base + r) + d.ph[P];
-        const int col = d.us * (d.col0 + c) + d.pw[P];
+        const int row = d.us_h * (d.row_base + r) + d.ph[P];
+        const int col = d.us_w * (d.col0 + c) + d.pw[P];
         const bool inside = r < d.rows_valid && row >= rr.lo && row <= rr.hi && col >= 0 && col < d.IW;
         tab[q] = inside ? (row - rr.lo) * d.IW + col : -1;
     }
@@ -161,13 +161,14 @@ struct CorrParams {
     const __nv_bfloat16 *U;     // input activations [N][G*Cu][IH][IW]
     const uint8_t *Wpk;         // packed weight blocks for this launch
     const __nv_bfloat16 *bias;  // [G*Cv] or nullptr
-    float *V;                   // output [N][G*Cv][OH][OW]
+    float *V;                   // output [N][G*Cv][OH][OW] (fp32, or bf16 when out_bf16)
+    int out_bf16;
     unsigned int *err;
     uint64_t wait_ns;
     int N, G, Cu, Cv, IH, IW, OH, OW;
     int Qh, Qw;                 // output grid (of this phase)
-    int vs, vr, vc;             // output element (vs*q + vr, vs*c + vc)
-    int us, row0, col0;         // plane sampling of U
+    int vs_h, vs_w, vr, vc;     // output element (vs_h*q + vr, vs_w*c + vc)
+    int us_h, us_w, row0, col0; // plane sampling of U
     int TH, Wp, MB, NT;         // tile rows, padded pitch, 128-row M blocks, N tile
     int n_rowblk, n_ntile, nkc; // tiles in rows, in output channels; 16-channel chunks
     int nplanes, plane_elems, scr_stride;
@@ -235,7 +236,7 @@ corr_kernel(const __grid_constant__ CorrParams p)
         d.U = p.U;
         d.U_elems = (int64_t)p.N * p.G * p.Cu * p.IH * p.IW;
         d.IH = p.IH; d.IW = p.IW; d.nch = 16;
-        d.us = p.us; d.row_base = qh0 + p.row0; d.col0 = p.col0;
+        d.us_h = p.us_h; d.us_w = p.us_w; d.row_base = qh0 + p.row0; d.col0 = p.col0;
         d.nplanes = p.nplanes; d.Wp = p.Wp; d.plane_elems = p.plane_elems; d.rows_valid = 1 << 30;
         d.scr_stride = p.scr_stride; d.ph = p.plane_ph; d.pw = p.plane_pw;
         const RowRange rr = stage_rows(d);
@@ -340,12 +341,12 @@ corr_kernel(const __grid_constant__ CorrParams p)
         // tcgen05.ld is warp-collective: take the decision once per warp
         ready = __all_sync(0xffffffffu, ready && !abort_flag);
         const int64_t out_hw = (int64_t)p.OH * p.OW;
-        float *vbase = p.V + ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv) * out_hw;
+        const int64_t vbase = ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv) * out_hw;   // element index in V
         for (int mb = 0; mb < p.MB; ++mb) {
             const int m = mb * 128 + lg * 32 + lane;
             const int r = m / p.Wp, c = m - r * p.Wp;
             const bool valid = ready && m < p.TH * p.Wp && c < p.Qw && qh0 + r < p.Qh;
-            const int64_t pix = (int64_t)(p.vs * (qh0 + r) + p.vr) * p.OW + (p.vs * c + p.vc);
+            const int64_t pix = (int64_t)(p.vs_h * (qh0 + r) + p.vr) * p.OW + (p.vs_w * c + p.vc);
             for (int v0 = half * 16; v0 < p.NT; v0 += 32) {
                 uint32_t acc[16];
                 if (p.ntaps > 0 && ready) {
@@ -362,7 +363,7 @@ corr_kernel(const __grid_constant__ CorrParams p)
                         if (v < p.Cv) {
                             float val = __uint_as_float(acc[j]);
                             if (p.bias) val += __bfloat162float(p.bias[g * p.Cv + v]);
-                            vbase[(int64_t)v * out_hw + pix] = val;
+                            store_out(p.V, vbase + (int64_t)v * out_hw + pix, val, p.out_bf16);
                         }
                     }
                 }
@@ -442,8 +443,8 @@ blockify_kernel(const __grid_constant__ BlockifyParams p)
     store_rows_coalesced(w, total, reinterpret_cast<uint4 *>(p.out));
 }
 
-// Stride-2 form of the blocked copy for the weight gradient: out[p][n][g][j][r][c][0..63]
-// = in[n][g*Cg + 64*j + e][r*s + roff[p]][c*s + coff[p]], zero outside the image.  Plane
+// Strided form of the blocked copy for the weight gradient: out[p][n][g][j][r][c][0..63]
+// = in[n][g*Cg + 64*j + e][r*s_h + roff[p]][c*s_w + coff[p]], zero outside the image.  Plane
 // p holds one stride phase of the padded input, so a strided tap of that phase reads
 // the plane at a plain (row, column) shift; each plane is laid out exactly like the
 // stride-1 blocked copy.
@@ -451,7 +452,7 @@ struct PhaseBlockifyParams {
     const __nv_bfloat16 *in;
     __nv_bfloat16 *out;
     int N, G, Cg, nchunk, IH, IW, R, C;
-    int s, nplane;
+    int s_h, s_w, nplane;
     int roff[kMaxPlanes], coff[kMaxPlanes];
 };
 
@@ -473,7 +474,7 @@ blockify_phase_kernel(const __grid_constant__ PhaseBlockifyParams p)
         const int64_t t = blk / p.nchunk;
         const int64_t ng = t % ((int64_t)p.N * p.G);       // n*G + g
         const int pl = (int)(t / ((int64_t)p.N * p.G));
-        const int row = r * p.s + p.roff[pl], col = c * p.s + p.coff[pl];
+        const int row = r * p.s_h + p.roff[pl], col = c * p.s_w + p.coff[pl];
         const bool inside = row >= 0 && row < p.IH && col >= 0 && col < p.IW;
         const int cvalid = inside ? min(64, p.Cg - 64 * j) : 0;
         const int64_t plane = (int64_t)p.IH * p.IW;
@@ -865,7 +866,8 @@ struct Corr2Params {
     const __nv_bfloat16 *UB;    // blocked input [N][G][nchu][R][Wp][64]
     const uint8_t *Wpk;         // packed weight blocks [G][n_vtile][nchu][ntaps][16 KB]
     const __nv_bfloat16 *bias;  // [G*Cv] or nullptr
-    float *V;                   // output [N][G*Cv][Qh][Qw]
+    float *V;                   // output [N][G*Cv][Qh][Qw] (fp32, or bf16 when out_bf16)
+    int out_bf16;
     unsigned int *err;
     uint64_t wait_ns;
     int N, G, Cu, Cv, Qh, Qw, R, Wp, nchu;
@@ -1152,7 +1154,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                 float *tbp = epi + (2 + part) * (32 * 17);          // lower warp's sums
                 const int v0 = part * 32;
                 const int vcount = min(32, p.Cv - v0);
-                float *vout = p.V + ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv + v0) * out_hw;
+                const int64_t vout = ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv + v0) * out_hw;   // element index
                 const float bias_lane = (p.bias && !upper && lane < vcount) ? __bfloat162float(p.bias[g * p.Cv + v0 + lane]) : 0.f;
                 for (int pc = 0; pc < p.tile_pos; pc += 16) {
                     uint32_t a[16];
@@ -1172,8 +1174,9 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                         const int pos = p0 + jc;
                         const int qh = pos / p.Wp, qw = pos - qh * p.Wp;
                         if (jc < p.tile_pos && qh < p.Qh && qw < p.Qw) {
-                            float *o = vout + (int64_t)qh * p.Qw + qw;
-                            for (int vv = lane >> 4; vv < vcount; vv += 2) o[vv * out_hw] = tbp[vv * 17 + (lane & 15)];
+                            const int64_t o = vout + (int64_t)qh * p.Qw + qw;
+                            for (int vv = lane >> 4; vv < vcount; vv += 2)
+                                store_out(p.V, o + vv * out_hw, tbp[vv * 17 + (lane & 15)], p.out_bf16);
                         }
                     }
                     ptx::named_sync(2 + part, 64);   // the upper warp may overwrite hb
@@ -1181,7 +1184,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
             } else {
             const int v0 = vt * 128 + lg * 32;
             const int vcount = min(32, p.Cv - v0);
-            float *vout = p.V + ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv + v0) * out_hw;
+            const int64_t vout = ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv + v0) * out_hw;   // element index
             const float bias_lane = (p.bias && lane < vcount) ? __bfloat162float(p.bias[g * p.Cv + v0 + lane]) : 0.f;
             for (int pc = 0; pc < 256; pc += 32) {
                 uint32_t a0[16], a1[16];
@@ -1199,8 +1202,8 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                     const int pos = p0 + pc + lane;
                     const int qh = pos / p.Wp, qw = pos - qh * p.Wp;
                     if (qh < p.Qh && qw < p.Qw) {
-                        float *o = vout + (int64_t)qh * p.Qw + qw;
-                        for (int vv = 0; vv < vcount; ++vv) o[vv * out_hw] = tb[vv * 33 + lane];
+                        const int64_t o = vout + (int64_t)qh * p.Qw + qw;
+                        for (int vv = 0; vv < vcount; ++vv) store_out(p.V, o + vv * out_hw, tb[vv * 33 + lane], p.out_bf16);
                     }
                     __syncwarp();
                 }
@@ -1339,7 +1342,7 @@ int floordiv(int a, int b) { return (a >= 0) ? a / b : -((-a + b - 1) / b); }
 int next_pow2(int v) { int p = 32; while (p < v) p <<= 1; return p; }
 int round_up(int v, int m) { return (v + m - 1) / m * m; }
 
-// A tap reads input (us*(q_h + A) + ph, us*(q_w + B) + pw) for output (q_h, q_w).
+// A tap reads input (us_h*(q_h + A) + ph, us_w*(q_w + B) + pw) for output (q_h, q_w).
 struct Tap { int A, B, ph, pw, k; };
 
 // Planes, origin and per-tap offsets shared by the correlation and weight kernels.
@@ -1349,14 +1352,14 @@ struct TapGeometry {
     std::vector<int> tap_plane, tap_a, tap_b;
 };
 
-bool tap_geometry(const std::vector<Tap> &taps, int us, TapGeometry *tg)
+bool tap_geometry(const std::vector<Tap> &taps, int us_h, int us_w, TapGeometry *tg)
 {
     if (taps.empty()) { tg->nplanes = 1; return true; }
     std::vector<int> ids;
     int minA = taps[0].A, minB = taps[0].B;
     for (const Tap &t : taps) { minA = std::min(minA, t.A); minB = std::min(minB, t.B); }
     for (const Tap &t : taps) {
-        const int id = t.ph * us + t.pw;
+        const int id = t.ph * us_w + t.pw;
         int idx = (int)(std::find(ids.begin(), ids.end(), id) - ids.begin());
         if (idx == (int)ids.size()) ids.push_back(id);
         tg->tap_plane.push_back(idx);
@@ -1367,7 +1370,7 @@ bool tap_geometry(const std::vector<Tap> &taps, int us, TapGeometry *tg)
     }
     if ((int)ids.size() > kMaxPlanes) return false;
     tg->nplanes = (int)ids.size();
-    for (int i = 0; i < tg->nplanes; ++i) { tg->plane_ph[i] = ids[i] / us; tg->plane_pw[i] = ids[i] % us; }
+    for (int i = 0; i < tg->nplanes; ++i) { tg->plane_ph[i] = ids[i] / us_w; tg->plane_pw[i] = ids[i] % us_w; }
     tg->row0 = minA;
     tg->col0 = minB;
     return true;
@@ -1378,9 +1381,9 @@ std::vector<Tap> forward_taps(const Geom &g)
     std::vector<Tap> taps;
     for (int kh = 0; kh < g.kH; ++kh)
         for (int kw = 0; kw < g.kW; ++kw) {
-            const int eh = kh * g.d - g.pt, ew = kw * g.d - g.pl;
-            const int A = floordiv(eh, g.s), B = floordiv(ew, g.s);
-            taps.push_back(Tap{A, B, eh - A * g.s, ew - B * g.s, kh * g.kW + kw});
+            const int eh = kh * g.d_h - g.pt, ew = kw * g.d_w - g.pl;
+            const int A = floordiv(eh, g.s_h), B = floordiv(ew, g.s_w);
+            taps.push_back(Tap{A, B, eh - A * g.s_h, ew - B * g.s_w, kh * g.kW + kw});
         }
     return taps;
 }
@@ -1393,8 +1396,8 @@ struct CorrLaunch {
     int grid = 0;
 };
 
-bool build_corr(const Geom &g, bool bwd_data, const std::vector<Tap> &taps, int Qh, int Qw, int vs, int vr,
-                int vc, int us, CorrLaunch *L)
+bool build_corr(const Geom &g, bool bwd_data, const std::vector<Tap> &taps, int Qh, int Qw, int vs_h, int vs_w,
+                int vr, int vc, int us_h, int us_w, CorrLaunch *L)
 {
     CorrParams &c = L->cp;
     c = CorrParams{};
@@ -1402,13 +1405,13 @@ bool build_corr(const Geom &g, bool bwd_data, const std::vector<Tap> &taps, int 
     const int Cv = bwd_data ? g.Cgi : g.Cgo;
     if (Cu < 8 || Cv < 16 || (int)taps.size() > kMaxTaps) return false;
     TapGeometry tg;
-    if (!tap_geometry(taps, us, &tg)) return false;
+    if (!tap_geometry(taps, us_h, us_w, &tg)) return false;
     c.N = g.N; c.G = g.G; c.Cu = Cu; c.Cv = Cv;
     c.IH = bwd_data ? g.Ho : g.H;
     c.IW = bwd_data ? g.Wo : g.W;
     c.OH = bwd_data ? g.H : g.Ho;
     c.OW = bwd_data ? g.W : g.Wo;
-    c.Qh = Qh; c.Qw = Qw; c.vs = vs; c.vr = vr; c.vc = vc; c.us = us;
+    c.Qh = Qh; c.Qw = Qw; c.vs_h = vs_h; c.vs_w = vs_w; c.vr = vr; c.vc = vc; c.us_h = us_h; c.us_w = us_w;
     c.NT = std::min(256, round_up(Cv, 16));
     c.n_ntile = (Cv + c.NT - 1) / c.NT;
     c.nkc = (Cu + 15) / 16;
@@ -1433,7 +1436,7 @@ bool build_corr(const Geom &g, bool bwd_data, const std::vector<Tap> &taps, int 
         const int MBe = (TH * c.Wp + 127) / 128;
         const int plane_elems = round_up(MBe * 128 + max_off, 8);
         const int rows_touched = (plane_elems + c.Wp - 1) / c.Wp;
-        const int scr_stride = round_up((us * rows_touched + 1) * c.IW + 16, 8);
+        const int scr_stride = round_up((us_h * rows_touched + 1) * c.IW + 16, 8);
         const size_t smem = (size_t)4 * c.nplanes * plane_elems * 16 + (size_t)kWeightStages * c.bps * wblk +
                             (size_t)16 * scr_stride * 2 + (size_t)(c.nplanes * plane_elems + 16) * sizeof(int);
         if (smem > kMaxSmem) continue;
@@ -1466,27 +1469,27 @@ bool build_corr(const Geom &g, bool bwd_data, const std::vector<Tap> &taps, int 
 
 bool build_fwd(const Geom &g, CorrLaunch *L)
 {
-    if (g.s > 2) return false;
-    return build_corr(g, false, forward_taps(g), g.Ho, g.Wo, 1, 0, 0, g.s, L);
+    if (g.s_h > 2 || g.s_w > 2) return false;
+    return build_corr(g, false, forward_taps(g), g.Ho, g.Wo, 1, 1, 0, 0, g.s_h, g.s_w, L);
 }
 
 // Backward-data output phase (rh, rw): dx rows s*q + rh read dy rows q + (rh + pt - kh*d)/s.
 bool build_bwd_data_phase(const Geom &g, int rh, int rw, CorrLaunch *L, bool *empty)
 {
-    const int Qh = (g.H - rh + g.s - 1) / g.s, Qw = (g.W - rw + g.s - 1) / g.s;
+    const int Qh = (g.H - rh + g.s_h - 1) / g.s_h, Qw = (g.W - rw + g.s_w - 1) / g.s_w;
     *empty = Qh <= 0 || Qw <= 0;
     if (*empty) return true;
     std::vector<Tap> taps;
     for (int kh = 0; kh < g.kH; ++kh) {
-        const int th = rh + g.pt - kh * g.d;
-        if (((th % g.s) + g.s) % g.s) continue;
+        const int th = rh + g.pt - kh * g.d_h;
+        if (((th % g.s_h) + g.s_h) % g.s_h) continue;
         for (int kw = 0; kw < g.kW; ++kw) {
-            const int tw = rw + g.pl - kw * g.d;
-            if (((tw % g.s) + g.s) % g.s) continue;
-            taps.push_back(Tap{floordiv(th, g.s), floordiv(tw, g.s), 0, 0, kh * g.kW + kw});
+            const int tw = rw + g.pl - kw * g.d_w;
+            if (((tw % g.s_w) + g.s_w) % g.s_w) continue;
+            taps.push_back(Tap{floordiv(th, g.s_h), floordiv(tw, g.s_w), 0, 0, kh * g.kW + kw});
         }
     }
-    return build_corr(g, true, taps, Qh, Qw, g.s, rh, rw, 1, L);
+    return build_corr(g, true, taps, Qh, Qw, g.s_h, g.s_w, rh, rw, 1, 1, L);
 }
 
 
@@ -1638,11 +1641,11 @@ void set_wgrad_tma(WgradParams *w)
 
 bool build_wgrad(const Geom &g, WgradLaunch *L)
 {
-    if (g.s != 1 || g.Cgi < 8 || g.Cgo < 16) return false;
+    if (g.s_h != 1 || g.s_w != 1 || g.Cgi < 8 || g.Cgo < 16) return false;
     const std::vector<Tap> taps = forward_taps(g);
     if ((int)taps.size() > kMaxTaps) return false;
     TapGeometry tg;
-    if (!tap_geometry(taps, 1, &tg)) return false;
+    if (!tap_geometry(taps, 1, 1, &tg)) return false;
     WgradParams &w = L->wp;
     w = WgradParams{};
     w.N = g.N; w.G = g.G; w.Cgi = g.Cgi; w.Cgo = g.Cgo; w.kHW = g.kH * g.kW;
@@ -1688,7 +1691,7 @@ struct Corr2Launch {
 // position of dx a full correlation, no phases).
 bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
 {
-    if (g.s != 1) return false;
+    if (g.s_h != 1 || g.s_w != 1) return false;
     const int Cu = bwd_data ? g.Cgo : g.Cgi;    // reduced channels (K)
     const int Cv = bwd_data ? g.Cgi : g.Cgo;    // produced channels (M)
     if (Cu < 16 || Cv < 16) return false;
@@ -1697,7 +1700,7 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
     Corr2Params &c = L->cp;
     c = Corr2Params{};
     const int Qh = bwd_data ? g.H : g.Ho, Qw = bwd_data ? g.W : g.Wo;
-    const int maxa = (g.kH - 1) * g.d, maxb = (g.kW - 1) * g.d;
+    const int maxa = (g.kH - 1) * g.d_h, maxb = (g.kW - 1) * g.d_w;
     c.N = g.N; c.G = g.G; c.Cv = Cv; c.Qh = Qh; c.Qw = Qw;
     c.Wp = Qw + maxb;
     c.R = Qh + maxa;
@@ -1708,18 +1711,18 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
     // that are neighbours (d positions apart) in a row of the kernel -- when the MMA work per
     // tile outweighs the heavier paired epilogue (measured: a 5x5 kernel over two chunks
     // gains, a 3x3 kernel over one chunk loses).
-    const bool pair = Cv <= 64 && g.kW >= 2 && g.d <= 16 && c.nchu * ntaps >= 16;
+    const bool pair = Cv <= 64 && g.kW >= 2 && g.d_w <= 16 && c.nchu * ntaps >= 16;
     Pack2Params &k = L->pk;
     k = Pack2Params{};
     int nblk = 0, maxoff = 0;
     for (int kh = 0; kh < g.kH; ++kh) {
-        const int a = bwd_data ? (g.kH - 1 - kh) * g.d : kh * g.d;
+        const int a = bwd_data ? (g.kH - 1 - kh) * g.d_h : kh * g.d_h;
         // the row's taps in increasing offset b
         std::vector<std::pair<int, int>> row;   // (b, weight tap index)
-        for (int kw = 0; kw < g.kW; ++kw) row.push_back({bwd_data ? (g.kW - 1 - kw) * g.d : kw * g.d, kh * g.kW + kw});
+        for (int kw = 0; kw < g.kW; ++kw) row.push_back({bwd_data ? (g.kW - 1 - kw) * g.d_w : kw * g.d_w, kh * g.kW + kw});
         std::sort(row.begin(), row.end());
         for (size_t i = 0; i < row.size(); ++nblk) {
-            const bool two = pair && i + 1 < row.size() && row[i + 1].first == row[i].first + g.d;
+            const bool two = pair && i + 1 < row.size() && row[i + 1].first == row[i].first + g.d_w;
             c.tap_off[nblk] = a * c.Wp + row[i].first;
             k.tk1[nblk] = row[i].second;
             k.tk2[nblk] = two ? row[i + 1].second : -1;
@@ -1728,7 +1731,7 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
         }
     }
     c.ntaps = nblk;
-    c.pair_delta = pair ? g.d : 0;
+    c.pair_delta = pair ? g.d_w : 0;
     c.nmma = pair ? 240 : 256;
     c.tile_pos = c.nmma - c.pair_delta;
     const int positions = Qh * c.Wp;   // padded output grid rows that hold real outputs
@@ -1783,11 +1786,11 @@ struct WgradPhaseLaunch {
 
 bool build_wgrad_phases(const Geom &g, WgradPhaseLaunch *L)
 {
-    if (g.s != 2 || g.Cgi < 8 || g.Cgo < 16) return false;
+    if ((g.s_h == 1 && g.s_w == 1) || g.s_h > 2 || g.s_w > 2 || g.Cgi < 8 || g.Cgo < 16) return false;
     const std::vector<Tap> taps = forward_taps(g);
     if ((int)taps.size() > kMaxTaps) return false;
     TapGeometry tg;
-    if (!tap_geometry(taps, g.s, &tg)) return false;
+    if (!tap_geometry(taps, g.s_h, g.s_w, &tg)) return false;
     WgradParams c{};
     c.N = g.N; c.G = g.G; c.Cgi = g.Cgi; c.Cgo = g.Cgo; c.kHW = g.kH * g.kW;
     c.Ho = g.Ho;
@@ -1828,10 +1831,10 @@ bool build_wgrad_phases(const Geom &g, WgradPhaseLaunch *L)
     PhaseBlockifyParams &bx = L->bx;
     bx = PhaseBlockifyParams{};
     bx.N = g.N; bx.G = g.G; bx.Cg = g.Cgi; bx.nchunk = c.ncx; bx.IH = g.H; bx.IW = g.W;
-    bx.R = c.Rx; bx.C = c.Wp; bx.s = g.s; bx.nplane = tg.nplanes;
+    bx.R = c.Rx; bx.C = c.Wp; bx.s_h = g.s_h; bx.s_w = g.s_w; bx.nplane = tg.nplanes;
     for (int pl = 0; pl < tg.nplanes; ++pl) {
-        bx.roff[pl] = tg.row0 * g.s + tg.plane_ph[pl];
-        bx.coff[pl] = tg.col0 * g.s + tg.plane_pw[pl];
+        bx.roff[pl] = tg.row0 * g.s_h + tg.plane_ph[pl];
+        bx.coff[pl] = tg.col0 * g.s_w + tg.plane_pw[pl];
     }
     BlockifyParams &by = L->by;
     by = BlockifyParams{};
@@ -1863,8 +1866,8 @@ void launch_blockify(const BlockifyParams &b, cudaStream_t s)
     blockify_kernel<<<(unsigned)((total + kBlockifyThreads - 1) / kBlockifyThreads), kBlockifyThreads, 0, s>>>(b);
 }
 
-gconv_status launch_corr2(Corr2Launch &L, const void *U, const void *w, const void *bias, float *out, uint8_t *ws,
-                          cudaStream_t s)
+gconv_status launch_corr2(Corr2Launch &L, const void *U, const void *w, const void *bias, float *out, int out_bf16,
+                          uint8_t *ws, cudaStream_t s)
 {
     unsigned int *err = device_error_word();
     if (!err) return GCONV_ERR_CUDA;
@@ -1881,6 +1884,7 @@ gconv_status launch_corr2(Corr2Launch &L, const void *U, const void *w, const vo
     L.cp.Wpk = wpk;
     L.cp.bias = static_cast<const __nv_bfloat16 *>(bias);
     L.cp.V = out;
+    L.cp.out_bf16 = out_bf16;
     L.cp.err = err;
     L.cp.wait_ns = (uint64_t)wait_limit();
     size_t trace_bytes = 0;
@@ -1892,7 +1896,7 @@ gconv_status launch_corr2(Corr2Launch &L, const void *U, const void *w, const vo
     return GCONV_OK;
 }
 
-gconv_status launch_corr(CorrLaunch &L, const void *U, const void *w, const void *bias, float *out,
+gconv_status launch_corr(CorrLaunch &L, const void *U, const void *w, const void *bias, float *out, int out_bf16,
                          uint8_t *wpk, cudaStream_t s)
 {
     unsigned int *err = device_error_word();
@@ -1908,6 +1912,7 @@ gconv_status launch_corr(CorrLaunch &L, const void *U, const void *w, const void
     L.cp.Wpk = wpk;
     L.cp.bias = static_cast<const __nv_bfloat16 *>(bias);
     L.cp.V = out;
+    L.cp.out_bf16 = out_bf16;
     L.cp.err = err;
     L.cp.wait_ns = (uint64_t)wait_limit();
     if (!smem_attr_once((const void *)corr_kernel, 0)) return GCONV_ERR_CUDA;
@@ -1938,11 +1943,11 @@ bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p)
         return true;
     }
     if (pass == GCONV_PASS_BWD_DATA) {
-        if (g.s > 2) return false;
+        if (g.s_h > 2 || g.s_w > 2) return false;
         size_t ws = 0;
         int launches = 0;
-        for (int rh = 0; rh < g.s; ++rh)
-            for (int rw = 0; rw < g.s; ++rw) {
+        for (int rh = 0; rh < g.s_h; ++rh)
+            for (int rw = 0; rw < g.s_w; ++rw) {
                 CorrLaunch L;
                 bool empty = false;
                 if (!build_bwd_data_phase(g, rh, rw, &L, &empty)) return false;
@@ -1955,7 +1960,7 @@ bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p)
         p->ws_bytes = ws;
         return true;
     }
-    if (pass == GCONV_PASS_BWD_WEIGHT && g.s == 2) {
+    if (pass == GCONV_PASS_BWD_WEIGHT && (g.s_h != 1 || g.s_w != 1)) {
         WgradPhaseLaunch L;
         if (!build_wgrad_phases(g, &L)) return false;
         p->path = GCONV_PATH_TC_IGEMM;
@@ -1980,28 +1985,28 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
     uint8_t *wsb = static_cast<uint8_t *>(ws);
     if (pass == GCONV_PASS_FWD || pass == GCONV_PASS_BWD_DATA) {
         Corr2Launch L2;
-        if (build_corr2(g, pass == GCONV_PASS_BWD_DATA, &L2)) return launch_corr2(L2, a, b, bias, out, wsb, s);
+        if (build_corr2(g, pass == GCONV_PASS_BWD_DATA, &L2)) return launch_corr2(L2, a, b, bias, out, g.out_bf16, wsb, s);
     }
     if (pass == GCONV_PASS_FWD) {
         CorrLaunch L;
         if (!build_fwd(g, &L)) return GCONV_ERR_UNSUPPORTED;
-        return launch_corr(L, a, b, bias, out, wsb, s);
+        return launch_corr(L, a, b, bias, out, g.out_bf16, wsb, s);
     }
     if (pass == GCONV_PASS_BWD_DATA) {
         size_t off = 0;
-        for (int rh = 0; rh < g.s; ++rh)
-            for (int rw = 0; rw < g.s; ++rw) {
+        for (int rh = 0; rh < g.s_h; ++rh)
+            for (int rw = 0; rw < g.s_w; ++rw) {
                 CorrLaunch L;
                 bool empty = false;
                 if (!build_bwd_data_phase(g, rh, rw, &L, &empty)) return GCONV_ERR_UNSUPPORTED;
                 if (empty) continue;
-                gconv_status st = launch_corr(L, a, b, nullptr, out, wsb + off, s);
+                gconv_status st = launch_corr(L, a, b, nullptr, out, g.out_bf16, wsb + off, s);
                 if (st != GCONV_OK) return st;
                 off += (L.wpk_bytes + 255) / 256 * 256;
             }
         return GCONV_OK;
     }
-    if (pass == GCONV_PASS_BWD_WEIGHT && g.s == 2) {
+    if (pass == GCONV_PASS_BWD_WEIGHT && (g.s_h != 1 || g.s_w != 1)) {
         WgradPhaseLaunch L;
         if (!build_wgrad_phases(g, &L)) return GCONV_ERR_UNSUPPORTED;
         unsigned int *err = device_error_word();

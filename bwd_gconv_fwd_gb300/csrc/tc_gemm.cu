@@ -29,7 +29,8 @@ constexpr int kBM = 128, kBK = 64;
 constexpr uint64_t kGemmDrainNs = 1000000000ull;
 
 struct GemmParams {
-    float *C;                    // [M][ldc] fp32
+    float *C;                    // [M][ldc] fp32, or bf16 when out_bf16
+    int out_bf16;
     const __nv_bfloat16 *bias;   // per column, or nullptr
     unsigned int *err;
     uint64_t wait_ns;
@@ -189,7 +190,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             ptx::tc_fence_after();
             const int mb = tile % p.n_mblk, nb = tile / p.n_mblk;
             const int row = mb * kBM + lg * 32 + lane;
-            float *crow = p.C + (int64_t)row * p.ldc + (int64_t)nb * BN;
+            const int64_t crow = (int64_t)row * p.ldc + (int64_t)nb * BN;   // element index in C
             for (int c0 = 0; c0 < BN; c0 += 16) {
                 uint32_t acc[16];
                 ptx::tmem_ld16(tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)(buf * BN + c0), acc);
@@ -205,10 +206,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     if (col0 + 16 <= p.N && (p.ldc & 3) == 0) {
                         #pragma unroll
                         for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4 *>(crow + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                            store_out4(p.C, crow + c0 + j, v[j], v[j + 1], v[j + 2], v[j + 3], p.out_bf16);
                     } else {
                         for (int j = 0; j < 16; ++j)
-                            if (col0 + j < p.N) crow[c0 + j] = v[j];
+                            if (col0 + j < p.N) store_out(p.C, crow + c0 + j, v[j], p.out_bf16);
                     }
                 }
             }
@@ -314,7 +315,7 @@ int pick_bn(int M, int N)
 bool fc_supported(const Geom &g)
 {
     // input size == kernel size, no padding, dilation 1: X is a plain [N][C*H*W] matrix
-    if (!(g.H == g.kH && g.W == g.kW && g.pt == 0 && g.pb == 0 && g.pl == 0 && g.pr == 0 && g.d == 1))
+    if (!(g.H == g.kH && g.W == g.kW && g.pt == 0 && g.pb == 0 && g.pl == 0 && g.pr == 0 && g.d_h == 1 && g.d_w == 1))
         return false;
     if (g.G != 1) return false;
     const int64_t Kin = (int64_t)g.Cin * g.kH * g.kW;
@@ -358,6 +359,7 @@ gconv_status tc_fc_launch(const Geom &g, const Plan &, gconv_pass pass, const vo
     if (!err) return GCONV_ERR_CUDA;
     GemmParams gp{};
     gp.C = out;
+    gp.out_bf16 = pass == GCONV_PASS_BWD_WEIGHT ? 0 : g.out_bf16;
     gp.bias = pass == GCONV_PASS_FWD ? static_cast<const __nv_bfloat16 *>(bias) : nullptr;
     gp.err = err;
     gp.wait_ns = (uint64_t)wait_limit();

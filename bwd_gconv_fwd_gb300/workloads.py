@@ -108,16 +108,27 @@ def model_zoo(N):
     return out
 
 
+def per_axis(geom):
+    """The 16-integer form ``(N, C_in, H, W, C_out, kH, kW, stride_h, stride_w, pad_top,
+    pad_bottom, pad_left, pad_right, dilation_h, dilation_w, groups)`` of a 14- or
+    16-integer geometry (a 14-tuple has one stride and one dilation for both axes)."""
+    geom = tuple(int(v) for v in geom)
+    if len(geom) == 16:
+        return geom
+    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+    return (N, Cin, H, W, Cout, kH, kW, s, s, pt, pb, pl, pr, d, d, G)
+
+
 def out_hw(geom):
     """Output extent by the floor formula (shape bookkeeping for allocation only)."""
-    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
-    ho = (H + pt + pb - d * (kH - 1) - 1) // s + 1
-    wo = (W + pl + pr - d * (kW - 1) - 1) // s + 1
+    N, Cin, H, W, Cout, kH, kW, sh, sw, pt, pb, pl, pr, dh, dw, G = per_axis(geom)
+    ho = (H + pt + pb - dh * (kH - 1) - 1) // sh + 1
+    wo = (W + pl + pr - dw * (kW - 1) - 1) // sw + 1
     return ho, wo
 
 
 def tensor_shapes(geom):
-    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+    N, Cin, H, W, Cout, kH, kW, sh, sw, pt, pb, pl, pr, dh, dw, G = per_axis(geom)
     ho, wo = out_hw(geom)
     return dict(x=(N, Cin, H, W), w=(Cout, Cin // G, kH, kW), b=(Cout,), dy=(N, Cout, ho, wo))
 
@@ -152,8 +163,19 @@ def make_inputs(wl: Workload, seed: int = SEED, with_bias: bool = True):
     return x, w, b, dy
 
 
-def random_geometry(rng, max_n=2, max_c=24, max_hw=13, max_k=3, max_s=3, max_d=2, max_pad=2):
-    """A random small geometry that has at least one output pixel (parity sweeps)."""
+def random_geometry(rng, max_n=2, max_c=24, max_hw=13, max_k=3, max_s=3, max_d=2, max_pad=2, axes=False):
+    """A random small geometry that has at least one output pixel (parity sweeps); with
+    axes=True a 16-integer geometry whose strides and dilations differ per axis."""
+    if axes:
+        while True:
+            g14 = random_geometry(rng, max_n, max_c, max_hw, max_k, max_s, max_d, max_pad)
+            N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = g14
+            sw = int(rng.integers(1, max_s + 1))
+            dw = int(rng.integers(1, max_d + 1))
+            geom = (N, Cin, H, W, Cout, kH, kW, s, sw, pt, pb, pl, pr, d, dw, G)
+            ho, wo = out_hw(geom)
+            if ho >= 1 and wo >= 1:
+                return geom
     while True:
         G = int(rng.choice([1, 1, 2, 3, 4]))
         cgi = int(rng.integers(1, max(2, max_c // G) + 1))

@@ -35,9 +35,8 @@
  * Requirements: C_in, H, W, C_out, kH, kW, stride, dilation, groups >= 1;
  * N >= 0; pads >= 0; C_in and C_out divisible by groups; Ho, Wo >= 1; every
  * tensor below 2^31 elements.  N == 0 (an empty batch) launches no convolution
- * kernel: y and dx are empty, and dw and db, being sums over no terms, are set
- * to zero (so their pointers must be valid even then).  The host-level
- * N == 0 pointer checks of gconv_fwd and gconv_bwd_data are skipped.
+ * kernel: y and dx are empty (their pointers may then be NULL), and dw and db,
+ * being sums over no terms, are set to zero (their pointers must be valid).
  *
  * Ownership.  The caller owns every buffer; the library allocates no device or
  * host memory and keeps no per-call state.  Device pointers must be device
@@ -93,6 +92,25 @@ typedef enum {
     GCONV_PATH_REDUCE = 4       /* CUDA-core warp-shuffle reduction (bias gradient) */
 } gconv_path;
 
+/* Geometry with stride and dilation given per axis.  The 14-integer entry points
+ * above and below are the case stride_h == stride_w and dilation_h == dilation_w; the
+ * *_ex entry points take this record instead.  Per-axis stride and padding are the
+ * arguments of the SpatialConvolution(nInputPlane, nOutputPlane, kW, kH, dW, dH, padW,
+ * padH, groups) constructor the clnn issue #4 thread points to (with padding further
+ * split per side); dilation, which the pages never mention, is read the same way.
+ * With per-axis values the definitions above read
+ *   ih = oh*stride_h - pad_top + kh*dilation_h,   iw = ow*stride_w - pad_left + kw*dilation_w
+ *   Ho = floor((H + pad_top + pad_bottom - dilation_h*(kH-1) - 1) / stride_h) + 1
+ *   Wo = floor((W + pad_left + pad_right - dilation_w*(kW-1) - 1) / stride_w) + 1
+ * and the requirements are the same, per axis.  The record is read during the call only. */
+typedef struct {
+    int N, C_in, H, W, C_out, kH, kW;
+    int stride_h, stride_w;
+    int pad_top, pad_bottom, pad_left, pad_right;
+    int dilation_h, dilation_w;
+    int groups;
+} gconv_geometry;
+
 /* Output extent (formula above).  GCONV_ERR_INVALID_ARG when the geometry is
  * malformed or leaves no output pixel.  Ho, Wo must be non-null host pointers. */
 gconv_status gconv_out_shape(int N, int C_in, int H, int W, int C_out, int kH, int kW,
@@ -101,7 +119,9 @@ gconv_status gconv_out_shape(int N, int C_in, int H, int W, int C_out, int kH, i
 
 /* Bytes of caller-provided device workspace the given pass needs (0 if none;
  * (size_t)-1 for an invalid geometry).  The size depends only on the
- * arguments, so it can be queried once and the buffer reused. */
+ * arguments, so it can be queried once and the buffer reused.  For
+ * GCONV_PASS_BWD_WEIGHT it also covers a bias gradient computed in the same
+ * call (gconv_bwd_weight_ex with db). */
 size_t gconv_workspace_size(int N, int C_in, int H, int W, int C_out, int kH, int kW,
                             int stride, int pad_top, int pad_bottom, int pad_left,
                             int pad_right, int dilation, int groups, gconv_dtype dtype,
@@ -154,6 +174,34 @@ gconv_status gconv_bwd_bias(int N, int C_in, int H, int W, int C_out, int kH, in
                             int pad_right, int dilation, int groups, gconv_dtype dtype,
                             const void *dy, float *db,
                             void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---- Per-axis geometry, output dtype, fused bias gradient ----------------------
+ *
+ * The same four operations with a gconv_geometry record (NULL: GCONV_ERR_INVALID_ARG).
+ * gconv_fwd_ex and gconv_bwd_data_ex also take the dtype of their output (y, dx):
+ * GCONV_F32 or GCONV_BF16 (the fp32 accumulator rounded once, to nearest even, when the
+ * output is stored).  gconv_bwd_weight_ex optionally computes the bias gradient of the
+ * same gradOutput in the same call: db, fp32 [C_out], or NULL for none (the DLPrimitives
+ * blog, "Pointwise Broadcast Reduce": the bias gradient is the sum of gradOutput over
+ * dims 0, 2, 3).  dw and db stay fp32.  gconv_workspace_size_ex(..., GCONV_PASS_BWD_WEIGHT)
+ * covers the fused bias gradient; gconv_workspace_size does too.  Layouts, ownership,
+ * errors and stream semantics are those of the 14-integer entry points. */
+gconv_status gconv_out_shape_ex(const gconv_geometry *geometry, int *Ho, int *Wo);
+size_t gconv_workspace_size_ex(const gconv_geometry *geometry, gconv_dtype dtype, gconv_pass pass);
+gconv_status gconv_plan_ex(const gconv_geometry *geometry, gconv_dtype dtype, gconv_pass pass,
+                           int *path, int *launches);
+gconv_status gconv_fwd_ex(const gconv_geometry *geometry, gconv_dtype dtype, gconv_dtype out_dtype,
+                          const void *x, const void *w, const void *bias, void *y,
+                          void *workspace, size_t workspace_bytes, void *stream);
+gconv_status gconv_bwd_data_ex(const gconv_geometry *geometry, gconv_dtype dtype, gconv_dtype out_dtype,
+                               const void *dy, const void *w, void *dx,
+                               void *workspace, size_t workspace_bytes, void *stream);
+gconv_status gconv_bwd_weight_ex(const gconv_geometry *geometry, gconv_dtype dtype,
+                                 const void *x, const void *dy, float *dw, float *db,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+gconv_status gconv_bwd_bias_ex(const gconv_geometry *geometry, gconv_dtype dtype,
+                               const void *dy, float *db,
+                               void *workspace, size_t workspace_bytes, void *stream);
 
 /* Weight gradient that allocates nothing, for callers that cannot allocate device
  * memory themselves: code embedded in a host application that owns every

@@ -9,7 +9,9 @@ defining sum per output element); this module compiles it with gcc and wraps it
 with ctypes.  Inputs are float64 numpy arrays in NCHW / [C_out, C_in/G, kH, kW]
 layout; geometry is the 14-tuple
 ``(N, C_in, H, W, C_out, kH, kW, stride, pad_top, pad_bottom, pad_left, pad_right,
-dilation, groups)``.
+dilation, groups)`` (stride and dilation the same on both axes) or the 16-tuple
+``(N, C_in, H, W, C_out, kH, kW, stride_h, stride_w, pad_top, pad_bottom, pad_left,
+pad_right, dilation_h, dilation_w, groups)``.
 
 Parity status: every entry point is pinned in ``tests/test_oracle.py`` against
 brute force, library routines (scipy correlate2d, numpy matmul, torch conv2d in
@@ -30,8 +32,20 @@ _SRC = os.path.join(_HERE, "gconv_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
-GEOM_FIELDS = ("N", "C_in", "H", "W", "C_out", "kH", "kW", "stride",
-               "pad_top", "pad_bottom", "pad_left", "pad_right", "dilation", "groups")
+GEOM_FIELDS = ("N", "C_in", "H", "W", "C_out", "kH", "kW", "stride_h", "stride_w",
+               "pad_top", "pad_bottom", "pad_left", "pad_right", "dilation_h", "dilation_w", "groups")
+
+
+def geom16(g):
+    """The 16-integer geometry of a 14- or 16-tuple (a 14-tuple has one stride and one
+    dilation for both axes)."""
+    g = tuple(int(v) for v in g)
+    if len(g) == 14:
+        N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = g
+        return (N, Cin, H, W, Cout, kH, kW, s, s, pt, pb, pl, pr, d, d, G)
+    if len(g) == 16:
+        return g
+    raise ValueError("geometry must have 14 or 16 integers")
 
 
 def build(force: bool = False) -> str:
@@ -75,10 +89,7 @@ def _load():
 
 
 def _geom(g) -> ctypes.Array:
-    g = tuple(int(v) for v in g)
-    if len(g) != 14:
-        raise ValueError("geometry must have 14 integers")
-    return (ctypes.c_int * 14)(*g)
+    return (ctypes.c_int * 16)(*geom16(g))
 
 
 def _dptr(a):
@@ -104,7 +115,7 @@ def out_shape(g):
 
 def shapes(g):
     """Shapes of x, w, b, y for geometry g."""
-    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = (int(v) for v in g)
+    N, Cin, H, W, Cout, kH, kW, sh, sw, pt, pb, pl, pr, dh, dw, G = geom16(g)
     Ho, Wo = out_shape(g)
     return dict(x=(N, Cin, H, W), w=(Cout, Cin // G, kH, kW), b=(Cout,), y=(N, Cout, Ho, Wo))
 

@@ -31,14 +31,19 @@
  *  - Backward-data is the data gradient of the forward, over the full C_out of
  *    the group.  ("Support groups in DenseConvDims", NNlib.jl PR #289, the
  *    remark on the conv-data gradient needing the ungrouped channel count.)
- *  - Output size: floor((H + pt + pb - d*(kH-1) - 1)/s) + 1, likewise for W
- *    (the pages print no formula; this is the standard floor reading).
+ *  - Output size: floor((H + pt + pb - d_h*(kH-1) - 1)/s_h) + 1, likewise for W
+ *    with d_w and s_w (the pages print no formula; this is the standard floor
+ *    reading).
+ *  - Stride and padding are given per axis, as in the constructor the clnn
+ *    issue #4 thread points to (SpatialConvolution(nInputPlane, nOutputPlane,
+ *    kW, kH, dW, dH, padW, padH, groups)); dilation, which the pages never
+ *    mention, is read the same way: a tap at (kh*d_h, kw*d_w).
  *  - Gradients overwrite their outputs (gradients after zeroGradParameters in
  *    the cudnn.torch script are the same thing for one call).
  *
- * Geometry is passed as int p[14] in this order:
- *   N, C_in, H, W, C_out, kH, kW, stride, pad_top, pad_bottom, pad_left,
- *   pad_right, dilation, groups
+ * Geometry is passed as int p[16] in this order:
+ *   N, C_in, H, W, C_out, kH, kW, stride_h, stride_w, pad_top, pad_bottom,
+ *   pad_left, pad_right, dilation_h, dilation_w, groups
  */
 #include <stdint.h>
 #include <stddef.h>
@@ -46,7 +51,7 @@
 #include <omp.h>
 #endif
 
-enum { P_N, P_CIN, P_H, P_W, P_COUT, P_KH, P_KW, P_S, P_PT, P_PB, P_PL, P_PR, P_D, P_G };
+enum { P_N, P_CIN, P_H, P_W, P_COUT, P_KH, P_KW, P_SH, P_SW, P_PT, P_PB, P_PL, P_PR, P_DH, P_DW, P_G, P_COUNT };
 
 /* Output extent along one axis, or 0 when the geometry leaves no output. */
 static int64_t out_extent(int64_t in, int64_t pa, int64_t pb, int64_t k, int64_t d, int64_t s)
@@ -59,14 +64,14 @@ static int64_t out_extent(int64_t in, int64_t pa, int64_t pb, int64_t k, int64_t
 /* Returns 0 and fills Ho/Wo when the geometry is well formed, 1 otherwise. */
 int oracle_out_shape(const int *p, int *Ho, int *Wo)
 {
-    for (int i = 0; i < 14; ++i) {
+    for (int i = 0; i < P_COUNT; ++i) {
         if (i >= P_PT && i <= P_PR) { if (p[i] < 0) return 1; }
         else if (i == P_N) { if (p[i] < 0) return 1; }
         else if (p[i] < 1) return 1;
     }
     if (p[P_CIN] % p[P_G] != 0 || p[P_COUT] % p[P_G] != 0) return 1;
-    int64_t ho = out_extent(p[P_H], p[P_PT], p[P_PB], p[P_KH], p[P_D], p[P_S]);
-    int64_t wo = out_extent(p[P_W], p[P_PL], p[P_PR], p[P_KW], p[P_D], p[P_S]);
+    int64_t ho = out_extent(p[P_H], p[P_PT], p[P_PB], p[P_KH], p[P_DH], p[P_SH]);
+    int64_t wo = out_extent(p[P_W], p[P_PL], p[P_PR], p[P_KW], p[P_DW], p[P_SW]);
     if (ho < 1 || wo < 1) return 1;
     *Ho = (int)ho;
     *Wo = (int)wo;
@@ -74,21 +79,22 @@ int oracle_out_shape(const int *p, int *Ho, int *Wo)
 }
 
 /* y[n,o,oh,ow] = b[o] + sum_{c<Cgi, kh<kH, kw<kW} w[o,c,kh,kw] *
- *                x[n, g*Cgi + c, oh*s - pt + kh*d, ow*s - pl + kw*d],  g = o / Cgo,
+ *                x[n, g*Cgi + c, oh*s_h - pt + kh*d_h, ow*s_w - pl + kw*d_w],  g = o / Cgo,
  * with x read as 0 outside [0,H) x [0,W).  b may be NULL (no bias). */
 double oracle_y_at(const int *p, const double *x, const double *w, const double *b,
                    int64_t n, int64_t o, int64_t oh, int64_t ow)
 {
     const int64_t Cin = p[P_CIN], H = p[P_H], W = p[P_W], Cout = p[P_COUT];
-    const int64_t kH = p[P_KH], kW = p[P_KW], s = p[P_S], d = p[P_D], G = p[P_G];
+    const int64_t kH = p[P_KH], kW = p[P_KW], G = p[P_G];
+    const int64_t sh = p[P_SH], sw = p[P_SW], dh = p[P_DH], dw = p[P_DW];
     const int64_t Cgi = Cin / G, Cgo = Cout / G, g = o / Cgo;
     double acc = 0.0;
     for (int64_t c = 0; c < Cgi; ++c)
         for (int64_t kh = 0; kh < kH; ++kh) {
-            int64_t ih = oh * s - p[P_PT] + kh * d;
+            int64_t ih = oh * sh - p[P_PT] + kh * dh;
             if (ih < 0 || ih >= H) continue;
             for (int64_t kw = 0; kw < kW; ++kw) {
-                int64_t iw = ow * s - p[P_PL] + kw * d;
+                int64_t iw = ow * sw - p[P_PL] + kw * dw;
                 if (iw < 0 || iw >= W) continue;
                 acc += w[((o * Cgi + c) * kH + kh) * kW + kw] *
                        x[((n * Cin + g * Cgi + c) * H + ih) * W + iw];
@@ -100,26 +106,27 @@ double oracle_y_at(const int *p, const double *x, const double *w, const double 
 
 /* dx[n,ci,ih,iw] = sum over o in the group of ci, kh, kw of
  *   w[o, ci - g*Cgi, kh, kw] * dy[n, o, oh, ow]
- * where oh = (ih + pt - kh*d)/s must be an exact, in-range integer, and the same
- * for ow with pl and kw.  Pixels no tap reaches get exactly 0. */
+ * where oh = (ih + pt - kh*d_h)/s_h must be an exact, in-range integer, and the
+ * same for ow with pl, kw, d_w and s_w.  Pixels no tap reaches get exactly 0. */
 double oracle_dx_at(const int *p, const double *dy, const double *w,
                     int64_t n, int64_t ci, int64_t ih, int64_t iw, int64_t Ho, int64_t Wo)
 {
     const int64_t Cin = p[P_CIN], Cout = p[P_COUT];
-    const int64_t kH = p[P_KH], kW = p[P_KW], s = p[P_S], d = p[P_D], G = p[P_G];
+    const int64_t kH = p[P_KH], kW = p[P_KW], G = p[P_G];
+    const int64_t sh = p[P_SH], sw = p[P_SW], dh = p[P_DH], dw = p[P_DW];
     const int64_t Cgi = Cin / G, Cgo = Cout / G, g = ci / Cgi, c = ci - g * Cgi;
     double acc = 0.0;
     for (int64_t oo = 0; oo < Cgo; ++oo) {
         const int64_t o = g * Cgo + oo;
         for (int64_t kh = 0; kh < kH; ++kh) {
-            int64_t th = ih + p[P_PT] - kh * d;
-            if (th < 0 || th % s != 0) continue;
-            int64_t oh = th / s;
+            int64_t th = ih + p[P_PT] - kh * dh;
+            if (th < 0 || th % sh != 0) continue;
+            int64_t oh = th / sh;
             if (oh >= Ho) continue;
             for (int64_t kw = 0; kw < kW; ++kw) {
-                int64_t tw = iw + p[P_PL] - kw * d;
-                if (tw < 0 || tw % s != 0) continue;
-                int64_t ow = tw / s;
+                int64_t tw = iw + p[P_PL] - kw * dw;
+                if (tw < 0 || tw % sw != 0) continue;
+                int64_t ow = tw / sw;
                 if (ow >= Wo) continue;
                 acc += w[((o * Cgi + c) * kH + kh) * kW + kw] *
                        dy[((n * Cout + o) * Ho + oh) * Wo + ow];
@@ -129,20 +136,20 @@ double oracle_dx_at(const int *p, const double *dy, const double *w,
     return acc;
 }
 
-/* dw[o,c,kh,kw] = sum_{n,oh,ow} dy[n,o,oh,ow] * x[n, g*Cgi + c, oh*s - pt + kh*d, ow*s - pl + kw*d] */
+/* dw[o,c,kh,kw] = sum_{n,oh,ow} dy[n,o,oh,ow] * x[n, g*Cgi + c, oh*s_h - pt + kh*d_h, ow*s_w - pl + kw*d_w] */
 double oracle_dw_at(const int *p, const double *x, const double *dy,
                     int64_t o, int64_t c, int64_t kh, int64_t kw, int64_t Ho, int64_t Wo)
 {
     const int64_t N = p[P_N], Cin = p[P_CIN], H = p[P_H], W = p[P_W], Cout = p[P_COUT];
-    const int64_t s = p[P_S], d = p[P_D], G = p[P_G];
+    const int64_t sh = p[P_SH], sw = p[P_SW], dh = p[P_DH], dw = p[P_DW], G = p[P_G];
     const int64_t Cgi = Cin / G, Cgo = Cout / G, g = o / Cgo;
     double acc = 0.0;
     for (int64_t n = 0; n < N; ++n)
         for (int64_t oh = 0; oh < Ho; ++oh) {
-            int64_t ih = oh * s - p[P_PT] + kh * d;
+            int64_t ih = oh * sh - p[P_PT] + kh * dh;
             if (ih < 0 || ih >= H) continue;
             for (int64_t ow = 0; ow < Wo; ++ow) {
-                int64_t iw = ow * s - p[P_PL] + kw * d;
+                int64_t iw = ow * sw - p[P_PL] + kw * dw;
                 if (iw < 0 || iw >= W) continue;
                 acc += dy[((n * Cout + o) * Ho + oh) * Wo + ow] *
                        x[((n * Cin + g * Cgi + c) * H + ih) * W + iw];

@@ -21,11 +21,19 @@ static long errors = 0;
 #define CHECK(cond, ...) do { if (!(cond)) { if (errors++ < 10) { printf("FAIL: " __VA_ARGS__); printf("\n"); } } } while (0)
 int main(int argc, char **argv)
 {
-    int v[14];
-    for (int i = 0; i < 14; ++i) v[i] = atoi(argv[1 + i]);
-    const int span_h = v[2] + v[8] + v[9] - v[12] * (v[5] - 1) - 1, span_w = v[3] + v[10] + v[11] - v[12] * (v[6] - 1) - 1;
-    Geom g{v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], v[8], v[9], v[10], v[11], v[12], v[13], span_h / v[7] + 1,
-           span_w / v[7] + 1, v[1] / v[13], v[4] / v[13]};
+    // 14 geometry integers (one stride, one dilation) or 16 (per axis)
+    int v[16];
+    if (argc == 15) {
+        int a[14];
+        for (int i = 0; i < 14; ++i) a[i] = atoi(argv[1 + i]);
+        const int e[16] = {a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7], a[7], a[8], a[9], a[10], a[11], a[12], a[12], a[13]};
+        for (int i = 0; i < 16; ++i) v[i] = e[i];
+    } else {
+        for (int i = 0; i < 16; ++i) v[i] = atoi(argv[1 + i]);
+    }
+    const int span_h = v[2] + v[9] + v[10] - v[13] * (v[5] - 1) - 1, span_w = v[3] + v[11] + v[12] - v[14] * (v[6] - 1) - 1;
+    Geom g{v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15],
+           span_h / v[7] + 1, span_w / v[8] + 1, v[1] / v[15], v[4] / v[15]};
     for (int bd = 0; bd < 2; ++bd) {
         Corr2Launch C;
         if (!build_corr2(g, bd == 1, &C)) { printf("corr2 %d not served\n", bd); continue; }
@@ -45,7 +53,7 @@ int main(int argc, char **argv)
         for (int b = 0; b < c.ntaps; ++b)
             if (k.tk2[b] >= 0) {
                 auto off = [&](int t) { const int kh = t / g.kW, kw = t % g.kW;
-                    const int a = bd ? (g.kH - 1 - kh) * g.d : kh * g.d, bb = bd ? (g.kW - 1 - kw) * g.d : kw * g.d; return a * c.Wp + bb; };
+                    const int a = bd ? (g.kH - 1 - kh) * g.d_h : kh * g.d_h, bb = bd ? (g.kW - 1 - kw) * g.d_w : kw * g.d_w; return a * c.Wp + bb; };
                 CHECK(off(k.tk1[b]) == c.tap_off[b] && off(k.tk2[b]) == c.tap_off[b] + c.pair_delta, "pair offsets");
                 CHECK(c.Cv <= 64 && c.n_vtile == 1, "pair needs one 64-row half");
             }

@@ -200,13 +200,21 @@ static void replay_wgrad3(const Geom &g, int V)
 
 int main(int argc, char **argv)
 {
-    if (argc < 16) { printf("usage: thin3_plan_replay <14 geometry ints> <dtype>\n"); return 2; }
-    int v[14];
-    for (int i = 0; i < 14; ++i) v[i] = atoi(argv[1 + i]);
-    const int V = atoi(argv[15]) == 1 ? 8 : 4;
-    const int span_h = v[2] + v[8] + v[9] - v[12] * (v[5] - 1) - 1, span_w = v[3] + v[10] + v[11] - v[12] * (v[6] - 1) - 1;
-    Geom g{v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], v[8], v[9], v[10], v[11], v[12], v[13], span_h / v[7] + 1,
-           span_w / v[7] + 1, v[1] / v[13], v[4] / v[13]};
+    if (argc != 16 && argc != 18) { printf("usage: thin3_plan_replay <14 or 16 geometry ints> <dtype>\n"); return 2; }
+    // 14 geometry integers (one stride, one dilation) or 16 (per axis), then the dtype
+    int v[16];
+    const int V = atoi(argv[argc - 1]) == 1 ? 8 : 4;
+    if (argc == 16) {
+        int a[14];
+        for (int i = 0; i < 14; ++i) a[i] = atoi(argv[1 + i]);
+        const int e[16] = {a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7], a[7], a[8], a[9], a[10], a[11], a[12], a[12], a[13]};
+        for (int i = 0; i < 16; ++i) v[i] = e[i];
+    } else {
+        for (int i = 0; i < 16; ++i) v[i] = atoi(argv[1 + i]);
+    }
+    const int span_h = v[2] + v[9] + v[10] - v[13] * (v[5] - 1) - 1, span_w = v[3] + v[11] + v[12] - v[14] * (v[6] - 1) - 1;
+    Geom g{v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15],
+           span_h / v[7] + 1, span_w / v[8] + 1, v[1] / v[15], v[4] / v[15]};
     replay_conv3(g, false, V);
     replay_conv3(g, true, V);
     replay_wgrad3(g, V);

@@ -20,11 +20,19 @@ static long errors = 0;
 #define CHECK(cond, ...) do { if (!(cond)) { if (errors++ < 10) { printf("FAIL: " __VA_ARGS__); printf("\n"); } } } while (0)
 int main(int argc, char **argv)
 {
-    int v[14];
-    for (int i = 0; i < 14; ++i) v[i] = atoi(argv[1 + i]);
-    const int span_h = v[2] + v[8] + v[9] - v[12] * (v[5] - 1) - 1, span_w = v[3] + v[10] + v[11] - v[12] * (v[6] - 1) - 1;
-    Geom g{v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], v[8], v[9], v[10], v[11], v[12], v[13], span_h / v[7] + 1,
-           span_w / v[7] + 1, v[1] / v[13], v[4] / v[13]};
+    // 14 geometry integers (one stride, one dilation) or 16 (per axis)
+    int v[16];
+    if (argc == 15) {
+        int a[14];
+        for (int i = 0; i < 14; ++i) a[i] = atoi(argv[1 + i]);
+        const int e[16] = {a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7], a[7], a[8], a[9], a[10], a[11], a[12], a[12], a[13]};
+        for (int i = 0; i < 16; ++i) v[i] = e[i];
+    } else {
+        for (int i = 0; i < 16; ++i) v[i] = atoi(argv[1 + i]);
+    }
+    const int span_h = v[2] + v[9] + v[10] - v[13] * (v[5] - 1) - 1, span_w = v[3] + v[11] + v[12] - v[14] * (v[6] - 1) - 1;
+    Geom g{v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15],
+           span_h / v[7] + 1, span_w / v[8] + 1, v[1] / v[15], v[4] / v[15]};
     WgradPhaseLaunch L;
     if (!build_wgrad_phases(g, &L)) { printf("not served by this path\nerrors: 0\n"); return 0; }
     printf("Ho=%d Wo=%d nphase=%d xplane_elems=%zu ws=%zu\n", g.Ho, g.Wo, L.nphase, L.xplane_elems, L.ws_bytes);
@@ -43,7 +51,7 @@ int main(int argc, char **argv)
             const int64_t t = blk / p.nchunk;
             const int64_t ng = t % ((int64_t)p.N * p.G);
             const int pl = (int)(t / ((int64_t)p.N * p.G));
-            const int row = r * p.s + p.roff[pl], col = c * p.s + p.coff[pl];
+            const int row = r * p.s_h + p.roff[pl], col = c * p.s_w + p.coff[pl];
             const bool inside = row >= 0 && row < p.IH && col >= 0 && col < p.IW;
             const int cvalid = inside ? std::min(64, p.Cg - 64 * j) : 0;
             const int64_t plane = (int64_t)p.IH * p.IW;

@@ -20,11 +20,19 @@ static long errors = 0;
 #define CHECK(cond, ...) do { if (!(cond)) { if (errors++ < 10) { printf("FAIL: " __VA_ARGS__); printf("\n"); } } } while (0)
 int main(int argc, char **argv)
 {
-    int v[14];
-    for (int i = 0; i < 14; ++i) v[i] = atoi(argv[1 + i]);
-    const int span_h = v[2] + v[8] + v[9] - v[12] * (v[5] - 1) - 1, span_w = v[3] + v[10] + v[11] - v[12] * (v[6] - 1) - 1;
-    Geom g{v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], v[8], v[9], v[10], v[11], v[12], v[13], span_h / v[7] + 1,
-           span_w / v[7] + 1, v[1] / v[13], v[4] / v[13]};
+    // 14 geometry integers (one stride, one dilation) or 16 (per axis)
+    int v[16];
+    if (argc == 15) {
+        int a[14];
+        for (int i = 0; i < 14; ++i) a[i] = atoi(argv[1 + i]);
+        const int e[16] = {a[0], a[1], a[2], a[3], a[4], a[5], a[6], a[7], a[7], a[8], a[9], a[10], a[11], a[12], a[12], a[13]};
+        for (int i = 0; i < 16; ++i) v[i] = e[i];
+    } else {
+        for (int i = 0; i < 16; ++i) v[i] = atoi(argv[1 + i]);
+    }
+    const int span_h = v[2] + v[9] + v[10] - v[13] * (v[5] - 1) - 1, span_w = v[3] + v[11] + v[12] - v[14] * (v[6] - 1) - 1;
+    Geom g{v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7], v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15],
+           span_h / v[7] + 1, span_w / v[8] + 1, v[1] / v[15], v[4] / v[15]};
     WgradLaunch L;
     if (!build_wgrad(g, &L)) { printf("not served by this path\nerrors: 0\n"); return 0; }
     printf("Ho=%d Wo=%d grid=%d smem=%zu ws=%zu\n", g.Ho, g.Wo, L.grid, L.smem, L.ws_bytes);

@@ -35,12 +35,13 @@ def _inputs(rng, geom):
 
 
 def _torch_ref(geom, x, w, b, dy):
-    """torch conv2d in float64 (asymmetric pads via F.pad), gradients by autograd."""
-    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+    """torch conv2d in float64 (asymmetric pads via F.pad, per-axis stride and dilation as
+    tuples), gradients by autograd."""
+    N, Cin, H, W, Cout, kH, kW, sh, sw, pt, pb, pl, pr, dh, dw, G = wlm.per_axis(geom)
     xt = torch.tensor(x, dtype=torch.float64, requires_grad=True)
     wt = torch.tensor(w, dtype=torch.float64, requires_grad=True)
     bt = torch.tensor(b, dtype=torch.float64, requires_grad=True)
-    y = F.conv2d(F.pad(xt, (pl, pr, pt, pb)), wt, bt, stride=s, dilation=d, groups=G)
+    y = F.conv2d(F.pad(xt, (pl, pr, pt, pb)), wt, bt, stride=(sh, sw), dilation=(dh, dw), groups=G)
     y.backward(torch.tensor(dy, dtype=torch.float64))
     return y.detach().numpy(), xt.grad.numpy(), wt.grad.numpy(), bt.grad.numpy()
 
@@ -52,7 +53,7 @@ def _brute_operators(geom):
       B_x[y_idx, w_idx] (built from x):  y = B_x w + b,  dw = B_x^T dy
     so the backward passes are checked as matrix transposes, not index inversions.
     """
-    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+    N, Cin, H, W, Cout, kH, kW, sh, sw, pt, pb, pl, pr, dh, dw, G = wlm.per_axis(geom)
     Ho, Wo = wlm.out_hw(geom)
     Cgi, Cgo = Cin // G, Cout // G
     conns = []  # (y_idx, x_idx, w_idx)
@@ -60,7 +61,7 @@ def _brute_operators(geom):
         g = o // Cgo
         yi = ((n * Cout + o) * Ho + oh) * Wo + ow
         for c, kh, kw in itertools.product(range(Cgi), range(kH), range(kW)):
-            ih, iw = oh * s - pt + kh * d, ow * s - pl + kw * d
+            ih, iw = oh * sh - pt + kh * dh, ow * sw - pl + kw * dw
             if 0 <= ih < H and 0 <= iw < W:
                 xi = ((n * Cin + g * Cgi + c) * H + ih) * W + iw
                 wi = ((o * Cgi + c) * kH + kh) * kW + kw
@@ -83,6 +84,11 @@ TINY_GEOMS = [
     (1, 4, 3, 3, 4, 3, 3, 1, 1, 1, 1, 1, 1, 4),   # depthwise, pad 1
     (2, 2, 4, 4, 2, 4, 4, 1, 0, 0, 0, 0, 1, 1),   # input == kernel
     (1, 2, 5, 5, 2, 2, 2, 3, 0, 0, 0, 0, 1, 1),   # stride > kernel: untouched pixels
+    # per-axis stride and dilation (N, C_in, H, W, C_out, kH, kW, s_h, s_w, pads, d_h, d_w, G)
+    (1, 2, 7, 6, 4, 3, 2, 2, 1, 1, 0, 0, 1, 1, 2, 2),
+    (2, 3, 5, 8, 3, 2, 3, 1, 3, 0, 1, 2, 0, 2, 1, 3),
+    (1, 4, 9, 5, 2, 3, 3, 3, 2, 2, 1, 1, 0, 1, 2, 2),
+    (1, 2, 6, 7, 2, 1, 2, 2, 1, 0, 0, 0, 0, 1, 3, 1),
 ]
 
 
@@ -120,6 +126,33 @@ def test_random_geometries_vs_torch_float64(oracle_mod):
         assert _rel(oracle_mod.bwd_data(geom, dy, w), dx_t) <= 1e-12, geom
         assert _rel(oracle_mod.bwd_weight(geom, x, dy), dw_t) <= 1e-12, geom
         assert _rel(oracle_mod.bwd_bias(geom, dy), db_t) <= 1e-12, geom
+
+
+def test_per_axis_geometries_vs_torch_float64(oracle_mod):
+    """Library pin for per-axis stride and dilation (the cudnn constructor's dW, dH): torch
+    conv2d with stride=(s_h, s_w), dilation=(d_h, d_w) in float64 + autograd."""
+    rng = np.random.default_rng(2025)
+    for _ in range(40):
+        geom = wlm.random_geometry(rng, axes=True)
+        x, w, b, dy = _inputs(rng, geom)
+        y_t, dx_t, dw_t, db_t = _torch_ref(geom, x, w, b, dy)
+        assert _rel(oracle_mod.fwd(geom, x, w, b), y_t) <= 1e-12, geom
+        assert _rel(oracle_mod.bwd_data(geom, dy, w), dx_t) <= 1e-12, geom
+        assert _rel(oracle_mod.bwd_weight(geom, x, dy), dw_t) <= 1e-12, geom
+        assert _rel(oracle_mod.bwd_bias(geom, dy), db_t) <= 1e-12, geom
+
+
+def test_square_geometry_has_one_reading(oracle_mod):
+    """A 14-integer geometry and its 16-integer form (equal strides and dilations) are the
+    same request: identical results."""
+    rng = np.random.default_rng(11)
+    for _ in range(10):
+        g14 = wlm.random_geometry(rng)
+        g16 = wlm.per_axis(g14)
+        x, w, b, dy = _inputs(rng, g14)
+        assert np.array_equal(oracle_mod.fwd(g14, x, w, b), oracle_mod.fwd(g16, x, w, b))
+        assert np.array_equal(oracle_mod.bwd_data(g14, dy, w), oracle_mod.bwd_data(g16, dy, w))
+        assert np.array_equal(oracle_mod.bwd_weight(g14, x, dy), oracle_mod.bwd_weight(g16, x, dy))
 
 
 def _scipy_ungrouped(geom, x, w):

@@ -33,8 +33,8 @@ def dev(oracle_mod):
 
 
 def _kw(geom):
-    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
-    return dict(stride=s, padding=(pt, pb, pl, pr), dilation=d, groups=G)
+    N, Cin, H, W, Cout, kH, kW, sh, sw, pt, pb, pl, pr, dh, dw, G = wl.per_axis(geom)
+    return dict(stride=(sh, sw), padding=(pt, pb, pl, pr), dilation=(dh, dw), groups=G)
 
 
 # Guard regions around every output: 4 KiB of a NaN bit pattern no kernel computes, checked
@@ -65,7 +65,7 @@ def check_guards(name, buf):
 def run_gpu(geom, x, w, b, dy, dev, passes=("y", "dx", "dw", "db")):
     """All four passes on the GPU; returns fp32 CPU tensors.  Every output sits between guard
     regions that must come back untouched."""
-    N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
+    N, Cin, H, W, Cout, kH, kW = wl.per_axis(geom)[:7]
     Ho, Wo = wl.out_hw(geom)
     kw = _kw(geom)
     xd, wd, dyd = x.to(dev), w.to(dev), dy.to(dev)
@@ -394,3 +394,104 @@ def test_tensor_core_thresholds_full(dev, oracle_mod, geom, paths):
     wk = wl.Workload("threshold", geom, "bf16", w=("normal", 0.2))
     x, w, b, dy = wl.make_inputs(wk, seed=sum(geom) * 17)
     full_compare(geom, "bf16", x, w, b, dy, dev, oracle_mod, label=f"threshold {geom}")
+
+
+# Per-axis stride and dilation (the 16-integer geometry of the *_ex entry points): whole
+# tensors against the oracle, on the families the planner picks (asserted).
+PER_AXIS = [
+    # (N, C_in, H, W, C_out, kH, kW, s_h, s_w, pt, pb, pl, pr, d_h, d_w, G), dtype, families
+    ((2, 32, 13, 12, 32, 3, 3, 2, 1, 1, 1, 1, 1, 1, 1, 1), "bf16", (TC, TC, TC, RD)),
+    ((2, 32, 12, 15, 64, 3, 3, 1, 2, 1, 0, 1, 1, 1, 2, 1), "bf16", (TC, TC, TC, RD)),
+    ((2, 32, 11, 13, 32, 3, 3, 1, 1, 2, 2, 1, 1, 1, 2, 1), "bf16", (TC, TC, TC, RD)),
+    ((2, 32, 12, 9, 64, 3, 5, 1, 1, 1, 1, 2, 2, 2, 1, 2), "bf16", (TC, TC, TC, RD)),
+    ((2, 16, 14, 10, 16, 5, 3, 2, 1, 2, 2, 1, 1, 1, 2, 1), "bf16", (TC, TC, TC, RD)),
+    ((2, 12, 13, 12, 12, 3, 3, 2, 1, 1, 1, 1, 1, 1, 1, 3), "bf16", (CC, CC, CC, RD)),
+    ((2, 8, 11, 14, 8, 3, 2, 1, 3, 0, 2, 1, 0, 2, 1, 8), "bf16", (CC, CC, CC, RD)),
+    ((2, 12, 13, 12, 12, 3, 3, 2, 1, 1, 1, 1, 1, 1, 1, 3), "f32", (CC, CC, CC, RD)),
+    ((1, 6, 9, 17, 9, 2, 3, 3, 2, 1, 0, 2, 1, 2, 3, 3), "f32", (CC, CC, CC, RD)),
+]
+
+
+@pytest.mark.parametrize("geom,dtype,paths", PER_AXIS)
+def test_per_axis_geometries_full(dev, oracle_mod, geom, dtype, paths):
+    assert_paths(geom, dtype, paths)
+    wk = wl.Workload("axes", geom, dtype, w=("normal", 0.2))
+    x, w, b, dy = wl.make_inputs(wk, seed=sum(geom) * 19)
+    full_compare(geom, dtype, x, w, b, dy, dev, oracle_mod, label=f"axes {geom}")
+
+
+def test_per_axis_random_sweep(dev, oracle_mod):
+    rng = np.random.default_rng(4321)
+    for i in range(30):
+        geom = wl.random_geometry(rng, max_n=3, max_c=40, max_hw=15, max_k=4, axes=True)
+        dtype = "bf16" if i % 3 else "f32"
+        wk = wl.Workload("axes_sweep", geom, dtype, w=("normal", 0.3))
+        x, w, b, dy = wl.make_inputs(wk, seed=7000 + i)
+        full_compare(geom, dtype, x, w, b, dy, dev, oracle_mod, label=f"axes sweep{i} {geom}")
+
+
+@pytest.mark.parametrize("geom", [
+    (3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2),       # tensor-core weight gradient
+    (2, 32, 12, 12, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8),         # CUDA-core weight gradient
+    (2, 128, 6, 6, 96, 6, 6, 1, 0, 0, 0, 0, 1, 1),          # fully-connected mode
+])
+def test_weight_gradient_with_bias_gradient(dev, oracle_mod, geom):
+    """gconv_bwd_weight_ex with db: dw and db from one call, equal bit for bit to the two
+    separate entry points and within tolerance of the oracle."""
+    wk = wl.Workload("wdb", geom, "bf16", w=("normal", 0.2))
+    x, w, b, dy = wl.make_inputs(wk, seed=55)
+    sep = run_gpu(geom, x, w, b, dy, dev, passes=("dw", "db"))
+    xd, dyd = x.to(dev), dy.to(dev)
+    dw, bw = guarded(tuple(w.shape), dev)
+    db, bb = guarded((geom[4],), dev)
+    gc.gconv_bwd_weight(xd, dyd, dw, db=db, **_kw(geom))
+    torch.cuda.synchronize()
+    assert gc.gconv_check_device_error() == B.GCONV_OK
+    check_guards("fused dw", bw)
+    check_guards("fused db", bb)
+    assert torch.equal(dw.cpu(), sep["dw"]) and torch.equal(db.cpu(), sep["db"])
+    check("fused db", db.cpu().numpy(), oracle_mod.bwd_bias(geom, f64(dy)), TOL["bf16"])
+
+
+# bf16 outputs (y, dx through the *_ex entry points): the stored value is the fp32 result
+# rounded once to nearest even, so it must equal the fp32 output rounded by torch, bit for
+# bit; against the oracle the bound adds that rounding, half a bf16 ulp (2^-8 relative).
+BF16_OUT = [
+    ((3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2), (TC, TC)),    # stride-1 correlation, paired taps
+    ((2, 64, 19, 16, 64, 3, 3, 2, 0, 1, 0, 1, 1, 1), (TC, TC)),     # stride-2 correlation, phases
+    ((2, 128, 6, 6, 96, 6, 6, 1, 0, 0, 0, 0, 1, 1), (CC, CC)),      # 1x1 output, too few images for the GEMM
+    ((64, 64, 4, 4, 128, 4, 4, 1, 0, 0, 0, 0, 1, 1), (FC, FC)),     # FC GEMM
+    ((2, 32, 12, 12, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8), (CC, CC)),     # thin 3x3
+    ((2, 12, 13, 12, 12, 3, 3, 2, 1, 1, 1, 1, 1, 1, 1, 3), (CC, CC)),   # CUDA-core tiles, per-axis stride
+    ((1, 8, 9, 7, 12, 1, 1, 1, 0, 0, 0, 0, 1, 1), (CC, CC)),        # 1x1, 8 channels
+]
+
+
+@pytest.mark.parametrize("geom,paths", BF16_OUT)
+def test_bf16_outputs(dev, oracle_mod, geom, paths):
+    got = tuple(gc.gconv_plan(geom, B.GCONV_BF16, p)[0] for p in range(2))
+    assert got == paths, (geom, got)
+    N, Cin, H, W, Cout = wl.per_axis(geom)[:5]
+    Ho, Wo = wl.out_hw(geom)
+    wk = wl.Workload("bf16out", geom, "bf16", w=("normal", 0.2))
+    x, w, b, dy = wl.make_inputs(wk, seed=sum(geom) * 23)
+    xd, wd, bd, dyd = (t.to(dev) for t in (x, w, b, dy))
+    kw = _kw(geom)
+    y32 = torch.empty((N, Cout, Ho, Wo), device=dev)
+    dx32 = torch.empty((N, Cin, H, W), device=dev)
+    y16 = torch.full((N, Cout, Ho, Wo), float("nan"), device=dev, dtype=torch.bfloat16)
+    dx16 = torch.full((N, Cin, H, W), float("nan"), device=dev, dtype=torch.bfloat16)
+    gc.gconv_fwd(xd, wd, bd, y32, **kw)
+    gc.gconv_bwd_data(dyd, wd, dx32, **kw)
+    gc.gconv_fwd(xd, wd, bd, y16, **kw)
+    gc.gconv_bwd_data(dyd, wd, dx16, **kw)
+    torch.cuda.synchronize()
+    assert gc.gconv_check_device_error() == B.GCONV_OK
+    assert torch.equal(y16, y32.to(torch.bfloat16)), geom
+    assert torch.equal(dx16, dx32.to(torch.bfloat16)), geom
+    for name, got16, ref in (("y", y16, oracle_mod.fwd(geom, f64(x), f64(w), f64(b))),
+                             ("dx", dx16, oracle_mod.bwd_data(geom, f64(dy), f64(w)))):
+        g = got16.cpu().double().numpy()
+        rms = float(np.sqrt(np.mean(ref * ref)))
+        bound = 1e-2 * rms + 2.0 ** -8 * np.abs(ref)
+        assert np.all(np.abs(g - ref) <= bound), (name, geom, float(np.max(np.abs(g - ref) - bound)))

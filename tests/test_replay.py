@@ -52,6 +52,9 @@ STRIDE1 = [
     (1, 96, 13, 40, 160, 3, 3, 1, 1, 1, 1, 1, 1, 2),        # wide rows, 80 produced channels
     (1, 40, 7, 23, 24, 2, 4, 1, 0, 3, 1, 0, 1, 1),          # odd channel counts, 2 x 4 kernel
     (2, 64, 20, 20, 64, 7, 7, 1, 3, 3, 3, 3, 1, 1),         # 49 taps
+    # per-axis dilation (16 integers: ..., s_h, s_w, pads, d_h, d_w, G)
+    (2, 32, 11, 13, 32, 3, 3, 1, 1, 2, 2, 1, 1, 1, 2, 1),
+    (2, 32, 12, 9, 64, 3, 5, 1, 1, 1, 1, 2, 2, 2, 1, 2),
 ]
 
 
@@ -72,6 +75,9 @@ STRIDE2 = [
     (2, 32, 15, 15, 64, 5, 5, 2, 2, 2, 2, 2, 1, 2),
     (1, 48, 13, 17, 32, 3, 3, 2, 1, 1, 1, 1, 1, 1),
     (2, 16, 12, 12, 32, 3, 3, 2, 2, 2, 2, 2, 2, 1),         # dilation 2
+    # per-axis strides: one stride-2 axis and one stride-1 axis (two phase planes)
+    (2, 32, 13, 12, 32, 3, 3, 2, 1, 1, 1, 1, 1, 1, 1, 1),
+    (2, 32, 12, 15, 64, 3, 3, 1, 2, 1, 0, 1, 1, 1, 2, 1),
 ]
 
 
