@@ -177,6 +177,7 @@ Plan plan_pass(const Geom &g, gconv_dtype dt, gconv_pass pass)
         return p;
     }
     p.path = GCONV_PATH_DIRECT;
+    if (pass != GCONV_PASS_BWD_BIAS && thin_plan_pass(g, dt, pass, &p)) return p;
     if (tiled_plan(g, pass, &p)) {
         p.tc[0] = 1;   // shared-memory tiled kernels
         return p;
@@ -299,6 +300,9 @@ static gconv_status run_pass(const Geom &g, gconv_dtype dt, gconv_dtype out_dt, 
         st = tc_igemm_launch(gk, p, pass, a, b, bias, o, ws, s);
     } else if (p.path == GCONV_PATH_TC_FC) {
         st = tc_fc_launch(gk, p, pass, a, b, bias, o, ws, s);
+    } else if (p.path == GCONV_PATH_DIRECT && p.tc[0] == 2) {
+        st = thin_launch(gk, dt, pass, a, b, bias, o, pass == GCONV_PASS_BWD_WEIGHT ? db : nullptr, ws, s);
+        if (pass == GCONV_PASS_BWD_WEIGHT) db = nullptr;   // written by the same kernels
     } else if (p.path == GCONV_PATH_DIRECT && p.tc[0] == 1) {
         st = tiled_launch(gk, p, dt, pass, a, b, bias, o, ws, s);
     } else if (dt == GCONV_BF16) {

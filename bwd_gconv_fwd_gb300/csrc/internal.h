@@ -43,6 +43,13 @@ bool tiled_plan(const Geom &g, gconv_pass pass, Plan *p);
 gconv_status tiled_launch(const Geom &g, const Plan &p, gconv_dtype dt, gconv_pass pass, const void *a,
                           const void *b, const void *bias, float *out, void *ws, cudaStream_t s);
 
+// CUDA-core kernels for 3x3 layers with 1, 2 or 4 channels per group on both sides,
+// stride 1 or 2, that stage whole plane strips in shared memory (thin_plane.cu).  The
+// plan marks them tc[0] = 2; their weight gradient can produce the bias gradient too.
+bool thin_plan_pass(const Geom &g, gconv_dtype dt, gconv_pass pass, Plan *p);
+gconv_status thin_launch(const Geom &g, gconv_dtype dt, gconv_pass pass, const void *a, const void *b,
+                         const void *bias, float *out, float *db, void *ws, cudaStream_t s);
+
 // Tensor map for TMA loads of 128-byte position rows (tc_gemm.cu); false when the
 // driver entry point is unavailable or the box is invalid.
 bool encode_rows_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t planes, uint32_t box_rows);

@@ -1,0 +1,513 @@
+// thin_plane.cu -- CUDA-core kernels for 3 x 3 grouped convolutions whose groups hold one,
+// two or four channels on both sides (depthwise layers, ResNeXt-style 4-channel groups),
+// stride 1 or 2, dilation 1.  These layers move far more bytes than they compute (9 or 36
+// FMAs per output against 2 bytes read and 4 written), so the kernels are built around
+// reading every input element once from HBM and writing every output once, with enough
+// loads in flight to keep HBM busy:
+//
+//  * A block of 128 threads owns one plane group (image n, group g: the group's CG input
+//    planes) and a strip of TH output rows.  It copies the input rows the strip reads --
+//    a contiguous range of each plane in NCHW -- into shared memory with 16-byte loads,
+//    all issued before any is used, and keeps them in the input dtype.
+//  * Each thread then produces CPL consecutive outputs of one row for all CG output
+//    channels, from a 3 x (S*(CPL-1)+3) window of each staged plane read once per input
+//    channel (consecutive threads take consecutive column segments, so shared-memory
+//    reads and global stores run along rows); outputs leave as 8- or 16-byte stores.
+//  * Forward and backward-data are the same kernel: backward-data at stride 1 is the
+//    correlation of gradOutput with the mirrored, transposed weights and pads 2 - pt,
+//    2 - pl; at stride 2 each thread takes the taps whose division by the stride is exact.
+//  * The weight gradient stages x and gradOutput the same way for a chunk of images and
+//    keeps 9 accumulators per (output, input) channel pair plus one for the bias
+//    gradient, so gradOutput is read once for both (the DLPrimitives blog's "Pointwise
+//    Broadcast Reduce": the bias gradient is the sum of gradOutput over dims 0, 2, 3).
+//    Lanes and warps are added in a fixed order into per-block partial sums, and a
+//    second kernel adds the blocks in a fixed order: bitwise reproducible.
+#include "internal.h"
+
+#include <algorithm>
+
+namespace gconv {
+namespace {
+
+constexpr int kThinThreads = 128;
+constexpr int kThinSmem = 40 * 1024;   // staged rows per block (several blocks share an SM)
+
+struct ThinParams {
+    const void *src;     // forward: x; backward-data: gradOutput; weight gradient: x
+    const void *dy;      // weight gradient: gradOutput
+    const void *w;       // [C_out][C_in/G][3][3]
+    const void *bias;    // forward only, or nullptr
+    float *out;          // y / dx (fp32 or bf16), or the weight gradient's partial sums
+    int out_bf16;
+    int N, G;
+    int IH, IW;          // source extent
+    int OH, OW;          // produced extent (y / dx); the weight gradient: gradOutput's
+    int S;               // stride of the forward convolution
+    int pt, pl;          // forward / weight gradient: pads; backward-data: see thin_corr_kernel
+    int TH, n_strip;     // output rows per block, strips per plane
+    int bwd;             // backward-data
+    int nchunk, per_chunk;   // weight gradient: image chunks, images per chunk
+};
+
+// Copies n elements src[0..n) (global) to dst[0..n) (shared) with 16-byte loads where the
+// two sides share their alignment; the caller places dst so that they do.
+template <typename T>
+__device__ __forceinline__ void copy_run(const T *__restrict__ src, T *dst, int n, int tid, int nthr)
+{
+    constexpr int V = 16 / (int)sizeof(T);
+    const int head = (int)(((16 - (reinterpret_cast<uintptr_t>(src) & 15)) & 15) / sizeof(T));
+    const int h = min(head, n);
+    for (int i = tid; i < h; i += nthr) dst[i] = src[i];
+    const int nv = (n - h) / V;
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src + h);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst + h);
+    for (int i = tid; i < nv; i += nthr) d4[i] = __ldg(s4 + i);
+    for (int i = h + nv * V + tid; i < n; i += nthr) dst[i] = src[i];
+}
+
+// Shared-memory offset (in elements) that gives dst the 16-byte alignment of src.
+template <typename T>
+__device__ __forceinline__ int align_like(const T *src)
+{
+    return (int)((reinterpret_cast<uintptr_t>(src) & 15) / sizeof(T));
+}
+
+// Copies rows [lo, hi] of CG consecutive planes of src into shared memory: plane c goes to
+// stage + c*pitch + align_like(its first row), `pitch` elements a plane (a multiple of 16
+// bytes, at least the rows plus 16 bytes); staged_plane() gives where its row lo starts.
+template <typename T>
+__device__ __forceinline__ void stage_planes(const T *__restrict__ src, int64_t plane, int CG, int IW, int lo,
+                                             int hi, T *stage, int pitch)
+{
+    const int n = (hi - lo + 1) * IW;
+    for (int c = 0; c < CG; ++c) {
+        const T *s = src + c * plane + (int64_t)lo * IW;
+        copy_run(s, stage + c * pitch + align_like(s), n, threadIdx.x, kThinThreads);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ const T *staged_plane(const T *stage, int pitch, const T *src, int64_t plane, int c, int IW,
+                                                 int lo)
+{
+    return stage + c * pitch + align_like(src + c * plane + (int64_t)lo * IW);
+}
+
+// ---------------------------------------------------------------------------
+// Forward / backward-data.  Block: (image n, group g, strip of TH produced rows).
+// Produced value (o, r, c) = sum over input planes i < CG, taps (a, b) of
+//   Wt[o][i][a][b] * src[i][r*S - pt + a][c*S - pl + b]                     (forward)
+// and for backward-data (src = gradOutput, produced = dx):
+//   S = 1: Wt[c][o][a][b] = w[g*CG + o][c][2-a][2-b], src row r - (2 - pt) + a
+//   S = 2: dx[c][r][q] = sum over (a, b) with r + pt - a and q + pl - b even of
+//          w[g*CG + o][c][a][b] * dy[o][(r + pt - a)/2][(q + pl - b)/2]
+template <typename T, int CG, int S, int CPL>
+__global__ void __launch_bounds__(kThinThreads)
+thin_corr_kernel(const __grid_constant__ ThinParams p)
+{
+    extern __shared__ __align__(16) unsigned char thin_sm[];
+    __shared__ float ws[CG * CG * 9];          // [out][in][tap], the tap order of the sum above
+    const T *src = static_cast<const T *>(p.src);
+    const T *W = static_cast<const T *>(p.w);
+    int b = blockIdx.x;
+    const int strip = b % p.n_strip; b /= p.n_strip;
+    const int g = b % p.G;
+    const int n = b / p.G;
+    const int r0 = strip * p.TH;
+    const int rows = min(p.TH, p.OH - r0);
+    // weights of the group, in the orientation of this pass
+    for (int i = threadIdx.x; i < CG * CG * 9; i += kThinThreads) {
+        const int o = i / (CG * 9), rem = i - o * CG * 9, ci = rem / 9, tap = rem - ci * 9;
+        float v;
+        if (!p.bwd) v = to_f(W[((int64_t)(g * CG + o) * CG + ci) * 9 + tap]);
+        else if (S == 1) v = to_f(W[((int64_t)(g * CG + ci) * CG + o) * 9 + (8 - tap)]);
+        else v = to_f(W[((int64_t)(g * CG + ci) * CG + o) * 9 + tap]);
+        ws[i] = v;
+    }
+    // source rows this strip reads
+    int lo, hi;
+    if (!p.bwd || S == 1) {
+        lo = r0 * S - p.pt;
+        hi = (r0 + rows - 1) * S - p.pt + 2;
+    } else {   // stride-2 backward-data: dy rows (r + pt - a)/2 for a in 0..2
+        lo = (r0 + p.pt - 2) >> 1;               // floor division (arithmetic shift)
+        hi = (r0 + rows - 1 + p.pt) >> 1;
+    }
+    const int slo = max(lo, 0), shi = min(hi, p.IH - 1);
+    const int64_t plane = (int64_t)p.IH * p.IW;
+    const int pitch = (((shi - slo + 1) * p.IW + 16 + 7) / 8) * 8;   // elements per staged plane
+    T *stage = reinterpret_cast<T *>(thin_sm);
+    const T *srcg = src + ((int64_t)n * p.G + g) * CG * plane;
+    if (shi >= slo) stage_planes(srcg, plane, CG, p.IW, slo, shi, stage, pitch);
+    __syncthreads();
+    const T *sp0[CG];
+    #pragma unroll
+    for (int ci = 0; ci < CG; ++ci) sp0[ci] = staged_plane(stage, pitch, srcg, plane, ci, p.IW, slo);
+    float bias[CG];
+    #pragma unroll
+    for (int o = 0; o < CG; ++o) bias[o] = (p.bias && !p.bwd) ? to_f(static_cast<const T *>(p.bias)[g * CG + o]) : 0.f;
+    const int nseg = (p.OW + CPL - 1) / CPL;
+    const int64_t out_plane = (int64_t)p.OH * p.OW;
+    const int64_t obase = ((int64_t)n * p.G + g) * CG * out_plane;
+    for (int idx = threadIdx.x; idx < rows * nseg; idx += kThinThreads) {
+        const int rr = idx / nseg, seg = idx - rr * nseg;
+        const int r = r0 + rr, c0 = seg * CPL;
+        float acc[CG][CPL];
+        #pragma unroll
+        for (int o = 0; o < CG; ++o)
+            #pragma unroll
+            for (int j = 0; j < CPL; ++j) acc[o][j] = bias[o];
+        if (!p.bwd || S == 1) {
+            // window: rows r*S - pt + a, columns c0*S - pl + k, k < WN
+            constexpr int WN = S * (CPL - 1) + 3;
+            const int ir0 = r * S - p.pt, ic0 = c0 * S - p.pl;
+            bool rv[3];
+            int roff[3];
+            #pragma unroll
+            for (int a = 0; a < 3; ++a) {
+                const int ih = ir0 + a;
+                rv[a] = ih >= slo && ih <= shi;
+                roff[a] = (ih - slo) * p.IW;
+            }
+            bool cv[WN];
+            #pragma unroll
+            for (int k = 0; k < WN; ++k) cv[k] = ic0 + k >= 0 && ic0 + k < p.IW;
+            #pragma unroll
+            for (int ci = 0; ci < CG; ++ci) {
+                const T *sp = sp0[ci];
+                float win[3][WN];
+                #pragma unroll
+                for (int a = 0; a < 3; ++a)
+                    #pragma unroll
+                    for (int k = 0; k < WN; ++k) win[a][k] = (rv[a] && cv[k]) ? to_f(sp[roff[a] + ic0 + k]) : 0.f;
+                #pragma unroll
+                for (int o = 0; o < CG; ++o)
+                    #pragma unroll
+                    for (int a = 0; a < 3; ++a)
+                        #pragma unroll
+                        for (int bb = 0; bb < 3; ++bb) {
+                            const float wv = ws[(o * CG + ci) * 9 + a * 3 + bb];
+                            #pragma unroll
+                            for (int j = 0; j < CPL; ++j) acc[o][j] = fmaf(wv, win[a][j * S + bb], acc[o][j]);
+                        }
+            }
+        } else {
+            // stride-2 backward-data: tap a reaches row r when r + pt - a is even
+            #pragma unroll
+            for (int a = 0; a < 3; ++a) {
+                const int th = r + p.pt - a;
+                if (th & 1) continue;
+                const int oh = th >> 1;
+                if (oh < slo || oh > shi) continue;
+                const int ro = (oh - slo) * p.IW;
+                #pragma unroll
+                for (int j = 0; j < CPL; ++j) {
+                    const int q = c0 + j;
+                    #pragma unroll
+                    for (int bb = 0; bb < 3; ++bb) {
+                        const int tw = q + p.pl - bb;
+                        const int ow = tw >> 1;
+                        if ((tw & 1) || ow < 0 || ow >= p.IW) continue;
+                        #pragma unroll
+                        for (int ci = 0; ci < CG; ++ci) {
+                            const float v = to_f(sp0[ci][ro + ow]);
+                            #pragma unroll
+                            for (int o = 0; o < CG; ++o) acc[o][j] = fmaf(ws[(o * CG + ci) * 9 + a * 3 + bb], v, acc[o][j]);
+                        }
+                    }
+                }
+            }
+        }
+        const int64_t rowi = obase + (int64_t)r * p.OW + c0;
+        const bool full = c0 + CPL <= p.OW && ((rowi & 3) == 0) && (out_plane & 3) == 0;
+        #pragma unroll
+        for (int o = 0; o < CG; ++o) {
+            const int64_t oi = rowi + o * out_plane;
+            if (CPL % 4 == 0 && full) {
+                #pragma unroll
+                for (int j = 0; j < CPL; j += 4)
+                    store_out4(p.out, oi + j, acc[o][j], acc[o][j + 1], acc[o][j + 2], acc[o][j + 3], p.out_bf16);
+            } else {
+                #pragma unroll
+                for (int j = 0; j < CPL; ++j)
+                    if (c0 + j < p.OW) store_out(p.out, oi + j, acc[o][j], p.out_bf16);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Weight gradient + bias gradient.  Block: (group g, image chunk, strip of TH gradOutput
+// rows).  Warp w takes output channel o = w % CG and every (4/CG)-th row segment; per
+// (o, i, tap) it accumulates dy[o][r][c] * x[i][r*S - pt + a][c*S - pl + b] over its
+// positions and images, and sum dy[o] for the bias.  Lanes, then warps of the same o,
+// are added in a fixed order into part[block][o][i*9 + tap] and part[block][o][CG*9].
+template <typename T, int CG, int S, int CPL>
+__global__ void __launch_bounds__(kThinThreads)
+thin_wgrad_kernel(const __grid_constant__ ThinParams p)
+{
+    extern __shared__ __align__(16) unsigned char thin_sm[];
+    constexpr int NA = CG * 9 + 1;            // accumulators per thread
+    constexpr int WPO = 4 / CG;               // warps per output channel
+    __shared__ float red[4][NA];
+    const T *X = static_cast<const T *>(p.src);
+    const T *DY = static_cast<const T *>(p.dy);
+    int b = blockIdx.x;
+    const int strip = b % p.n_strip; b /= p.n_strip;
+    const int chunk = b % p.nchunk;
+    const int g = b / p.nchunk;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int o = warp % CG, part_w = warp / CG;
+    const int r0 = strip * p.TH;
+    const int rows = min(p.TH, p.OH - r0);
+    const int lo = r0 * S - p.pt, hi = (r0 + rows - 1) * S - p.pt + 2;
+    const int slo = max(lo, 0), shi = min(hi, p.IH - 1);
+    const int64_t xplane = (int64_t)p.IH * p.IW, yplane = (int64_t)p.OH * p.OW;
+    const int xpitch = (((shi - slo + 1) * p.IW + 16 + 7) / 8) * 8;
+    const int ypitch = ((rows * p.OW + 16 + 7) / 8) * 8;
+    T *xs = reinterpret_cast<T *>(thin_sm);
+    T *ys = xs + CG * xpitch;
+    float acc[NA];
+    #pragma unroll
+    for (int k = 0; k < NA; ++k) acc[k] = 0.f;
+    const int nseg = (p.OW + CPL - 1) / CPL;
+    constexpr int WN = S * (CPL - 1) + 3;
+    const int n0 = chunk * p.per_chunk, n1 = min(p.N, n0 + p.per_chunk);
+    for (int n = n0; n < n1; ++n) {
+        const T *xg = X + ((int64_t)n * p.G + g) * CG * xplane;
+        const T *yg = DY + ((int64_t)n * p.G + g) * CG * yplane;
+        if (shi >= slo) stage_planes(xg, xplane, CG, p.IW, slo, shi, xs, xpitch);
+        stage_planes(yg, yplane, CG, p.OW, r0, r0 + rows - 1, ys, ypitch);
+        __syncthreads();
+        const T *yo = staged_plane(ys, ypitch, yg, yplane, o, p.OW, r0);
+        const T *xp0[CG];
+        #pragma unroll
+        for (int ci = 0; ci < CG; ++ci) xp0[ci] = staged_plane(xs, xpitch, xg, xplane, ci, p.IW, slo);
+        for (int idx = part_w * 32 + lane; idx < rows * nseg; idx += WPO * 32) {
+            const int rr = idx / nseg, seg = idx - rr * nseg;
+            const int c0 = seg * CPL;
+            float d[CPL];
+            #pragma unroll
+            for (int j = 0; j < CPL; ++j)
+                d[j] = c0 + j < p.OW ? to_f(yo[rr * p.OW + c0 + j]) : 0.f;
+            #pragma unroll
+            for (int j = 0; j < CPL; ++j) acc[CG * 9] += d[j];
+            const int ir0 = (r0 + rr) * S - p.pt, ic0 = c0 * S - p.pl;
+            bool rv[3];
+            int roff[3];
+            #pragma unroll
+            for (int a = 0; a < 3; ++a) {
+                const int ih = ir0 + a;
+                rv[a] = ih >= slo && ih <= shi;
+                roff[a] = (ih - slo) * p.IW;
+            }
+            bool cv[WN];
+            #pragma unroll
+            for (int k = 0; k < WN; ++k) cv[k] = ic0 + k >= 0 && ic0 + k < p.IW;
+            #pragma unroll
+            for (int ci = 0; ci < CG; ++ci) {
+                const T *sp = xp0[ci];
+                float win[3][WN];
+                #pragma unroll
+                for (int a = 0; a < 3; ++a)
+                    #pragma unroll
+                    for (int k = 0; k < WN; ++k) win[a][k] = (rv[a] && cv[k]) ? to_f(sp[roff[a] + ic0 + k]) : 0.f;
+                #pragma unroll
+                for (int a = 0; a < 3; ++a)
+                    #pragma unroll
+                    for (int bb = 0; bb < 3; ++bb)
+                        #pragma unroll
+                        for (int j = 0; j < CPL; ++j)
+                            acc[ci * 9 + a * 3 + bb] = fmaf(d[j], win[a][j * S + bb], acc[ci * 9 + a * 3 + bb]);
+            }
+        }
+        __syncthreads();   // the staged planes are no longer read
+    }
+    // lanes in a fixed order (butterfly), then the warps of one output channel in warp order
+    #pragma unroll
+    for (int k = 0; k < NA; ++k) {
+        float v = acc[k];
+        #pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        acc[k] = v;
+    }
+    if (lane == 0)
+        #pragma unroll
+        for (int k = 0; k < NA; ++k) red[warp][k] = acc[k];
+    __syncthreads();
+    float *dst = p.out + (int64_t)blockIdx.x * CG * NA;
+    for (int i = threadIdx.x; i < CG * NA; i += kThinThreads) {
+        const int oo = i / NA, k = i - oo * NA;
+        float s = 0.f;
+        for (int q = 0; q < WPO; ++q) s += red[q * CG + oo][k];
+        dst[i] = s;
+    }
+}
+
+// dw[g*CG + o][i][tap] and db[g*CG + o] from the blocks' partial sums, added in block order.
+template <int CG>
+__global__ void thin_wgrad_finish_kernel(const float *__restrict__ part, int G, int blocks_per_group,
+                                         float *__restrict__ dw, float *__restrict__ db)
+{
+    constexpr int NA = CG * 9 + 1;
+    const int total = G * CG * NA;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+        const int g = e / (CG * NA), rem = e - g * CG * NA;
+        const float *pp = part + (int64_t)g * blocks_per_group * CG * NA + rem;
+        float s = 0.f;
+        for (int k = 0; k < blocks_per_group; ++k) s += pp[(int64_t)k * CG * NA];
+        const int o = rem / NA, a = rem - o * NA;
+        if (a < CG * 9) dw[(int64_t)(g * CG + o) * CG * 9 + a] = s;
+        else if (db) db[g * CG + o] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Planning and launch
+
+int thin_cpl(int ow) { return ow >= 48 ? 4 : (ow >= 16 ? 2 : 1); }
+
+// Staged elements of one block for a strip of `th` produced rows.
+int64_t thin_stage_elems(const ThinParams &p, int CG, int th, bool wgrad, int esize)
+{
+    int in_rows;
+    if (!p.bwd || p.S == 1) in_rows = (th - 1) * p.S + 3;
+    else in_rows = (th + 1) / 2 + 2;
+    in_rows = std::min(in_rows, p.IH);
+    int64_t e = (int64_t)CG * ((((int64_t)in_rows * p.IW + 16 + 7) / 8) * 8);
+    if (wgrad) e += (int64_t)CG * ((((int64_t)th * p.OW + 16 + 7) / 8) * 8);
+    return e * esize;
+}
+
+bool thin_eligible(const Geom &g)
+{
+    return g.kH == 3 && g.kW == 3 && g.d_h == 1 && g.d_w == 1 && g.s_h == g.s_w && g.s_h <= 2 && g.Cgi == g.Cgo &&
+           (g.Cgi == 1 || g.Cgi == 2 || g.Cgi == 4) && g.pt <= 2 && g.pl <= 2;
+}
+
+// Strip height: about 4 resident blocks' worth of work per SM in total, staged rows within
+// the shared-memory budget.
+bool thin_plan(const Geom &g, gconv_pass pass, int esize, ThinParams *p, int *grid, size_t *smem, size_t *ws)
+{
+    if (!thin_eligible(g)) return false;
+    if (pass != GCONV_PASS_FWD && pass != GCONV_PASS_BWD_DATA && pass != GCONV_PASS_BWD_WEIGHT) return false;
+    const int CG = g.Cgi;
+    *p = ThinParams{};
+    p->N = g.N; p->G = g.G; p->S = g.s_h;
+    p->bwd = pass == GCONV_PASS_BWD_DATA ? 1 : 0;
+    if (pass == GCONV_PASS_BWD_DATA) {
+        p->IH = g.Ho; p->IW = g.Wo; p->OH = g.H; p->OW = g.W;
+        p->pt = g.s_h == 1 ? 2 - g.pt : g.pt;
+        p->pl = g.s_h == 1 ? 2 - g.pl : g.pl;
+        if (g.s_h == 1 && (p->pt < 0 || p->pl < 0)) return false;
+    } else {
+        p->IH = g.H; p->IW = g.W; p->OH = g.Ho; p->OW = g.Wo;
+        p->pt = g.pt; p->pl = g.pl;
+    }
+    const bool wg = pass == GCONV_PASS_BWD_WEIGHT;
+    const int64_t planes = (int64_t)g.N * g.G;
+    const int64_t target_blocks = (int64_t)num_sms() * 16;
+    int th = p->OH;
+    if (!wg) {
+        // split rows until there are enough blocks, but keep strips of 8 rows or more
+        while (th > 8 && planes * ((p->OH + th - 1) / th) < target_blocks) th = (th + 1) / 2;
+    }
+    while (th > 1 && thin_stage_elems(*p, CG, th, wg, esize) > kThinSmem) th = (th + 1) / 2;
+    if (thin_stage_elems(*p, CG, th, wg, esize) > kThinSmem) return false;
+    p->TH = th;
+    p->n_strip = (p->OH + th - 1) / th;
+    *smem = (size_t)thin_stage_elems(*p, CG, th, wg, esize);
+    *ws = 0;
+    if (!wg) {
+        *grid = (int)(planes * p->n_strip);
+        return true;
+    }
+    // weight gradient: chunks of images so that groups x chunks x strips fill the SMs
+    const int64_t per_g = std::max<int64_t>(1, (target_blocks + (int64_t)g.G * p->n_strip - 1) / ((int64_t)g.G * p->n_strip));
+    p->nchunk = (int)std::min<int64_t>(g.N, per_g);
+    p->per_chunk = (g.N + p->nchunk - 1) / p->nchunk;
+    p->nchunk = (g.N + p->per_chunk - 1) / p->per_chunk;
+    *grid = g.G * p->nchunk * p->n_strip;
+    *ws = (size_t)(*grid) * CG * (CG * 9 + 1) * sizeof(float);
+    return true;
+}
+
+template <typename T, int CG, int S>
+gconv_status thin_launch_t(const ThinParams &p, int grid, size_t smem, bool wgrad, float *dw, float *db, cudaStream_t s)
+{
+    const int cpl = thin_cpl(wgrad ? p.OW : p.OW);
+    if (wgrad) {
+        switch (cpl) {
+        case 4: thin_wgrad_kernel<T, CG, S, 4><<<grid, kThinThreads, smem, s>>>(p); break;
+        case 2: thin_wgrad_kernel<T, CG, S, 2><<<grid, kThinThreads, smem, s>>>(p); break;
+        default: thin_wgrad_kernel<T, CG, S, 1><<<grid, kThinThreads, smem, s>>>(p); break;
+        }
+        const int total = p.G * CG * (CG * 9 + 1);
+        thin_wgrad_finish_kernel<CG><<<(total + 255) / 256, 256, 0, s>>>(p.out, p.G, p.nchunk * p.n_strip, dw, db);
+        return GCONV_OK;
+    }
+    switch (cpl) {
+    case 4: thin_corr_kernel<T, CG, S, 4><<<grid, kThinThreads, smem, s>>>(p); break;
+    case 2: thin_corr_kernel<T, CG, S, 2><<<grid, kThinThreads, smem, s>>>(p); break;
+    default: thin_corr_kernel<T, CG, S, 1><<<grid, kThinThreads, smem, s>>>(p); break;
+    }
+    return GCONV_OK;
+}
+
+template <typename T>
+gconv_status thin_launch_dt(const Geom &g, const ThinParams &p, int grid, size_t smem, bool wgrad, float *dw,
+                            float *db, cudaStream_t s)
+{
+    const int key = g.Cgi * 10 + g.s_h;
+    switch (key) {
+    case 11: return thin_launch_t<T, 1, 1>(p, grid, smem, wgrad, dw, db, s);
+    case 12: return thin_launch_t<T, 1, 2>(p, grid, smem, wgrad, dw, db, s);
+    case 21: return thin_launch_t<T, 2, 1>(p, grid, smem, wgrad, dw, db, s);
+    case 22: return thin_launch_t<T, 2, 2>(p, grid, smem, wgrad, dw, db, s);
+    case 41: return thin_launch_t<T, 4, 1>(p, grid, smem, wgrad, dw, db, s);
+    case 42: return thin_launch_t<T, 4, 2>(p, grid, smem, wgrad, dw, db, s);
+    }
+    return GCONV_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+bool thin_plan_pass(const Geom &g, gconv_dtype dt, gconv_pass pass, Plan *plan)
+{
+    ThinParams p;
+    int grid = 0;
+    size_t smem = 0, ws = 0;
+    if (!thin_plan(g, pass, dt == GCONV_BF16 ? 2 : 4, &p, &grid, &smem, &ws)) return false;
+    plan->path = GCONV_PATH_DIRECT;
+    plan->tc[0] = 2;   // thin-plane kernels
+    plan->launches = pass == GCONV_PASS_BWD_WEIGHT ? 2 : 1;
+    plan->ws_bytes = ws;
+    return true;
+}
+
+bool thin_fuses_bias(const Geom &g, gconv_dtype dt)
+{
+    Plan p;
+    return thin_plan_pass(g, dt, GCONV_PASS_BWD_WEIGHT, &p);
+}
+
+gconv_status thin_launch(const Geom &g, gconv_dtype dt, gconv_pass pass, const void *a, const void *b,
+                         const void *bias, float *out, float *db, void *ws, cudaStream_t s)
+{
+    ThinParams p;
+    int grid = 0;
+    size_t smem = 0, wsb = 0;
+    if (!thin_plan(g, pass, dt == GCONV_BF16 ? 2 : 4, &p, &grid, &smem, &wsb)) return GCONV_ERR_UNSUPPORTED;
+    const bool wg = pass == GCONV_PASS_BWD_WEIGHT;
+    p.src = a;
+    p.w = wg ? nullptr : b;
+    p.dy = wg ? b : nullptr;
+    p.bias = pass == GCONV_PASS_FWD ? bias : nullptr;
+    p.out = wg ? static_cast<float *>(ws) : out;
+    p.out_bf16 = wg ? 0 : g.out_bf16;
+    if (smem > 48 * 1024) return GCONV_ERR_UNSUPPORTED;   // within the default dynamic limit
+    return dt == GCONV_BF16 ? thin_launch_dt<__nv_bfloat16>(g, p, grid, smem, wg, out, db, s)
+                            : thin_launch_dt<float>(g, p, grid, smem, wg, out, db, s);
+}
+
+}  // namespace gconv

@@ -495,3 +495,37 @@ def test_bf16_outputs(dev, oracle_mod, geom, paths):
         rms = float(np.sqrt(np.mean(ref * ref)))
         bound = 1e-2 * rms + 2.0 ** -8 * np.abs(ref)
         assert np.all(np.abs(g - ref) <= bound), (name, geom, float(np.max(np.abs(g - ref) - bound)))
+
+
+# The thin-plane kernels (3x3, one, two or four channels per group on both sides, stride 1 or
+# 2): widths that select 1, 2 and 4 outputs per thread, pads 0..2, strips of rows, both
+# input dtypes, and the weight gradient with its bias gradient from the same call.
+THIN_PLANE = [
+    (2, 16, 10, 10, 16, 3, 3, 1, 1, 1, 1, 1, 1, 16),        # depthwise, 1 output per thread
+    (2, 8, 21, 20, 8, 3, 3, 1, 0, 2, 2, 0, 1, 8),           # depthwise, pads 0/2/2/0, 2 per thread
+    (2, 8, 9, 60, 8, 3, 3, 1, 2, 1, 1, 2, 1, 2),            # 4 channels per group, 4 per thread
+    (3, 12, 17, 33, 12, 3, 3, 2, 1, 1, 1, 1, 1, 6),         # 2 channels per group, stride 2
+    (2, 32, 23, 50, 32, 3, 3, 2, 0, 1, 0, 1, 1, 8),         # 4 per group, stride 2, asymmetric pads
+    (1, 6, 7, 7, 6, 3, 3, 2, 1, 1, 1, 1, 1, 6),             # depthwise stride 2, tiny plane
+    (4, 64, 7, 7, 64, 3, 3, 1, 1, 1, 1, 1, 1, 64),          # small planes, many groups
+]
+
+
+@pytest.mark.parametrize("geom", THIN_PLANE)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_thin_plane_kernels_full(dev, oracle_mod, geom, dtype):
+    assert_paths(geom, dtype, (CC, CC, CC, RD))
+    wk = wl.Workload("thin", geom, dtype, w=("normal", 0.3))
+    x, w, b, dy = wl.make_inputs(wk, seed=sum(geom) * 29 + (dtype == "f32"))
+    got = full_compare(geom, dtype, x, w, b, dy, dev, oracle_mod, label=f"thin {geom}")
+    # the bias gradient computed with the weight gradient: identical to the separate pass
+    xd, dyd = x.to(dev), dy.to(dev)
+    dw, bw = guarded(tuple(w.shape), dev)
+    db, bb = guarded((geom[4],), dev)
+    gc.gconv_bwd_weight(xd, dyd, dw, db=db, **_kw(geom))
+    torch.cuda.synchronize()
+    assert gc.gconv_check_device_error() == B.GCONV_OK
+    check_guards("thin fused dw", bw)
+    check_guards("thin fused db", bb)
+    assert torch.equal(dw.cpu(), got["dw"])
+    check("thin fused db", db.cpu().numpy(), oracle_mod.bwd_bias(geom, f64(dy)), TOL[dtype])
