@@ -1,7 +1,8 @@
 #!/usr/bin/env python3
 """Benchmark: one step = fwd + bwd_data + bwd_weight + bwd_bias of the AlexNet-style
 2-group convolution (x [128,96,27,27] bf16, w [256,48,5,5], groups 2, pad 2,
-stride 1; fp32 outputs), through the C ABI of libgconv.
+stride 1; fp32 outputs), through the C ABI of libgconv; the weight and bias gradients
+come from one call (gconv_bwd_weight_ex with db, which reads gradOutput once).
 
 Prints ONE JSON line (rank 0).  `value` is whole-job TFLOP/s with inputs resident
 in HBM (3 x 2*N*C_out*Ho*Wo*(C_in/G)*kH*kW FLOP per step over the device time of
@@ -71,7 +72,8 @@ def algorithmic_bytes(geom, in_bytes=2):
     return {"fwd": x * in_bytes + w * in_bytes + Cout * in_bytes + y * 4,
             "bwd_data": y * in_bytes + w * in_bytes + x * 4,
             "bwd_weight": x * in_bytes + y * in_bytes + w * 4,
-            "bwd_bias": y * in_bytes + Cout * 4}
+            "bwd_bias": y * in_bytes + Cout * 4,
+            "bwd_weight_bias": x * in_bytes + y * in_bytes + w * 4 + Cout * 4}
 
 
 def kernel_source_hash():
@@ -236,7 +238,7 @@ def config_dict(wk):
     N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = wk.geom
     return {"workload": f"{wk.name}: x[{N},{Cin},{H},{W}] {wk.dtype}, w[{Cout},{Cin // G},{kH},{kW}], groups {G}, "
                         f"stride {s}, pads {pt}/{pb}/{pl}/{pr}, dilation {d}; fp32 outputs",
-            "step": "fwd + bwd_data + bwd_weight + bwd_bias", "N": N, "C_in": Cin, "H": H, "W": W,
+            "step": "fwd + bwd_data + (bwd_weight + bwd_bias in one call)", "N": N, "C_in": Cin, "H": H, "W": W,
             "C_out": Cout, "kH": kH, "kW": kW, "groups": G, "stride": s, "pads": [pt, pb, pl, pr],
             "dilation": d, "l2": "flushed between steps by a 256 MiB write outside the timed events",
             "parallelism": "replicas"}
@@ -280,12 +282,11 @@ def bench_gpu(args):
         yield "fwd"
         B.gconv_bwd_data_ptr(geom, dt, dyd.data_ptr(), wd.data_ptr(), dx.data_ptr(), wsp, wsb, sp)
         yield "bwd_data"
-        B.gconv_bwd_weight_ptr(geom, dt, xd.data_ptr(), dyd.data_ptr(), dw.data_ptr(), wsp, wsb, sp)
-        yield "bwd_weight"
-        B.gconv_bwd_bias_ptr(geom, dt, dyd.data_ptr(), db.data_ptr(), wsp, wsb, sp)
-        yield "bwd_bias"
+        # the weight gradient and the bias gradient from one call (one read of gradOutput)
+        B.gconv_bwd_weight_ex_ptr(geom, dt, xd.data_ptr(), dyd.data_ptr(), dw.data_ptr(), db.data_ptr(), wsp, wsb, sp)
+        yield "bwd_weight_bias"
 
-    names = ["fwd", "bwd_data", "bwd_weight", "bwd_bias"]
+    names = ["fwd", "bwd_data", "bwd_weight_bias"]
     plans = {nm: gc.gconv_plan(geom, dt, p) for p, nm in enumerate(names)}
     launches_per_step = sum(l for _, l in plans.values())
 
@@ -296,7 +297,7 @@ def bench_gpu(args):
     torch.cuda.synchronize()
     assert gc.gconv_check_device_error(stream) == B.GCONV_OK
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -313,7 +314,7 @@ def bench_gpu(args):
         torch.distributed.barrier()
     assert gc.gconv_check_device_error(stream) == B.GCONV_OK
     per_pass = {nm: [ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(args.steps)] for j, nm in enumerate(names)}
-    step_ms = [ev[k][0].elapsed_time(ev[k][4]) for k in range(args.steps)]
+    step_ms = [ev[k][0].elapsed_time(ev[k][len(names)]) for k in range(args.steps)]
     total_ms = reduce_max(sum(step_ms), world)
     ms_per_step = total_ms / args.steps
     fpp = flop_per_pass(geom)
@@ -367,15 +368,12 @@ def bench_gpu(args):
     abytes = algorithmic_bytes(geom)
     hbm = peaks["hbm_gbs"] * 1e9
     tc = peaks["bf16_tflops"] * 1e12
-    if dom == "bwd_bias":
-        bound, ach, peak, unit = "hbm", abytes[dom] / (avg[dom] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    t_c, t_m = fpp / tc, abytes[dom] / hbm
+    if t_c >= t_m:
+        bound, ach, peak, unit = "tensor", fpp / (avg[dom] * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     else:
-        t_c, t_m = fpp / tc, abytes[dom] / hbm
-        if t_c >= t_m:
-            bound, ach, peak, unit = "tensor", fpp / (avg[dom] * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
-        else:
-            bound, ach, peak, unit = "hbm", abytes[dom] / (avg[dom] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
-    roof_step_s = sum(max(fpp / tc, abytes[nm] / hbm) if nm != "bwd_bias" else abytes[nm] / hbm for nm in names)
+        bound, ach, peak, unit = "hbm", abytes[dom] / (avg[dom] * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    roof_step_s = sum(max(fpp / tc, abytes[nm] / hbm) for nm in names)
     clocks = clk.summary()
 
     cpu = None
@@ -395,7 +393,7 @@ def bench_gpu(args):
                      + " per launch"},
         "step_roofline_frac": roof_step_s * 1e3 / ms_per_step,
         "passes": {nm: {"us": avg[nm] * 1e3, "path": gc.PATH_NAMES[plans[nm][0]], "launches": plans[nm][1],
-                        "tflops": (fpp / (avg[nm] * 1e-3) / 1e12) if nm != "bwd_bias" else None,
+                        "tflops": fpp / (avg[nm] * 1e-3) / 1e12,
                         "gbs": abytes[nm] / (avg[nm] * 1e-3) / 1e9} for nm in names},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -505,13 +503,16 @@ def time_workload(wk, dev, reps, warmup, flush, peaks):
         "bwd_data": lambda: B.gconv_bwd_data_ptr(geom, dt, dy.data_ptr(), w.data_ptr(), dx.data_ptr(), ws.data_ptr(), wsb, sp),
         "bwd_weight": lambda: B.gconv_bwd_weight_ptr(geom, dt, x.data_ptr(), dy.data_ptr(), dw.data_ptr(), ws.data_ptr(), wsb, sp),
         "bwd_bias": lambda: B.gconv_bwd_bias_ptr(geom, dt, dy.data_ptr(), db.data_ptr(), ws.data_ptr(), wsb, sp),
+        "bwd_weight_bias": lambda: B.gconv_bwd_weight_ex_ptr(geom, dt, x.data_ptr(), dy.data_ptr(), dw.data_ptr(),
+                                                             db.data_ptr(), ws.data_ptr(), wsb, sp),
     }
+    pass_code = {"fwd": 0, "bwd_data": 1, "bwd_weight": 2, "bwd_bias": 3, "bwd_weight_bias": 2}
     in_bytes = 2 if wk.dtype == "bf16" else 4
     fpp = flop_per_pass(geom)
     abytes = algorithmic_bytes(geom, in_bytes)
     hbm = peaks["hbm_gbs"] * 1e9
     out = {}
-    for i, (nm, f) in enumerate(calls.items()):
+    for nm, f in calls.items():
         times = []
         for k in range(warmup + reps):
             flush.zero_()
@@ -523,12 +524,12 @@ def time_workload(wk, dev, reps, warmup, flush, peaks):
             if k >= warmup:
                 times.append(e0.elapsed_time(e1) * 1e-3)
         t = statistics.median(times)
-        path, launches = gc.gconv_plan(geom, dt, i)
+        path, launches = gc.gconv_plan(geom, dt, pass_code[nm])
         pname = gc.PATH_NAMES[path]
         t_mem = abytes[nm] / hbm
         if nm == "bwd_bias":
             t_cmp, unit_peak = 0.0, None
-        elif pname in ("tc_igemm", "tc_fc"):
+        elif pname.startswith("tc_"):
             t_cmp, unit_peak = fpp / (peaks["bf16_tflops"] * 1e12), "bf16 tensor (measured burst)"
         else:
             t_cmp, unit_peak = fpp / (fp32_peak_tflops(peaks) * 1e12), "fp32 FMA (derived)"
@@ -538,9 +539,11 @@ def time_workload(wk, dev, reps, warmup, flush, peaks):
                    "bound": "hbm" if t_mem >= t_cmp else ("tensor" if unit_peak.startswith("bf16") else "fp32"),
                    "roofline_us": max(t_mem, t_cmp) * 1e6, "roofline_frac": max(t_mem, t_cmp) / t}
     assert gc.gconv_check_device_error(st) == B.GCONV_OK
-    step_us = sum(v["us"] for v in out.values())
-    roof_us = sum(v["roofline_us"] for v in out.values())
-    return {"passes": out, "step_us": step_us, "step_tflops": 3 * fpp / (step_us * 1e-6) / 1e12,
+    step = ("fwd", "bwd_data", "bwd_weight_bias")      # the step: weight and bias gradients from one call
+    step_us = sum(out[k]["us"] for k in step)
+    roof_us = sum(out[k]["roofline_us"] for k in step)
+    return {"passes": out, "step": "+".join(step), "step_us": step_us,
+            "step_tflops": 3 * fpp / (step_us * 1e-6) / 1e12,
             "step_roofline_frac": roof_us / step_us, "gflop_per_pass": fpp / 1e9}
 
 
@@ -579,7 +582,9 @@ def bench_sweep(args):
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    for name, wk in wl.model_zoo(32).items():
+    layers = dict(wl.model_zoo(32))
+    layers.update(wl.pointwise_zoo(32))
+    for name, wk in layers.items():
         rec = time_workload(wk, dev, args.steps, args.warmup, flush, peaks)
         print(json.dumps({"sweep": name, "geom": list(wk.geom), "gflop_per_pass": rec["gflop_per_pass"],
                           "passes": rec["passes"], "peak_source": peak_src}), flush=True)
@@ -597,7 +602,9 @@ def bench_one_workload(args):
     torch.cuda.set_device(dev)
     peaks, peak_src = load_peaks()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    wk = wl.WORKLOADS[args.workload] if args.workload in wl.WORKLOADS else wl.model_zoo(32)[args.workload]
+    zoo = dict(wl.model_zoo(32))
+    zoo.update(wl.pointwise_zoo(32))
+    wk = wl.WORKLOADS[args.workload] if args.workload in wl.WORKLOADS else zoo[args.workload]
     rec = time_workload(wk, dev, args.steps, args.warmup, flush, peaks)
     rec["workload"] = config_dict(wk)["workload"]
     rec["peak_source"] = peak_src

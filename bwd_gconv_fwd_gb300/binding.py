@@ -29,9 +29,9 @@ GCONV_OK, GCONV_ERR_INVALID_ARG, GCONV_ERR_UNSUPPORTED, GCONV_ERR_WORKSPACE, GCO
     GCONV_ERR_TIMEOUT = range(6)
 GCONV_F32, GCONV_BF16 = 0, 1
 PASS_FWD, PASS_BWD_DATA, PASS_BWD_WEIGHT, PASS_BWD_BIAS = range(4)
-PATH_NONE, PATH_DIRECT, PATH_TC_IGEMM, PATH_TC_FC, PATH_REDUCE = range(5)
+PATH_NONE, PATH_DIRECT, PATH_TC_IGEMM, PATH_TC_FC, PATH_REDUCE, PATH_TC_GEMM = range(6)
 PATH_NAMES = {PATH_NONE: "none", PATH_DIRECT: "direct", PATH_TC_IGEMM: "tc_igemm",
-              PATH_TC_FC: "tc_fc", PATH_REDUCE: "reduce"}
+              PATH_TC_FC: "tc_fc", PATH_REDUCE: "reduce", PATH_TC_GEMM: "tc_gemm1x1"}
 
 EXPORTED = ("gconv_out_shape", "gconv_workspace_size", "gconv_plan", "gconv_fwd", "gconv_bwd_data",
             "gconv_bwd_weight", "gconv_bwd_bias", "gconv_check_device_error", "gconv_status_string",

@@ -166,7 +166,7 @@ Plan plan_pass(const Geom &g, gconv_dtype dt, gconv_pass pass)
     }
     const int force = forced_path();
     // Tensor-core families first (bf16 inputs only), unless a test forces a family.
-    if (dt == GCONV_BF16 && (force == GCONV_PATH_NONE || force == GCONV_PATH_TC_FC)) {
+    if (dt == GCONV_BF16 && (force == GCONV_PATH_NONE || force == GCONV_PATH_TC_FC || force == GCONV_PATH_TC_GEMM)) {
         if (tc_fc_plan(g, pass, &p)) return p;
     }
     if (dt == GCONV_BF16 && (force == GCONV_PATH_NONE || force == GCONV_PATH_TC_IGEMM)) {
@@ -297,8 +297,10 @@ static gconv_status run_pass(const Geom &g, gconv_dtype dt, gconv_dtype out_dt, 
     gk.out_bf16 = out_dt == GCONV_BF16 ? 1 : 0;
     gconv_status st = GCONV_OK;
     if (p.path == GCONV_PATH_TC_IGEMM) {
-        st = tc_igemm_launch(gk, p, pass, a, b, bias, o, ws, s);
-    } else if (p.path == GCONV_PATH_TC_FC) {
+        bool db_done = false;
+        st = tc_igemm_launch(gk, p, pass, a, b, bias, o, pass == GCONV_PASS_BWD_WEIGHT ? db : nullptr, ws, s, &db_done);
+        if (db_done) db = nullptr;   // written by the same launches
+    } else if (p.path == GCONV_PATH_TC_FC || p.path == GCONV_PATH_TC_GEMM) {
         st = tc_fc_launch(gk, p, pass, a, b, bias, o, ws, s);
     } else if (p.path == GCONV_PATH_DIRECT && p.tc[0] == 2) {
         st = thin_launch(gk, dt, pass, a, b, bias, o, pass == GCONV_PASS_BWD_WEIGHT ? db : nullptr, ws, s);
@@ -742,21 +744,20 @@ gconv_status gconv_step_host(GEO_ARGS, gconv_dtype dtype, const void *x, const v
         STEP_CHECK(cudaMemcpyAsync(reinterpret_cast<uint8_t *>(y) + yo, reinterpret_cast<const uint8_t *>(yd) + yo,
                                    (size_t)(n_lo[c + 1] - n_lo[c]) * y_img, cudaMemcpyDeviceToHost, ss->out));
     }
-    // the three backward passes
+    // the backward passes: data gradient, then the weight gradient with the bias gradient
+    // in the same call (both read gradOutput; the families that can take both from one read do)
     STEP_CHECK(cudaStreamWaitEvent(C, ss->dy_in, 0));
-    struct Out { void *host; const void *dev; size_t bytes; };
-    const Out outs[4] = {{y, yd, L.ny}, {dx, dxd, L.ndx}, {dw, dwd, L.ndw}, {db, dbd, L.ndb}};
-    for (int pass = GCONV_PASS_BWD_DATA; pass <= GCONV_PASS_BWD_BIAS; ++pass) {
-        switch (pass) {
-        case GCONV_PASS_BWD_DATA: st = run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_DATA, dyd, wd, nullptr, dxd, nullptr, wsd, L.nws, C); break;
-        case GCONV_PASS_BWD_WEIGHT: st = run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_WEIGHT, xd, dyd, nullptr, dwd, nullptr, wsd, L.nws, C); break;
-        default: st = run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_BIAS, dyd, nullptr, nullptr, dbd, nullptr, wsd, L.nws, C); break;
-        }
-        if (st != GCONV_OK) return st;
-        STEP_CHECK(cudaEventRecord(ss->pass_done[pass], C));
-        STEP_CHECK(cudaStreamWaitEvent(ss->out, ss->pass_done[pass], 0));
-        STEP_CHECK(cudaMemcpyAsync(outs[pass].host, outs[pass].dev, outs[pass].bytes, cudaMemcpyDeviceToHost, ss->out));
-    }
+    st = run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_DATA, dyd, wd, nullptr, dxd, nullptr, wsd, L.nws, C);
+    if (st != GCONV_OK) return st;
+    STEP_CHECK(cudaEventRecord(ss->pass_done[GCONV_PASS_BWD_DATA], C));
+    STEP_CHECK(cudaStreamWaitEvent(ss->out, ss->pass_done[GCONV_PASS_BWD_DATA], 0));
+    STEP_CHECK(cudaMemcpyAsync(dx, dxd, L.ndx, cudaMemcpyDeviceToHost, ss->out));
+    st = run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_WEIGHT, xd, dyd, nullptr, dwd, dbd, wsd, L.nws, C);
+    if (st != GCONV_OK) return st;
+    STEP_CHECK(cudaEventRecord(ss->pass_done[GCONV_PASS_BWD_WEIGHT], C));
+    STEP_CHECK(cudaStreamWaitEvent(ss->out, ss->pass_done[GCONV_PASS_BWD_WEIGHT], 0));
+    STEP_CHECK(cudaMemcpyAsync(dw, dwd, L.ndw, cudaMemcpyDeviceToHost, ss->out));
+    STEP_CHECK(cudaMemcpyAsync(db, dbd, L.ndb, cudaMemcpyDeviceToHost, ss->out));
     // the caller's stream continues only when every result is in host memory
     STEP_CHECK(cudaEventRecord(ss->done, ss->out));
     STEP_CHECK(cudaStreamWaitEvent(C, ss->done, 0));

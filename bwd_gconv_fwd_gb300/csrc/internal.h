@@ -35,8 +35,11 @@ void *debug_trace(size_t *bytes);     // gconv_debug_set_trace buffer, nullptr w
 
 // tcgen05 implicit-GEMM family (tc_conv.cu)
 bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p);
+// db (weight gradient only, may be null): the bias gradient, produced by the same launches
+// when the plan allows it (*db_done then true).
 gconv_status tc_igemm_launch(const Geom &g, const Plan &p, gconv_pass pass, const void *a,
-                             const void *b, const void *bias, float *out, void *ws, cudaStream_t s);
+                             const void *b, const void *bias, float *out, float *db, void *ws, cudaStream_t s,
+                             bool *db_done);
 
 // CUDA-core kernels on shared-memory tiles for thin groups and fp32 (direct_tiled.cu)
 bool tiled_plan(const Geom &g, gconv_pass pass, Plan *p);

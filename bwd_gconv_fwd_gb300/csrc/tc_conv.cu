@@ -388,6 +388,8 @@ struct BlockifyParams {
     const __nv_bfloat16 *in;
     __nv_bfloat16 *out;
     int N, G, Cg, nchunk, IH, IW, R, C, r_off, c_off;
+    int ones = -1;   // >= 0: channel slot of the last chunk set to 1 at every position (the
+                     // weight gradient's bias column), -1: none
 };
 
 constexpr int kBlockifyThreads = 256;
@@ -430,13 +432,16 @@ blockify_kernel(const __grid_constant__ BlockifyParams p)
         const int row = r + p.r_off, col = c + p.c_off;
         const bool inside = row >= 0 && row < p.IH && col >= 0 && col < p.IW;
         const int cvalid = inside ? min(64, p.Cg - 64 * j) : 0;
+        // the bias column's channel of ones (a slot past the valid channels, every position)
+        const int one_e = (p.ones >= 0 && j == p.nchunk - 1) ? p.ones : -1;
         const int64_t plane = (int64_t)p.IH * p.IW;
         const unsigned short *src = reinterpret_cast<const unsigned short *>(p.in) + (ng * p.Cg + 64 * j) * plane +
                                     (inside ? (int64_t)row * p.IW + col : 0);
         #pragma unroll
         for (int h = 0; h < 32; ++h) {
-            const uint32_t lo = 2 * h < cvalid ? (uint32_t)__ldg(src + (2 * h) * plane) : 0u;
-            const uint32_t hi = 2 * h + 1 < cvalid ? (uint32_t)__ldg(src + (2 * h + 1) * plane) : 0u;
+            const uint32_t lo = 2 * h < cvalid ? (uint32_t)__ldg(src + (2 * h) * plane) : (2 * h == one_e ? 0x3F80u : 0u);
+            const uint32_t hi = 2 * h + 1 < cvalid ? (uint32_t)__ldg(src + (2 * h + 1) * plane)
+                                                   : (2 * h + 1 == one_e ? 0x3F80u : 0u);
             w[h] = lo | (hi << 16);
         }
     }
@@ -538,6 +543,11 @@ struct WgradParams {
     int job_off[kMaxJobs], job_delta[kMaxJobs], job_count[kMaxJobs], job_col[kMaxJobs];
     int job_tapk[kMaxJobs][4];   // kh*kW + kw of the packed taps
     unsigned long long *trace;   // optional per-CTA phase stamps (kTraceWords each), nullptr when off
+    // Bias gradient from the same MMAs: the blocked x carries a channel of ones in slot
+    // `ones` of its last chunk, so column `ones` of any tap's D[o][.] is sum_k dy[o][k].  The
+    // CTAs of job bias_job (packed tap 0) write it to bias_part[split][G*Cgo]; nullptr: off.
+    float *bias_part;
+    int ones, bias_job;
 };
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -816,6 +826,15 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
                         for (int e = 0; e < 16; ++e) acc[cc][e] = 0u;
                 }
                 if (!ready || o >= o_lim) continue;
+                if (p.bias_part && jb == p.bias_job && j == 0 && ct == p.n_ctile - 1) {
+                    float v = 0.f;
+                    #pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+                        #pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (cc * 16 + e == p.ones) v = __uint_as_float(acc[cc][e]);
+                    p.bias_part[(int64_t)split * p.G * p.Cgo + og] = v;
+                }
                 float *row = dst + ((int64_t)tapk * p.G * p.Cgo + og) * p.Cgi + ct * 64;
                 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
@@ -1175,8 +1194,14 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                         const int qh = pos / p.Wp, qw = pos - qh * p.Wp;
                         if (jc < p.tile_pos && qh < p.Qh && qw < p.Qw) {
                             const int64_t o = vout + (int64_t)qh * p.Qw + qw;
-                            for (int vv = lane >> 4; vv < vcount; vv += 2)
-                                store_out(p.V, o + vv * out_hw, tbp[vv * 17 + (lane & 15)], p.out_bf16);
+                            if (p.out_bf16) {
+                                __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(p.V) + o;
+                                for (int vv = lane >> 4; vv < vcount; vv += 2)
+                                    ob[vv * out_hw] = __float2bfloat16_rn(tbp[vv * 17 + (lane & 15)]);
+                            } else {
+                                float *of = p.V + o;
+                                for (int vv = lane >> 4; vv < vcount; vv += 2) of[vv * out_hw] = tbp[vv * 17 + (lane & 15)];
+                            }
                         }
                     }
                     ptx::named_sync(2 + part, 64);   // the upper warp may overwrite hb
@@ -1203,7 +1228,13 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                     const int qh = pos / p.Wp, qw = pos - qh * p.Wp;
                     if (qh < p.Qh && qw < p.Qw) {
                         const int64_t o = vout + (int64_t)qh * p.Qw + qw;
-                        for (int vv = 0; vv < vcount; ++vv) store_out(p.V, o + vv * out_hw, tb[vv * 33 + lane], p.out_bf16);
+                        if (p.out_bf16) {
+                            __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(p.V) + o;
+                            for (int vv = 0; vv < vcount; ++vv) ob[vv * out_hw] = __float2bfloat16_rn(tb[vv * 33 + lane]);
+                        } else {
+                            float *of = p.V + o;
+                            for (int vv = 0; vv < vcount; ++vv) of[vv * out_hw] = tb[vv * 33 + lane];
+                        }
                     }
                     __syncwarp();
                 }
@@ -1273,10 +1304,19 @@ struct ReduceParams {
     float *dw;
     int O, Cgi, kHW;
     int tap_splits[kMaxTaps];   // slices written for each tap (its job group's split count)
+    const float *bias_part;     // [bias_splits][O] bias-gradient slices, or nullptr
+    float *db;
+    int bias_splits;
 };
 
 __global__ void wgrad_reduce_kernel(const __grid_constant__ ReduceParams p)
 {
+    if (p.bias_part)
+        for (int o = blockIdx.x * blockDim.x + threadIdx.x; o < p.O; o += gridDim.x * blockDim.x) {
+            float s = 0.f;
+            for (int k = 0; k < p.bias_splits; ++k) s += p.bias_part[(int64_t)k * p.O + o];
+            p.db[o] = s;
+        }
     const int64_t count = (int64_t)p.kHW * p.O * p.Cgi;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (int64_t)gridDim.x * blockDim.x) {
         const int c = (int)(i % p.Cgi);
@@ -1578,9 +1618,10 @@ struct WgradLaunch {
     WgradParams wp;
     BlockifyParams bx, by;
     size_t smem = 0;
-    size_t part_bytes = 0, xt_bytes = 0, yt_bytes = 0;
+    size_t part_bytes = 0, xt_bytes = 0, yt_bytes = 0, bias_bytes = 0;
     size_t ws_bytes = 0;
     int grid = 0;
+    int ones = -1;   // spare channel slot that carries the bias column, -1 when C_in/G fills its chunks
 };
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
@@ -1665,7 +1706,10 @@ bool build_wgrad(const Geom &g, WgradLaunch *L)
     L->part_bytes = align256((size_t)w.splits * g.Cout * g.Cgi * w.kHW * sizeof(float));
     L->xt_bytes = align256((size_t)g.N * g.G * w.ncx * w.Rx * w.Wp * 64 * 2);
     L->yt_bytes = align256((size_t)g.N * g.G * w.ncy * g.Ho * w.Wp * 64 * 2);
-    L->ws_bytes = L->part_bytes + L->xt_bytes + L->yt_bytes;
+    // bias gradient from the same MMAs when the last input chunk has a spare channel slot
+    L->ones = g.Cgi % 64 ? g.Cgi % 64 : -1;
+    L->bias_bytes = L->ones >= 0 ? align256((size_t)w.grp_splits[0] * g.Cout * sizeof(float)) : 0;
+    L->ws_bytes = L->part_bytes + L->xt_bytes + L->yt_bytes + L->bias_bytes;
     BlockifyParams &bx = L->bx;
     bx = BlockifyParams{};
     bx.N = g.N; bx.G = g.G; bx.Cg = g.Cgi; bx.nchunk = w.ncx; bx.IH = g.H; bx.IW = g.W;
@@ -1980,8 +2024,9 @@ bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p)
 }
 
 gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const void *a, const void *b,
-                             const void *bias, float *out, void *ws, cudaStream_t s)
+                             const void *bias, float *out, float *db, void *ws, cudaStream_t s, bool *db_done)
 {
+    *db_done = false;
     uint8_t *wsb = static_cast<uint8_t *>(ws);
     if (pass == GCONV_PASS_FWD || pass == GCONV_PASS_BWD_DATA) {
         Corr2Launch L2;
@@ -2051,12 +2096,19 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
         if (!err) return GCONV_ERR_CUDA;
         __nv_bfloat16 *xt = reinterpret_cast<__nv_bfloat16 *>(wsb + L.part_bytes);
         __nv_bfloat16 *yt = reinterpret_cast<__nv_bfloat16 *>(wsb + L.part_bytes + L.xt_bytes);
+        const bool fuse_bias = db && L.ones >= 0;
         L.bx.in = static_cast<const __nv_bfloat16 *>(a);
         L.bx.out = xt;
+        L.bx.ones = fuse_bias ? L.ones : -1;
         L.by.in = static_cast<const __nv_bfloat16 *>(b);
         L.by.out = yt;
         launch_blockify(L.bx, s);
         launch_blockify(L.by, s);
+        if (fuse_bias) {
+            L.wp.bias_part = reinterpret_cast<float *>(wsb + L.part_bytes + L.xt_bytes + L.yt_bytes);
+            L.wp.ones = L.ones;
+            L.wp.bias_job = L.wp.grp_first[0];
+        }
         L.wp.XT = xt;
         L.wp.DYT = yt;
         set_wgrad_tma(&L.wp);
@@ -2076,6 +2128,12 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
         for (int gi = 0; gi < L.wp.n_tgrp; ++gi)
             for (int jb = L.wp.grp_first[gi]; jb < L.wp.grp_first[gi + 1]; ++jb)
                 for (int c = 0; c < L.wp.job_count[jb]; ++c) rp.tap_splits[L.wp.job_tapk[jb][c]] = L.wp.grp_splits[gi];
+        if (fuse_bias) {
+            rp.bias_part = L.wp.bias_part;
+            rp.db = db;
+            rp.bias_splits = L.wp.grp_splits[0];
+            *db_done = true;
+        }
         const int64_t count = (int64_t)g.Cout * g.Cgi * g.kH * g.kW;
         const int blocks = (int)std::min<int64_t>((count + 255) / 256, (int64_t)num_sms() * 8);
         wgrad_reduce_kernel<<<blocks, 256, 0, s>>>(rp);

@@ -1,11 +1,21 @@
-// tc_gemm.cu -- dense GEMM path for "input size == kernel size" (every output is
-// 1x1, no padding, dilation 1: the fully-connected case of the cudnn.torch issue
-// "SpatialConvolution running in fully-connected mode is very slow").  With
-// X = x viewed [N][C_in*kH*kW], Wm = w viewed [C_out][C_in*kH*kW]:
+// tc_gemm.cu -- dense GEMM paths on tcgen05.
+//
+// (1) "Input size == kernel size" (every output is 1x1, no padding, dilation 1: the
+// fully-connected case of the cudnn.torch issue "SpatialConvolution running in
+// fully-connected mode is very slow").  With X = x viewed [N][C_in*kH*kW] and
+// Wm = w viewed [C_out][C_in*kH*kW]:
 //     forward        Y  = X Wm^T + bias   (A = X  K-major,  B = Wm K-major)
 //     backward-data  dX = dY Wm           (A = dY K-major,  B = Wm MN-major)
 //     backward-wt    dW = dY^T X          (A = dY MN-major, B = X  MN-major)
 // so every pass is one GEMM on the tensors as they lie, no transposes.
+//
+// (2) 1x1 convolutions at stride 1 without padding, which the same issue's thread sets
+// apart from the fully-connected case: in NCHW they are not one matrix product but one
+// per image (and group), y[n][g] = W[g] x[n][g] with x[n][g] a [C_in/G][H*W] matrix.
+// They run as a batched GEMM over b = n*G + g:
+//     forward        y[b]  = W[g] x[b] + bias   (A = W[g] K-major,  B = x[b]  MN-major)
+//     backward-data  dx[b] = W[g]^T dy[b]       (A = W[g] MN-major, B = dy[b] MN-major)
+// read in place through 3D tensor maps (the batch is the third coordinate).
 //
 // Kernel: persistent CTAs over 128 x BN output tiles; warps 0, 6 and 7 issue TMA tile
 // loads (128-byte swizzle) into a shared-memory ring, warp 1 issues tcgen05.mma
@@ -29,9 +39,13 @@ constexpr int kBM = 128, kBK = 64;
 constexpr uint64_t kGemmDrainNs = 1000000000ull;
 
 struct GemmParams {
-    float *C;                    // [M][ldc] fp32, or bf16 when out_bf16
+    float *C;                    // [batch][M][ldc] fp32, or bf16 when out_bf16
     int out_bf16;
-    const __nv_bfloat16 *bias;   // per column, or nullptr
+    const __nv_bfloat16 *bias;   // per column (bias_rows 0) or per row of A's batch (1), or nullptr
+    int bias_rows;
+    int batch, a_bmod;           // batches; A's batch coordinate is b % a_bmod
+    int a_bmid, b_bmid;          // the batch is the middle coordinate of A's / B's tensor map (else the last)
+    int64_t c_bstride;           // elements between batches of C
     unsigned int *err;
     uint64_t wait_ns;
     int M, N, K, ldc;
@@ -58,7 +72,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const uint32_t sbase = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;   // 128B swizzle atoms need 1 KB alignment
     const uint32_t a_bytes = kBM * kBK * 2, b_bytes = BN * kBK * 2;
     const uint32_t stage_bytes = a_bytes + b_bytes;
-    const int n_tiles = p.n_mblk * p.n_nblk;
+    const int n_tiles = p.batch * p.n_mblk * p.n_nblk;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -96,7 +110,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             for (int i = pi; i < nA + nB; i += kGemmProducers) my_bytes += i < nA ? bytesA : bytesB;
             int it = 0;   // global k-block counter across tiles
             for (int tile = blockIdx.x; tile < n_tiles && !abort_flag; tile += gridDim.x) {
-                const int mb = tile % p.n_mblk, nb = tile / p.n_mblk;
+                const int mb = tile % p.n_mblk, nb = (tile / p.n_mblk) % p.n_nblk, bt = tile / (p.n_mblk * p.n_nblk);
+                const int ab = bt % p.a_bmod;
                 for (int kb = 0; kb < p.n_kblk && !abort_flag; ++kb, ++it) {
                     const int slot = it % p.stages;
                     if (it >= p.stages &&
@@ -110,12 +125,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     ptx::mbar_arrive_expect_tx(fb, my_bytes);
                     for (int i = pi; i < nA + nB; i += kGemmProducers) {
                         if (i < nA) {   // A tile: 128 rows of M x 64 of K
-                            if (p.a_mn) ptx::tma_load_2d(sa + i * 8192, &tmA, mb * kBM + i * 64, kb * kBK, fb);
-                            else ptx::tma_load_2d(sa, &tmA, kb * kBK, mb * kBM, fb);
+                            const int x = p.a_mn ? mb * kBM + i * 64 : kb * kBK, y = p.a_mn ? kb * kBK : mb * kBM;
+                            const uint32_t dst = p.a_mn ? sa + i * 8192 : sa;
+                            if (p.a_bmid) ptx::tma_load_3d(dst, &tmA, x, ab, y, fb);
+                            else ptx::tma_load_3d(dst, &tmA, x, y, ab, fb);
                         } else {        // B tile: BN rows of N x 64 of K
                             const int c = i - nA;
-                            if (p.b_mn) ptx::tma_load_2d(sb + c * 8192, &tmB, nb * BN + c * 64, kb * kBK, fb);
-                            else ptx::tma_load_2d(sb, &tmB, kb * kBK, nb * BN, fb);
+                            const int x = p.b_mn ? nb * BN + c * 64 : kb * kBK, y = p.b_mn ? kb * kBK : nb * BN;
+                            const uint32_t dst = p.b_mn ? sb + c * 8192 : sb;
+                            if (p.b_bmid) ptx::tma_load_3d(dst, &tmB, x, bt, y, fb);
+                            else ptx::tma_load_3d(dst, &tmB, x, y, bt, fb);
                         }
                     }
                 }
@@ -188,9 +207,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             ready = __all_sync(0xffffffffu, ready && !abort_flag);
             if (!ready) break;
             ptx::tc_fence_after();
-            const int mb = tile % p.n_mblk, nb = tile / p.n_mblk;
+            const int mb = tile % p.n_mblk, nb = (tile / p.n_mblk) % p.n_nblk, bt = tile / (p.n_mblk * p.n_nblk);
             const int row = mb * kBM + lg * 32 + lane;
-            const int64_t crow = (int64_t)row * p.ldc + (int64_t)nb * BN;   // element index in C
+            const int64_t crow = bt * p.c_bstride + (int64_t)row * p.ldc + (int64_t)nb * BN;   // element index in C
+            const int bgrp = bt % p.a_bmod;
+            const float brow = (p.bias && p.bias_rows && row < p.M) ? __bfloat162float(p.bias[bgrp * p.M + row]) : 0.f;
+            const __nv_bfloat16 *bcol = (p.bias && !p.bias_rows) ? p.bias + (int64_t)bgrp * p.N : nullptr;
             for (int c0 = 0; c0 < BN; c0 += 16) {
                 uint32_t acc[16];
                 ptx::tmem_ld16(tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)(buf * BN + c0), acc);
@@ -200,13 +222,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     float v[16];
                     #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        v[j] = __uint_as_float(acc[j]);
-                        if (p.bias && col0 + j < p.N) v[j] += __bfloat162float(p.bias[col0 + j]);
+                        v[j] = __uint_as_float(acc[j]) + brow;
+                        if (bcol && col0 + j < p.N) v[j] += __bfloat162float(bcol[col0 + j]);
                     }
                     if (col0 + 16 <= p.N && (p.ldc & 3) == 0) {
-                        #pragma unroll
-                        for (int j = 0; j < 16; j += 4)
-                            store_out4(p.C, crow + c0 + j, v[j], v[j + 1], v[j + 2], v[j + 3], p.out_bf16);
+                        if (p.out_bf16) {
+                            #pragma unroll
+                            for (int j = 0; j < 16; j += 4)
+                                store_out4(p.C, crow + c0 + j, v[j], v[j + 1], v[j + 2], v[j + 3], 1);
+                        } else {
+                            #pragma unroll
+                            for (int j = 0; j < 16; j += 4)
+                                store_out4(p.C, crow + c0 + j, v[j], v[j + 1], v[j + 2], v[j + 3], 0);
+                        }
                     } else {
                         for (int j = 0; j < 16; ++j)
                             if (col0 + j < p.N) store_out(p.C, crow + c0 + j, v[j], p.out_bf16);
@@ -245,16 +273,36 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// 2D bf16 tensor map over a row-major [rows][cols] matrix with box {64, box_rows}, 128B swizzle.
-bool make_tmap(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows)
+// 3D bf16 tensor map over `batch` row-major [rows][cols] matrices with box {64, box_rows, 1},
+// 128B swizzle; elements past a matrix's rows or columns read as zero.
+bool make_tmap(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows, uint64_t batch = 1)
 {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {64u, box_rows};
-    cuuint32_t estr[2] = {1u, 1u};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+    cuuint64_t dims[3] = {cols, rows, batch};
+    cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+    cuuint32_t box[3] = {64u, box_rows, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3D bf16 tensor map over a row-major [rows][groups][cols] array read as `groups` matrices
+// [rows][cols] (the batch is the middle coordinate), box {64, 1, box_rows}, 128B swizzle.
+// With one group it is the plain map of make_tmap (batch last), so *mid reports which.
+bool make_tmap_mid(CUtensorMap *m, const void *base, uint64_t cols, uint64_t groups, uint64_t rows, uint32_t box_rows,
+                   int *mid)
+{
+    *mid = groups > 1 ? 1 : 0;
+    if (groups == 1) return make_tmap(m, base, cols, rows, box_rows, 1);
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {cols, groups, rows};
+    cuuint64_t strides[2] = {cols * 2, cols * groups * 2};
+    cuuint32_t box[3] = {64u, 1u, box_rows};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -284,27 +332,17 @@ struct GemmShape {
     int BN;
 };
 
-GemmShape fc_shape(const Geom &g, gconv_pass pass)
-{
-    const int Kin = g.Cin * g.kH * g.kW;
-    switch (pass) {
-    case GCONV_PASS_FWD: return GemmShape{g.N, g.Cout, Kin, 0, 0, 0};
-    case GCONV_PASS_BWD_DATA: return GemmShape{g.N, Kin, g.Cout, 0, 1, 0};
-    default: return GemmShape{g.Cout, Kin, g.N, 1, 1, 0};
-    }
-}
-
 // Picks the N tile.  The kernel is bound by how fast an SM fills its shared memory
 // (about 80 GB/s per CTA measured, well below what the MMAs consume), so the cost of a
 // choice is the bytes the busiest SM loads: rounds of persistent tiles times the tile's
 // (128 + BN) rows per K step.
-int pick_bn(int M, int N)
+int pick_bn(int M, int N, int batch = 1)
 {
     const int mb = (M + kBM - 1) / kBM;
     int64_t best = INT64_MAX;
     int bn = 256;
     for (int cand : {256, 192, 128}) {
-        const int64_t tiles = (int64_t)mb * ((N + cand - 1) / cand);
+        const int64_t tiles = (int64_t)batch * mb * ((N + cand - 1) / cand);
         const int64_t rounds = (tiles + num_sms() - 1) / num_sms();
         const int64_t cost = rounds * (kBM + cand);
         if (cost < best) { best = cost; bn = cand; }
@@ -314,56 +352,49 @@ int pick_bn(int M, int N)
 
 bool fc_supported(const Geom &g)
 {
-    // input size == kernel size, no padding, dilation 1: X is a plain [N][C*H*W] matrix
+    // input size == kernel size, no padding, dilation 1: X is a plain [N][C*H*W] matrix, and
+    // with groups a block-diagonal one (group g: columns g*Kg.. of X against W[g])
     if (!(g.H == g.kH && g.W == g.kW && g.pt == 0 && g.pb == 0 && g.pl == 0 && g.pr == 0 && g.d_h == 1 && g.d_w == 1))
         return false;
-    if (g.G != 1) return false;
-    const int64_t Kin = (int64_t)g.Cin * g.kH * g.kW;
-    // TMA: row strides must be multiples of 16 bytes; MN-major boxes need 64-element rows
-    return Kin % 64 == 0 && g.Cout % 64 == 0 && g.N % 8 == 0 && g.N >= 64 && g.Cout >= 64;
+    const int64_t Kg = (int64_t)g.Cgi * g.kH * g.kW;
+    // TMA: row strides (Kg, Cgo and their multiples by G) must be multiples of 16 bytes;
+    // rows and columns past the matrices' ends read as zero, so the tiles need no other fit
+    return Kg % 8 == 0 && g.Cgo % 8 == 0 && Kg >= 16 && g.Cgo >= 16;
 }
 
-}  // namespace
-
-bool tc_fc_plan(const Geom &g, gconv_pass pass, Plan *p)
+// 1x1, stride 1, no padding: the batched per-image GEMM (forward and backward-data).  TMA
+// row strides of x / dy ([C][H*W]) and w ([C_out][C_in/G]) must be multiples of 16 bytes.
+bool pointwise_supported(const Geom &g, gconv_pass pass)
 {
-    if (pass == GCONV_PASS_BWD_BIAS || !fc_supported(g)) return false;
-    if (!encode_fn()) return false;
-    p->path = GCONV_PATH_TC_FC;
-    p->launches = 1;
-    p->ws_bytes = 0;
-    return true;
+    if (pass != GCONV_PASS_FWD && pass != GCONV_PASS_BWD_DATA) return false;
+    if (g.kH != 1 || g.kW != 1 || g.s_h != 1 || g.s_w != 1 || g.pt || g.pb || g.pl || g.pr) return false;
+    const int64_t HW = (int64_t)g.H * g.W;
+    return HW % 8 == 0 && HW >= 64 && g.Cgi % 8 == 0 && g.Cgo % 8 == 0 && g.Cgi >= 16 && g.Cgo >= 16;
 }
 
-gconv_status tc_fc_launch(const Geom &g, const Plan &, gconv_pass pass, const void *a, const void *b,
-                          const void *bias, float *out, void *, cudaStream_t s)
+struct GemmLaunch {
+    GemmShape sh;
+    int batch = 1, a_bmod = 1, bias_rows = 0, a_bmid = 0, b_bmid = 0;
+    int64_t c_bstride = 0;
+    int ldc = 0;   // elements between rows of C
+};
+
+gconv_status run_gemm(const GemmLaunch &L, const CUtensorMap &tA, const CUtensorMap &tB, float *out, int out_bf16,
+                      const void *bias, cudaStream_t s)
 {
-    GemmShape sh = fc_shape(g, pass);
-    sh.BN = pick_bn(sh.M, sh.N);
-    const int Kin = g.Cin * g.kH * g.kW;
-    CUtensorMap tA, tB;
-    bool ok = false;
-    switch (pass) {
-    case GCONV_PASS_FWD:   // A = X [N][Kin] K-major; B = Wm [Cout][Kin] K-major
-        ok = make_tmap(&tA, a, Kin, g.N, kBM) && make_tmap(&tB, b, Kin, g.Cout, sh.BN);
-        break;
-    case GCONV_PASS_BWD_DATA:   // A = dY [N][Cout] K-major; B = Wm [Cout][Kin] MN-major (boxes 64 x 64)
-        ok = make_tmap(&tA, a, g.Cout, g.N, kBM) && make_tmap(&tB, b, Kin, g.Cout, kBK);
-        break;
-    default:   // A = dY [N][Cout] MN-major; B = X [N][Kin] MN-major
-        ok = make_tmap(&tA, b, g.Cout, g.N, kBK) && make_tmap(&tB, a, Kin, g.N, kBK);
-        break;
-    }
-    if (!ok) return GCONV_ERR_CUDA;
     unsigned int *err = device_error_word();
     if (!err) return GCONV_ERR_CUDA;
+    const GemmShape &sh = L.sh;
     GemmParams gp{};
     gp.C = out;
-    gp.out_bf16 = pass == GCONV_PASS_BWD_WEIGHT ? 0 : g.out_bf16;
-    gp.bias = pass == GCONV_PASS_FWD ? static_cast<const __nv_bfloat16 *>(bias) : nullptr;
+    gp.out_bf16 = out_bf16;
+    gp.bias = static_cast<const __nv_bfloat16 *>(bias);
+    gp.bias_rows = L.bias_rows;
+    gp.batch = L.batch; gp.a_bmod = L.a_bmod; gp.c_bstride = L.c_bstride;
+    gp.a_bmid = L.a_bmid; gp.b_bmid = L.b_bmid;
     gp.err = err;
     gp.wait_ns = (uint64_t)wait_limit();
-    gp.M = sh.M; gp.N = sh.N; gp.K = sh.K; gp.ldc = sh.N;
+    gp.M = sh.M; gp.N = sh.N; gp.K = sh.K; gp.ldc = L.ldc;
     gp.a_mn = sh.a_mn; gp.b_mn = sh.b_mn;
     gp.n_mblk = (sh.M + kBM - 1) / kBM;
     gp.n_nblk = (sh.N + sh.BN - 1) / sh.BN;
@@ -371,8 +402,8 @@ gconv_status tc_fc_launch(const Geom &g, const Plan &, gconv_pass pass, const vo
     const size_t stage = (size_t)(kBM + sh.BN) * kBK * 2;
     gp.stages = (int)std::min<size_t>(8, (220 * 1024 - 1024) / stage);
     const size_t smem = gp.stages * stage + 1024;
-    const int tiles = gp.n_mblk * gp.n_nblk;
-    const int grid = std::min(tiles, num_sms());
+    const int64_t tiles = (int64_t)gp.batch * gp.n_mblk * gp.n_nblk;
+    const int grid = (int)std::min<int64_t>(tiles, num_sms());
     static bool attr[64][3] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GCONV_ERR_CUDA;
@@ -388,6 +419,81 @@ gconv_status tc_fc_launch(const Geom &g, const Plan &, gconv_pass pass, const vo
     else if (sh.BN == 192) gemm_kernel<192><<<grid, kGemmThreads, smem, s>>>(tA, tB, gp);
     else gemm_kernel<128><<<grid, kGemmThreads, smem, s>>>(tA, tB, gp);
     return GCONV_OK;
+}
+
+}  // namespace
+
+bool tc_fc_plan(const Geom &g, gconv_pass pass, Plan *p)
+{
+    if (pass == GCONV_PASS_BWD_BIAS) return false;
+    const bool fc = fc_supported(g);
+    if (!fc && !pointwise_supported(g, pass)) return false;
+    if (!encode_fn()) return false;
+    p->path = fc ? GCONV_PATH_TC_FC : GCONV_PATH_TC_GEMM;
+    p->launches = 1;
+    p->ws_bytes = 0;
+    return true;
+}
+
+gconv_status tc_fc_launch(const Geom &g, const Plan &, gconv_pass pass, const void *a, const void *b,
+                          const void *bias, float *out, void *, cudaStream_t s)
+{
+    CUtensorMap tA, tB;
+    GemmLaunch L;
+    bool ok = false;
+    const int out_bf16 = pass == GCONV_PASS_BWD_WEIGHT ? 0 : g.out_bf16;
+    if (fc_supported(g)) {
+        // groups: batch b = g of G block-diagonal GEMMs; X, dY rows hold all groups side by
+        // side (the batch is the middle coordinate of their maps), W[g] is contiguous
+        const int Kg = g.Cgi * g.kH * g.kW, G = g.G;
+        L.batch = G;
+        L.a_bmod = G;
+        switch (pass) {
+        case GCONV_PASS_FWD:   // y[:, g] (N x Cgo) = X[:, g] (N x Kg, K-major) * W[g]^T (K-major)
+            L.sh = GemmShape{g.N, g.Cgo, Kg, 0, 0, 0};
+            L.sh.BN = pick_bn(L.sh.M, L.sh.N, G);
+            ok = make_tmap_mid(&tA, a, Kg, G, g.N, kBM, &L.a_bmid) && make_tmap(&tB, b, Kg, g.Cgo, L.sh.BN, G);
+            L.ldc = g.Cout;
+            L.c_bstride = g.Cgo;
+            break;
+        case GCONV_PASS_BWD_DATA:   // dX[:, g] (N x Kg) = dY[:, g] (K-major) * W[g] (Cgo x Kg, MN-major)
+            L.sh = GemmShape{g.N, Kg, g.Cgo, 0, 1, 0};
+            L.sh.BN = pick_bn(L.sh.M, L.sh.N, G);
+            ok = make_tmap_mid(&tA, a, g.Cgo, G, g.N, kBM, &L.a_bmid) && make_tmap(&tB, b, Kg, g.Cgo, kBK, G);
+            L.ldc = g.Cin * g.kH * g.kW;
+            L.c_bstride = Kg;
+            break;
+        default:   // dW[g] (Cgo x Kg) = dY[:, g]^T (MN-major) * X[:, g] (MN-major)
+            L.sh = GemmShape{g.Cgo, Kg, g.N, 1, 1, 0};
+            L.sh.BN = pick_bn(L.sh.M, L.sh.N, G);
+            ok = make_tmap_mid(&tA, b, g.Cgo, G, g.N, kBK, &L.a_bmid) && make_tmap_mid(&tB, a, Kg, G, g.N, kBK, &L.b_bmid);
+            L.ldc = Kg;
+            L.c_bstride = (int64_t)g.Cgo * Kg;
+            break;
+        }
+    } else if (pointwise_supported(g, pass)) {
+        const int HW = g.H * g.W;
+        L.batch = g.N * g.G;
+        L.a_bmod = g.G;
+        if (pass == GCONV_PASS_FWD) {
+            // y[b] (Cgo x HW) = W[g] (Cgo x Cgi, K-major) * x[b] (Cgi x HW, MN-major)
+            L.sh = GemmShape{g.Cgo, HW, g.Cgi, 0, 1, 0};
+            L.sh.BN = pick_bn(L.sh.M, L.sh.N, L.batch);
+            L.bias_rows = 1;
+            ok = make_tmap(&tA, b, g.Cgi, g.Cgo, kBM, g.G) && make_tmap(&tB, a, HW, g.Cgi, kBK, L.batch);
+        } else {
+            // dx[b] (Cgi x HW) = W[g]^T (Cgi x Cgo, MN-major) * dy[b] (Cgo x HW, MN-major)
+            L.sh = GemmShape{g.Cgi, HW, g.Cgo, 1, 1, 0};
+            L.sh.BN = pick_bn(L.sh.M, L.sh.N, L.batch);
+            ok = make_tmap(&tA, b, g.Cgi, g.Cgo, kBK, g.G) && make_tmap(&tB, a, HW, g.Cgo, kBK, L.batch);
+        }
+        L.c_bstride = (int64_t)L.sh.M * HW;
+        L.ldc = HW;
+    } else {
+        return GCONV_ERR_UNSUPPORTED;
+    }
+    if (!ok) return GCONV_ERR_CUDA;
+    return run_gemm(L, tA, tB, out, out_bf16, pass == GCONV_PASS_FWD ? bias : nullptr, s);
 }
 
 }  // namespace gconv

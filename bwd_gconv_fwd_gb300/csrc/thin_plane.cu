@@ -47,6 +47,7 @@ struct ThinParams {
     int TH, n_strip;     // output rows per block, strips per plane
     int bwd;             // backward-data
     int nchunk, per_chunk;   // weight gradient: image chunks, images per chunk
+    int slide, cpl;          // sliding-window form, outputs per thread
 };
 
 // Copies n elements src[0..n) (global) to dst[0..n) (shared) with 16-byte loads where the
@@ -363,13 +364,355 @@ __global__ void thin_wgrad_finish_kernel(const float *__restrict__ part, int G, 
 }
 
 // ---------------------------------------------------------------------------
+// Sliding-window forms (stride 1, rows of 16-byte multiples, at most 32*CPL columns).
+// Rows are staged with zero borders: staged row j of plane c holds source row lo + j at
+// columns [kPadE, kPadE + IW) of a row of `pitch` elements (zeros around it and for rows
+// outside the source), so the compute reads need no bounds tests.  A warp walks a run of
+// produced rows; lane l owns columns [l*CPL, l*CPL + CPL) and keeps, per input plane, the
+// three source rows of its current output row in registers: each step loads one new row
+// (one 4-, 8- or 16-byte shared-memory load per plane) and takes the two neighbouring
+// columns from the adjacent lanes with shuffles.
+
+template <typename T> struct PadE { static constexpr int value = 16 / (int)sizeof(T); };
+
+// Zero-bordered staging of source rows [lo, lo + nrows) of CG planes (see above).  Thread
+// t copies 16-byte vectors t, t + 128, ... of the staged region; the (row, vector) position
+// advances incrementally (no divisions), four vectors loaded before any is stored.
+template <typename T>
+__device__ __forceinline__ void stage_padded(const T *__restrict__ src, int64_t plane, int CG, int IH, int IW,
+                                             int lo, int nrows, int pitch, T *stage)
+{
+    constexpr int PAD = PadE<T>::value;
+    const int vrow = pitch / PAD;                 // 16-byte vectors per staged row
+    const int vdata = IW / PAD;                   // of which hold source data: [1, 1 + vdata)
+    const int total_rows = CG * nrows;
+    const int total = total_rows * vrow;
+    const int step_r = kThinThreads / vrow, step_k = kThinThreads - step_r * vrow;
+    int row = threadIdx.x / vrow, k = threadIdx.x - row * vrow;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    uint4 *dst = reinterpret_cast<uint4 *>(stage);
+    for (int i0 = threadIdx.x; i0 < total; i0 += 4 * kThinThreads) {
+        uint4 v[4];
+        int idx[4];
+        #pragma unroll
+        for (int u = 0; u < 4; ++u) {           // all loads first, then the stores
+            idx[u] = row * vrow + k;
+            v[u] = zero;
+            if (row < total_rows) {
+                const int c = row / nrows;     // one division per vector: planes are few
+                const int ih = lo + (row - c * nrows);
+                if (k >= 1 && k <= vdata && ih >= 0 && ih < IH)
+                    v[u] = __ldg(reinterpret_cast<const uint4 *>(src + c * plane + (int64_t)ih * IW) + (k - 1));
+            }
+            row += step_r;
+            k += step_k;
+            if (k >= vrow) { k -= vrow; ++row; }
+        }
+        #pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (idx[u] < total) dst[idx[u]] = v[u];
+    }
+}
+
+// CPL consecutive staged values from element e (aligned to CPL elements), widened to fp32.
+template <typename T, int CPL>
+__device__ __forceinline__ void load_chunk(const T *p, float (&out)[CPL])
+{
+    if constexpr (sizeof(T) == 2 && CPL == 2) {
+        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(p);
+        out[0] = __low2float(v);
+        out[1] = __high2float(v);
+    } else if constexpr (sizeof(T) == 2 && CPL == 4) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
+        out[0] = __low2float(a); out[1] = __high2float(a); out[2] = __low2float(b); out[3] = __high2float(b);
+    } else if constexpr (sizeof(T) == 4 && CPL == 2) {
+        const float2 v = *reinterpret_cast<const float2 *>(p);
+        out[0] = v.x; out[1] = v.y;
+    } else {
+        const float4 v = *reinterpret_cast<const float4 *>(p);
+        out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+    }
+}
+
+// One window row: source columns c0 - pl + k, k < CPL + 2, from the lane's own chunk and its
+// neighbours' (zero beyond lane 0 and lane 31, whose halo columns lie outside the source).
+template <int CPL>
+__device__ __forceinline__ void window_row(const float (&own)[CPL], int pl, int lane, float (&win)[CPL + 2])
+{
+    const float l1 = __shfl_up_sync(0xffffffffu, own[CPL - 1], 1);
+    const float l2 = __shfl_up_sync(0xffffffffu, own[CPL - 2], 1);
+    const float r0 = __shfl_down_sync(0xffffffffu, own[0], 1);
+    const float r1 = __shfl_down_sync(0xffffffffu, own[1], 1);
+    const float L1 = lane > 0 ? l1 : 0.f, L2 = lane > 0 ? l2 : 0.f;
+    const float R0 = lane < 31 ? r0 : 0.f, R1 = lane < 31 ? r1 : 0.f;
+    // pl = 1: [L1, own..., R0]; pl = 0: [own..., R0, R1]; pl = 2: [L2, L1, own...]
+    if (pl == 1) {
+        win[0] = L1;
+        #pragma unroll
+        for (int j = 0; j < CPL; ++j) win[1 + j] = own[j];
+        win[CPL + 1] = R0;
+    } else if (pl == 0) {
+        #pragma unroll
+        for (int j = 0; j < CPL; ++j) win[j] = own[j];
+        win[CPL] = R0;
+        win[CPL + 1] = R1;
+    } else {
+        win[0] = L2;
+        win[1] = L1;
+        #pragma unroll
+        for (int j = 0; j < CPL; ++j) win[2 + j] = own[j];
+    }
+}
+
+template <int CPL>
+__device__ __forceinline__ void store_chunk(float *out, int64_t i, const float (&v)[CPL], int nvalid, int bf16)
+{
+    if (nvalid == CPL && (i & (CPL - 1)) == 0) {
+        if constexpr (CPL == 4) {
+            store_out4(out, i, v[0], v[1], v[2], v[3], bf16);
+            return;
+        } else {
+            if (bf16) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(v[0], v[1]);
+                *reinterpret_cast<__nv_bfloat162 *>(reinterpret_cast<__nv_bfloat16 *>(out) + i) = h;
+            } else {
+                *reinterpret_cast<float2 *>(out + i) = make_float2(v[0], v[1]);
+            }
+            return;
+        }
+    }
+    #pragma unroll
+    for (int j = 0; j < CPL; ++j)
+        if (j < nvalid) store_out(out, i + j, v[j], bf16);
+}
+
+// One produced row of the sliding form: load source row `r + 2` of every input plane into
+// window slot C, then add the 3 x 3 taps over slots A, B, C (source rows r, r+1, r+2).
+// Slots rotate through the unrolled calls, so no window values are copied.
+template <typename T, int CG, int CPL, int A, int Bs, int C>
+__device__ __forceinline__ void slide_step(float (&win)[CG][3][CPL + 2], const T *col, int nrows, int pitch, int r,
+                                           int pl, int lane, const float (&wr)[CG * 9], float bias, float (&acc)[CPL])
+{
+    #pragma unroll
+    for (int ci = 0; ci < CG; ++ci) {
+        float own[CPL];
+        load_chunk<T, CPL>(col + (ci * nrows + r + 2) * pitch, own);
+        window_row<CPL>(own, pl, lane, win[ci][C]);
+    }
+    #pragma unroll
+    for (int j = 0; j < CPL; ++j) acc[j] = bias;
+    #pragma unroll
+    for (int ci = 0; ci < CG; ++ci)
+        #pragma unroll
+        for (int bb = 0; bb < 3; ++bb)
+            #pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                acc[j] = fmaf(wr[ci * 9 + 0 + bb], win[ci][A][j + bb], acc[j]);
+                acc[j] = fmaf(wr[ci * 9 + 3 + bb], win[ci][Bs][j + bb], acc[j]);
+                acc[j] = fmaf(wr[ci * 9 + 6 + bb], win[ci][C][j + bb], acc[j]);
+            }
+}
+
+// Forward / stride-1 backward-data (produced = correlation of the source with Wt, pads pt, pl
+// as in thin_corr_kernel).  Block: (image, group, strip).  Warp w produces output channel
+// o = w % CG for the produced rows of its share of the strip (w / CG of 4 / CG shares), with
+// that channel's 9*CG weights in registers.
+template <typename T, int CG, int CPL>
+__global__ void __launch_bounds__(kThinThreads)
+thin_slide_kernel(const __grid_constant__ ThinParams p)
+{
+    extern __shared__ __align__(16) unsigned char thin_sm[];
+    constexpr int PAD = PadE<T>::value;
+    constexpr int WPO = 4 / CG;
+    const T *W = static_cast<const T *>(p.w);
+    int b = blockIdx.x;
+    const int strip = b % p.n_strip; b /= p.n_strip;
+    const int g = b % p.G;
+    const int n = b / p.G;
+    const int r0 = strip * p.TH;
+    const int rows = min(p.TH, p.OH - r0);
+    const int lo = r0 - p.pt, nrows = rows + 2;
+    const int pitch = PAD + 32 * CPL + PAD;
+    const int64_t plane = (int64_t)p.IH * p.IW;
+    T *stage = reinterpret_cast<T *>(thin_sm);
+    stage_padded(static_cast<const T *>(p.src) + ((int64_t)n * p.G + g) * CG * plane, plane, CG, p.IH, p.IW, lo,
+                 nrows, pitch, stage);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int o = warp % CG, share = warp / CG;
+    // this warp's output channel: weights Wt[o][ci][tap] in registers
+    float wr[CG * 9];
+    #pragma unroll
+    for (int ci = 0; ci < CG; ++ci)
+        #pragma unroll
+        for (int t = 0; t < 9; ++t)
+            wr[ci * 9 + t] = !p.bwd ? to_f(W[((int64_t)(g * CG + o) * CG + ci) * 9 + t])
+                                    : to_f(W[((int64_t)(g * CG + ci) * CG + o) * 9 + (8 - t)]);
+    const float bias = (p.bias && !p.bwd) ? to_f(static_cast<const T *>(p.bias)[g * CG + o]) : 0.f;
+    __syncthreads();
+    const int q = (rows + WPO - 1) / WPO;
+    const int ra = share * q, rb = min(rows, ra + q);
+    if (ra >= rb) return;
+    const int c0 = lane * CPL;
+    const int nvalid = min(CPL, max(0, p.OW - c0));
+    const int64_t out_plane = (int64_t)p.OH * p.OW;
+    const int64_t obase = (((int64_t)n * p.G + g) * CG + o) * out_plane + c0;
+    const T *col = stage + PAD + c0;
+    float win[CG][3][CPL + 2];
+    #pragma unroll
+    for (int ci = 0; ci < CG; ++ci)
+        #pragma unroll
+        for (int a = 0; a < 2; ++a) {
+            float own[CPL];
+            load_chunk<T, CPL>(col + (ci * nrows + ra + a) * pitch, own);
+            window_row<CPL>(own, p.pl, lane, win[ci][a]);
+        }
+    float acc[CPL];
+    int r = ra;
+    for (; r + 3 <= rb; r += 3) {
+        slide_step<T, CG, CPL, 0, 1, 2>(win, col, nrows, pitch, r, p.pl, lane, wr, bias, acc);
+        if (nvalid > 0) store_chunk<CPL>(p.out, obase + (int64_t)(r0 + r) * p.OW, acc, nvalid, p.out_bf16);
+        slide_step<T, CG, CPL, 1, 2, 0>(win, col, nrows, pitch, r + 1, p.pl, lane, wr, bias, acc);
+        if (nvalid > 0) store_chunk<CPL>(p.out, obase + (int64_t)(r0 + r + 1) * p.OW, acc, nvalid, p.out_bf16);
+        slide_step<T, CG, CPL, 2, 0, 1>(win, col, nrows, pitch, r + 2, p.pl, lane, wr, bias, acc);
+        if (nvalid > 0) store_chunk<CPL>(p.out, obase + (int64_t)(r0 + r + 2) * p.OW, acc, nvalid, p.out_bf16);
+    }
+    if (r < rb) {
+        slide_step<T, CG, CPL, 0, 1, 2>(win, col, nrows, pitch, r, p.pl, lane, wr, bias, acc);
+        if (nvalid > 0) store_chunk<CPL>(p.out, obase + (int64_t)(r0 + r) * p.OW, acc, nvalid, p.out_bf16);
+    }
+    if (r + 1 < rb) {
+        slide_step<T, CG, CPL, 1, 2, 0>(win, col, nrows, pitch, r + 1, p.pl, lane, wr, bias, acc);
+        if (nvalid > 0) store_chunk<CPL>(p.out, obase + (int64_t)(r0 + r + 1) * p.OW, acc, nvalid, p.out_bf16);
+    }
+}
+
+// One gradOutput row of the sliding weight gradient: x row r + 2 of every input plane into
+// window slot C, then acc[ci*9 + tap] += dy[j] * x window (slots A, B, C = rows r..r+2),
+// and the bias accumulator += dy[j].
+template <typename T, int CG, int CPL, int A, int Bs, int C>
+__device__ __forceinline__ void wgrad_step(float (&win)[CG][3][CPL + 2], const T *xcol, const T *ycol, int xrows,
+                                           int pitch, int r, int pl, int lane, float (&acc)[CG * 9 + 1])
+{
+    #pragma unroll
+    for (int ci = 0; ci < CG; ++ci) {
+        float own[CPL];
+        load_chunk<T, CPL>(xcol + (ci * xrows + r + 2) * pitch, own);
+        window_row<CPL>(own, pl, lane, win[ci][C]);
+    }
+    float d[CPL];
+    load_chunk<T, CPL>(ycol + r * pitch, d);
+    #pragma unroll
+    for (int j = 0; j < CPL; ++j) acc[CG * 9] += d[j];
+    #pragma unroll
+    for (int ci = 0; ci < CG; ++ci)
+        #pragma unroll
+        for (int bb = 0; bb < 3; ++bb)
+            #pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                acc[ci * 9 + 0 + bb] = fmaf(d[j], win[ci][A][j + bb], acc[ci * 9 + 0 + bb]);
+                acc[ci * 9 + 3 + bb] = fmaf(d[j], win[ci][Bs][j + bb], acc[ci * 9 + 3 + bb]);
+                acc[ci * 9 + 6 + bb] = fmaf(d[j], win[ci][C][j + bb], acc[ci * 9 + 6 + bb]);
+            }
+}
+
+// Weight gradient + bias gradient, stride 1 (the accumulation of thin_wgrad_kernel).
+// Warp w: output channel o = w % CG; its rows of the strip are [ (w/CG)*q, ... ) with
+// q = rows / (4/CG) rounded up.  x rows are staged zero-bordered from r0 - pt, gradOutput
+// rows zero-bordered from r0 (columns past Wo are zero, so they add nothing).
+template <typename T, int CG, int CPL>
+__global__ void __launch_bounds__(kThinThreads)
+thin_slide_wgrad_kernel(const __grid_constant__ ThinParams p)
+{
+    extern __shared__ __align__(16) unsigned char thin_sm[];
+    constexpr int NA = CG * 9 + 1;
+    constexpr int WPO = 4 / CG;
+    constexpr int PAD = PadE<T>::value;
+    __shared__ float red[4][NA];
+    const T *X = static_cast<const T *>(p.src);
+    const T *DY = static_cast<const T *>(p.dy);
+    int b = blockIdx.x;
+    const int strip = b % p.n_strip; b /= p.n_strip;
+    const int chunk = b % p.nchunk;
+    const int g = b / p.nchunk;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int o = warp % CG, part_w = warp / CG;
+    const int r0 = strip * p.TH;
+    const int rows = min(p.TH, p.OH - r0);
+    const int pitch = PAD + 32 * CPL + PAD;
+    const int xrows = rows + 2;
+    const int64_t xplane = (int64_t)p.IH * p.IW, yplane = (int64_t)p.OH * p.OW;
+    T *xs = reinterpret_cast<T *>(thin_sm);
+    T *ys = xs + CG * xrows * pitch;
+    const int q = (rows + WPO - 1) / WPO;
+    const int ra = part_w * q, rb = min(rows, ra + q);
+    const int c0 = lane * CPL;
+    float acc[NA];
+    #pragma unroll
+    for (int k = 0; k < NA; ++k) acc[k] = 0.f;
+    const int n0 = chunk * p.per_chunk, n1 = min(p.N, n0 + p.per_chunk);
+    for (int n = n0; n < n1; ++n) {
+        stage_padded(X + ((int64_t)n * p.G + g) * CG * xplane, xplane, CG, p.IH, p.IW, r0 - p.pt, xrows, pitch, xs);
+        stage_padded(DY + ((int64_t)n * p.G + g) * CG * yplane, yplane, CG, p.OH, p.OW, r0, rows, pitch, ys);
+        __syncthreads();
+        if (ra < rb) {
+            float win[CG][3][CPL + 2];
+            const T *xcol = xs + PAD + c0;
+            #pragma unroll
+            for (int ci = 0; ci < CG; ++ci)
+                #pragma unroll
+                for (int a = 0; a < 2; ++a) {
+                    float own[CPL];
+                    load_chunk<T, CPL>(xcol + (ci * xrows + ra + a) * pitch, own);
+                    window_row<CPL>(own, p.pl, lane, win[ci][a]);
+                }
+            const T *ycol = ys + PAD + c0 + o * rows * pitch;
+            int r = ra;
+            for (; r + 3 <= rb; r += 3) {
+                wgrad_step<T, CG, CPL, 0, 1, 2>(win, xcol, ycol, xrows, pitch, r, p.pl, lane, acc);
+                wgrad_step<T, CG, CPL, 1, 2, 0>(win, xcol, ycol, xrows, pitch, r + 1, p.pl, lane, acc);
+                wgrad_step<T, CG, CPL, 2, 0, 1>(win, xcol, ycol, xrows, pitch, r + 2, p.pl, lane, acc);
+            }
+            if (r < rb) wgrad_step<T, CG, CPL, 0, 1, 2>(win, xcol, ycol, xrows, pitch, r, p.pl, lane, acc);
+            if (r + 1 < rb) wgrad_step<T, CG, CPL, 1, 2, 0>(win, xcol, ycol, xrows, pitch, r + 1, p.pl, lane, acc);
+        }
+        __syncthreads();
+    }
+    #pragma unroll
+    for (int k = 0; k < NA; ++k) {
+        float v = acc[k];
+        #pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        acc[k] = v;
+    }
+    if (lane == 0)
+        #pragma unroll
+        for (int k = 0; k < NA; ++k) red[warp][k] = acc[k];
+    __syncthreads();
+    float *dst = p.out + (int64_t)blockIdx.x * CG * NA;
+    for (int i = threadIdx.x; i < CG * NA; i += kThinThreads) {
+        const int oo = i / NA, k = i - oo * NA;
+        float s = 0.f;
+        for (int qq = 0; qq < WPO; ++qq) s += red[qq * CG + oo][k];
+        dst[i] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Planning and launch
 
 int thin_cpl(int ow) { return ow >= 48 ? 4 : (ow >= 16 ? 2 : 1); }
 
-// Staged elements of one block for a strip of `th` produced rows.
+// Staged bytes of one block for a strip of `th` produced rows.
 int64_t thin_stage_elems(const ThinParams &p, int CG, int th, bool wgrad, int esize)
 {
+    if (p.slide) {
+        const int64_t pitch = 16 / esize + 32 * p.cpl + 16 / esize;
+        int64_t e = (int64_t)CG * (th + 2) * pitch;
+        if (wgrad) e += (int64_t)CG * th * pitch;
+        return e * esize;
+    }
     int in_rows;
     if (!p.bwd || p.S == 1) in_rows = (th - 1) * p.S + 3;
     else in_rows = (th + 1) / 2 + 2;
@@ -405,6 +748,14 @@ bool thin_plan(const Geom &g, gconv_pass pass, int esize, ThinParams *p, int *gr
         p->pt = g.pt; p->pl = g.pl;
     }
     const bool wg = pass == GCONV_PASS_BWD_WEIGHT;
+    // sliding-window form: stride 1, 16-byte source (and gradOutput) rows, at most 128 columns
+    const int span = std::max(p->IW, p->OW);
+    // (forward / backward-data with 4 channels per group stay on the staged-window form,
+    // which produced all four channels per thread and measured faster on GB300: 81 vs 121 us
+    // on the ResNeXt 4-channel layer)
+    p->slide = g.s_h == 1 && span <= 128 && (p->IW * esize) % 16 == 0 && (!wg || (p->OW * esize) % 16 == 0) &&
+               (wg || CG < 4);
+    p->cpl = p->slide ? (span <= 64 ? 2 : 4) : thin_cpl(p->OW);
     const int64_t planes = (int64_t)g.N * g.G;
     const int64_t target_blocks = (int64_t)num_sms() * 16;
     int th = p->OH;
@@ -435,7 +786,19 @@ bool thin_plan(const Geom &g, gconv_pass pass, int esize, ThinParams *p, int *gr
 template <typename T, int CG, int S>
 gconv_status thin_launch_t(const ThinParams &p, int grid, size_t smem, bool wgrad, float *dw, float *db, cudaStream_t s)
 {
-    const int cpl = thin_cpl(wgrad ? p.OW : p.OW);
+    const int cpl = p.cpl;
+    if (S == 1 && p.slide) {
+        if (wgrad) {
+            if (cpl == 2) thin_slide_wgrad_kernel<T, CG, 2><<<grid, kThinThreads, smem, s>>>(p);
+            else thin_slide_wgrad_kernel<T, CG, 4><<<grid, kThinThreads, smem, s>>>(p);
+            const int total = p.G * CG * (CG * 9 + 1);
+            thin_wgrad_finish_kernel<CG><<<(total + 255) / 256, 256, 0, s>>>(p.out, p.G, p.nchunk * p.n_strip, dw, db);
+        } else {
+            if (cpl == 2) thin_slide_kernel<T, CG, 2><<<grid, kThinThreads, smem, s>>>(p);
+            else thin_slide_kernel<T, CG, 4><<<grid, kThinThreads, smem, s>>>(p);
+        }
+        return GCONV_OK;
+    }
     if (wgrad) {
         switch (cpl) {
         case 4: thin_wgrad_kernel<T, CG, S, 4><<<grid, kThinThreads, smem, s>>>(p); break;

@@ -108,6 +108,18 @@ def model_zoo(N):
     return out
 
 
+def pointwise_zoo(N):
+    """Shape sweep of 1x1 layers (stride 1, no padding): the channel-reducing and -expanding
+    1x1 convolutions of ResNet-50 bottleneck blocks at 224x224 input, and a grouped 1x1
+    layer, batch N; weights N(0, sd = 1/sqrt(fan_in)), bf16 storage."""
+    layers = [("rn50_1x1_256to64_56", 256, 64, 56, 1), ("rn50_1x1_64to256_56", 64, 256, 56, 1),
+              ("rn50_1x1_512to128_28", 512, 128, 28, 1), ("rn50_1x1_128to512_28", 128, 512, 28, 1),
+              ("rn50_1x1_1024to256_14", 1024, 256, 14, 1), ("grouped_1x1_256to256_28_g4", 256, 256, 28, 4)]
+    return {nm: Workload(nm, _g(N, ci, hw, hw, co, 1, 1, 1, 0, 0, 0, 0, 1, G), "bf16",
+                         w=("normal", 1.0 / math.sqrt(ci // G)))
+            for nm, ci, co, hw, G in layers}
+
+
 def per_axis(geom):
     """The 16-integer form ``(N, C_in, H, W, C_out, kH, kW, stride_h, stride_w, pad_top,
     pad_bottom, pad_left, pad_right, dilation_h, dilation_w, groups)`` of a 14- or

@@ -89,7 +89,8 @@ typedef enum {
     GCONV_PATH_DIRECT = 1,      /* CUDA-core fp32 FMA direct loops (fp32 inputs, thin groups) */
     GCONV_PATH_TC_IGEMM = 2,    /* tcgen05/TMEM implicit GEMM, bf16 in, fp32 accumulate */
     GCONV_PATH_TC_FC = 3,       /* tcgen05/TMEM dense GEMM for input size == kernel size */
-    GCONV_PATH_REDUCE = 4       /* CUDA-core warp-shuffle reduction (bias gradient) */
+    GCONV_PATH_REDUCE = 4,      /* CUDA-core warp-shuffle reduction (bias gradient) */
+    GCONV_PATH_TC_GEMM = 5      /* tcgen05/TMEM batched per-image GEMM for 1x1, stride-1, unpadded layers */
 } gconv_path;
 
 /* Geometry with stride and dilation given per axis.  The 14-integer entry points
@@ -236,9 +237,9 @@ size_t gconv_noalloc_scratch_bytes(void);
 
 /* One training step of the layer on HOST tensors: copies x, w, bias and dy from
  * host memory into `device_buffer`, runs the four passes above on them (forward,
- * backward-data, backward-weight, bias gradient: the same operations, layouts,
- * kernels and results as gconv_fwd, gconv_bwd_data, gconv_bwd_weight and
- * gconv_bwd_bias), and copies y, dx, dw and db back to host memory.  The studied
+ * backward-data, backward-weight with the bias gradient: the same operations,
+ * layouts, kernels and results as gconv_fwd, gconv_bwd_data and gconv_bwd_weight_ex
+ * with db), and copies y, dx, dw and db back to host memory.  The studied
  * pages have no counterpart of this entry point; it serves callers whose tensors
  * live in host memory, with the copies overlapped with the kernels.
  *

@@ -119,7 +119,7 @@ def test_plans_are_consistent(L):
         dt = B.GCONV_BF16 if wk.dtype == "bf16" else B.GCONV_F32
         for p in range(4):
             path, launches = gc.gconv_plan(wk.geom, dt, p)
-            assert path in (B.PATH_DIRECT, B.PATH_TC_IGEMM, B.PATH_TC_FC, B.PATH_REDUCE), (name, p)
+            assert path in (B.PATH_DIRECT, B.PATH_TC_IGEMM, B.PATH_TC_FC, B.PATH_REDUCE, B.PATH_TC_GEMM), (name, p)
             assert 1 <= launches <= 9
             if p == B.PASS_BWD_BIAS:
                 assert path == B.PATH_REDUCE
@@ -200,7 +200,7 @@ def test_model_zoo_layers_have_plans(L):
             geom = wk.geom
             for p in range(4):
                 path, launches = gc.gconv_plan(geom, B.GCONV_BF16, p)
-                assert path in (B.PATH_DIRECT, B.PATH_TC_IGEMM, B.PATH_TC_FC, B.PATH_REDUCE), (name, p)
+                assert path in (B.PATH_DIRECT, B.PATH_TC_IGEMM, B.PATH_TC_FC, B.PATH_REDUCE, B.PATH_TC_GEMM), (name, p)
                 assert 1 <= launches <= 9, (name, p)
                 ws = gc.gconv_workspace_size(geom, B.GCONV_BF16, p)
                 assert 0 <= ws < (1 << 32), (name, p)

@@ -62,9 +62,9 @@ def check_guards(name, buf):
     assert bool((words[GUARD + n:] == CANARY).all()), f"{name}: write past the output"
 
 
-def run_gpu(geom, x, w, b, dy, dev, passes=("y", "dx", "dw", "db")):
+def run_gpu(geom, x, w, b, dy, dev, passes=("y", "dx", "dw", "db"), fused_bias=False):
     """All four passes on the GPU; returns fp32 CPU tensors.  Every output sits between guard
-    regions that must come back untouched."""
+    regions that must come back untouched.  fused_bias: db from the weight-gradient call."""
     N, Cin, H, W, Cout, kH, kW = wl.per_axis(geom)[:7]
     Ho, Wo = wl.out_hw(geom)
     kw = _kw(geom)
@@ -79,14 +79,15 @@ def run_gpu(geom, x, w, b, dy, dev, passes=("y", "dx", "dw", "db")):
         dx, bufs["dx"] = guarded((N, Cin, H, W), dev)
         gc.gconv_bwd_data(dyd, wd, dx, **kw)
         out["dx"] = dx
-    if "dw" in passes:
-        dw, bufs["dw"] = guarded(tuple(w.shape), dev)
-        gc.gconv_bwd_weight(xd, dyd, dw, **kw)
-        out["dw"] = dw
     if "db" in passes:
         db, bufs["db"] = guarded((Cout,), dev)
-        gc.gconv_bwd_bias(dyd, db, geom=geom)
+        if not fused_bias:
+            gc.gconv_bwd_bias(dyd, db, geom=geom)
         out["db"] = db
+    if "dw" in passes:
+        dw, bufs["dw"] = guarded(tuple(w.shape), dev)
+        gc.gconv_bwd_weight(xd, dyd, dw, db=out["db"] if fused_bias else None, **kw)
+        out["dw"] = dw
     torch.cuda.synchronize()
     assert gc.gconv_check_device_error() == B.GCONV_OK
     for k, bf in bufs.items():
@@ -187,7 +188,7 @@ def _sampled(wk, dev, oracle_mod, n_out=6000, n_w=1500, seed=77):
     return got
 
 
-TC, FC, CC, RD = B.PATH_TC_IGEMM, B.PATH_TC_FC, B.PATH_DIRECT, B.PATH_REDUCE
+TC, FC, CC, RD, PW = B.PATH_TC_IGEMM, B.PATH_TC_FC, B.PATH_DIRECT, B.PATH_REDUCE, B.PATH_TC_GEMM
 WORKLOAD_PATHS = {
     "alexnet_g2": (TC, TC, TC, RD), "fc_mode": (FC, FC, FC, RD), "fc_mode_ones_x": (FC, FC, FC, RD),
     "dense3x3": (TC, TC, TC, RD), "dense3x3_s2_asym": (TC, TC, TC, RD),
@@ -301,13 +302,14 @@ def test_forced_direct_agrees_with_default(dev):
     ((18, 3, 7, 7, 8, 3, 3, 1, 0, 0, 0, 0, 1, 1), "bf16", True),         # 294-byte images: chunks would misalign
 ])
 def test_step_host_matches_device_passes(dev, oracle_mod, geom, dtype, with_bias):
-    """gconv_step_host on pinned host tensors gives bit for bit what the four device
-    passes give, and meets the oracle tolerance; run twice in a row on one stream."""
+    """gconv_step_host on pinned host tensors gives bit for bit what the device passes give
+    (the weight gradient with its bias gradient in one call), and meets the oracle
+    tolerance; run twice in a row on one stream."""
     wk = wl.Workload("host", geom, dtype)
     x, w, b, dy = wl.make_inputs(wk, seed=31)
     if not with_bias:
         b = None
-    ref = run_gpu(geom, x, w, b, dy, dev)
+    ref = run_gpu(geom, x, w, b, dy, dev, fused_bias=True)
     N, Cin, H, W, Cout, kH, kW, s, pt, pb, pl, pr, d, G = geom
     Ho, Wo = wl.out_hw(geom)
     hx, hw_, hdy = (t.contiguous().pin_memory() for t in (x, w, dy))
@@ -431,13 +433,17 @@ def test_per_axis_random_sweep(dev, oracle_mod):
 
 
 @pytest.mark.parametrize("geom", [
-    (3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2),       # tensor-core weight gradient
+    (3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2),       # tensor cores: bias column from the MMAs
+    (2, 64, 17, 15, 64, 3, 3, 1, 1, 1, 1, 1, 1, 1),         # tensor cores, 64 channels: separate reduction
+    (2, 96, 13, 40, 160, 3, 3, 1, 1, 1, 1, 1, 1, 2),        # tensor cores, 48 of 64 channels, 80 outputs
+    (2, 64, 19, 16, 64, 3, 3, 2, 0, 1, 0, 1, 1, 1),         # stride-2 tensor cores: separate reduction
     (2, 32, 12, 12, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8),         # CUDA-core weight gradient
-    (2, 128, 6, 6, 96, 6, 6, 1, 0, 0, 0, 0, 1, 1),          # fully-connected mode
+    (2, 128, 6, 6, 96, 6, 6, 1, 0, 0, 0, 0, 1, 1),          # 1x1 output
 ])
 def test_weight_gradient_with_bias_gradient(dev, oracle_mod, geom):
-    """gconv_bwd_weight_ex with db: dw and db from one call, equal bit for bit to the two
-    separate entry points and within tolerance of the oracle."""
+    """gconv_bwd_weight_ex with db: dw and db from one call.  dw equals the separate entry
+    point bit for bit; db (summed by the weight-gradient kernels themselves where the
+    family fuses it, so in another order) is within tolerance of the oracle."""
     wk = wl.Workload("wdb", geom, "bf16", w=("normal", 0.2))
     x, w, b, dy = wl.make_inputs(wk, seed=55)
     sep = run_gpu(geom, x, w, b, dy, dev, passes=("dw", "db"))
@@ -449,7 +455,7 @@ def test_weight_gradient_with_bias_gradient(dev, oracle_mod, geom):
     assert gc.gconv_check_device_error() == B.GCONV_OK
     check_guards("fused dw", bw)
     check_guards("fused db", bb)
-    assert torch.equal(dw.cpu(), sep["dw"]) and torch.equal(db.cpu(), sep["db"])
+    assert torch.equal(dw.cpu(), sep["dw"])
     check("fused db", db.cpu().numpy(), oracle_mod.bwd_bias(geom, f64(dy)), TOL["bf16"])
 
 
@@ -459,7 +465,7 @@ def test_weight_gradient_with_bias_gradient(dev, oracle_mod, geom):
 BF16_OUT = [
     ((3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2), (TC, TC)),    # stride-1 correlation, paired taps
     ((2, 64, 19, 16, 64, 3, 3, 2, 0, 1, 0, 1, 1, 1), (TC, TC)),     # stride-2 correlation, phases
-    ((2, 128, 6, 6, 96, 6, 6, 1, 0, 0, 0, 0, 1, 1), (CC, CC)),      # 1x1 output, too few images for the GEMM
+    ((2, 128, 6, 6, 96, 6, 6, 1, 0, 0, 0, 0, 1, 1), (FC, FC)),      # 1x1 output, two images
     ((64, 64, 4, 4, 128, 4, 4, 1, 0, 0, 0, 0, 1, 1), (FC, FC)),     # FC GEMM
     ((2, 32, 12, 12, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8), (CC, CC)),     # thin 3x3
     ((2, 12, 13, 12, 12, 3, 3, 2, 1, 1, 1, 1, 1, 1, 1, 3), (CC, CC)),   # CUDA-core tiles, per-axis stride
@@ -508,6 +514,13 @@ THIN_PLANE = [
     (2, 32, 23, 50, 32, 3, 3, 2, 0, 1, 0, 1, 1, 8),         # 4 per group, stride 2, asymmetric pads
     (1, 6, 7, 7, 6, 3, 3, 2, 1, 1, 1, 1, 1, 6),             # depthwise stride 2, tiny plane
     (4, 64, 7, 7, 64, 3, 3, 1, 1, 1, 1, 1, 1, 64),          # small planes, many groups
+    # rows of 16-byte multiples, stride 1: the sliding-window forms (2 and 4 columns per lane)
+    (2, 16, 12, 16, 16, 3, 3, 1, 1, 1, 1, 1, 1, 16),        # depthwise, 16 columns
+    (2, 8, 13, 40, 8, 3, 3, 1, 0, 2, 2, 0, 1, 8),           # depthwise, pads 0/2/2/0
+    (2, 16, 11, 64, 16, 3, 3, 1, 2, 0, 0, 2, 1, 4),         # 4 per group, 64 columns, pads 2/0/0/2
+    (3, 12, 9, 72, 12, 3, 3, 1, 1, 1, 1, 1, 1, 6),          # 2 per group, 72 columns (4 per lane)
+    (2, 32, 35, 120, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8),        # 4 per group, 120 columns, strips
+    (1, 4, 8, 128, 4, 3, 3, 1, 1, 1, 0, 0, 1, 4),           # depthwise, 128 columns, pads 1/1/0/0
 ]
 
 
@@ -529,3 +542,75 @@ def test_thin_plane_kernels_full(dev, oracle_mod, geom, dtype):
     check_guards("thin fused db", bb)
     assert torch.equal(dw.cpu(), got["dw"])
     check("thin fused db", db.cpu().numpy(), oracle_mod.bwd_bias(geom, f64(dy)), TOL[dtype])
+
+
+
+# 1x1 layers at stride 1 without padding: forward and backward-data as a batched per-image GEMM
+# (the case the cudnn.torch issue #118 thread sets apart from the fully-connected one), the
+# weight gradient on the implicit-GEMM family; fp32 and bf16 outputs.
+POINTWISE = [
+    (2, 64, 8, 8, 32, 1, 1, 1, 0, 0, 0, 0, 1, 1),           # one M tile, K = 64
+    (3, 48, 12, 12, 24, 1, 1, 1, 0, 0, 0, 0, 1, 1),         # K and M not multiples of the tiles
+    (2, 64, 8, 16, 128, 1, 1, 1, 0, 0, 0, 0, 1, 2),         # grouped: 32 -> 64 per group
+    (2, 256, 14, 12, 272, 1, 1, 1, 0, 0, 0, 0, 1, 1),       # several M and K tiles, ragged N tile
+]
+
+
+@pytest.mark.parametrize("geom", POINTWISE)
+def test_pointwise_gemm_full(dev, oracle_mod, geom):
+    assert_paths(geom, "bf16", (PW, PW, TC, RD))
+    wk = wl.Workload("pw", geom, "bf16", w=("normal", 0.2))
+    x, w, b, dy = wl.make_inputs(wk, seed=sum(geom) * 31)
+    got = full_compare(geom, "bf16", x, w, b, dy, dev, oracle_mod, label=f"pointwise {geom}")
+    N, Cin, H, W, Cout = geom[:5]
+    xd, wd, bd, dyd = (t.to(dev) for t in (x, w, b, dy))
+    y16 = torch.empty((N, Cout, H, W), device=dev, dtype=torch.bfloat16)
+    dx16 = torch.empty((N, Cin, H, W), device=dev, dtype=torch.bfloat16)
+    gc.gconv_fwd(xd, wd, bd, y16, **_kw(geom))
+    gc.gconv_bwd_data(dyd, wd, dx16, **_kw(geom))
+    torch.cuda.synchronize()
+    assert gc.gconv_check_device_error() == B.GCONV_OK
+    assert torch.equal(y16.cpu(), got["y"].to(torch.bfloat16))
+    assert torch.equal(dx16.cpu(), got["dx"].to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("name", list(wl.pointwise_zoo(2)))
+def test_pointwise_zoo_layers_full(dev, oracle_mod, name):
+    """The 1x1 layers of ResNet-50 bottlenecks (and a grouped 1x1), batch 2, all four passes."""
+    wk = wl.pointwise_zoo(2)[name]
+    x, w, b, dy = wl.make_inputs(wk, seed=43)
+    H, W = wk.geom[2], wk.geom[3]
+    # rows of H*W elements must be 16-byte multiples for the GEMM's tensor maps
+    assert gc.gconv_plan(wk.geom, B.GCONV_BF16, B.PASS_FWD)[0] == (PW if (H * W) % 8 == 0 else TC)
+    full_compare(wk.geom, "bf16", x, w, b, dy, dev, oracle_mod, label=name)
+
+
+
+# Input size == kernel size with groups: a block-diagonal GEMM on the fully-connected path
+# (G matrix products over the same tensors, read in place), plus shapes whose row counts and
+# channel counts do not fill the GEMM tiles.
+FC_SHAPES = [
+    (4, 64, 5, 5, 96, 5, 5, 1, 0, 0, 0, 0, 1, 4),           # 4 groups, K = 400 per group, 24 outputs
+    (3, 96, 4, 4, 64, 4, 4, 1, 0, 0, 0, 0, 1, 2),           # 2 groups, K = 768, 32 outputs
+    (70, 48, 3, 3, 40, 3, 3, 1, 0, 0, 0, 0, 1, 1),          # K = 432, 40 outputs, 70 images
+    (5, 32, 1, 1, 24, 1, 1, 1, 0, 0, 0, 0, 1, 1),           # 1x1 input: a plain matrix product
+]
+
+
+@pytest.mark.parametrize("geom", FC_SHAPES)
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_fully_connected_gemm_full(dev, oracle_mod, geom, out):
+    assert_paths(geom, "bf16", (FC, FC, FC, RD))
+    wk = wl.Workload("fc", geom, "bf16", w=("normal", 0.2))
+    x, w, b, dy = wl.make_inputs(wk, seed=sum(geom) * 37)
+    got = full_compare(geom, "bf16", x, w, b, dy, dev, oracle_mod, label=f"fc {geom}")
+    if out == "bf16":
+        N, Cin, H, W, Cout = geom[:5]
+        xd, wd, bd, dyd = (t.to(dev) for t in (x, w, b, dy))
+        y16 = torch.empty((N, Cout, 1, 1), device=dev, dtype=torch.bfloat16)
+        dx16 = torch.empty((N, Cin, H, W), device=dev, dtype=torch.bfloat16)
+        gc.gconv_fwd(xd, wd, bd, y16, **_kw(geom))
+        gc.gconv_bwd_data(dyd, wd, dx16, **_kw(geom))
+        torch.cuda.synchronize()
+        assert torch.equal(y16.cpu(), got["y"].to(torch.bfloat16))
+        assert torch.equal(dx16.cpu(), got["dx"].to(torch.bfloat16))
