@@ -23,14 +23,19 @@
 //    Lanes and warps are added in a fixed order into per-block partial sums, and a
 //    second kernel adds the blocks in a fixed order: bitwise reproducible.
 #include "internal.h"
+#include "ptx.cuh"
 
 #include <algorithm>
+#include <mutex>
+#include <utility>
+#include <vector>
 
 namespace gconv {
 namespace {
 
 constexpr int kThinThreads = 128;
-constexpr int kThinSmem = 40 * 1024;   // staged rows per block (several blocks share an SM)
+constexpr int kThinSmem = 40 * 1024;      // staged rows per block, single-buffered forms
+constexpr int kThinSmemMax = 80 * 1024;   // double-buffered (pipelined) forms
 
 struct ThinParams {
     const void *src;     // forward: x; backward-data: gradOutput; weight gradient: x
@@ -488,106 +493,6 @@ __device__ __forceinline__ void store_chunk(float *out, int64_t i, const float (
         if (j < nvalid) store_out(out, i + j, v[j], bf16);
 }
 
-// One produced row of the sliding form: load source row `r + 2` of every input plane into
-// window slot C, then add the 3 x 3 taps over slots A, B, C (source rows r, r+1, r+2).
-// Slots rotate through the unrolled calls, so no window values are copied.
-template <typename T, int CG, int CPL, int A, int Bs, int C>
-__device__ __forceinline__ void slide_step(float (&win)[CG][3][CPL + 2], const T *col, int nrows, int pitch, int r,
-                                           int pl, int lane, const float (&wr)[CG * 9], float bias, float (&acc)[CPL])
-{
-    #pragma unroll
-    for (int ci = 0; ci < CG; ++ci) {
-        float own[CPL];
-        load_chunk<T, CPL>(col + (ci * nrows + r + 2) * pitch, own);
-        window_row<CPL>(own, pl, lane, win[ci][C]);
-    }
-    #pragma unroll
-    for (int j = 0; j < CPL; ++j) acc[j] = bias;
-    #pragma unroll
-    for (int ci = 0; ci < CG; ++ci)
-        #pragma unroll
-        for (int bb = 0; bb < 3; ++bb)
-            #pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                acc[j] = fmaf(wr[ci * 9 + 0 + bb], win[ci][A][j + bb], acc[j]);
-                acc[j] = fmaf(wr[ci * 9 + 3 + bb], win[ci][Bs][j + bb], acc[j]);
-                acc[j] = fmaf(wr[ci * 9 + 6 + bb], win[ci][C][j + bb], acc[j]);
-            }
-}
-
-// Forward / stride-1 backward-data (produced = correlation of the source with Wt, pads pt, pl
-// as in thin_corr_kernel).  Block: (image, group, strip).  Warp w produces output channel
-// o = w % CG for the produced rows of its share of the strip (w / CG of 4 / CG shares), with
-// that channel's 9*CG weights in registers.
-template <typename T, int CG, int CPL>
-__global__ void __launch_bounds__(kThinThreads)
-thin_slide_kernel(const __grid_constant__ ThinParams p)
-{
-    extern __shared__ __align__(16) unsigned char thin_sm[];
-    constexpr int PAD = PadE<T>::value;
-    constexpr int WPO = 4 / CG;
-    const T *W = static_cast<const T *>(p.w);
-    int b = blockIdx.x;
-    const int strip = b % p.n_strip; b /= p.n_strip;
-    const int g = b % p.G;
-    const int n = b / p.G;
-    const int r0 = strip * p.TH;
-    const int rows = min(p.TH, p.OH - r0);
-    const int lo = r0 - p.pt, nrows = rows + 2;
-    const int pitch = PAD + 32 * CPL + PAD;
-    const int64_t plane = (int64_t)p.IH * p.IW;
-    T *stage = reinterpret_cast<T *>(thin_sm);
-    stage_padded(static_cast<const T *>(p.src) + ((int64_t)n * p.G + g) * CG * plane, plane, CG, p.IH, p.IW, lo,
-                 nrows, pitch, stage);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int o = warp % CG, share = warp / CG;
-    // this warp's output channel: weights Wt[o][ci][tap] in registers
-    float wr[CG * 9];
-    #pragma unroll
-    for (int ci = 0; ci < CG; ++ci)
-        #pragma unroll
-        for (int t = 0; t < 9; ++t)
-            wr[ci * 9 + t] = !p.bwd ? to_f(W[((int64_t)(g * CG + o) * CG + ci) * 9 + t])
-                                    : to_f(W[((int64_t)(g * CG + ci) * CG + o) * 9 + (8 - t)]);
-    const float bias = (p.bias && !p.bwd) ? to_f(static_cast<const T *>(p.bias)[g * CG + o]) : 0.f;
-    __syncthreads();
-    const int q = (rows + WPO - 1) / WPO;
-    const int ra = share * q, rb = min(rows, ra + q);
-    if (ra >= rb) return;
-    const int c0 = lane * CPL;
-    const int nvalid = min(CPL, max(0, p.OW - c0));
-    const int64_t out_plane = (int64_t)p.OH * p.OW;
-    const int64_t obase = (((int64_t)n * p.G + g) * CG + o) * out_plane + c0;
-    const T *col = stage + PAD + c0;
-    float win[CG][3][CPL + 2];
-    #pragma unroll
-    for (int ci = 0; ci < CG; ++ci)
-        #pragma unroll
-        for (int a = 0; a < 2; ++a) {
-            float own[CPL];
-            load_chunk<T, CPL>(col + (ci * nrows + ra + a) * pitch, own);
-            window_row<CPL>(own, p.pl, lane, win[ci][a]);
-        }
-    float acc[CPL];
-    int r = ra;
-    for (; r + 3 <= rb; r += 3) {
-        slide_step<T, CG, CPL, 0, 1, 2>(win, col, nrows, pitch, r, p.pl, lane, wr, bias, acc);
-        if (nvalid > 0) store_chunk<CPL>(p.out, obase + (int64_t)(r0 + r) * p.OW, acc, nvalid, p.out_bf16);
-        slide_step<T, CG, CPL, 1, 2, 0>(win, col, nrows, pitch, r + 1, p.pl, lane, wr, bias, acc);
-        if (nvalid > 0) store_chunk<CPL>(p.out, obase + (int64_t)(r0 + r + 1) * p.OW, acc, nvalid, p.out_bf16);
-        slide_step<T, CG, CPL, 2, 0, 1>(win, col, nrows, pitch, r + 2, p.pl, lane, wr, bias, acc);
-        if (nvalid > 0) store_chunk<CPL>(p.out, obase + (int64_t)(r0 + r + 2) * p.OW, acc, nvalid, p.out_bf16);
-    }
-    if (r < rb) {
-        slide_step<T, CG, CPL, 0, 1, 2>(win, col, nrows, pitch, r, p.pl, lane, wr, bias, acc);
-        if (nvalid > 0) store_chunk<CPL>(p.out, obase + (int64_t)(r0 + r) * p.OW, acc, nvalid, p.out_bf16);
-    }
-    if (r + 1 < rb) {
-        slide_step<T, CG, CPL, 1, 2, 0>(win, col, nrows, pitch, r + 1, p.pl, lane, wr, bias, acc);
-        if (nvalid > 0) store_chunk<CPL>(p.out, obase + (int64_t)(r0 + r + 1) * p.OW, acc, nvalid, p.out_bf16);
-    }
-}
-
 // One gradOutput row of the sliding weight gradient: x row r + 2 of every input plane into
 // window slot C, then acc[ci*9 + tap] += dy[j] * x window (slots A, B, C = rows r..r+2),
 // and the bias accumulator += dy[j].
@@ -617,13 +522,199 @@ __device__ __forceinline__ void wgrad_step(float (&win)[CG][3][CPL + 2], const T
             }
 }
 
-// Weight gradient + bias gradient, stride 1 (the accumulation of thin_wgrad_kernel).
-// Warp w: output channel o = w % CG; its rows of the strip are [ (w/CG)*q, ... ) with
-// q = rows / (4/CG) rounded up.  x rows are staged zero-bordered from r0 - pt, gradOutput
-// rows zero-bordered from r0 (columns past Wo are zero, so they add nothing).
+// ---------------------------------------------------------------------------
+// Pipelined forms (stride 1, the sliding window's row and column limits).  A block walks
+// work items persistently and double-buffers their staged rows: while it computes item k
+// from one buffer, the 16-byte cp.async copies of item k+1 (zero-filled where a row or
+// column lies outside the source) land in the other, so load latency is not paid per item.
+
+// Staged-row copies of rows [lo, lo + nrows) of CG planes into a zero-bordered buffer of
+// CG*nrows_max rows (cp.async; vectors outside the source are zero-filled).
+template <typename T, int CG>
+__device__ __forceinline__ void issue_rows(const T *__restrict__ src, int64_t plane, int IH, int IW, int lo, int nrows,
+                                           int nrows_max, int pitch, T *buf)
+{
+    constexpr int PAD = PadE<T>::value;
+    const int vrow = pitch / PAD, vdata = IW / PAD;
+    const int total_rows = CG * nrows_max;
+    const int total = total_rows * vrow;
+    const int step_r = kThinThreads / vrow, step_k = kThinThreads - step_r * vrow;
+    int row = threadIdx.x / vrow, k = threadIdx.x - row * vrow;
+    const uint32_t dst0 = ptx::smem_u32(buf);
+    for (int i = threadIdx.x; i < total; i += kThinThreads) {
+        const int c = CG == 1 ? 0 : row / nrows_max;
+        const int j = row - c * nrows_max;
+        const int ih = lo + j;
+        const bool data = j < nrows && k >= 1 && k <= vdata && ih >= 0 && ih < IH;
+        const T *sp = data ? src + c * plane + (int64_t)ih * IW + (k - 1) * PAD : src;
+        ptx::cp_async16(dst0 + (uint32_t)((row * vrow + k) * 16), sp, data ? 16u : 0u);
+        row += step_r;
+        k += step_k;
+        if (k >= vrow) { k -= vrow; ++row; }
+    }
+}
+
+// One produced row for every output channel of the group: source row r + 2 of each input
+// plane into window slot C, then the 3 x 3 taps over slots A, B, C.
+template <typename T, int CG, int CPL, int A, int Bs, int C>
+__device__ __forceinline__ void pipe_step(float (&win)[CG][3][CPL + 2], const T *col, int nrows_max, int pitch, int r,
+                                          int pl, int lane, const float *wsm, const float (&bias)[CG],
+                                          float (&acc)[CG][CPL])
+{
+    #pragma unroll
+    for (int ci = 0; ci < CG; ++ci) {
+        float own[CPL];
+        load_chunk<T, CPL>(col + (ci * nrows_max + r + 2) * pitch, own);
+        window_row<CPL>(own, pl, lane, win[ci][C]);
+    }
+    #pragma unroll
+    for (int o = 0; o < CG; ++o) {
+        #pragma unroll
+        for (int j = 0; j < CPL; ++j) acc[o][j] = bias[o];
+        #pragma unroll
+        for (int ci = 0; ci < CG; ++ci) {
+            const float4 *w4 = reinterpret_cast<const float4 *>(wsm + (o * CG + ci) * 12);
+            const float4 w0 = w4[0], w1 = w4[1], w2 = w4[2];
+            const float wv[9] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w, w2.x};
+            #pragma unroll
+            for (int bb = 0; bb < 3; ++bb)
+                #pragma unroll
+                for (int j = 0; j < CPL; ++j) {
+                    acc[o][j] = fmaf(wv[0 + bb], win[ci][A][j + bb], acc[o][j]);
+                    acc[o][j] = fmaf(wv[3 + bb], win[ci][Bs][j + bb], acc[o][j]);
+                    acc[o][j] = fmaf(wv[6 + bb], win[ci][C][j + bb], acc[o][j]);
+                }
+        }
+    }
+}
+
+template <int CG, int CPL>
+__device__ __forceinline__ void pipe_store(float *out, int64_t base, int64_t out_plane, const float (&acc)[CG][CPL],
+                                           int nvalid, int bf16)
+{
+    #pragma unroll
+    for (int o = 0; o < CG; ++o) store_chunk<CPL>(out, base + o * out_plane, acc[o], nvalid, bf16);
+}
+
+// Forward / stride-1 backward-data, pipelined.  Item = (image, group, strip); the four
+// warps split the strip's produced rows, each thread produces CPL columns of every output
+// channel of the group (weights Wt[o][i][tap] from shared memory, per item).
 template <typename T, int CG, int CPL>
 __global__ void __launch_bounds__(kThinThreads)
-thin_slide_wgrad_kernel(const __grid_constant__ ThinParams p)
+thin_pipe_kernel(const __grid_constant__ ThinParams p)
+{
+    extern __shared__ __align__(16) unsigned char thin_sm[];
+    __shared__ __align__(16) float ws[2][CG * CG * 12];   // [out][in][12]: 9 taps, 3 pad
+    constexpr int PAD = PadE<T>::value;
+    constexpr int NW = CG * CG * 9;
+    constexpr int WPT = (NW + kThinThreads - 1) / kThinThreads;   // weights loaded per thread
+    const T *W = static_cast<const T *>(p.w);
+    const T *src = static_cast<const T *>(p.src);
+    const int pitch = PAD + 32 * CPL + PAD;
+    const int nrows_max = p.TH + 2;
+    const int buf_elems = CG * nrows_max * pitch;
+    T *bufs = reinterpret_cast<T *>(thin_sm);
+    const int64_t plane = (int64_t)p.IH * p.IW;
+    const int items = p.N * p.G * p.n_strip;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    auto issue = [&](int it, int b, float (&wv)[WPT]) {
+        int t = it;
+        const int strip = t % p.n_strip; t /= p.n_strip;
+        const int g = t % p.G;
+        const int n = t / p.G;
+        const int r0 = strip * p.TH;
+        const int rows = min(p.TH, p.OH - r0);
+        issue_rows<T, CG>(src + ((int64_t)n * p.G + g) * CG * plane, plane, p.IH, p.IW, r0 - p.pt, rows + 2, nrows_max,
+                          pitch, bufs + b * buf_elems);
+        #pragma unroll
+        for (int u = 0; u < WPT; ++u) {
+            const int i = threadIdx.x + u * kThinThreads;
+            float v = 0.f;
+            if (i < NW) {
+                const int o = i / (CG * 9), rem = i - o * CG * 9, ci = rem / 9, tap = rem - ci * 9;
+                v = !p.bwd ? to_f(W[((int64_t)(g * CG + o) * CG + ci) * 9 + tap])
+                           : to_f(W[((int64_t)(g * CG + ci) * CG + o) * 9 + (8 - tap)]);
+            }
+            wv[u] = v;
+        }
+    };
+    float wnext[WPT];
+    int b = 0;
+    if ((int)blockIdx.x < items) issue(blockIdx.x, 0, wnext);
+    ptx::cp_async_commit();
+    for (int it = blockIdx.x; it < items; it += gridDim.x, b ^= 1) {
+        float wcur[WPT];
+        #pragma unroll
+        for (int u = 0; u < WPT; ++u) wcur[u] = wnext[u];
+        if (it + (int)gridDim.x < items) issue(it + gridDim.x, b ^ 1, wnext);
+        ptx::cp_async_commit();
+        #pragma unroll
+        for (int u = 0; u < WPT; ++u) {
+            const int i = threadIdx.x + u * kThinThreads;
+            if (i < NW) ws[b][(i / 9) * 12 + i % 9] = wcur[u];
+        }
+        ptx::cp_async_wait_group<1>();   // this item's rows have landed (the next item's may not)
+        __syncthreads();
+        int t = it;
+        const int strip = t % p.n_strip; t /= p.n_strip;
+        const int g = t % p.G;
+        const int n = t / p.G;
+        const int r0 = strip * p.TH;
+        const int rows = min(p.TH, p.OH - r0);
+        const int q = (rows + 3) >> 2;
+        const int ra = warp * q, rb = min(rows, ra + q);
+        if (ra < rb) {
+            float bias[CG];
+            #pragma unroll
+            for (int o = 0; o < CG; ++o) bias[o] = (p.bias && !p.bwd) ? to_f(static_cast<const T *>(p.bias)[g * CG + o]) : 0.f;
+            const int c0 = lane * CPL;
+            const int nvalid = min(CPL, max(0, p.OW - c0));
+            const int64_t out_plane = (int64_t)p.OH * p.OW;
+            const int64_t obase = ((int64_t)n * p.G + g) * CG * out_plane + c0;
+            const T *col = bufs + b * buf_elems + PAD + c0;
+            const float *wsm = ws[b];
+            float win[CG][3][CPL + 2];
+            #pragma unroll
+            for (int ci = 0; ci < CG; ++ci)
+                #pragma unroll
+                for (int a = 0; a < 2; ++a) {
+                    float own[CPL];
+                    load_chunk<T, CPL>(col + (ci * nrows_max + ra + a) * pitch, own);
+                    window_row<CPL>(own, p.pl, lane, win[ci][a]);
+                }
+            float acc[CG][CPL];
+            int r = ra;
+            for (; r + 3 <= rb; r += 3) {
+                pipe_step<T, CG, CPL, 0, 1, 2>(win, col, nrows_max, pitch, r, p.pl, lane, wsm, bias, acc);
+                if (nvalid > 0) pipe_store<CG, CPL>(p.out, obase + (int64_t)(r0 + r) * p.OW, out_plane, acc, nvalid, p.out_bf16);
+                pipe_step<T, CG, CPL, 1, 2, 0>(win, col, nrows_max, pitch, r + 1, p.pl, lane, wsm, bias, acc);
+                if (nvalid > 0)
+                    pipe_store<CG, CPL>(p.out, obase + (int64_t)(r0 + r + 1) * p.OW, out_plane, acc, nvalid, p.out_bf16);
+                pipe_step<T, CG, CPL, 2, 0, 1>(win, col, nrows_max, pitch, r + 2, p.pl, lane, wsm, bias, acc);
+                if (nvalid > 0)
+                    pipe_store<CG, CPL>(p.out, obase + (int64_t)(r0 + r + 2) * p.OW, out_plane, acc, nvalid, p.out_bf16);
+            }
+            if (r < rb) {
+                pipe_step<T, CG, CPL, 0, 1, 2>(win, col, nrows_max, pitch, r, p.pl, lane, wsm, bias, acc);
+                if (nvalid > 0) pipe_store<CG, CPL>(p.out, obase + (int64_t)(r0 + r) * p.OW, out_plane, acc, nvalid, p.out_bf16);
+            }
+            if (r + 1 < rb) {
+                pipe_step<T, CG, CPL, 1, 2, 0>(win, col, nrows_max, pitch, r + 1, p.pl, lane, wsm, bias, acc);
+                if (nvalid > 0)
+                    pipe_store<CG, CPL>(p.out, obase + (int64_t)(r0 + r + 1) * p.OW, out_plane, acc, nvalid, p.out_bf16);
+            }
+        }
+        __syncthreads();   // buffer b and ws[b] are free again
+    }
+    ptx::cp_async_wait_group<0>();   // nothing may land after the block exits
+}
+
+// Weight gradient + bias gradient, stride 1, pipelined over the images of a block's item
+// (group, image chunk, strip): x and gradOutput rows of image n+1 land while image n is
+// accumulated.  Warp w: output channel o = w % CG, its share w / CG of the strip's rows.
+template <typename T, int CG, int CPL>
+__global__ void __launch_bounds__(kThinThreads)
+thin_pipe_wgrad_kernel(const __grid_constant__ ThinParams p)
 {
     extern __shared__ __align__(16) unsigned char thin_sm[];
     constexpr int NA = CG * 9 + 1;
@@ -641,22 +732,34 @@ thin_slide_wgrad_kernel(const __grid_constant__ ThinParams p)
     const int r0 = strip * p.TH;
     const int rows = min(p.TH, p.OH - r0);
     const int pitch = PAD + 32 * CPL + PAD;
-    const int xrows = rows + 2;
+    const int xrows_max = p.TH + 2, yrows_max = p.TH;
+    const int buf_elems = CG * (xrows_max + yrows_max) * pitch;
+    T *bufs = reinterpret_cast<T *>(thin_sm);
     const int64_t xplane = (int64_t)p.IH * p.IW, yplane = (int64_t)p.OH * p.OW;
-    T *xs = reinterpret_cast<T *>(thin_sm);
-    T *ys = xs + CG * xrows * pitch;
     const int q = (rows + WPO - 1) / WPO;
     const int ra = part_w * q, rb = min(rows, ra + q);
     const int c0 = lane * CPL;
+    auto issue = [&](int n, int bi) {
+        T *xs = bufs + bi * buf_elems;
+        T *ys = xs + CG * xrows_max * pitch;
+        issue_rows<T, CG>(X + ((int64_t)n * p.G + g) * CG * xplane, xplane, p.IH, p.IW, r0 - p.pt, rows + 2, xrows_max,
+                          pitch, xs);
+        issue_rows<T, CG>(DY + ((int64_t)n * p.G + g) * CG * yplane, yplane, p.OH, p.OW, r0, rows, yrows_max, pitch, ys);
+    };
     float acc[NA];
     #pragma unroll
     for (int k = 0; k < NA; ++k) acc[k] = 0.f;
     const int n0 = chunk * p.per_chunk, n1 = min(p.N, n0 + p.per_chunk);
-    for (int n = n0; n < n1; ++n) {
-        stage_padded(X + ((int64_t)n * p.G + g) * CG * xplane, xplane, CG, p.IH, p.IW, r0 - p.pt, xrows, pitch, xs);
-        stage_padded(DY + ((int64_t)n * p.G + g) * CG * yplane, yplane, CG, p.OH, p.OW, r0, rows, pitch, ys);
+    if (n0 < n1) issue(n0, 0);
+    ptx::cp_async_commit();
+    for (int n = n0, bi = 0; n < n1; ++n, bi ^= 1) {
+        if (n + 1 < n1) issue(n + 1, bi ^ 1);
+        ptx::cp_async_commit();
+        ptx::cp_async_wait_group<1>();
         __syncthreads();
         if (ra < rb) {
+            const T *xs = bufs + bi * buf_elems;
+            const T *ys = xs + CG * xrows_max * pitch;
             float win[CG][3][CPL + 2];
             const T *xcol = xs + PAD + c0;
             #pragma unroll
@@ -664,21 +767,22 @@ thin_slide_wgrad_kernel(const __grid_constant__ ThinParams p)
                 #pragma unroll
                 for (int a = 0; a < 2; ++a) {
                     float own[CPL];
-                    load_chunk<T, CPL>(xcol + (ci * xrows + ra + a) * pitch, own);
+                    load_chunk<T, CPL>(xcol + (ci * xrows_max + ra + a) * pitch, own);
                     window_row<CPL>(own, p.pl, lane, win[ci][a]);
                 }
-            const T *ycol = ys + PAD + c0 + o * rows * pitch;
+            const T *ycol = ys + PAD + c0 + o * yrows_max * pitch;
             int r = ra;
             for (; r + 3 <= rb; r += 3) {
-                wgrad_step<T, CG, CPL, 0, 1, 2>(win, xcol, ycol, xrows, pitch, r, p.pl, lane, acc);
-                wgrad_step<T, CG, CPL, 1, 2, 0>(win, xcol, ycol, xrows, pitch, r + 1, p.pl, lane, acc);
-                wgrad_step<T, CG, CPL, 2, 0, 1>(win, xcol, ycol, xrows, pitch, r + 2, p.pl, lane, acc);
+                wgrad_step<T, CG, CPL, 0, 1, 2>(win, xcol, ycol, xrows_max, pitch, r, p.pl, lane, acc);
+                wgrad_step<T, CG, CPL, 1, 2, 0>(win, xcol, ycol, xrows_max, pitch, r + 1, p.pl, lane, acc);
+                wgrad_step<T, CG, CPL, 2, 0, 1>(win, xcol, ycol, xrows_max, pitch, r + 2, p.pl, lane, acc);
             }
-            if (r < rb) wgrad_step<T, CG, CPL, 0, 1, 2>(win, xcol, ycol, xrows, pitch, r, p.pl, lane, acc);
-            if (r + 1 < rb) wgrad_step<T, CG, CPL, 1, 2, 0>(win, xcol, ycol, xrows, pitch, r + 1, p.pl, lane, acc);
+            if (r < rb) wgrad_step<T, CG, CPL, 0, 1, 2>(win, xcol, ycol, xrows_max, pitch, r, p.pl, lane, acc);
+            if (r + 1 < rb) wgrad_step<T, CG, CPL, 1, 2, 0>(win, xcol, ycol, xrows_max, pitch, r + 1, p.pl, lane, acc);
         }
         __syncthreads();
     }
+    ptx::cp_async_wait_group<0>();
     #pragma unroll
     for (int k = 0; k < NA; ++k) {
         float v = acc[k];
@@ -704,14 +808,32 @@ thin_slide_wgrad_kernel(const __grid_constant__ ThinParams p)
 
 int thin_cpl(int ow) { return ow >= 48 ? 4 : (ow >= 16 ? 2 : 1); }
 
+// Raises a kernel's dynamic shared-memory limit (once per device and kernel) when a launch
+// needs more than the default 48 KB.
+bool allow_smem(const void *fn, size_t bytes)
+{
+    if (bytes <= 48 * 1024) return true;
+    static std::mutex mu;
+    static std::vector<std::pair<int, const void *>> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto &d : done)
+        if (d.first == dev && d.second == fn) return true;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kThinSmemMax) != cudaSuccess)
+        return false;
+    done.push_back({dev, fn});
+    return true;
+}
+
 // Staged bytes of one block for a strip of `th` produced rows.
 int64_t thin_stage_elems(const ThinParams &p, int CG, int th, bool wgrad, int esize)
 {
-    if (p.slide) {
+    if (p.slide) {   // two buffers of zero-bordered rows
         const int64_t pitch = 16 / esize + 32 * p.cpl + 16 / esize;
         int64_t e = (int64_t)CG * (th + 2) * pitch;
         if (wgrad) e += (int64_t)CG * th * pitch;
-        return e * esize;
+        return 2 * e * esize;
     }
     int in_rows;
     if (!p.bwd || p.S == 1) in_rows = (th - 1) * p.S + 3;
@@ -748,13 +870,13 @@ bool thin_plan(const Geom &g, gconv_pass pass, int esize, ThinParams *p, int *gr
         p->pt = g.pt; p->pl = g.pl;
     }
     const bool wg = pass == GCONV_PASS_BWD_WEIGHT;
-    // sliding-window form: stride 1, 16-byte source (and gradOutput) rows, at most 128 columns
+    // pipelined sliding-window form: stride 1, 16-byte source (and gradOutput) rows, at most
+    // 128 columns
     const int span = std::max(p->IW, p->OW);
-    // (forward / backward-data with 4 channels per group stay on the staged-window form,
-    // which produced all four channels per thread and measured faster on GB300: 81 vs 121 us
-    // on the ResNeXt 4-channel layer)
+    // (the forward and backward-data with four channels per group stay on the staged-window
+    // form: a thread of the sliding form would hold 4 planes' windows and 4 channels' sums)
     p->slide = g.s_h == 1 && span <= 128 && (p->IW * esize) % 16 == 0 && (!wg || (p->OW * esize) % 16 == 0) &&
-               (wg || CG < 4);
+               (wg || CG <= 2);
     p->cpl = p->slide ? (span <= 64 ? 2 : 4) : thin_cpl(p->OW);
     const int64_t planes = (int64_t)g.N * g.G;
     const int64_t target_blocks = (int64_t)num_sms() * 16;
@@ -763,8 +885,9 @@ bool thin_plan(const Geom &g, gconv_pass pass, int esize, ThinParams *p, int *gr
         // split rows until there are enough blocks, but keep strips of 8 rows or more
         while (th > 8 && planes * ((p->OH + th - 1) / th) < target_blocks) th = (th + 1) / 2;
     }
-    while (th > 1 && thin_stage_elems(*p, CG, th, wg, esize) > kThinSmem) th = (th + 1) / 2;
-    if (thin_stage_elems(*p, CG, th, wg, esize) > kThinSmem) return false;
+    const int64_t budget = p->slide ? kThinSmemMax : kThinSmem;
+    while (th > 1 && thin_stage_elems(*p, CG, th, wg, esize) > budget) th = (th + 1) / 2;
+    if (thin_stage_elems(*p, CG, th, wg, esize) > budget) return false;
     p->TH = th;
     p->n_strip = (p->OH + th - 1) / th;
     *smem = (size_t)thin_stage_elems(*p, CG, th, wg, esize);
@@ -789,13 +912,22 @@ gconv_status thin_launch_t(const ThinParams &p, int grid, size_t smem, bool wgra
     const int cpl = p.cpl;
     if (S == 1 && p.slide) {
         if (wgrad) {
-            if (cpl == 2) thin_slide_wgrad_kernel<T, CG, 2><<<grid, kThinThreads, smem, s>>>(p);
-            else thin_slide_wgrad_kernel<T, CG, 4><<<grid, kThinThreads, smem, s>>>(p);
+            const void *fn = cpl == 2 ? (const void *)thin_pipe_wgrad_kernel<T, CG, 2>
+                                      : (const void *)thin_pipe_wgrad_kernel<T, CG, 4>;
+            if (!allow_smem(fn, smem)) return GCONV_ERR_CUDA;
+            if (cpl == 2) thin_pipe_wgrad_kernel<T, CG, 2><<<grid, kThinThreads, smem, s>>>(p);
+            else thin_pipe_wgrad_kernel<T, CG, 4><<<grid, kThinThreads, smem, s>>>(p);
             const int total = p.G * CG * (CG * 9 + 1);
             thin_wgrad_finish_kernel<CG><<<(total + 255) / 256, 256, 0, s>>>(p.out, p.G, p.nchunk * p.n_strip, dw, db);
         } else {
-            if (cpl == 2) thin_slide_kernel<T, CG, 2><<<grid, kThinThreads, smem, s>>>(p);
-            else thin_slide_kernel<T, CG, 4><<<grid, kThinThreads, smem, s>>>(p);
+            const void *fn = cpl == 2 ? (const void *)thin_pipe_kernel<T, CG, 2> : (const void *)thin_pipe_kernel<T, CG, 4>;
+            if (!allow_smem(fn, smem)) return GCONV_ERR_CUDA;
+            int per_sm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThinThreads, smem) != cudaSuccess || per_sm < 1)
+                per_sm = 1;
+            const int pgrid = std::min(grid, num_sms() * per_sm);   // persistent: items walked by a resident grid
+            if (cpl == 2) thin_pipe_kernel<T, CG, 2><<<pgrid, kThinThreads, smem, s>>>(p);
+            else thin_pipe_kernel<T, CG, 4><<<pgrid, kThinThreads, smem, s>>>(p);
         }
         return GCONV_OK;
     }
@@ -868,7 +1000,6 @@ gconv_status thin_launch(const Geom &g, gconv_dtype dt, gconv_pass pass, const v
     p.bias = pass == GCONV_PASS_FWD ? bias : nullptr;
     p.out = wg ? static_cast<float *>(ws) : out;
     p.out_bf16 = wg ? 0 : g.out_bf16;
-    if (smem > 48 * 1024) return GCONV_ERR_UNSUPPORTED;   // within the default dynamic limit
     return dt == GCONV_BF16 ? thin_launch_dt<__nv_bfloat16>(g, p, grid, smem, wg, out, db, s)
                             : thin_launch_dt<float>(g, p, grid, smem, wg, out, db, s);
 }
