@@ -1211,7 +1211,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
             const int vcount = min(32, p.Cv - v0);
             const int64_t vout = ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv + v0) * out_hw;   // element index
             const float bias_lane = (p.bias && lane < vcount) ? __bfloat162float(p.bias[g * p.Cv + v0 + lane]) : 0.f;
-            for (int pc = 0; pc < 256; pc += 32) {
+            for (int pc = 0; pc < p.tile_pos; pc += 32) {
                 uint32_t a0[16], a1[16];
                 const uint32_t taddr = tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)(acc * 256 + pc);
                 ptx::tmem_ld16(taddr, a0);
@@ -1226,7 +1226,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                     __syncwarp();
                     const int pos = p0 + pc + lane;
                     const int qh = pos / p.Wp, qw = pos - qh * p.Wp;
-                    if (qh < p.Qh && qw < p.Qw) {
+                    if (pc + lane < p.tile_pos && qh < p.Qh && qw < p.Qw) {
                         const int64_t o = vout + (int64_t)qh * p.Qw + qw;
                         if (p.out_bf16) {
                             __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(p.V) + o;
@@ -1480,7 +1480,11 @@ bool build_corr(const Geom &g, bool bwd_data, const std::vector<Tap> &taps, int 
         const size_t smem = (size_t)4 * c.nplanes * plane_elems * 16 + (size_t)kWeightStages * c.bps * wblk +
                             (size_t)16 * scr_stride * 2 + (size_t)(c.nplanes * plane_elems + 16) * sizeof(int);
         if (smem > kMaxSmem) continue;
-        long cost = (long)blocks * MBe * 128 * (8 + 8 / MBe);
+        // one CTA per SM (its shared memory): time ~ waves of CTAs x a CTA's work, which is
+        // about 8 units per 128-position M block plus 8 for staging and the weight stream
+        const long ctas = (long)g.G * g.N * blocks * c.n_ntile;
+        const long waves = (ctas + num_sms() - 1) / num_sms();
+        long cost = waves * (8L * MBe + 8);
         if (next_pow2(MBe * c.NT) > 256) cost = cost * 5 / 4;
         if (best < 0 || cost < best) {
             best = cost;
@@ -1776,9 +1780,15 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
     }
     c.ntaps = nblk;
     c.pair_delta = pair ? g.d_w : 0;
-    c.nmma = pair ? 240 : 256;
-    c.tile_pos = c.nmma - c.pair_delta;
     const int positions = Qh * c.Wp;   // padded output grid rows that hold real outputs
+    c.nmma = pair ? 240 : 256;
+    if (!pair) {
+        // the narrowest MMA (a multiple of 16) that keeps the number of tiles per image: the
+        // weight stream per tile is unchanged and the MMAs over positions past the grid shrink
+        const int nt = (positions + 255) / 256;
+        c.nmma = std::min(256, round_up((positions + nt - 1) / nt, 16));
+    }
+    c.tile_pos = c.nmma - c.pair_delta;
     c.Cu = Cu;
     c.n_ptile = (positions + c.tile_pos - 1) / c.tile_pos;
     c.n_tiles = g.N * g.G * c.n_vtile * c.n_ptile;

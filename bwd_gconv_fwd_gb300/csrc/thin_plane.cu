@@ -919,7 +919,7 @@ gconv_status thin_launch_t(const ThinParams &p, int grid, size_t smem, bool wgra
             else thin_pipe_wgrad_kernel<T, CG, 4><<<grid, kThinThreads, smem, s>>>(p);
             const int total = p.G * CG * (CG * 9 + 1);
             thin_wgrad_finish_kernel<CG><<<(total + 255) / 256, 256, 0, s>>>(p.out, p.G, p.nchunk * p.n_strip, dw, db);
-        } else {
+        } else if constexpr (CG <= 2) {   // (planning keeps four-channel groups off this form)
             const void *fn = cpl == 2 ? (const void *)thin_pipe_kernel<T, CG, 2> : (const void *)thin_pipe_kernel<T, CG, 4>;
             if (!allow_smem(fn, smem)) return GCONV_ERR_CUDA;
             int per_sm = 0;
@@ -928,6 +928,8 @@ gconv_status thin_launch_t(const ThinParams &p, int grid, size_t smem, bool wgra
             const int pgrid = std::min(grid, num_sms() * per_sm);   // persistent: items walked by a resident grid
             if (cpl == 2) thin_pipe_kernel<T, CG, 2><<<pgrid, kThinThreads, smem, s>>>(p);
             else thin_pipe_kernel<T, CG, 4><<<pgrid, kThinThreads, smem, s>>>(p);
+        } else {
+            return GCONV_ERR_UNSUPPORTED;
         }
         return GCONV_OK;
     }

@@ -81,7 +81,7 @@ int main(int argc, char **argv)
                     }
             CHECK((((size_t)gg * c.n_vtile + vt) + 1) * c.nchu * c.ntaps * kWblkBytes <= C.wpk_bytes, "weights");
             // stores: each tile writes positions [p0, p0 + tile_pos) that are real outputs
-            const int cols = c.pair_delta ? c.tile_pos : 256;
+            const int cols = c.tile_pos;
             for (int j = 0; j < cols; ++j) {
                 const int pos = p0 + j, qh = pos / c.Wp, qw = pos % c.Wp;
                 if (!(qh < c.Qh && qw < c.Qw)) continue;
@@ -94,7 +94,7 @@ int main(int argc, char **argv)
         // coverage: every real output position belongs to exactly one tile
         std::vector<int> cov(plane, 0);
         for (int pt = 0; pt < c.n_ptile; ++pt)
-            for (int j = 0; j < (c.pair_delta ? c.tile_pos : 256); ++j) if (pt * c.tile_pos + j < plane) cov[pt * c.tile_pos + j]++;
+            for (int j = 0; j < c.tile_pos; ++j) if (pt * c.tile_pos + j < plane) cov[pt * c.tile_pos + j]++;
         for (int pos = 0; pos < c.Qh * c.Wp; ++pos) if (pos % c.Wp < c.Qw) CHECK(cov[pos] == 1, "coverage %d: %d", pos, cov[pos]);
     }
     printf("errors: %ld\n", errors);
