@@ -171,6 +171,12 @@ Plan plan_pass(const Geom &g, gconv_dtype dt, gconv_pass pass)
     }
     if (dt == GCONV_BF16 && (force == GCONV_PATH_NONE || force == GCONV_PATH_TC_IGEMM)) {
         if (tc_igemm_plan(g, pass, &p)) return p;
+        // groups too thin for the tensor-core kernels: merged groups on the same kernels,
+        // unless the thin-plane CUDA-core kernels (1, 2 or 4 channels a group) serve them
+        Plan thin{};
+        if ((force == GCONV_PATH_TC_IGEMM || !thin_plan_pass(g, dt, pass, &thin)) && tc_merged_plan(g, pass, &p))
+            return p;
+        p = Plan{};
     }
     if (force != GCONV_PATH_NONE && force != GCONV_PATH_DIRECT) {
         p.path = -1;   // forced family cannot serve this request
@@ -298,7 +304,9 @@ static gconv_status run_pass(const Geom &g, gconv_dtype dt, gconv_dtype out_dt, 
     gconv_status st = GCONV_OK;
     if (p.path == GCONV_PATH_TC_IGEMM) {
         bool db_done = false;
-        st = tc_igemm_launch(gk, p, pass, a, b, bias, o, pass == GCONV_PASS_BWD_WEIGHT ? db : nullptr, ws, s, &db_done);
+        float *dbp = pass == GCONV_PASS_BWD_WEIGHT ? db : nullptr;
+        st = p.merge > 1 ? tc_merged_launch(gk, p, pass, a, b, bias, o, dbp, ws, s, &db_done)
+                         : tc_igemm_launch(gk, p, pass, a, b, bias, o, dbp, ws, s, &db_done);
         if (db_done) db = nullptr;   // written by the same launches
     } else if (p.path == GCONV_PATH_TC_FC || p.path == GCONV_PATH_TC_GEMM) {
         st = tc_fc_launch(gk, p, pass, a, b, bias, o, ws, s);

@@ -23,6 +23,8 @@ struct Plan {
     int64_t pos_per_split = 0;
     int n_per_split = 0;
     int tc[32] = {};          // tensor-core family parameters (see the family's .cu)
+    int merge = 1;            // tensor-core family on merged groups: groups run as one (1: none)
+    size_t merge_ws = 0;      // of ws_bytes, the part the merged geometry's kernels use
 };
 
 gconv_status make_geom(int N, int C_in, int H, int W, int C_out, int kH, int kW, int stride,
@@ -40,6 +42,12 @@ bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p);
 gconv_status tc_igemm_launch(const Geom &g, const Plan &p, gconv_pass pass, const void *a,
                              const void *b, const void *bias, float *out, float *db, void *ws, cudaStream_t s,
                              bool *db_done);
+
+// The same family for groups too thin for it (fewer than 16 channels a side): consecutive
+// groups merged into one with block-diagonal weights (tc_conv.cu).  The plan sets merge.
+bool tc_merged_plan(const Geom &g, gconv_pass pass, Plan *p);
+gconv_status tc_merged_launch(const Geom &g, const Plan &p, gconv_pass pass, const void *a, const void *b,
+                              const void *bias, float *out, float *db, void *ws, cudaStream_t s, bool *db_done);
 
 // CUDA-core kernels on shared-memory tiles for thin groups and fp32 (direct_tiled.cu)
 bool tiled_plan(const Geom &g, gconv_pass pass, Plan *p);

@@ -533,8 +533,8 @@ struct WgradParams {
     int splits;                  // partial slices in the workspace (the largest group split count)
     int nbuf;                    // staging buffers (2 or 3)
     int tma;                     // 1: tiles arrive by TMA (tm_x, tm_dy); 0: by cp.async
-    alignas(64) CUtensorMap tm_x;   // blocked x  as [N*G*ncx][Rx*Wp][64], box {64, xb, 1}
-    alignas(64) CUtensorMap tm_dy;  // blocked dy as [N*G*ncy][Ho*Wp][64], box {64, TH*Wp, 1}
+    CUtensorMap tm_x;              // blocked x  as [N*G*ncx][Rx*Wp][64], box {64, xb, 1}
+    CUtensorMap tm_dy;             // blocked dy as [N*G*ncy][Ho*Wp][64], box {64, TH*Wp, 1}
     int cta_per_cg;              // CTAs per (group, o tile, c tile): sum of the group split counts
     int grp_splits[kMaxJobs];    // split count of each job group
     int grp_cta0[kMaxJobs + 1];  // first CTA index of each job group within cta_per_cg
@@ -2150,6 +2150,113 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
         return GCONV_OK;
     }
     return GCONV_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------------------
+// Merged groups.  A layer whose groups hold too few channels for the kernels above (the
+// correlation kernels want 16 produced channels, the weight gradient 8 input and 16 output
+// channels a group) runs m consecutive groups as one group of m*C_in/G input and m*C_out/G
+// output channels whose weights are block-diagonal: zero between channels of different
+// original groups, so every output still sums over its own group only (exact zeros added in
+// fp32).  Channel c of a merged group is channel c of the layer, so x, y, gradOutput and dx
+// keep their layout: the forward and backward-data widen the weights into the workspace,
+// and the weight gradient computes the merged group's full blocks and keeps the diagonal
+// ones.  The tensor cores do m times the useful MACs, which these layers can afford: at 8
+// channels a group they do 144 FLOP per output element against 6 bytes moved, far below
+// the tensor-core ridge.  m is the largest divisor of G that keeps both merged sides within
+// one 64-channel chunk.
+namespace {
+
+Geom merged_groups(const Geom &g, int m)
+{
+    Geom d = g;
+    d.G = g.G / m;
+    d.Cgi = g.Cgi * m;
+    d.Cgo = g.Cgo * m;
+    return d;
+}
+
+size_t merged_extra_bytes(const Geom &g, int m, gconv_pass pass)
+{
+    const size_t elems = (size_t)g.Cout * g.Cgi * m * g.kH * g.kW;
+    return elems * (pass == GCONV_PASS_BWD_WEIGHT ? sizeof(float) : sizeof(__nv_bfloat16));
+}
+
+// wd[co][ci][t] (the merged group's Cgi*m input channels) from w[co][i][t]: w where ci lies
+// in co's own original group (ci / Cgi == (co / Cgo) % m), zero elsewhere.
+__global__ void widen_weights_kernel(const __nv_bfloat16 *__restrict__ w, __nv_bfloat16 *__restrict__ wd,
+                                     int64_t total, int Cgo, int Cgi, int m, int KK)
+{
+    const int CgiM = Cgi * m;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total; idx += (int64_t)gridDim.x * blockDim.x) {
+        const int t = (int)(idx % KK);
+        const int64_t r = idx / KK;
+        const int ci = (int)(r % CgiM);
+        const int64_t co = r / CgiM;
+        const int own = (int)((co / Cgo) % m), blk = ci / Cgi;
+        wd[idx] = blk == own ? w[(co * Cgi + (ci - blk * Cgi)) * KK + t] : __float2bfloat16_rn(0.f);
+    }
+}
+
+// dw[co][i][t] = dwd[co][own * Cgi + i][t]: the diagonal blocks of the merged weight gradient.
+__global__ void diagonal_weights_kernel(const float *__restrict__ dwd, float *__restrict__ dw, int64_t total, int Cgo,
+                                        int Cgi, int m, int KK)
+{
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total; idx += (int64_t)gridDim.x * blockDim.x) {
+        const int t = (int)(idx % KK);
+        const int64_t r = idx / KK;
+        const int i = (int)(r % Cgi);
+        const int64_t co = r / Cgi;
+        const int own = (int)((co / Cgo) % m);
+        dw[idx] = dwd[(co * Cgi * m + own * Cgi + i) * KK + t];
+    }
+}
+
+}  // namespace
+
+bool tc_merged_plan(const Geom &g, gconv_pass pass, Plan *p)
+{
+    if (pass != GCONV_PASS_FWD && pass != GCONV_PASS_BWD_DATA && pass != GCONV_PASS_BWD_WEIGHT) return false;
+    const int side = std::max(g.Cgi, g.Cgo);
+    for (int m = std::min(g.G, 64 / side); m >= 2; --m) {
+        if (g.G % m) continue;
+        Plan q{};
+        if (!tc_igemm_plan(merged_groups(g, m), pass, &q)) continue;
+        *p = q;
+        p->merge = m;
+        p->merge_ws = q.ws_bytes;
+        p->ws_bytes = (q.ws_bytes + 255) / 256 * 256 + merged_extra_bytes(g, m, pass);
+        p->launches = q.launches + 1;   // the weight widening, or the diagonal extraction
+        return true;
+    }
+    return false;
+}
+
+gconv_status tc_merged_launch(const Geom &g, const Plan &p, gconv_pass pass, const void *a, const void *b,
+                              const void *bias, float *out, float *db, void *ws, cudaStream_t s, bool *db_done)
+{
+    *db_done = false;
+    const int m = p.merge;
+    if (m < 2 || g.G % m) return GCONV_ERR_UNSUPPORTED;
+    const Geom d = merged_groups(g, m);
+    void *extra = static_cast<uint8_t *>(ws) + (p.merge_ws + 255) / 256 * 256;
+    const int KK = g.kH * g.kW;
+    const int64_t total_wide = (int64_t)g.Cout * g.Cgi * m * KK;
+    const int blocks_wide = (int)std::min<int64_t>((total_wide + 255) / 256, (int64_t)num_sms() * 8);
+    if (pass == GCONV_PASS_FWD || pass == GCONV_PASS_BWD_DATA) {
+        __nv_bfloat16 *wd = static_cast<__nv_bfloat16 *>(extra);
+        widen_weights_kernel<<<blocks_wide, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(b), wd, total_wide, g.Cgo,
+                                                         g.Cgi, m, KK);
+        return tc_igemm_launch(d, p, pass, a, wd, bias, out, nullptr, ws, s, db_done);
+    }
+    if (pass != GCONV_PASS_BWD_WEIGHT) return GCONV_ERR_UNSUPPORTED;
+    float *dwd = static_cast<float *>(extra);
+    const gconv_status st = tc_igemm_launch(d, p, pass, a, b, bias, dwd, db, ws, s, db_done);
+    if (st != GCONV_OK) return st;
+    const int64_t total = (int64_t)g.Cout * g.Cgi * KK;
+    const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms() * 8);
+    diagonal_weights_kernel<<<blocks, 256, 0, s>>>(dwd, out, total, g.Cgo, g.Cgi, m, KK);
+    return GCONV_OK;
 }
 
 }  // namespace gconv

@@ -383,10 +383,11 @@ def test_tensor_core_edges_full(dev, oracle_mod, geom, paths, untouched):
 
 
 # The thresholds of the tensor-core families: a group with 8 input and 16 output channels
-# (forward and weight gradient on tensor cores, backward-data on CUDA cores), and the mirror.
+# (forward and weight gradient on the kernels directly, backward-data on two merged groups),
+# and the mirror.
 THRESHOLDS = [
-    ((2, 16, 10, 10, 32, 3, 3, 1, 1, 1, 1, 1, 1, 2), (TC, CC, TC, RD)),
-    ((2, 32, 10, 10, 16, 3, 3, 1, 1, 1, 1, 1, 1, 2), (CC, TC, CC, RD)),
+    ((2, 16, 10, 10, 32, 3, 3, 1, 1, 1, 1, 1, 1, 2), (TC, TC, TC, RD)),
+    ((2, 32, 10, 10, 16, 3, 3, 1, 1, 1, 1, 1, 1, 2), (TC, TC, TC, RD)),
 ]
 
 
@@ -396,6 +397,46 @@ def test_tensor_core_thresholds_full(dev, oracle_mod, geom, paths):
     wk = wl.Workload("threshold", geom, "bf16", w=("normal", 0.2))
     x, w, b, dy = wl.make_inputs(wk, seed=sum(geom) * 17)
     full_compare(geom, "bf16", x, w, b, dy, dev, oracle_mod, label=f"threshold {geom}")
+
+
+# Groups too thin for the tensor-core kernels that the thin-plane kernels do not take (8
+# channels a side, mixed 8/4 and 8/16, 1x1, stride 2, 5x5): consecutive groups merged into
+# one with block-diagonal weights, whole tensors against the oracle.
+MERGED = [
+    (2, 64, 13, 12, 64, 3, 3, 1, 1, 1, 1, 1, 1, 8),          # 8 a side: all 8 groups as one
+    (2, 64, 14, 13, 64, 3, 3, 2, 1, 1, 1, 1, 1, 8),          # stride 2
+    (2, 48, 11, 11, 24, 3, 3, 1, 1, 1, 1, 1, 1, 6),          # 8 in, 4 out: 6 groups as one
+    (2, 24, 9, 10, 48, 5, 5, 1, 2, 2, 2, 2, 1, 3),           # 8 in, 16 out: backward-data merged
+    (2, 64, 9, 9, 64, 1, 1, 1, 0, 0, 0, 0, 1, 8),            # 1x1
+    (3, 128, 10, 11, 128, 3, 3, 1, 0, 2, 1, 1, 1, 16),       # 2 merged groups, asymmetric pads
+]
+
+
+@pytest.mark.parametrize("geom", MERGED)
+def test_merged_groups_full(dev, oracle_mod, geom):
+    assert_paths(geom, "bf16", (TC, TC, TC, RD))
+    wk = wl.Workload("merged", geom, "bf16", w=("normal", 0.2))
+    x, w, b, dy = wl.make_inputs(wk, seed=sum(geom) * 23)
+    full_compare(geom, "bf16", x, w, b, dy, dev, oracle_mod, label=f"merged {geom}")
+
+
+def test_merged_groups_forced_on_thin_layer(dev, oracle_mod):
+    """A 4-channel-group layer the thin-plane kernels normally serve, forced onto the
+    tensor-core family: 8 groups merged into one of 32 channels."""
+    geom = (2, 32, 12, 12, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8)
+    assert_paths(geom, "bf16", (CC, CC, CC, RD))
+    B.gconv_debug_force_path(B.PATH_TC_IGEMM)
+    try:
+        assert tuple(gc.gconv_plan(geom, B.GCONV_BF16, p)[0] for p in range(3)) == (TC, TC, TC)
+        wk = wl.Workload("merged_forced", geom, "bf16", w=("normal", 0.2))
+        x, w, b, dy = wl.make_inputs(wk, seed=97)
+        got = run_gpu(geom, x, w, b, dy, dev, passes=("y", "dx", "dw"))
+    finally:
+        B.gconv_debug_force_path(B.PATH_NONE)
+    tol = TOL["bf16"]
+    check("forced merged y", got["y"].numpy(), oracle_mod.fwd(geom, f64(x), f64(w), f64(b)), tol)
+    check("forced merged dx", got["dx"].numpy(), oracle_mod.bwd_data(geom, f64(dy), f64(w)), tol)
+    check("forced merged dw", got["dw"].numpy(), oracle_mod.bwd_weight(geom, f64(x), f64(dy)), tol)
 
 
 # Per-axis stride and dilation (the 16-integer geometry of the *_ex entry points): whole
@@ -439,6 +480,8 @@ def test_per_axis_random_sweep(dev, oracle_mod):
     (2, 64, 19, 16, 64, 3, 3, 2, 0, 1, 0, 1, 1, 1),         # stride-2 tensor cores: separate reduction
     (2, 32, 12, 12, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8),         # CUDA-core weight gradient
     (2, 128, 6, 6, 96, 6, 6, 1, 0, 0, 0, 0, 1, 1),          # 1x1 output
+    (2, 64, 13, 12, 64, 3, 3, 1, 1, 1, 1, 1, 1, 8),         # merged groups, 64 channels: separate reduction
+    (2, 48, 11, 11, 24, 3, 3, 1, 1, 1, 1, 1, 1, 6),         # merged groups, 48 channels: bias column
 ])
 def test_weight_gradient_with_bias_gradient(dev, oracle_mod, geom):
     """gconv_bwd_weight_ex with db: dw and db from one call.  dw equals the separate entry
@@ -468,6 +511,7 @@ BF16_OUT = [
     ((2, 128, 6, 6, 96, 6, 6, 1, 0, 0, 0, 0, 1, 1), (FC, FC)),      # 1x1 output, two images
     ((64, 64, 4, 4, 128, 4, 4, 1, 0, 0, 0, 0, 1, 1), (FC, FC)),     # FC GEMM
     ((2, 32, 12, 12, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8), (CC, CC)),     # thin 3x3
+    ((2, 64, 13, 12, 64, 3, 3, 1, 1, 1, 1, 1, 1, 8), (TC, TC)),     # merged groups
     ((2, 12, 13, 12, 12, 3, 3, 2, 1, 1, 1, 1, 1, 1, 1, 3), (CC, CC)),   # CUDA-core tiles, per-axis stride
     ((1, 8, 9, 7, 12, 1, 1, 1, 0, 0, 0, 0, 1, 1), (CC, CC)),        # 1x1, 8 channels
 ]

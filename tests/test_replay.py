@@ -55,6 +55,13 @@ STRIDE1 = [
     # per-axis dilation (16 integers: ..., s_h, s_w, pads, d_h, d_w, G)
     (2, 32, 11, 13, 32, 3, 3, 1, 1, 2, 2, 1, 1, 1, 2, 1),
     (2, 32, 12, 9, 64, 3, 5, 1, 1, 1, 1, 2, 2, 2, 1, 2),
+    # merged groups: the geometry the kernels see when consecutive thin groups run as one
+    # (8 groups of 8 channels as one of 64; 6 groups of 8/4 as one of 48/24; 16 groups as 2)
+    (2, 64, 13, 12, 64, 3, 3, 1, 1, 1, 1, 1, 1, 1),
+    (2, 48, 11, 11, 24, 3, 3, 1, 1, 1, 1, 1, 1, 1),
+    (2, 24, 9, 10, 48, 5, 5, 1, 2, 2, 2, 2, 1, 1),
+    (3, 128, 10, 11, 128, 3, 3, 1, 0, 2, 1, 1, 1, 2),
+    (2, 256, 28, 28, 256, 3, 3, 1, 1, 1, 1, 1, 1, 4),      # ResNeXt 256x28, 8 channels a group, merged
 ]
 
 
@@ -78,6 +85,9 @@ STRIDE2 = [
     # per-axis strides: one stride-2 axis and one stride-1 axis (two phase planes)
     (2, 32, 13, 12, 32, 3, 3, 2, 1, 1, 1, 1, 1, 1, 1, 1),
     (2, 32, 12, 15, 64, 3, 3, 1, 2, 1, 0, 1, 1, 1, 2, 1),
+    # merged groups (see above)
+    (2, 64, 14, 13, 64, 3, 3, 2, 1, 1, 1, 1, 1, 1),
+    (2, 256, 56, 56, 256, 3, 3, 2, 1, 1, 1, 1, 1, 4),      # ResNeXt 256x56 stride 2, merged
 ]
 
 
