@@ -52,7 +52,8 @@ struct ThinParams {
     int TH, n_strip;     // output rows per block, strips per plane
     int bwd;             // backward-data
     int nchunk, per_chunk;   // weight gradient: image chunks, images per chunk
-    int slide, cpl;          // sliding-window form, outputs per thread
+    int tile, cpl;           // register-tile form; outputs per thread (staged-window form)
+    int pitch;               // register-tile form: elements per staged row
 };
 
 // Copies n elements src[0..n) (global) to dst[0..n) (shared) with 16-byte loads where the
@@ -369,164 +370,21 @@ __global__ void thin_wgrad_finish_kernel(const float *__restrict__ part, int G, 
 }
 
 // ---------------------------------------------------------------------------
-// Sliding-window forms (stride 1, rows of 16-byte multiples, at most 32*CPL columns).
-// Rows are staged with zero borders: staged row j of plane c holds source row lo + j at
-// columns [kPadE, kPadE + IW) of a row of `pitch` elements (zeros around it and for rows
-// outside the source), so the compute reads need no bounds tests.  A warp walks a run of
-// produced rows; lane l owns columns [l*CPL, l*CPL + CPL) and keeps, per input plane, the
-// three source rows of its current output row in registers: each step loads one new row
-// (one 4-, 8- or 16-byte shared-memory load per plane) and takes the two neighbouring
-// columns from the adjacent lanes with shuffles.
+// Register-tile forms (stride 1, source and gradOutput rows of 16-byte multiples).  Rows
+// are staged with zero borders: staged row j of plane c holds source row lo + j at columns
+// [PAD, PAD + IW) of a row of `pitch` elements, zeros around it and for rows outside the
+// source, so the compute reads need no bounds tests.  A thread owns 4 consecutive produced
+// columns [c0, c0 + 4) of a run of rows and slides a 3-row window down them: each step
+// loads one new staged row per input plane -- the 6 source columns c0 - pl .. c0 - pl + 5
+// its outputs read, straight from shared memory -- and does the 9 taps of its 4 outputs for
+// every output channel of the group.  The left pad pl (0, 1 or 2) is a template argument,
+// so the columns a window takes are fixed at compile time.  The block's threads split a
+// strip as (4-column chunk, run of rows), so narrow planes keep the lanes busy.  Blocks
+// walk their items persistently and double-buffer the staged rows: while a block computes
+// item k from one buffer, the 16-byte cp.async copies of item k + 1 land in the other.
 
 template <typename T> struct PadE { static constexpr int value = 16 / (int)sizeof(T); };
-
-// Zero-bordered staging of source rows [lo, lo + nrows) of CG planes (see above).  Thread
-// t copies 16-byte vectors t, t + 128, ... of the staged region; the (row, vector) position
-// advances incrementally (no divisions), four vectors loaded before any is stored.
-template <typename T>
-__device__ __forceinline__ void stage_padded(const T *__restrict__ src, int64_t plane, int CG, int IH, int IW,
-                                             int lo, int nrows, int pitch, T *stage)
-{
-    constexpr int PAD = PadE<T>::value;
-    const int vrow = pitch / PAD;                 // 16-byte vectors per staged row
-    const int vdata = IW / PAD;                   // of which hold source data: [1, 1 + vdata)
-    const int total_rows = CG * nrows;
-    const int total = total_rows * vrow;
-    const int step_r = kThinThreads / vrow, step_k = kThinThreads - step_r * vrow;
-    int row = threadIdx.x / vrow, k = threadIdx.x - row * vrow;
-    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    uint4 *dst = reinterpret_cast<uint4 *>(stage);
-    for (int i0 = threadIdx.x; i0 < total; i0 += 4 * kThinThreads) {
-        uint4 v[4];
-        int idx[4];
-        #pragma unroll
-        for (int u = 0; u < 4; ++u) {           // all loads first, then the stores
-            idx[u] = row * vrow + k;
-            v[u] = zero;
-            if (row < total_rows) {
-                const int c = row / nrows;     // one division per vector: planes are few
-                const int ih = lo + (row - c * nrows);
-                if (k >= 1 && k <= vdata && ih >= 0 && ih < IH)
-                    v[u] = __ldg(reinterpret_cast<const uint4 *>(src + c * plane + (int64_t)ih * IW) + (k - 1));
-            }
-            row += step_r;
-            k += step_k;
-            if (k >= vrow) { k -= vrow; ++row; }
-        }
-        #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (idx[u] < total) dst[idx[u]] = v[u];
-    }
-}
-
-// CPL consecutive staged values from element e (aligned to CPL elements), widened to fp32.
-template <typename T, int CPL>
-__device__ __forceinline__ void load_chunk(const T *p, float (&out)[CPL])
-{
-    if constexpr (sizeof(T) == 2 && CPL == 2) {
-        const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(p);
-        out[0] = __low2float(v);
-        out[1] = __high2float(v);
-    } else if constexpr (sizeof(T) == 2 && CPL == 4) {
-        const uint2 u = *reinterpret_cast<const uint2 *>(p);
-        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
-        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
-        out[0] = __low2float(a); out[1] = __high2float(a); out[2] = __low2float(b); out[3] = __high2float(b);
-    } else if constexpr (sizeof(T) == 4 && CPL == 2) {
-        const float2 v = *reinterpret_cast<const float2 *>(p);
-        out[0] = v.x; out[1] = v.y;
-    } else {
-        const float4 v = *reinterpret_cast<const float4 *>(p);
-        out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
-    }
-}
-
-// One window row: source columns c0 - pl + k, k < CPL + 2, from the lane's own chunk and its
-// neighbours' (zero beyond lane 0 and lane 31, whose halo columns lie outside the source).
-template <int CPL>
-__device__ __forceinline__ void window_row(const float (&own)[CPL], int pl, int lane, float (&win)[CPL + 2])
-{
-    const float l1 = __shfl_up_sync(0xffffffffu, own[CPL - 1], 1);
-    const float l2 = __shfl_up_sync(0xffffffffu, own[CPL - 2], 1);
-    const float r0 = __shfl_down_sync(0xffffffffu, own[0], 1);
-    const float r1 = __shfl_down_sync(0xffffffffu, own[1], 1);
-    const float L1 = lane > 0 ? l1 : 0.f, L2 = lane > 0 ? l2 : 0.f;
-    const float R0 = lane < 31 ? r0 : 0.f, R1 = lane < 31 ? r1 : 0.f;
-    // pl = 1: [L1, own..., R0]; pl = 0: [own..., R0, R1]; pl = 2: [L2, L1, own...]
-    if (pl == 1) {
-        win[0] = L1;
-        #pragma unroll
-        for (int j = 0; j < CPL; ++j) win[1 + j] = own[j];
-        win[CPL + 1] = R0;
-    } else if (pl == 0) {
-        #pragma unroll
-        for (int j = 0; j < CPL; ++j) win[j] = own[j];
-        win[CPL] = R0;
-        win[CPL + 1] = R1;
-    } else {
-        win[0] = L2;
-        win[1] = L1;
-        #pragma unroll
-        for (int j = 0; j < CPL; ++j) win[2 + j] = own[j];
-    }
-}
-
-template <int CPL>
-__device__ __forceinline__ void store_chunk(float *out, int64_t i, const float (&v)[CPL], int nvalid, int bf16)
-{
-    if (nvalid == CPL && (i & (CPL - 1)) == 0) {
-        if constexpr (CPL == 4) {
-            store_out4(out, i, v[0], v[1], v[2], v[3], bf16);
-            return;
-        } else {
-            if (bf16) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(v[0], v[1]);
-                *reinterpret_cast<__nv_bfloat162 *>(reinterpret_cast<__nv_bfloat16 *>(out) + i) = h;
-            } else {
-                *reinterpret_cast<float2 *>(out + i) = make_float2(v[0], v[1]);
-            }
-            return;
-        }
-    }
-    #pragma unroll
-    for (int j = 0; j < CPL; ++j)
-        if (j < nvalid) store_out(out, i + j, v[j], bf16);
-}
-
-// One gradOutput row of the sliding weight gradient: x row r + 2 of every input plane into
-// window slot C, then acc[ci*9 + tap] += dy[j] * x window (slots A, B, C = rows r..r+2),
-// and the bias accumulator += dy[j].
-template <typename T, int CG, int CPL, int A, int Bs, int C>
-__device__ __forceinline__ void wgrad_step(float (&win)[CG][3][CPL + 2], const T *xcol, const T *ycol, int xrows,
-                                           int pitch, int r, int pl, int lane, float (&acc)[CG * 9 + 1])
-{
-    #pragma unroll
-    for (int ci = 0; ci < CG; ++ci) {
-        float own[CPL];
-        load_chunk<T, CPL>(xcol + (ci * xrows + r + 2) * pitch, own);
-        window_row<CPL>(own, pl, lane, win[ci][C]);
-    }
-    float d[CPL];
-    load_chunk<T, CPL>(ycol + r * pitch, d);
-    #pragma unroll
-    for (int j = 0; j < CPL; ++j) acc[CG * 9] += d[j];
-    #pragma unroll
-    for (int ci = 0; ci < CG; ++ci)
-        #pragma unroll
-        for (int bb = 0; bb < 3; ++bb)
-            #pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                acc[ci * 9 + 0 + bb] = fmaf(d[j], win[ci][A][j + bb], acc[ci * 9 + 0 + bb]);
-                acc[ci * 9 + 3 + bb] = fmaf(d[j], win[ci][Bs][j + bb], acc[ci * 9 + 3 + bb]);
-                acc[ci * 9 + 6 + bb] = fmaf(d[j], win[ci][C][j + bb], acc[ci * 9 + 6 + bb]);
-            }
-}
-
-// ---------------------------------------------------------------------------
-// Pipelined forms (stride 1, the sliding window's row and column limits).  A block walks
-// work items persistently and double-buffers their staged rows: while it computes item k
-// from one buffer, the 16-byte cp.async copies of item k+1 (zero-filled where a row or
-// column lies outside the source) land in the other, so load latency is not paid per item.
+constexpr int kTileCols = 4;
 
 // Staged-row copies of rows [lo, lo + nrows) of CG planes into a zero-bordered buffer of
 // CG*nrows_max rows (cp.async; vectors outside the source are zero-filled).
@@ -554,69 +412,178 @@ __device__ __forceinline__ void issue_rows(const T *__restrict__ src, int64_t pl
     }
 }
 
-// One produced row for every output channel of the group: source row r + 2 of each input
-// plane into window slot C, then the 3 x 3 taps over slots A, B, C.
-template <typename T, int CG, int CPL, int A, int Bs, int C>
-__device__ __forceinline__ void pipe_step(float (&win)[CG][3][CPL + 2], const T *col, int nrows_max, int pitch, int r,
-                                          int pl, int lane, const float *wsm, const float (&bias)[CG],
-                                          float (&acc)[CG][CPL])
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+// Source columns c0 - PL + k, k < 6, of one staged row; `r` points at the staged element of
+// column c0 (c0 a multiple of 4: r is 8-byte aligned for bf16, 16-byte aligned for fp32).
+template <int PL>
+__device__ __forceinline__ void load_window(const __nv_bfloat16 *r, float (&v)[6])
+{
+    const uint2 m = *reinterpret_cast<const uint2 *>(r);
+    const float m0 = bf_lo(m.x), m1 = bf_hi(m.x), m2 = bf_lo(m.y), m3 = bf_hi(m.y);
+    if constexpr (PL == 0) {
+        const uint32_t e = *reinterpret_cast<const uint32_t *>(r + 4);
+        v[0] = m0; v[1] = m1; v[2] = m2; v[3] = m3; v[4] = bf_lo(e); v[5] = bf_hi(e);
+    } else if constexpr (PL == 1) {
+        const uint32_t l = *reinterpret_cast<const uint32_t *>(r - 2);
+        const uint32_t e = *reinterpret_cast<const uint32_t *>(r + 4);
+        v[0] = bf_hi(l); v[1] = m0; v[2] = m1; v[3] = m2; v[4] = m3; v[5] = bf_lo(e);
+    } else {
+        const uint32_t l = *reinterpret_cast<const uint32_t *>(r - 2);
+        v[0] = bf_lo(l); v[1] = bf_hi(l); v[2] = m0; v[3] = m1; v[4] = m2; v[5] = m3;
+    }
+}
+
+template <int PL>
+__device__ __forceinline__ void load_window(const float *r, float (&v)[6])
+{
+    const float4 m = *reinterpret_cast<const float4 *>(r);
+    if constexpr (PL == 0) {
+        const float2 e = *reinterpret_cast<const float2 *>(r + 4);
+        v[0] = m.x; v[1] = m.y; v[2] = m.z; v[3] = m.w; v[4] = e.x; v[5] = e.y;
+    } else if constexpr (PL == 1) {
+        const float2 l = *reinterpret_cast<const float2 *>(r - 2);
+        const float2 e = *reinterpret_cast<const float2 *>(r + 4);
+        v[0] = l.y; v[1] = m.x; v[2] = m.y; v[3] = m.z; v[4] = m.w; v[5] = e.x;
+    } else {
+        const float2 l = *reinterpret_cast<const float2 *>(r - 2);
+        v[0] = l.x; v[1] = l.y; v[2] = m.x; v[3] = m.y; v[4] = m.z; v[5] = m.w;
+    }
+}
+
+// Staged columns c0 .. c0 + 3.
+__device__ __forceinline__ void load4(const __nv_bfloat16 *r, float (&d)[4])
+{
+    const uint2 m = *reinterpret_cast<const uint2 *>(r);
+    d[0] = bf_lo(m.x); d[1] = bf_hi(m.x); d[2] = bf_lo(m.y); d[3] = bf_hi(m.y);
+}
+
+__device__ __forceinline__ void load4(const float *r, float (&d)[4])
+{
+    const float4 m = *reinterpret_cast<const float4 *>(r);
+    d[0] = m.x; d[1] = m.y; d[2] = m.z; d[3] = m.w;
+}
+
+// The group's weights in the orientation of the pass, in registers (one or two channels a
+// group; four channels keep them in shared memory, see tile_row4).
+template <int CG> struct TileWeights {
+    float r[CG * CG * 9];
+};
+
+// One produced row for every output channel of the group (one or two channels a group):
+// staged row r + 2 of each input plane into window slot C, then the 3 x 3 taps over slots
+// A (row r), Bs (r + 1), C (r + 2).
+template <typename T, int CG, int PL, int A, int Bs, int C>
+__device__ __forceinline__ void tile_step(float (&win)[CG][3][6], const T *col, int nrows_max, int pitch, int r,
+                                          const TileWeights<CG> &wr, const float (&bias)[CG],
+                                          float (&acc)[CG][kTileCols])
 {
     #pragma unroll
-    for (int ci = 0; ci < CG; ++ci) {
-        float own[CPL];
-        load_chunk<T, CPL>(col + (ci * nrows_max + r + 2) * pitch, own);
-        window_row<CPL>(own, pl, lane, win[ci][C]);
-    }
+    for (int ci = 0; ci < CG; ++ci) load_window<PL>(col + (ci * nrows_max + r + 2) * pitch, win[ci][C]);
     #pragma unroll
     for (int o = 0; o < CG; ++o) {
         #pragma unroll
-        for (int j = 0; j < CPL; ++j) acc[o][j] = bias[o];
+        for (int j = 0; j < kTileCols; ++j) acc[o][j] = bias[o];
         #pragma unroll
-        for (int ci = 0; ci < CG; ++ci) {
-            const float4 *w4 = reinterpret_cast<const float4 *>(wsm + (o * CG + ci) * 12);
-            const float4 w0 = w4[0], w1 = w4[1], w2 = w4[2];
-            const float wv[9] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w, w2.x};
+        for (int ci = 0; ci < CG; ++ci)
             #pragma unroll
-            for (int bb = 0; bb < 3; ++bb)
+            for (int a = 0; a < 3; ++a) {
+                const int s = a == 0 ? A : (a == 1 ? Bs : C);
+                const float w0 = wr.r[(o * CG + ci) * 9 + a * 3];
+                const float w1 = wr.r[(o * CG + ci) * 9 + a * 3 + 1];
+                const float w2 = wr.r[(o * CG + ci) * 9 + a * 3 + 2];
                 #pragma unroll
-                for (int j = 0; j < CPL; ++j) {
-                    acc[o][j] = fmaf(wv[0 + bb], win[ci][A][j + bb], acc[o][j]);
-                    acc[o][j] = fmaf(wv[3 + bb], win[ci][Bs][j + bb], acc[o][j]);
-                    acc[o][j] = fmaf(wv[6 + bb], win[ci][C][j + bb], acc[o][j]);
+                for (int j = 0; j < kTileCols; ++j) {
+                    acc[o][j] = fmaf(w0, win[ci][s][j], acc[o][j]);
+                    acc[o][j] = fmaf(w1, win[ci][s][j + 1], acc[o][j]);
+                    acc[o][j] = fmaf(w2, win[ci][s][j + 2], acc[o][j]);
                 }
+            }
+    }
+}
+
+// One produced row of a four-channel group: the three staged rows of each input plane in
+// turn (a sliding window over four planes would hold 72 values next to 16 sums), each tap
+// one float4 of the four output channels' weights, wq[(ci*9 + tap)*4 + o], read where it
+// is used (hoisted out of the row loop, 144 weights would not fit in registers).
+template <typename T, int PL>
+__device__ __forceinline__ void tile_row4(const T *col, int nrows_max, int pitch, int r, const float *wq,
+                                          const float (&bias)[4], float (&acc)[4][kTileCols])
+{
+    asm volatile("" ::: "memory");
+    #pragma unroll
+    for (int o = 0; o < 4; ++o)
+        #pragma unroll
+        for (int j = 0; j < kTileCols; ++j) acc[o][j] = bias[o];
+    #pragma unroll
+    for (int ci = 0; ci < 4; ++ci) {
+        float win[3][6];
+        #pragma unroll
+        for (int a = 0; a < 3; ++a) load_window<PL>(col + (ci * nrows_max + r + a) * pitch, win[a]);
+        #pragma unroll
+        for (int a = 0; a < 3; ++a)
+            #pragma unroll
+            for (int bb = 0; bb < 3; ++bb) {
+                const float4 w4 = *reinterpret_cast<const float4 *>(wq + (ci * 9 + a * 3 + bb) * 4);
+                #pragma unroll
+                for (int j = 0; j < kTileCols; ++j) {
+                    const float v = win[a][j + bb];
+                    acc[0][j] = fmaf(w4.x, v, acc[0][j]);
+                    acc[1][j] = fmaf(w4.y, v, acc[1][j]);
+                    acc[2][j] = fmaf(w4.z, v, acc[2][j]);
+                    acc[3][j] = fmaf(w4.w, v, acc[3][j]);
+                }
+            }
+    }
+}
+
+template <int CG>
+__device__ __forceinline__ void tile_store(float *out, int64_t i, int64_t out_plane, const float (&acc)[CG][kTileCols],
+                                           int ncol, bool vec, int bf16)
+{
+    #pragma unroll
+    for (int o = 0; o < CG; ++o) {
+        const int64_t oi = i + o * out_plane;
+        if (vec) {
+            store_out4(out, oi, acc[o][0], acc[o][1], acc[o][2], acc[o][3], bf16);
+        } else {
+            #pragma unroll
+            for (int j = 0; j < kTileCols; ++j)
+                if (j < ncol) store_out(out, oi + j, acc[o][j], bf16);
         }
     }
 }
 
-template <int CG, int CPL>
-__device__ __forceinline__ void pipe_store(float *out, int64_t base, int64_t out_plane, const float (&acc)[CG][CPL],
-                                           int nvalid, int bf16)
-{
-    #pragma unroll
-    for (int o = 0; o < CG; ++o) store_chunk<CPL>(out, base + o * out_plane, acc[o], nvalid, bf16);
-}
-
-// Forward / stride-1 backward-data, pipelined.  Item = (image, group, strip); the four
-// warps split the strip's produced rows, each thread produces CPL columns of every output
-// channel of the group (weights Wt[o][i][tap] from shared memory, per item).
-template <typename T, int CG, int CPL>
+// Forward / stride-1 backward-data.  Item = (image, group, strip of TH produced rows).
+// Produced value (o, r, c) = sum over input planes i, taps (a, b) of
+//   Wt[o][i][a][b] * src[i][r - pt + a][c - pl + b]
+// with Wt = w (forward) or the mirrored, transposed weights (backward-data, whose pads are
+// 2 - pt, 2 - pl).  The weights are staged per item in shared memory and, for CG <= 2,
+// copied into registers.
+template <typename T, int CG, int PL>
 __global__ void __launch_bounds__(kThinThreads)
-thin_pipe_kernel(const __grid_constant__ ThinParams p)
+thin_tile_kernel(const __grid_constant__ ThinParams p)
 {
     extern __shared__ __align__(16) unsigned char thin_sm[];
-    __shared__ __align__(16) float ws[2][CG * CG * 12];   // [out][in][12]: 9 taps, 3 pad
+    __shared__ __align__(16) float ws[2][CG * CG * 9];   // per buffer: [o][ci][tap], four channels [ci][tap][o]
     constexpr int PAD = PadE<T>::value;
     constexpr int NW = CG * CG * 9;
     constexpr int WPT = (NW + kThinThreads - 1) / kThinThreads;   // weights loaded per thread
     const T *W = static_cast<const T *>(p.w);
     const T *src = static_cast<const T *>(p.src);
-    const int pitch = PAD + 32 * CPL + PAD;
+    const int pitch = p.pitch;
     const int nrows_max = p.TH + 2;
     const int buf_elems = CG * nrows_max * pitch;
     T *bufs = reinterpret_cast<T *>(thin_sm);
     const int64_t plane = (int64_t)p.IH * p.IW;
     const int items = p.N * p.G * p.n_strip;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nch = (p.OW + kTileCols - 1) / kTileCols;
+    const int nsub = kThinThreads / nch;
+    const int chunk = threadIdx.x % nch, sub = threadIdx.x / nch;
+    const int c0 = chunk * kTileCols;
+    const int ncol = min(kTileCols, p.OW - c0);
+    const bool vec = (p.OW % kTileCols) == 0;   // whole chunks; y / dx and its planes 16-byte aligned
     auto issue = [&](int it, int b, float (&wv)[WPT]) {
         int t = it;
         const int strip = t % p.n_strip; t /= p.n_strip;
@@ -651,7 +618,14 @@ thin_pipe_kernel(const __grid_constant__ ThinParams p)
         #pragma unroll
         for (int u = 0; u < WPT; ++u) {
             const int i = threadIdx.x + u * kThinThreads;
-            if (i < NW) ws[b][(i / 9) * 12 + i % 9] = wcur[u];
+            if (i < NW) {
+                if constexpr (CG == 4) {   // [ci][tap][o]
+                    const int o = i / 36, rem = i - o * 36;
+                    ws[b][rem * 4 + o] = wcur[u];
+                } else {                   // [o][ci][tap]
+                    ws[b][i] = wcur[u];
+                }
+            }
         }
         ptx::cp_async_wait_group<1>();   // this item's rows have landed (the next item's may not)
         __syncthreads();
@@ -661,47 +635,54 @@ thin_pipe_kernel(const __grid_constant__ ThinParams p)
         const int n = t / p.G;
         const int r0 = strip * p.TH;
         const int rows = min(p.TH, p.OH - r0);
-        const int q = (rows + 3) >> 2;
-        const int ra = warp * q, rb = min(rows, ra + q);
-        if (ra < rb) {
+        const int sr = (rows + nsub - 1) / nsub;
+        const int ra = sub * sr, rb = min(rows, ra + sr);
+        if (sub < nsub && ra < rb) {
+            const float *wsm = ws[b];
             float bias[CG];
             #pragma unroll
             for (int o = 0; o < CG; ++o) bias[o] = (p.bias && !p.bwd) ? to_f(static_cast<const T *>(p.bias)[g * CG + o]) : 0.f;
-            const int c0 = lane * CPL;
-            const int nvalid = min(CPL, max(0, p.OW - c0));
             const int64_t out_plane = (int64_t)p.OH * p.OW;
-            const int64_t obase = ((int64_t)n * p.G + g) * CG * out_plane + c0;
+            int64_t oi = ((int64_t)n * p.G + g) * CG * out_plane + (int64_t)(r0 + ra) * p.OW + c0;
             const T *col = bufs + b * buf_elems + PAD + c0;
-            const float *wsm = ws[b];
-            float win[CG][3][CPL + 2];
-            #pragma unroll
-            for (int ci = 0; ci < CG; ++ci)
-                #pragma unroll
-                for (int a = 0; a < 2; ++a) {
-                    float own[CPL];
-                    load_chunk<T, CPL>(col + (ci * nrows_max + ra + a) * pitch, own);
-                    window_row<CPL>(own, p.pl, lane, win[ci][a]);
+            float acc[CG][kTileCols];
+            if constexpr (CG == 4) {
+                for (int r = ra; r < rb; ++r) {
+                    tile_row4<T, PL>(col, nrows_max, pitch, r, wsm, bias, acc);
+                    tile_store<CG>(p.out, oi, out_plane, acc, ncol, vec, p.out_bf16);
+                    oi += p.OW;
                 }
-            float acc[CG][CPL];
-            int r = ra;
-            for (; r + 3 <= rb; r += 3) {
-                pipe_step<T, CG, CPL, 0, 1, 2>(win, col, nrows_max, pitch, r, p.pl, lane, wsm, bias, acc);
-                if (nvalid > 0) pipe_store<CG, CPL>(p.out, obase + (int64_t)(r0 + r) * p.OW, out_plane, acc, nvalid, p.out_bf16);
-                pipe_step<T, CG, CPL, 1, 2, 0>(win, col, nrows_max, pitch, r + 1, p.pl, lane, wsm, bias, acc);
-                if (nvalid > 0)
-                    pipe_store<CG, CPL>(p.out, obase + (int64_t)(r0 + r + 1) * p.OW, out_plane, acc, nvalid, p.out_bf16);
-                pipe_step<T, CG, CPL, 2, 0, 1>(win, col, nrows_max, pitch, r + 2, p.pl, lane, wsm, bias, acc);
-                if (nvalid > 0)
-                    pipe_store<CG, CPL>(p.out, obase + (int64_t)(r0 + r + 2) * p.OW, out_plane, acc, nvalid, p.out_bf16);
-            }
-            if (r < rb) {
-                pipe_step<T, CG, CPL, 0, 1, 2>(win, col, nrows_max, pitch, r, p.pl, lane, wsm, bias, acc);
-                if (nvalid > 0) pipe_store<CG, CPL>(p.out, obase + (int64_t)(r0 + r) * p.OW, out_plane, acc, nvalid, p.out_bf16);
-            }
-            if (r + 1 < rb) {
-                pipe_step<T, CG, CPL, 1, 2, 0>(win, col, nrows_max, pitch, r + 1, p.pl, lane, wsm, bias, acc);
-                if (nvalid > 0)
-                    pipe_store<CG, CPL>(p.out, obase + (int64_t)(r0 + r + 1) * p.OW, out_plane, acc, nvalid, p.out_bf16);
+            } else {
+                TileWeights<CG> wr;
+                #pragma unroll
+                for (int i = 0; i < NW; ++i) wr.r[i] = wsm[i];
+                float win[CG][3][6];
+                #pragma unroll
+                for (int ci = 0; ci < CG; ++ci) {
+                    load_window<PL>(col + (ci * nrows_max + ra) * pitch, win[ci][0]);
+                    load_window<PL>(col + (ci * nrows_max + ra + 1) * pitch, win[ci][1]);
+                }
+                int r = ra;
+                for (; r + 3 <= rb; r += 3) {
+                    tile_step<T, CG, PL, 0, 1, 2>(win, col, nrows_max, pitch, r, wr, bias, acc);
+                    tile_store<CG>(p.out, oi, out_plane, acc, ncol, vec, p.out_bf16);
+                    oi += p.OW;
+                    tile_step<T, CG, PL, 1, 2, 0>(win, col, nrows_max, pitch, r + 1, wr, bias, acc);
+                    tile_store<CG>(p.out, oi, out_plane, acc, ncol, vec, p.out_bf16);
+                    oi += p.OW;
+                    tile_step<T, CG, PL, 2, 0, 1>(win, col, nrows_max, pitch, r + 2, wr, bias, acc);
+                    tile_store<CG>(p.out, oi, out_plane, acc, ncol, vec, p.out_bf16);
+                    oi += p.OW;
+                }
+                if (r < rb) {
+                    tile_step<T, CG, PL, 0, 1, 2>(win, col, nrows_max, pitch, r, wr, bias, acc);
+                    tile_store<CG>(p.out, oi, out_plane, acc, ncol, vec, p.out_bf16);
+                    oi += p.OW;
+                }
+                if (r + 1 < rb) {
+                    tile_step<T, CG, PL, 1, 2, 0>(win, col, nrows_max, pitch, r + 1, wr, bias, acc);
+                    tile_store<CG>(p.out, oi, out_plane, acc, ncol, vec, p.out_bf16);
+                }
             }
         }
         __syncthreads();   // buffer b and ws[b] are free again
@@ -709,36 +690,68 @@ thin_pipe_kernel(const __grid_constant__ ThinParams p)
     ptx::cp_async_wait_group<0>();   // nothing may land after the block exits
 }
 
-// Weight gradient + bias gradient, stride 1, pipelined over the images of a block's item
-// (group, image chunk, strip): x and gradOutput rows of image n+1 land while image n is
-// accumulated.  Warp w: output channel o = w % CG, its share w / CG of the strip's rows.
-template <typename T, int CG, int CPL>
+// One gradOutput row of the weight gradient: x row r + 2 of every input plane into window
+// slot C, then acc[ci*9 + a*3 + b] += sum over the 4 columns of dy * x window (slots A, Bs,
+// C = rows r .. r + 2), and the bias accumulator += the 4 gradOutput values.
+template <typename T, int CG, int PL, int A, int Bs, int C>
+__device__ __forceinline__ void tile_wgrad_step(float (&win)[CG][3][6], const T *xcol, const T *ycol, int xrows,
+                                                int pitch, int r, float (&acc)[CG * 9 + 1])
+{
+    #pragma unroll
+    for (int ci = 0; ci < CG; ++ci) load_window<PL>(xcol + (ci * xrows + r + 2) * pitch, win[ci][C]);
+    float d[kTileCols];
+    load4(ycol + r * pitch, d);
+    acc[CG * 9] += (d[0] + d[1]) + (d[2] + d[3]);
+    #pragma unroll
+    for (int ci = 0; ci < CG; ++ci)
+        #pragma unroll
+        for (int a = 0; a < 3; ++a) {
+            const int s = a == 0 ? A : (a == 1 ? Bs : C);
+            #pragma unroll
+            for (int bb = 0; bb < 3; ++bb)
+                #pragma unroll
+                for (int j = 0; j < kTileCols; ++j)
+                    acc[ci * 9 + a * 3 + bb] = fmaf(d[j], win[ci][s][j + bb], acc[ci * 9 + a * 3 + bb]);
+        }
+}
+
+// Weight gradient + bias gradient, stride 1.  Block: (group g, image chunk, strip of TH
+// gradOutput rows); the images of the chunk are double-buffered (x and gradOutput rows of
+// image n + 1 land while image n is accumulated).  Warp w serves output channel
+// o = w % CG; the 32 * 4 / CG threads of an output channel split the strip as (4-column
+// chunk, run of rows).  Lanes, then the warps of the same o, are added in a fixed order
+// into part[block][o][i*9 + tap] and part[block][o][CG*9] (the bias).
+template <typename T, int CG, int PL>
 __global__ void __launch_bounds__(kThinThreads)
-thin_pipe_wgrad_kernel(const __grid_constant__ ThinParams p)
+thin_tile_wgrad_kernel(const __grid_constant__ ThinParams p)
 {
     extern __shared__ __align__(16) unsigned char thin_sm[];
     constexpr int NA = CG * 9 + 1;
-    constexpr int WPO = 4 / CG;
+    constexpr int WPO = 4 / CG;   // warps per output channel
     constexpr int PAD = PadE<T>::value;
     __shared__ float red[4][NA];
     const T *X = static_cast<const T *>(p.src);
     const T *DY = static_cast<const T *>(p.dy);
     int b = blockIdx.x;
     const int strip = b % p.n_strip; b /= p.n_strip;
-    const int chunk = b % p.nchunk;
+    const int chunkn = b % p.nchunk;
     const int g = b / p.nchunk;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int o = warp % CG, part_w = warp / CG;
+    const int o = warp % CG;
+    const int t = (warp / CG) * 32 + lane;   // index among the threads of output channel o
+    const int nch = (p.OW + kTileCols - 1) / kTileCols;
+    const int nsub = (32 * WPO) / nch;
+    const int chunk = t % nch, sub = t / nch;
+    const int c0 = chunk * kTileCols;
     const int r0 = strip * p.TH;
     const int rows = min(p.TH, p.OH - r0);
-    const int pitch = PAD + 32 * CPL + PAD;
+    const int pitch = p.pitch;
     const int xrows_max = p.TH + 2, yrows_max = p.TH;
     const int buf_elems = CG * (xrows_max + yrows_max) * pitch;
     T *bufs = reinterpret_cast<T *>(thin_sm);
     const int64_t xplane = (int64_t)p.IH * p.IW, yplane = (int64_t)p.OH * p.OW;
-    const int q = (rows + WPO - 1) / WPO;
-    const int ra = part_w * q, rb = min(rows, ra + q);
-    const int c0 = lane * CPL;
+    const int sr = (rows + nsub - 1) / nsub;
+    const int ra = sub * sr, rb = min(rows, ra + sr);
     auto issue = [&](int n, int bi) {
         T *xs = bufs + bi * buf_elems;
         T *ys = xs + CG * xrows_max * pitch;
@@ -749,7 +762,7 @@ thin_pipe_wgrad_kernel(const __grid_constant__ ThinParams p)
     float acc[NA];
     #pragma unroll
     for (int k = 0; k < NA; ++k) acc[k] = 0.f;
-    const int n0 = chunk * p.per_chunk, n1 = min(p.N, n0 + p.per_chunk);
+    const int n0 = chunkn * p.per_chunk, n1 = min(p.N, n0 + p.per_chunk);
     if (n0 < n1) issue(n0, 0);
     ptx::cp_async_commit();
     for (int n = n0, bi = 0; n < n1; ++n, bi ^= 1) {
@@ -757,28 +770,25 @@ thin_pipe_wgrad_kernel(const __grid_constant__ ThinParams p)
         ptx::cp_async_commit();
         ptx::cp_async_wait_group<1>();
         __syncthreads();
-        if (ra < rb) {
+        if (sub < nsub && ra < rb) {
             const T *xs = bufs + bi * buf_elems;
             const T *ys = xs + CG * xrows_max * pitch;
-            float win[CG][3][CPL + 2];
             const T *xcol = xs + PAD + c0;
-            #pragma unroll
-            for (int ci = 0; ci < CG; ++ci)
-                #pragma unroll
-                for (int a = 0; a < 2; ++a) {
-                    float own[CPL];
-                    load_chunk<T, CPL>(xcol + (ci * xrows_max + ra + a) * pitch, own);
-                    window_row<CPL>(own, p.pl, lane, win[ci][a]);
-                }
             const T *ycol = ys + PAD + c0 + o * yrows_max * pitch;
+            float win[CG][3][6];
+            #pragma unroll
+            for (int ci = 0; ci < CG; ++ci) {
+                load_window<PL>(xcol + (ci * xrows_max + ra) * pitch, win[ci][0]);
+                load_window<PL>(xcol + (ci * xrows_max + ra + 1) * pitch, win[ci][1]);
+            }
             int r = ra;
             for (; r + 3 <= rb; r += 3) {
-                wgrad_step<T, CG, CPL, 0, 1, 2>(win, xcol, ycol, xrows_max, pitch, r, p.pl, lane, acc);
-                wgrad_step<T, CG, CPL, 1, 2, 0>(win, xcol, ycol, xrows_max, pitch, r + 1, p.pl, lane, acc);
-                wgrad_step<T, CG, CPL, 2, 0, 1>(win, xcol, ycol, xrows_max, pitch, r + 2, p.pl, lane, acc);
+                tile_wgrad_step<T, CG, PL, 0, 1, 2>(win, xcol, ycol, xrows_max, pitch, r, acc);
+                tile_wgrad_step<T, CG, PL, 1, 2, 0>(win, xcol, ycol, xrows_max, pitch, r + 1, acc);
+                tile_wgrad_step<T, CG, PL, 2, 0, 1>(win, xcol, ycol, xrows_max, pitch, r + 2, acc);
             }
-            if (r < rb) wgrad_step<T, CG, CPL, 0, 1, 2>(win, xcol, ycol, xrows_max, pitch, r, p.pl, lane, acc);
-            if (r + 1 < rb) wgrad_step<T, CG, CPL, 1, 2, 0>(win, xcol, ycol, xrows_max, pitch, r + 1, p.pl, lane, acc);
+            if (r < rb) tile_wgrad_step<T, CG, PL, 0, 1, 2>(win, xcol, ycol, xrows_max, pitch, r, acc);
+            if (r + 1 < rb) tile_wgrad_step<T, CG, PL, 1, 2, 0>(win, xcol, ycol, xrows_max, pitch, r + 1, acc);
         }
         __syncthreads();
     }
@@ -829,10 +839,9 @@ bool allow_smem(const void *fn, size_t bytes)
 // Staged bytes of one block for a strip of `th` produced rows.
 int64_t thin_stage_elems(const ThinParams &p, int CG, int th, bool wgrad, int esize)
 {
-    if (p.slide) {   // two buffers of zero-bordered rows
-        const int64_t pitch = 16 / esize + 32 * p.cpl + 16 / esize;
-        int64_t e = (int64_t)CG * (th + 2) * pitch;
-        if (wgrad) e += (int64_t)CG * th * pitch;
+    if (p.tile) {   // two buffers of zero-bordered rows
+        int64_t e = (int64_t)CG * (th + 2) * p.pitch;
+        if (wgrad) e += (int64_t)CG * th * p.pitch;
         return 2 * e * esize;
     }
     int in_rows;
@@ -870,14 +879,17 @@ bool thin_plan(const Geom &g, gconv_pass pass, int esize, ThinParams *p, int *gr
         p->pt = g.pt; p->pl = g.pl;
     }
     const bool wg = pass == GCONV_PASS_BWD_WEIGHT;
-    // pipelined sliding-window form: stride 1, 16-byte source (and gradOutput) rows, at most
-    // 128 columns
-    const int span = std::max(p->IW, p->OW);
-    // (the forward and backward-data with four channels per group stay on the staged-window
-    // form: a thread of the sliding form would hold 4 planes' windows and 4 channels' sums)
-    p->slide = g.s_h == 1 && span <= 128 && (p->IW * esize) % 16 == 0 && (!wg || (p->OW * esize) % 16 == 0) &&
-               (wg || CG <= 2);
-    p->cpl = p->slide ? (span <= 64 ? 2 : 4) : thin_cpl(p->OW);
+    // register-tile form: stride 1, 16-byte source (and gradOutput) rows, 4-column chunks
+    // within the threads of a block (the weight gradient: of an output channel)
+    const int nch = (p->OW + 3) / 4;
+    p->tile = g.s_h == 1 && (p->IW * esize) % 16 == 0 && (!wg || (p->OW * esize) % 16 == 0) &&
+              nch <= (wg ? 32 * (4 / CG) : kThinThreads);
+    p->cpl = p->tile ? 4 : thin_cpl(p->OW);
+    if (p->tile) {
+        // zero-bordered rows: PAD elements before the data; windows read up to column OW + 4
+        const int pad = 16 / esize;
+        p->pitch = pad + (std::max(p->IW, p->OW + 5) + pad - 1) / pad * pad;
+    }
     const int64_t planes = (int64_t)g.N * g.G;
     const int64_t target_blocks = (int64_t)num_sms() * 16;
     int th = p->OH;
@@ -885,7 +897,7 @@ bool thin_plan(const Geom &g, gconv_pass pass, int esize, ThinParams *p, int *gr
         // split rows until there are enough blocks, but keep strips of 8 rows or more
         while (th > 8 && planes * ((p->OH + th - 1) / th) < target_blocks) th = (th + 1) / 2;
     }
-    const int64_t budget = p->slide ? kThinSmemMax : kThinSmem;
+    const int64_t budget = p->tile ? kThinSmemMax : kThinSmem;
     while (th > 1 && thin_stage_elems(*p, CG, th, wg, esize) > budget) th = (th + 1) / 2;
     if (thin_stage_elems(*p, CG, th, wg, esize) > budget) return false;
     p->TH = th;
@@ -906,32 +918,39 @@ bool thin_plan(const Geom &g, gconv_pass pass, int esize, ThinParams *p, int *gr
     return true;
 }
 
+template <typename T, int CG, int PL>
+gconv_status thin_tile_launch(const ThinParams &p, int grid, size_t smem, bool wgrad, float *dw, float *db,
+                              cudaStream_t s)
+{
+    if (wgrad) {
+        const void *fn = (const void *)thin_tile_wgrad_kernel<T, CG, PL>;
+        if (!allow_smem(fn, smem)) return GCONV_ERR_CUDA;
+        thin_tile_wgrad_kernel<T, CG, PL><<<grid, kThinThreads, smem, s>>>(p);
+        const int total = p.G * CG * (CG * 9 + 1);
+        thin_wgrad_finish_kernel<CG><<<(total + 255) / 256, 256, 0, s>>>(p.out, p.G, p.nchunk * p.n_strip, dw, db);
+        return GCONV_OK;
+    }
+    const void *fn = (const void *)thin_tile_kernel<T, CG, PL>;
+    if (!allow_smem(fn, smem)) return GCONV_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThinThreads, smem) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const int pgrid = std::min(grid, num_sms() * per_sm);   // persistent: items walked by a resident grid
+    thin_tile_kernel<T, CG, PL><<<pgrid, kThinThreads, smem, s>>>(p);
+    return GCONV_OK;
+}
+
 template <typename T, int CG, int S>
 gconv_status thin_launch_t(const ThinParams &p, int grid, size_t smem, bool wgrad, float *dw, float *db, cudaStream_t s)
 {
     const int cpl = p.cpl;
-    if (S == 1 && p.slide) {
-        if (wgrad) {
-            const void *fn = cpl == 2 ? (const void *)thin_pipe_wgrad_kernel<T, CG, 2>
-                                      : (const void *)thin_pipe_wgrad_kernel<T, CG, 4>;
-            if (!allow_smem(fn, smem)) return GCONV_ERR_CUDA;
-            if (cpl == 2) thin_pipe_wgrad_kernel<T, CG, 2><<<grid, kThinThreads, smem, s>>>(p);
-            else thin_pipe_wgrad_kernel<T, CG, 4><<<grid, kThinThreads, smem, s>>>(p);
-            const int total = p.G * CG * (CG * 9 + 1);
-            thin_wgrad_finish_kernel<CG><<<(total + 255) / 256, 256, 0, s>>>(p.out, p.G, p.nchunk * p.n_strip, dw, db);
-        } else if constexpr (CG <= 2) {   // (planning keeps four-channel groups off this form)
-            const void *fn = cpl == 2 ? (const void *)thin_pipe_kernel<T, CG, 2> : (const void *)thin_pipe_kernel<T, CG, 4>;
-            if (!allow_smem(fn, smem)) return GCONV_ERR_CUDA;
-            int per_sm = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThinThreads, smem) != cudaSuccess || per_sm < 1)
-                per_sm = 1;
-            const int pgrid = std::min(grid, num_sms() * per_sm);   // persistent: items walked by a resident grid
-            if (cpl == 2) thin_pipe_kernel<T, CG, 2><<<pgrid, kThinThreads, smem, s>>>(p);
-            else thin_pipe_kernel<T, CG, 4><<<pgrid, kThinThreads, smem, s>>>(p);
-        } else {
-            return GCONV_ERR_UNSUPPORTED;
+    if (S == 1 && p.tile) {
+        switch (p.pl) {
+        case 0: return thin_tile_launch<T, CG, 0>(p, grid, smem, wgrad, dw, db, s);
+        case 1: return thin_tile_launch<T, CG, 1>(p, grid, smem, wgrad, dw, db, s);
+        case 2: return thin_tile_launch<T, CG, 2>(p, grid, smem, wgrad, dw, db, s);
         }
-        return GCONV_OK;
+        return GCONV_ERR_UNSUPPORTED;
     }
     if (wgrad) {
         switch (cpl) {

@@ -558,8 +558,11 @@ THIN_PLANE = [
     (2, 32, 23, 50, 32, 3, 3, 2, 0, 1, 0, 1, 1, 8),         # 4 per group, stride 2, asymmetric pads
     (1, 6, 7, 7, 6, 3, 3, 2, 1, 1, 1, 1, 1, 6),             # depthwise stride 2, tiny plane
     (4, 64, 7, 7, 64, 3, 3, 1, 1, 1, 1, 1, 1, 64),          # small planes, many groups
-    # rows of 16-byte multiples, stride 1: the sliding-window forms (2 and 4 columns per lane)
+    # rows of 16-byte multiples, stride 1: the register-tile forms (4 columns per thread)
     (2, 16, 12, 16, 16, 3, 3, 1, 1, 1, 1, 1, 1, 16),        # depthwise, 16 columns
+    (2, 16, 12, 16, 16, 3, 3, 1, 1, 1, 1, 0, 1, 16),        # 15 produced columns: ragged last chunk
+    (1, 2, 6, 200, 2, 3, 3, 1, 1, 1, 1, 1, 1, 2),           # depthwise, 200 columns
+    (1, 4, 5, 256, 4, 3, 3, 1, 1, 1, 1, 1, 1, 2),           # 2 per group, 256 columns
     (2, 8, 13, 40, 8, 3, 3, 1, 0, 2, 2, 0, 1, 8),           # depthwise, pads 0/2/2/0
     (2, 16, 11, 64, 16, 3, 3, 1, 2, 0, 0, 2, 1, 4),         # 4 per group, 64 columns, pads 2/0/0/2
     (3, 12, 9, 72, 12, 3, 3, 1, 1, 1, 1, 1, 1, 6),          # 2 per group, 72 columns (4 per lane)

@@ -9,6 +9,7 @@ compile the included CUDA source) but no GPU.
 import os
 import shutil
 import subprocess
+from concurrent.futures import ThreadPoolExecutor
 
 import pytest
 
@@ -27,14 +28,19 @@ def replay_bins(tmp_path_factory):
     if not nvcc:
         pytest.skip("nvcc not available")
     out = tmp_path_factory.mktemp("replay")
-    bins = {}
-    for name in ("corr2_plan_replay", "wgrad_plan_replay", "wgrad_phase_replay", "thin3_plan_replay"):
+    names = ("corr2_plan_replay", "wgrad_plan_replay", "wgrad_phase_replay", "thin3_plan_replay", "thin_tile_replay")
+
+    def build(name):
         exe = str(out / name)
         cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O1", "-std=c++17", "-o", exe,
                os.path.join(HERE, "replay", name + ".cu"), "-lcuda"]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        assert r.returncode == 0, r.stderr[-2000:]
-        bins[name] = exe
+        return name, exe, subprocess.run(cmd, capture_output=True, text=True)
+
+    bins = {}
+    with ThreadPoolExecutor(max_workers=len(names)) as pool:
+        for name, exe, r in pool.map(build, names):
+            assert r.returncode == 0, r.stderr[-2000:]
+            bins[name] = exe
     return bins
 
 
@@ -111,3 +117,31 @@ THIN3 = [
                          + [wk.geom for wk in wl.model_zoo(32).values() if wk.geom[7] == 1])
 def test_thin_3x3_plan_replay(replay_bins, geom, dtype):
     _run(replay_bins["thin3_plan_replay"], geom, dtype)
+
+
+# The register-tile thin-group kernels (stride 1, 1, 2 or 4 channels a group, rows of
+# 16-byte multiples): the parity tests' layers, the workloads and the model-zoo layers.
+THIN_TILE = [
+    (2, 16, 12, 16, 16, 3, 3, 1, 1, 1, 1, 1, 1, 16),
+    (2, 16, 12, 16, 16, 3, 3, 1, 1, 1, 1, 0, 1, 16),
+    (2, 8, 13, 40, 8, 3, 3, 1, 0, 2, 2, 0, 1, 8),
+    (2, 16, 11, 64, 16, 3, 3, 1, 2, 0, 0, 2, 1, 4),
+    (3, 12, 9, 72, 12, 3, 3, 1, 1, 1, 1, 1, 1, 6),
+    (2, 32, 35, 120, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8),
+    (1, 4, 8, 128, 4, 3, 3, 1, 1, 1, 0, 0, 1, 4),
+    (1, 2, 6, 200, 2, 3, 3, 1, 1, 1, 1, 1, 1, 2),
+    (1, 4, 5, 256, 4, 3, 3, 1, 1, 1, 1, 1, 1, 2),
+]
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+@pytest.mark.parametrize("geom", THIN_TILE + [wk.geom for wk in wl.model_zoo(2).values() if wk.geom[7] == 1])
+def test_thin_tile_plan_replay(replay_bins, geom, dtype):
+    _run(replay_bins["thin_tile_replay"], geom, dtype)
+
+
+@pytest.mark.parametrize("name", [n for n, wk in wl.WORKLOADS.items() if wk.geom[5:8] == (3, 3, 1)])
+def test_thin_tile_plan_replay_workloads(replay_bins, name):
+    """The full-size workloads in their storage dtype (their plans depend on the batch)."""
+    wk = wl.WORKLOADS[name]
+    _run(replay_bins["thin_tile_replay"], wk.geom, 0 if wk.dtype == "bf16" else 1)
