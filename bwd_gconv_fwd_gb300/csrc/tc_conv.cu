@@ -902,14 +902,15 @@ struct Corr2Params {
 };
 
 constexpr int kWblkBytes = 128 * 128;   // one packed weight block: 128 rows x 64 channels (bf16)
-constexpr int kC2EpiWarps = 4;          // warps 0-3: epilogue (TMEM lane groups 0-3)
+constexpr int kC2EpiWarps = 4;          // warps 0-3: epilogue, first half of each tile's columns
+constexpr int kC2WarpEpi2 = 13;         // warps 13-16: epilogue, second half (lane groups 1, 2, 3, 0)
 constexpr int kC2StageWarps = 4;        // warps 4-7: staging
 constexpr int kC2StageThreads = kC2StageWarps * 32;
 constexpr int kC2WarpMma = 8;           // TMEM allocation and MMA issue
 constexpr int kC2WarpProd = 9;          // warps 9-12: weight producers (one issuing lane each)
 constexpr int kC2MaxWStages = 4;
-constexpr int kC2Threads = (kC2WarpProd + kC2MaxWStages) * 32;
-constexpr int kC2EpiBytes = kC2EpiWarps * 32 * 33 * 4;
+constexpr int kC2Threads = (kC2WarpEpi2 + kC2EpiWarps) * 32;
+constexpr int kC2EpiBytes = 2 * kC2EpiWarps * 32 * 33 * 4;   // a 32 x 33 transpose block per epilogue warp
 // Correlation-kernel trace words per CTA: start, SM id, MMA issuer's waits for staged
 // chunks, for weight blocks and for a free accumulator (ns), time of the last MMA,
 // epilogue warp 0's waits for accumulators (ns), end.
@@ -985,7 +986,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
             ptx::mbar_init(ptx::smem_u32(&bar_sfull[i]), kC2StageThreads);
             ptx::mbar_init(ptx::smem_u32(&bar_sempty[i]), 1);
             ptx::mbar_init(ptx::smem_u32(&bar_afull[i]), 1);
-            ptx::mbar_init(ptx::smem_u32(&bar_aempty[i]), kC2EpiWarps);
+            ptx::mbar_init(ptx::smem_u32(&bar_aempty[i]), 2 * kC2EpiWarps);
         }
         for (int i = 0; i < kC2MaxWStages; ++i) {
             ptx::mbar_init(ptx::smem_u32(&bar_wfull[i]), 1);
@@ -1141,10 +1142,14 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
             ptx::mma_commit(ptx::smem_u32(&bar_drain));
             if (!ptx::mbar_wait(ptx::smem_u32(&bar_drain), 0, kDrainNs)) raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
         }
-    } else if (warp < kC2EpiWarps) {
+    } else if (warp < kC2EpiWarps || warp >= kC2WarpEpi2) {
         // ---------------- epilogue: TMEM -> 32 x 32 smem transpose -> coalesced NCHW rows ----------------
-        const int lg = warp;
-        float *tb = epi + warp * (32 * 33);
+        // two warps per TMEM lane group (warps 0-3 and 13-16, which can read the same lanes),
+        // taking alternate column blocks of every tile
+        const int lg = warp & 3;
+        const int half = warp >= kC2WarpEpi2 ? 1 : 0;
+        float *epih = epi + half * (kC2EpiWarps * 32 * 33);
+        float *tb = epih + lg * (32 * 33);
         const int64_t out_hw = (int64_t)p.Qh * p.Qw;
         uint64_t w_epi = 0;
         int k = 0;
@@ -1157,7 +1162,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
             if (trace) w_epi += ptx::globaltimer() - t0;
             ready = __all_sync(0xffffffffu, ready) && !abort_flag;
             // paired warps must take the same decision: they meet on named barriers below
-            if (p.pair_delta) ready = !ptx::bar_red_or(2 + (lg & 1), 64, !ready);
+            if (p.pair_delta) ready = !ptx::bar_red_or(2 + (lg & 1) + 2 * half, 64, !ready);
             if (!ready) {
                 if (lane == 0) { abort_flag = 1; raise_device_error(p.err, DEVERR_WAIT_TIMEOUT); }
                 break;
@@ -1166,16 +1171,18 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
             const int p0 = ptile * p.tile_pos;
             if (p.pair_delta) {
                 // lane groups 0, 1: first taps (rows v), 2, 3: second taps (rows 64 + v); the
-                // warps lg and lg + 2 hold the same channels and meet on named barrier 2 + (lg & 1)
+                // warps lg and lg + 2 of a half hold the same channels and meet on named
+                // barrier 2 + (lg & 1) + 2 * half
                 const int part = lg & 1;
                 const bool upper = lg >= 2;
-                float *hb = epi + part * (32 * 17);                 // upper warp's columns
-                float *tbp = epi + (2 + part) * (32 * 17);          // lower warp's sums
+                const int bid = 2 + part + 2 * half;
+                float *hb = epih + part * (32 * 17);                 // upper warp's columns
+                float *tbp = epih + (2 + part) * (32 * 17);          // lower warp's sums
                 const int v0 = part * 32;
                 const int vcount = min(32, p.Cv - v0);
                 const int64_t vout = ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv + v0) * out_hw;   // element index
                 const float bias_lane = (p.bias && !upper && lane < vcount) ? __bfloat162float(p.bias[g * p.Cv + v0 + lane]) : 0.f;
-                for (int pc = 0; pc < p.tile_pos; pc += 16) {
+                for (int pc = half * 16; pc < p.tile_pos; pc += 32) {
                     uint32_t a[16];
                     const uint32_t col = (uint32_t)(acc * 256 + pc + (upper ? p.pair_delta : 0));
                     ptx::tmem_ld16(tmem + ((uint32_t)(lg * 32) << 16) + col, a);
@@ -1184,7 +1191,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                         #pragma unroll
                         for (int j = 0; j < 16; ++j) hb[lane * 17 + j] = __uint_as_float(a[j]);
                     }
-                    ptx::named_sync(2 + part, 64);
+                    ptx::named_sync(bid, 64);
                     if (!upper) {
                         #pragma unroll
                         for (int j = 0; j < 16; ++j) tbp[lane * 17 + j] = __uint_as_float(a[j]) + hb[lane * 17 + j] + bias_lane;
@@ -1204,14 +1211,14 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                             }
                         }
                     }
-                    ptx::named_sync(2 + part, 64);   // the upper warp may overwrite hb
+                    ptx::named_sync(bid, 64);   // the upper warp may overwrite hb
                 }
             } else {
             const int v0 = vt * 128 + lg * 32;
             const int vcount = min(32, p.Cv - v0);
             const int64_t vout = ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv + v0) * out_hw;   // element index
             const float bias_lane = (p.bias && lane < vcount) ? __bfloat162float(p.bias[g * p.Cv + v0 + lane]) : 0.f;
-            for (int pc = 0; pc < p.tile_pos; pc += 32) {
+            for (int pc = half * 32; pc < p.tile_pos; pc += 64) {
                 uint32_t a0[16], a1[16];
                 const uint32_t taddr = tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)(acc * 256 + pc);
                 ptx::tmem_ld16(taddr, a0);
