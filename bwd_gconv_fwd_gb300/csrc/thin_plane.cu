@@ -584,36 +584,55 @@ thin_tile_kernel(const __grid_constant__ ThinParams p)
     const int c0 = chunk * kTileCols;
     const int ncol = min(kTileCols, p.OW - c0);
     const bool vec = (p.OW % kTileCols) == 0;   // whole chunks; y / dx and its planes 16-byte aligned
-    auto issue = [&](int it, int b, float (&wv)[WPT]) {
-        int t = it;
-        const int strip = t % p.n_strip; t /= p.n_strip;
-        const int g = t % p.G;
-        const int n = t / p.G;
-        const int r0 = strip * p.TH;
+    // items in one contiguous run per block, walked in (image, group, strip) order: the next
+    // item's coordinates follow by increments, not divisions
+    struct Pos {
+        int strip, g, n;
+    };
+    auto advance = [&](Pos &q) {
+        if (++q.strip == p.n_strip) {
+            q.strip = 0;
+            if (++q.g == p.G) { q.g = 0; ++q.n; }
+        }
+    };
+    auto issue = [&](const Pos &q, int b, float (&wv)[WPT]) {
+        const int r0 = q.strip * p.TH;
         const int rows = min(p.TH, p.OH - r0);
-        issue_rows<T, CG>(src + ((int64_t)n * p.G + g) * CG * plane, plane, p.IH, p.IW, r0 - p.pt, rows + 2, nrows_max,
-                          pitch, bufs + b * buf_elems);
+        issue_rows<T, CG>(src + ((int64_t)q.n * p.G + q.g) * CG * plane, plane, p.IH, p.IW, r0 - p.pt, rows + 2,
+                          nrows_max, pitch, bufs + b * buf_elems);
         #pragma unroll
         for (int u = 0; u < WPT; ++u) {
             const int i = threadIdx.x + u * kThinThreads;
             float v = 0.f;
             if (i < NW) {
                 const int o = i / (CG * 9), rem = i - o * CG * 9, ci = rem / 9, tap = rem - ci * 9;
-                v = !p.bwd ? to_f(W[((int64_t)(g * CG + o) * CG + ci) * 9 + tap])
-                           : to_f(W[((int64_t)(g * CG + ci) * CG + o) * 9 + (8 - tap)]);
+                v = !p.bwd ? to_f(W[((int64_t)(q.g * CG + o) * CG + ci) * 9 + tap])
+                           : to_f(W[((int64_t)(q.g * CG + ci) * CG + o) * 9 + (8 - tap)]);
             }
             wv[u] = v;
         }
     };
+    const int it0 = (int)((int64_t)blockIdx.x * items / gridDim.x);
+    const int it1 = (int)((int64_t)(blockIdx.x + 1) * items / gridDim.x);
+    Pos cur;
+    {
+        int t = it0;
+        cur.strip = t % p.n_strip; t /= p.n_strip;
+        cur.g = t % p.G;
+        cur.n = t / p.G;
+    }
+    Pos nxt = cur;
+    advance(nxt);
+    const int sr_full = (p.TH + nsub - 1) / nsub;
     float wnext[WPT];
     int b = 0;
-    if ((int)blockIdx.x < items) issue(blockIdx.x, 0, wnext);
+    if (it0 < it1) issue(cur, 0, wnext);
     ptx::cp_async_commit();
-    for (int it = blockIdx.x; it < items; it += gridDim.x, b ^= 1) {
+    for (int it = it0; it < it1; ++it, b ^= 1, cur = nxt, advance(nxt)) {
         float wcur[WPT];
         #pragma unroll
         for (int u = 0; u < WPT; ++u) wcur[u] = wnext[u];
-        if (it + (int)gridDim.x < items) issue(it + gridDim.x, b ^ 1, wnext);
+        if (it + 1 < it1) issue(nxt, b ^ 1, wnext);
         ptx::cp_async_commit();
         #pragma unroll
         for (int u = 0; u < WPT; ++u) {
@@ -629,13 +648,10 @@ thin_tile_kernel(const __grid_constant__ ThinParams p)
         }
         ptx::cp_async_wait_group<1>();   // this item's rows have landed (the next item's may not)
         __syncthreads();
-        int t = it;
-        const int strip = t % p.n_strip; t /= p.n_strip;
-        const int g = t % p.G;
-        const int n = t / p.G;
-        const int r0 = strip * p.TH;
+        const int g = cur.g, n = cur.n;
+        const int r0 = cur.strip * p.TH;
         const int rows = min(p.TH, p.OH - r0);
-        const int sr = (rows + nsub - 1) / nsub;
+        const int sr = rows == p.TH ? sr_full : (rows + nsub - 1) / nsub;
         const int ra = sub * sr, rb = min(rows, ra + sr);
         if (sub < nsub && ra < rb) {
             const float *wsm = ws[b];

@@ -27,7 +27,8 @@
  *   bias,db [C_out]
  *   y, dy   [N][C_out][Ho][Wo]
  * Inputs x, w, bias, dy are `dtype` (fp32 or bf16); outputs y, dx, dw, db are
- * always fp32.  Outputs are overwritten, never accumulated into.
+ * fp32 (the *_ex entry points below can store y and dx as bf16, rounded once to
+ * nearest even).  Outputs are overwritten, never accumulated into.
  *
  * Common leading arguments of every call, in this order:
  *   N, C_in, H, W, C_out, kH, kW, stride, pad_top, pad_bottom, pad_left,

@@ -142,6 +142,28 @@ int main(int argc, char **argv)
                 }
             }
             for (int64_t i = 0; i < out_total; ++i) CHECK(written[i] == 1, "output %lld written %d times", (long long)i, written[i]);
+            // persistent grids: each block walks a contiguous run of items, the coordinates of
+            // the next item advanced by increments; they must match the divided ones and the
+            // runs must cover every item once
+            const int items = g.N * g.G * p.n_strip;
+            for (int per_sm = 1; per_sm <= 16; per_sm *= 2) {
+                const int pgrid = std::min(grid, 152 * per_sm);
+                std::vector<unsigned char> cover(items, 0);
+                for (int blk = 0; blk < pgrid; ++blk) {
+                    const int it0 = (int)((int64_t)blk * items / pgrid), it1 = (int)((int64_t)(blk + 1) * items / pgrid);
+                    int t = it0;
+                    int strip = t % p.n_strip; t /= p.n_strip;
+                    int gg = t % g.G, n = t / g.G;
+                    for (int it = it0; it < it1; ++it) {
+                        int u = it;
+                        const int es = u % p.n_strip; u /= p.n_strip;
+                        CHECK(strip == es && gg == u % g.G && n == u / g.G, "incremental item coordinates");
+                        cover[it]++;
+                        if (++strip == p.n_strip) { strip = 0; if (++gg == g.G) { gg = 0; ++n; } }
+                    }
+                }
+                for (int i = 0; i < items; ++i) CHECK(cover[i] == 1, "item %d walked %d times", i, cover[i]);
+            }
         } else {
             const int WPO = 4 / CG;
             const int nsub = (32 * WPO) / nch;
