@@ -506,16 +506,20 @@ __device__ __forceinline__ void tile_step(float (&win)[CG][3][6], const T *col, 
 // One produced row of a four-channel group: the three staged rows of each input plane in
 // turn (a sliding window over four planes would hold 72 values next to 16 sums), each tap
 // one float4 of the four output channels' weights, wq[(ci*9 + tap)*4 + o], read where it
-// is used (hoisted out of the row loop, 144 weights would not fit in registers).
+// is used (hoisted out of the row loop, 144 weights would not fit in registers), and two
+// packed FMAs per window value (output channels 0-1 and 2-3; each lane rounds once, as
+// fmaf does, and adds its taps in the same order).
 template <typename T, int PL>
 __device__ __forceinline__ void tile_row4(const T *col, int nrows_max, int pitch, int r, const float *wq,
-                                          const float (&bias)[4], float (&acc)[4][kTileCols])
+                                          const float (&bias)[4], float2 (&acc)[2][kTileCols])
 {
     asm volatile("" ::: "memory");
+    // acc[h][j]: output channels (2h, 2h + 1) of column j, one packed FMA per pair
     #pragma unroll
-    for (int o = 0; o < 4; ++o)
-        #pragma unroll
-        for (int j = 0; j < kTileCols; ++j) acc[o][j] = bias[o];
+    for (int j = 0; j < kTileCols; ++j) {
+        acc[0][j] = make_float2(bias[0], bias[1]);
+        acc[1][j] = make_float2(bias[2], bias[3]);
+    }
     #pragma unroll
     for (int ci = 0; ci < 4; ++ci) {
         float win[3][6];
@@ -526,13 +530,13 @@ __device__ __forceinline__ void tile_row4(const T *col, int nrows_max, int pitch
             #pragma unroll
             for (int bb = 0; bb < 3; ++bb) {
                 const float4 w4 = *reinterpret_cast<const float4 *>(wq + (ci * 9 + a * 3 + bb) * 4);
+                const float2 w01 = make_float2(w4.x, w4.y), w23 = make_float2(w4.z, w4.w);
                 #pragma unroll
                 for (int j = 0; j < kTileCols; ++j) {
                     const float v = win[a][j + bb];
-                    acc[0][j] = fmaf(w4.x, v, acc[0][j]);
-                    acc[1][j] = fmaf(w4.y, v, acc[1][j]);
-                    acc[2][j] = fmaf(w4.z, v, acc[2][j]);
-                    acc[3][j] = fmaf(w4.w, v, acc[3][j]);
+                    const float2 vv = make_float2(v, v);
+                    acc[0][j] = __ffma2_rn(w01, vv, acc[0][j]);
+                    acc[1][j] = __ffma2_rn(w23, vv, acc[1][j]);
                 }
             }
     }
@@ -664,7 +668,13 @@ thin_tile_kernel(const __grid_constant__ ThinParams p)
             float acc[CG][kTileCols];
             if constexpr (CG == 4) {
                 for (int r = ra; r < rb; ++r) {
-                    tile_row4<T, PL>(col, nrows_max, pitch, r, wsm, bias, acc);
+                    float2 a2[2][kTileCols];
+                    tile_row4<T, PL>(col, nrows_max, pitch, r, wsm, bias, a2);
+                    #pragma unroll
+                    for (int j = 0; j < kTileCols; ++j) {
+                        acc[0][j] = a2[0][j].x; acc[1][j] = a2[0][j].y;
+                        acc[2][j] = a2[1][j].x; acc[3][j] = a2[1][j].y;
+                    }
                     tile_store<CG>(p.out, oi, out_plane, acc, ncol, vec, p.out_bf16);
                     oi += p.OW;
                 }
