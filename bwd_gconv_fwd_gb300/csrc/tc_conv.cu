@@ -398,7 +398,7 @@ constexpr int kBlockifyThreads = 256;
 // words) with every store instruction covering four whole consecutive rows (512
 // contiguous bytes): the rows pass through shared memory, 16-byte pieces, row pitch
 // 144 bytes so neither the writes nor the reads collide on banks.
-__device__ __forceinline__ void store_rows_coalesced(const uint32_t (&w)[32], int64_t total, uint4 *out)
+__device__ __forceinline__ void store_rows_coalesced(const uint32_t (&w)[32], int64_t total, uint4 *out, int blk)
 {
     __shared__ __align__(16) uint4 stage[kBlockifyThreads * 9];
     uint4 *mine = stage + threadIdx.x * 9;
@@ -409,17 +409,17 @@ __device__ __forceinline__ void store_rows_coalesced(const uint32_t (&w)[32], in
     #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const int row = base + 4 * k + (lane >> 3), piece = lane & 7;
-        const int64_t q = (int64_t)blockIdx.x * kBlockifyThreads + row;
+        const int64_t q = (int64_t)blk * kBlockifyThreads + row;
         if (q < total) out[q * 8 + piece] = stage[row * 9 + piece];
     }
 }
 
-__global__ void __launch_bounds__(kBlockifyThreads)
-blockify_kernel(const __grid_constant__ BlockifyParams p)
+// Rows [blk * 256, blk * 256 + 256) of one blocked copy.
+__device__ __forceinline__ void blockify_block(const BlockifyParams &p, int blk)
 {
     const int plane_out = p.R * p.C;
     const int64_t total = (int64_t)p.N * p.G * p.nchunk * plane_out;
-    const int64_t q = (int64_t)blockIdx.x * kBlockifyThreads + threadIdx.x;
+    const int64_t q = (int64_t)blk * kBlockifyThreads + threadIdx.x;
     uint32_t w[32];
     #pragma unroll
     for (int h = 0; h < 32; ++h) w[h] = 0u;
@@ -445,7 +445,28 @@ blockify_kernel(const __grid_constant__ BlockifyParams p)
             w[h] = lo | (hi << 16);
         }
     }
-    store_rows_coalesced(w, total, reinterpret_cast<uint4 *>(p.out));
+    store_rows_coalesced(w, total, reinterpret_cast<uint4 *>(p.out), blk);
+}
+
+int blockify_blocks(const BlockifyParams &b)
+{
+    const int64_t total = (int64_t)b.N * b.G * b.nchunk * b.R * b.C;
+    return (int)((total + kBlockifyThreads - 1) / kBlockifyThreads);
+}
+
+__global__ void __launch_bounds__(kBlockifyThreads)
+blockify_kernel(const __grid_constant__ BlockifyParams p)
+{
+    blockify_block(p, blockIdx.x);
+}
+
+// Two blocked copies in one launch (the weight gradient's x and gradOutput): blocks
+// [0, nb_a) build a, the rest b.
+__global__ void __launch_bounds__(kBlockifyThreads)
+blockify2_kernel(const __grid_constant__ BlockifyParams a, const __grid_constant__ BlockifyParams b, int nb_a)
+{
+    if ((int)blockIdx.x < nb_a) blockify_block(a, blockIdx.x);
+    else blockify_block(b, blockIdx.x - nb_a);
 }
 
 // Strided form of the blocked copy for the weight gradient: out[p][n][g][j][r][c][0..63]
@@ -492,7 +513,7 @@ blockify_phase_kernel(const __grid_constant__ PhaseBlockifyParams p)
             w[h] = lo | (hi << 16);
         }
     }
-    store_rows_coalesced(w, total, reinterpret_cast<uint4 *>(p.out));
+    store_rows_coalesced(w, total, reinterpret_cast<uint4 *>(p.out), blockIdx.x);
 }
 
 // ===========================================================================
@@ -1274,11 +1295,12 @@ struct Pack2Params {
     int tk1[kMaxTaps], tk2[kMaxTaps];   // weight tap index (kh*kW + kw) of each block; tk2 -1: none
 };
 
-__global__ void pack2_kernel(const __grid_constant__ Pack2Params p)
+// Pieces e = b0*256 + t, stepping by nb*256: the packing work of blocks b0 of nb.
+__device__ __forceinline__ void pack2_body(const Pack2Params &p, int b0, int nb)
 {
     // 32-bit index arithmetic: the packed blocks of any supported layer stay far below 2^31 pieces
     const int pieces = p.G * p.n_vtile * p.nchu * p.ntaps * 128 * 8;
-    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < pieces; e += gridDim.x * blockDim.x) {
+    for (int e = b0 * 256 + threadIdx.x; e < pieces; e += nb * 256) {
         const int k = e & 7;
         const int r = (e >> 3) & 127;
         int b = e >> 10;
@@ -1304,6 +1326,21 @@ __global__ void pack2_kernel(const __grid_constant__ Pack2Params p)
         uint8_t *blk = p.out + (int64_t)(e >> 10) * kWblkBytes;
         *reinterpret_cast<uint4 *>(blk + r * 128 + ((k ^ (r & 7)) << 4)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
     }
+}
+
+int pack2_blocks(const Pack2Params &p)
+{
+    const int64_t pieces = (int64_t)p.G * p.n_vtile * p.nchu * p.ntaps * 1024;
+    return (int)std::min<int64_t>((pieces + 255) / 256, 4096);
+}
+
+// The correlation kernel's blocked input copy and weight packing in one launch: blocks
+// [0, nb_a) build the copy, the remaining ones pack the weights.
+__global__ void __launch_bounds__(kBlockifyThreads)
+blockify_pack_kernel(const __grid_constant__ BlockifyParams a, const __grid_constant__ Pack2Params pk, int nb_a)
+{
+    if ((int)blockIdx.x < nb_a) blockify_block(a, blockIdx.x);
+    else pack2_body(pk, blockIdx.x - nb_a, gridDim.x - nb_a);
 }
 
 struct ReduceParams {
@@ -1936,11 +1973,10 @@ gconv_status launch_corr2(Corr2Launch &L, const void *U, const void *w, const vo
     uint8_t *wpk = ws + L.ub_bytes;
     L.bu.in = static_cast<const __nv_bfloat16 *>(U);
     L.bu.out = ub;
-    launch_blockify(L.bu, s);
     L.pk.w = static_cast<const __nv_bfloat16 *>(w);
     L.pk.out = wpk;
-    const int64_t pieces = (int64_t)L.pk.G * L.pk.n_vtile * L.pk.nchu * L.pk.ntaps * 1024;
-    pack2_kernel<<<(int)std::min<int64_t>((pieces + 255) / 256, 4096), 256, 0, s>>>(L.pk);
+    const int nb_a = blockify_blocks(L.bu);
+    blockify_pack_kernel<<<nb_a + pack2_blocks(L.pk), kBlockifyThreads, 0, s>>>(L.bu, L.pk, nb_a);
     L.cp.UB = ub;
     L.cp.Wpk = wpk;
     L.cp.bias = static_cast<const __nv_bfloat16 *>(bias);
@@ -2119,8 +2155,10 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
         L.bx.ones = fuse_bias ? L.ones : -1;
         L.by.in = static_cast<const __nv_bfloat16 *>(b);
         L.by.out = yt;
-        launch_blockify(L.bx, s);
-        launch_blockify(L.by, s);
+        {
+            const int nb_x = blockify_blocks(L.bx), nb_y = blockify_blocks(L.by);
+            blockify2_kernel<<<nb_x + nb_y, kBlockifyThreads, 0, s>>>(L.bx, L.by, nb_x);
+        }
         if (fuse_bias) {
             L.wp.bias_part = reinterpret_cast<float *>(wsb + L.part_bytes + L.xt_bytes + L.yt_bytes);
             L.wp.ones = L.ones;
