@@ -55,6 +55,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity (try_wait may suspend the thread
+// for a while before it answers; this does not).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Gives up after
 // `limit_ns` nanoseconds of %globaltimer (0: after the first failed poll) and
 // returns false; the caller then records the error and unwinds.

@@ -944,6 +944,19 @@ __device__ __forceinline__ void corr2_tile(const Corr2Params &p, int t, int *pti
     *g = t / p.n_vtile;
 }
 
+// Slow path of the weight-slot wait, out of line: with the bounded polling loop inlined
+// into the issue loop, the code between consecutive taps' MMAs grew and the tensor core
+// idled (measured on a replica of this loop: 215 -> 153 cycles per MMA); the issuing thread
+// runs only about one MMA ahead of the tensor core.  Adds the time waited to *waited.
+static __device__ __noinline__ bool corr2_wait_slot(uint32_t bar, uint32_t phase, uint64_t wait_ns,
+                                                    uint64_t *waited)
+{
+    const uint64_t t0 = ptx::globaltimer();
+    const bool ok = ptx::mbar_wait(bar, phase, wait_ns);
+    *waited += ptx::globaltimer() - t0;
+    return ok;
+}
+
 // Issues one staged chunk's MMAs: for every weight block, wait for its ring slot, then
 // NKS K steps of 16 channels against the chunk's rows shifted by the block's tap offset,
 // then release the slot.  NKS is a template argument so that no branch sits between the
@@ -958,15 +971,14 @@ __device__ __forceinline__ bool corr2_issue_taps(uint32_t d, uint64_t adesc0, ui
 {
     int off_next = tap_off[0];
     uint32_t acc = acc_first;
+    bool ok = true;
     for (int tp = 0; tp < ntaps; ++tp) {
         const int off = off_next;
         off_next = tap_off[tp + 1];
         const uint32_t wbar = wfull0 + (uint32_t)(slot * 8);
-        if (!ptx::mbar_try_wait(wbar, wphase)) {
-            const uint64_t t0 = ptx::globaltimer();
-            if (!ptx::mbar_wait(wbar, wphase, wait_ns)) return false;
-            w_weight += ptx::globaltimer() - t0;
-        }
+        // one exit only: a slot that timed out still gets its MMAs (the caller aborts after
+        // the chunk), so that the loop has no second exit between the MMAs
+        if (!ptx::mbar_test_wait(wbar, wphase) && ok) ok = corr2_wait_slot(wbar, wphase, wait_ns, &w_weight);
         ptx::tc_fence_after();
         const uint64_t ad = adesc0 + (uint64_t)(slot * (kWblkBytes >> 4));
         const uint64_t bd = bdesc_c + (uint64_t)(off * 8);     // off rows of 128 bytes
@@ -980,7 +992,7 @@ __device__ __forceinline__ bool corr2_issue_taps(uint32_t d, uint64_t adesc0, ui
         slot = nxt == wstages ? 0 : nxt;
         wphase ^= nxt == wstages ? 1u : 0u;
     }
-    return true;
+    return ok;
 }
 
 __global__ void __launch_bounds__(kC2Threads, 1)
