@@ -82,6 +82,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// The bounded wait as an out-of-line call, for the MMA-issuing threads: with the polling
+// loop inlined into an issue loop, the code between consecutive MMAs grew and the tensor
+// core idled (the issuing thread runs only about one MMA ahead of it).  Their fast path is
+// one mbar_test_wait; only a wait that is needed takes this call.  Adds the nanoseconds
+// waited to *waited when it is not null.
+static __device__ __noinline__ bool mbar_wait_ool(uint32_t bar, uint32_t parity, uint64_t limit_ns, uint64_t *waited)
+{
+    const uint64_t t0 = globaltimer();
+    const bool ok = mbar_wait(bar, parity, limit_ns);
+    if (waited) *waited += globaltimer() - t0;
+    return ok;
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor-core operand reads, bulk copies).
 __device__ __forceinline__ void fence_proxy_async_smem()

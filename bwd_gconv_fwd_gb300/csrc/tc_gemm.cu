@@ -165,19 +165,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++local) {
                 const int buf = local & 1;
-                if (local >= 2 &&
-                    !ptx::mbar_wait(ptx::smem_u32(&bar_acc_empty[buf]), ((local >> 1) - 1) & 1, p.wait_ns)) {
-                    ok = false;
-                    break;
-                }
+                if (local >= 2 && !ptx::mbar_test_wait(ptx::smem_u32(&bar_acc_empty[buf]), ((local >> 1) - 1) & 1))
+                    ok = ptx::mbar_wait_ool(ptx::smem_u32(&bar_acc_empty[buf]), ((local >> 1) - 1) & 1, p.wait_ns, nullptr);
+                if (!ok) break;
                 ptx::tc_fence_after();
                 const uint32_t dt = tmem + (uint32_t)(buf * BN);
+                // one exit and an out-of-line slow wait (the issuing thread runs about one MMA
+                // ahead of the tensor core): a block whose wait timed out still gets its MMAs
+                // on stale data, and the tile loop ends after it
                 for (int kb = 0; kb < p.n_kblk; ++kb) {
                     const uint32_t fb = ptx::smem_u32(&bar_full[slot]);
-                    if (!ptx::mbar_try_wait(fb, phase) && !ptx::mbar_wait(fb, phase, p.wait_ns)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!ptx::mbar_test_wait(fb, phase) && ok) ok = ptx::mbar_wait_ool(fb, phase, p.wait_ns, nullptr);
                     ptx::tc_fence_after();
                     const uint64_t so = (uint64_t)((slot * stage_bytes) >> 4);
                     const uint64_t ad = a0 + so, bd = b0 + so;
