@@ -37,6 +37,8 @@
 #include "ptx.cuh"
 
 #include <algorithm>
+#include <climits>
+#include <array>
 #include <vector>
 #include <tuple>
 
@@ -49,6 +51,8 @@ constexpr int kWarpMma = kStageWarps + 1;           // MMA issuer
 constexpr int kTcThreads = kStageThreads + 64;
 constexpr int kMaxTaps = 64;
 constexpr int kMaxPlanes = 4;
+constexpr int kMaxBlk = 512;     // correlation weight blocks per tile (all chunks)
+constexpr int kMaxChunk = 64;    // staged chunks per correlation tile (stride phases x 64-channel chunks)
 constexpr int kWeightStages = 4;
 constexpr uint64_t kDrainNs = 1000000000ull;   // bound on draining own async work at exit
 constexpr size_t kMaxSmem = 220 * 1024;
@@ -390,6 +394,10 @@ struct BlockifyParams {
     int N, G, Cg, nchunk, IH, IW, R, C, r_off, c_off;
     int ones = -1;   // >= 0: channel slot of the last chunk set to 1 at every position (the
                      // weight gradient's bias column), -1: none
+    // stride phases (nchc > 0): chunk j is 64-channel chunk j % nchc of phase plane
+    // j / nchc, whose (r, c) is the source's (r*sh + roff[plane], c*sw + coff[plane])
+    int nchc = 0, sh = 1, sw = 1;
+    int roff[4] = {}, coff[4] = {};
 };
 
 constexpr int kBlockifyThreads = 256;
@@ -427,9 +435,15 @@ __device__ __forceinline__ void blockify_block(const BlockifyParams &p, int blk)
         const int64_t blk = q / plane_out;                 // (n*G + g)*nchunk + j
         const int pos = (int)(q - blk * plane_out);
         const int r = pos / p.C, c = pos - r * p.C;
-        const int j = (int)(blk % p.nchunk);
+        int j = (int)(blk % p.nchunk);
         const int64_t ng = blk / p.nchunk;                 // n*G + g
-        const int row = r + p.r_off, col = c + p.c_off;
+        int row = r + p.r_off, col = c + p.c_off;
+        if (p.nchc > 0) {                                  // stride-phase planes
+            const int pl = j / p.nchc;
+            j -= pl * p.nchc;
+            row = r * p.sh + p.roff[pl];
+            col = c * p.sw + p.coff[pl];
+        }
         const bool inside = row >= 0 && row < p.IH && col >= 0 && col < p.IW;
         const int cvalid = inside ? min(64, p.Cg - 64 * j) : 0;
         // the bias column's channel of ones (a slot past the valid channels, every position)
@@ -903,7 +917,7 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
 // so that a warp stores 32 consecutive pixels of one output channel.
 struct Corr2Params {
     const __nv_bfloat16 *UB;    // blocked input [N][G][nchu][R][Wp][64]
-    const uint8_t *Wpk;         // packed weight blocks [G][n_vtile][nchu][ntaps][16 KB]
+    const uint8_t *Wpk;         // packed weight blocks [G][n_vtile][nblk][16 KB]
     const __nv_bfloat16 *bias;  // [G*Cv] or nullptr
     float *V;                   // output [N][G*Cv][Qh][Qw] (fp32, or bf16 when out_bf16)
     int out_bf16;
@@ -914,10 +928,15 @@ struct Corr2Params {
     int nmma;                   // MMA N: 256, or 240 with paired taps
     int tile_pos;               // output positions per tile: nmma, or nmma - pair_delta with paired taps
     int pair_delta;             // paired taps: the second tap's row shift past the first (0: unpaired)
+    // output grid: element (qh, qw) of the tile grid is output (qh*o_sh + o_rh, qw*o_sw + o_rw)
+    // of planes oH x oW (a stride-2 backward-data phase writes every o_sh-th row and column)
+    int oH, oW, o_sh, o_sw, o_rh, o_rw;
     int stage_rows;             // positions staged per chunk (nmma + farthest tap, multiple of 8)
     int nsb, wstages;           // staging buffers (1 or 2), weight ring depth (3 or 4)
-    int ntaps;                  // weight blocks per chunk (taps, or tap pairs)
-    int tap_off[kMaxTaps];      // row shift of each block's (first) tap
+    int nchc;                   // 64-channel chunks of the reduced channels (nchu / stride phases)
+    int nblk;                   // weight blocks per tile: every chunk's taps (or tap pairs)
+    int blk0[kMaxChunk + 1];    // first block of each staged chunk (a stride phase has its own taps)
+    int tap_off[kMaxBlk];       // row shift of each block's (first) tap
     unsigned long long *trace;  // optional per-CTA phase stamps (kTraceWords each), nullptr when off
 };
 
@@ -991,15 +1010,15 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
         bar_wempty[kC2MaxWStages], bar_afull[2], bar_aempty[2], bar_drain;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
-    __shared__ int tap_off_sh[kMaxTaps + 1];   // one spare entry: the issue loop reads one tap ahead
+    __shared__ int tap_off_sh[kMaxBlk + 1];   // one spare entry: the issue loop reads one tap ahead
 
     uint8_t *smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int stage_bytes = p.stage_rows * 128;
-    if (threadIdx.x <= p.ntaps) tap_off_sh[threadIdx.x] = threadIdx.x < p.ntaps ? p.tap_off[threadIdx.x] : 0;
+    for (int i = threadIdx.x; i <= p.nblk; i += blockDim.x) tap_off_sh[i] = i < p.nblk ? p.tap_off[i] : 0;
     uint8_t *ring = smem + p.nsb * stage_bytes;
     float *epi = reinterpret_cast<float *>(ring + p.wstages * kWblkBytes);
-    const int nblocks = p.nchu * p.ntaps;
+    const int nblocks = p.nblk;
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -1133,14 +1152,17 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                     }
                     ptx::tc_fence_after();
                     const uint64_t bdesc_c = bdesc0 + (uint64_t)((sb * stage_bytes) >> 4);
-                    const int nks = min(4, (p.Cu - 64 * kc + 15) >> 4);
+                    const int jc = kc % p.nchc;   // chunk kc: channel chunk jc of stride phase kc / nchc
+                    const int nks = min(4, (p.Cu - 64 * jc + 15) >> 4);
+                    const int b0 = p.blk0[kc], nbk = p.blk0[kc + 1] - b0;
+                    const int *toff = tap_off_sh + b0;
                     const uint32_t acc_first = kc > 0 ? 1u : 0u;
                     const uint32_t wf0 = ptx::smem_u32(&bar_wfull[0]), we0 = ptx::smem_u32(&bar_wempty[0]);
                     switch (nks) {
-                    case 4: ok = corr2_issue_taps<4>(d, adesc0, bdesc_c, idesc, acc_first, tap_off_sh, p.ntaps, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
-                    case 3: ok = corr2_issue_taps<3>(d, adesc0, bdesc_c, idesc, acc_first, tap_off_sh, p.ntaps, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
-                    case 2: ok = corr2_issue_taps<2>(d, adesc0, bdesc_c, idesc, acc_first, tap_off_sh, p.ntaps, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
-                    default: ok = corr2_issue_taps<1>(d, adesc0, bdesc_c, idesc, acc_first, tap_off_sh, p.ntaps, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                    case 4: ok = corr2_issue_taps<4>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                    case 3: ok = corr2_issue_taps<3>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                    case 2: ok = corr2_issue_taps<2>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                    default: ok = corr2_issue_taps<1>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
                     }
                     if (!ok) break;
                     ptx::mma_commit(ptx::smem_u32(&bar_sempty[sb]));
@@ -1171,7 +1193,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
         const int half = warp >= kC2WarpEpi2 ? 1 : 0;
         float *epih = epi + half * (kC2EpiWarps * 32 * 33);
         float *tb = epih + lg * (32 * 33);
-        const int64_t out_hw = (int64_t)p.Qh * p.Qw;
+        const int64_t out_hw = (int64_t)p.oH * p.oW;
         uint64_t w_epi = 0;
         int k = 0;
         for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++k) {
@@ -1221,7 +1243,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                         const int pos = p0 + jc;
                         const int qh = pos / p.Wp, qw = pos - qh * p.Wp;
                         if (jc < p.tile_pos && qh < p.Qh && qw < p.Qw) {
-                            const int64_t o = vout + (int64_t)qh * p.Qw + qw;
+                            const int64_t o = vout + (int64_t)(qh * p.o_sh + p.o_rh) * p.oW + (qw * p.o_sw + p.o_rw);
                             if (p.out_bf16) {
                                 __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(p.V) + o;
                                 for (int vv = lane >> 4; vv < vcount; vv += 2)
@@ -1255,7 +1277,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                     const int pos = p0 + pc + lane;
                     const int qh = pos / p.Wp, qw = pos - qh * p.Wp;
                     if (pc + lane < p.tile_pos && qh < p.Qh && qw < p.Qw) {
-                        const int64_t o = vout + (int64_t)qh * p.Qw + qw;
+                        const int64_t o = vout + (int64_t)(qh * p.o_sh + p.o_rh) * p.oW + (qw * p.o_sw + p.o_rw);
                         if (p.out_bf16) {
                             __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(p.V) + o;
                             for (int vv = 0; vv < vcount; ++vv) ob[vv * out_hw] = __float2bfloat16_rn(tb[vv * 33 + lane]);
@@ -1288,27 +1310,28 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
 struct Pack2Params {
     const __nv_bfloat16 *w;
     uint8_t *out;
-    int G, Cu, Cv, n_vtile, nchu, ntaps;
+    int G, Cu, Cv, n_vtile, nblk;
     int transpose;          // 0 forward, 1 backward-data
     int w_cin_g, kHW;
     int pair;               // 1: rows 0..63 from tap tk1, rows 64..127 from tap tk2 (Cv <= 64)
-    int tk1[kMaxTaps], tk2[kMaxTaps];   // weight tap index (kh*kW + kw) of each block; tk2 -1: none
+    int tk1[kMaxBlk], tk2[kMaxBlk];   // weight tap index (kh*kW + kw) of each block; tk2 -1: none
+    int jc[kMaxBlk];        // 64-channel chunk of the reduced channels each block covers
 };
 
 // Pieces e = b0*256 + t, stepping by nb*256: the packing work of blocks b0 of nb.
 __device__ __forceinline__ void pack2_body(const Pack2Params &p, int b0, int nb)
 {
     // 32-bit index arithmetic: the packed blocks of any supported layer stay far below 2^31 pieces
-    const int pieces = p.G * p.n_vtile * p.nchu * p.ntaps * 128 * 8;
+    const int pieces = p.G * p.n_vtile * p.nblk * 128 * 8;
     for (int e = b0 * 256 + threadIdx.x; e < pieces; e += nb * 256) {
         const int k = e & 7;
         const int r = (e >> 3) & 127;
         int b = e >> 10;
-        const int tp = b % p.ntaps; b /= p.ntaps;
-        const int kc = b % p.nchu; b /= p.nchu;
+        const int bk = b % p.nblk; b /= p.nblk;
+        const int kc = p.jc[bk];
         const int vt = b % p.n_vtile;
         const int g = b / p.n_vtile;
-        const int tap = (p.pair && r >= 64) ? p.tk2[tp] : p.tk1[tp];
+        const int tap = (p.pair && r >= 64) ? p.tk2[bk] : p.tk1[bk];
         const int v = vt * 128 + (p.pair ? (r & 63) : r);
         uint32_t wv[4] = {0u, 0u, 0u, 0u};
         if (tap >= 0 && v < p.Cv) {
@@ -1330,7 +1353,7 @@ __device__ __forceinline__ void pack2_body(const Pack2Params &p, int b0, int nb)
 
 int pack2_blocks(const Pack2Params &p)
 {
-    const int64_t pieces = (int64_t)p.G * p.n_vtile * p.nchu * p.ntaps * 1024;
+    const int64_t pieces = (int64_t)p.G * p.n_vtile * p.nblk * 1024;
     return (int)std::min<int64_t>((pieces + 255) / 256, 4096);
 }
 
@@ -1778,12 +1801,24 @@ struct Corr2Launch {
     int grid = 0;
 };
 
-// Stride-1 correlation on the blocked layout: the forward pass, or backward-data as the
-// correlation of gradOutput with the mirrored taps (stride 1 makes every output
-// position of dx a full correlation, no phases).
-bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
+// Correlation on the blocked layout: the forward pass, or backward-data as the correlation
+// of gradOutput with the mirrored taps (stride 1 makes every output position of dx a full
+// correlation, no phases).  A stride-2 forward pass reads its input as stride-phase planes:
+// tap (kh, kw) of output (oh, ow) reads x[s*(oh + A) + ph][s*(ow + B) + pw], i.e. plane
+// (ph, pw) at the plain shift (A, B), so each plane is a staged chunk with its own taps and
+// the tile sums over all planes' chunks.
+// A stride-2 backward-data pass runs as one launch per output phase (rh, rw): dx rows
+// s*q + rh take the taps kh with (rh + pt - kh*d) divisible by s, which read gradOutput row
+// q + (rh + pt - kh*d)/s, a plain shift.  Every phase reads one blocked copy of gradOutput
+// whose origin is the smallest shift over all phases; a phase with output positions but
+// no taps sets *no_taps (its dx positions are zero).
+bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L, int rh = -1, int rw = -1, bool *no_taps = nullptr)
 {
-    if (g.s_h != 1 || g.s_w != 1) return false;
+    if (no_taps) *no_taps = false;
+    const bool strided = g.s_h != 1 || g.s_w != 1;
+    const bool bphase = strided && bwd_data;
+    if (strided && (g.s_h > 2 || g.s_w > 2)) return false;
+    if (bphase && (rh < 0 || rw < 0)) return false;
     const int Cu = bwd_data ? g.Cgo : g.Cgi;    // reduced channels (K)
     const int Cv = bwd_data ? g.Cgi : g.Cgo;    // produced channels (M)
     if (Cu < 16 || Cv < 16) return false;
@@ -1791,38 +1826,127 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
     if (ntaps > kMaxTaps) return false;
     Corr2Params &c = L->cp;
     c = Corr2Params{};
-    const int Qh = bwd_data ? g.H : g.Ho, Qw = bwd_data ? g.W : g.Wo;
-    const int maxa = (g.kH - 1) * g.d_h, maxb = (g.kW - 1) * g.d_w;
+    int Qh = bwd_data ? g.H : g.Ho, Qw = bwd_data ? g.W : g.Wo;
+    if (bphase) {
+        Qh = (g.H - rh + g.s_h - 1) / g.s_h;
+        Qw = (g.W - rw + g.s_w - 1) / g.s_w;
+        if (Qh <= 0 || Qw <= 0) return false;
+    }
+    // every tap as (phase plane, row shift, column shift, weight tap index)
+    struct PTap { int plane, a, b, k; };
+    std::vector<PTap> tl;
+    int nplanes = 1, maxa = 0, maxb = 0;
+    int Qh_grid = Qh, Qw_grid = Qw;   // extent the blocked copy is laid out for
+    int minA = 0, minB = 0;
+    TapGeometry tg;
+    if (bphase) {
+        // shifts over every output phase, so that one blocked copy serves them all
+        int maxA = INT_MIN, maxB = INT_MIN;
+        minA = INT_MAX;
+        minB = INT_MAX;
+        Qh_grid = 0;
+        Qw_grid = 0;
+        for (int ph = 0; ph < g.s_h; ++ph)
+            for (int pw = 0; pw < g.s_w; ++pw) {
+                Qh_grid = std::max(Qh_grid, (g.H - ph + g.s_h - 1) / g.s_h);
+                Qw_grid = std::max(Qw_grid, (g.W - pw + g.s_w - 1) / g.s_w);
+                for (int kh = 0; kh < g.kH; ++kh) {
+                    const int th = ph + g.pt - kh * g.d_h;
+                    if (th - floordiv(th, g.s_h) * g.s_h) continue;
+                    for (int kw = 0; kw < g.kW; ++kw) {
+                        const int tw = pw + g.pl - kw * g.d_w;
+                        if (tw - floordiv(tw, g.s_w) * g.s_w) continue;
+                        minA = std::min(minA, floordiv(th, g.s_h)); maxA = std::max(maxA, floordiv(th, g.s_h));
+                        minB = std::min(minB, floordiv(tw, g.s_w)); maxB = std::max(maxB, floordiv(tw, g.s_w));
+                    }
+                }
+            }
+        if (maxA == INT_MIN) { if (no_taps) *no_taps = true; return false; }
+        for (int kh = 0; kh < g.kH; ++kh) {
+            const int th = rh + g.pt - kh * g.d_h;
+            if (th - floordiv(th, g.s_h) * g.s_h) continue;
+            for (int kw = 0; kw < g.kW; ++kw) {
+                const int tw = rw + g.pl - kw * g.d_w;
+                if (tw - floordiv(tw, g.s_w) * g.s_w) continue;
+                tl.push_back(PTap{0, floordiv(th, g.s_h) - minA, floordiv(tw, g.s_w) - minB, kh * g.kW + kw});
+            }
+        }
+        if (tl.empty()) { if (no_taps) *no_taps = true; return false; }
+        maxa = maxA - minA;
+        maxb = maxB - minB;
+    } else if (!strided) {
+        for (int kh = 0; kh < g.kH; ++kh)
+            for (int kw = 0; kw < g.kW; ++kw)
+                tl.push_back(PTap{0, bwd_data ? (g.kH - 1 - kh) * g.d_h : kh * g.d_h,
+                                  bwd_data ? (g.kW - 1 - kw) * g.d_w : kw * g.d_w, kh * g.kW + kw});
+        maxa = (g.kH - 1) * g.d_h;
+        maxb = (g.kW - 1) * g.d_w;
+    } else {
+        const std::vector<Tap> taps = forward_taps(g);
+        if (!tap_geometry(taps, g.s_h, g.s_w, &tg)) return false;
+        for (size_t i = 0; i < taps.size(); ++i) tl.push_back(PTap{tg.tap_plane[i], tg.tap_a[i], tg.tap_b[i], taps[i].k});
+        nplanes = tg.nplanes;
+        maxa = tg.maxa;
+        maxb = tg.maxb;
+    }
     c.N = g.N; c.G = g.G; c.Cv = Cv; c.Qh = Qh; c.Qw = Qw;
-    c.Wp = Qw + maxb;
-    c.R = Qh + maxa;
-    c.nchu = (Cu + 63) / 64;
+    c.Wp = Qw_grid + maxb;
+    c.R = Qh_grid + maxa;
+    c.oH = Qh; c.oW = Qw; c.o_sh = 1; c.o_sw = 1; c.o_rh = 0; c.o_rw = 0;
+    if (bphase) {
+        c.oH = g.H; c.oW = g.W;
+        c.o_sh = g.s_h; c.o_sw = g.s_w;
+        c.o_rh = rh; c.o_rw = rw;
+    }
+    c.nchc = (Cu + 63) / 64;
+    c.nchu = nplanes * c.nchc;
+    if (c.nchu > kMaxChunk) return false;
     c.n_vtile = (Cv + 127) / 128;
-    c.ntaps = ntaps;
     // Weight blocks: one per tap, or, with at most 64 produced channels, one per pair of taps
     // that are neighbours (d positions apart) in a row of the kernel -- when the MMA work per
     // tile outweighs the heavier paired epilogue (measured: a 5x5 kernel over two chunks
     // gains, a 3x3 kernel over one chunk loses).
-    const bool pair = Cv <= 64 && g.kW >= 2 && g.d_w <= 16 && c.nchu * ntaps >= 16;
+    const bool pair = !strided && Cv <= 64 && g.kW >= 2 && g.d_w <= 16 && c.nchc * ntaps >= 16;
     Pack2Params &k = L->pk;
     k = Pack2Params{};
-    int nblk = 0, maxoff = 0;
-    for (int kh = 0; kh < g.kH; ++kh) {
-        const int a = bwd_data ? (g.kH - 1 - kh) * g.d_h : kh * g.d_h;
-        // the row's taps in increasing offset b
-        std::vector<std::pair<int, int>> row;   // (b, weight tap index)
-        for (int kw = 0; kw < g.kW; ++kw) row.push_back({bwd_data ? (g.kW - 1 - kw) * g.d_w : kw * g.d_w, kh * g.kW + kw});
-        std::sort(row.begin(), row.end());
-        for (size_t i = 0; i < row.size(); ++nblk) {
-            const bool two = pair && i + 1 < row.size() && row[i + 1].first == row[i].first + g.d_w;
-            c.tap_off[nblk] = a * c.Wp + row[i].first;
-            k.tk1[nblk] = row[i].second;
-            k.tk2[nblk] = two ? row[i + 1].second : -1;
-            maxoff = std::max(maxoff, c.tap_off[nblk]);
-            i += two ? 2 : 1;
+    // one plane's blocks: kernel rows in increasing row shift, a row's taps in increasing
+    // column shift (pairs of neighbours d_w apart when pairing)
+    std::vector<std::vector<std::array<int, 3>>> plane_blk(nplanes);   // (offset, tk1, tk2)
+    int maxoff = 0;
+    for (int pl = 0; pl < nplanes; ++pl) {
+        std::vector<int> rows_a;
+        for (const PTap &t : tl) if (t.plane == pl) rows_a.push_back(t.a);
+        std::sort(rows_a.begin(), rows_a.end());
+        rows_a.erase(std::unique(rows_a.begin(), rows_a.end()), rows_a.end());
+        for (int a : rows_a) {
+            std::vector<std::pair<int, int>> row;   // (b, weight tap index)
+            for (const PTap &t : tl) if (t.plane == pl && t.a == a) row.push_back({t.b, t.k});
+            std::sort(row.begin(), row.end());
+            for (size_t i = 0; i < row.size();) {
+                const bool two = pair && i + 1 < row.size() && row[i + 1].first == row[i].first + g.d_w;
+                const int off = a * c.Wp + row[i].first;
+                plane_blk[pl].push_back({off, row[i].second, two ? row[i + 1].second : -1});
+                maxoff = std::max(maxoff, off);
+                i += two ? 2 : 1;
+            }
+        }
+        if (plane_blk[pl].empty()) return false;   // every staged chunk has MMAs (the first initialises)
+    }
+    int nblk = 0;
+    for (int kc = 0; kc < c.nchu; ++kc) {
+        const int pl = kc / c.nchc, jc = kc % c.nchc;
+        c.blk0[kc] = nblk;
+        for (const auto &bk : plane_blk[pl]) {
+            if (nblk >= kMaxBlk) return false;
+            c.tap_off[nblk] = bk[0];
+            k.tk1[nblk] = bk[1];
+            k.tk2[nblk] = bk[2];
+            k.jc[nblk] = jc;
+            ++nblk;
         }
     }
-    c.ntaps = nblk;
+    c.blk0[c.nchu] = nblk;
+    c.nblk = nblk;
     c.pair_delta = pair ? g.d_w : 0;
     const int positions = Qh * c.Wp;   // padded output grid rows that hold real outputs
     c.nmma = pair ? 240 : 256;
@@ -1851,7 +1975,7 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
     if (!fit) return false;
     L->smem = std::max(L->smem, (size_t)120 * 1024);
     L->grid = std::min(c.n_tiles, num_sms());
-    k.G = g.G; k.Cu = Cu; k.Cv = Cv; k.n_vtile = c.n_vtile; k.nchu = c.nchu; k.ntaps = c.ntaps;
+    k.G = g.G; k.Cu = Cu; k.Cv = Cv; k.n_vtile = c.n_vtile; k.nblk = c.nblk;
     k.transpose = bwd_data ? 1 : 0;
     k.w_cin_g = g.Cgi; k.kHW = ntaps;
     k.pair = pair ? 1 : 0;
@@ -1862,10 +1986,78 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L)
     bu.R = c.R; bu.C = c.Wp;
     bu.r_off = bwd_data ? g.pt - maxa : -g.pt;
     bu.c_off = bwd_data ? g.pl - maxb : -g.pl;
+    if (bphase) {
+        bu.r_off = minA;
+        bu.c_off = minB;
+    } else if (strided) {
+        // plane pl, staged (r, c) = x[s_h*(r + row0) + ph][s_w*(c + col0) + pw]
+        bu.nchc = c.nchc;
+        bu.sh = g.s_h;
+        bu.sw = g.s_w;
+        for (int pl = 0; pl < nplanes; ++pl) {
+            bu.roff[pl] = g.s_h * tg.row0 + tg.plane_ph[pl];
+            bu.coff[pl] = g.s_w * tg.col0 + tg.plane_pw[pl];
+        }
+    }
     L->ub_bytes = align256((size_t)g.N * g.G * c.nchu * c.R * c.Wp * 128);
-    L->wpk_bytes = align256((size_t)g.G * c.n_vtile * c.nchu * c.ntaps * kWblkBytes);
+    L->wpk_bytes = align256((size_t)g.G * c.n_vtile * c.nblk * kWblkBytes);
     L->ws_bytes = L->ub_bytes + L->wpk_bytes;
     return true;
+}
+
+// Stride-2 backward-data on the correlation kernel: one launch per output phase that has
+// taps, one blocked copy of gradOutput for all of them (every phase lays it out alike), and
+// a zero fill for phases with outputs but no taps.
+struct Corr2PhaseSet {
+    int n = 0;                          // phases with taps
+    Corr2Launch L[kMaxPlanes];
+    int nzero = 0;                      // phases whose dx positions no tap reaches
+    int zr[kMaxPlanes] = {}, zc[kMaxPlanes] = {};
+    size_t ub_bytes = 0, wpk_off[kMaxPlanes] = {}, ws_bytes = 0;
+};
+
+bool build_corr2_phases(const Geom &g, Corr2PhaseSet *S)
+{
+    *S = Corr2PhaseSet{};
+    if ((g.s_h == 1 && g.s_w == 1) || g.s_h > 2 || g.s_w > 2) return false;
+    for (int rh = 0; rh < g.s_h; ++rh)
+        for (int rw = 0; rw < g.s_w; ++rw) {
+            const bool has_out = g.H - rh > 0 && g.W - rw > 0;
+            bool no_taps = false;
+            if (build_corr2(g, true, &S->L[S->n], rh, rw, &no_taps)) {
+                ++S->n;
+            } else if (no_taps && has_out) {
+                S->zr[S->nzero] = rh;
+                S->zc[S->nzero] = rw;
+                ++S->nzero;
+            } else if (has_out) {
+                return false;   // a phase the kernel does not serve
+            }
+        }
+    if (S->n == 0) return false;
+    S->ub_bytes = S->L[0].ub_bytes;
+    size_t off = S->ub_bytes;
+    for (int i = 0; i < S->n; ++i) {
+        if (S->L[i].ub_bytes != S->ub_bytes) return false;   // one shared blocked copy
+        S->wpk_off[i] = off;
+        off += S->L[i].wpk_bytes;
+    }
+    S->ws_bytes = off;
+    return true;
+}
+
+// dx at rows rh, rh + s_h, ... and columns rw, rw + s_w, ... of every plane: zero (no tap
+// of the kernel reaches them).
+__global__ void zero_phase_kernel(float *out, int64_t planes, int H, int W, int s_h, int s_w, int rh, int rw, int bf16)
+{
+    const int Qh = (H - rh + s_h - 1) / s_h, Qw = (W - rw + s_w - 1) / s_w;
+    const int64_t total = planes * Qh * Qw;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t pl = i / ((int64_t)Qh * Qw);
+        const int rem = (int)(i - pl * Qh * Qw);
+        const int q = rem / Qw, qq = rem - q * Qw;
+        store_out(out, pl * H * W + (int64_t)(q * s_h + rh) * W + (qq * s_w + rw), 0.f, bf16);
+    }
 }
 
 // Stride 2: the input is blocked as its stride phases (one plane per phase) and every
@@ -1964,19 +2156,12 @@ void launch_blockify(const BlockifyParams &b, cudaStream_t s)
     blockify_kernel<<<(unsigned)((total + kBlockifyThreads - 1) / kBlockifyThreads), kBlockifyThreads, 0, s>>>(b);
 }
 
-gconv_status launch_corr2(Corr2Launch &L, const void *U, const void *w, const void *bias, float *out, int out_bf16,
-                          uint8_t *ws, cudaStream_t s)
+// The correlation kernel alone, on a blocked copy and packed weights already in place.
+gconv_status launch_corr2_kernel(Corr2Launch &L, const __nv_bfloat16 *ub, const uint8_t *wpk, const void *bias,
+                                 float *out, int out_bf16, cudaStream_t s)
 {
     unsigned int *err = device_error_word();
     if (!err) return GCONV_ERR_CUDA;
-    __nv_bfloat16 *ub = reinterpret_cast<__nv_bfloat16 *>(ws);
-    uint8_t *wpk = ws + L.ub_bytes;
-    L.bu.in = static_cast<const __nv_bfloat16 *>(U);
-    L.bu.out = ub;
-    L.pk.w = static_cast<const __nv_bfloat16 *>(w);
-    L.pk.out = wpk;
-    const int nb_a = blockify_blocks(L.bu);
-    blockify_pack_kernel<<<nb_a + pack2_blocks(L.pk), kBlockifyThreads, 0, s>>>(L.bu, L.pk, nb_a);
     L.cp.UB = ub;
     L.cp.Wpk = wpk;
     L.cp.bias = static_cast<const __nv_bfloat16 *>(bias);
@@ -1990,6 +2175,50 @@ gconv_status launch_corr2(Corr2Launch &L, const void *U, const void *w, const vo
                                                                               : nullptr;
     if (!smem_attr_once((const void *)corr2_kernel, 2)) return GCONV_ERR_CUDA;
     corr2_kernel<<<L.grid, kC2Threads, L.smem, s>>>(L.cp);
+    return GCONV_OK;
+}
+
+gconv_status launch_corr2(Corr2Launch &L, const void *U, const void *w, const void *bias, float *out, int out_bf16,
+                          uint8_t *ws, cudaStream_t s)
+{
+    __nv_bfloat16 *ub = reinterpret_cast<__nv_bfloat16 *>(ws);
+    uint8_t *wpk = ws + L.ub_bytes;
+    L.bu.in = static_cast<const __nv_bfloat16 *>(U);
+    L.bu.out = ub;
+    L.pk.w = static_cast<const __nv_bfloat16 *>(w);
+    L.pk.out = wpk;
+    const int nb_a = blockify_blocks(L.bu);
+    blockify_pack_kernel<<<nb_a + pack2_blocks(L.pk), kBlockifyThreads, 0, s>>>(L.bu, L.pk, nb_a);
+    return launch_corr2_kernel(L, ub, wpk, bias, out, out_bf16, s);
+}
+
+// Stride-2 backward-data: the blocked copy of gradOutput and phase 0's weights in one launch,
+// the other phases' weights, zero fills, then one correlation launch per phase.
+gconv_status launch_corr2_phases(Corr2PhaseSet &S, const Geom &g, const void *dy, const void *w, float *out,
+                                 uint8_t *ws, cudaStream_t s)
+{
+    __nv_bfloat16 *ub = reinterpret_cast<__nv_bfloat16 *>(ws);
+    for (int i = 0; i < S.n; ++i) {
+        Corr2Launch &L = S.L[i];
+        L.pk.w = static_cast<const __nv_bfloat16 *>(w);
+        L.pk.out = ws + S.wpk_off[i];
+        if (i == 0) {
+            L.bu.in = static_cast<const __nv_bfloat16 *>(dy);
+            L.bu.out = ub;
+            const int nb_a = blockify_blocks(L.bu);
+            blockify_pack_kernel<<<nb_a + pack2_blocks(L.pk), kBlockifyThreads, 0, s>>>(L.bu, L.pk, nb_a);
+        } else {
+            blockify_pack_kernel<<<pack2_blocks(L.pk), kBlockifyThreads, 0, s>>>(S.L[0].bu, L.pk, 0);
+        }
+    }
+    for (int z = 0; z < S.nzero; ++z) {
+        const int64_t planes = (int64_t)g.N * g.Cin;
+        zero_phase_kernel<<<num_sms() * 4, 256, 0, s>>>(out, planes, g.H, g.W, g.s_h, g.s_w, S.zr[z], S.zc[z], g.out_bf16);
+    }
+    for (int i = 0; i < S.n; ++i) {
+        const gconv_status st = launch_corr2_kernel(S.L[i], ub, ws + S.wpk_off[i], nullptr, out, g.out_bf16, s);
+        if (st != GCONV_OK) return st;
+    }
     return GCONV_OK;
 }
 
@@ -2041,6 +2270,15 @@ bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p)
     }
     if (pass == GCONV_PASS_BWD_DATA) {
         if (g.s_h > 2 || g.s_w > 2) return false;
+        {
+            Corr2PhaseSet S;
+            if (build_corr2_phases(g, &S)) {
+                p->path = GCONV_PATH_TC_IGEMM;
+                p->launches = S.n + S.nzero + S.n;   // copy/packing launches, zero fills, correlations
+                p->ws_bytes = S.ws_bytes;
+                return true;
+            }
+        }
         size_t ws = 0;
         int launches = 0;
         for (int rh = 0; rh < g.s_h; ++rh)
@@ -2091,6 +2329,10 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
         return launch_corr(L, a, b, bias, out, g.out_bf16, wsb, s);
     }
     if (pass == GCONV_PASS_BWD_DATA) {
+        {
+            Corr2PhaseSet S;
+            if (build_corr2_phases(g, &S)) return launch_corr2_phases(S, g, a, b, out, wsb, s);
+        }
         size_t off = 0;
         for (int rh = 0; rh < g.s_h; ++rh)
             for (int rw = 0; rw < g.s_w; ++rw) {

@@ -68,6 +68,8 @@ STRIDE1 = [
     (2, 24, 9, 10, 48, 5, 5, 1, 2, 2, 2, 2, 1, 1),
     (3, 128, 10, 11, 128, 3, 3, 1, 0, 2, 1, 1, 1, 2),
     (2, 256, 28, 28, 256, 3, 3, 1, 1, 1, 1, 1, 1, 4),      # ResNeXt 256x28, 8 channels a group, merged
+    (2, 512, 14, 14, 512, 3, 3, 1, 1, 1, 1, 1, 1, 8),      # ResNeXt 512x14, 16 a group, merged by 4
+    (2, 1024, 7, 7, 1024, 3, 3, 1, 1, 1, 1, 1, 1, 16),     # ResNeXt 1024x7, 32 a group, merged by 2
 ]
 
 
@@ -94,7 +96,16 @@ STRIDE2 = [
     # merged groups (see above)
     (2, 64, 14, 13, 64, 3, 3, 2, 1, 1, 1, 1, 1, 1),
     (2, 256, 56, 56, 256, 3, 3, 2, 1, 1, 1, 1, 1, 4),      # ResNeXt 256x56 stride 2, merged
+    (2, 512, 28, 28, 512, 3, 3, 2, 1, 1, 1, 1, 1, 8),      # ResNeXt 512x28 stride 2, merged by 4
+    (2, 1024, 14, 14, 1024, 3, 3, 2, 1, 1, 1, 1, 1, 16),   # ResNeXt 1024x14 stride 2, merged by 2
 ]
+
+
+@pytest.mark.parametrize("geom", STRIDE2 + [wk.geom for wk in wl.WORKLOADS.values() if wk.geom[7] == 2]
+                         + [wk.geom for wk in wl.model_zoo(2).values() if wk.geom[7] == 2])
+def test_stride2_correlation_plan_replay(replay_bins, geom):
+    """The stride-2 forward on the correlation kernel: stride-phase planes as staged chunks."""
+    _run(replay_bins["corr2_plan_replay"], geom)
 
 
 @pytest.mark.parametrize("geom", STRIDE2 + [wk.geom for wk in wl.WORKLOADS.values() if wk.geom[7] == 2]
