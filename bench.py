@@ -1,8 +1,10 @@
 #!/usr/bin/env python3
 """Benchmark: one step = fwd + bwd_data + bwd_weight + bwd_bias of the AlexNet-style
 2-group convolution (x [128,96,27,27] bf16, w [256,48,5,5], groups 2, pad 2,
-stride 1; fp32 outputs), through the C ABI of libgconv; the weight and bias gradients
-come from one call (gconv_bwd_weight_ex with db, which reads gradOutput once).
+stride 1; fp32 outputs), through the C ABI of libgconv: one gconv_step_ex call, which
+builds each blocked copy once for all three passes and takes the bias gradient from the
+weight gradient's MMAs.  Per-pass times come from events the step records at its pass
+boundaries (gconv_debug_set_step_events).
 
 Prints ONE JSON line (rank 0).  `value` is whole-job TFLOP/s with inputs resident
 in HBM (3 x 2*N*C_out*Ho*Wo*(C_in/G)*kH*kW FLOP per step over the device time of
@@ -277,42 +279,62 @@ def bench_gpu(args):
     sp = stream.cuda_stream
     wsp, wsb = ws.data_ptr(), ws.numel()
 
-    def step_passes():
-        B.gconv_fwd_ptr(geom, dt, xd.data_ptr(), wd.data_ptr(), bd.data_ptr(), y.data_ptr(), wsp, wsb, sp)
-        yield "fwd"
-        B.gconv_bwd_data_ptr(geom, dt, dyd.data_ptr(), wd.data_ptr(), dx.data_ptr(), wsp, wsb, sp)
-        yield "bwd_data"
-        # the weight gradient and the bias gradient from one call (one read of gradOutput)
-        B.gconv_bwd_weight_ex_ptr(geom, dt, xd.data_ptr(), dyd.data_ptr(), dw.data_ptr(), db.data_ptr(), wsp, wsb, sp)
-        yield "bwd_weight_bias"
+    # one step = one gconv_step_ex call: y, dx, dw and db (the bias gradient from the weight
+    # gradient's own MMAs); the library shares the blocked copies between the passes where it can
+    step_ws = gc.gconv_step_workspace_size(geom, dt)
+    sws = torch.empty(max(step_ws, 16), dtype=torch.uint8, device=dev)
+
+    def step():
+        B.gconv_step_ex_ptr(geom, dt, B.GCONV_F32, xd.data_ptr(), wd.data_ptr(), bd.data_ptr(), dyd.data_ptr(),
+                            y.data_ptr(), dx.data_ptr(), dw.data_ptr(), db.data_ptr(), sws.data_ptr(), sws.numel(), sp)
 
     names = ["fwd", "bwd_data", "bwd_weight_bias"]
     plans = {nm: gc.gconv_plan(geom, dt, p) for p, nm in enumerate(names)}
-    launches_per_step = sum(l for _, l in plans.values())
+    shared, launches_per_step = gc.gconv_step_plan(geom, dt)
+    pass_launches = {nm: plans[nm][1] for nm in names}
+    if shared:
+        # the weight gradient reads the other passes' blocked copies
+        pass_launches["bwd_weight_bias"] = launches_per_step - pass_launches["fwd"] - pass_launches["bwd_data"]
 
     for _ in range(args.warmup):
         flush.zero_()
-        for _ in step_passes():
-            pass
+        step()
     torch.cuda.synchronize()
     assert gc.gconv_check_device_error(stream) == B.GCONV_OK
 
+    # the step records these at its pass boundaries (each event recorded once first, so that
+    # its handle exists)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
+    for row in ev:
+        for e in row:
+            e.record(stream)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        wall0 = time.perf_counter()
-        for k in range(args.steps):
-            flush.zero_()
-            ev[k][0].record(stream)
-            for j, _ in enumerate(step_passes()):
-                ev[k][j + 1].record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
+    try:
+        with ClockSampler(local) as clk:
+            wall0 = time.perf_counter()
+            for k in range(args.steps):
+                flush.zero_()
+                B.gconv_debug_set_step_events(ev[k])
+                step()
+            torch.cuda.synchronize()
+            wall = time.perf_counter() - wall0
+    finally:
+        B.gconv_debug_set_step_events(None)
     if world > 1:
         torch.distributed.barrier()
     assert gc.gconv_check_device_error(stream) == B.GCONV_OK
+    # the step's results are the separate passes' results, bit for bit
+    ref = {k: torch.empty_like(t) for k, t in (("y", y), ("dx", dx), ("dw", dw), ("db", db))}
+    B.gconv_fwd_ptr(geom, dt, xd.data_ptr(), wd.data_ptr(), bd.data_ptr(), ref["y"].data_ptr(), wsp, wsb, sp)
+    B.gconv_bwd_data_ptr(geom, dt, dyd.data_ptr(), wd.data_ptr(), ref["dx"].data_ptr(), wsp, wsb, sp)
+    B.gconv_bwd_weight_ex_ptr(geom, dt, xd.data_ptr(), dyd.data_ptr(), ref["dw"].data_ptr(), ref["db"].data_ptr(),
+                              wsp, wsb, sp)
+    torch.cuda.synchronize()
+    for k, t in (("y", y), ("dx", dx), ("dw", dw), ("db", db)):
+        assert torch.equal(t, ref[k]), f"step {k} differs from the separate passes"
+    del ref
     per_pass = {nm: [ev[k][j].elapsed_time(ev[k][j + 1]) for k in range(args.steps)] for j, nm in enumerate(names)}
     step_ms = [ev[k][0].elapsed_time(ev[k][len(names)]) for k in range(args.steps)]
     total_ms = reduce_max(sum(step_ms), world)
@@ -387,12 +409,13 @@ def bench_gpu(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_dict(wk),
         "roofline": {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
-                     "traffic": recorded_traffic(dom), "kernel": f"{dom} ({plans[dom][1]} launch(es), "
+                     "traffic": recorded_traffic(dom), "kernel": f"{dom} ({pass_launches[dom]} launch(es), "
                      f"{gc.PATH_NAMES[plans[dom][0]]})", "peak_source": f"{peak_src} (burst)",
                      "algorithmic": (f"{fpp / 1e9:.2f} GFLOP" if bound == "tensor" else f"{abytes[dom] / 1e6:.1f} MB")
                      + " per launch"},
         "step_roofline_frac": roof_step_s * 1e3 / ms_per_step,
-        "passes": {nm: {"us": avg[nm] * 1e3, "path": gc.PATH_NAMES[plans[nm][0]], "launches": plans[nm][1],
+        "step": {"call": "gconv_step_ex", "shared_copies": shared, "launches": launches_per_step},
+        "passes": {nm: {"us": avg[nm] * 1e3, "path": gc.PATH_NAMES[plans[nm][0]], "launches": pass_launches[nm],
                         "tflops": fpp / (avg[nm] * 1e-3) / 1e12,
                         "gbs": abytes[nm] / (avg[nm] * 1e-3) / 1e9} for nm in names},
         "cpu_baseline": cpu,

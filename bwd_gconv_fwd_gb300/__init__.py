@@ -7,6 +7,7 @@ from .binding import (  # noqa: F401
     GCONV_BF16, GCONV_F32, PASS_BWD_BIAS, PASS_BWD_DATA, PASS_BWD_WEIGHT, PASS_FWD,
     PATH_DIRECT, PATH_NAMES, PATH_NONE, PATH_REDUCE, PATH_TC_FC, PATH_TC_GEMM, PATH_TC_IGEMM,
     GconvError, gconv_bwd_bias, gconv_bwd_data, gconv_bwd_weight, gconv_check_device_error,
-    gconv_fwd, gconv_out_shape, gconv_plan, gconv_step_device_bytes, gconv_step_host, gconv_workspace_size,
+    gconv_fwd, gconv_out_shape, gconv_plan, gconv_step, gconv_step_device_bytes, gconv_step_host,
+    gconv_step_plan, gconv_step_workspace_size, gconv_workspace_size,
     geometry, lib,
 )

@@ -38,7 +38,8 @@ EXPORTED = ("gconv_out_shape", "gconv_workspace_size", "gconv_plan", "gconv_fwd"
             "gconv_debug_force_path", "gconv_debug_set_wait_limit", "gconv_debug_set_trace", "gconv_bwd_weight_noalloc",
             "gconv_noalloc_scratch_bytes", "gconv_step_host", "gconv_step_device_bytes",
             "gconv_out_shape_ex", "gconv_workspace_size_ex", "gconv_plan_ex", "gconv_fwd_ex", "gconv_bwd_data_ex",
-            "gconv_bwd_weight_ex", "gconv_bwd_bias_ex")
+            "gconv_bwd_weight_ex", "gconv_bwd_bias_ex", "gconv_step_workspace_size_ex", "gconv_step_plan_ex", "gconv_step_ex",
+            "gconv_debug_set_step_events")
 
 
 class Geometry(ctypes.Structure):
@@ -138,6 +139,14 @@ def lib():
     L.gconv_bwd_weight_ex.restype = i
     L.gconv_bwd_bias_ex.argtypes = [gp, i, vp, vp, vp, sz, vp]
     L.gconv_bwd_bias_ex.restype = i
+    L.gconv_step_workspace_size_ex.argtypes = [gp, i]
+    L.gconv_step_workspace_size_ex.restype = sz
+    L.gconv_step_ex.argtypes = [gp, i, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.gconv_step_ex.restype = i
+    L.gconv_step_plan_ex.argtypes = [gp, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+    L.gconv_step_plan_ex.restype = i
+    L.gconv_debug_set_step_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i]
+    L.gconv_debug_set_step_events.restype = None
     _lib = L
     return L
 
@@ -187,6 +196,25 @@ def gconv_plan(geom, dtype: int, pass_: int):
     return path.value, launches.value
 
 
+def gconv_step_workspace_size(geom, dtype: int) -> int:
+    """Workspace bytes gconv_step_ex needs for this geometry (14 or 16 integers)."""
+    rec = geometry_record(per_axis(geom))
+    n = lib().gconv_step_workspace_size_ex(ctypes.byref(rec), int(dtype))
+    if n == ctypes.c_size_t(-1).value:
+        raise GconvError(GCONV_ERR_INVALID_ARG, "gconv_step_workspace_size_ex")
+    return int(n)
+
+
+def gconv_step_plan(geom, dtype: int):
+    """(shared, launches) of gconv_step_ex for this geometry: whether the passes share their
+    blocked copies, and the step's kernel launches without db."""
+    rec = geometry_record(per_axis(geom))
+    shared, launches = ctypes.c_int(), ctypes.c_int()
+    _check(lib().gconv_step_plan_ex(ctypes.byref(rec), int(dtype), ctypes.byref(shared), ctypes.byref(launches)),
+           "gconv_step_plan_ex")
+    return bool(shared.value), launches.value
+
+
 def gconv_debug_force_path(path: int):
     lib().gconv_debug_force_path(int(path))
 
@@ -199,6 +227,18 @@ def gconv_debug_set_wait_limit(limit: int):
 def gconv_debug_set_trace(device_ptr: int, nbytes: int):
     """Sets (or, with 0, clears) the device buffer the correlation kernel writes phase stamps to."""
     lib().gconv_debug_set_trace(ctypes.c_void_p(device_ptr or None), int(nbytes))
+
+
+def gconv_debug_set_step_events(events):
+    """Sets (a sequence of four torch.cuda.Event, each recorded once so that it exists) or,
+    with None, clears the events gconv_step_ex records at its pass boundaries."""
+    if not events:
+        lib().gconv_debug_set_step_events(None, 0)
+        return
+    if len(events) != 4:
+        raise ValueError("four events: start, after forward, after backward-data, after the weight gradient")
+    arr = (ctypes.c_void_p * 4)(*(ctypes.c_void_p(e.cuda_event) for e in events))
+    lib().gconv_debug_set_step_events(arr, 4)
 
 
 def gconv_check_device_error(stream=None) -> int:
@@ -361,6 +401,27 @@ def _host(t, name: str):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def gconv_step(x, w, bias, dy, y, dx, dw, db=None, *, stride=1, padding=0, dilation=1, groups=1, workspace=None,
+               stream=None):
+    """One step on device tensors: y <- forward(x, w, bias), dx <- backward-data(dy, w),
+    dw <- weight gradient(x, dy) and, with db, the bias gradient; y and dx fp32 or bf16
+    (the same dtype), dw and db fp32.  Equal bit for bit to the separate passes."""
+    geom = per_axis(geometry(x.shape, w.shape, stride, padding, dilation, groups))
+    dt, odt = dtype_code(x.dtype), _out_code(y)
+    if _out_code(dx) != odt:
+        raise TypeError("y and dx must have the same dtype")
+    need = gconv_step_workspace_size(geom, dt)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws = ctypes.c_void_p(workspace.data_ptr()) if need else None
+    wsb = workspace.numel() * workspace.element_size() if need else 0
+    rec = geometry_record(geom)
+    _check(lib().gconv_step_ex(ctypes.byref(rec), dt, odt, _dev(x, "x"), _dev(w, "w"), _dev(bias, "bias"),
+                               _dev(dy, "dy"), _dev(y, "y"), _dev(dx, "dx"), _dev(dw, "dw"), _dev(db, "db"), ws, wsb,
+                               _stream_ptr(stream)), "gconv_step_ex")
+    return y, dx, dw, db
+
+
 def gconv_step_host(x, w, bias, dy, y, dx, dw, db, device_buffer, *, stride=1, padding=0, dilation=1,
                     groups=1, stream=None):
     """One step on host tensors (pinned for overlap): inputs copied in, the four passes,
@@ -433,6 +494,13 @@ def gconv_bwd_data_ex_ptr(geom, dt, out_dt, dy, w, dx, ws=0, ws_bytes=0, stream=
     rec = geometry_record(geom)
     _check(lib().gconv_bwd_data_ex(ctypes.byref(rec), int(dt), int(out_dt), dy, w, dx, ws or None, int(ws_bytes),
                                    stream or None), "gconv_bwd_data_ex")
+
+
+def gconv_step_ex_ptr(geom, dt, out_dt, x, w, bias, dy, y, dx, dw, db=0, ws=0, ws_bytes=0, stream=0):
+    """Pointer-level gconv_step_ex: y, dx, dw and (db not 0) db of one layer in one call."""
+    rec = geometry_record(per_axis(geom))
+    _check(lib().gconv_step_ex(ctypes.byref(rec), int(dt), int(out_dt), x, w, bias or None, dy, y, dx, dw,
+                               db or None, ws or None, int(ws_bytes), stream or None), "gconv_step_ex")
 
 
 def gconv_bwd_weight_ex_ptr(geom, dt, x, dy, dw, db=0, ws=0, ws_bytes=0, stream=0):

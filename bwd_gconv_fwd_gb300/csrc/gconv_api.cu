@@ -53,6 +53,8 @@ static int g_force_path = GCONV_PATH_NONE;
 static long long g_wait_limit = -1;
 static void *g_trace = nullptr;
 static size_t g_trace_bytes = 0;
+static cudaEvent_t g_step_events[4] = {};
+static bool g_step_marks = false;
 
 long long wait_limit()
 {
@@ -522,6 +524,109 @@ gconv_status noalloc_weight(const Geom &g, gconv_dtype dtype, const void *x, con
                     kNoAllocScratchBytes, stream);
 }
 
+// The training step's route: the tensor-core kernels with shared blocked copies when every
+// pass would run there (unmerged) on compatible copies, else the three passes in turn.
+bool step_shared(const Geom &g, gconv_dtype dt, size_t *ws, int *launches = nullptr)
+{
+    if (dt != GCONV_BF16 || forced_path() != GCONV_PATH_NONE || g.N == 0) return false;
+    for (gconv_pass pass : {GCONV_PASS_FWD, GCONV_PASS_BWD_DATA, GCONV_PASS_BWD_WEIGHT}) {
+        const Plan p = plan_pass(g, dt, pass);
+        if (p.path != GCONV_PATH_TC_IGEMM || p.merge != 1) return false;
+    }
+    return tc_step_plan(g, ws, launches);
+}
+
+gconv_status step_plan(const Geom &g, gconv_dtype dt, int *shared, int *launches)
+{
+    if (dt != GCONV_F32 && dt != GCONV_BF16) return GCONV_ERR_INVALID_ARG;
+    size_t ws = 0;
+    int n = 0;
+    const bool sh = step_shared(g, dt, &ws, &n);
+    if (!sh) {
+        n = 0;
+        for (gconv_pass pass : {GCONV_PASS_FWD, GCONV_PASS_BWD_DATA, GCONV_PASS_BWD_WEIGHT}) {
+            const Plan p = plan_pass(g, dt, pass);
+            if (p.path < 0) return GCONV_ERR_UNSUPPORTED;
+            n += p.launches;
+        }
+    }
+    if (shared) *shared = sh ? 1 : 0;
+    if (launches) *launches = n;
+    return GCONV_OK;
+}
+
+// Workspace of the step: the shared route's, or the largest of the three passes' (the
+// weight gradient's covers the bias gradient), and in either case the standalone bias
+// gradient's (used when the weight gradient cannot produce it).
+size_t step_workspace(const Geom &g, gconv_dtype dt)
+{
+    size_t need = 0;
+    for (gconv_pass pass : {GCONV_PASS_FWD, GCONV_PASS_BWD_DATA, GCONV_PASS_BWD_WEIGHT}) {
+        const size_t w = workspace_of(g, dt, pass);
+        if (w == (size_t)-1) return (size_t)-1;
+        need = std::max(need, w);
+    }
+    size_t shared = 0;
+    if (step_shared(g, dt, &shared)) {
+        const size_t wb = workspace_of(g, dt, GCONV_PASS_BWD_BIAS);
+        if (wb == (size_t)-1) return (size_t)-1;
+        need = std::max(shared, wb);
+    }
+    return need;
+}
+
+gconv_status step_ex(const Geom &g0, gconv_dtype dt, gconv_dtype out_dt, const void *x, const void *w,
+                     const void *bias, const void *dy, void *y, void *dx, float *dw, float *db, void *ws,
+                     size_t ws_bytes, void *stream)
+{
+    if (dt != GCONV_F32 && dt != GCONV_BF16) return GCONV_ERR_INVALID_ARG;
+    if (out_dt != GCONV_F32 && out_dt != GCONV_BF16) return GCONV_ERR_INVALID_ARG;
+    if (g0.N == 0) {
+        // y and dx are empty; the passes deliver dw and db as zeros
+        gconv_status st = run_pass(g0, dt, GCONV_F32, GCONV_PASS_BWD_WEIGHT, x, dy, nullptr, dw, db, ws, ws_bytes, stream);
+        return st;
+    }
+    // every argument is checked before the first launch, so a bad call enqueues nothing
+    if (!x || !w || !dy || !y || !dx || !dw) return GCONV_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(dy) || !aligned16(y) || !aligned16(dx) || !aligned16(dw) ||
+        (bias && !aligned16(bias)) || (db && !aligned16(db)))
+        return GCONV_ERR_INVALID_ARG;
+    const size_t need = step_workspace(g0, dt);
+    if (need == (size_t)-1) return GCONV_ERR_UNSUPPORTED;
+    if (need > 0) {
+        if (!ws || ws_bytes < need) return GCONV_ERR_WORKSPACE;
+        if (!aligned16(ws)) return GCONV_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaEvent_t *marks = g_step_marks ? g_step_events : nullptr;
+    if (marks) cudaEventRecord(marks[0], s);
+    size_t shared = 0;
+    if (!step_shared(g0, dt, &shared)) {
+        // the three passes in turn, one workspace
+        gconv_status st = run_pass(g0, dt, out_dt, GCONV_PASS_FWD, x, w, bias, y, nullptr, ws, ws_bytes, stream);
+        if (st == GCONV_OK && marks) cudaEventRecord(marks[1], s);
+        if (st == GCONV_OK) st = run_pass(g0, dt, out_dt, GCONV_PASS_BWD_DATA, dy, w, nullptr, dx, nullptr, ws, ws_bytes, stream);
+        if (st == GCONV_OK && marks) cudaEventRecord(marks[2], s);
+        if (st == GCONV_OK) st = run_pass(g0, dt, GCONV_F32, GCONV_PASS_BWD_WEIGHT, x, dy, nullptr, dw, db, ws, ws_bytes, stream);
+        if (st == GCONV_OK && marks) cudaEventRecord(marks[3], s);
+        return st;
+    }
+    cudaGetLastError();   // clear a stale error so the check below is about this call
+    Geom g = g0;
+    g.out_bf16 = out_dt == GCONV_BF16 ? 1 : 0;
+    bool db_done = false;
+    gconv_status st = tc_step_launch(g, x, w, bias, dy, static_cast<float *>(y), static_cast<float *>(dx), dw, db, ws,
+                                     s, &db_done, marks ? marks + 1 : nullptr);
+    if (st != GCONV_OK) return st;
+    if (db && !db_done) {
+        const Plan pb = plan_pass(g0, dt, GCONV_PASS_BWD_BIAS);
+        if (pb.path < 0) return GCONV_ERR_UNSUPPORTED;
+        launch_direct<__nv_bfloat16>(g0, pb, GCONV_PASS_BWD_BIAS, dy, nullptr, nullptr, db, ws, s);
+    }
+    if (marks && !db_done) cudaEventRecord(marks[3], s);
+    return cudaGetLastError() == cudaSuccess ? GCONV_OK : GCONV_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -651,6 +756,31 @@ gconv_status gconv_bwd_bias_ex(const gconv_geometry *geometry, gconv_dtype dtype
     const gconv_status st = make_geom_ex(geometry, &g);
     return st != GCONV_OK ? st : run_pass(g, dtype, GCONV_F32, GCONV_PASS_BWD_BIAS, dy, nullptr, nullptr, db,
                                           nullptr, workspace, workspace_bytes, stream);
+}
+
+size_t gconv_step_workspace_size_ex(const gconv_geometry *geometry, gconv_dtype dtype)
+{
+    Geom g;
+    if (make_geom_ex(geometry, &g) != GCONV_OK || (dtype != GCONV_F32 && dtype != GCONV_BF16)) return (size_t)-1;
+    return step_workspace(g, dtype);
+}
+
+gconv_status gconv_step_plan_ex(const gconv_geometry *geometry, gconv_dtype dtype, int *shared, int *launches)
+{
+    Geom g;
+    const gconv_status st = make_geom_ex(geometry, &g);
+    return st != GCONV_OK ? st : step_plan(g, dtype, shared, launches);
+}
+
+gconv_status gconv_step_ex(const gconv_geometry *geometry, gconv_dtype dtype, gconv_dtype out_dtype, const void *x,
+                           const void *w, const void *bias, const void *dy, void *y, void *dx, float *dw, float *db,
+                           void *workspace, size_t workspace_bytes, void *stream)
+{
+    Geom g;
+    const gconv_status st = make_geom_ex(geometry, &g);
+    if (st != GCONV_OK) return st;
+    if (dtype != GCONV_F32 && dtype != GCONV_BF16) return GCONV_ERR_INVALID_ARG;
+    return step_ex(g, dtype, out_dtype, x, w, bias, dy, y, dx, dw, db, workspace, workspace_bytes, stream);
 }
 
 // ---- status, host step ----------------------------------------------------------
@@ -783,6 +913,17 @@ gconv_status gconv_step_host(GEO_ARGS, gconv_dtype dtype, const void *x, const v
 void gconv_debug_force_path(int path) { g_force_path = path; }
 
 void gconv_debug_set_wait_limit(long long limit) { g_wait_limit = limit; }
+
+void gconv_debug_set_step_events(void *const *events, int n)
+{
+    if (!events || n == 0) {
+        g_step_marks = false;
+        return;
+    }
+    if (n != 4) return;
+    for (int i = 0; i < 4; ++i) g_step_events[i] = static_cast<cudaEvent_t>(events[i]);
+    g_step_marks = true;
+}
 
 void gconv_debug_set_trace(void *device_buffer, size_t bytes)
 {

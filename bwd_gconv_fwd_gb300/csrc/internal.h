@@ -61,9 +61,21 @@ bool thin_plan_pass(const Geom &g, gconv_dtype dt, gconv_pass pass, Plan *p);
 gconv_status thin_launch(const Geom &g, gconv_dtype dt, gconv_pass pass, const void *a, const void *b,
                          const void *bias, float *out, float *db, void *ws, cudaStream_t s);
 
-// Tensor map for TMA loads of 128-byte position rows (tc_gemm.cu); false when the
-// driver entry point is unavailable or the box is invalid.
-bool encode_rows_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t planes, uint32_t box_rows);
+// Tensor map for TMA loads of 128-byte position rows (tc_gemm.cu): `planes` planes of `rows`
+// rows, consecutive planes plane_rows rows apart (0: rows); false when the driver entry
+// point is unavailable or the box is invalid.
+bool encode_rows_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t planes, uint32_t box_rows,
+                      uint64_t plane_rows = 0);
+
+// One training step on the tensor-core kernels with the blocked copies shared between the
+// passes (tc_conv.cu): forward, backward-data, weight gradient (+ bias).  The plan fails
+// for layers whose passes do not all run there on compatible copies.
+bool tc_step_plan(const Geom &g, size_t *ws_bytes, int *launches = nullptr);
+// marks: nullptr, or three events recorded after the forward pass, backward-data and the
+// weight gradient.
+gconv_status tc_step_launch(const Geom &g, const void *x, const void *w, const void *bias, const void *dy,
+                            float *y, float *dx, float *dw, float *db, void *ws, cudaStream_t s, bool *db_done,
+                            const cudaEvent_t *marks);
 
 // tcgen05 dense-GEMM family for input size == kernel size (tc_gemm.cu)
 bool tc_fc_plan(const Geom &g, gconv_pass pass, Plan *p);

@@ -2248,6 +2248,48 @@ gconv_status launch_corr(CorrLaunch &L, const void *U, const void *w, const void
 
 }  // namespace
 
+// The stride-1 weight gradient on blocked copies already in place (L.wp.XT, L.wp.DYT and
+// their tensor maps set): the kernel and the fixed-order split-K reduction; with db, the
+// bias column of the same MMAs (x's blocked copy carries the ones channel).
+gconv_status launch_wgrad_blocked(WgradLaunch &L, const Geom &g, float *dw, float *db, uint8_t *part_ws,
+                                  uint8_t *bias_ws, cudaStream_t s, bool *db_done)
+{
+    unsigned int *err = device_error_word();
+    if (!err) return GCONV_ERR_CUDA;
+    const bool fuse_bias = db && L.ones >= 0;
+    if (fuse_bias) {
+        L.wp.bias_part = reinterpret_cast<float *>(bias_ws);
+        L.wp.ones = L.ones;
+        L.wp.bias_job = L.wp.grp_first[0];
+    }
+    L.wp.part = reinterpret_cast<float *>(part_ws);
+    L.wp.err = err;
+    L.wp.wait_ns = (uint64_t)wait_limit();
+    size_t trace_bytes = 0;
+    void *trace = debug_trace(&trace_bytes);
+    L.wp.trace = (trace && trace_bytes >= (size_t)L.grid * kTraceWords * 8) ? static_cast<unsigned long long *>(trace)
+                                                                             : nullptr;
+    if (!smem_attr_once((const void *)wgrad_kernel, 1)) return GCONV_ERR_CUDA;
+    wgrad_kernel<<<L.grid, kTcThreads, L.smem, s>>>(L.wp);
+    ReduceParams rp{};
+    rp.part = L.wp.part;
+    rp.dw = dw;
+    rp.O = g.Cout; rp.Cgi = g.Cgi; rp.kHW = g.kH * g.kW;
+    for (int gi = 0; gi < L.wp.n_tgrp; ++gi)
+        for (int jb = L.wp.grp_first[gi]; jb < L.wp.grp_first[gi + 1]; ++jb)
+            for (int c = 0; c < L.wp.job_count[jb]; ++c) rp.tap_splits[L.wp.job_tapk[jb][c]] = L.wp.grp_splits[gi];
+    if (fuse_bias) {
+        rp.bias_part = L.wp.bias_part;
+        rp.db = db;
+        rp.bias_splits = L.wp.grp_splits[0];
+        *db_done = true;
+    }
+    const int64_t count = (int64_t)g.Cout * g.Cgi * g.kH * g.kW;
+    const int blocks = (int)std::min<int64_t>((count + 255) / 256, (int64_t)num_sms() * 8);
+    wgrad_reduce_kernel<<<blocks, 256, 0, s>>>(rp);
+    return GCONV_OK;
+}
+
 bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p)
 {
     if (fc_like(g) && forced_path() != GCONV_PATH_TC_IGEMM) return false;
@@ -2255,7 +2297,7 @@ bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p)
         Corr2Launch L2;
         if (build_corr2(g, pass == GCONV_PASS_BWD_DATA, &L2)) {
             p->path = GCONV_PATH_TC_IGEMM;
-            p->launches = 3;   // blocked input copy, weight packing, the correlation kernel
+            p->launches = 2;   // blocked input copy with the weight packing, the correlation kernel
             p->ws_bytes = L2.ws_bytes;
             return true;
         }
@@ -2307,7 +2349,7 @@ bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p)
         WgradLaunch L;
         if (!build_wgrad(g, &L)) return false;
         p->path = GCONV_PATH_TC_IGEMM;
-        p->launches = 4;   // two blocked copies, the weight-gradient kernel, the slice reduction
+        p->launches = 3;   // both blocked copies, the weight-gradient kernel, the slice reduction
         p->ws_bytes = L.ws_bytes;
         return true;
     }
@@ -2387,8 +2429,6 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
     if (pass == GCONV_PASS_BWD_WEIGHT) {
         WgradLaunch L;
         if (!build_wgrad(g, &L)) return GCONV_ERR_UNSUPPORTED;
-        unsigned int *err = device_error_word();
-        if (!err) return GCONV_ERR_CUDA;
         __nv_bfloat16 *xt = reinterpret_cast<__nv_bfloat16 *>(wsb + L.part_bytes);
         __nv_bfloat16 *yt = reinterpret_cast<__nv_bfloat16 *>(wsb + L.part_bytes + L.xt_bytes);
         const bool fuse_bias = db && L.ones >= 0;
@@ -2401,42 +2441,119 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
             const int nb_x = blockify_blocks(L.bx), nb_y = blockify_blocks(L.by);
             blockify2_kernel<<<nb_x + nb_y, kBlockifyThreads, 0, s>>>(L.bx, L.by, nb_x);
         }
-        if (fuse_bias) {
-            L.wp.bias_part = reinterpret_cast<float *>(wsb + L.part_bytes + L.xt_bytes + L.yt_bytes);
-            L.wp.ones = L.ones;
-            L.wp.bias_job = L.wp.grp_first[0];
-        }
         L.wp.XT = xt;
         L.wp.DYT = yt;
         set_wgrad_tma(&L.wp);
-        L.wp.part = reinterpret_cast<float *>(wsb);
-        L.wp.err = err;
-        L.wp.wait_ns = (uint64_t)wait_limit();
-        size_t trace_bytes = 0;
-        void *trace = debug_trace(&trace_bytes);
-        L.wp.trace = (trace && trace_bytes >= (size_t)L.grid * kTraceWords * 8) ? static_cast<unsigned long long *>(trace)
-                                                                                 : nullptr;
-        if (!smem_attr_once((const void *)wgrad_kernel, 1)) return GCONV_ERR_CUDA;
-        wgrad_kernel<<<L.grid, kTcThreads, L.smem, s>>>(L.wp);
-        ReduceParams rp{};
-        rp.part = L.wp.part;
-        rp.dw = out;
-        rp.O = g.Cout; rp.Cgi = g.Cgi; rp.kHW = g.kH * g.kW;
-        for (int gi = 0; gi < L.wp.n_tgrp; ++gi)
-            for (int jb = L.wp.grp_first[gi]; jb < L.wp.grp_first[gi + 1]; ++jb)
-                for (int c = 0; c < L.wp.job_count[jb]; ++c) rp.tap_splits[L.wp.job_tapk[jb][c]] = L.wp.grp_splits[gi];
-        if (fuse_bias) {
-            rp.bias_part = L.wp.bias_part;
-            rp.db = db;
-            rp.bias_splits = L.wp.grp_splits[0];
-            *db_done = true;
-        }
-        const int64_t count = (int64_t)g.Cout * g.Cgi * g.kH * g.kW;
-        const int blocks = (int)std::min<int64_t>((count + 255) / 256, (int64_t)num_sms() * 8);
-        wgrad_reduce_kernel<<<blocks, 256, 0, s>>>(rp);
-        return GCONV_OK;
+        return launch_wgrad_blocked(L, g, out, fuse_bias ? db : nullptr, wsb,
+                                    wsb + L.part_bytes + L.xt_bytes + L.yt_bytes, s, db_done);
     }
     return GCONV_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------------------
+// One training step with shared blocked copies.  The forward pass's blocked copy of x is
+// exactly the weight gradient's (same origin, pitch and rows at stride 1), and for a layer
+// whose output is as wide as its input the backward-data pass's blocked copy of gradOutput
+// holds the weight gradient's at a constant position offset with a longer plane.  So the
+// step builds each copy once: the weight gradient reads the other passes' copies (its
+// tensor maps take the plane stride), and x's copy carries the bias column's ones channel,
+// which the forward weights multiply by packed zeros.
+namespace {
+
+struct TcStep {
+    Corr2Launch F, B;
+    WgradLaunch W;
+    int64_t y_off = 0;          // the weight gradient's first gradOutput position in the backward copy
+    size_t off_fx = 0, off_bx = 0, off_part = 0, off_bias = 0, ws_bytes = 0;
+};
+
+// Source (row, column) of element (r, c) of a blocked copy, or (-1, -1) where it is zero.
+void blocked_source(const BlockifyParams &b, int r, int c, int *sr, int *sc)
+{
+    const int row = r + b.r_off, col = c + b.c_off;
+    const bool in = row >= 0 && row < b.IH && col >= 0 && col < b.IW;
+    *sr = in ? row : -1;
+    *sc = in ? col : -1;
+}
+
+bool tc_step_build(const Geom &g, TcStep *S)
+{
+    *S = TcStep{};
+    if (g.s_h != 1 || g.s_w != 1) return false;
+    if (!build_corr2(g, false, &S->F) || !build_corr2(g, true, &S->B) || !build_wgrad(g, &S->W)) return false;
+    const BlockifyParams &fx = S->F.bu, &wx = S->W.bx, &by = S->B.bu, &wy = S->W.by;
+    // x: the same copy
+    if (fx.nchc || fx.N != wx.N || fx.G != wx.G || fx.Cg != wx.Cg || fx.nchunk != wx.nchunk || fx.IH != wx.IH ||
+        fx.IW != wx.IW || fx.R != wx.R || fx.C != wx.C || fx.r_off != wx.r_off || fx.c_off != wx.c_off)
+        return false;
+    // gradOutput: the same pitch, the weight gradient's plane a window of the backward copy's
+    if (by.nchc || by.N != wy.N || by.G != wy.G || by.Cg != wy.Cg || by.nchunk != wy.nchunk || by.IH != wy.IH ||
+        by.IW != wy.IW || by.C != wy.C)
+        return false;
+    const int64_t off = (int64_t)(wy.r_off - by.r_off) * by.C + (wy.c_off - by.c_off);
+    if (off < 0 || off + (int64_t)wy.R * wy.C > (int64_t)by.R * by.C) return false;
+    for (int r = 0; r < wy.R; ++r)
+        for (int c = 0; c < wy.C; ++c) {
+            int ar, ac, br, bc;
+            blocked_source(wy, r, c, &ar, &ac);
+            const int64_t q = off + (int64_t)r * wy.C + c;
+            blocked_source(by, (int)(q / by.C), (int)(q % by.C), &br, &bc);
+            if (ar != br || ac != bc) return false;
+        }
+    S->y_off = off;
+    S->off_fx = 0;                                           // blocked x, then the forward's packed weights
+    S->off_bx = S->F.ub_bytes + S->F.wpk_bytes;              // blocked gradOutput, then the backward's packed weights
+    S->off_part = S->off_bx + S->B.ub_bytes + S->B.wpk_bytes;
+    S->off_bias = S->off_part + S->W.part_bytes;
+    S->ws_bytes = S->off_bias + S->W.bias_bytes;
+    return true;
+}
+
+}  // namespace
+
+bool tc_step_plan(const Geom &g, size_t *ws_bytes, int *launches)
+{
+    TcStep S;
+    if (!tc_step_build(g, &S)) return false;
+    *ws_bytes = S.ws_bytes;
+    // per correlation pass its blocked copy with the weight packing and the kernel; the
+    // weight-gradient kernel and its slice reduction
+    if (launches) *launches = 6;
+    return true;
+}
+
+gconv_status tc_step_launch(const Geom &g, const void *x, const void *w, const void *bias, const void *dy,
+                            float *y, float *dx, float *dw, float *db, void *ws, cudaStream_t s, bool *db_done,
+                            const cudaEvent_t *marks)
+{
+    *db_done = false;
+    TcStep S;
+    if (!tc_step_build(g, &S)) return GCONV_ERR_UNSUPPORTED;
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    const __nv_bfloat16 *xb = reinterpret_cast<const __nv_bfloat16 *>(wsb + S.off_fx);
+    const __nv_bfloat16 *yb = reinterpret_cast<const __nv_bfloat16 *>(wsb + S.off_bx);
+    // the weight gradient's tensor maps over the shared copies, before anything is launched
+    WgradParams &wp = S.W.wp;
+    wp.XT = xb;
+    wp.DYT = yb + S.y_off * 64;
+    const uint64_t plane_x = (uint64_t)wp.Rx * wp.Wp, plane_y = (uint64_t)wp.Ho * wp.Wp;
+    const uint64_t planes_x = (uint64_t)wp.N * wp.G * wp.ncx, planes_y = (uint64_t)wp.N * wp.G * wp.ncy;
+    if (!encode_rows_tmap(&wp.tm_x, wp.XT, plane_x, planes_x, (uint32_t)wp.xb) ||
+        !encode_rows_tmap(&wp.tm_dy, wp.DYT, plane_y, planes_y, (uint32_t)(wp.TH * wp.Wp),
+                          (uint64_t)S.B.cp.R * S.B.cp.Wp))
+        return GCONV_ERR_UNSUPPORTED;
+    wp.tma = 1;
+    const bool fuse_bias = db && S.W.ones >= 0;
+    S.F.bu.ones = fuse_bias ? S.W.ones : -1;   // zero-weighted in the forward pass
+    gconv_status st = launch_corr2(S.F, x, w, bias, y, g.out_bf16, wsb + S.off_fx, s);
+    if (st != GCONV_OK) return st;
+    if (marks) cudaEventRecord(marks[0], s);
+    st = launch_corr2(S.B, dy, w, nullptr, dx, g.out_bf16, wsb + S.off_bx, s);
+    if (st != GCONV_OK) return st;
+    if (marks) cudaEventRecord(marks[1], s);
+    st = launch_wgrad_blocked(S.W, g, dw, fuse_bias ? db : nullptr, wsb + S.off_part, wsb + S.off_bias, s, db_done);
+    if (st == GCONV_OK && marks && *db_done) cudaEventRecord(marks[2], s);
+    return st;
 }
 
 // ---------------------------------------------------------------------------

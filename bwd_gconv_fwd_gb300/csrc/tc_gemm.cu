@@ -309,12 +309,15 @@ bool make_tmap_mid(CUtensorMap *m, const void *base, uint64_t cols, uint64_t gro
 
 // 3D bf16 tensor map over planes of 128-byte rows ([planes][rows][64]), box
 // {64, box_rows, 1}, 128-byte swizzle; rows past a plane's end read as zero.
-bool encode_rows_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t planes, uint32_t box_rows)
+bool encode_rows_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t planes, uint32_t box_rows,
+                      uint64_t plane_rows)
 {
     auto fn = encode_fn();
     if (!fn || box_rows == 0 || box_rows > 256) return false;
+    if (plane_rows == 0) plane_rows = rows;
+    if (plane_rows < rows) return false;
     cuuint64_t dims[3] = {64, rows, planes};
-    cuuint64_t strides[2] = {128, rows * 128};
+    cuuint64_t strides[2] = {128, plane_rows * 128};
     cuuint32_t box[3] = {64u, box_rows, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,

@@ -205,6 +205,27 @@ gconv_status gconv_bwd_bias_ex(const gconv_geometry *geometry, gconv_dtype dtype
                                const void *dy, float *db,
                                void *workspace, size_t workspace_bytes, void *stream);
 
+/* One training step of the layer on device tensors, in one call: y = forward(x, w, bias),
+ * dx = backward-data(dy, w), dw = weight gradient(x, dy) and, when db is not NULL, db = the
+ * bias gradient of dy.  Results equal those of the separate _ex calls bit for bit.  Where
+ * all three passes run on the tensor-core kernels (bf16, stride 1, a layer whose output
+ * is as wide as its input), the step builds each blocked copy once: the weight gradient
+ * reads the forward pass's copy of x and the backward-data pass's copy of dy.  Otherwise it
+ * runs the three passes in turn.  The workspace must hold gconv_step_workspace_size_ex
+ * bytes ((size_t)-1: invalid geometry or dtype).  Layouts, ownership, errors and stream
+ * semantics are those of the _ex calls; x, w, bias and dy are dtype, y and dx out_dtype,
+ * dw and db fp32. */
+size_t gconv_step_workspace_size_ex(const gconv_geometry *geometry, gconv_dtype dtype);
+/* Host-only query: *shared = 1 when gconv_step_ex would share the blocked copies, 0 when it
+ * runs the passes in turn; *launches = its kernel launches without db (with db, one more
+ * where the weight-gradient family cannot produce the bias gradient from its own MMAs).
+ * Either pointer may be NULL.  GCONV_ERR_INVALID_ARG / _UNSUPPORTED as gconv_plan_ex. */
+gconv_status gconv_step_plan_ex(const gconv_geometry *geometry, gconv_dtype dtype, int *shared, int *launches);
+gconv_status gconv_step_ex(const gconv_geometry *geometry, gconv_dtype dtype, gconv_dtype out_dtype,
+                           const void *x, const void *w, const void *bias, const void *dy,
+                           void *y, void *dx, float *dw, float *db,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
 /* Weight gradient that allocates nothing, for callers that cannot allocate device
  * memory themselves: code embedded in a host application that owns every
  * device allocation through its own pool or budget (plug-ins, engines with a
@@ -312,6 +333,15 @@ void gconv_debug_set_wait_limit(long long limit);
  * waits; the kernels' sources list the words).  NULL turns tracing off.  The
  * buffer stays owned by the caller. */
 void gconv_debug_set_trace(void *device_buffer, size_t bytes);
+
+/* Pass boundaries of gconv_step_ex (process-wide, not thread-safe).  While set
+ * (n == 4 cudaEvent_t handles, created by the caller on the step's device), each
+ * gconv_step_ex call with N > 0 that passes its argument checks records events[0] on its stream before its first launch,
+ * events[1] after the forward pass, events[2] after backward-data and events[3]
+ * after the weight and bias gradients, so that a caller can time each pass of
+ * one call.  n == 0 (or NULL) turns it off; other n is ignored.  The events stay
+ * owned by the caller. */
+void gconv_debug_set_step_events(void *const *events, int n);
 
 #ifdef __cplusplus
 }

@@ -14,7 +14,7 @@ int num_sms() { return 152; }
 unsigned int *device_error_word() { return nullptr; }
 int forced_path() { return 0; }
 void *debug_trace(size_t *b) { *b = 0; return nullptr; }
-bool encode_rows_tmap(CUtensorMap *, const void *, uint64_t, uint64_t, uint32_t) { return false; }
+bool encode_rows_tmap(CUtensorMap *, const void *, uint64_t, uint64_t, uint32_t, uint64_t) { return false; }
 }
 using namespace gconv;
 static long errors = 0;

@@ -205,3 +205,59 @@ def test_model_zoo_layers_have_plans(L):
                 ws = gc.gconv_workspace_size(geom, B.GCONV_BF16, p)
                 assert 0 <= ws < (1 << 32), (name, p)
             assert gc.gconv_step_device_bytes(geom, B.GCONV_BF16, True) > 0, name
+
+
+def test_step_ex_sizing_and_argument_checks(L):
+    """gconv_step_ex: its workspace covers each pass's (or the shared route's), and a bad
+    argument is rejected before anything is enqueued (no GPU needed)."""
+    for name, wk in wl.WORKLOADS.items():
+        geom = B.per_axis(wk.geom)
+        dt = B.GCONV_BF16 if wk.dtype == "bf16" else B.GCONV_F32
+        need = gc.gconv_step_workspace_size(geom, dt)
+        assert 0 <= need < (1 << 34), name
+        rec = B.geometry_record(geom)
+        ok = ctypes.c_void_p(1 << 20)
+        mis = ctypes.c_void_p((1 << 20) + 8)
+        step = lambda *a: L.gconv_step_ex(ctypes.byref(rec), *a)
+        full = [ok, ok, None, ok, ok, ok, ok, None]   # x w bias dy y dx dw db
+        if need:
+            assert step(dt, B.GCONV_F32, *full, ok, need - 16, None) == B.GCONV_ERR_WORKSPACE, name
+            assert step(dt, B.GCONV_F32, *full, None, 0, None) == B.GCONV_ERR_WORKSPACE, name
+            assert step(dt, B.GCONV_F32, *full, mis, need, None) == B.GCONV_ERR_INVALID_ARG, name
+        for i in (0, 1, 3, 4, 5, 6):
+            args = list(full)
+            args[i] = None
+            assert step(dt, B.GCONV_F32, *args, ok, need, None) == B.GCONV_ERR_INVALID_ARG, (name, i)
+            args[i] = mis
+            assert step(dt, B.GCONV_F32, *args, ok, need, None) == B.GCONV_ERR_INVALID_ARG, (name, i)
+        assert step(dt, 7, *full, ok, need, None) == B.GCONV_ERR_INVALID_ARG, name
+        assert step(9, B.GCONV_F32, *full, ok, need, None) == B.GCONV_ERR_INVALID_ARG, name
+    with pytest.raises(gc.GconvError):
+        gc.gconv_step_workspace_size((1, 8, 6, 6, 8, 9, 9, 1, 0, 0, 0, 0, 1, 1), B.GCONV_BF16)
+
+
+def test_step_plan_routes(L):
+    """gconv_step_plan_ex: which layers share the blocked copies between the passes (bf16,
+    every pass on the tensor-core kernels unmerged at stride 1, output as wide as the input),
+    and the step's launch count; every other layer runs its passes in turn (host-only)."""
+    bf, f32 = B.GCONV_BF16, B.GCONV_F32
+    assert gc.gconv_step_plan(wl.WORKLOADS["alexnet_g2"].geom, bf) == (True, 6)
+    assert gc.gconv_step_plan(wl.WORKLOADS["dense3x3"].geom, bf) == (True, 6)
+    assert gc.gconv_step_plan(wl.WORKLOADS["dense3x3"].geom, f32)[0] is False
+    for name in ("dense3x3_s2_asym", "resnext_g32", "depthwise", "fc_mode", "tiny_g5"):
+        geom = wl.WORKLOADS[name].geom
+        dt = bf if wl.WORKLOADS[name].dtype == "bf16" else f32
+        shared, launches = gc.gconv_step_plan(geom, dt)
+        assert not shared, name
+        assert launches == sum(gc.gconv_plan(geom, dt, p)[1] for p in range(3)), name
+    # an output narrower than the input: the backward-data copy has another pitch
+    assert gc.gconv_step_plan((2, 32, 14, 13, 64, 3, 3, 1, 1, 0, 2, 1, 1, 2), bf)[0] is False
+    assert gc.gconv_step_plan((2, 64, 17, 15, 64, 3, 3, 1, 1, 1, 1, 1, 1, 1), bf) == (True, 6)
+    # a forced family turns sharing off
+    B.gconv_debug_force_path(B.PATH_TC_IGEMM)
+    try:
+        assert gc.gconv_step_plan(wl.WORKLOADS["alexnet_g2"].geom, bf)[0] is False
+    finally:
+        B.gconv_debug_force_path(B.PATH_NONE)
+    with pytest.raises(gc.GconvError):
+        gc.gconv_step_plan((1, 8, 6, 6, 8, 3, 3, 1, 0, 0, 0, 0, 1, 1), 5)

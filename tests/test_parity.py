@@ -333,6 +333,100 @@ def test_step_host_matches_device_passes(dev, oracle_mod, geom, dtype, with_bias
     check("host db", outs["db"].numpy(), oracle_mod.bwd_bias(geom, f64(dy)), TOL[dtype])
 
 
+STEP_EX = [
+    # (geometry, dtype, bias, db, output dtype)
+    ((3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2), "bf16", True, True, "f32"),     # shared copies, db fused
+    ((3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2), "bf16", True, True, "bf16"),    # y and dx as bf16
+    ((2, 64, 17, 15, 64, 3, 3, 1, 1, 1, 1, 1, 1, 1), "bf16", True, True, "f32"),      # shared, no spare slot: db apart
+    ((2, 16, 9, 9, 16, 3, 3, 1, 2, 2, 2, 2, 2, 1), "bf16", False, False, "f32"),      # shared, dilation 2, no db
+    ((2, 96, 10, 12, 64, 3, 3, 1, 0, 2, 2, 0, 1, 1), "bf16", True, True, "f32"),      # shared, one-sided pads
+    ((2, 32, 11, 13, 32, 3, 3, 1, 1, 1, 1, 2, 2, 1, 2, 1), "bf16", False, True, "f32"),  # shared, per-axis dilation
+    ((2, 32, 14, 13, 64, 3, 3, 1, 1, 0, 2, 1, 1, 2), "bf16", True, True, "f32"),      # passes in turn (widths differ)
+    ((2, 64, 19, 16, 64, 3, 3, 2, 0, 1, 0, 1, 1, 1), "bf16", True, True, "f32"),      # stride 2: passes in turn
+    ((2, 64, 12, 12, 64, 3, 3, 1, 1, 1, 1, 1, 1, 8), "bf16", True, True, "f32"),      # merged groups: passes in turn
+    ((2, 32, 12, 12, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8), "f32", True, True, "f32"),       # CUDA-core passes
+    ((0, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2), "bf16", True, True, "f32"),     # empty batch
+]
+
+
+@pytest.mark.parametrize("geom,dtype,with_bias,with_db,out", STEP_EX)
+def test_step_ex_matches_device_passes(dev, oracle_mod, geom, dtype, with_bias, with_db, out):
+    """gconv_step_ex (y, dx, dw and db from one call, blocked copies shared where the
+    tensor-core route allows) gives bit for bit what the separate passes give, twice in a
+    row on one workspace, and meets the oracle tolerance."""
+    wk = wl.Workload("step", geom, dtype)
+    x, w, b, dy = wl.make_inputs(wk, seed=43)
+    if not with_bias:
+        b = None
+    N, Cin, H, W, Cout = wl.per_axis(geom)[:5]
+    Ho, Wo = wl.out_hw(geom)
+    kw = _kw(geom)
+    odt = torch.bfloat16 if out == "bf16" else torch.float32
+    xd, wd, dyd = x.to(dev), w.to(dev), dy.to(dev)
+    bd = None if b is None else b.to(dev)
+    # the separate passes
+    ry = torch.empty((N, Cout, Ho, Wo), dtype=odt, device=dev)
+    rdx = torch.empty((N, Cin, H, W), dtype=odt, device=dev)
+    rdw = torch.empty(tuple(w.shape), device=dev)
+    rdb = torch.empty((Cout,), device=dev) if with_db else None
+    gc.gconv_fwd(xd, wd, bd, ry, **kw)
+    gc.gconv_bwd_data(dyd, wd, rdx, **kw)
+    gc.gconv_bwd_weight(xd, dyd, rdw, db=rdb, **kw)
+    ws = torch.empty(max(1, gc.gconv_step_workspace_size(B.per_axis(geom), B.GCONV_BF16 if dtype == "bf16"
+                                                         else B.GCONV_F32)), dtype=torch.uint8, device=dev)
+    for rep in range(2):
+        bufs = {}
+        if out == "f32":
+            y, bufs["y"] = guarded((N, Cout, Ho, Wo), dev)
+            dx, bufs["dx"] = guarded((N, Cin, H, W), dev)
+        else:
+            y = torch.full((N, Cout, Ho, Wo), float("nan"), dtype=odt, device=dev)
+            dx = torch.full((N, Cin, H, W), float("nan"), dtype=odt, device=dev)
+        dw, bufs["dw"] = guarded(tuple(w.shape), dev)
+        db = None
+        if with_db:
+            db, bufs["db"] = guarded((Cout,), dev)
+        gc.gconv_step(xd, wd, bd, dyd, y, dx, dw, db, workspace=ws, **kw)
+        torch.cuda.synchronize()
+        assert gc.gconv_check_device_error() == B.GCONV_OK
+        for k, bf in bufs.items():
+            check_guards(f"step {geom} {k}", bf)
+        assert torch.equal(y, ry), rep
+        assert torch.equal(dx, rdx), rep
+        assert torch.equal(dw, rdw), rep
+        if with_db:
+            assert torch.equal(db, rdb), rep
+    tol = TOL[dtype] if out == "f32" else 2e-2
+    check("step y", y.float().cpu().numpy(), oracle_mod.fwd(geom, f64(x), f64(w), f64(b)), tol)
+    check("step dx", dx.float().cpu().numpy(), oracle_mod.bwd_data(geom, f64(dy), f64(w)), tol)
+    check("step dw", dw.cpu().numpy(), oracle_mod.bwd_weight(geom, f64(x), f64(dy)), TOL[dtype])
+    if with_db:
+        check("step db", db.cpu().numpy(), oracle_mod.bwd_bias(geom, f64(dy)), TOL[dtype])
+
+
+def test_step_ex_full_size_alexnet_matches_passes(dev):
+    """The benchmark's layer at full size: gconv_step_ex on the shared copies equals the
+    separate passes bit for bit (the passes meet the oracle in the sampled workload test)."""
+    wk = wl.WORKLOADS["alexnet_g2"]
+    x, w, b, dy = (t.to(dev) for t in wl.make_inputs(wk, seed=5))
+    geom = wk.geom
+    N, Cin, H, W, Cout = geom[:5]
+    Ho, Wo = wl.out_hw(geom)
+    kw = _kw(geom)
+    ry, y = (torch.empty((N, Cout, Ho, Wo), device=dev) for _ in range(2))
+    rdx, dx = (torch.empty((N, Cin, H, W), device=dev) for _ in range(2))
+    rdw, dw = (torch.empty(tuple(w.shape), device=dev) for _ in range(2))
+    rdb, db = (torch.empty((Cout,), device=dev) for _ in range(2))
+    gc.gconv_fwd(x, w, b, ry, **kw)
+    gc.gconv_bwd_data(dy, w, rdx, **kw)
+    gc.gconv_bwd_weight(x, dy, rdw, db=rdb, **kw)
+    gc.gconv_step(x, w, b, dy, y, dx, dw, db, **kw)
+    torch.cuda.synchronize()
+    assert gc.gconv_check_device_error() == B.GCONV_OK
+    for a, r in ((y, ry), (dx, rdx), (dw, rdw), (db, rdb)):
+        assert torch.equal(a, r)
+
+
 @pytest.mark.parametrize("name", list(wl.model_zoo(2)))
 def test_model_zoo_layers_full(dev, oracle_mod, name):
     """The grouped 3x3 layers of ResNeXt-50 (32x4d) and the depthwise 3x3 layers of

@@ -28,7 +28,8 @@ def replay_bins(tmp_path_factory):
     if not nvcc:
         pytest.skip("nvcc not available")
     out = tmp_path_factory.mktemp("replay")
-    names = ("corr2_plan_replay", "wgrad_plan_replay", "wgrad_phase_replay", "thin3_plan_replay", "thin_tile_replay")
+    names = ("corr2_plan_replay", "wgrad_plan_replay", "wgrad_phase_replay", "thin3_plan_replay", "thin_tile_replay",
+             "step_plan_replay")
 
     def build(name):
         exe = str(out / name)
@@ -156,3 +157,28 @@ def test_thin_tile_plan_replay_workloads(replay_bins, name):
     """The full-size workloads in their storage dtype (their plans depend on the batch)."""
     wk = wl.WORKLOADS[name]
     _run(replay_bins["thin_tile_replay"], wk.geom, 0 if wk.dtype == "bf16" else 1)
+
+
+# The training step's shared blocked copies: (geometry, whether the step shares them).  The
+# step shares when every pass runs on the tensor-core kernels at stride 1 and the output is
+# as wide as the input (the backward-data copy of gradOutput then has the weight gradient's
+# pitch).
+STEP = [
+    ((128, 96, 27, 27, 256, 5, 5, 1, 2, 2, 2, 2, 1, 2), 1),      # AlexNet-style 2-group layer
+    ((3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2), 1),
+    ((2, 64, 17, 15, 64, 3, 3, 1, 1, 1, 1, 1, 1, 1), 1),
+    ((2, 16, 9, 9, 16, 3, 3, 1, 2, 2, 2, 2, 2, 1), 1),           # dilation 2
+    ((2, 256, 9, 9, 256, 3, 3, 1, 1, 1, 1, 1, 1, 1), 1),         # several channel chunks
+    ((2, 64, 20, 20, 64, 7, 7, 1, 3, 3, 3, 3, 1, 1), 1),
+    ((2, 32, 11, 13, 32, 3, 3, 1, 1, 1, 1, 2, 2, 1, 2, 1), 1),    # per-axis dilation
+    ((2, 32, 11, 13, 32, 3, 3, 1, 1, 2, 2, 1, 1, 1, 2, 1), 0),    # per-axis dilation, output 2 columns narrower
+    ((2, 96, 10, 12, 64, 3, 3, 1, 0, 2, 2, 0, 1, 1), 1),         # one-sided pads
+    ((1, 40, 7, 23, 24, 2, 4, 1, 0, 3, 1, 0, 1, 1), 0),          # output narrower than the input
+    ((2, 32, 14, 13, 64, 3, 3, 1, 1, 0, 2, 1, 1, 2), 0),         # output wider than the input
+    ((2, 64, 16, 16, 64, 3, 3, 2, 1, 1, 1, 1, 1, 1), 0),         # stride 2
+]
+
+
+@pytest.mark.parametrize("geom,shared", STEP)
+def test_step_shared_copy_replay(replay_bins, geom, shared):
+    _run(replay_bins["step_plan_replay"], geom, shared)
