@@ -39,6 +39,7 @@
 #include <algorithm>
 #include <climits>
 #include <array>
+#include <mutex>
 #include <vector>
 #include <tuple>
 
@@ -1376,24 +1377,78 @@ struct ReduceParams {
     int bias_splits;
 };
 
-__global__ void wgrad_reduce_kernel(const __grid_constant__ ReduceParams p)
+// Fixed-order sum of the split-K slices.  A block of 256 threads takes 256 / WAYS
+// consecutive outputs; way w of an output sums slices w, w + WAYS, ... in order (coalesced
+// loads, issued ahead of the adds), and way 0 adds the ways' sums in way order.  The
+// order depends only on the slice counts, so results are bitwise reproducible.  Blocks
+// past the weight outputs reduce the bias slices the same way.
+constexpr int kReduceThreads = 256;
+template <int WAYS>
+__global__ void __launch_bounds__(kReduceThreads)
+wgrad_reduce_kernel(const __grid_constant__ ReduceParams p)
 {
-    if (p.bias_part)
-        for (int o = blockIdx.x * blockDim.x + threadIdx.x; o < p.O; o += gridDim.x * blockDim.x) {
-            float s = 0.f;
-            for (int k = 0; k < p.bias_splits; ++k) s += p.bias_part[(int64_t)k * p.O + o];
-            p.db[o] = s;
-        }
+    __shared__ float part_sum[WAYS > 1 ? kReduceThreads : 1];
+    constexpr int per = kReduceThreads / WAYS;             // outputs per block
+    const int ol = threadIdx.x % per, way = threadIdx.x / per;
     const int64_t count = (int64_t)p.kHW * p.O * p.Cgi;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t wblocks = (count + per - 1) / per;
+    const int64_t blk = blockIdx.x;
+    float s = 0.f;
+    int64_t i;
+    bool valid;
+    if (blk < wblocks) {
+        i = blk * per + ol;
+        valid = i < count;
+        const int tap = valid ? (int)(i / ((int64_t)p.O * p.Cgi)) : 0;
+        const int ns = valid ? p.tap_splits[tap] : 0;
+        #pragma unroll 8
+        for (int k = way; k < ns; k += WAYS) s += p.part[(int64_t)k * count + i];
+    } else {
+        i = (blk - wblocks) * per + ol;
+        valid = i < p.O;
+        if (valid) {
+            #pragma unroll 8
+            for (int k = way; k < p.bias_splits; k += WAYS) s += p.bias_part[(int64_t)k * p.O + i];
+        }
+    }
+    if (WAYS > 1) {
+        part_sum[threadIdx.x] = s;
+        __syncthreads();
+        if (way != 0) return;
+        #pragma unroll
+        for (int w = 1; w < WAYS; ++w) s += part_sum[w * per + ol];
+    }
+    if (!valid) return;
+    if (blk < wblocks) {
         const int c = (int)(i % p.Cgi);
         const int64_t t2 = i / p.Cgi;
         const int o = (int)(t2 % p.O);
         const int tap = (int)(t2 / p.O);
-        float s = 0.f;
-        for (int k = 0; k < p.tap_splits[tap]; ++k) s += p.part[(int64_t)k * count + i];
         p.dw[((int64_t)o * p.Cgi + c) * p.kHW + tap] = s;
+    } else {
+        p.db[i] = s;
     }
+}
+
+template <int WAYS>
+void launch_wgrad_reduce_ways(const ReduceParams &p, cudaStream_t s)
+{
+    constexpr int per = kReduceThreads / WAYS;
+    const int64_t count = (int64_t)p.kHW * p.O * p.Cgi;
+    const int64_t blocks = (count + per - 1) / per + (p.bias_part ? (p.O + per - 1) / per : 0);
+    wgrad_reduce_kernel<WAYS><<<(unsigned)blocks, kReduceThreads, 0, s>>>(p);
+}
+
+// One thread per output up to 32 slices (measured faster there than splitting the sum);
+// past that 2, 4 or 8 ways, so that no thread sums more than 32 slices.
+void launch_wgrad_reduce(const ReduceParams &p, cudaStream_t s)
+{
+    int max_splits = p.bias_part ? p.bias_splits : 1;
+    for (int t = 0; t < p.kHW; ++t) max_splits = std::max(max_splits, p.tap_splits[t]);
+    if (max_splits <= 32) launch_wgrad_reduce_ways<1>(p, s);
+    else if (max_splits <= 64) launch_wgrad_reduce_ways<2>(p, s);
+    else if (max_splits <= 128) launch_wgrad_reduce_ways<4>(p, s);
+    else launch_wgrad_reduce_ways<8>(p, s);
 }
 
 // ===========================================================================
@@ -2178,18 +2233,22 @@ gconv_status launch_corr2_kernel(Corr2Launch &L, const __nv_bfloat16 *ub, const 
     return GCONV_OK;
 }
 
+// The correlation kernel's blocked input copy and packed weights, in one launch, into ws.
+void launch_corr2_copy(Corr2Launch &L, const void *U, const void *w, uint8_t *ws, cudaStream_t s)
+{
+    L.bu.in = static_cast<const __nv_bfloat16 *>(U);
+    L.bu.out = reinterpret_cast<__nv_bfloat16 *>(ws);
+    L.pk.w = static_cast<const __nv_bfloat16 *>(w);
+    L.pk.out = ws + L.ub_bytes;
+    const int nb_a = blockify_blocks(L.bu);
+    blockify_pack_kernel<<<nb_a + pack2_blocks(L.pk), kBlockifyThreads, 0, s>>>(L.bu, L.pk, nb_a);
+}
+
 gconv_status launch_corr2(Corr2Launch &L, const void *U, const void *w, const void *bias, float *out, int out_bf16,
                           uint8_t *ws, cudaStream_t s)
 {
-    __nv_bfloat16 *ub = reinterpret_cast<__nv_bfloat16 *>(ws);
-    uint8_t *wpk = ws + L.ub_bytes;
-    L.bu.in = static_cast<const __nv_bfloat16 *>(U);
-    L.bu.out = ub;
-    L.pk.w = static_cast<const __nv_bfloat16 *>(w);
-    L.pk.out = wpk;
-    const int nb_a = blockify_blocks(L.bu);
-    blockify_pack_kernel<<<nb_a + pack2_blocks(L.pk), kBlockifyThreads, 0, s>>>(L.bu, L.pk, nb_a);
-    return launch_corr2_kernel(L, ub, wpk, bias, out, out_bf16, s);
+    launch_corr2_copy(L, U, w, ws, s);
+    return launch_corr2_kernel(L, reinterpret_cast<__nv_bfloat16 *>(ws), ws + L.ub_bytes, bias, out, out_bf16, s);
 }
 
 // Stride-2 backward-data: the blocked copy of gradOutput and phase 0's weights in one launch,
@@ -2284,9 +2343,7 @@ gconv_status launch_wgrad_blocked(WgradLaunch &L, const Geom &g, float *dw, floa
         rp.bias_splits = L.wp.grp_splits[0];
         *db_done = true;
     }
-    const int64_t count = (int64_t)g.Cout * g.Cgi * g.kH * g.kW;
-    const int blocks = (int)std::min<int64_t>((count + 255) / 256, (int64_t)num_sms() * 8);
-    wgrad_reduce_kernel<<<blocks, 256, 0, s>>>(rp);
+    launch_wgrad_reduce(rp, s);
     return GCONV_OK;
 }
 
@@ -2421,9 +2478,7 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
         rp.part = reinterpret_cast<float *>(wsb);
         rp.dw = out;
         rp.O = g.Cout; rp.Cgi = g.Cgi; rp.kHW = g.kH * g.kW;
-        const int64_t count = (int64_t)g.Cout * g.Cgi * g.kH * g.kW;
-        const int blocks = (int)std::min<int64_t>((count + 255) / 256, (int64_t)num_sms() * 8);
-        wgrad_reduce_kernel<<<blocks, 256, 0, s>>>(rp);
+        launch_wgrad_reduce(rp, s);
         return GCONV_OK;
     }
     if (pass == GCONV_PASS_BWD_WEIGHT) {
@@ -2511,6 +2566,38 @@ bool tc_step_build(const Geom &g, TcStep *S)
 
 }  // namespace
 
+// Side stream of the training step, per device: created on first use, kept until exit.
+// The mutex makes one step's fork/join sequence atomic with respect to other threads
+// (the events are shared).
+namespace {
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool tried = false;
+};
+std::mutex g_side_mutex;
+SideStream g_side[64];
+
+// Caller holds g_side_mutex.  nullptr when the stream cannot be made (the step then runs
+// on the caller's stream alone).
+SideStream *side_stream()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    SideStream &S = g_side[dev];
+    if (!S.tried) {
+        S.tried = true;
+        if (cudaStreamCreateWithFlags(&S.s, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&S.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&S.join, cudaEventDisableTiming) != cudaSuccess) {
+            S.s = nullptr;
+            cudaGetLastError();
+        }
+    }
+    return S.s ? &S : nullptr;
+}
+}  // namespace
+
 bool tc_step_plan(const Geom &g, size_t *ws_bytes, int *launches)
 {
     TcStep S;
@@ -2545,10 +2632,32 @@ gconv_status tc_step_launch(const Geom &g, const void *x, const void *w, const v
     wp.tma = 1;
     const bool fuse_bias = db && S.W.ones >= 0;
     S.F.bu.ones = fuse_bias ? S.W.ones : -1;   // zero-weighted in the forward pass
-    gconv_status st = launch_corr2(S.F, x, w, bias, y, g.out_bf16, wsb + S.off_fx, s);
-    if (st != GCONV_OK) return st;
-    if (marks) cudaEventRecord(marks[0], s);
-    st = launch_corr2(S.B, dy, w, nullptr, dx, g.out_bf16, wsb + S.off_bx, s);
+    gconv_status st = GCONV_OK;
+    {
+        // gradOutput's blocked copy runs on the side stream beside the forward correlation
+        // (a tensor-core-bound kernel that leaves HBM and issue slots free); the fork follows
+        // x's copy, so everything earlier on the caller's stream precedes it too
+        std::lock_guard<std::mutex> lock(g_side_mutex);
+        SideStream *side = side_stream();
+        launch_corr2_copy(S.F, x, w, wsb + S.off_fx, s);
+        if (side) {
+            if (cudaEventRecord(side->fork, s) != cudaSuccess || cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
+                return GCONV_ERR_CUDA;
+            launch_corr2_copy(S.B, dy, w, wsb + S.off_bx, side->s);
+            if (cudaEventRecord(side->join, side->s) != cudaSuccess) return GCONV_ERR_CUDA;
+        }
+        st = launch_corr2_kernel(S.F, reinterpret_cast<__nv_bfloat16 *>(wsb + S.off_fx), wsb + S.off_fx + S.F.ub_bytes,
+                                 bias, y, g.out_bf16, s);
+        if (st != GCONV_OK) return st;
+        if (marks) cudaEventRecord(marks[0], s);
+        if (side) {
+            if (cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess) return GCONV_ERR_CUDA;
+        } else {
+            launch_corr2_copy(S.B, dy, w, wsb + S.off_bx, s);
+        }
+    }
+    st = launch_corr2_kernel(S.B, reinterpret_cast<__nv_bfloat16 *>(wsb + S.off_bx), wsb + S.off_bx + S.B.ub_bytes,
+                             nullptr, dx, g.out_bf16, s);
     if (st != GCONV_OK) return st;
     if (marks) cudaEventRecord(marks[1], s);
     st = launch_wgrad_blocked(S.W, g, dw, fuse_bias ? db : nullptr, wsb + S.off_part, wsb + S.off_bias, s, db_done);
