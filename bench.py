@@ -24,7 +24,6 @@ exchange); the step time is the max over ranks and value sums all ranks' work.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -78,11 +77,18 @@ def algorithmic_bytes(geom, in_bytes=2):
             "bwd_weight_bias": x * in_bytes + y * in_bytes + w * 4 + Cout * 4}
 
 
+# The sources of the headline step's kernels and their launch planning (the tensor-core
+# convolution family and the headers it includes): recorded ncu traffic stays valid while
+# these are unchanged.
+STEP_SOURCES = ("bwd_gconv_fwd_gb300/csrc/tc_conv.cu", "bwd_gconv_fwd_gb300/csrc/ptx.cuh",
+                "bwd_gconv_fwd_gb300/csrc/internal.h", "bwd_gconv_fwd_gb300/csrc/common.cuh", "include/gconv.h")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "bwd_gconv_fwd_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode() + fh.read())
+    for rel in STEP_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(os.path.basename(rel).encode() + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -501,9 +507,11 @@ def fp32_peak_tflops(peaks):
     return sms * FP32_FMA_PER_SM_CLK * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
 
 
-def time_workload(wk, dev, reps, warmup, flush, peaks):
+def time_workload(wk, dev, reps, warmup, flush, peaks, only=None):
     """Per-pass timing of one workload: CUDA events on the current stream around each call, L2
-    flushed before every call, median of `reps` after `warmup`.  Returns the passes' records."""
+    flushed before every call, median of `reps` after `warmup`.  Returns the passes' records,
+    and the one-call step (gconv_step_ex: y, dx, dw and db) as "step".  `only`: names of the
+    calls to time (default all)."""
     import torch
     import bwd_gconv_fwd_gb300 as gc
     from bwd_gconv_fwd_gb300 import binding as B
@@ -521,6 +529,8 @@ def time_workload(wk, dev, reps, warmup, flush, peaks):
     db = torch.empty((Cout,), device=dev)
     wsb = max(16, max(gc.gconv_workspace_size(geom, dt, p) for p in range(4)))
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    swsb = max(16, gc.gconv_step_workspace_size(geom, dt))
+    sws = torch.empty(swsb, dtype=torch.uint8, device=dev)
     calls = {
         "fwd": lambda: B.gconv_fwd_ptr(geom, dt, x.data_ptr(), w.data_ptr(), b.data_ptr(), y.data_ptr(), ws.data_ptr(), wsb, sp),
         "bwd_data": lambda: B.gconv_bwd_data_ptr(geom, dt, dy.data_ptr(), w.data_ptr(), dx.data_ptr(), ws.data_ptr(), wsb, sp),
@@ -528,13 +538,19 @@ def time_workload(wk, dev, reps, warmup, flush, peaks):
         "bwd_bias": lambda: B.gconv_bwd_bias_ptr(geom, dt, dy.data_ptr(), db.data_ptr(), ws.data_ptr(), wsb, sp),
         "bwd_weight_bias": lambda: B.gconv_bwd_weight_ex_ptr(geom, dt, x.data_ptr(), dy.data_ptr(), dw.data_ptr(),
                                                              db.data_ptr(), ws.data_ptr(), wsb, sp),
+        "step": lambda: B.gconv_step_ex_ptr(geom, dt, B.GCONV_F32, x.data_ptr(), w.data_ptr(), b.data_ptr(),
+                                            dy.data_ptr(), y.data_ptr(), dx.data_ptr(), dw.data_ptr(), db.data_ptr(),
+                                            sws.data_ptr(), swsb, sp),
     }
+    if only:
+        calls = {k: v for k, v in calls.items() if k in only}
     pass_code = {"fwd": 0, "bwd_data": 1, "bwd_weight": 2, "bwd_bias": 3, "bwd_weight_bias": 2}
     in_bytes = 2 if wk.dtype == "bf16" else 4
     fpp = flop_per_pass(geom)
     abytes = algorithmic_bytes(geom, in_bytes)
     hbm = peaks["hbm_gbs"] * 1e9
     out = {}
+    step_rec = None
     for nm, f in calls.items():
         times = []
         for k in range(warmup + reps):
@@ -547,6 +563,11 @@ def time_workload(wk, dev, reps, warmup, flush, peaks):
             if k >= warmup:
                 times.append(e0.elapsed_time(e1) * 1e-3)
         t = statistics.median(times)
+        if nm == "step":
+            shared, launches = gc.gconv_step_plan(geom, dt)
+            step_rec = {"us": t * 1e6, "shared_copies": shared, "launches": launches,
+                        "tflops": 3 * fpp / t / 1e12}
+            continue
         path, launches = gc.gconv_plan(geom, dt, pass_code[nm])
         pname = gc.PATH_NAMES[path]
         t_mem = abytes[nm] / hbm
@@ -562,12 +583,16 @@ def time_workload(wk, dev, reps, warmup, flush, peaks):
                    "bound": "hbm" if t_mem >= t_cmp else ("tensor" if unit_peak.startswith("bf16") else "fp32"),
                    "roofline_us": max(t_mem, t_cmp) * 1e6, "roofline_frac": max(t_mem, t_cmp) / t}
     assert gc.gconv_check_device_error(st) == B.GCONV_OK
-    step = ("fwd", "bwd_data", "bwd_weight_bias")      # the step: weight and bias gradients from one call
-    step_us = sum(out[k]["us"] for k in step)
-    roof_us = sum(out[k]["roofline_us"] for k in step)
-    return {"passes": out, "step": "+".join(step), "step_us": step_us,
-            "step_tflops": 3 * fpp / (step_us * 1e-6) / 1e12,
-            "step_roofline_frac": roof_us / step_us, "gflop_per_pass": fpp / 1e9}
+    rec = {"passes": out, "gflop_per_pass": fpp / 1e9}
+    step = ("fwd", "bwd_data", "bwd_weight_bias")      # the step's passes (weight and bias gradients in one)
+    if all(k in out for k in step):
+        roof_us = sum(out[k]["roofline_us"] for k in step)
+        rec["passes_sum_us"] = sum(out[k]["us"] for k in step)
+        if step_rec:
+            step_rec["roofline_frac"] = roof_us / step_rec["us"]
+    if step_rec:
+        rec["step"] = step_rec
+    return rec
 
 
 # The other configurations of the metric, each timed pass by pass (c1 also as a graph, in
@@ -607,8 +632,9 @@ def bench_sweep(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     layers = dict(wl.model_zoo(32))
     layers.update(wl.pointwise_zoo(32))
+    only = set(args.passes.split(",")) if args.passes else None
     for name, wk in layers.items():
-        rec = time_workload(wk, dev, args.steps, args.warmup, flush, peaks)
+        rec = time_workload(wk, dev, args.steps, args.warmup, flush, peaks, only)
         print(json.dumps({"sweep": name, "geom": list(wk.geom), "gflop_per_pass": rec["gflop_per_pass"],
                           "passes": rec["passes"], "peak_source": peak_src}), flush=True)
     return 0
@@ -628,7 +654,8 @@ def bench_one_workload(args):
     zoo = dict(wl.model_zoo(32))
     zoo.update(wl.pointwise_zoo(32))
     wk = wl.WORKLOADS[args.workload] if args.workload in wl.WORKLOADS else zoo[args.workload]
-    rec = time_workload(wk, dev, args.steps, args.warmup, flush, peaks)
+    only = set(args.passes.split(",")) if args.passes else None
+    rec = time_workload(wk, dev, args.steps, args.warmup, flush, peaks, only)
     rec["workload"] = config_dict(wk)["workload"]
     rec["peak_source"] = peak_src
     print(json.dumps(rec), flush=True)
@@ -646,6 +673,9 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config pass timings")
     ap.add_argument("--sweep", action="store_true", help="time the model-zoo layer sweep instead")
     ap.add_argument("--workload", default=None, help="time the passes of one named workload only")
+    ap.add_argument("--passes", default=None,
+                    help="with --workload: comma list of calls to time (fwd, bwd_data, bwd_weight, bwd_bias, "
+                         "bwd_weight_bias, step)")
     args = ap.parse_args()
     if args.workload:
         return bench_one_workload(args)
