@@ -636,7 +636,7 @@ def bench_sweep(args):
     for name, wk in layers.items():
         rec = time_workload(wk, dev, args.steps, args.warmup, flush, peaks, only)
         print(json.dumps({"sweep": name, "geom": list(wk.geom), "gflop_per_pass": rec["gflop_per_pass"],
-                          "passes": rec["passes"], "peak_source": peak_src}), flush=True)
+                          "passes": rec["passes"], "step": rec.get("step"), "peak_source": peak_src}), flush=True)
     return 0
 
 
