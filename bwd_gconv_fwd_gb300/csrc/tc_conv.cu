@@ -924,20 +924,27 @@ struct Corr2Params {
     int out_bf16;
     unsigned int *err;
     uint64_t wait_ns;
-    int N, G, Cu, Cv, Qh, Qw, R, Wp, nchu;
-    int n_ptile, n_vtile, n_tiles;  // position tiles per image, 128-channel tiles, all tiles
+    int N, G, Cu, Cv, R, Wp, nchu;
+    int n_vtile, n_tiles;       // 128-channel tiles, all tiles
     int nmma;                   // MMA N: 256, or 240 with paired taps
     int tile_pos;               // output positions per tile: nmma, or nmma - pair_delta with paired taps
     int pair_delta;             // paired taps: the second tap's row shift past the first (0: unpaired)
-    // output grid: element (qh, qw) of the tile grid is output (qh*o_sh + o_rh, qw*o_sw + o_rw)
-    // of planes oH x oW (a stride-2 backward-data phase writes every o_sh-th row and column)
-    int oH, oW, o_sh, o_sw, o_rh, o_rw;
     int stage_rows;             // positions staged per chunk (nmma + farthest tap, multiple of 8)
     int nsb, wstages;           // staging buffers (1 or 2), weight ring depth (3 or 4)
     int nchc;                   // 64-channel chunks of the reduced channels (nchu / stride phases)
-    int nblk;                   // weight blocks per tile: every chunk's taps (or tap pairs)
-    int blk0[kMaxChunk + 1];    // first block of each staged chunk (a stride phase has its own taps)
+    int nblk;                   // weight blocks of all output phases ([g][vt][nblk] packed blocks)
     int tap_off[kMaxBlk];       // row shift of each block's (first) tap
+    // Output phases: one launch may carry several (the output phases of a stride-2
+    // backward-data pass), each with its own taps over the same blocked copy.  Tiles
+    // [ph_tile0[i], ph_tile0[i+1]) belong to phase i; element (qh, qw) of its grid is output
+    // (qh*o_sh + o_rh[i], qw*o_sw + o_rw[i]) of planes oH x oW, for qh < Qh[i], qw < Qw[i].
+    // The plain forms have one phase (o_sh = o_sw = 1, o_rh = o_rw = 0).
+    int nph;
+    int ph_tile0[kMaxPlanes + 1];
+    int oH, oW, o_sh, o_sw;
+    int Qh[kMaxPlanes], Qw[kMaxPlanes], o_rh[kMaxPlanes], o_rw[kMaxPlanes];
+    int n_ptile[kMaxPlanes];    // position tiles per image
+    int blk0[kMaxPlanes][kMaxChunk + 1];   // phase i's blocks of staged chunk kc: [blk0[i][kc], blk0[i][kc+1])
     unsigned long long *trace;  // optional per-CTA phase stamps (kTraceWords each), nullptr when off
 };
 
@@ -955,9 +962,13 @@ constexpr int kC2EpiBytes = 2 * kC2EpiWarps * 32 * 33 * 4;   // a 32 x 33 transp
 // chunks, for weight blocks and for a free accumulator (ns), time of the last MMA,
 // epilogue warp 0's waits for accumulators (ns), end.
 
-__device__ __forceinline__ void corr2_tile(const Corr2Params &p, int t, int *ptile, int *n, int *vt, int *g)
+__device__ __forceinline__ void corr2_tile(const Corr2Params &p, int t, int *ph, int *ptile, int *n, int *vt, int *g)
 {
-    *ptile = t % p.n_ptile; t /= p.n_ptile;
+    int i = 0;
+    while (i + 1 < p.nph && t >= p.ph_tile0[i + 1]) ++i;
+    *ph = i;
+    t -= p.ph_tile0[i];
+    *ptile = t % p.n_ptile[i]; t /= p.n_ptile[i];
     *n = t % p.N; t /= p.N;
     *vt = t % p.n_vtile;
     *g = t / p.n_vtile;
@@ -1057,8 +1068,8 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
         int seq = 0;
         bool stop = false;
         for (int t = blockIdx.x; t < p.n_tiles && !stop; t += gridDim.x) {
-            int ptile, n, vt, g;
-            corr2_tile(p, t, &ptile, &n, &vt, &g);
+            int oph, ptile, n, vt, g;
+            corr2_tile(p, t, &oph, &ptile, &n, &vt, &g);
             const int p0 = ptile * p.tile_pos;
             for (int kc = 0; kc < p.nchu; ++kc, ++seq) {
                 const int sb = seq % p.nsb;
@@ -1091,10 +1102,12 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
             int b = 0, last = -1;
             bool stop = false;
             for (int t = blockIdx.x; t < p.n_tiles && !stop; t += gridDim.x) {
-                int ptile, n, vt, g;
-                corr2_tile(p, t, &ptile, &n, &vt, &g);
+                int oph, ptile, n, vt, g;
+                corr2_tile(p, t, &oph, &ptile, &n, &vt, &g);
+                // this tile's phase's blocks, in the order the issuer consumes them
                 const uint8_t *wsrc = p.Wpk + ((size_t)g * p.n_vtile + vt) * (size_t)nblocks * kWblkBytes;
-                for (int j = 0; j < nblocks; ++j, ++b) {
+                const int jend = p.blk0[oph][p.nchu];
+                for (int j = p.blk0[oph][0]; j < jend; ++j, ++b) {
                     if (b % p.wstages != q) continue;
                     if (b >= p.wstages &&
                         !ptx::mbar_wait(ptx::smem_u32(&bar_wempty[q]), (b / p.wstages - 1) & 1, p.wait_ns)) {
@@ -1129,6 +1142,8 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
             int k = 0;
             for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++k) {
                 const int acc = k & 1;
+                int oph = 0;
+                while (oph + 1 < p.nph && t >= p.ph_tile0[oph + 1]) ++oph;
                 if (k >= 2) {
                     const uint32_t bar = ptx::smem_u32(&bar_aempty[acc]);
                     const uint32_t ph = (k / 2 - 1) & 1;
@@ -1155,7 +1170,7 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                     const uint64_t bdesc_c = bdesc0 + (uint64_t)((sb * stage_bytes) >> 4);
                     const int jc = kc % p.nchc;   // chunk kc: channel chunk jc of stride phase kc / nchc
                     const int nks = min(4, (p.Cu - 64 * jc + 15) >> 4);
-                    const int b0 = p.blk0[kc], nbk = p.blk0[kc + 1] - b0;
+                    const int b0 = p.blk0[oph][kc], nbk = p.blk0[oph][kc + 1] - b0;
                     const int *toff = tap_off_sh + b0;
                     const uint32_t acc_first = kc > 0 ? 1u : 0u;
                     const uint32_t wf0 = ptx::smem_u32(&bar_wfull[0]), we0 = ptx::smem_u32(&bar_wempty[0]);
@@ -1198,8 +1213,9 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
         uint64_t w_epi = 0;
         int k = 0;
         for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++k) {
-            int ptile, n, vt, g;
-            corr2_tile(p, t, &ptile, &n, &vt, &g);
+            int oph, ptile, n, vt, g;
+            corr2_tile(p, t, &oph, &ptile, &n, &vt, &g);
+            const int Qh = p.Qh[oph], Qw = p.Qw[oph], o_rh = p.o_rh[oph], o_rw = p.o_rw[oph];
             const int acc = k & 1;
             const uint64_t t0 = trace ? ptx::globaltimer() : 0;
             bool ready = ptx::mbar_wait(ptx::smem_u32(&bar_afull[acc]), (k / 2) & 1, p.wait_ns);
@@ -1243,8 +1259,8 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                         const int jc = pc + (lane & 15);
                         const int pos = p0 + jc;
                         const int qh = pos / p.Wp, qw = pos - qh * p.Wp;
-                        if (jc < p.tile_pos && qh < p.Qh && qw < p.Qw) {
-                            const int64_t o = vout + (int64_t)(qh * p.o_sh + p.o_rh) * p.oW + (qw * p.o_sw + p.o_rw);
+                        if (jc < p.tile_pos && qh < Qh && qw < Qw) {
+                            const int64_t o = vout + (int64_t)(qh * p.o_sh + o_rh) * p.oW + (qw * p.o_sw + o_rw);
                             if (p.out_bf16) {
                                 __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(p.V) + o;
                                 for (int vv = lane >> 4; vv < vcount; vv += 2)
@@ -1277,8 +1293,8 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                     __syncwarp();
                     const int pos = p0 + pc + lane;
                     const int qh = pos / p.Wp, qw = pos - qh * p.Wp;
-                    if (pc + lane < p.tile_pos && qh < p.Qh && qw < p.Qw) {
-                        const int64_t o = vout + (int64_t)(qh * p.o_sh + p.o_rh) * p.oW + (qw * p.o_sw + p.o_rw);
+                    if (pc + lane < p.tile_pos && qh < Qh && qw < Qw) {
+                        const int64_t o = vout + (int64_t)(qh * p.o_sh + o_rh) * p.oW + (qw * p.o_sw + o_rw);
                         if (p.out_bf16) {
                             __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(p.V) + o;
                             for (int vv = 0; vv < vcount; ++vv) ob[vv * out_hw] = __float2bfloat16_rn(tb[vv * 33 + lane]);
@@ -1856,6 +1872,27 @@ struct Corr2Launch {
     int grid = 0;
 };
 
+// Staging buffers, weight ring depth, shared memory and grid of a correlation launch whose
+// tiles and stage_rows are set: two staging buffers and four weight slots when they fit;
+// never below 120 KB, so that one CTA holds its SM (it takes all 512 TMEM columns).
+bool size_corr2(Corr2Launch *L)
+{
+    Corr2Params &c = L->cp;
+    const size_t stage = (size_t)c.stage_rows * 128;
+    const int shapes[3][2] = {{2, 4}, {2, 3}, {1, 4}};
+    bool fit = false;
+    for (const auto &sh : shapes) {
+        c.nsb = sh[0];
+        c.wstages = sh[1];
+        L->smem = 1024 + c.nsb * stage + (size_t)c.wstages * kWblkBytes + kC2EpiBytes;
+        if (L->smem <= kMaxSmem) { fit = true; break; }
+    }
+    if (!fit) return false;
+    L->smem = std::max(L->smem, (size_t)120 * 1024);
+    L->grid = std::min(c.n_tiles, num_sms());
+    return true;
+}
+
 // Correlation on the blocked layout: the forward pass, or backward-data as the correlation
 // of gradOutput with the mirrored taps (stride 1 makes every output position of dx a full
 // correlation, no phases).  A stride-2 forward pass reads its input as stride-phase planes:
@@ -1944,14 +1981,16 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L, int rh = -1, int 
         maxa = tg.maxa;
         maxb = tg.maxb;
     }
-    c.N = g.N; c.G = g.G; c.Cv = Cv; c.Qh = Qh; c.Qw = Qw;
+    c.N = g.N; c.G = g.G; c.Cv = Cv;
+    c.nph = 1;
+    c.Qh[0] = Qh; c.Qw[0] = Qw;
     c.Wp = Qw_grid + maxb;
     c.R = Qh_grid + maxa;
-    c.oH = Qh; c.oW = Qw; c.o_sh = 1; c.o_sw = 1; c.o_rh = 0; c.o_rw = 0;
+    c.oH = Qh; c.oW = Qw; c.o_sh = 1; c.o_sw = 1; c.o_rh[0] = 0; c.o_rw[0] = 0;
     if (bphase) {
         c.oH = g.H; c.oW = g.W;
         c.o_sh = g.s_h; c.o_sw = g.s_w;
-        c.o_rh = rh; c.o_rw = rw;
+        c.o_rh[0] = rh; c.o_rw[0] = rw;
     }
     c.nchc = (Cu + 63) / 64;
     c.nchu = nplanes * c.nchc;
@@ -1990,7 +2029,7 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L, int rh = -1, int 
     int nblk = 0;
     for (int kc = 0; kc < c.nchu; ++kc) {
         const int pl = kc / c.nchc, jc = kc % c.nchc;
-        c.blk0[kc] = nblk;
+        c.blk0[0][kc] = nblk;
         for (const auto &bk : plane_blk[pl]) {
             if (nblk >= kMaxBlk) return false;
             c.tap_off[nblk] = bk[0];
@@ -2000,7 +2039,7 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L, int rh = -1, int 
             ++nblk;
         }
     }
-    c.blk0[c.nchu] = nblk;
+    c.blk0[0][c.nchu] = nblk;
     c.nblk = nblk;
     c.pair_delta = pair ? g.d_w : 0;
     const int positions = Qh * c.Wp;   // padded output grid rows that hold real outputs
@@ -2013,23 +2052,12 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L, int rh = -1, int 
     }
     c.tile_pos = c.nmma - c.pair_delta;
     c.Cu = Cu;
-    c.n_ptile = (positions + c.tile_pos - 1) / c.tile_pos;
-    c.n_tiles = g.N * g.G * c.n_vtile * c.n_ptile;
+    c.n_ptile[0] = (positions + c.tile_pos - 1) / c.tile_pos;
+    c.n_tiles = g.N * g.G * c.n_vtile * c.n_ptile[0];
+    c.ph_tile0[0] = 0;
+    c.ph_tile0[1] = c.n_tiles;
     c.stage_rows = round_up(c.nmma + maxoff, 8);
-    const size_t stage = (size_t)c.stage_rows * 128;
-    // Two staging buffers and four weight slots when they fit; never below 120 KB, so
-    // that one CTA holds its SM (it takes all 512 TMEM columns).
-    const int shapes[3][2] = {{2, 4}, {2, 3}, {1, 4}};
-    bool fit = false;
-    for (const auto &sh : shapes) {
-        c.nsb = sh[0];
-        c.wstages = sh[1];
-        L->smem = 1024 + c.nsb * stage + (size_t)c.wstages * kWblkBytes + kC2EpiBytes;
-        if (L->smem <= kMaxSmem) { fit = true; break; }
-    }
-    if (!fit) return false;
-    L->smem = std::max(L->smem, (size_t)120 * 1024);
-    L->grid = std::min(c.n_tiles, num_sms());
+    if (!size_corr2(L)) return false;
     k.G = g.G; k.Cu = Cu; k.Cv = Cv; k.n_vtile = c.n_vtile; k.nblk = c.nblk;
     k.transpose = bwd_data ? 1 : 0;
     k.w_cin_g = g.Cgi; k.kHW = ntaps;
@@ -2069,7 +2097,68 @@ struct Corr2PhaseSet {
     int nzero = 0;                      // phases whose dx positions no tap reaches
     int zr[kMaxPlanes] = {}, zc[kMaxPlanes] = {};
     size_t ub_bytes = 0, wpk_off[kMaxPlanes] = {}, ws_bytes = 0;
+    bool merged = false;                // all phases in one launch (M)
+    Corr2Launch M;
 };
+
+// All output phases in one correlation launch.  The phases share the blocked copy's
+// geometry (rows, pitch, chunks), so their tiles run in one persistent grid, each tile
+// taking its phase's blocks, grid extent and output rows and columns from the launch's phase
+// tables, and all phases' weight blocks are packed by one launch ([g][vt][blocks of every
+// phase]).  One grid instead of one per phase: a phase has few tiles (a quarter of the
+// outputs), so a launch per phase gives each CTA a single tile and costs that tile's
+// latency.
+bool merge_corr2_phases(const Corr2PhaseSet &S, Corr2Launch *M)
+{
+    if (S.n < 1 || S.n > kMaxPlanes) return false;
+    *M = S.L[0];
+    Corr2Params &c = M->cp;
+    Pack2Params &k = M->pk;
+    int nblk = 0, nmma = 0, maxoff = 0;
+    for (int i = 0; i < S.n; ++i) {
+        const Corr2Params &q = S.L[i].cp;
+        if (q.nph != 1 || q.pair_delta || q.Cu != c.Cu || q.Cv != c.Cv || q.R != c.R || q.Wp != c.Wp ||
+            q.nchu != c.nchu || q.nchc != c.nchc || q.n_vtile != c.n_vtile || q.oH != c.oH || q.oW != c.oW ||
+            q.o_sh != c.o_sh || q.o_sw != c.o_sw || S.L[i].ub_bytes != M->ub_bytes)
+            return false;
+        nmma = std::max(nmma, q.nmma);
+        nblk += q.nblk;
+    }
+    if (nblk > kMaxBlk) return false;
+    c.nmma = nmma;
+    c.tile_pos = nmma;
+    c.nph = S.n;
+    int b = 0, tiles = 0;
+    for (int i = 0; i < S.n; ++i) {
+        const Corr2Params &q = S.L[i].cp;
+        const Pack2Params &qk = S.L[i].pk;
+        c.Qh[i] = q.Qh[0];
+        c.Qw[i] = q.Qw[0];
+        c.o_rh[i] = q.o_rh[0];
+        c.o_rw[i] = q.o_rw[0];
+        c.n_ptile[i] = (q.Qh[0] * c.Wp + c.tile_pos - 1) / c.tile_pos;
+        c.ph_tile0[i] = tiles;
+        tiles += c.N * c.G * c.n_vtile * c.n_ptile[i];
+        for (int kc = 0; kc <= c.nchu; ++kc) c.blk0[i][kc] = b + q.blk0[0][kc];
+        for (int j = 0; j < q.nblk; ++j) {
+            c.tap_off[b + j] = q.tap_off[j];
+            k.tk1[b + j] = qk.tk1[j];
+            k.tk2[b + j] = qk.tk2[j];
+            k.jc[b + j] = qk.jc[j];
+            maxoff = std::max(maxoff, q.tap_off[j]);
+        }
+        b += q.nblk;
+    }
+    c.ph_tile0[S.n] = tiles;
+    c.n_tiles = tiles;
+    c.nblk = nblk;
+    k.nblk = nblk;
+    c.stage_rows = round_up(c.nmma + maxoff, 8);
+    if (!size_corr2(M)) return false;
+    M->wpk_bytes = align256((size_t)c.G * c.n_vtile * c.nblk * kWblkBytes);
+    M->ws_bytes = M->ub_bytes + M->wpk_bytes;
+    return true;
+}
 
 bool build_corr2_phases(const Geom &g, Corr2PhaseSet *S)
 {
@@ -2098,6 +2187,8 @@ bool build_corr2_phases(const Geom &g, Corr2PhaseSet *S)
         off += S->L[i].wpk_bytes;
     }
     S->ws_bytes = off;
+    S->merged = merge_corr2_phases(*S, &S->M);
+    if (S->merged) S->ws_bytes = S->M.ws_bytes;
     return true;
 }
 
@@ -2257,6 +2348,16 @@ gconv_status launch_corr2_phases(Corr2PhaseSet &S, const Geom &g, const void *dy
                                  uint8_t *ws, cudaStream_t s)
 {
     __nv_bfloat16 *ub = reinterpret_cast<__nv_bfloat16 *>(ws);
+    if (S.merged) {
+        // the blocked copy with every phase's weights, zero fills, one correlation launch
+        launch_corr2_copy(S.M, dy, w, ws, s);
+        for (int z = 0; z < S.nzero; ++z) {
+            const int64_t planes = (int64_t)g.N * g.Cin;
+            zero_phase_kernel<<<num_sms() * 4, 256, 0, s>>>(out, planes, g.H, g.W, g.s_h, g.s_w, S.zr[z], S.zc[z],
+                                                            g.out_bf16);
+        }
+        return launch_corr2_kernel(S.M, ub, ws + S.M.ub_bytes, nullptr, out, g.out_bf16, s);
+    }
     for (int i = 0; i < S.n; ++i) {
         Corr2Launch &L = S.L[i];
         L.pk.w = static_cast<const __nv_bfloat16 *>(w);
@@ -2373,7 +2474,8 @@ bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p)
             Corr2PhaseSet S;
             if (build_corr2_phases(g, &S)) {
                 p->path = GCONV_PATH_TC_IGEMM;
-                p->launches = S.n + S.nzero + S.n;   // copy/packing launches, zero fills, correlations
+                // copy/packing launches, zero fills, correlations
+                p->launches = S.merged ? 2 + S.nzero : S.n + S.nzero + S.n;
                 p->ws_bytes = S.ws_bytes;
                 return true;
             }
