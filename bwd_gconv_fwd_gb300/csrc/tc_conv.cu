@@ -576,6 +576,8 @@ struct WgradParams {
     int grp_cta0[kMaxJobs + 1];  // first CTA index of each job group within cta_per_cg
     int grp_first[kMaxJobs + 1]; // jobs of group gi: [grp_first[gi], grp_first[gi+1])
     int grp_cols[kMaxJobs];      // TMEM columns allocated by group gi (power of two)
+    int grp_plane[kMaxJobs];     // stride-phase plane of x that group gi reads (0 at stride 1)
+    int nxplane;                 // stride-phase planes of x's blocked copy (1 at stride 1)
     int job_off[kMaxJobs], job_delta[kMaxJobs], job_count[kMaxJobs], job_col[kMaxJobs];
     int job_tapk[kMaxJobs][4];   // kh*kW + kw of the packed taps
     unsigned long long *trace;   // optional per-CTA phase stamps (kTraceWords each), nullptr when off
@@ -605,6 +607,7 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
     int gi = 0;
     while (gi + 1 < p.n_tgrp && r >= p.grp_cta0[gi + 1]) ++gi;
     const int split = r - p.grp_cta0[gi];
+    const int xpl = p.grp_plane[gi] * p.N * p.G * p.ncx;   // first blocked-copy plane of the group's x phase
     const int job0 = p.grp_first[gi], job1 = p.grp_first[gi + 1];
     const int tmem_cols = p.grp_cols[gi];
     const int total_tiles = p.N * p.n_rowblk;
@@ -693,7 +696,7 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
                     } else {
                         const int i = c - 2;
                         ptx::tma_load_3d(buf + (uint32_t)(dy_bytes + i * p.xb * 128), &p.tm_x, 0, pos0 + i * p.xb,
-                                         ((n * p.G + g) * p.ncx + ct), fb);
+                                         xpl + ((n * p.G + g) * p.ncx + ct), fb);
                     }
                 }
                 issued = k + 1;
@@ -730,7 +733,7 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
             for (int idx = threadIdx.x; idx < p.plane_elems * 8; idx += kStageThreads) {
                 const int m = idx >> 3, k = idx & 7;
                 const bool ok = pos0 + m < plane_x;
-                const __nv_bfloat16 *src = ok ? p.XT + ((((int64_t)n * p.G + g) * p.ncx + ct) * plane_x + pos0 + m) * 64 + k * 8
+                const __nv_bfloat16 *src = ok ? p.XT + ((xpl + ((int64_t)n * p.G + g) * p.ncx + ct) * plane_x + pos0 + m) * 64 + k * 8
                                               : p.XT;
                 ptx::cp_async16(buf + (uint32_t)(dy_bytes + m * 128 + ((k ^ (m & 7)) << 4)), src, ok ? 16u : 0u);
             }
@@ -1817,7 +1820,8 @@ bool size_wgrad(const Geom &g, WgradParams *wp, size_t *smem, int *grid)
 void set_wgrad_tma(WgradParams *w)
 {
     const uint64_t plane_x = (uint64_t)w->Rx * w->Wp, plane_y = (uint64_t)w->Ho * w->Wp;
-    w->tma = (encode_rows_tmap(&w->tm_x, w->XT, plane_x, (uint64_t)w->N * w->G * w->ncx, (uint32_t)w->xb) &&
+    const uint64_t planes_x = (uint64_t)w->N * w->G * w->ncx * std::max(1, w->nxplane);
+    w->tma = (encode_rows_tmap(&w->tm_x, w->XT, plane_x, planes_x, (uint32_t)w->xb) &&
               encode_rows_tmap(&w->tm_dy, w->DYT, plane_y, (uint64_t)w->N * w->G * w->ncy, (uint32_t)(w->TH * w->Wp)))
                  ? 1 : 0;
 }
@@ -2206,15 +2210,16 @@ __global__ void zero_phase_kernel(float *out, int64_t planes, int H, int W, int 
     }
 }
 
-// Stride 2: the input is blocked as its stride phases (one plane per phase) and every
-// phase runs the stride-1 weight-gradient kernel on its own taps, which are plain
-// shifts within its plane; the launches write disjoint taps of the same split-K
-// slices, and one reduction adds them.
+// Stride 2: the input is blocked as its stride phases (one plane per phase).  A strided
+// tap is a plain shift within its phase's plane, so each phase's taps form ordinary
+// stride-1 jobs; one launch carries the job groups of every phase (group gi reads x plane
+// grp_plane[gi]), so the phases share one grid of CTAs.  Each tap belongs to one phase, so
+// the groups write disjoint taps of the split-K slices, and one reduction adds them.
 struct WgradPhaseLaunch {
     int nphase = 0;
-    WgradParams wp[kMaxPlanes];
-    size_t smem[kMaxPlanes] = {};
-    int grid[kMaxPlanes] = {};
+    WgradParams wp;
+    size_t smem = 0;
+    int grid = 0;
     PhaseBlockifyParams bx;
     BlockifyParams by;
     size_t part_bytes = 0, xt_bytes = 0, xplane_elems = 0, yt_bytes = 0, ws_bytes = 0;
@@ -2238,8 +2243,12 @@ bool build_wgrad_phases(const Geom &g, WgradPhaseLaunch *L)
     if (c.TH < 1) return false;
     c.n_rowblk = (g.Ho + c.TH - 1) / c.TH;
     c.plane_elems = round_up(128 + tg.maxa * c.Wp + tg.maxb + 8, 8);
-    int max_splits = 1;
+    c.nxplane = tg.nplanes;
     L->nphase = tg.nplanes;
+    WgradParams &m = L->wp;
+    m = c;
+    int njob = 0;
+    m.n_tgrp = 0;
     for (int pl = 0; pl < tg.nplanes; ++pl) {
         TapGeometry sub;
         sub.nplanes = 1;
@@ -2253,13 +2262,30 @@ bool build_wgrad_phases(const Geom &g, WgradPhaseLaunch *L)
                 sub.tap_b.push_back(tg.tap_b[i]);
                 st.push_back(taps[i]);
             }
-        WgradParams &w = L->wp[pl];
-        w = c;
+        if (st.empty()) continue;
+        WgradParams w = c;
         if (!build_wgrad_jobs(sub, st, w.Wp, &w)) return false;
-        if (!size_wgrad(g, &w, &L->smem[pl], &L->grid[pl])) return false;
-        max_splits = std::max(max_splits, w.splits);
+        const int nj = w.grp_first[w.n_tgrp];
+        if (m.n_tgrp + w.n_tgrp > kMaxJobs || njob + nj > kMaxJobs) return false;
+        for (int gq = 0; gq < w.n_tgrp; ++gq) {
+            m.grp_first[m.n_tgrp + gq] = njob + w.grp_first[gq];
+            m.grp_cols[m.n_tgrp + gq] = w.grp_cols[gq];
+            m.grp_plane[m.n_tgrp + gq] = pl;
+        }
+        for (int j = 0; j < nj; ++j) {
+            m.job_off[njob + j] = w.job_off[j];
+            m.job_delta[njob + j] = w.job_delta[j];
+            m.job_count[njob + j] = w.job_count[j];
+            m.job_col[njob + j] = w.job_col[j];
+            for (int q = 0; q < 4; ++q) m.job_tapk[njob + j][q] = w.job_tapk[j][q];
+        }
+        m.n_tgrp += w.n_tgrp;
+        njob += nj;
     }
-    L->part_bytes = align256((size_t)max_splits * g.Cout * g.Cgi * c.kHW * sizeof(float));
+    if (m.n_tgrp == 0) return false;
+    m.grp_first[m.n_tgrp] = njob;
+    if (!size_wgrad(g, &m, &L->smem, &L->grid)) return false;
+    L->part_bytes = align256((size_t)m.splits * g.Cout * g.Cgi * c.kHW * sizeof(float));
     L->xplane_elems = (size_t)g.N * g.G * c.ncx * c.Rx * c.Wp * 64;
     L->xt_bytes = align256((size_t)tg.nplanes * L->xplane_elems * 2);
     L->yt_bytes = align256((size_t)g.N * g.G * c.ncy * g.Ho * c.Wp * 64 * 2);
@@ -2500,7 +2526,7 @@ bool tc_igemm_plan(const Geom &g, gconv_pass pass, Plan *p)
         WgradPhaseLaunch L;
         if (!build_wgrad_phases(g, &L)) return false;
         p->path = GCONV_PATH_TC_IGEMM;
-        p->launches = 3 + L.nphase;   // two blocked copies, a weight-gradient kernel per phase, the reduction
+        p->launches = 4;   // two blocked copies, the weight-gradient kernel, the reduction
         p->ws_bytes = L.ws_bytes;
         return true;
     }
@@ -2563,20 +2589,18 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
         launch_blockify(L.by, s);
         if (!smem_attr_once((const void *)wgrad_kernel, 1)) return GCONV_ERR_CUDA;
         ReduceParams rp{};
-        for (int pl = 0; pl < L.nphase; ++pl) {
-            WgradParams &w = L.wp[pl];
-            w.XT = xt + (size_t)pl * L.xplane_elems;
-            w.DYT = yt;
-            set_wgrad_tma(&w);
-            w.part = reinterpret_cast<float *>(wsb);
-            w.err = err;
-            w.wait_ns = (uint64_t)wait_limit();
-            w.trace = nullptr;
-            wgrad_kernel<<<L.grid[pl], kTcThreads, L.smem[pl], s>>>(w);
-            for (int gi = 0; gi < w.n_tgrp; ++gi)
-                for (int jb = w.grp_first[gi]; jb < w.grp_first[gi + 1]; ++jb)
-                    for (int c = 0; c < w.job_count[jb]; ++c) rp.tap_splits[w.job_tapk[jb][c]] = w.grp_splits[gi];
-        }
+        WgradParams &w = L.wp;
+        w.XT = xt;
+        w.DYT = yt;
+        set_wgrad_tma(&w);
+        w.part = reinterpret_cast<float *>(wsb);
+        w.err = err;
+        w.wait_ns = (uint64_t)wait_limit();
+        w.trace = nullptr;
+        wgrad_kernel<<<L.grid, kTcThreads, L.smem, s>>>(w);
+        for (int gi = 0; gi < w.n_tgrp; ++gi)
+            for (int jb = w.grp_first[gi]; jb < w.grp_first[gi + 1]; ++jb)
+                for (int c = 0; c < w.job_count[jb]; ++c) rp.tap_splits[w.job_tapk[jb][c]] = w.grp_splits[gi];
         rp.part = reinterpret_cast<float *>(wsb);
         rp.dw = out;
         rp.O = g.Cout; rp.Cgi = g.Cgi; rp.kHW = g.kH * g.kW;
