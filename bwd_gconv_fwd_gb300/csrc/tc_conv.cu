@@ -469,7 +469,7 @@ int blockify_blocks(const BlockifyParams &b)
     return (int)((total + kBlockifyThreads - 1) / kBlockifyThreads);
 }
 
-__global__ void __launch_bounds__(kBlockifyThreads)
+__global__ void __launch_bounds__(kBlockifyThreads, 4)
 blockify_kernel(const __grid_constant__ BlockifyParams p)
 {
     blockify_block(p, blockIdx.x);
@@ -477,7 +477,7 @@ blockify_kernel(const __grid_constant__ BlockifyParams p)
 
 // Two blocked copies in one launch (the weight gradient's x and gradOutput): blocks
 // [0, nb_a) build a, the rest b.
-__global__ void __launch_bounds__(kBlockifyThreads)
+__global__ void __launch_bounds__(kBlockifyThreads, 4)
 blockify2_kernel(const __grid_constant__ BlockifyParams a, const __grid_constant__ BlockifyParams b, int nb_a)
 {
     if ((int)blockIdx.x < nb_a) blockify_block(a, blockIdx.x);
@@ -497,7 +497,7 @@ struct PhaseBlockifyParams {
     int roff[kMaxPlanes], coff[kMaxPlanes];
 };
 
-__global__ void __launch_bounds__(kBlockifyThreads)
+__global__ void __launch_bounds__(kBlockifyThreads, 4)
 blockify_phase_kernel(const __grid_constant__ PhaseBlockifyParams p)
 {
     const int plane_out = p.R * p.C;
@@ -1379,7 +1379,7 @@ int pack2_blocks(const Pack2Params &p)
 
 // The correlation kernel's blocked input copy and weight packing in one launch: blocks
 // [0, nb_a) build the copy, the remaining ones pack the weights.
-__global__ void __launch_bounds__(kBlockifyThreads)
+__global__ void __launch_bounds__(kBlockifyThreads, 4)
 blockify_pack_kernel(const __grid_constant__ BlockifyParams a, const __grid_constant__ Pack2Params pk, int nb_a)
 {
     if ((int)blockIdx.x < nb_a) blockify_block(a, blockIdx.x);
