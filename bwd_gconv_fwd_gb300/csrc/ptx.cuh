@@ -255,5 +255,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, 
          | ((uint32_t)(M >> 4) << 24);        // M / 16
 }
 
+// Programmatic dependent launch.  griddep_wait: wait until the grids this launch depends on
+// have completed and their memory operations are visible (returns at once when it was not
+// launched as a programmatic dependent).  griddep_launch_dependents: this CTA allows the
+// next launch on the stream to start (its CTAs then take resources as they free up, and
+// wait in griddep_wait before touching memory).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace ptx
 }  // namespace gconv

@@ -45,6 +45,28 @@
 
 namespace gconv {
 
+// Launches a kernel as a programmatic dependent of the previous kernel on the stream: its
+// CTAs may be placed (and run their prologue) while that kernel drains.  Every kernel
+// launched this way calls ptx::griddep_wait before it touches global memory, so the result
+// is the same as a plain launch.  Errors surface through cudaGetLastError.
+template <typename... KArgs, typename... Args>
+void launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                      const Args &...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+
 constexpr int kStageWarps = 8;                      // staging + epilogue warps
 constexpr int kStageThreads = kStageWarps * 32;
 constexpr int kWarpAux = kStageWarps;               // TMEM allocation, weight producer
@@ -472,6 +494,7 @@ int blockify_blocks(const BlockifyParams &b)
 __global__ void __launch_bounds__(kBlockifyThreads, 4)
 blockify_kernel(const __grid_constant__ BlockifyParams p)
 {
+    ptx::griddep_wait();   // a programmatic dependent reads and writes nothing before this
     blockify_block(p, blockIdx.x);
 }
 
@@ -480,6 +503,7 @@ blockify_kernel(const __grid_constant__ BlockifyParams p)
 __global__ void __launch_bounds__(kBlockifyThreads, 4)
 blockify2_kernel(const __grid_constant__ BlockifyParams a, const __grid_constant__ BlockifyParams b, int nb_a)
 {
+    ptx::griddep_wait();   // a programmatic dependent reads and writes nothing before this
     if ((int)blockIdx.x < nb_a) blockify_block(a, blockIdx.x);
     else blockify_block(b, blockIdx.x - nb_a);
 }
@@ -660,6 +684,11 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
+    // programmatic dependent: the prologue overlaps the previous kernel's tail; global memory
+    // is touched only after it completes.  One CTA holds its SM to the end, so the next launch
+    // may start now.
+    ptx::griddep_wait();
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
 
     if (warp < kStageWarps && p.tma) {
         // ---------------- staging by TMA: producer q (warp q, lane 0) issues copy q of each tile ----------------
@@ -1058,6 +1087,11 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
+    // launched as a programmatic dependent: the prologue above overlaps the previous kernel's
+    // tail; nothing in global memory is touched before that kernel has completed.  This CTA
+    // holds its SM to the end, so the next launch may start now (its CTAs land as ours exit).
+    ptx::griddep_wait();
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
     unsigned long long *trace = p.trace ? p.trace + (size_t)blockIdx.x * kTraceWords : nullptr;
     if (trace && threadIdx.x == 0) {
         trace[0] = ptx::globaltimer();
@@ -1382,6 +1416,7 @@ int pack2_blocks(const Pack2Params &p)
 __global__ void __launch_bounds__(kBlockifyThreads, 4)
 blockify_pack_kernel(const __grid_constant__ BlockifyParams a, const __grid_constant__ Pack2Params pk, int nb_a)
 {
+    ptx::griddep_wait();   // a programmatic dependent reads and writes nothing before this
     if ((int)blockIdx.x < nb_a) blockify_block(a, blockIdx.x);
     else pack2_body(pk, blockIdx.x - nb_a, gridDim.x - nb_a);
 }
@@ -1406,6 +1441,7 @@ template <int WAYS>
 __global__ void __launch_bounds__(kReduceThreads)
 wgrad_reduce_kernel(const __grid_constant__ ReduceParams p)
 {
+    ptx::griddep_wait();   // a programmatic dependent reads nothing before this
     __shared__ float part_sum[WAYS > 1 ? kReduceThreads : 1];
     constexpr int per = kReduceThreads / WAYS;             // outputs per block
     const int ol = threadIdx.x % per, way = threadIdx.x / per;
@@ -1455,7 +1491,7 @@ void launch_wgrad_reduce_ways(const ReduceParams &p, cudaStream_t s)
     constexpr int per = kReduceThreads / WAYS;
     const int64_t count = (int64_t)p.kHW * p.O * p.Cgi;
     const int64_t blocks = (count + per - 1) / per + (p.bias_part ? (p.O + per - 1) / per : 0);
-    wgrad_reduce_kernel<WAYS><<<(unsigned)blocks, kReduceThreads, 0, s>>>(p);
+    launch_dependent(wgrad_reduce_kernel<WAYS>, (unsigned)blocks, kReduceThreads, 0, s, p);
 }
 
 // One thread per output up to 32 slices (measured faster there than splitting the sum);
@@ -2346,7 +2382,7 @@ gconv_status launch_corr2_kernel(Corr2Launch &L, const __nv_bfloat16 *ub, const 
     L.cp.trace = (trace && trace_bytes >= (size_t)L.grid * kTraceWords * 8) ? static_cast<unsigned long long *>(trace)
                                                                               : nullptr;
     if (!smem_attr_once((const void *)corr2_kernel, 2)) return GCONV_ERR_CUDA;
-    corr2_kernel<<<L.grid, kC2Threads, L.smem, s>>>(L.cp);
+    launch_dependent(corr2_kernel, (unsigned)L.grid, kC2Threads, L.smem, s, L.cp);
     return GCONV_OK;
 }
 
@@ -2358,7 +2394,7 @@ void launch_corr2_copy(Corr2Launch &L, const void *U, const void *w, uint8_t *ws
     L.pk.w = static_cast<const __nv_bfloat16 *>(w);
     L.pk.out = ws + L.ub_bytes;
     const int nb_a = blockify_blocks(L.bu);
-    blockify_pack_kernel<<<nb_a + pack2_blocks(L.pk), kBlockifyThreads, 0, s>>>(L.bu, L.pk, nb_a);
+    launch_dependent(blockify_pack_kernel, (unsigned)(nb_a + pack2_blocks(L.pk)), kBlockifyThreads, 0, s, L.bu, L.pk, nb_a);
 }
 
 gconv_status launch_corr2(Corr2Launch &L, const void *U, const void *w, const void *bias, float *out, int out_bf16,
@@ -2456,7 +2492,7 @@ gconv_status launch_wgrad_blocked(WgradLaunch &L, const Geom &g, float *dw, floa
     L.wp.trace = (trace && trace_bytes >= (size_t)L.grid * kTraceWords * 8) ? static_cast<unsigned long long *>(trace)
                                                                              : nullptr;
     if (!smem_attr_once((const void *)wgrad_kernel, 1)) return GCONV_ERR_CUDA;
-    wgrad_kernel<<<L.grid, kTcThreads, L.smem, s>>>(L.wp);
+    launch_dependent(wgrad_kernel, (unsigned)L.grid, kTcThreads, L.smem, s, L.wp);
     ReduceParams rp{};
     rp.part = L.wp.part;
     rp.dw = dw;
@@ -2597,7 +2633,7 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
         w.err = err;
         w.wait_ns = (uint64_t)wait_limit();
         w.trace = nullptr;
-        wgrad_kernel<<<L.grid, kTcThreads, L.smem, s>>>(w);
+        launch_dependent(wgrad_kernel, (unsigned)L.grid, kTcThreads, L.smem, s, w);
         for (int gi = 0; gi < w.n_tgrp; ++gi)
             for (int jb = w.grp_first[gi]; jb < w.grp_first[gi + 1]; ++jb)
                 for (int c = 0; c < w.job_count[jb]; ++c) rp.tap_splits[w.job_tapk[jb][c]] = w.grp_splits[gi];
@@ -2620,7 +2656,7 @@ gconv_status tc_igemm_launch(const Geom &g, const Plan &, gconv_pass pass, const
         L.by.out = yt;
         {
             const int nb_x = blockify_blocks(L.bx), nb_y = blockify_blocks(L.by);
-            blockify2_kernel<<<nb_x + nb_y, kBlockifyThreads, 0, s>>>(L.bx, L.by, nb_x);
+            launch_dependent(blockify2_kernel, (unsigned)(nb_x + nb_y), kBlockifyThreads, 0, s, L.bx, L.by, nb_x);
         }
         L.wp.XT = xt;
         L.wp.DYT = yt;

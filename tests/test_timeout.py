@@ -25,6 +25,8 @@ CASES = [
     ("stride-1 correlation (backward-data)", (3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2), B.PASS_BWD_DATA,
      B.PATH_TC_IGEMM),
     ("stride-2 correlation (forward)", (2, 64, 19, 16, 64, 3, 3, 2, 0, 1, 0, 1, 1, 1), B.PASS_FWD, B.PATH_TC_IGEMM),
+    ("stride-2 correlation (backward-data, every output phase in one launch)",
+     (2, 64, 19, 16, 64, 3, 3, 2, 0, 1, 0, 1, 1, 1), B.PASS_BWD_DATA, B.PATH_TC_IGEMM),
     ("weight gradient", (2, 32, 14, 13, 64, 3, 3, 1, 1, 0, 2, 1, 1, 2), B.PASS_BWD_WEIGHT, B.PATH_TC_IGEMM),
     ("stride-2 weight gradient", (2, 64, 19, 16, 64, 3, 3, 2, 0, 1, 0, 1, 1, 1), B.PASS_BWD_WEIGHT,
      B.PATH_TC_IGEMM),
