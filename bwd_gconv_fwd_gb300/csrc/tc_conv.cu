@@ -961,6 +961,8 @@ struct Corr2Params {
     int nmma;                   // MMA N: 256, or 240 with paired taps
     int tile_pos;               // output positions per tile: nmma, or nmma - pair_delta with paired taps
     int pair_delta;             // paired taps: the second tap's row shift past the first (0: unpaired)
+    int dup;                    // unpaired with at most 64 produced channels: rows 64.. repeat rows 0..
+                                // (the same MMAs), so every epilogue lane group has a copy to drain
     int stage_rows;             // positions staged per chunk (nmma + farthest tap, multiple of 8)
     int nsb, wstages;           // staging buffers (1 or 2), weight ring depth (3 or 4)
     int nchc;                   // 64-channel chunks of the reduced channels (nchu / stride phases)
@@ -1311,11 +1313,14 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                     ptx::named_sync(bid, 64);   // the upper warp may overwrite hb
                 }
             } else {
-            const int v0 = vt * 128 + lg * 32;
+            // dup: rows 64.. repeat rows 0.. (at most 64 produced channels), so the four warps
+            // of a 32-channel group (two lane groups, two halves) split the columns four ways
+            const int v0 = vt * 128 + (p.dup ? (lg & 1) : lg) * 32;
             const int vcount = min(32, p.Cv - v0);
             const int64_t vout = ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv + v0) * out_hw;   // element index
             const float bias_lane = (p.bias && lane < vcount) ? __bfloat162float(p.bias[g * p.Cv + v0 + lane]) : 0.f;
-            for (int pc = half * 32; pc < p.tile_pos; pc += 64) {
+            const int pc_step = p.dup ? 128 : 64;
+            for (int pc = (p.dup ? half + 2 * (lg >> 1) : half) * 32; pc < p.tile_pos; pc += pc_step) {
                 uint32_t a0[16], a1[16];
                 const uint32_t taddr = tmem + ((uint32_t)(lg * 32) << 16) + (uint32_t)(acc * 256 + pc);
                 ptx::tmem_ld16(taddr, a0);
@@ -1368,6 +1373,7 @@ struct Pack2Params {
     int transpose;          // 0 forward, 1 backward-data
     int w_cin_g, kHW;
     int pair;               // 1: rows 0..63 from tap tk1, rows 64..127 from tap tk2 (Cv <= 64)
+    int dup;                // 1: rows 64..127 repeat rows 0..63 (unpaired, Cv <= 64)
     int tk1[kMaxBlk], tk2[kMaxBlk];   // weight tap index (kh*kW + kw) of each block; tk2 -1: none
     int jc[kMaxBlk];        // 64-channel chunk of the reduced channels each block covers
 };
@@ -1386,7 +1392,7 @@ __device__ __forceinline__ void pack2_body(const Pack2Params &p, int b0, int nb)
         const int vt = b % p.n_vtile;
         const int g = b / p.n_vtile;
         const int tap = (p.pair && r >= 64) ? p.tk2[bk] : p.tk1[bk];
-        const int v = vt * 128 + (p.pair ? (r & 63) : r);
+        const int v = vt * 128 + ((p.pair || p.dup) ? (r & 63) : r);
         uint32_t wv[4] = {0u, 0u, 0u, 0u};
         if (tap >= 0 && v < p.Cv) {
             unsigned short h[8];
@@ -2102,6 +2108,8 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L, int rh = -1, int 
     k.transpose = bwd_data ? 1 : 0;
     k.w_cin_g = g.Cgi; k.kHW = ntaps;
     k.pair = pair ? 1 : 0;
+    k.dup = (!pair && Cv <= 64) ? 1 : 0;
+    c.dup = k.dup;
     BlockifyParams &bu = L->bu;
     bu = BlockifyParams{};
     bu.N = g.N; bu.G = g.G; bu.Cg = Cu; bu.nchunk = c.nchu;
