@@ -526,14 +526,17 @@ gconv_status noalloc_weight(const Geom &g, gconv_dtype dtype, const void *x, con
 
 // The training step's route: the tensor-core kernels with shared blocked copies when every
 // pass would run there (unmerged) on compatible copies, else the three passes in turn.
-bool step_shared(const Geom &g, gconv_dtype dt, size_t *ws, int *launches = nullptr)
+bool step_shared(const Geom &g, gconv_dtype dt, size_t *ws, int *launches = nullptr, int *merge = nullptr)
 {
     if (dt != GCONV_BF16 || forced_path() != GCONV_PATH_NONE || g.N == 0) return false;
+    int m = 0;   // the passes' common merge factor (1: unmerged)
     for (gconv_pass pass : {GCONV_PASS_FWD, GCONV_PASS_BWD_DATA, GCONV_PASS_BWD_WEIGHT}) {
         const Plan p = plan_pass(g, dt, pass);
-        if (p.path != GCONV_PATH_TC_IGEMM || p.merge != 1) return false;
+        if (p.path != GCONV_PATH_TC_IGEMM || (m && p.merge != m)) return false;
+        m = p.merge;
     }
-    return tc_step_plan(g, ws, launches);
+    if (merge) *merge = m;
+    return m == 1 ? tc_step_plan(g, ws, launches) : tc_step_plan_merged(g, m, ws, launches);
 }
 
 gconv_status step_plan(const Geom &g, gconv_dtype dt, int *shared, int *launches)
@@ -601,7 +604,8 @@ gconv_status step_ex(const Geom &g0, gconv_dtype dt, gconv_dtype out_dt, const v
     const cudaEvent_t *marks = g_step_marks ? g_step_events : nullptr;
     if (marks) cudaEventRecord(marks[0], s);
     size_t shared = 0;
-    if (!step_shared(g0, dt, &shared)) {
+    int merge = 1;
+    if (!step_shared(g0, dt, &shared, nullptr, &merge)) {
         // the three passes in turn, one workspace
         gconv_status st = run_pass(g0, dt, out_dt, GCONV_PASS_FWD, x, w, bias, y, nullptr, ws, ws_bytes, stream);
         if (st == GCONV_OK && marks) cudaEventRecord(marks[1], s);
@@ -615,8 +619,11 @@ gconv_status step_ex(const Geom &g0, gconv_dtype dt, gconv_dtype out_dt, const v
     Geom g = g0;
     g.out_bf16 = out_dt == GCONV_BF16 ? 1 : 0;
     bool db_done = false;
-    gconv_status st = tc_step_launch(g, x, w, bias, dy, static_cast<float *>(y), static_cast<float *>(dx), dw, db, ws,
-                                     s, &db_done, marks ? marks + 1 : nullptr);
+    gconv_status st =
+        merge > 1 ? tc_step_launch_merged(g, merge, x, w, bias, dy, static_cast<float *>(y), static_cast<float *>(dx), dw,
+                                          db, ws, s, &db_done, marks ? marks + 1 : nullptr)
+                  : tc_step_launch(g, x, w, bias, dy, static_cast<float *>(y), static_cast<float *>(dx), dw, db, ws, s,
+                                   &db_done, marks ? marks + 1 : nullptr);
     if (st != GCONV_OK) return st;
     if (db && !db_done) {
         const Plan pb = plan_pass(g0, dt, GCONV_PASS_BWD_BIAS);

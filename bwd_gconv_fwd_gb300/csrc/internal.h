@@ -71,8 +71,14 @@ bool encode_rows_tmap(CUtensorMap *m, const void *base, uint64_t rows, uint64_t 
 // passes (tc_conv.cu): forward, backward-data, weight gradient (+ bias).  The plan fails
 // for layers whose passes do not all run there on compatible copies.
 bool tc_step_plan(const Geom &g, size_t *ws_bytes, int *launches = nullptr);
+// The same on merged groups (m groups run as one, block-diagonal weights), for layers whose
+// passes all run merged by m.
+bool tc_step_plan_merged(const Geom &g, int m, size_t *ws_bytes, int *launches = nullptr);
+gconv_status tc_step_launch_merged(const Geom &g, int m, const void *x, const void *w, const void *bias, const void *dy,
+                                   float *y, float *dx, float *dw, float *db, void *ws, cudaStream_t s, bool *db_done,
+                                   const cudaEvent_t *marks);
 // marks: nullptr, or three events recorded after the forward pass, backward-data and the
-// weight gradient.
+// weight gradient (the third skipped when nullptr).
 gconv_status tc_step_launch(const Geom &g, const void *x, const void *w, const void *bias, const void *dy,
                             float *y, float *dx, float *dw, float *db, void *ws, cudaStream_t s, bool *db_done,
                             const cudaEvent_t *marks);

@@ -2831,7 +2831,7 @@ gconv_status tc_step_launch(const Geom &g, const void *x, const void *w, const v
     if (st != GCONV_OK) return st;
     if (marks) cudaEventRecord(marks[1], s);
     st = launch_wgrad_blocked(S.W, g, dw, fuse_bias ? db : nullptr, wsb + S.off_part, wsb + S.off_bias, s, db_done);
-    if (st == GCONV_OK && marks && *db_done) cudaEventRecord(marks[2], s);
+    if (st == GCONV_OK && marks && marks[2] && *db_done) cudaEventRecord(marks[2], s);
     return st;
 }
 
@@ -2939,6 +2939,49 @@ gconv_status tc_merged_launch(const Geom &g, const Plan &p, gconv_pass pass, con
     const int64_t total = (int64_t)g.Cout * g.Cgi * KK;
     const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms() * 8);
     diagonal_weights_kernel<<<blocks, 256, 0, s>>>(dwd, out, total, g.Cgo, g.Cgi, m, KK);
+    return GCONV_OK;
+}
+
+// The training step on merged groups: the weights are widened once (block-diagonal, for
+// the forward and backward-data passes alike), the merged geometry runs the shared-copy
+// step (x, y, gradOutput and dx keep their layout), and dw is the diagonal of the merged
+// weight gradient.  Workspace: [the merged step's][widened weights][merged weight gradient].
+bool tc_step_plan_merged(const Geom &g, int m, size_t *ws_bytes, int *launches)
+{
+    if (m < 2 || g.G % m) return false;
+    size_t ws = 0;
+    int l = 0;
+    if (!tc_step_plan(merged_groups(g, m), &ws, &l)) return false;
+    *ws_bytes = align256(ws) + align256(merged_extra_bytes(g, m, GCONV_PASS_FWD)) +
+                align256(merged_extra_bytes(g, m, GCONV_PASS_BWD_WEIGHT));
+    if (launches) *launches = l + 2;   // the widening and the diagonal extraction
+    return true;
+}
+
+gconv_status tc_step_launch_merged(const Geom &g, int m, const void *x, const void *w, const void *bias, const void *dy,
+                                   float *y, float *dx, float *dw, float *db, void *ws, cudaStream_t s, bool *db_done,
+                                   const cudaEvent_t *marks)
+{
+    *db_done = false;
+    size_t sws = 0;
+    if (m < 2 || g.G % m) return GCONV_ERR_UNSUPPORTED;
+    const Geom d = merged_groups(g, m);
+    if (!tc_step_plan(d, &sws)) return GCONV_ERR_UNSUPPORTED;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    __nv_bfloat16 *wd = reinterpret_cast<__nv_bfloat16 *>(base + align256(sws));
+    float *dwd = reinterpret_cast<float *>(base + align256(sws) + align256(merged_extra_bytes(g, m, GCONV_PASS_FWD)));
+    const int KK = g.kH * g.kW;
+    const int64_t total_wide = (int64_t)g.Cout * g.Cgi * m * KK;
+    const int blocks_wide = (int)std::min<int64_t>((total_wide + 255) / 256, (int64_t)num_sms() * 8);
+    widen_weights_kernel<<<blocks_wide, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w), wd, total_wide, g.Cgo, g.Cgi, m,
+                                                     KK);
+    const cudaEvent_t inner[3] = {marks ? marks[0] : nullptr, marks ? marks[1] : nullptr, nullptr};
+    gconv_status st = tc_step_launch(d, x, wd, bias, dy, y, dx, dwd, db, ws, s, db_done, marks ? inner : nullptr);
+    if (st != GCONV_OK) return st;
+    const int64_t total = (int64_t)g.Cout * g.Cgi * KK;
+    const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)num_sms() * 8);
+    diagonal_weights_kernel<<<blocks, 256, 0, s>>>(dwd, dw, total, g.Cgo, g.Cgi, m, KK);
+    if (marks && *db_done) cudaEventRecord(marks[2], s);
     return GCONV_OK;
 }
 

@@ -253,6 +253,10 @@ def test_step_plan_routes(L):
     # an output narrower than the input: the backward-data copy has another pitch
     assert gc.gconv_step_plan((2, 32, 14, 13, 64, 3, 3, 1, 1, 0, 2, 1, 1, 2), bf)[0] is False
     assert gc.gconv_step_plan((2, 64, 17, 15, 64, 3, 3, 1, 1, 1, 1, 1, 1, 1), bf) == (True, 6)
+    # groups of 8 channels run merged (block-diagonal weights): the step shares the merged
+    # geometry's copies, with the weight widening and the diagonal extraction around it
+    assert gc.gconv_step_plan((2, 64, 12, 12, 64, 3, 3, 1, 1, 1, 1, 1, 1, 8), bf) == (True, 8)
+    assert gc.gconv_step_plan(wl.model_zoo(2)["resnext_s1_256x28"].geom, bf) == (True, 8)
     # a forced family turns sharing off
     B.gconv_debug_force_path(B.PATH_TC_IGEMM)
     try:

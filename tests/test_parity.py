@@ -343,7 +343,9 @@ STEP_EX = [
     ((2, 32, 11, 13, 32, 3, 3, 1, 1, 1, 1, 2, 2, 1, 2, 1), "bf16", False, True, "f32"),  # shared, per-axis dilation
     ((2, 32, 14, 13, 64, 3, 3, 1, 1, 0, 2, 1, 1, 2), "bf16", True, True, "f32"),      # passes in turn (widths differ)
     ((2, 64, 19, 16, 64, 3, 3, 2, 0, 1, 0, 1, 1, 1), "bf16", True, True, "f32"),      # stride 2: passes in turn
-    ((2, 64, 12, 12, 64, 3, 3, 1, 1, 1, 1, 1, 1, 8), "bf16", True, True, "f32"),      # merged groups: passes in turn
+    ((2, 64, 12, 12, 64, 3, 3, 1, 1, 1, 1, 1, 1, 8), "bf16", True, True, "f32"),      # merged groups, shared copies
+    ((2, 48, 10, 10, 48, 3, 3, 1, 1, 1, 1, 1, 1, 6), "bf16", True, True, "f32"),      # merged by 6: db fused
+    ((2, 48, 10, 10, 48, 3, 3, 1, 1, 1, 1, 1, 1, 6), "bf16", True, True, "bf16"),     # the same, bf16 y and dx
     ((2, 32, 12, 12, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8), "f32", True, True, "f32"),       # CUDA-core passes
     ((0, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2), "bf16", True, True, "f32"),     # empty batch
 ]
