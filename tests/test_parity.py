@@ -333,6 +333,19 @@ def test_step_host_matches_device_passes(dev, oracle_mod, geom, dtype, with_bias
     check("host db", outs["db"].numpy(), oracle_mod.bwd_bias(geom, f64(dy)), TOL[dtype])
 
 
+@pytest.mark.parametrize("geom", [
+    (2, 256, 14, 14, 256, 3, 3, 2, 1, 1, 1, 1, 1, 1),   # stride 2, two 128-channel tiles in every output phase
+    (1, 128, 15, 15, 128, 5, 5, 2, 2, 2, 2, 2, 1, 1),   # stride 2, 5x5: output phases with 9, 6, 6 and 4 taps
+])
+def test_stride2_tensor_core_wide_full(dev, oracle_mod, geom):
+    """Stride-2 layers on the tensor-core kernels (one launch a pass for every phase) over
+    whole tensors against the oracle."""
+    assert_paths(geom, "bf16", (B.PATH_TC_IGEMM, B.PATH_TC_IGEMM, B.PATH_TC_IGEMM, B.PATH_REDUCE))
+    wk = wl.Workload("s2wide", geom, "bf16")
+    x, w, b, dy = wl.make_inputs(wk, seed=808)
+    full_compare(geom, "bf16", x, w, b, dy, dev, oracle_mod, label="s2 wide")
+
+
 STEP_EX = [
     # (geometry, dtype, bias, db, output dtype)
     ((3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2), "bf16", True, True, "f32"),     # shared copies, db fused

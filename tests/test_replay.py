@@ -91,6 +91,8 @@ STRIDE2 = [
     (2, 32, 15, 15, 64, 5, 5, 2, 2, 2, 2, 2, 1, 2),
     (1, 48, 13, 17, 32, 3, 3, 2, 1, 1, 1, 1, 1, 1),
     (2, 16, 12, 12, 32, 3, 3, 2, 2, 2, 2, 2, 2, 1),         # dilation 2
+    (2, 256, 14, 14, 256, 3, 3, 2, 1, 1, 1, 1, 1, 1),       # two 128-channel tiles in every phase
+    (1, 128, 15, 15, 128, 5, 5, 2, 2, 2, 2, 2, 1, 1),       # 5x5: the phases have 9, 6, 6 and 4 taps
     # per-axis strides: one stride-2 axis and one stride-1 axis (two phase planes)
     (2, 32, 13, 12, 32, 3, 3, 2, 1, 1, 1, 1, 1, 1, 1, 1),
     (2, 32, 12, 15, 64, 3, 3, 1, 2, 1, 0, 1, 1, 1, 2, 1),
