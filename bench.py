@@ -84,11 +84,20 @@ STEP_SOURCES = ("bwd_gconv_fwd_gb300/csrc/tc_conv.cu", "bwd_gconv_fwd_gb300/csrc
                 "bwd_gconv_fwd_gb300/csrc/internal.h", "bwd_gconv_fwd_gb300/csrc/common.cuh", "include/gconv.h")
 
 
+def _code_only(text):
+    """Source text without comments and with whitespace collapsed (comment edits do not
+    change a kernel)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for rel in STEP_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as fh:
-            h.update(os.path.basename(rel).encode() + fh.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as fh:
+            h.update(os.path.basename(rel).encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

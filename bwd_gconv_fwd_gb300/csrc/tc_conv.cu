@@ -1945,7 +1945,8 @@ bool size_corr2(Corr2Launch *L)
 // tap (kh, kw) of output (oh, ow) reads x[s*(oh + A) + ph][s*(ow + B) + pw], i.e. plane
 // (ph, pw) at the plain shift (A, B), so each plane is a staged chunk with its own taps and
 // the tile sums over all planes' chunks.
-// A stride-2 backward-data pass runs as one launch per output phase (rh, rw): dx rows
+// A stride-2 backward-data pass is built here one output phase (rh, rw) at a time (the
+// phases then run merged into one launch, merge_corr2_phases): dx rows
 // s*q + rh take the taps kh with (rh + pt - kh*d) divisible by s, which read gradOutput row
 // q + (rh + pt - kh*d)/s, a plain shift.  Every phase reads one blocked copy of gradOutput
 // whose origin is the smallest shift over all phases; a phase with output positions but
@@ -2136,9 +2137,10 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L, int rh = -1, int 
     return true;
 }
 
-// Stride-2 backward-data on the correlation kernel: one launch per output phase that has
-// taps, one blocked copy of gradOutput for all of them (every phase lays it out alike), and
-// a zero fill for phases with outputs but no taps.
+// Stride-2 backward-data on the correlation kernel: the output phases that have taps (each
+// built alone, then merged into one launch when their geometry agrees), one blocked copy of
+// gradOutput for all of them (every phase lays it out alike), and a zero fill for phases
+// with outputs but no taps.
 struct Corr2PhaseSet {
     int n = 0;                          // phases with taps
     Corr2Launch L[kMaxPlanes];
@@ -2412,8 +2414,9 @@ gconv_status launch_corr2(Corr2Launch &L, const void *U, const void *w, const vo
     return launch_corr2_kernel(L, reinterpret_cast<__nv_bfloat16 *>(ws), ws + L.ub_bytes, bias, out, out_bf16, s);
 }
 
-// Stride-2 backward-data: the blocked copy of gradOutput and phase 0's weights in one launch,
-// the other phases' weights, zero fills, then one correlation launch per phase.
+// Stride-2 backward-data.  Merged: the blocked copy of gradOutput with every phase's weights,
+// zero fills, one correlation launch.  Otherwise: the copy with phase 0's weights, the other
+// phases' weights, zero fills, then one correlation launch per phase.
 gconv_status launch_corr2_phases(Corr2PhaseSet &S, const Geom &g, const void *dy, const void *w, float *out,
                                  uint8_t *ws, cudaStream_t s)
 {
