@@ -33,8 +33,8 @@ namespace gconv {
 
 namespace {
 
-constexpr int kGemmThreads = 256;   // warps 0, 6, 7: TMA producers; 1: MMA; 2-5: epilogue
-constexpr int kGemmProducers = 3;
+constexpr int kGemmThreads = 352;   // warps 0, 6-10: TMA producers; 1: MMA; 2-5: epilogue
+constexpr int kGemmProducers = 6;
 constexpr int kBM = 128, kBK = 64;
 constexpr uint64_t kGemmDrainNs = 1000000000ull;
 
@@ -100,12 +100,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 
     if (warp == 0 || warp >= 6) {
         // ---------------- TMA producers ----------------
-        // a stage is 1-2 A boxes and 1-4 B boxes; producer pi issues boxes pi, pi + 3, ...
-        // (one thread's copy stream alone is capped well below what the MMAs consume)
+        // a stage is 2 A boxes and BN / 64 B boxes of 8 KB (64 rows or columns each); producer
+        // pi issues boxes pi, pi + kGemmProducers, ... (one thread's copy stream alone is
+        // capped well below what the MMAs consume)
         if (lane == 0) {
             const int pi = warp == 0 ? 0 : warp - 5;
-            const int nA = p.a_mn ? 2 : 1, nB = p.b_mn ? BN / 64 : 1;
-            const uint32_t bytesA = p.a_mn ? 8192u : 16384u, bytesB = p.b_mn ? 8192u : (uint32_t)BN * 128u;
+            const int nA = 2, nB = BN / 64;
+            const uint32_t bytesA = 8192u, bytesB = 8192u;
             uint32_t my_bytes = 0;
             for (int i = pi; i < nA + nB; i += kGemmProducers) my_bytes += i < nA ? bytesA : bytesB;
             int it = 0;   // global k-block counter across tiles
@@ -124,15 +125,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     const uint32_t sa = sbase + slot * stage_bytes, sb = sa + a_bytes;
                     ptx::mbar_arrive_expect_tx(fb, my_bytes);
                     for (int i = pi; i < nA + nB; i += kGemmProducers) {
-                        if (i < nA) {   // A tile: 128 rows of M x 64 of K
-                            const int x = p.a_mn ? mb * kBM + i * 64 : kb * kBK, y = p.a_mn ? kb * kBK : mb * kBM;
-                            const uint32_t dst = p.a_mn ? sa + i * 8192 : sa;
+                        if (i < nA) {   // A tile: 128 rows of M x 64 of K, as two 64-row (or column) boxes
+                            const int x = p.a_mn ? mb * kBM + i * 64 : kb * kBK, y = p.a_mn ? kb * kBK : mb * kBM + i * 64;
+                            const uint32_t dst = sa + i * 8192;
                             if (p.a_bmid) ptx::tma_load_3d(dst, &tmA, x, ab, y, fb);
                             else ptx::tma_load_3d(dst, &tmA, x, y, ab, fb);
-                        } else {        // B tile: BN rows of N x 64 of K
+                        } else {        // B tile: BN rows of N x 64 of K, as 64-row (or column) boxes
                             const int c = i - nA;
-                            const int x = p.b_mn ? nb * BN + c * 64 : kb * kBK, y = p.b_mn ? kb * kBK : nb * BN;
-                            const uint32_t dst = p.b_mn ? sb + c * 8192 : sb;
+                            const int x = p.b_mn ? nb * BN + c * 64 : kb * kBK, y = p.b_mn ? kb * kBK : nb * BN + c * 64;
+                            const uint32_t dst = sb + c * 8192;
                             if (p.b_bmid) ptx::tma_load_3d(dst, &tmB, x, bt, y, fb);
                             else ptx::tma_load_3d(dst, &tmB, x, y, bt, fb);
                         }
@@ -453,14 +454,14 @@ gconv_status tc_fc_launch(const Geom &g, const Plan &, gconv_pass pass, const vo
         case GCONV_PASS_FWD:   // y[:, g] (N x Cgo) = X[:, g] (N x Kg, K-major) * W[g]^T (K-major)
             L.sh = GemmShape{g.N, g.Cgo, Kg, 0, 0, 0};
             L.sh.BN = pick_bn(L.sh.M, L.sh.N, G);
-            ok = make_tmap_mid(&tA, a, Kg, G, g.N, kBM, &L.a_bmid) && make_tmap(&tB, b, Kg, g.Cgo, L.sh.BN, G);
+            ok = make_tmap_mid(&tA, a, Kg, G, g.N, 64, &L.a_bmid) && make_tmap(&tB, b, Kg, g.Cgo, 64, G);
             L.ldc = g.Cout;
             L.c_bstride = g.Cgo;
             break;
         case GCONV_PASS_BWD_DATA:   // dX[:, g] (N x Kg) = dY[:, g] (K-major) * W[g] (Cgo x Kg, MN-major)
             L.sh = GemmShape{g.N, Kg, g.Cgo, 0, 1, 0};
             L.sh.BN = pick_bn(L.sh.M, L.sh.N, G);
-            ok = make_tmap_mid(&tA, a, g.Cgo, G, g.N, kBM, &L.a_bmid) && make_tmap(&tB, b, Kg, g.Cgo, kBK, G);
+            ok = make_tmap_mid(&tA, a, g.Cgo, G, g.N, 64, &L.a_bmid) && make_tmap(&tB, b, Kg, g.Cgo, kBK, G);
             L.ldc = g.Cin * g.kH * g.kW;
             L.c_bstride = Kg;
             break;
@@ -481,7 +482,7 @@ gconv_status tc_fc_launch(const Geom &g, const Plan &, gconv_pass pass, const vo
             L.sh = GemmShape{g.Cgo, HW, g.Cgi, 0, 1, 0};
             L.sh.BN = pick_bn(L.sh.M, L.sh.N, L.batch);
             L.bias_rows = 1;
-            ok = make_tmap(&tA, b, g.Cgi, g.Cgo, kBM, g.G) && make_tmap(&tB, a, HW, g.Cgi, kBK, L.batch);
+            ok = make_tmap(&tA, b, g.Cgi, g.Cgo, 64, g.G) && make_tmap(&tB, a, HW, g.Cgi, kBK, L.batch);
         } else {
             // dx[b] (Cgi x HW) = W[g]^T (Cgi x Cgo, MN-major) * dy[b] (Cgo x HW, MN-major)
             L.sh = GemmShape{g.Cgi, HW, g.Cgo, 1, 1, 0};
