@@ -406,7 +406,7 @@ static bool step_layout(const Geom &g, gconv_dtype dt, bool with_bias, StepLayou
 // and so was letting the kernels write results straight into host memory (1.71 ms).
 // The forward pass runs in kFwdChunks batch chunks, so that its result (the largest)
 // starts copying out after the first chunk instead of after the whole pass.
-constexpr int kFwdChunks = 4;
+constexpr int kFwdChunks = 8;
 constexpr int kFwdChunkMinN = 4;
 
 struct StepStreams {

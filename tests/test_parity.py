@@ -297,9 +297,9 @@ def test_forced_direct_agrees_with_default(dev):
     ((3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2), "bf16", True),     # tensor-core passes
     ((2, 32, 12, 12, 32, 3, 3, 1, 1, 1, 1, 1, 1, 8), "f32", False),      # CUDA-core passes, no bias
     ((2, 128, 6, 6, 96, 6, 6, 1, 0, 0, 0, 0, 1, 1), "bf16", True),       # FC mode
-    ((17, 32, 10, 9, 64, 3, 3, 1, 1, 1, 1, 1, 1, 2), "bf16", True),      # forward in four batch chunks, ragged
-    ((16, 16, 8, 8, 16, 3, 3, 1, 1, 1, 1, 1, 1, 4), "f32", True),        # chunks on the CUDA-core path
-    ((18, 3, 7, 7, 8, 3, 3, 1, 0, 0, 0, 0, 1, 1), "bf16", True),         # 294-byte images: chunks would misalign
+    ((35, 32, 10, 9, 64, 3, 3, 1, 1, 1, 1, 1, 1, 2), "bf16", True),      # forward in eight batch chunks, ragged
+    ((32, 16, 8, 8, 16, 3, 3, 1, 1, 1, 1, 1, 1, 4), "f32", True),        # chunks on the CUDA-core path
+    ((36, 3, 7, 7, 8, 3, 3, 1, 0, 0, 0, 0, 1, 1), "bf16", True),         # 294-byte images: chunks would misalign
 ])
 def test_step_host_matches_device_passes(dev, oracle_mod, geom, dtype, with_bias):
     """gconv_step_host on pinned host tensors gives bit for bit what the device passes give
