@@ -770,3 +770,41 @@ def test_fully_connected_gemm_full(dev, oracle_mod, geom, out):
         torch.cuda.synchronize()
         assert torch.equal(y16.cpu(), got["y"].to(torch.bfloat16))
         assert torch.equal(dx16.cpu(), got["dx"].to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("geom", [
+    (3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2),    # shared copies, side stream, dependent launches
+    (2, 64, 19, 16, 64, 3, 3, 2, 0, 1, 0, 1, 1, 1),     # stride 2: passes in turn, phases in one launch
+])
+def test_step_ex_in_a_cuda_graph(dev, geom):
+    """gconv_step_ex captured into a CUDA graph (its side-stream fork and join and its
+    programmatic dependent launches are captured with it) and replayed twice gives the
+    eager call's results bit for bit."""
+    wk = wl.Workload("graph", geom, "bf16")
+    x, w, b, dy = (t.to(dev) for t in wl.make_inputs(wk, seed=515))
+    N, Cin, H, W, Cout = wl.per_axis(geom)[:5]
+    Ho, Wo = wl.out_hw(geom)
+    kw = _kw(geom)
+    ws = torch.empty(max(1, gc.gconv_step_workspace_size(B.per_axis(geom), B.GCONV_BF16)), dtype=torch.uint8,
+                     device=dev)
+    outs = lambda: (torch.empty((N, Cout, Ho, Wo), device=dev), torch.empty((N, Cin, H, W), device=dev),
+                    torch.empty(tuple(w.shape), device=dev), torch.empty((Cout,), device=dev))
+    ref = outs()
+    gc.gconv_step(x, w, b, dy, *ref, workspace=ws, **kw)
+    torch.cuda.synchronize()
+    got = outs()
+    for t in got:
+        t.fill_(float("nan"))
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        gc.gconv_step(x, w, b, dy, *got, workspace=ws, **kw)
+    for _ in range(2):
+        for t in got:
+            t.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gc.gconv_check_device_error() == B.GCONV_OK
+        for a, r in zip(got, ref):
+            assert torch.equal(a, r)
