@@ -30,6 +30,28 @@ struct Plan {
 gconv_status make_geom(int N, int C_in, int H, int W, int C_out, int kH, int kW, int stride,
                        int pt, int pb, int pl, int pr, int dil, int groups, Geom *g);
 Plan plan_pass(const Geom &g, gconv_dtype dt, gconv_pass pass);
+
+// Launches a kernel as a programmatic dependent of the previous kernel on the stream: its
+// CTAs may be placed (and run their prologue) while that kernel drains.  Every kernel
+// launched this way calls ptx::griddep_wait before it touches global memory, so the result
+// is the same as a plain launch.  Errors surface through cudaGetLastError.
+template <typename... KArgs, typename... Args>
+void launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                      const Args &...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 long long wait_limit();
 unsigned int *device_error_word();   // device address of the error word, nullptr on failure
 int forced_path();

@@ -45,26 +45,6 @@
 
 namespace gconv {
 
-// Launches a kernel as a programmatic dependent of the previous kernel on the stream: its
-// CTAs may be placed (and run their prologue) while that kernel drains.  Every kernel
-// launched this way calls ptx::griddep_wait before it touches global memory, so the result
-// is the same as a plain launch.  Errors surface through cudaGetLastError.
-template <typename... KArgs, typename... Args>
-void launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s,
-                      const Args &...args)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaLaunchKernelEx(&cfg, kernel, args...);
-}
 
 
 constexpr int kStageWarps = 8;                      // staging + epilogue warps

@@ -97,6 +97,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
+    // programmatic dependent: the prologue above overlaps the previous kernel's tail; global
+    // memory is touched only after it completes.  One CTA holds its SM to the end, so the
+    // next launch may start now.
+    ptx::griddep_wait();
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
 
     if (warp == 0 || warp >= 6) {
         // ---------------- TMA producers ----------------
@@ -417,9 +422,9 @@ gconv_status run_gemm(const GemmLaunch &L, const CUtensorMap &tA, const CUtensor
             return GCONV_ERR_CUDA;
         attr[dev][ai] = true;
     }
-    if (sh.BN == 256) gemm_kernel<256><<<grid, kGemmThreads, smem, s>>>(tA, tB, gp);
-    else if (sh.BN == 192) gemm_kernel<192><<<grid, kGemmThreads, smem, s>>>(tA, tB, gp);
-    else gemm_kernel<128><<<grid, kGemmThreads, smem, s>>>(tA, tB, gp);
+    if (sh.BN == 256) launch_dependent(gemm_kernel<256>, (unsigned)grid, kGemmThreads, smem, s, tA, tB, gp);
+    else if (sh.BN == 192) launch_dependent(gemm_kernel<192>, (unsigned)grid, kGemmThreads, smem, s, tA, tB, gp);
+    else launch_dependent(gemm_kernel<128>, (unsigned)grid, kGemmThreads, smem, s, tA, tB, gp);
     return GCONV_OK;
 }
 
