@@ -475,6 +475,7 @@ __global__ void __launch_bounds__(kBlockifyThreads, 4)
 blockify_kernel(const __grid_constant__ BlockifyParams p)
 {
     ptx::griddep_wait();   // a programmatic dependent reads and writes nothing before this
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();   // all CTAs have started once all pass here
     blockify_block(p, blockIdx.x);
 }
 
@@ -484,6 +485,7 @@ __global__ void __launch_bounds__(kBlockifyThreads, 4)
 blockify2_kernel(const __grid_constant__ BlockifyParams a, const __grid_constant__ BlockifyParams b, int nb_a)
 {
     ptx::griddep_wait();   // a programmatic dependent reads and writes nothing before this
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();   // all CTAs have started once all pass here
     if ((int)blockIdx.x < nb_a) blockify_block(a, blockIdx.x);
     else blockify_block(b, blockIdx.x - nb_a);
 }
@@ -1403,6 +1405,7 @@ __global__ void __launch_bounds__(kBlockifyThreads, 4)
 blockify_pack_kernel(const __grid_constant__ BlockifyParams a, const __grid_constant__ Pack2Params pk, int nb_a)
 {
     ptx::griddep_wait();   // a programmatic dependent reads and writes nothing before this
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();   // all CTAs have started once all pass here
     if ((int)blockIdx.x < nb_a) blockify_block(a, blockIdx.x);
     else pack2_body(pk, blockIdx.x - nb_a, gridDim.x - nb_a);
 }
@@ -1428,6 +1431,7 @@ __global__ void __launch_bounds__(kReduceThreads)
 wgrad_reduce_kernel(const __grid_constant__ ReduceParams p)
 {
     ptx::griddep_wait();   // a programmatic dependent reads nothing before this
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
     __shared__ float part_sum[WAYS > 1 ? kReduceThreads : 1];
     constexpr int per = kReduceThreads / WAYS;             // outputs per block
     const int ol = threadIdx.x % per, way = threadIdx.x / per;

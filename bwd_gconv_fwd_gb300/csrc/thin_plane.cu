@@ -356,6 +356,11 @@ template <int CG>
 __global__ void thin_wgrad_finish_kernel(const float *__restrict__ part, int G, int blocks_per_group,
                                          float *__restrict__ dw, float *__restrict__ db)
 {
+    // programmatic dependent: nothing in global memory is touched before the previous kernel
+    // has completed; every CTA of this grid has started once all have passed here, so the
+    // next launch may be placed now
+    ptx::griddep_wait();
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
     constexpr int NA = CG * 9 + 1;
     const int total = G * CG * NA;
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
@@ -569,6 +574,11 @@ template <typename T, int CG, int PL>
 __global__ void __launch_bounds__(kThinThreads)
 thin_tile_kernel(const __grid_constant__ ThinParams p)
 {
+    // programmatic dependent: nothing in global memory is touched before the previous kernel
+    // has completed; every CTA of this grid has started once all have passed here, so the
+    // next launch may be placed now
+    ptx::griddep_wait();
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
     extern __shared__ __align__(16) unsigned char thin_sm[];
     __shared__ __align__(16) float ws[2][CG * CG * 9];   // per buffer: [o][ci][tap], four channels [ci][tap][o]
     constexpr int PAD = PadE<T>::value;
@@ -751,6 +761,11 @@ template <typename T, int CG, int PL>
 __global__ void __launch_bounds__(kThinThreads)
 thin_tile_wgrad_kernel(const __grid_constant__ ThinParams p)
 {
+    // programmatic dependent: nothing in global memory is touched before the previous kernel
+    // has completed; every CTA of this grid has started once all have passed here, so the
+    // next launch may be placed now
+    ptx::griddep_wait();
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
     extern __shared__ __align__(16) unsigned char thin_sm[];
     constexpr int NA = CG * 9 + 1;
     constexpr int WPO = 4 / CG;   // warps per output channel
@@ -951,9 +966,10 @@ gconv_status thin_tile_launch(const ThinParams &p, int grid, size_t smem, bool w
     if (wgrad) {
         const void *fn = (const void *)thin_tile_wgrad_kernel<T, CG, PL>;
         if (!allow_smem(fn, smem)) return GCONV_ERR_CUDA;
-        thin_tile_wgrad_kernel<T, CG, PL><<<grid, kThinThreads, smem, s>>>(p);
+        launch_dependent(thin_tile_wgrad_kernel<T, CG, PL>, (unsigned)grid, kThinThreads, smem, s, p);
         const int total = p.G * CG * (CG * 9 + 1);
-        thin_wgrad_finish_kernel<CG><<<(total + 255) / 256, 256, 0, s>>>(p.out, p.G, p.nchunk * p.n_strip, dw, db);
+        launch_dependent(thin_wgrad_finish_kernel<CG>, (unsigned)((total + 255) / 256), 256, 0, s, (const float *)p.out, p.G,
+                         p.nchunk * p.n_strip, dw, db);
         return GCONV_OK;
     }
     const void *fn = (const void *)thin_tile_kernel<T, CG, PL>;
@@ -962,7 +978,7 @@ gconv_status thin_tile_launch(const ThinParams &p, int grid, size_t smem, bool w
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThinThreads, smem) != cudaSuccess || per_sm < 1)
         per_sm = 1;
     const int pgrid = std::min(grid, num_sms() * per_sm);   // persistent: items walked by a resident grid
-    thin_tile_kernel<T, CG, PL><<<pgrid, kThinThreads, smem, s>>>(p);
+    launch_dependent(thin_tile_kernel<T, CG, PL>, (unsigned)pgrid, kThinThreads, smem, s, p);
     return GCONV_OK;
 }
 
