@@ -922,14 +922,15 @@ wgrad_kernel(const __grid_constant__ WgradParams p)
 //   B = the blocked input's position rows [p0, p0 + stage_rows) of one chunk, staged
 //       by cp.async into the 128-byte swizzle layout; tap t reads them tap_off[t]
 //       rows further on (a whole-row shift of the descriptor's start address).
-// Every MMA is M = 128, N = 256, K = 16; K steps past the last real channel of a
-// chunk are skipped.  With at most 64 produced channels the tile's upper 64 rows would be
+// Every MMA is M = 128, K = 16 and N at most 256 (the narrowest multiple of 16 that keeps the
+// number of tiles per image); K steps past the last real channel of a chunk are skipped.  With at most 64 produced channels the tile's upper 64 rows would be
 // idle, so taps are paired: rows 64.. hold the weights of a second tap lying pair_delta
 // positions after the first in the same row of the kernel; both rows read the first
 // tap's shifted B, so the upper rows accumulate the second tap's contribution to the
 // output pair_delta positions earlier, and the epilogue adds lower row j and upper row
-// j + pair_delta (N = 240 then, tile_pos = 240 - pair_delta outputs per tile).  The epilogue transposes 32 x 32 blocks through shared memory
-// so that a warp stores 32 consecutive pixels of one output channel.
+// j + pair_delta (N at most 240 then, tile_pos = N - pair_delta outputs per tile).  The
+// epilogue transposes 32 x 32 blocks through shared memory so that a warp stores 32
+// consecutive pixels of one output channel.
 struct Corr2Params {
     const __nv_bfloat16 *UB;    // blocked input [N][G][nchu][R][Wp][64]
     const uint8_t *Wpk;         // packed weight blocks [G][n_vtile][nblk][16 KB]
@@ -947,6 +948,8 @@ struct Corr2Params {
                                 // (the same MMAs), so every epilogue lane group has a copy to drain
     int stage_rows;             // positions staged per chunk (nmma + farthest tap, multiple of 8)
     int nsb, wstages;           // staging buffers (1 or 2), weight ring depth (3 or 4)
+    int spb;                    // weight blocks per ring slot (1 or 2): one barrier hand-off
+                                // (wait, commit, refill) per slot, never across chunks
     int nchc;                   // 64-channel chunks of the reduced channels (nchu / stride phases)
     int nblk;                   // weight blocks of all output phases ([g][vt][nblk] packed blocks)
     int tap_off[kMaxBlk];       // row shift of each block's (first) tap
@@ -990,39 +993,61 @@ __device__ __forceinline__ void corr2_tile(const Corr2Params &p, int t, int *ph,
     *g = t / p.n_vtile;
 }
 
-// Issues one staged chunk's MMAs: for every weight block, wait for its ring slot, then
-// NKS K steps of 16 channels against the chunk's rows shifted by the block's tap offset,
-// then release the slot.  NKS is a template argument so that no branch sits between the
-// MMAs: with branches around them the issuing thread fell behind the tensor core
-// (measured about 190 cycles per 128 x 256 x 16 MMA against 128 without), and for the same
-// reason the slot wait's slow path is out of line and the loop has one exit (measured on
-// the AlexNet-style layer: 63.8 -> 56.5 us per CTA).  Returns false when a slot wait runs
-// out of time.
+// Issues one staged chunk's MMAs: for every ring slot (SPB weight blocks, the chunk's last
+// slot possibly holding fewer), wait for it, then NKS K steps of 16 channels per block
+// against the chunk's rows shifted by the block's tap offset, then release the slot.  NKS
+// and SPB are template arguments so that no branch sits between the MMAs: with branches
+// around them the issuing thread fell behind the tensor core (measured about 190 cycles per
+// 128 x 256 x 16 MMA against 128 without), and for the same reason the slot wait's slow path
+// is out of line and the loop has one exit (measured on the AlexNet-style layer: 63.8 ->
+// 56.5 us per CTA).  Each hand-off costs the issuing thread about 200 cycles that the tensor
+// core sees (it runs only about one MMA behind), so two blocks a slot halve that cost.
+// Returns false when a slot wait runs out of time.
 template <int NKS>
+__device__ __forceinline__ void corr2_block_mmas(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc)
+{
+    ptx::mma_f16(d, ad, bd, idesc, acc);
+    if (NKS > 1) ptx::mma_f16(d, ad + 2, bd + 2, idesc, 1u);   // +32 bytes: next 16 channels
+    if (NKS > 2) ptx::mma_f16(d, ad + 4, bd + 4, idesc, 1u);
+    if (NKS > 3) ptx::mma_f16(d, ad + 6, bd + 6, idesc, 1u);
+}
+
+template <int NKS, int SPB>
 __device__ __forceinline__ bool corr2_issue_taps(uint32_t d, uint64_t adesc0, uint64_t bdesc_c, uint32_t idesc,
                                                  uint32_t acc_first, const int *tap_off, int ntaps, int wstages,
                                                  uint32_t wfull0, uint32_t wempty0, int &slot, uint32_t &wphase,
                                                  uint64_t wait_ns, uint64_t &w_weight)
 {
-    int off_next = tap_off[0];
+    constexpr uint32_t kSlotDesc = (uint32_t)(SPB * kWblkBytes) >> 4;   // slot stride in descriptor units
     uint32_t acc = acc_first;
     bool ok = true;
-    for (int tp = 0; tp < ntaps; ++tp) {
+    const int nfull = ntaps / SPB;
+    int off_next = tap_off[0];
+    for (int i = 0; i < nfull; ++i) {
         const int off = off_next;
-        off_next = tap_off[tp + 1];
+        const int off2 = SPB > 1 ? tap_off[i * SPB + 1] : 0;
+        off_next = tap_off[(i + 1) * SPB];
         const uint32_t wbar = wfull0 + (uint32_t)(slot * 8);
         // one exit only: a slot that timed out still gets its MMAs (the caller aborts after
         // the chunk), so that the loop has no second exit between the MMAs
         if (!ptx::mbar_test_wait(wbar, wphase) && ok) ok = ptx::mbar_wait_ool(wbar, wphase, wait_ns, &w_weight);
         ptx::tc_fence_after();
-        const uint64_t ad = adesc0 + (uint64_t)(slot * (kWblkBytes >> 4));
-        const uint64_t bd = bdesc_c + (uint64_t)(off * 8);     // off rows of 128 bytes
-        ptx::mma_f16(d, ad, bd, idesc, acc);
-        if (NKS > 1) ptx::mma_f16(d, ad + 2, bd + 2, idesc, 1u);   // +32 bytes: next 16 channels
-        if (NKS > 2) ptx::mma_f16(d, ad + 4, bd + 4, idesc, 1u);
-        if (NKS > 3) ptx::mma_f16(d, ad + 6, bd + 6, idesc, 1u);
+        const uint64_t ad = adesc0 + (uint64_t)(slot * kSlotDesc);
+        corr2_block_mmas<NKS>(d, ad, bdesc_c + (uint64_t)(off * 8), idesc, acc);   // off rows of 128 bytes
+        if (SPB > 1) corr2_block_mmas<NKS>(d, ad + (kWblkBytes >> 4), bdesc_c + (uint64_t)(off2 * 8), idesc, 1u);
         ptx::mma_commit(wempty0 + (uint32_t)(slot * 8));
         acc = 1u;
+        const int nxt = slot + 1;
+        slot = nxt == wstages ? 0 : nxt;
+        wphase ^= nxt == wstages ? 1u : 0u;
+    }
+    if (SPB > 1 && nfull * SPB < ntaps) {
+        // the chunk's last slot holds one block
+        const uint32_t wbar = wfull0 + (uint32_t)(slot * 8);
+        if (!ptx::mbar_test_wait(wbar, wphase) && ok) ok = ptx::mbar_wait_ool(wbar, wphase, wait_ns, &w_weight);
+        ptx::tc_fence_after();
+        corr2_block_mmas<NKS>(d, adesc0 + (uint64_t)(slot * kSlotDesc), bdesc_c + (uint64_t)(off_next * 8), idesc, acc);
+        ptx::mma_commit(wempty0 + (uint32_t)(slot * 8));
         const int nxt = slot + 1;
         slot = nxt == wstages ? 0 : nxt;
         wphase ^= nxt == wstages ? 1u : 0u;
@@ -1045,7 +1070,8 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
     const int stage_bytes = p.stage_rows * 128;
     for (int i = threadIdx.x; i <= p.nblk; i += blockDim.x) tap_off_sh[i] = i < p.nblk ? p.tap_off[i] : 0;
     uint8_t *ring = smem + p.nsb * stage_bytes;
-    float *epi = reinterpret_cast<float *>(ring + p.wstages * kWblkBytes);
+    const int slot_bytes = p.spb * kWblkBytes;
+    float *epi = reinterpret_cast<float *>(ring + p.wstages * slot_bytes);
     const int nblocks = p.nblk;
 
     if (threadIdx.x == 0) {
@@ -1120,26 +1146,29 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
         // ---------------- weight producers: producer q owns ring slot q ----------------
         if (lane == 0) {
             const int q = warp - kC2WarpProd;
-            int b = 0, last = -1;
+            int b = 0, last = -1;   // b counts ring slots filled, in the issuer's order
             bool stop = false;
             for (int t = blockIdx.x; t < p.n_tiles && !stop; t += gridDim.x) {
                 int oph, ptile, n, vt, g;
                 corr2_tile(p, t, &oph, &ptile, &n, &vt, &g);
-                // this tile's phase's blocks, in the order the issuer consumes them
+                // this tile's phase's blocks, chunk by chunk, spb consecutive blocks a slot
                 const uint8_t *wsrc = p.Wpk + ((size_t)g * p.n_vtile + vt) * (size_t)nblocks * kWblkBytes;
-                const int jend = p.blk0[oph][p.nchu];
-                for (int j = p.blk0[oph][0]; j < jend; ++j, ++b) {
-                    if (b % p.wstages != q) continue;
-                    if (b >= p.wstages &&
-                        !ptx::mbar_wait(ptx::smem_u32(&bar_wempty[q]), (b / p.wstages - 1) & 1, p.wait_ns)) {
-                        abort_flag = 1;
-                        raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
+                for (int kc = 0; kc < p.nchu && !stop; ++kc) {
+                    const int jend = p.blk0[oph][kc + 1];
+                    for (int j = p.blk0[oph][kc]; j < jend; j += p.spb, ++b) {
+                        if (b % p.wstages != q) continue;
+                        if (b >= p.wstages &&
+                            !ptx::mbar_wait(ptx::smem_u32(&bar_wempty[q]), (b / p.wstages - 1) & 1, p.wait_ns)) {
+                            abort_flag = 1;
+                            raise_device_error(p.err, DEVERR_WAIT_TIMEOUT);
+                        }
+                        if (abort_flag) { stop = true; break; }
+                        const uint32_t bytes = (uint32_t)(min(p.spb, jend - j) * kWblkBytes);
+                        const uint32_t fb = ptx::smem_u32(&bar_wfull[q]);
+                        ptx::mbar_arrive_expect_tx(fb, bytes);
+                        ptx::bulk_g2s(ptx::smem_u32(ring + q * slot_bytes), wsrc + (size_t)j * kWblkBytes, bytes, fb);
+                        last = b;
                     }
-                    if (abort_flag) { stop = true; break; }
-                    const uint32_t fb = ptx::smem_u32(&bar_wfull[q]);
-                    ptx::mbar_arrive_expect_tx(fb, kWblkBytes);
-                    ptx::bulk_g2s(ptx::smem_u32(ring + q * kWblkBytes), wsrc + (size_t)j * kWblkBytes, kWblkBytes, fb);
-                    last = b;
                 }
             }
             // the last copy into this slot must land before the CTA exits
@@ -1195,11 +1224,20 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                     const int *toff = tap_off_sh + b0;
                     const uint32_t acc_first = kc > 0 ? 1u : 0u;
                     const uint32_t wf0 = ptx::smem_u32(&bar_wfull[0]), we0 = ptx::smem_u32(&bar_wempty[0]);
-                    switch (nks) {
-                    case 4: ok = corr2_issue_taps<4>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
-                    case 3: ok = corr2_issue_taps<3>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
-                    case 2: ok = corr2_issue_taps<2>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
-                    default: ok = corr2_issue_taps<1>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                    if (p.spb == 2) {
+                        switch (nks) {
+                        case 4: ok = corr2_issue_taps<4, 2>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                        case 3: ok = corr2_issue_taps<3, 2>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                        case 2: ok = corr2_issue_taps<2, 2>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                        default: ok = corr2_issue_taps<1, 2>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                        }
+                    } else {
+                        switch (nks) {
+                        case 4: ok = corr2_issue_taps<4, 1>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                        case 3: ok = corr2_issue_taps<3, 1>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                        case 2: ok = corr2_issue_taps<2, 1>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                        default: ok = corr2_issue_taps<1, 1>(d, adesc0, bdesc_c, idesc, acc_first, toff, nbk, p.wstages, wf0, we0, slot, wphase, p.wait_ns, w_weight); break;
+                        }
                     }
                     if (!ok) break;
                     ptx::mma_commit(ptx::smem_u32(&bar_sempty[sb]));
@@ -1902,19 +1940,21 @@ struct Corr2Launch {
     int grid = 0;
 };
 
-// Staging buffers, weight ring depth, shared memory and grid of a correlation launch whose
-// tiles and stage_rows are set: two staging buffers and four weight slots when they fit;
-// never below 120 KB, so that one CTA holds its SM (it takes all 512 TMEM columns).
+// Staging buffers, weight ring, shared memory and grid of a correlation launch whose tiles
+// and stage_rows are set: two staging buffers and three slots of two weight blocks when they
+// fit, else slots of one block (four, then three); never below 120 KB, so that one CTA holds
+// its SM (it takes all 512 TMEM columns).
 bool size_corr2(Corr2Launch *L)
 {
     Corr2Params &c = L->cp;
     const size_t stage = (size_t)c.stage_rows * 128;
-    const int shapes[3][2] = {{2, 4}, {2, 3}, {1, 4}};
+    const int shapes[4][3] = {{2, 3, 2}, {2, 4, 1}, {2, 3, 1}, {1, 4, 1}};   // buffers, slots, blocks a slot
     bool fit = false;
     for (const auto &sh : shapes) {
         c.nsb = sh[0];
         c.wstages = sh[1];
-        L->smem = 1024 + c.nsb * stage + (size_t)c.wstages * kWblkBytes + kC2EpiBytes;
+        c.spb = sh[2];
+        L->smem = 1024 + c.nsb * stage + (size_t)c.wstages * c.spb * kWblkBytes + kC2EpiBytes;
         if (L->smem <= kMaxSmem) { fit = true; break; }
     }
     if (!fit) return false;
@@ -2074,12 +2114,14 @@ bool build_corr2(const Geom &g, bool bwd_data, Corr2Launch *L, int rh = -1, int 
     c.nblk = nblk;
     c.pair_delta = pair ? g.d_w : 0;
     const int positions = Qh * c.Wp;   // padded output grid rows that hold real outputs
-    c.nmma = pair ? 240 : 256;
-    if (!pair) {
+    {
         // the narrowest MMA (a multiple of 16) that keeps the number of tiles per image: the
         // weight stream per tile is unchanged and the MMAs over positions past the grid shrink
-        const int nt = (positions + 255) / 256;
-        c.nmma = std::min(256, round_up((positions + nt - 1) / nt, 16));
+        // (paired taps: at most 240, so that the epilogue's reads of the second tap's columns,
+        // pair_delta further on, stay inside the 256-column accumulator)
+        const int maxn = pair ? 240 : 256;
+        const int nt = (positions + maxn - c.pair_delta - 1) / (maxn - c.pair_delta);
+        c.nmma = std::min(maxn, round_up((positions + nt - 1) / nt + c.pair_delta, 16));
     }
     c.tile_pos = c.nmma - c.pair_delta;
     c.Cu = Cu;

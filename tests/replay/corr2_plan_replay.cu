@@ -99,6 +99,26 @@ static void check_launch(const Geom &g, int bd, const Corr2Launch &C, std::vecto
             CHECK(off(k.tk1[b]) == c.tap_off[b] && off(k.tk2[b]) == c.tap_off[b] + c.pair_delta, "pair offsets");
             CHECK(c.Cv <= 64 && c.n_vtile == 1, "pair needs one 64-row half");
         }
+    // shared memory: staging buffers, ring slots of spb blocks, the epilogue's transposes
+    CHECK(c.spb == 1 || c.spb == 2, "blocks a slot %d", c.spb);
+    CHECK(c.wstages >= 3 && c.wstages <= kC2MaxWStages && (c.nsb == 1 || c.nsb == 2), "ring %d, buffers %d", c.wstages, c.nsb);
+    CHECK(1024 + (size_t)c.nsb * c.stage_rows * 128 + (size_t)c.wstages * c.spb * kWblkBytes + kC2EpiBytes <= C.smem &&
+              C.smem <= (size_t)kMaxSmem, "shared memory layout");
+    // ring slots: the producers' order (chunk by chunk, spb consecutive blocks a slot) and the
+    // issuer's (full slots, then a one-block slot where a chunk's count is odd) name the
+    // same blocks, so every wait meets the copy it waits for
+    for (int ph = 0; ph < c.nph; ++ph) {
+        std::vector<std::pair<int, int>> prod, iss;   // (first block, blocks)
+        for (int kc = 0; kc < c.nchu; ++kc) {
+            const int b0 = c.blk0[ph][kc], jend = c.blk0[ph][kc + 1];
+            CHECK(jend > b0, "phase %d chunk %d without blocks", ph, kc);
+            for (int j = b0; j < jend; j += c.spb) prod.push_back({j, std::min(c.spb, jend - j)});
+            const int nbk = jend - b0, nfull = nbk / c.spb;
+            for (int i = 0; i < nfull; ++i) iss.push_back({b0 + i * c.spb, c.spb});
+            if (nfull * c.spb < nbk) iss.push_back({b0 + nfull * c.spb, 1});
+        }
+        CHECK(prod == iss, "phase %d: producer and issuer slot sequences differ", ph);
+    }
     // TMEM columns read by the epilogue stay in the 256-column buffer
     if (c.pair_delta) {
         int maxcol = 0;
