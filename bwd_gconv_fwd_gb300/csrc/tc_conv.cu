@@ -59,6 +59,9 @@ constexpr int kMaxChunk = 64;    // staged chunks per correlation tile (stride p
 constexpr int kWeightStages = 4;
 constexpr uint64_t kDrainNs = 1000000000ull;   // bound on draining own async work at exit
 constexpr size_t kMaxSmem = 220 * 1024;
+// The correlation kernel's dynamic shared memory may take the whole per-block maximum (227 KB)
+// less its static shared memory (3 KB: the barriers and the tap-offset table).
+constexpr size_t kC2MaxSmem = 227 * 1024 - 3 * 1024;
 
 // One staged operand: channels [0, nch) (a multiple of 8) of image `n` starting at
 // channel `c_first` of a tensor [N][Ctot][IH][IW].  Plane row r / column c maps to
@@ -1955,7 +1958,7 @@ bool size_corr2(Corr2Launch *L)
         c.wstages = sh[1];
         c.spb = sh[2];
         L->smem = 1024 + c.nsb * stage + (size_t)c.wstages * c.spb * kWblkBytes + kC2EpiBytes;
-        if (L->smem <= kMaxSmem) { fit = true; break; }
+        if (L->smem <= kC2MaxSmem) { fit = true; break; }
     }
     if (!fit) return false;
     L->smem = std::max(L->smem, (size_t)120 * 1024);
@@ -2380,13 +2383,13 @@ bool build_wgrad_phases(const Geom &g, WgradPhaseLaunch *L)
 bool fc_like(const Geom &g) { return g.Ho == 1 && g.Wo == 1; }
 
 // Raises the dynamic shared-memory limit of a kernel once per device.
-bool smem_attr_once(const void *fn, int slot)
+bool smem_attr_once(const void *fn, int slot, size_t limit = kMaxSmem)
 {
     static bool done[64][4] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     if (!done[dev][slot]) {
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem) != cudaSuccess)
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit) != cudaSuccess)
             return false;
         done[dev][slot] = true;
     }
@@ -2417,7 +2420,7 @@ gconv_status launch_corr2_kernel(Corr2Launch &L, const __nv_bfloat16 *ub, const 
     void *trace = debug_trace(&trace_bytes);
     L.cp.trace = (trace && trace_bytes >= (size_t)L.grid * kTraceWords * 8) ? static_cast<unsigned long long *>(trace)
                                                                               : nullptr;
-    if (!smem_attr_once((const void *)corr2_kernel, 2)) return GCONV_ERR_CUDA;
+    if (!smem_attr_once((const void *)corr2_kernel, 2, kC2MaxSmem)) return GCONV_ERR_CUDA;
     launch_dependent(corr2_kernel, (unsigned)L.grid, kC2Threads, L.smem, s, L.cp);
     return GCONV_OK;
 }

@@ -103,7 +103,7 @@ static void check_launch(const Geom &g, int bd, const Corr2Launch &C, std::vecto
     CHECK(c.spb == 1 || c.spb == 2, "blocks a slot %d", c.spb);
     CHECK(c.wstages >= 3 && c.wstages <= kC2MaxWStages && (c.nsb == 1 || c.nsb == 2), "ring %d, buffers %d", c.wstages, c.nsb);
     CHECK(1024 + (size_t)c.nsb * c.stage_rows * 128 + (size_t)c.wstages * c.spb * kWblkBytes + kC2EpiBytes <= C.smem &&
-              C.smem <= (size_t)kMaxSmem, "shared memory layout");
+              C.smem <= (size_t)kC2MaxSmem, "shared memory layout");
     // ring slots: the producers' order (chunk by chunk, spb consecutive blocks a slot) and the
     // issuer's (full slots, then a one-block slot where a chunk's count is odd) name the
     // same blocks, so every wait meets the copy it waits for
