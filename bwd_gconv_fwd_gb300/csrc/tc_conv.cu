@@ -1058,7 +1058,9 @@ __device__ __forceinline__ bool corr2_issue_taps(uint32_t d, uint64_t adesc0, ui
     return ok;
 }
 
-__global__ void __launch_bounds__(kC2Threads, 1)
+// At most 80 registers a thread (72 used): 17 warps of 544 threads then leave room on the
+// SM for a copy block from another stream.
+__global__ void __maxnreg__(80)
 corr2_kernel(const __grid_constant__ Corr2Params p)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1327,6 +1329,10 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                                 __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(p.V) + o;
                                 for (int vv = lane >> 4; vv < vcount; vv += 2)
                                     ob[vv * out_hw] = __float2bfloat16_rn(tbp[vv * 17 + (lane & 15)]);
+                            } else if (vcount == 32) {
+                                float *of = p.V + o + (lane >> 4) * out_hw;
+                                #pragma unroll 8
+                                for (int vv = lane >> 4; vv < 32; vv += 2, of += 2 * out_hw) *of = tbp[vv * 17 + (lane & 15)];
                             } else {
                                 float *of = p.V + o;
                                 for (int vv = lane >> 4; vv < vcount; vv += 2) of[vv * out_hw] = tbp[vv * 17 + (lane & 15)];
@@ -1363,6 +1369,11 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                         if (p.out_bf16) {
                             __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(p.V) + o;
                             for (int vv = 0; vv < vcount; ++vv) ob[vv * out_hw] = __float2bfloat16_rn(tb[vv * 33 + lane]);
+                        } else if (vcount == 32) {
+                            // all 32 channels real: straight-line stores, one pointer step each
+                            float *of = p.V + o;
+                            #pragma unroll 8
+                            for (int vv = 0; vv < 32; ++vv, of += out_hw) *of = tb[vv * 33 + lane];
                         } else {
                             float *of = p.V + o;
                             for (int vv = 0; vv < vcount; ++vv) of[vv * out_hw] = tb[vv * 33 + lane];
