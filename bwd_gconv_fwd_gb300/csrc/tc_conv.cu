@@ -979,7 +979,8 @@ constexpr int kC2WarpMma = 8;           // TMEM allocation and MMA issue
 constexpr int kC2WarpProd = 9;          // warps 9-12: weight producers (one issuing lane each)
 constexpr int kC2MaxWStages = 4;
 constexpr int kC2Threads = (kC2WarpEpi2 + kC2EpiWarps) * 32;
-constexpr int kC2EpiBytes = 2 * kC2EpiWarps * 32 * 33 * 4;   // a 32 x 33 transpose block per epilogue warp
+constexpr int kC2EpiBytes = 2 * kC2EpiWarps * 32 * 33 * 4;   // 32 x 33 floats per epilogue warp (a swizzled
+                                                             // 32 x 32 transpose, or 32 x 16 ones with paired taps)
 // Correlation-kernel trace words per CTA: start, SM id, MMA issuer's waits for staged
 // chunks, for weight blocks and for a free accumulator (ns), time of the last MMA,
 // epilogue warp 0's waits for accumulators (ns), end.
@@ -1300,8 +1301,11 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                 const int part = lg & 1;
                 const bool upper = lg >= 2;
                 const int bid = 2 + part + 2 * half;
+                // 32 rows x 16 columns each, 16-byte piece k of row r at piece k ^ ((r >> 1) & 3):
+                // whole-row 16-byte accesses and column reads are both free of bank conflicts
                 float *hb = epih + part * (32 * 17);                 // upper warp's columns
                 float *tbp = epih + (2 + part) * (32 * 17);          // lower warp's sums
+                const int rsw = (lane >> 1) & 3;
                 const int v0 = part * 32;
                 const int vcount = min(32, p.Cv - v0);
                 const int64_t vout = ((int64_t)n * p.G * p.Cv + (int64_t)g * p.Cv + v0) * out_hw;   // element index
@@ -1313,13 +1317,26 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                     ptx::tmem_ld_wait();
                     if (upper) {
                         #pragma unroll
-                        for (int j = 0; j < 16; ++j) hb[lane * 17 + j] = __uint_as_float(a[j]);
+                        for (int k = 0; k < 4; ++k)
+                            *reinterpret_cast<float4 *>(hb + lane * 16 + ((k ^ rsw) << 2)) =
+                                make_float4(__uint_as_float(a[4 * k]), __uint_as_float(a[4 * k + 1]),
+                                            __uint_as_float(a[4 * k + 2]), __uint_as_float(a[4 * k + 3]));
                     }
                     ptx::named_sync(bid, 64);
                     if (!upper) {
                         #pragma unroll
-                        for (int j = 0; j < 16; ++j) tbp[lane * 17 + j] = __uint_as_float(a[j]) + hb[lane * 17 + j] + bias_lane;
+                        for (int k = 0; k < 4; ++k) {
+                            const int off = lane * 16 + ((k ^ rsw) << 2);
+                            const float4 h = *reinterpret_cast<const float4 *>(hb + off);
+                            *reinterpret_cast<float4 *>(tbp + off) =
+                                make_float4(__uint_as_float(a[4 * k]) + h.x + bias_lane, __uint_as_float(a[4 * k + 1]) + h.y + bias_lane,
+                                            __uint_as_float(a[4 * k + 2]) + h.z + bias_lane, __uint_as_float(a[4 * k + 3]) + h.w + bias_lane);
+                        }
                         __syncwarp();
+                        // element (row vv, column c) of the swizzled rows
+                        auto tbp_at = [&](int vv) {
+                            return tbp[vv * 16 + ((((lane & 15) >> 2) ^ ((vv >> 1) & 3)) << 2) + (lane & 3)];
+                        };
                         const int jc = pc + (lane & 15);
                         const int pos = p0 + jc;
                         const int qh = pos / p.Wp, qw = pos - qh * p.Wp;
@@ -1327,15 +1344,14 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                             const int64_t o = vout + (int64_t)(qh * p.o_sh + o_rh) * p.oW + (qw * p.o_sw + o_rw);
                             if (p.out_bf16) {
                                 __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(p.V) + o;
-                                for (int vv = lane >> 4; vv < vcount; vv += 2)
-                                    ob[vv * out_hw] = __float2bfloat16_rn(tbp[vv * 17 + (lane & 15)]);
+                                for (int vv = lane >> 4; vv < vcount; vv += 2) ob[vv * out_hw] = __float2bfloat16_rn(tbp_at(vv));
                             } else if (vcount == 32) {
                                 float *of = p.V + o + (lane >> 4) * out_hw;
                                 #pragma unroll 8
-                                for (int vv = lane >> 4; vv < 32; vv += 2, of += 2 * out_hw) *of = tbp[vv * 17 + (lane & 15)];
+                                for (int vv = lane >> 4; vv < 32; vv += 2, of += 2 * out_hw) *of = tbp_at(vv);
                             } else {
                                 float *of = p.V + o;
-                                for (int vv = lane >> 4; vv < vcount; vv += 2) of[vv * out_hw] = tbp[vv * 17 + (lane & 15)];
+                                for (int vv = lane >> 4; vv < vcount; vv += 2) of[vv * out_hw] = tbp_at(vv);
                             }
                         }
                     }
@@ -1356,27 +1372,34 @@ corr2_kernel(const __grid_constant__ Corr2Params p)
                 ptx::tmem_ld16(taddr + 16, a1);
                 ptx::tmem_ld_wait();
                 if (vcount > 0) {
+                    // 32 x 32, 16-byte piece k of row r at piece k ^ (r & 7): whole-row 16-byte
+                    // writes and column reads are both free of bank conflicts
                     #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        tb[lane * 33 + j] = __uint_as_float(a0[j]) + bias_lane;
-                        tb[lane * 33 + 16 + j] = __uint_as_float(a1[j]) + bias_lane;
+                    for (int k = 0; k < 4; ++k) {
+                        *reinterpret_cast<float4 *>(tb + lane * 32 + ((k ^ (lane & 7)) << 2)) =
+                            make_float4(__uint_as_float(a0[4 * k]) + bias_lane, __uint_as_float(a0[4 * k + 1]) + bias_lane,
+                                        __uint_as_float(a0[4 * k + 2]) + bias_lane, __uint_as_float(a0[4 * k + 3]) + bias_lane);
+                        *reinterpret_cast<float4 *>(tb + lane * 32 + (((k + 4) ^ (lane & 7)) << 2)) =
+                            make_float4(__uint_as_float(a1[4 * k]) + bias_lane, __uint_as_float(a1[4 * k + 1]) + bias_lane,
+                                        __uint_as_float(a1[4 * k + 2]) + bias_lane, __uint_as_float(a1[4 * k + 3]) + bias_lane);
                     }
                     __syncwarp();
+                    auto tb_at = [&](int vv) { return tb[vv * 32 + (((lane >> 2) ^ (vv & 7)) << 2) + (lane & 3)]; };
                     const int pos = p0 + pc + lane;
                     const int qh = pos / p.Wp, qw = pos - qh * p.Wp;
                     if (pc + lane < p.tile_pos && qh < Qh && qw < Qw) {
                         const int64_t o = vout + (int64_t)(qh * p.o_sh + o_rh) * p.oW + (qw * p.o_sw + o_rw);
                         if (p.out_bf16) {
                             __nv_bfloat16 *ob = reinterpret_cast<__nv_bfloat16 *>(p.V) + o;
-                            for (int vv = 0; vv < vcount; ++vv) ob[vv * out_hw] = __float2bfloat16_rn(tb[vv * 33 + lane]);
+                            for (int vv = 0; vv < vcount; ++vv) ob[vv * out_hw] = __float2bfloat16_rn(tb_at(vv));
                         } else if (vcount == 32) {
                             // all 32 channels real: straight-line stores, one pointer step each
                             float *of = p.V + o;
                             #pragma unroll 8
-                            for (int vv = 0; vv < 32; ++vv, of += out_hw) *of = tb[vv * 33 + lane];
+                            for (int vv = 0; vv < 32; ++vv, of += out_hw) *of = tb_at(vv);
                         } else {
                             float *of = p.V + o;
-                            for (int vv = 0; vv < vcount; ++vv) of[vv * out_hw] = tb[vv * 33 + lane];
+                            for (int vv = 0; vv < vcount; ++vv) of[vv * out_hw] = tb_at(vv);
                         }
                     }
                     __syncwarp();
