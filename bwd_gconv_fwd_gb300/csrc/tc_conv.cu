@@ -1059,8 +1059,8 @@ __device__ __forceinline__ bool corr2_issue_taps(uint32_t d, uint64_t adesc0, ui
     return ok;
 }
 
-// At most 80 registers a thread (72 used): 17 warps of 544 threads then leave room on the
-// SM for a copy block from another stream.
+// At most 80 registers a thread: 17 warps of 544 threads then leave room on the SM for a
+// copy block (256 threads x 64 registers) from another stream.
 __global__ void __maxnreg__(80)
 corr2_kernel(const __grid_constant__ Corr2Params p)
 {
