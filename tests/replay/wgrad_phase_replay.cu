@@ -66,6 +66,7 @@ int main(int argc, char **argv)
     std::vector<int> tap_seen(g.kH * g.kW, 0);
     const WgradParams &p = L.wp;
     printf(" one launch: grid %d smem %zu groups %d x planes %d\n", L.grid, L.smem, p.n_tgrp, p.nxplane);
+    CHECK(L.smem >= 1024 + (size_t)kWgradEpiBytes && L.smem <= kMaxSmem, "shared memory %zu", L.smem);
     CHECK(p.nxplane == L.nphase && p.nxplane == L.bx.nplane, "x plane count");
     for (int gi = 0; gi < p.n_tgrp; ++gi) {
         CHECK(p.grp_plane[gi] >= 0 && p.grp_plane[gi] < p.nxplane, "group %d plane", gi);

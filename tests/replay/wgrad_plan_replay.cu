@@ -37,6 +37,7 @@ int main(int argc, char **argv)
     if (!build_wgrad(g, &L)) { printf("not served by this path\nerrors: 0\n"); return 0; }
     printf("Ho=%d Wo=%d grid=%d smem=%zu ws=%zu\n", g.Ho, g.Wo, L.grid, L.smem, L.ws_bytes);
     CHECK(L.smem <= kMaxSmem, "shared memory %zu", L.smem);
+    CHECK(L.smem >= 1024 + (size_t)kWgradEpiBytes, "room for the epilogue's transposes: %zu", L.smem);
     // blocked copies: every source element inside x / gradOutput, every row inside its buffer
     for (int which = 0; which < 2; ++which) {
         const BlockifyParams &p = which ? L.by : L.bx;
@@ -111,6 +112,30 @@ int main(int argc, char **argv)
                                           std::min(64, p.Cgi - ct * 64) - 1;
                         CHECK((size_t)e < part_elems, "part");
                     }
+            // the epilogue's row-order stores: every (row, 16-byte piece) of a warp's block
+            // exactly once, its shared-memory reads inside the warp's 32 x 68-float area
+            if ((p.Cgi & 3) == 0 && p.Cgi <= 64) {
+                const int nchk = std::min(64, p.Cgi - ct * 64) >> 2;
+                for (int lg = 0; lg < 4; ++lg) {
+                    const int rows = std::max(0, std::min(32, std::min(128, p.Cgo - ot * 128) - lg * 32));
+                    std::vector<int> seen(32 * 16, 0);
+                    for (int lane = 0; lane < 32; ++lane) {
+                        const int dr = 32 / nchk, dk = 32 - dr * nchk;
+                        int rr = lane / nchk, kk = lane - rr * nchk;
+                        for (int i = lane; i < rows * nchk; i += 32) {
+                            CHECK(rr >= 0 && rr < rows && kk >= 0 && kk < nchk, "epilogue piece (%d,%d)", rr, kk);
+                            if (rr >= 0 && rr < 32 && kk >= 0 && kk < 16) seen[rr * 16 + kk]++;
+                            rr += dr;
+                            kk += dk;
+                            if (kk >= nchk) { kk -= nchk; ++rr; }
+                        }
+                    }
+                    for (int r2 = 0; r2 < rows; ++r2)
+                        for (int k2 = 0; k2 < nchk; ++k2)
+                            CHECK(seen[r2 * 16 + k2] == 1, "epilogue piece (%d,%d) stored %d times", r2, k2, seen[r2 * 16 + k2]);
+                    CHECK(rows == 0 || (rows - 1) * 68 + 4 * nchk <= 32 * 68, "epilogue area");
+                }
+            }
         }
     }
     for (int k = 0; k < g.kH * g.kW; ++k) CHECK(tap_seen[k] == 1, "tap %d covered %d times", k, tap_seen[k]);
