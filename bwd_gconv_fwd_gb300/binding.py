@@ -39,7 +39,7 @@ EXPORTED = ("gconv_out_shape", "gconv_workspace_size", "gconv_plan", "gconv_fwd"
             "gconv_noalloc_scratch_bytes", "gconv_step_host", "gconv_step_device_bytes",
             "gconv_out_shape_ex", "gconv_workspace_size_ex", "gconv_plan_ex", "gconv_fwd_ex", "gconv_bwd_data_ex",
             "gconv_bwd_weight_ex", "gconv_bwd_bias_ex", "gconv_step_workspace_size_ex", "gconv_step_plan_ex", "gconv_step_ex",
-            "gconv_debug_set_step_events")
+            "gconv_debug_set_step_events", "gconv_debug_set_wgrad_tma")
 
 
 class Geometry(ctypes.Structure):
@@ -122,6 +122,8 @@ def lib():
     L.gconv_debug_force_path.restype = None
     L.gconv_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
     L.gconv_debug_set_wait_limit.restype = None
+    L.gconv_debug_set_wgrad_tma.argtypes = [i]
+    L.gconv_debug_set_wgrad_tma.restype = None
     L.gconv_debug_set_trace.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
     L.gconv_debug_set_trace.restype = None
     gp = ctypes.POINTER(Geometry)
@@ -221,6 +223,11 @@ def gconv_debug_force_path(path: int):
 
 def gconv_debug_set_wait_limit(limit: int):
     lib().gconv_debug_set_wait_limit(int(limit))
+
+
+def gconv_debug_set_wgrad_tma(enable: bool):
+    """Test hook: False makes the tensor-core weight gradient stage its tiles by cp.async."""
+    lib().gconv_debug_set_wgrad_tma(1 if enable else 0)
 
 
 

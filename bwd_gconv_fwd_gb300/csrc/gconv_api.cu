@@ -62,6 +62,8 @@ long long wait_limit()
 }
 
 int forced_path() { return g_force_path; }
+static int g_wgrad_tma = 1;
+int wgrad_tma_enabled() { return g_wgrad_tma; }
 void *debug_trace(size_t *bytes)
 {
     *bytes = g_trace_bytes;
@@ -918,6 +920,7 @@ gconv_status gconv_step_host(GEO_ARGS, gconv_dtype dtype, const void *x, const v
 }
 
 void gconv_debug_force_path(int path) { g_force_path = path; }
+void gconv_debug_set_wgrad_tma(int enable) { g_wgrad_tma = enable ? 1 : 0; }
 
 void gconv_debug_set_wait_limit(long long limit) { g_wait_limit = limit; }
 

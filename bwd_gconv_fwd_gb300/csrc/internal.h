@@ -55,6 +55,7 @@ void launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block, s
 long long wait_limit();
 unsigned int *device_error_word();   // device address of the error word, nullptr on failure
 int forced_path();
+int wgrad_tma_enabled();   // 0: the tensor-core weight gradient stages its tiles by cp.async
 void *debug_trace(size_t *bytes);     // gconv_debug_set_trace buffer, nullptr when off
 
 // tcgen05 implicit-GEMM family (tc_conv.cu)

@@ -1957,7 +1957,7 @@ void set_wgrad_tma(WgradParams *w)
 {
     const uint64_t plane_x = (uint64_t)w->Rx * w->Wp, plane_y = (uint64_t)w->Ho * w->Wp;
     const uint64_t planes_x = (uint64_t)w->N * w->G * w->ncx * std::max(1, w->nxplane);
-    w->tma = (encode_rows_tmap(&w->tm_x, w->XT, plane_x, planes_x, (uint32_t)w->xb) &&
+    w->tma = (wgrad_tma_enabled() && encode_rows_tmap(&w->tm_x, w->XT, plane_x, planes_x, (uint32_t)w->xb) &&
               encode_rows_tmap(&w->tm_dy, w->DYT, plane_y, (uint64_t)w->N * w->G * w->ncy, (uint32_t)(w->TH * w->Wp)))
                  ? 1 : 0;
 }
@@ -2805,7 +2805,8 @@ void blocked_source(const BlockifyParams &b, int r, int c, int *sr, int *sc)
 bool tc_step_build(const Geom &g, TcStep *S)
 {
     *S = TcStep{};
-    if (g.s_h != 1 || g.s_w != 1) return false;
+    // the shared copies reach the weight gradient through tensor maps only
+    if (g.s_h != 1 || g.s_w != 1 || !wgrad_tma_enabled()) return false;
     if (!build_corr2(g, false, &S->F) || !build_corr2(g, true, &S->B) || !build_wgrad(g, &S->W)) return false;
     const BlockifyParams &fx = S->F.bu, &wx = S->W.bx, &by = S->B.bu, &wy = S->W.by;
     // x: the same copy

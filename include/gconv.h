@@ -322,9 +322,14 @@ const char *gconv_status_string(gconv_status status);
  * first unsuccessful poll, which exercises the timeout path (the kernel records
  * GCONV_ERR_TIMEOUT, drains its own copies and MMAs, frees its tensor memory and
  * returns) without hanging anything.  Waits that drain a kernel's own in-flight
- * work at exit keep their own one-second bound. */
+ * work at exit keep their own one-second bound.
+ * gconv_debug_set_wgrad_tma: 0 makes the tensor-core weight gradient stage its
+ * tiles with cp.async copies (the form it takes when a tensor map cannot be
+ * encoded) and the one-call step run its passes separately; 1 (the default)
+ * restores TMA staging. */
 void gconv_debug_force_path(int path);
 void gconv_debug_set_wait_limit(long long limit);
+void gconv_debug_set_wgrad_tma(int enable);
 
 /* Phase trace of the tensor-core kernels (process-wide, not thread-safe).
  * While a device buffer is set, every launch of the stride-1 correlation kernel

@@ -611,6 +611,42 @@ def test_weight_gradient_with_bias_gradient(dev, oracle_mod, geom):
     check("fused db", db.cpu().numpy(), oracle_mod.bwd_bias(geom, f64(dy)), TOL["bf16"])
 
 
+@pytest.mark.parametrize("geom", [
+    (3, 48, 11, 11, 128, 5, 5, 1, 2, 2, 2, 2, 1, 2),        # AlexNet-like, ragged, bias column
+    (2, 64, 19, 16, 64, 3, 3, 2, 0, 1, 0, 1, 1, 1),         # stride 2: stride-phase planes, asymmetric pads
+    (2, 16, 9, 9, 16, 3, 3, 1, 2, 2, 2, 2, 2, 1),           # dilation 2
+    (2, 32, 15, 14, 32, 7, 7, 1, 3, 3, 3, 3, 1, 1),         # 7 x 7: 49 taps in several job groups
+    (2, 64, 13, 12, 64, 3, 3, 1, 1, 1, 1, 1, 1, 8),         # merged groups
+    (2, 256, 9, 9, 256, 3, 3, 1, 1, 1, 1, 1, 1, 1),         # several channel tiles
+])
+def test_weight_gradient_cp_async_staging(dev, oracle_mod, geom):
+    """The tensor-core weight gradient's cp.async staging (the form it takes when a tensor
+    map cannot be encoded) gives the same dw and db as its TMA staging, bit for bit: both
+    put the same rows in the same shared-memory layout for the same MMAs."""
+    assert gc.gconv_plan(geom, B.GCONV_BF16, B.PASS_BWD_WEIGHT)[0] == B.PATH_TC_IGEMM
+    wk = wl.Workload("cpasync", geom, "bf16", w=("normal", 0.2))
+    x, w, b, dy = wl.make_inputs(wk, seed=61)
+    xd, dyd = x.to(dev), dy.to(dev)
+    got = {}
+    for tma in (True, False):
+        B.gconv_debug_set_wgrad_tma(tma)
+        try:
+            dw, bw = guarded(tuple(w.shape), dev)
+            db, bb = guarded((geom[4],), dev)
+            gc.gconv_bwd_weight(xd, dyd, dw, db=db, **_kw(geom))
+            torch.cuda.synchronize()
+            assert gc.gconv_check_device_error() == B.GCONV_OK
+        finally:
+            B.gconv_debug_set_wgrad_tma(True)
+        check_guards(f"dw tma={tma}", bw)
+        check_guards(f"db tma={tma}", bb)
+        got[tma] = (dw.cpu(), db.cpu())
+    check("cp.async dw", got[False][0].numpy(), oracle_mod.bwd_weight(geom, f64(x), f64(dy)), TOL["bf16"])
+    check("cp.async db", got[False][1].numpy(), oracle_mod.bwd_bias(geom, f64(dy)), TOL["bf16"])
+    assert torch.equal(got[False][0], got[True][0])
+    assert torch.equal(got[False][1], got[True][1])
+
+
 # bf16 outputs (y, dx through the *_ex entry points): the stored value is the fp32 result
 # rounded once to nearest even, so it must equal the fp32 output rounded by torch, bit for
 # bit; against the oracle the bound adds that rounding, half a bf16 ulp (2^-8 relative).
