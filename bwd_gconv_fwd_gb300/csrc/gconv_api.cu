@@ -140,9 +140,19 @@ static void bias_plan(const Geom &g, gconv_dtype dt, Plan *p)
     p->launches = 2;
     const int64_t HW = (int64_t)g.Ho * g.Wo;
     if (HW >= kBiasPlaneMin) {
+        // S warps a plane where the planes alone give fewer than about 48 warps an SM (whole
+        // 16-byte chunks only, at least 64 chunks a warp), so that enough loads are in flight
+        const int V = dt == GCONV_BF16 ? 8 : 4;
+        const int64_t nplanes = (int64_t)g.N * g.Cout, nch = HW / V;
+        int64_t S = 1;
+        if (HW % V == 0) {
+            const int64_t want = ((int64_t)num_sms() * 48 + nplanes - 1) / nplanes;
+            S = std::max<int64_t>(1, std::min<int64_t>(want, nch / 64));
+        }
         p->tc[0] = 0;
-        p->splits = 1;
-        p->ws_bytes = (size_t)g.N * g.Cout * sizeof(float);
+        p->tc[1] = HW % V == 0 ? 1 : 0;
+        p->splits = (int)S;
+        p->ws_bytes = (size_t)nplanes * S * sizeof(float);
         return;
     }
     const int64_t L = (int64_t)g.Cout * HW;
@@ -239,10 +249,12 @@ static void launch_direct(const Geom &g, const Plan &p, gconv_pass pass, const v
         const int fin_grid = (g.Cout + kDirectThreads / 32 - 1) / (kDirectThreads / 32);   // a warp per channel
         if (p.tc[0] == 0) {
             const int64_t nplanes = (int64_t)g.N * g.Cout;
-            const int64_t blocks = (nplanes + kDirectThreads / 32 - 1) / (kDirectThreads / 32);
-            plane_sum_kernel<T><<<(int)std::min<int64_t>(blocks, (int64_t)num_sms() * 32), kDirectThreads, 0, st>>>(
-                A, nplanes, HW, part);
-            bias_finish_kernel<<<fin_grid, kDirectThreads, 0, st>>>(part, g.N, g.Cout, 1, g.Cout, out);
+            const int S = p.splits;
+            const int64_t blocks = (nplanes * S + kDirectThreads / 32 - 1) / (kDirectThreads / 32);
+            const int grid = (int)std::min<int64_t>(blocks, (int64_t)num_sms() * 32);
+            if (p.tc[1]) plane_sum_kernel<T, true><<<grid, kDirectThreads, 0, st>>>(A, nplanes, HW, S, part);
+            else plane_sum_kernel<T, false><<<grid, kDirectThreads, 0, st>>>(A, nplanes, HW, 1, part);
+            bias_finish_kernel<<<fin_grid, kDirectThreads, 0, st>>>(part, g.N, (int64_t)g.Cout * S, S, g.Cout, out);
         } else {
             const int64_t L = (int64_t)g.Cout * HW;
             const int64_t threads = p.tc[1] ? L / (16 / (int64_t)sizeof(T)) : L;

@@ -180,22 +180,32 @@ reduce_splits_kernel(const float *__restrict__ part, int splits, int64_t count,
 // Bias gradient db[o] = sum over n, h, w of dy[n][o][h][w], in two deterministic
 // stages (no atomics), chosen by the plane size HW = Ho*Wo.
 //
-// Planes of kBiasPlaneMin elements or more: one warp per (n, o) plane writes its sum
-// to psum[n*C_out + o]; the lanes take 16-byte chunks of the plane, issuing four
-// chunks per lane before adding them, and a fixed shuffle tree finishes the plane.
+// Planes of kBiasPlaneMin elements or more: S warps per (n, o) plane each write the sum of
+// one contiguous share of the plane's 16-byte chunks to psum[(n*C_out + o)*S + s]; the
+// lanes issue four chunks each before adding them, and a fixed shuffle tree finishes the
+// share.  ALIGNED (HW a multiple of the chunk's element count, so every plane starts on a
+// chunk): whole chunks with no per-element tests; S > 1 only then.  Otherwise S = 1 and the
+// chunks that straddle two planes are added element by element.
 constexpr int kBiasPlaneMin = 32;
 
-template <typename T>
+template <typename T, bool ALIGNED>
 __global__ void __launch_bounds__(kDirectThreads)
-plane_sum_kernel(const T *__restrict__ dy, int64_t nplanes, int64_t HW, float *__restrict__ psum)
+plane_sum_kernel(const T *__restrict__ dy, int64_t nplanes, int64_t HW, int S, float *__restrict__ psum)
 {
     constexpr int V = 16 / sizeof(T);
     const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * (kDirectThreads / 32);
     const int64_t full_chunks = nplanes * HW / V;     // whole 16-byte chunks of the array
-    for (int64_t pl = ((int64_t)blockIdx.x * kDirectThreads + threadIdx.x) >> 5; pl < nplanes; pl += nw) {
+    const int64_t items = nplanes * S;
+    for (int64_t it = ((int64_t)blockIdx.x * kDirectThreads + threadIdx.x) >> 5; it < items; it += nw) {
+        const int64_t pl = ALIGNED ? it / S : it;
         const int64_t begin = pl * HW, end = begin + HW;
-        const int64_t c0 = begin / V, c1 = (end + V - 1) / V;
+        int64_t c0 = begin / V, c1 = (end + V - 1) / V;
+        if (ALIGNED) {
+            const int64_t share = (c1 - c0 + S - 1) / S, sh = it - pl * S;
+            c0 += sh * share;
+            c1 = min(c1, c0 + share);
+        }
         float acc = 0.f;
         for (int64_t cb = c0; cb < c1; cb += 4 * 32) {
             uint4 raw[4];
@@ -209,8 +219,11 @@ plane_sum_kernel(const T *__restrict__ dy, int64_t nplanes, int64_t HW, float *_
             for (int u = 0; u < 4; ++u) {
                 const int64_t c = cb + u * 32 + lane;
                 if (c >= c1) continue;
-                if (c < full_chunks) {
-                    const T *v = reinterpret_cast<const T *>(&raw[u]);
+                const T *v = reinterpret_cast<const T *>(&raw[u]);
+                if (ALIGNED) {
+                    #pragma unroll
+                    for (int j = 0; j < V; ++j) acc += to_f(v[j]);
+                } else if (c < full_chunks) {
                     #pragma unroll
                     for (int j = 0; j < V; ++j) {
                         const int64_t idx = c * V + j;
@@ -226,7 +239,7 @@ plane_sum_kernel(const T *__restrict__ dy, int64_t nplanes, int64_t HW, float *_
         }
         #pragma unroll
         for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) psum[pl] = acc;
+        if (lane == 0) psum[it] = acc;
     }
 }
 
