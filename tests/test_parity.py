@@ -164,6 +164,33 @@ def test_random_sweep(dev, oracle_mod):
         full_compare(geom, dtype, x, w, b, dy, dev, oracle_mod, label=f"sweep{i} {geom}")
 
 
+def test_random_sweep_tensor_core(dev, oracle_mod):
+    """Random bf16 geometries that the planner sends to the tensor-core correlation and
+    weight-gradient kernels on all three contraction passes (at least 16 channels a group on
+    each side, kernels up to 5 x 5, stride and dilation up to 2, asymmetric pads), compared
+    over whole tensors; most of the generated cases must reach that family."""
+    rng = np.random.default_rng(4321)
+    ran = 0
+    for i in range(32):
+        G = int(rng.choice([1, 1, 2, 3]))
+        cgi, cgo = int(rng.integers(16, 65)), int(rng.integers(16, 97))
+        kH, kW = int(rng.integers(1, 6)), int(rng.integers(1, 6))
+        s, d = int(rng.integers(1, 3)), int(rng.integers(1, 3))
+        pads = [int(v) for v in rng.integers(0, 3, size=4)]
+        geom = (int(rng.integers(1, 4)), cgi * G, int(rng.integers(6, 17)), int(rng.integers(6, 17)), cgo * G,
+                kH, kW, s, *pads, d, G)
+        ho, wo = wl.out_hw(geom)
+        if ho < 1 or wo < 1:
+            continue
+        if any(gc.gconv_plan(geom, B.GCONV_BF16, p)[0] != B.PATH_TC_IGEMM for p in range(3)):
+            continue
+        wk = wl.Workload("tcsweep", geom, "bf16", w=("normal", 0.2))
+        x, w, b, dy = wl.make_inputs(wk, seed=7000 + i)
+        full_compare(geom, "bf16", x, w, b, dy, dev, oracle_mod, label=f"tcsweep{i} {geom}")
+        ran += 1
+    assert ran >= 20, ran
+
+
 def test_tiny_g5_full(dev, oracle_mod):
     """The NNlib.jl groups=5 example at its own size, fp32, whole tensors at 1e-4."""
     wk = wl.WORKLOADS["tiny_g5"]
