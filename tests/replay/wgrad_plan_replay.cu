@@ -12,6 +12,7 @@ long long wait_limit() { return 1000000000LL; }
 int num_sms() { return 152; }
 unsigned int *device_error_word() { return nullptr; }
 int forced_path() { return 0; }
+int wgrad_tma_enabled() { return 1; }
 void *debug_trace(size_t *b) { *b = 0; return nullptr; }
 bool encode_rows_tmap(CUtensorMap *, const void *, uint64_t, uint64_t, uint32_t, uint64_t) { return false; }
 }
