@@ -182,13 +182,14 @@ reduce_splits_kernel(const float *__restrict__ part, int splits, int64_t count,
 //
 // Planes of kBiasPlaneMin elements or more: S warps per (n, o) plane each write the sum of
 // one contiguous share of the plane's 16-byte chunks to psum[(n*C_out + o)*S + s]; the
-// lanes issue four chunks each before adding them, and a fixed shuffle tree finishes the
-// share.  ALIGNED (HW a multiple of the chunk's element count, so every plane starts on a
+// lanes issue their chunks before adding them, and a fixed shuffle tree finishes the
+// share (LOADS chunks a lane in flight: 8 for shares of 256 chunks or more, else 4; the lane
+// adds its chunks in index order whatever that count).  ALIGNED (HW a multiple of the chunk's element count, so every plane starts on a
 // chunk): whole chunks with no per-element tests; S > 1 only then.  Otherwise S = 1 and the
 // chunks that straddle two planes are added element by element.
 constexpr int kBiasPlaneMin = 32;
 
-template <typename T, bool ALIGNED>
+template <typename T, bool ALIGNED, int LOADS>
 __global__ void __launch_bounds__(kDirectThreads)
 plane_sum_kernel(const T *__restrict__ dy, int64_t nplanes, int64_t HW, int S, float *__restrict__ psum)
 {
@@ -207,16 +208,16 @@ plane_sum_kernel(const T *__restrict__ dy, int64_t nplanes, int64_t HW, int S, f
             c1 = min(c1, c0 + share);
         }
         float acc = 0.f;
-        for (int64_t cb = c0; cb < c1; cb += 4 * 32) {
-            uint4 raw[4];
+        for (int64_t cb = c0; cb < c1; cb += LOADS * 32) {
+            uint4 raw[LOADS];
             #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < LOADS; ++u) {
                 const int64_t c = cb + u * 32 + lane;
                 raw[u] = (c < c1 && c < full_chunks) ? __ldg(reinterpret_cast<const uint4 *>(dy) + c)
                                                      : make_uint4(0u, 0u, 0u, 0u);
             }
             #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < LOADS; ++u) {
                 const int64_t c = cb + u * 32 + lane;
                 if (c >= c1) continue;
                 const T *v = reinterpret_cast<const T *>(&raw[u]);
