@@ -3,6 +3,7 @@
 // the operation, layouts, ownership and error behaviour.
 #include "../../include/gconv.h"
 #include "common.cuh"
+#include "ptx.cuh"
 #include "kernels_direct.cuh"
 #include "internal.h"
 
@@ -255,10 +256,12 @@ static void launch_direct(const Geom &g, const Plan &p, gconv_pass pass, const v
             // eight 16-byte loads a lane in flight where a warp's share has 256 chunks or more
             // (depthwise 56x56 bias 34.4 -> 31.4 us), four on shorter shares
             const bool wide = p.tc[1] && HW / (16 / (int64_t)sizeof(T)) / S >= 256;
-            if (wide) plane_sum_kernel<T, true, 8><<<grid, kDirectThreads, 0, st>>>(A, nplanes, HW, S, part);
-            else if (p.tc[1]) plane_sum_kernel<T, true, 4><<<grid, kDirectThreads, 0, st>>>(A, nplanes, HW, S, part);
-            else plane_sum_kernel<T, false, 4><<<grid, kDirectThreads, 0, st>>>(A, nplanes, HW, 1, part);
-            bias_finish_kernel<<<fin_grid, kDirectThreads, 0, st>>>(part, g.N, (int64_t)g.Cout * S, S, g.Cout, out);
+            // programmatic dependents: each launch's blocks land as the previous kernel drains
+            if (wide) launch_dependent(plane_sum_kernel<T, true, 8>, (unsigned)grid, kDirectThreads, 0, st, A, nplanes, HW, S, part);
+            else if (p.tc[1]) launch_dependent(plane_sum_kernel<T, true, 4>, (unsigned)grid, kDirectThreads, 0, st, A, nplanes, HW, S, part);
+            else launch_dependent(plane_sum_kernel<T, false, 4>, (unsigned)grid, kDirectThreads, 0, st, A, nplanes, HW, 1, part);
+            launch_dependent(bias_finish_kernel, (unsigned)fin_grid, kDirectThreads, 0, st, (const float *)part, g.N,
+                             (int64_t)g.Cout * S, S, g.Cout, out);
         } else {
             const int64_t L = (int64_t)g.Cout * HW;
             const int64_t threads = p.tc[1] ? L / (16 / (int64_t)sizeof(T)) : L;

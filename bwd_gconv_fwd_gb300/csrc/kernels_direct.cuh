@@ -193,6 +193,8 @@ template <typename T, bool ALIGNED, int LOADS>
 __global__ void __launch_bounds__(kDirectThreads)
 plane_sum_kernel(const T *__restrict__ dy, int64_t nplanes, int64_t HW, int S, float *__restrict__ psum)
 {
+    ptx::griddep_wait();   // a programmatic dependent reads nothing before this
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
     constexpr int V = 16 / sizeof(T);
     const int lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * (kDirectThreads / 32);
@@ -284,6 +286,8 @@ __global__ void __launch_bounds__(kDirectThreads)
 bias_finish_kernel(const float *__restrict__ part, int rows, int64_t cols, int inner, int C_out,
                    float *__restrict__ out)
 {
+    ptx::griddep_wait();   // a programmatic dependent reads nothing before this
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
     const int o = blockIdx.x * (kDirectThreads / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (o >= C_out) return;
